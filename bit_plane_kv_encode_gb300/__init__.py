@@ -1,0 +1,83 @@
+"""GB300-native query-dependent prefix reads of a bit-plane K cache.
+
+The compute path is libbpkv (CUDA kernels for sm_103a behind the C ABI in
+``include/bpkv.h``).  This package is its thin Python binding: the functions
+named ``bpkv_*`` marshal torch tensors to the C entry points of the same name;
+``Cache`` holds one layer's cache buffers as torch tensors (torch is used only
+to own device or pinned host memory and streams).
+"""
+from __future__ import annotations
+
+import ctypes
+
+from ._binding import (  # noqa: F401
+    BpkvError, bpkv_alloc_depths, bpkv_cache, bpkv_clear_status, bpkv_decode_step, bpkv_dense_attend,
+    bpkv_encode_append, bpkv_fixed_depths, bpkv_read_status, bpkv_scan, bpkv_scan_topk, bpkv_sparse_attend,
+    bpkv_status_string, bpkv_step_args, bpkv_topk, bpkv_union, bpkv_version, bpkv_workspace_size, header_symbols, load)
+
+HEAD_DIM = 128
+WS_SCAN_TOPK, WS_ATTEND, WS_DENSE, WS_STEP = 1, 2, 4, 8
+DEPTH_WATERFILL, DEPTH_FIXED, DEPTH_DENSE = 0, 1, 2
+DEV_OVERFLOW, DEV_SELECT = 1, 2
+
+
+class Cache:
+    """One layer's bit-plane K cache and bf16 K/V rows for N sequences x H KV heads.
+
+    residency "hbm": all buffers in device memory.  "host": planes, scales and
+    rows in pinned host memory, read by the kernels in place over the host link.
+    """
+
+    def __init__(self, n_seq: int, n_kv_heads: int, group: int, cap_tokens: int, device="cuda",
+                 residency: str = "hbm"):
+        import torch
+        if cap_tokens % 512:
+            raise ValueError("cap_tokens must be a multiple of 512")
+        D, nb = HEAD_DIM, cap_tokens // 64
+        self.device = torch.device(device)
+        host = residency == "host"
+
+        def buf(shape, dtype):
+            if host:
+                return torch.empty(shape, dtype=dtype, pin_memory=True)
+            return torch.empty(shape, dtype=dtype, device=self.device)
+
+        self.planes = buf((n_seq, n_kv_heads, D, 4, nb), torch.int64)
+        self.scales = buf((n_seq, n_kv_heads, D, nb), torch.int16)
+        self.k_rows = buf((n_seq, n_kv_heads, cap_tokens, D), torch.bfloat16)
+        self.v_rows = buf((n_seq, n_kv_heads, cap_tokens, D), torch.bfloat16)
+        self.seq_len = torch.zeros(n_seq, dtype=torch.int64, device=self.device)
+        self.c = bpkv_cache(n_seq, n_kv_heads, group, D, cap_tokens, 0, 1 if host else 0, 0,
+                            self.planes.data_ptr(), self.scales.data_ptr(), self.k_rows.data_ptr(),
+                            self.v_rows.data_ptr(), self.seq_len.data_ptr())
+
+    @property
+    def n_max(self) -> int:
+        return int(self.c.n_max)
+
+    def append(self, k_new, v_new, stream=None):
+        """Append k_new/v_new [N][H][t][D] bf16 (device) to every sequence."""
+        bpkv_encode_append(self.c, k_new, v_new, k_new.shape[2], stream)
+
+    def workspace(self, k: int, what: int):
+        import torch
+        n = bpkv_workspace_size(self.c, k, what)
+        if n == 0:
+            raise BpkvError("bpkv_workspace_size", -1)
+        return torch.empty(n, dtype=torch.uint8, device=self.device)
+
+
+def cache_array(caches):
+    """ctypes array of the bpkv_cache structs of several layers (for bpkv_decode_step)."""
+    arr = (bpkv_cache * len(caches))(*[c.c for c in caches])
+    return arr
+
+
+def sync_n_max(caches, arr):
+    """Copy n_max back from a cache array after bpkv_decode_step raised it."""
+    for c, s in zip(caches, arr):
+        c.c.n_max = s.n_max
+
+
+__all__ = [n for n in dir() if n.startswith("bpkv_")] + ["Cache", "cache_array", "sync_n_max", "BpkvError"]
+_ = ctypes

@@ -1,0 +1,254 @@
+/*
+ * bpkv.h - C ABI of libbpkv: query-dependent prefix reads of a bit-plane K
+ * cache during decode, on one GB300 (sm_103a).
+ *
+ * The method is the one of "Fathom: per-query read depth for sparse decoding
+ * over an offloaded KV cache" (the Fathom page):
+ *   section 3.2   keys as 4-bit per-channel uniform symmetric codes, one fp16
+ *                 scale per 64-token block, stored as channel-major bit planes;
+ *   section 1     (observation 1) per-query depth per channel by reverse
+ *                 water-filling on g_j 4^-t_j; (observation 2) the first t planes
+ *                 of a channel are its t-bit mid-rise quantiser;
+ *   section 3.1   Eq. 1: the scan reads b n / 8 bytes per (sequence, layer, KV
+ *                 head), the winner rows k_U R;
+ *   section 2     ("Top-k decoding") 4 sink and 32 recent tokens always kept,
+ *                 the other k - 36 are each query head's top scores, exact
+ *                 attention over the selected set; ("SparQ") fixed channel sets
+ *                 ranked by the group's summed |q|.
+ *
+ * Conventions for every call:
+ *   - All pointers are caller-owned.  Device pointers unless stated otherwise.
+ *     The library allocates nothing: scratch comes from the caller's workspace
+ *     (size from bpkv_workspace_size).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *     enqueue work on it and return; results are ready when the stream is.
+ *   - Return value: BPKV_OK or a negative status.  Argument errors are detected
+ *     on the host before anything is enqueued.  BPKV_ECUDA reports a failed
+ *     launch (cudaGetLastError after enqueueing).  Errors found by kernels while
+ *     running are written to the workspace's status word; read it with
+ *     bpkv_read_status.
+ *   - Head dimension D = 128; group G in 1..8; cap_tokens a multiple of 512.
+ *   - Integer/bit outputs (planes, scales, depths, indices, union) are exact.
+ *     Scores are float32 sums; attention is float32 with float32 softmax.
+ */
+#ifndef BPKV_H
+#define BPKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------- status codes */
+#define BPKV_OK 0
+#define BPKV_EINVAL (-1)       /* invalid argument; nothing was enqueued */
+#define BPKV_ENOWORKSPACE (-2) /* workspace NULL or smaller than bpkv_workspace_size */
+#define BPKV_ECUDA (-3)        /* a CUDA launch or API call failed */
+#define BPKV_EUNSUPPORTED (-4) /* valid but unsupported shape (e.g. D != 128) */
+#define BPKV_EDEVICE (-5)      /* a kernel flagged an error in the status word */
+
+/* device status word bits (bpkv_read_status) */
+#define BPKV_DEV_OVERFLOW 1    /* append would pass cap_tokens; nothing written */
+#define BPKV_DEV_SELECT 2      /* a selection produced more rows than its output holds */
+
+#define BPKV_MAX_GROUP 8
+#define BPKV_HEAD_DIM 128
+
+/* ------------------------------------------------------------- the cache */
+/*
+ * One layer's cache for N sequences x H KV heads.  Layouts (row-major, last
+ * index fastest), NB = cap_tokens / 64:
+ *   planes  uint64 [N][H][D][4][NB]  word (j, p, b): bit i is bit (3 - p) of the
+ *                                    code of token 64 b + i (p = 0: most
+ *                                    significant bit = sign), so the first t
+ *                                    planes of channel j are t NB contiguous words
+ *   scales  uint16 [N][H][D][NB]     fp16 bit pattern of s = blockmax / 8
+ *                                    (round to nearest even, saturated at 65504)
+ *   k_rows  uint16 [N][H][cap][D]    bf16 keys as appended
+ *   v_rows  uint16 [N][H][cap][D]    bf16 values as appended
+ *   seq_len int64  [N]               device memory: tokens stored per sequence
+ * residency 0: planes, scales and rows are in device memory.  residency 1: they
+ * are in host memory the GPU can read (pinned with cudaHostAlloc/cudaHostRegister,
+ * or any memory on a system with address translation); kernels read them in
+ * place over the host link.  seq_len is always device memory.
+ * n_max is host state: an upper bound of every seq_len[i], used to size
+ * launches; bpkv_encode_append raises it.
+ */
+typedef struct bpkv_cache {
+  int32_t n_seq;
+  int32_t n_kv_heads;
+  int32_t group;
+  int32_t head_dim;
+  int64_t cap_tokens;
+  int64_t n_max;
+  int32_t residency;
+  int32_t reserved;
+  uint64_t *planes;
+  uint16_t *scales;
+  uint16_t *k_rows;
+  uint16_t *v_rows;
+  int64_t *seq_len;
+} bpkv_cache;
+
+/* ------------------------------------------------------------- workspace */
+#define BPKV_WS_SCAN_TOPK 1   /* bpkv_topk / bpkv_scan_topk */
+#define BPKV_WS_ATTEND 2      /* bpkv_sparse_attend */
+#define BPKV_WS_DENSE 4       /* bpkv_dense_attend */
+#define BPKV_WS_STEP 8        /* bpkv_decode_step (includes everything it needs) */
+
+/* Bytes of workspace the calls named in `what` (OR of BPKV_WS_*) need for this
+ * cache and selection size k.  0 on invalid arguments.  The workspace must be
+ * device memory aligned to 256 bytes; its first 256 bytes hold the status word. */
+size_t bpkv_workspace_size(const bpkv_cache *c, int32_t k, int32_t what);
+
+/* Clear the status word (enqueued on `stream`). */
+int bpkv_clear_status(void *ws, void *stream);
+
+/* Synchronise `stream`, then copy the status word to *status (0 = no error).
+ * Returns BPKV_EDEVICE when it is non-zero. */
+int bpkv_read_status(const void *ws, int32_t *status, void *stream);
+
+const char *bpkv_status_string(int status);
+int32_t bpkv_version(void);
+
+/* ------------------------------------------------------------- encode (F1, F2) */
+/*
+ * Fathom page section 3.2.  Append t_new tokens to every sequence: rows
+ * k_new/v_new [N][H][t_new][D] bf16 (device) are written at positions
+ * seq_len[i] .. seq_len[i]+t_new-1, every 64-token block they touch is
+ * (re)encoded from the stored rows (the open tail block is re-encoded because
+ * its blockmax, hence its scale, may grow), then seq_len[i] += t_new and
+ * c->n_max += t_new.  Per block and channel: a = max |k| over the tokens present,
+ * s = fp16(a / 8), c = clip(floor(k / s), -8, 7) + 8 (float32 IEEE division), all
+ * codes 8 when s rounds to 0; bits of absent tokens are 0.
+ * Errors: EINVAL when n_max + t_new > cap_tokens or t_new < 1.
+ */
+int bpkv_encode_append(bpkv_cache *c, const uint16_t *k_new, const uint16_t *v_new, int32_t t_new,
+                       void *stream);
+
+/* ------------------------------------------------------------- depths (F4, F5) */
+/*
+ * Fathom page section 1, observation 1.  For each (sequence, KV head):
+ * g_j = sum_h q_hj^2 sigma2_j over its G query heads (float32, heads in order,
+ * no fused multiply-add); items (j, t) for t = 0..3 with value g_j 4^-t; each
+ * costs 4 quarter-bits per token, plus 1 (the fp16 scale) for t = 0.  Items are
+ * taken in order of value (ties: lower channel first) until one has value <= 0
+ * or does not fit budget_q[i] quarter-bits.  depths[i][h][j] = bits taken.
+ *   q        float [N][H][G][D]
+ *   sigma2   float [N][H][D]   channel variances of the keys
+ *   budget_q int32 [N]         per-sequence budget in quarter-bits per token (4 b)
+ *   depths   uint8 [N][H][D]   out, values 0..4
+ */
+int bpkv_alloc_depths(const bpkv_cache *c, const float *q, const float *sigma2, const int32_t *budget_q,
+                      uint8_t *depths, void *stream);
+
+/*
+ * Fathom page section 2 ("SparQ", "thumbnail"): fixed-depth channel sets.  The
+ * n_channels channels with the largest sum_h |q_hj| (float32, heads in order,
+ * ties to the lower index) get depth `depth`, the others 0.  n_channels >= D
+ * reads all channels (the 2-bit thumbnail: n_channels = 128, depth = 2; the
+ * 136-bit SparQ r = 32 set: 32, 4).
+ */
+int bpkv_fixed_depths(const bpkv_cache *c, const float *q, int32_t n_channels, int32_t depth,
+                      uint8_t *depths, void *stream);
+
+/* ------------------------------------------------------------- scan (F3, F7) */
+/*
+ * Fathom page sections 1 and 3.1.  score[i][h][g][x] = sum_j q_gj khat_xj(t_j)
+ * for every token x < seq_len[i], where for t = depths[i][h][j] > 0
+ * khat = s ((c_t + 1/2) 2^(4-t) - 8), c_t the first t planes of the code and
+ * s the block scale; channels with t = 0 are not read.  No 1/sqrt(D) factor.
+ *   scores float [N][H][G][ld_scores], ld_scores >= n_max; entries past
+ *   seq_len[i] are not written.
+ */
+int bpkv_scan(const bpkv_cache *c, const float *q, const uint8_t *depths, float *scores, int64_t ld_scores,
+              void *stream);
+
+/* ------------------------------------------------------------- select (F8, F9) */
+/*
+ * Fathom page section 2 ("Top-k decoding").  For each query head, tokens
+ * [0, n_sink) and [n - n_recent, n) plus the k - n_sink - n_recent highest
+ * scores among the rest (ties: lower token index); all n tokens when those are
+ * at most k.  idx [N][H][G][k] int32 out: ascending token indices, -1 padded.
+ * Needs workspace BPKV_WS_SCAN_TOPK.  k >= n_sink + n_recent, k <= 8192.
+ */
+int bpkv_topk(const bpkv_cache *c, const float *scores, int64_t ld_scores, int32_t k, int32_t n_sink,
+              int32_t n_recent, int32_t *idx, void *ws, size_t ws_bytes, void *stream);
+
+/* bpkv_scan into the workspace followed by bpkv_topk. */
+int bpkv_scan_topk(const bpkv_cache *c, const float *q, const uint8_t *depths, int32_t k, int32_t n_sink,
+                   int32_t n_recent, int32_t *idx, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * GQA union of one KV head's G selections (Fathom page sections 1 and 3.1:
+ * k_U <= G k distinct winner rows per KV head, fetched once).
+ *   idx   int32 [N][H][G][k] ascending, -1 padded (as bpkv_topk writes it)
+ *   uidx  int32 [N][H][G*k]  out: distinct rows ascending, -1 padded
+ *   umask uint8 [N][H][G*k]  out: bit g set when query head g selected the row
+ *   ucount int32 [N][H]      out: union size
+ * G * k <= 16384.
+ */
+int bpkv_union(const bpkv_cache *c, const int32_t *idx, int32_t k, int32_t *uidx, uint8_t *umask,
+               int32_t *ucount, void *stream);
+
+/* ------------------------------------------------------------- attention (F10) */
+/*
+ * Fathom page section 2: exact attention of each query head over its own
+ * selected rows, o_g = sum_x softmax_x(q_g . k_x / sqrt(D)) v_x with the stored
+ * bf16 rows, read once per union row for all G heads (split over row chunks,
+ * combined with log-sum-exp).  A head with no selected row gets zeros.
+ *   uidx/umask/ucount as bpkv_union writes them, u_cap = their row stride (G k)
+ *   out float [N][H][G][D]
+ * Needs workspace BPKV_WS_ATTEND.
+ */
+int bpkv_sparse_attend(const bpkv_cache *c, const float *q, const int32_t *uidx, const uint8_t *umask,
+                       const int32_t *ucount, int32_t u_cap, float *out, void *ws, size_t ws_bytes,
+                       void *stream);
+
+/* Dense bf16 attention over every stored row (the dense baseline), same output
+ * layout.  Needs workspace BPKV_WS_DENSE. */
+int bpkv_dense_attend(const bpkv_cache *c, const float *q, float *out, void *ws, size_t ws_bytes,
+                      void *stream);
+
+/* ------------------------------------------------------------- decode step */
+#define BPKV_DEPTH_WATERFILL 0  /* bpkv_alloc_depths with sigma2 and budget_q */
+#define BPKV_DEPTH_FIXED 1      /* bpkv_fixed_depths(fixed_channels, fixed_depth) */
+#define BPKV_DEPTH_DENSE 2      /* no scan: dense attention over all rows */
+
+typedef struct bpkv_step_args {
+  const uint16_t *k_new;    /* [L][N][H][D] bf16: the one new token per sequence and layer */
+  const uint16_t *v_new;    /* [L][N][H][D] bf16 */
+  const float *q;           /* [L][N][H][G][D] */
+  const float *sigma2;      /* [L][N][H][D] (water-filling only) */
+  const int32_t *budget_q;  /* [N] quarter-bits per token (water-filling only) */
+  int32_t depth_rule;       /* BPKV_DEPTH_* */
+  int32_t fixed_channels;   /* BPKV_DEPTH_FIXED */
+  int32_t fixed_depth;      /* BPKV_DEPTH_FIXED */
+  int32_t k, n_sink, n_recent;
+  float *out;               /* [L][N][H][G][D] */
+  uint8_t *depths_out;      /* optional [L][N][H][D], NULL to skip */
+  int32_t *idx_out;         /* optional [L][N][H][G][k], NULL to skip */
+  void *const *stage_events;/* optional [L][BPKV_STAGE_EVENTS] cudaEvent_t, NULL to skip:
+                               recorded on `stream` (as external events, so they also
+                               time graph replays) before encode, depths, scan, top-k,
+                               union, attention and after attention */
+} bpkv_step_args;
+
+#define BPKV_STAGE_EVENTS 7
+
+/*
+ * One decode step over n_layers layers (each its own bpkv_cache, same shapes):
+ * append the new token (encode), choose depths, scan + top-k, union, sparse
+ * attention (or dense attention for BPKV_DEPTH_DENSE).  Every layer's n_max is
+ * raised by one.  Needs workspace BPKV_WS_STEP.
+ */
+int bpkv_decode_step(bpkv_cache *layers, int32_t n_layers, const bpkv_step_args *a, void *ws,
+                     size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BPKV_H */

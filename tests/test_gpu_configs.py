@@ -1,0 +1,84 @@
+"""Whole decode steps on the five workload shapes, through bpkv_decode_step in
+the launch configuration the bench times, checked against the oracle on every
+unit (small shapes) or on sampled (sequence, KV head) units (full sizes)."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import check_unit, decode_one_layer
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pk():
+    import __graft_entry__
+    __graft_entry__.build()
+    import bit_plane_kv_encode_gb300 as m
+    return m
+
+
+def test_tiny_all_units(pk, orc):
+    from workload import CONFIGS, gen_layer
+    cfg = CONFIGS["tiny"]
+    inp = gen_layer(cfg, 0, device="cpu")
+    cache, d, idx, out = decode_one_layer(inp, cfg)
+    same, _ = check_unit(orc, cfg, inp, cache, d, idx, out, 0, 0, what="tiny")
+    assert same >= 3
+
+
+@pytest.mark.parametrize("budget", [68, 92, 136])
+def test_qwen3_layer_all_units(pk, orc, budget):
+    from workload import CONFIGS, gen_layer
+    cfg = CONFIGS["qwen3_8b_layer"]
+    inp = gen_layer(cfg, 0, device="cuda")
+    inp.k, inp.v = inp.k.cpu(), inp.v.cpu()
+    b = torch.full((cfg.n_seq,), budget, dtype=torch.int32)
+    cache, d, idx, out = decode_one_layer(inp, cfg, budgets=b)
+    same_total, found = 0, 0
+    for h in range(cfg.n_kv_heads):
+        same, _ = check_unit(orc, cfg, inp, cache, d, idx, out, 0, h, budget_bits=budget, what=f"b{budget} h{h}")
+        same_total += same
+        sel = set(idx[0, h].flatten().tolist())
+        found += sum(int(p) in sel for p in inp.needles[0, h])
+    assert same_total >= cfg.n_kv_heads * cfg.group // 2
+    # quality, not parity: planted high |q.k| keys are found by some head of their KV head
+    assert found >= 0.9 * inp.needles.numel()
+
+
+@pytest.mark.parametrize("rule,fixed", [(1, (32, 4)), (1, (128, 2))])
+def test_full_step_layer_fixed_sampled(pk, orc, rule, fixed):
+    from workload import CONFIGS, gen_layer
+    cfg = CONFIGS["full_step"]
+    inp = gen_layer(cfg, 5, device="cuda")
+    cache, d, idx, out = decode_one_layer(inp, cfg, depth_rule=rule, fixed=fixed)
+    inp.k, inp.v = inp.k.cpu(), inp.v.cpu()
+    for (s, h) in [(0, 0), (3, 7)]:
+        check_unit(orc, cfg, inp, cache, d, idx, out, s, h, depth_rule=rule, fixed=fixed, what=f"fixed{fixed}")
+
+
+def test_full_step_layer_waterfill_sampled(pk, orc):
+    from workload import CONFIGS, gen_layer
+    cfg = CONFIGS["full_step"]
+    inp = gen_layer(cfg, 17, device="cuda")
+    b = torch.tensor([32, 68, 104, 136], dtype=torch.int32)
+    cache, d, idx, out = decode_one_layer(inp, cfg, budgets=b)
+    inp.k, inp.v = inp.k.cpu(), inp.v.cpu()
+    for (s, h) in [(0, 3), (1, 0), (2, 5), (3, 7)]:
+        check_unit(orc, cfg, inp, cache, d, idx, out, s, h, budget_bits=int(b[s]), what=f"s{s}h{h}")
+
+
+def test_multi_session_sampled(pk, orc):
+    from workload import CONFIGS, gen_layer
+    cfg = CONFIGS["multi_session"]
+    inp = gen_layer(cfg, 0, device="cuda")
+    cache, d, idx, out = decode_one_layer(inp, cfg)
+    inp.k, inp.v = inp.k.cpu(), inp.v.cpu()
+    for (s, h) in [(0, 0), (7, 3), (19, 6), (31, 7)]:
+        check_unit(orc, cfg, inp, cache, d, idx, out, s, h, what=f"s{s}h{h}")
+    # every sequence's depth vectors respect its own budget
+    from workload.bytes_model import depth_quarter_bits
+    dd = d.cpu().numpy()
+    for s in range(cfg.n_seq):
+        for h in range(cfg.n_kv_heads):
+            assert depth_quarter_bits(dd[s, h]) <= 4 * int(inp.budgets[s])

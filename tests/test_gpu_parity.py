@@ -1,0 +1,246 @@
+"""CUDA path vs CPU oracle, kernel by kernel, through the C ABI.
+
+Bars: planes, scales, depths, indices and unions bit-exact; scores within
+1e-5 max(|oracle|, sum_j |q_j khat_j|); top-k sets equal except keys within
+1e-4 max|score| of the k-th score; attention within 2e-3 max-abs.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import (ATTN_ATOL, abs_score_scale, bits16, bits64, build_cache, check_scores,
+                         check_topk_sets)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pk():
+    import __graft_entry__
+    __graft_entry__.build()
+    import bit_plane_kv_encode_gb300 as m
+    return m
+
+
+def _rand_kv(N, H, n, seed, scale=None, dev="cuda"):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    D = 128
+    sig = torch.exp(0.75 * torch.randn((N, H, 1, D), generator=g)) if scale is None else scale
+    k = (torch.randn((N, H, n, D), generator=g) * sig).to(torch.bfloat16)
+    v = torch.randn((N, H, n, D), generator=g).to(torch.bfloat16)
+    return k.to(dev), v.to(dev)
+
+
+# ------------------------------------------------------------------ encode
+
+@pytest.mark.parametrize("n,chunks", [(4096, None), (64 * 3 + 17, [1] * 70 + [63, 1, 64, 65]),
+                                      (1000, [500, 1, 1, 1, 200]), (64, [64]), (1, [1])])
+def test_encode_bitexact(pk, orc, n, chunks):
+    N, H = 2, 3
+    k, v = _rand_kv(N, H, n, seed=n)
+    k[0, 1, :, 5] = 0                                      # an all-zero channel
+    k[1, 2, : min(n, 40), 7] = torch.tensor(3.0e38).to(torch.bfloat16)  # scale saturates
+    c = build_cache(k, v, group=4, chunks=chunks)
+    torch.cuda.synchronize()
+    assert c.n_max == n and c.seq_len.tolist() == [n] * N
+    nb_cap = c.c.cap_tokens // 64
+    for s in range(N):
+        for h in range(H):
+            sc, pl = orc.encode(bits16(k[s, h]), nb_cap)
+            nb = (n + 63) // 64
+            assert np.array_equal(bits64(c.planes[s, h])[:, :, :nb], pl[:, :, :nb]), (s, h)
+            assert np.array_equal(bits16(c.scales[s, h])[:, :nb], sc[:, :nb]), (s, h)
+            assert torch.equal(c.k_rows[s, h, :n], k[s, h]) and torch.equal(c.v_rows[s, h, :n], v[s, h])
+
+
+def test_encode_token_by_token_equals_bulk(pk):
+    k, v = _rand_kv(1, 2, 300, seed=5)
+    bulk = build_cache(k, v, 4)
+    inc = build_cache(k, v, 4, chunks=[1] * 300)
+    torch.cuda.synchronize()
+    nb = (300 + 63) // 64
+    assert torch.equal(bulk.planes[..., :nb], inc.planes[..., :nb])
+    assert torch.equal(bulk.scales[..., :nb], inc.scales[..., :nb])
+
+
+def test_encode_rejects_overflow(pk):
+    k, v = _rand_kv(1, 1, 512, seed=6)
+    c = build_cache(k, v, 4, cap=512)
+    with pytest.raises(pk.BpkvError):
+        c.append(k[:, :, :1].contiguous(), v[:, :, :1].contiguous())
+
+
+# ------------------------------------------------------------------ depths
+
+def _depth_inputs(N, H, G, seed):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    q = torch.randn((N, H, G, 128), generator=g)
+    s2 = torch.exp(torch.randn((N, H, 128), generator=g) * 1.5)
+    q[0, 0] = 1.0          # equal g everywhere: all ties
+    s2[0, 0] = 1.0
+    q[0, 1, :, 10:20] = 0  # worthless channels
+    s2[1 % N, 1, 3] = 0
+    q[0, 2, :, 64:] = q[0, 2, :, :64]  # pairwise ties
+    s2[0, 2, 64:] = s2[0, 2, :64]
+    return q, s2
+
+
+@pytest.mark.parametrize("budget", [0, 1, 4, 5, 32, 44, 68, 92, 136, 200, 288, 544, 10000])
+def test_alloc_depths_bitexact(pk, orc, budget):
+    N, H, G = 3, 4, 4
+    q, s2 = _depth_inputs(N, H, G, seed=budget)
+    k, v = _rand_kv(N, H, 64, seed=1)
+    c = build_cache(k, v, G)
+    bq = torch.tensor([budget * 4, budget * 4 + 3, max(budget * 4 - 1, 0)], dtype=torch.int32)
+    d = torch.zeros((N, H, 128), dtype=torch.uint8, device="cuda")
+    pk.bpkv_alloc_depths(c.c, q.cuda(), s2.cuda(), bq.cuda(), d)
+    got = d.cpu().numpy()
+    for s in range(N):
+        for h in range(H):
+            want = orc.alloc_depths(q[s, h].numpy(), s2[s, h].numpy(), int(bq[s]))
+            assert np.array_equal(got[s, h], want), (s, h, budget)
+
+
+@pytest.mark.parametrize("r,t", [(32, 4), (16, 4), (128, 2), (0, 4), (200, 1), (7, 3)])
+def test_fixed_depths_bitexact(pk, orc, r, t):
+    N, H, G = 2, 3, 4
+    q, _ = _depth_inputs(N, H, G, seed=r * 10 + t)
+    k, v = _rand_kv(N, H, 64, seed=2)
+    c = build_cache(k, v, G)
+    d = torch.zeros((N, H, 128), dtype=torch.uint8, device="cuda")
+    pk.bpkv_fixed_depths(c.c, q.cuda(), r, t, d)
+    got = d.cpu().numpy()
+    for s in range(N):
+        for h in range(H):
+            assert np.array_equal(got[s, h], orc.fixed_depths(q[s, h].numpy(), r, t)), (s, h)
+
+
+# ------------------------------------------------------------------ scan
+
+@pytest.mark.parametrize("n,G,depth_kind", [(4096, 4, "water68"), (5000 + 17, 4, "random"), (777, 8, "full"),
+                                            (2048, 1, "thumb"), (130, 4, "water136"), (3, 2, "random")])
+def test_scan_scores(pk, orc, n, G, depth_kind):
+    N, H = 2, 2
+    k, v = _rand_kv(N, H, n, seed=n + G)
+    c = build_cache(k, v, G)
+    g = torch.Generator(device="cpu").manual_seed(7)
+    q = torch.randn((N, H, G, 128), generator=g)
+    if depth_kind == "random":
+        d = torch.randint(0, 5, (N, H, 128), generator=g, dtype=torch.uint8)
+    elif depth_kind == "full":
+        d = torch.full((N, H, 128), 4, dtype=torch.uint8)
+    elif depth_kind == "thumb":
+        d = torch.full((N, H, 128), 2, dtype=torch.uint8)
+    else:
+        b = int(depth_kind[5:])
+        s2 = torch.exp(torch.randn((N, H, 128), generator=g))
+        d = torch.stack([torch.stack([torch.from_numpy(orc.alloc_depths(q[s, h].numpy(), s2[s, h].numpy(), 4 * b))
+                                      for h in range(H)]) for s in range(N)])
+    scores = torch.full((N, H, G, c.c.cap_tokens), float("nan"), device="cuda")
+    pk.bpkv_scan(c.c, q.cuda(), d.cuda(), scores, c.c.cap_tokens)
+    got = scores.cpu().numpy()
+    nb_cap = c.c.cap_tokens // 64
+    for s in range(N):
+        for h in range(H):
+            kb = bits16(k[s, h])
+            sc, pl = orc.encode(kb, nb_cap)
+            ref = orc.scores(n, sc, pl, d[s, h].numpy(), q[s, h].numpy())
+            scale = abs_score_scale(q[s, h].numpy(), kb, d[s, h].numpy())
+            check_scores(got[s, h, :, :n], ref, scale, what=f"{depth_kind} s{s} h{h}")
+            assert np.isnan(got[s, h, :, n:]).all()  # nothing written past seq_len
+
+
+# ------------------------------------------------------------------ top-k / union
+
+@pytest.mark.parametrize("n,k,ties", [(4096, 64, 0.0), (4096, 64, 0.5), (100, 64, 0.3), (64, 64, 0.0),
+                                      (37, 36, 0.0), (1000, 36, 0.2), (20000, 512, 0.9), (5, 64, 0.0),
+                                      (600, 512, 0.0), (3000, 1024, 0.7)])
+def test_topk_exact_on_given_scores(pk, orc, n, k, ties):
+    from workload.gen import random_scores
+    N, H, G = 1, 2, 4
+    kk, vv = _rand_kv(N, H, n, seed=3)
+    c = build_cache(kk, vv, G)
+    sc = random_scores(N * H * G, n, seed=n + k, tie_frac=ties).reshape(N, H, G, n)
+    ld = c.c.cap_tokens
+    buf = torch.zeros((N, H, G, ld), device="cuda")
+    buf[..., :n] = sc.cuda()
+    idx = torch.zeros((N, H, G, k), dtype=torch.int32, device="cuda")
+    ws = c.workspace(k, pk.WS_SCAN_TOPK)
+    pk.bpkv_clear_status(ws)
+    pk.bpkv_topk(c.c, buf, ld, k, 4, 32, idx, ws, ws.numel())
+    assert pk.bpkv_read_status(ws) == 0
+    got = idx.cpu().numpy()
+    for h in range(H):
+        for g in range(G):
+            want = orc.topk(sc[0, h, g].numpy().astype(np.float64), k)
+            assert np.array_equal(got[0, h, g], want), (h, g)
+
+
+def test_union_exact(pk, orc):
+    N, H, G, k, n = 2, 3, 4, 64, 3000
+    kk, vv = _rand_kv(N, H, n, seed=4)
+    c = build_cache(kk, vv, G)
+    g = torch.Generator(device="cpu").manual_seed(9)
+    idx = torch.full((N, H, G, k), -1, dtype=torch.int32)
+    for s in range(N):
+        for h in range(H):
+            for q in range(G):
+                m = int(torch.randint(0, k + 1, (1,), generator=g))
+                pool = 200 if (s + h) % 2 else n  # heavy overlap in some units
+                idx[s, h, q, :m] = torch.sort(torch.randperm(pool, generator=g)[:m].to(torch.int32)).values
+    uidx = torch.zeros((N, H, G * k), dtype=torch.int32, device="cuda")
+    umask = torch.zeros((N, H, G * k), dtype=torch.uint8, device="cuda")
+    ucnt = torch.zeros((N, H), dtype=torch.int32, device="cuda")
+    pk.bpkv_union(c.c, idx.cuda(), k, uidx, umask, ucnt)
+    for s in range(N):
+        for h in range(H):
+            wu, wm = orc.union(idx[s, h].numpy())
+            u = int(ucnt[s, h])
+            assert u == len(wu)
+            assert np.array_equal(uidx[s, h, :u].cpu().numpy(), wu)
+            assert np.array_equal(umask[s, h, :u].cpu().numpy(), wm)
+            assert (uidx[s, h, u:] == -1).all()
+
+
+# ------------------------------------------------------------------ attention
+
+@pytest.mark.parametrize("n,k", [(4096, 64), (700, 512), (40, 64), (20000, 512)])
+def test_sparse_attend(pk, orc, n, k):
+    N, H, G = 2, 2, 4
+    kk, vv = _rand_kv(N, H, n, seed=n, scale=2.0)
+    c = build_cache(kk, vv, G)
+    g = torch.Generator(device="cpu").manual_seed(11)
+    q = torch.randn((N, H, G, 128), generator=g)
+    idx = torch.zeros((N, H, G, k), dtype=torch.int32)
+    refs = {}
+    for s in range(N):
+        for h in range(H):
+            for qh in range(G):
+                score = torch.randn(n, generator=g).numpy().astype(np.float64)
+                idx[s, h, qh] = torch.from_numpy(orc.topk(score, k))
+            refs[s, h] = orc.attend(q[s, h].numpy(), bits16(kk[s, h]), bits16(vv[s, h]), idx[s, h].numpy())
+    uidx = torch.zeros((N, H, G * k), dtype=torch.int32, device="cuda")
+    umask = torch.zeros((N, H, G * k), dtype=torch.uint8, device="cuda")
+    ucnt = torch.zeros((N, H), dtype=torch.int32, device="cuda")
+    pk.bpkv_union(c.c, idx.cuda(), k, uidx, umask, ucnt)
+    out = torch.zeros((N, H, G, 128), device="cuda")
+    ws = c.workspace(k, pk.WS_ATTEND)
+    pk.bpkv_sparse_attend(c.c, q.cuda(), uidx, umask, ucnt, G * k, out, ws, ws.numel())
+    got = out.cpu().numpy()
+    for (s, h), r in refs.items():
+        assert np.max(np.abs(got[s, h] - r)) <= ATTN_ATOL, (s, h, np.max(np.abs(got[s, h] - r)))
+
+
+@pytest.mark.parametrize("n", [1, 100, 4096, 5000])
+def test_dense_attend(pk, orc, n):
+    N, H, G = 1, 2, 4
+    kk, vv = _rand_kv(N, H, n, seed=n + 1, scale=2.0)
+    c = build_cache(kk, vv, G)
+    q = torch.randn((N, H, G, 128), generator=torch.Generator().manual_seed(3))
+    out = torch.zeros((N, H, G, 128), device="cuda")
+    ws = c.workspace(1, pk.WS_DENSE)
+    pk.bpkv_dense_attend(c.c, q.cuda(), out, ws, ws.numel())
+    got = out.cpu().numpy()
+    for h in range(H):
+        ref = orc.dense_attend(q[0, h].numpy(), bits16(kk[0, h]), bits16(vv[0, h]), n)
+        assert np.max(np.abs(got[0, h] - ref)) <= ATTN_ATOL
