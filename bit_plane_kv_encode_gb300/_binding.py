@@ -55,6 +55,7 @@ _SIGS = {
     "bpkv_scan": ([P, P, P, P, i64, P], ctypes.c_int),
     "bpkv_topk": ([P, P, i64, i32, i32, i32, P, P, sz, P], ctypes.c_int),
     "bpkv_scan_topk": ([P, P, P, i32, i32, i32, P, P, sz, P], ctypes.c_int),
+    "bpkv_scan_topk_noalloc": ([P, P, P, i32, i32, i32, P, P], ctypes.c_int),
     "bpkv_union": ([P, P, i32, P, P, P, P], ctypes.c_int),
     "bpkv_sparse_attend": ([P, P, P, P, P, i32, P, P, sz, P], ctypes.c_int),
     "bpkv_dense_attend": ([P, P, P, P, sz, P], ctypes.c_int),
@@ -176,6 +177,12 @@ def bpkv_scan_topk(cache, q, depths, k: int, n_sink: int, n_recent: int, idx, ws
     return _check("bpkv_scan_topk",
                   load().bpkv_scan_topk(ctypes.byref(cache), _ptr(q), _ptr(depths), int(k), int(n_sink),
                                         int(n_recent), _ptr(idx), _ptr(ws), int(ws_bytes), _stream(stream)))
+
+
+def bpkv_scan_topk_noalloc(cache, q, depths, k: int, n_sink: int, n_recent: int, idx, stream=None):
+    return _check("bpkv_scan_topk_noalloc",
+                  load().bpkv_scan_topk_noalloc(ctypes.byref(cache), _ptr(q), _ptr(depths), int(k), int(n_sink),
+                                                int(n_recent), _ptr(idx), _stream(stream)))
 
 
 def bpkv_union(cache, idx, k: int, uidx, umask, ucount, stream=None):

@@ -182,6 +182,25 @@ int bpkv_scan_topk(const bpkv_cache *c, const float *q, const uint8_t *depths, i
                    int32_t n_recent, int32_t *idx, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * bpkv_scan_topk without a workspace, for callers that cannot allocate device
+ * memory: for example a host program whose own pool already holds all of the
+ * GPU's memory, or a loop that must not pay the device-wide synchronisation a
+ * cudaMalloc/cudaFree can cause.  The Fathom page has no counterpart of this
+ * call; its results are identical to bpkv_scan_topk's.
+ * The score scratch is a fixed 16 MiB array built into the library, held on
+ * every GPU that loads the library until the process exits; requests needing
+ * more (N * H * G * round_up(n_max, 64) * 4 bytes > 16 MiB) return
+ * BPKV_ENOWORKSPACE.  The call allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library routine).  Its first call on a device looks up the
+ * array's device address once (with that device current); make that first
+ * call before any stream capture.  All calls on a device share the one array,
+ * so calls whose work overlaps on the GPU (other streams, other threads) race
+ * and must be serialised by the caller.  No device status word is reported.
+ */
+int bpkv_scan_topk_noalloc(const bpkv_cache *c, const float *q, const uint8_t *depths, int32_t k,
+                           int32_t n_sink, int32_t n_recent, int32_t *idx, void *stream);
+
+/*
  * GQA union of one KV head's G selections (Fathom page sections 1 and 3.1:
  * k_U <= G k distinct winner rows per KV head, fetched once).
  *   idx   int32 [N][H][G][k] ascending, -1 padded (as bpkv_topk writes it)
