@@ -1,12 +1,14 @@
 // Selection (Fathom page, section 2, "Top-k decoding") and the GQA union of
 // winner rows (section 1 / section 3.1: k_U <= G k distinct rows per KV head).
 //
-// Top-k: one CTA per query head.  An exact radix select over order-preserving
-// 32-bit keys of the candidate scores (8 bits per pass, most significant
-// first) finds the key of the (k - n_sink - n_recent)-th largest candidate and
-// how many candidates equal to it are still needed; an ordered compaction then
-// writes sinks, recent tokens, every candidate above that key and the
-// lowest-index candidates equal to it, in ascending token order.
+// Top-k: one CTA per query head.  Scores map to order-preserving 32-bit keys.
+// A histogram of the top 11 key bits over the candidates (tokens that are
+// neither sinks nor recent) locates the bucket holding the
+// (k - n_sink - n_recent)-th largest key; if that bucket is crowded the next 11
+// bits (then the last 10) refine it.  One more pass takes every key above the
+// bucket and gathers the bucket's keys, which a shared-memory bitonic sort by
+// (key desc, index asc) cuts at the exact count: ties go to the lower index.
+// Sinks, recent tokens and the winners are finally sorted ascending.
 //
 // Union: one CTA per KV head.  Each sorted list entry's rank in the merge of
 // the G lists is its own position plus binary-search counts in the other
@@ -55,7 +57,54 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* warp_t
   return r;
 }
 
+constexpr int kHistBits = 11;
+constexpr int kHistBins = 1 << kHistBits;
+constexpr int kCandCap = 4096;       // candidates kept from the threshold bucket
+constexpr int kSelCap = 8192;        // selected indices (k <= 8192)
+
+struct TopkSmem {
+  uint32_t hist[kHistBins];
+  unsigned long long cand[kCandCap];   // (key << 32) | ~index: larger = earlier
+  int32_t sel[kSelCap];
+  uint32_t warp_tot[32];
+  uint32_t n_cand, n_sel, digit, rem, tot;
+};
+
+// Bitonic sort of v[0..n2) (n2 a power of two) by the whole 64-bit value;
+// descending when desc, else ascending.  Called by the whole block.
+template <typename T>
+__device__ void block_bitonic(T* v, int n2, bool desc) {
+  for (int size = 2; size <= n2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int t = threadIdx.x; t < n2 / 2; t += blockDim.x) {
+        const int i = 2 * t - (t & (stride - 1));
+        const int j = i + stride;
+        const bool d = ((i & size) == 0) == desc;
+        const T x = v[i], y = v[j];
+        if ((x < y) == d) {
+          v[i] = y;
+          v[j] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+__device__ __forceinline__ void sel_push(TopkSmem& S, int32_t i) {
+  const uint32_t p = atomicAdd(&S.n_sel, 1u);
+  if (p < (uint32_t)kSelCap) S.sel[p] = i;
+}
+
+__device__ __forceinline__ int pow2_at_least(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
 __global__ void __launch_bounds__(kSelThreads) k_topk(TopkArgs a) {
+  extern __shared__ __align__(16) unsigned char topk_raw[];
+  TopkSmem& S = *reinterpret_cast<TopkSmem*>(topk_raw);
   const int row = blockIdx.x;
   const int s = row / (a.n_heads * a.group);
   const int64_t n = a.seq_len[s];
@@ -66,32 +115,39 @@ __global__ void __launch_bounds__(kSelThreads) k_topk(TopkArgs a) {
   const int64_t n_top = max(a.k - a.n_sink - a.n_recent, 0);
   const int tid = threadIdx.x;
 
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t warp_tot[32];
-  __shared__ uint32_t tot;
-  __shared__ uint32_t sh_digit;
-  __shared__ int64_t sh_rem;
+  if (tid == 0) {
+    S.n_cand = 0;
+    S.n_sel = 0;
+  }
+  __syncthreads();
+  // fixed tokens
+  for (int64_t i = tid; i < lo; i += kSelThreads) sel_push(S, (int32_t)i);
+  for (int64_t i = hi + tid; i < n; i += kSelThreads) sel_push(S, (int32_t)i);
 
-  const bool select_all = (hi - lo) <= n_top;
-  uint32_t thr = 0xFFFFFFFFu;  // with n_top == 0 no candidate passes
-  int64_t need = 0;
-  if (!select_all && n_top > 0) {
+  if (hi - lo <= n_top) {
+    for (int64_t i = lo + tid; i < hi; i += kSelThreads) sel_push(S, (int32_t)i);
+  } else if (n_top > 0) {
+    // Threshold bucket: up to three levels (11, 11, 10 bits), stopping once the
+    // bucket holding the n_top-th largest key has at most kCandCap keys.
     uint32_t pref = 0, pmask = 0;
-    int64_t rem = n_top;
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
-      if (tid < 256) hist[tid] = 0;
+    uint32_t rem = (uint32_t)n_top;
+    const int shifts[3] = {21, 10, 0};
+    const int widths[3] = {11, 11, 10};
+    for (int lvl = 0; lvl < 3; ++lvl) {
+      const int shift = shifts[lvl], nb = 1 << widths[lvl];
+      for (int b = tid; b < nb; b += kSelThreads) S.hist[b] = 0;
       __syncthreads();
       for (int64_t i = lo + tid; i < hi; i += kSelThreads) {
         const uint32_t u = ordered_key(sc[i]);
-        if ((u & pmask) == pref) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+        if ((u & pmask) == pref) atomicAdd(&S.hist[(u >> shift) & (nb - 1)], 1u);
       }
       __syncthreads();
       if (tid < 32) {
-        // lane l owns digits 255 - 8l ... 248 - 8l (descending)
+        // lane l owns bins [nb - (l+1) nb/32, nb - l nb/32), scanned from the top
+        const int per = nb / 32;
+        const int top = nb - 1 - tid * per;
         uint32_t loc = 0;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) loc += hist[255 - 8 * tid - q];
+        for (int q = 0; q < per; ++q) loc += S.hist[top - q];
         uint32_t incl = loc;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -99,64 +155,85 @@ __global__ void __launch_bounds__(kSelThreads) k_topk(TopkArgs a) {
           if (tid >= o) incl += y;
         }
         const uint32_t excl = incl - loc;
-        const bool here = excl < (uint64_t)rem && (uint64_t)rem <= incl;
-        if (here) {
+        if (excl < rem && rem <= incl) {
           uint32_t cum = excl;
-          int d = 255 - 8 * tid;
-          for (int q = 0; q < 8; ++q, --d) {
-            const uint32_t hcount = hist[d];
-            if (cum + hcount >= (uint64_t)rem) break;
-            cum += hcount;
+          int d = top;
+          for (int q = 0; q < per; ++q, --d) {
+            if (cum + S.hist[d] >= rem) break;
+            cum += S.hist[d];
           }
-          sh_digit = (uint32_t)d;
-          sh_rem = rem - cum;
+          S.digit = (uint32_t)d;
+          S.rem = rem - cum;
         }
       }
       __syncthreads();
-      pref |= sh_digit << shift;
-      pmask |= 255u << shift;
-      rem = sh_rem;
+      const uint32_t dgt = S.digit;
+      rem = S.rem;
+      pref |= dgt << shift;
+      pmask |= (uint32_t)(nb - 1) << shift;
+      const bool done = S.hist[dgt] <= (uint32_t)kCandCap;
       __syncthreads();
+      if (done) break;
     }
-    thr = pref;
-    need = rem;
-  }
-
-  // Ordered compaction over all n tokens.
-  uint32_t carry_sel = 0, carry_tie = 0;
-  for (int64_t base = 0; base < n; base += kSelThreads) {
-    const int64_t i = base + tid;
-    uint32_t fsel = 0, ftie = 0;
-    if (i < n) {
-      if (i < lo || i >= hi || select_all) {
-        fsel = 1;
-      } else {
+    // keys above the bucket are selected; keys in it are candidates
+    const uint32_t above = pref | ~pmask;
+    const bool exact = pmask == 0xFFFFFFFFu && S.hist[pref & (kHistBins / 2 - 1)] > (uint32_t)kCandCap;
+    if (!exact) {
+      for (int64_t i = lo + tid; i < hi; i += kSelThreads) {
         const uint32_t u = ordered_key(sc[i]);
-        if (u > thr) fsel = 1;
-        else if (u == thr) ftie = 1;
+        if (u > above) {
+          sel_push(S, (int32_t)i);
+        } else if ((u & pmask) == pref) {
+          const uint32_t c = atomicAdd(&S.n_cand, 1u);
+          if (c < (uint32_t)kCandCap)
+            S.cand[c] = ((unsigned long long)u << 32) | (0xFFFFFFFFu - (uint32_t)i);
+        }
+      }
+      __syncthreads();
+      const int nc = (int)min(S.n_cand, (uint32_t)kCandCap);
+      const int nc2 = pow2_at_least(max(nc, 2));
+      for (int e = nc + tid; e < nc2; e += kSelThreads) S.cand[e] = 0ull;
+      __syncthreads();
+      block_bitonic(S.cand, nc2, true);
+      for (int e = tid; e < (int)rem && e < nc; e += kSelThreads)
+        sel_push(S, (int32_t)(0xFFFFFFFFu - (uint32_t)S.cand[e]));
+    } else {
+      // more than kCandCap keys equal the threshold key: take the rem of them
+      // with the lowest indices by an ordered scan over the candidates
+      uint32_t carry = 0;
+      for (int64_t base = lo; base < hi; base += kSelThreads) {
+        const int64_t i = base + tid;
+        uint32_t tie = 0;
+        if (i < hi) {
+          const uint32_t u = ordered_key(sc[i]);
+          if (u > above) sel_push(S, (int32_t)i);
+          else if (u == pref) tie = 1;
+        }
+        const uint32_t ex = block_excl_scan(tie, S.warp_tot, &S.tot) + carry;
+        if (tie && ex < rem) sel_push(S, (int32_t)i);
+        carry += S.tot;
+        __syncthreads();
       }
     }
-    const uint32_t packed = fsel | (ftie << 16);
-    const uint32_t ex = block_excl_scan(packed, warp_tot, &tot);
-    const uint32_t ex_sel = (ex & 0xffffu) + carry_sel;
-    const uint32_t ex_tie = (ex >> 16) + carry_tie;
-    const bool take = fsel || (ftie && (int64_t)ex_tie < need);
-    if (take) {
-      const int64_t pos = (int64_t)ex_sel + min64(ex_tie, need);
-      if (pos < a.k) out[pos] = (int32_t)i;
-      else set_status(a.status, BPKV_DEV_SELECT);
-    }
-    carry_sel += tot & 0xffffu;
-    carry_tie += tot >> 16;
   }
-  const int64_t total = (int64_t)carry_sel + min64(carry_tie, need);
-  for (int64_t p = total + tid; p < a.k; p += kSelThreads) out[p] = -1;
+  __syncthreads();
+  const int ns = (int)S.n_sel;
+  if (ns > a.k && tid == 0) set_status(a.status, BPKV_DEV_SELECT);
+  const int cnt = min(ns, a.k);
+  const int n2 = pow2_at_least(max(cnt, 2));
+  for (int e = cnt + tid; e < n2; e += kSelThreads) S.sel[e] = 0x7FFFFFFF;
+  __syncthreads();
+  block_bitonic(S.sel, n2, false);
+  for (int e = tid; e < a.k; e += kSelThreads) out[e] = e < cnt ? S.sel[e] : -1;
 }
 
 cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
                         int32_t n_recent, int32_t* idx, int32_t* status, cudaStream_t st) {
   TopkArgs a{scores, ld, c.seq_len, idx, status, c.n_kv_heads, c.group, k, n_sink, n_recent};
-  k_topk<<<c.n_seq * c.n_kv_heads * c.group, kSelThreads, 0, st>>>(a);
+  const int smem = (int)sizeof(TopkSmem);
+  cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  k_topk<<<c.n_seq * c.n_kv_heads * c.group, kSelThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 

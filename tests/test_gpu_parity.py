@@ -244,3 +244,28 @@ def test_dense_attend(pk, orc, n):
     for h in range(H):
         ref = orc.dense_attend(q[0, h].numpy(), bits16(kk[0, h]), bits16(vv[0, h]), n)
         assert np.max(np.abs(got[0, h] - ref)) <= ATTN_ATOL
+
+
+@pytest.mark.parametrize("n_ties,n_above", [(10000, 100), (5000, 475), (6000, 0)])
+def test_topk_massive_ties(pk, orc, n_ties, n_above):
+    """More than 4096 scores equal to the threshold score: the lowest indices win."""
+    N, H, G, n, k = 1, 1, 4, 20000, 512
+    kk, vv = _rand_kv(N, H, n, seed=8)
+    c = build_cache(kk, vv, G)
+    g = torch.Generator(device="cpu").manual_seed(n_ties + n_above)
+    sc = torch.rand((N, H, G, n), generator=g) * 0.5          # below the tie value
+    for q in range(G):
+        perm = torch.randperm(n, generator=g)
+        sc[0, 0, q, perm[:n_ties]] = 1.0
+        sc[0, 0, q, perm[n_ties:n_ties + n_above]] = 2.0 + torch.rand(n_above, generator=g)
+    ld = c.c.cap_tokens
+    buf = torch.zeros((N, H, G, ld), device="cuda")
+    buf[..., :n] = sc.cuda()
+    idx = torch.zeros((N, H, G, k), dtype=torch.int32, device="cuda")
+    ws = c.workspace(k, pk.WS_SCAN_TOPK)
+    pk.bpkv_clear_status(ws)
+    pk.bpkv_topk(c.c, buf, ld, k, 4, 32, idx, ws, ws.numel())
+    assert pk.bpkv_read_status(ws) == 0
+    for q in range(G):
+        want = orc.topk(sc[0, 0, q].numpy().astype(np.float64), k)
+        assert np.array_equal(idx[0, 0, q].cpu().numpy(), want), q
