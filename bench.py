@@ -20,6 +20,8 @@ from __future__ import annotations
 
 import argparse
 import json
+
+import numpy as np
 import os
 import statistics
 import subprocess
@@ -45,6 +47,8 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--fused", action="store_true", help="one fused cluster kernel per pass where eligible")
+    p.add_argument("--budget", type=int, default=0, help="run this budget only (bits/token)")
     return p.parse_args()
 
 
@@ -126,65 +130,107 @@ class Clocks:
 
 # ------------------------------------------------------------------ workload
 
-def make_workload(cfg, steps: int, warmup: int, dev):
+def make_workload(cfg, steps: int, warmup: int, dev, step_flags: int = 0, budgets=None):
+    """Caches and step inputs.  One pass per budget; each pass decodes all the
+    config's layers (each layer its own cache).  Host-resident configs build each
+    layer's cache in device memory and move it to pinned host memory."""
+    import ctypes
     import torch
     import bit_plane_kv_encode_gb300 as pk
     from workload import gen_layer
 
-    inp = gen_layer(cfg, 0, device=dev)
-    N, H, n, D = inp.k.shape
-    G = cfg.group
+    L, N, H, G, D, n = cfg.n_layers, cfg.n_seq, cfg.n_kv_heads, cfg.group, cfg.head_dim, cfg.n_tokens
     cap = ((n + warmup + steps + 64 + 511) // 512) * 512
-    budgets = list(cfg.budgets)
+    budgets = list(budgets or cfg.budgets)
+    host = cfg.residency == "host"
+    caches = {b: [] for b in budgets}
+    q, s2, kn, vn = [], [], [], []
+    inp0 = None
+    for l in range(L):
+        inp = gen_layer(cfg, l, device=dev)
+        for b in budgets:
+            c = pk.Cache(N, H, G, cap, device=dev)
+            c.append(inp.k[:, :, : n - 1].contiguous(), inp.v[:, :, : n - 1].contiguous())
+            if host:
+                hc = pk.Cache(N, H, G, cap, device=dev, residency="host")
+                hc.copy_from(c)
+                torch.cuda.synchronize()
+                del c
+                c = hc
+            caches[b].append(c)
+        q.append(inp.q)
+        s2.append(inp.sigma2)
+        kn.append(inp.k[:, :, n - 1].contiguous())
+        vn.append(inp.v[:, :, n - 1].contiguous())
+        if l == 0:
+            inp0 = inp
+            inp0.k, inp0.v = inp.k[:1, :8].cpu(), inp.v[:1, :8].cpu()  # kept for the CPU oracle sample
+        del inp
+        torch.cuda.empty_cache()
+    torch.cuda.synchronize()
+    ws = caches[budgets[0]][0].workspace(cfg.k, pk.WS_STEP)
+    io = dict(q=torch.stack(q).to(dev).contiguous(), sigma2=torch.stack(s2).to(dev).contiguous(),
+              k_new=torch.stack(kn).to(dev).contiguous(), v_new=torch.stack(vn).to(dev).contiguous())
     passes = []
     for b in budgets:
-        c = pk.Cache(N, H, G, cap, device=dev)
-        c.append(inp.k[:, :, : n - 1].contiguous(), inp.v[:, :, : n - 1].contiguous())
-        passes.append(dict(budget=b, cache=c, cap=cap))
-    torch.cuda.synchronize()
-    ws = passes[0]["cache"].workspace(cfg.k, pk.WS_STEP)
-    io = dict(
-        q=inp.q.to(dev)[None].contiguous(),
-        sigma2=inp.sigma2.to(dev)[None].contiguous(),
-        k_new=inp.k[:, :, n - 1][None].contiguous(),
-        v_new=inp.v[:, :, n - 1][None].contiguous(),
-    )
-    for p in passes:
-        b = p["budget"]
+        p = dict(budget=b, caches=caches[b], cap=cap, L=L)
         p["budget_q"] = torch.full((N,), 4 * b, dtype=torch.int32, device=dev)
-        p["out"] = torch.zeros((1, N, H, G, D), dtype=torch.float32, device=dev)
-        p["depths"] = torch.zeros((1, N, H, D), dtype=torch.uint8, device=dev)
-        p["idx"] = torch.zeros((1, N, H, G, cfg.k), dtype=torch.int32, device=dev)
-        p["events"] = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
-        for e in p["events"]:
-            e.record()  # create the event handles
-        p["ev_arr"] = (__import__("ctypes").c_void_p * 7)(*[e.cuda_event for e in p["events"]])
-        p["arr"] = pk.cache_array([p["cache"]])
-        p["args"] = pk.bpkv_step_args(
-            io["k_new"].data_ptr(), io["v_new"].data_ptr(), io["q"].data_ptr(), io["sigma2"].data_ptr(),
-            p["budget_q"].data_ptr(), pk.DEPTH_WATERFILL, 0, 0, cfg.k, cfg.n_sink, cfg.n_recent,
-            p["out"].data_ptr(), p["depths"].data_ptr(), p["idx"].data_ptr(),
-            __import__("ctypes").cast(p["ev_arr"], __import__("ctypes").c_void_p))
+        p["out"] = torch.zeros((L, N, H, G, D), dtype=torch.float32, device=dev)
+        p["depths"] = torch.zeros((L, N, H, D), dtype=torch.uint8, device=dev)
+        p["idx"] = torch.zeros((L, N, H, G, cfg.k), dtype=torch.int32, device=dev)
+        p["events"] = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(L)]
+        for row in p["events"]:
+            for e in row:
+                e.record()  # create the event handles
+        p["ev_arr"] = (ctypes.c_void_p * (7 * L))(*[e.cuda_event for row in p["events"] for e in row])
+        p["arr"] = pk.cache_array(caches[b])
+        common = (io["k_new"].data_ptr(), io["v_new"].data_ptr(), io["q"].data_ptr(), io["sigma2"].data_ptr(),
+                  p["budget_q"].data_ptr(), pk.DEPTH_WATERFILL, 0, 0, cfg.k, cfg.n_sink, cfg.n_recent,
+                  p["out"].data_ptr(), p["depths"].data_ptr(), p["idx"].data_ptr())
+        # timed graph: no event nodes (each costs about 2 us inside a graph)
+        p["args"] = pk.bpkv_step_args(*common, None, step_flags)
+        # breakdown graph: events at every stage boundary
+        p["args_ev"] = pk.bpkv_step_args(*common, ctypes.cast(p["ev_arr"], ctypes.c_void_p), step_flags)
+        p["fused"] = bool(step_flags & pk.STEP_FUSED) and pk.bpkv_step_fused(caches[b][0].c, cfg.k, cfg.n_sink,
+                                                                             cfg.n_recent, pk.DEPTH_WATERFILL)
+        passes.append(p)
     torch.cuda.synchronize()
-    return inp, passes, ws, io
+    return inp0, passes, ws, io
 
 
-def run_step(passes, ws):
+def run_step(passes, ws, events=False):
     import bit_plane_kv_encode_gb300 as pk
     for p in passes:
         # n_max is the launch-sizing bound: the capacity, so that graph replays stay
         # valid while the sequences grow by one token per replay
-        p["arr"][0].n_max = p["cap"] - 1
-        pk.bpkv_decode_step(p["arr"], 1, p["args"], ws, ws.numel())
+        for layer in p["arr"]:
+            layer.n_max = p["cap"] - 1
+        pk.bpkv_decode_step(p["arr"], p["L"], p["args_ev"] if events else p["args"], ws, ws.numel())
 
 
 def stage_times_ms(passes):
     out = {s: 0.0 for s in STAGES}
     for p in passes:
-        ev = p["events"]
-        for i, s in enumerate(STAGES):
-            out[s] += ev[i].elapsed_time(ev[i + 1])
+        for ev in p["events"]:
+            for i, s in enumerate(STAGES):
+                out[s] += ev[i].elapsed_time(ev[i + 1])
     return out
+
+
+def link_h2d_gbs(dev) -> float:
+    """Pinned host -> device copy bandwidth (1 GiB, best of 10)."""
+    import torch
+    src = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    best = 0.0
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dst.copy_(src, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        best = max(best, (1 << 30) / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    return best
 
 
 def bench_ours(args, cfg, rank, world, local):
@@ -195,23 +241,28 @@ def bench_ours(args, cfg, rank, world, local):
     dev = torch.device("cuda", local)
     import __graft_entry__
     __graft_entry__.build()
-    inp, passes, ws, io = make_workload(cfg, args.steps, args.warmup, dev)
-    N, H, n, D = inp.k.shape
-    G = cfg.group
+    budgets = [args.budget] if args.budget else None
+    inp, passes, ws, io = make_workload(cfg, args.steps, args.warmup, dev, 1 if args.fused else 0, budgets)
+    N, H, n, D = cfg.n_seq, cfg.n_kv_heads, cfg.n_tokens, cfg.head_dim
+    G, L = cfg.group, cfg.n_layers
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
-    graph = None
+    graph = graph_ev = None
     stream = torch.cuda.Stream(device=dev)
     if not args.no_graph:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             run_step(passes, ws)
+        graph_ev = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_ev, stream=stream):
+            run_step(passes, ws, events=True)
 
-    def step():
-        if graph is not None:
-            graph.replay()
+    def step(events=False):
+        g = graph_ev if events else graph
+        if g is not None:
+            g.replay()
         else:
-            run_step(passes, ws)
+            run_step(passes, ws, events)
 
     pk.bpkv_clear_status(ws)
     for _ in range(args.warmup):
@@ -235,41 +286,64 @@ def bench_ours(args, cfg, rank, world, local):
         e1.record()
         e1.synchronize()
         step_ms.append(e0.elapsed_time(e1))
-        for s, v in stage_times_ms(passes).items():
-            stage_ms[s].append(v)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - t_wall
     clk = clocks.stop()
     assert pk.bpkv_read_status(ws) == 0
+    # stage breakdown (separate replays of the graph with event nodes)
+    ev_ms = []
+    for _ in range(min(args.steps, 20)):
+        flush.zero_()
+        e0.record()
+        step(events=True)
+        e1.record()
+        e1.synchronize()
+        ev_ms.append(e0.elapsed_time(e1))
+        for s, v in stage_times_ms(passes).items():
+            stage_ms[s].append(v)
 
     total_ms = all_max(sum(step_ms), world)
     ms_per_step = total_ms / args.steps
-    keys_per_step = len(passes) * N * H * n
+    keys_per_step = len(passes) * L * N * H * n
     value = world * keys_per_step / (ms_per_step / 1e3)
 
     # algorithmic bytes per pass (Fathom page, section 3.1 Eq. 1 terms)
     scan_bytes, rows_bytes, score_bytes = 0.0, 0.0, 0.0
     union_rows = 0
     for p in passes:
-        dd = p["depths"][0].cpu().numpy()
-        idx = p["idx"][0].cpu().numpy()
-        for s in range(N):
-            for h in range(H):
-                scan_bytes += depth_bits(dd[s, h]) * n / 8
-                u = len({int(i) for i in idx[s, h].ravel() if i >= 0})
-                union_rows += u
-                rows_bytes += u * row_bytes(D)
-        score_bytes += N * H * G * n * 4
+        dd = p["depths"].cpu().numpy()
+        idx = p["idx"].cpu().numpy()
+        for l in range(L):
+            for s in range(N):
+                for h in range(H):
+                    scan_bytes += depth_bits(dd[l, s, h]) * n / 8
+                    u = len(np.unique(idx[l, s, h][idx[l, s, h] >= 0]))
+                    union_rows += u
+                    rows_bytes += u * row_bytes(D)
+        score_bytes += L * N * H * G * n * 4
+    n_launch = len(passes) * L
     stage_mean = {s: statistics.mean(v) for s, v in stage_ms.items()}
-    stage_bytes = {"scan": scan_bytes, "topk": score_bytes, "attend": rows_bytes}
-    dom = max(stage_bytes, key=lambda s: stage_mean[s])
+    if all(p["fused"] for p in passes):
+        # one fused kernel per pass: it reads the plane prefixes and the union rows
+        dom, kbytes, kms = "k_decode_fused", scan_bytes + rows_bytes, stage_mean["encode"]
+    else:
+        stage_bytes = {"scan": scan_bytes, "topk": score_bytes, "attend": rows_bytes}
+        dom = max(stage_bytes, key=lambda s: stage_mean[s])
+        kbytes, kms = stage_bytes[dom], stage_mean[dom]
     hbm, peak_src = peaks()
-    achieved = stage_bytes[dom] / (stage_mean[dom] / 1e3) / 1e9
+    bound = "hbm"
+    link = None
+    if cfg.residency == "host":
+        # the scan and the row reads cross the host link: its measured copy rate is the peak
+        link = link_h2d_gbs(dev)
+        hbm, peak_src, bound = link, "of measured (pinned host-to-device copy, 1 GiB)", "host_link"
+    achieved = kbytes / (kms / 1e3) / 1e9
     traffic = load_traffic(dom)
-    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "peak_source": peak_src,
-                "traffic": traffic, "algorithmic_bytes_per_launch": round(stage_bytes[dom] / len(passes))}
+    roofline = {"bound": bound, "kernel": dom, "achieved": round(achieved, 1), "peak": round(hbm, 1),
+                "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_source": peak_src,
+                "traffic": traffic, "algorithmic_bytes_per_launch": round(kbytes / n_launch),
+                "launch_us": round(kms * 1e3 / n_launch, 2)}
 
     # end to end through host buffers: inputs copied in, outputs copied out, inside the timed region
     e2e = bench_e2e(args, passes, io, ws, flush, dev, keys_per_step, world)
@@ -280,23 +354,30 @@ def bench_ours(args, cfg, rank, world, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; K ~ N(0, sigma_j^2), sigma_j = exp(0.75 z), 8 planted needles/head)",
         "config": {"workload": cfg.name, "n_seq": N, "n_kv_heads": H, "group": G, "head_dim": D,
-                   "n_tokens": n, "budgets_bits": list(cfg.budgets), "k": cfg.k, "n_sink": cfg.n_sink,
+                   "n_layers": L, "n_tokens": n, "budgets_bits": [p["budget"] for p in passes], "k": cfg.k,
+                   "n_sink": cfg.n_sink,
                    "n_recent": cfg.n_recent, "residency": cfg.residency,
                    "l2": "flushed before every timed step (256 MiB write, outside the events)",
                    "cuda_graph": graph is not None, "parallelism": f"replicas x{world}"},
-        "decode_step_us_per_layer": round(ms_per_step * 1e3 / len(passes), 2),
+        "decode_step_us_per_layer": round(ms_per_step * 1e3 / n_launch, 2),
         "achieved_gbs_step": round((scan_bytes + rows_bytes) / (ms_per_step / 1e3) / 1e9, 1),
+        "fused_kernel": all(p["fused"] for p in passes),
         "stages_us_per_step": {s: round(v * 1e3, 2) for s, v in stage_mean.items()},
+        "stages_note": ("from separate replays with event nodes at every stage boundary "
+                        f"({statistics.mean(ev_ms) * 1e3:.1f} us/step with them); on the fused path "
+                        "'encode' holds the whole fused kernel and 'attend' the length update"),
         "bytes_per_step": {"scan": round(scan_bytes), "rows": round(rows_bytes), "scores_overhead": round(score_bytes),
                            "union_rows": union_rows},
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": args.steps * len(passes) * sum(LAUNCHES_PER_PASS.values()),
+        "gpu_launches": args.steps * L * sum(2 if p["fused"] else sum(LAUNCHES_PER_PASS.values()) for p in passes),
         "clocks": clk,
         "wall_s_timed": round(wall, 3),
     }
+    if link is not None:
+        line["link_h2d_gbs"] = round(link, 1)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg, inp, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(cfg, inp, args.cpu_seconds, [p["budget"] for p in passes])
     return line
 
 
@@ -374,9 +455,10 @@ def _oracle_units(cfg, inp):
     return o, units
 
 
-def _oracle_step(o, cfg, inp, units, pool):
-    """One decode step of the workload on the CPU oracle: per (budget, unit)
-    re-encode of the tail block, depths, scores, top-k, union, attention."""
+def _oracle_step(o, cfg, inp, units, pool, budgets):
+    """One decode pass per budget over the sampled units on the CPU oracle: per
+    (budget, unit) re-encode of the tail block, depths, scores, top-k, union,
+    attention."""
     import numpy as np
     n = inp.k.shape[2]
 
@@ -392,12 +474,12 @@ def _oracle_step(o, cfg, inp, units, pool):
         o.attend(q, kb, vb, idx)
         return sc_t.shape[0] + pl_t.shape[0]
 
-    jobs = [(b, u) for b in cfg.budgets for u in units]
+    jobs = [(b, u) for b in budgets for u in units]
     list(pool.map(one, jobs))
     return len(jobs)
 
 
-def cpu_baseline(cfg, inp, seconds: float) -> dict:
+def cpu_baseline(cfg, inp, seconds: float, budgets) -> dict:
     import concurrent.futures as cf
     cores = os.cpu_count() or 1
     o, units = _oracle_units(cfg, inp)
@@ -405,14 +487,13 @@ def cpu_baseline(cfg, inp, seconds: float) -> dict:
     done, t0 = 0, time.perf_counter()
     with cf.ThreadPoolExecutor(max_workers=cores) as pool:
         while True:
-            done += _oracle_step(o, cfg, inp, units, pool)
+            done += _oracle_step(o, cfg, inp, units, pool, budgets)
             el = time.perf_counter() - t0
             if el >= seconds:
                 break
     return {"value": round(done * n / el), "unit": "keys/s", "cores": cores, "kind": "oracle",
-            "sample": f"{done // len(units) // len(cfg.budgets)} full steps of {cfg.name} "
-                      f"({len(cfg.budgets)} budgets x {len(units)} (seq, KV head) units, n={n}), "
-                      f"{el:.1f} s, threads over units"}
+            "sample": f"{done // len(units) // len(budgets)} rounds of {len(budgets)} budgets x {len(units)} "
+                      f"(seq, KV head) units of layer 0 of {cfg.name} (n={n}), {el:.1f} s, threads over units"}
 
 
 def bench_reference(args, cfg, rank, world):
@@ -422,26 +503,29 @@ def bench_reference(args, cfg, rank, world):
     if rank != 0:
         return None
     inp = gen_layer(cfg, 0, device="cpu")
+    inp.k, inp.v = inp.k[:1, :8], inp.v[:1, :8]
+    budgets = [args.budget] if args.budget else list(cfg.budgets)
     o, units = _oracle_units(cfg, inp)
     n = inp.k.shape[2]
     cores = os.cpu_count() or 1
     times = []
     with cf.ThreadPoolExecutor(max_workers=cores) as pool:
         for _ in range(args.warmup):
-            _oracle_step(o, cfg, inp, units, pool)
+            _oracle_step(o, cfg, inp, units, pool, budgets)
         for _ in range(args.steps):
             t0 = time.perf_counter()
-            _oracle_step(o, cfg, inp, units, pool)
+            _oracle_step(o, cfg, inp, units, pool, budgets)
             times.append(time.perf_counter() - t0)
     ms = 1e3 * statistics.mean(times)
-    keys = len(cfg.budgets) * len(units) * n
+    keys = len(budgets) * len(units) * n
     val = round(keys / (ms / 1e3))
     return {"impl": "reference", "metric": "keys scored/s", "value": val, "unit": "keys/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg.name, "n_tokens": n, "budgets_bits": list(cfg.budgets), "k": cfg.k},
+            "config": {"workload": cfg.name, "n_tokens": n, "budgets_bits": budgets, "k": cfg.k},
             "cpu_baseline": {"value": val, "unit": "keys/s", "cores": cores, "kind": "oracle",
-                             "sample": f"every step is one full {cfg.name} step on the host cores"},
+                             "sample": f"every step: {len(budgets)} budgets x {len(units)} (seq, KV head) units "
+                                       f"of layer 0 of {cfg.name} on the host cores"},
             "e2e": {"value": val, "unit": "keys/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

@@ -13,12 +13,13 @@ import ctypes
 from ._binding import (  # noqa: F401
     BpkvError, bpkv_alloc_depths, bpkv_cache, bpkv_clear_status, bpkv_decode_step, bpkv_dense_attend,
     bpkv_encode_append, bpkv_fixed_depths, bpkv_read_status, bpkv_scan, bpkv_scan_topk, bpkv_scan_topk_noalloc, bpkv_sparse_attend,
-    bpkv_status_string, bpkv_step_args, bpkv_topk, bpkv_union, bpkv_version, bpkv_workspace_size, header_symbols, load)
+    bpkv_status_string, bpkv_step_args, bpkv_step_fused, bpkv_topk, bpkv_union, bpkv_version, bpkv_workspace_size, header_symbols, load)
 
 HEAD_DIM = 128
 WS_SCAN_TOPK, WS_ATTEND, WS_DENSE, WS_STEP = 1, 2, 4, 8
 DEPTH_WATERFILL, DEPTH_FIXED, DEPTH_DENSE = 0, 1, 2
 DEV_OVERFLOW, DEV_SELECT = 1, 2
+STEP_FUSED = 1
 
 
 class Cache:
@@ -58,6 +59,13 @@ class Cache:
     def append(self, k_new, v_new, stream=None):
         """Append k_new/v_new [N][H][t][D] bf16 (device) to every sequence."""
         bpkv_encode_append(self.c, k_new, v_new, k_new.shape[2], stream)
+
+    def copy_from(self, other: "Cache"):
+        """Take over another cache's contents (same shapes), e.g. a host-resident
+        copy of a cache built in device memory; copies run on the current stream."""
+        for name in ("planes", "scales", "k_rows", "v_rows", "seq_len"):
+            getattr(self, name).copy_(getattr(other, name), non_blocking=True)
+        self.c.n_max = other.c.n_max
 
     def workspace(self, k: int, what: int):
         import torch

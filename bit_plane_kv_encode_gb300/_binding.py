@@ -39,7 +39,7 @@ class bpkv_step_args(ctypes.Structure):
         ("k_new", P), ("v_new", P), ("q", P), ("sigma2", P), ("budget_q", P),
         ("depth_rule", i32), ("fixed_channels", i32), ("fixed_depth", i32),
         ("k", i32), ("n_sink", i32), ("n_recent", i32),
-        ("out", P), ("depths_out", P), ("idx_out", P), ("stage_events", P),
+        ("out", P), ("depths_out", P), ("idx_out", P), ("stage_events", P), ("flags", i32),
     ]
 
 
@@ -60,6 +60,7 @@ _SIGS = {
     "bpkv_sparse_attend": ([P, P, P, P, P, i32, P, P, sz, P], ctypes.c_int),
     "bpkv_dense_attend": ([P, P, P, P, sz, P], ctypes.c_int),
     "bpkv_decode_step": ([P, i32, P, P, sz, P], ctypes.c_int),
+    "bpkv_step_fused": ([P, i32, i32, i32, i32], ctypes.c_int),
 }
 
 _lib = None
@@ -200,6 +201,10 @@ def bpkv_dense_attend(cache, q, out, ws, ws_bytes: int, stream=None):
     return _check("bpkv_dense_attend",
                   load().bpkv_dense_attend(ctypes.byref(cache), _ptr(q), _ptr(out), _ptr(ws), int(ws_bytes),
                                            _stream(stream)))
+
+
+def bpkv_step_fused(cache, k: int, n_sink: int, n_recent: int, depth_rule: int) -> bool:
+    return bool(load().bpkv_step_fused(ctypes.byref(cache), int(k), int(n_sink), int(n_recent), int(depth_rule)))
 
 
 def bpkv_decode_step(layers_array, n_layers: int, args, ws, ws_bytes: int, stream=None):

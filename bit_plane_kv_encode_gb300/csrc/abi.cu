@@ -21,6 +21,13 @@ cudaError_t launch_attend(const bpkv_cache& c, const float* q, const int32_t* ui
                           const int32_t* ucount, int32_t u_cap, float* part, float* out, bool dense,
                           cudaStream_t st);
 size_t attend_part_bytes(const bpkv_cache& c, int64_t rows, bool dense);
+cudaError_t launch_bump_len(const bpkv_cache& c, int32_t t_new, cudaStream_t st);
+bool fused_eligible(const bpkv_cache& c, int32_t k, int32_t n_sink, int32_t n_recent, int32_t depth_rule);
+cudaError_t launch_decode_fused(const bpkv_cache& c, const uint16_t* k_new, const uint16_t* v_new, const float* q,
+                                const float* sigma2, const int32_t* budget_q, int32_t depth_rule,
+                                int32_t fixed_channels, int32_t fixed_depth, int32_t k, int32_t n_sink,
+                                int32_t n_recent, float* out, uint8_t* depths_out, int32_t* idx_out,
+                                cudaStream_t st);
 }  // namespace bpkv
 
 using namespace bpkv;
@@ -233,6 +240,11 @@ int bpkv_dense_attend(const bpkv_cache* c, const float* q, float* out, void* ws,
                                    out, true, as_stream(stream)));
 }
 
+int bpkv_step_fused(const bpkv_cache* c, int32_t k, int32_t n_sink, int32_t n_recent, int32_t depth_rule) {
+  if (check_cache(c) != BPKV_OK || check_k(k, n_sink, n_recent) != BPKV_OK) return 0;
+  return fused_eligible(*c, k, n_sink, n_recent, depth_rule) ? 1 : 0;
+}
+
 int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args* a, void* ws, size_t ws_bytes,
                      void* stream) {
   if (!layers || n_layers < 1 || !a) return BPKV_EINVAL;
@@ -277,6 +289,19 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
     const float* q = a->q + (size_t)l * NH * G * kD;
     float* out = a->out + (size_t)l * NH * G * kD;
     BPKV_TRY(mark(l, 0));
+    if (!dense && (a->flags & BPKV_STEP_FUSED) && fused_eligible(c, a->k, a->n_sink, a->n_recent, a->depth_rule)) {
+      uint8_t* dout = a->depths_out ? a->depths_out + (size_t)l * NH * kD : nullptr;
+      int32_t* iout = a->idx_out ? a->idx_out + (size_t)l * NH * G * a->k : nullptr;
+      const float* s2 = a->sigma2 ? a->sigma2 + (size_t)l * NH * kD : nullptr;
+      BPKV_TRY(cuda_status(launch_decode_fused(c, kn, vn, q, s2, a->budget_q, a->depth_rule, a->fixed_channels,
+                                               a->fixed_depth, a->k, a->n_sink, a->n_recent, out, dout, iout,
+                                               st)));
+      for (int e = 1; e <= 5; ++e) BPKV_TRY(mark(l, e));
+      BPKV_TRY(cuda_status(launch_bump_len(c, 1, st)));
+      BPKV_TRY(mark(l, 6));
+      c.n_max += 1;
+      continue;
+    }
     BPKV_TRY(cuda_status(launch_encode_append(c, kn, vn, 1, st)));
     c.n_max += 1;
     if (dense) {

@@ -1,0 +1,79 @@
+// Device building block of the bit-plane encoder (Fathom page, section 3.2),
+// shared by the append kernel and the fused decode kernel.  See encode.cu.
+#pragma once
+
+#include "common.cuh"
+
+namespace bpkv {
+
+// Append the tokens of one 64-token block of one unit and re-encode the block.
+// Rows t0 .. t0 + cnt - 1 are the block's tokens; those below n_old come from
+// the stored rows, the others from knew/vnew (row r of the new tokens is
+// token n_old + r), which are also copied into the row store.  Threads:
+// PARTS per channel (blockDim.x == PARTS * 128), 64 / PARTS tokens each.
+template <int PARTS>
+__device__ void encode_block_cta(uint16_t (*kb)[kD], uint16_t* krow, uint16_t* vrow, const uint16_t* knew,
+                                 const uint16_t* vnew, int64_t n_old, int64_t t0, int cnt, uint64_t* pw_base,
+                                 uint16_t* scale_base, int64_t nb_cap, int64_t blk) {
+  constexpr int TOK = kBlock / PARTS;
+  for (int v = threadIdx.x; v < cnt * 16; v += blockDim.x) {
+    const int r = v >> 4, c8 = (v & 15) * 8;
+    const int64_t tok = t0 + r;
+    uint4 val;
+    if (tok < n_old) {
+      val = *reinterpret_cast<const uint4*>(krow + tok * kD + c8);
+    } else {
+      const int64_t src = (tok - n_old) * kD + c8;
+      val = *reinterpret_cast<const uint4*>(knew + src);
+      *reinterpret_cast<uint4*>(krow + tok * kD + c8) = val;
+      *reinterpret_cast<uint4*>(vrow + tok * kD + c8) = *reinterpret_cast<const uint4*>(vnew + src);
+    }
+    *reinterpret_cast<uint4*>(&kb[r][c8]) = val;
+  }
+  __syncthreads();
+  // thread = (channel j, part qd): tokens TOK qd .. TOK qd + TOK - 1; the parts
+  // of a channel are adjacent lanes.
+  const int j = threadIdx.x / PARTS, qd = threadIdx.x % PARTS;
+  const int r0 = TOK * qd, r1 = min(r0 + TOK, cnt);
+  float amax = 0.f;
+  for (int r = r0; r < r1; ++r) amax = fmaxf(amax, fabsf(bf16_bits_to_float(kb[r][j])));
+#pragma unroll
+  for (int o = 1; o < PARTS; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  // a/8 is exact in float32; values past the largest half saturate to it.
+  const __half hs = __float2half_rn(fminf(amax * 0.125f, 65504.f));
+  const uint16_t s16 = __half_as_ushort(hs);
+  const float sc = __half2float(hs);
+  uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;  // this part's TOK bits of each plane
+  for (int r = r0; r < r1; ++r) {
+    int c = 8;
+    if (s16 != 0) {
+      float f = floorf(__fdiv_rn(bf16_bits_to_float(kb[r][j]), sc));
+      f = fminf(fmaxf(f, -8.f), 7.f);
+      c = static_cast<int>(f) + 8;
+    }
+    const uint32_t bit = 1u << (r - r0);
+    if (c & 8) w0 |= bit;
+    if (c & 4) w1 |= bit;
+    if (c & 2) w2 |= bit;
+    if (c & 1) w3 |= bit;
+  }
+  // each part owns TOK / 8 bytes of the little-endian 64-bit word
+  uint64_t* pw = pw_base + (int64_t)j * kPlanes * nb_cap + blk;
+  if constexpr (PARTS == 4) {
+    uint16_t* p = reinterpret_cast<uint16_t*>(pw) + qd;
+    p[0] = (uint16_t)w0;
+    p[4 * nb_cap] = (uint16_t)w1;
+    p[8 * nb_cap] = (uint16_t)w2;
+    p[12 * nb_cap] = (uint16_t)w3;
+  } else {
+    static_assert(PARTS == 2, "2 or 4 parts per channel");
+    uint32_t* p = reinterpret_cast<uint32_t*>(pw) + qd;
+    p[0] = w0;
+    p[2 * nb_cap] = w1;
+    p[4 * nb_cap] = w2;
+    p[6 * nb_cap] = w3;
+  }
+  if (qd == 0) scale_base[(int64_t)j * nb_cap + blk] = s16;
+}
+
+}  // namespace bpkv

@@ -1,0 +1,275 @@
+// Device building blocks of the prefix-plane scan, shared by the stand-alone
+// scan kernel and the fused decode kernel.  See scan.cu for the method.
+#pragma once
+
+#include "common.cuh"
+
+namespace bpkv {
+
+constexpr int kScanBlocks = 8;                  // 64-token blocks per CTA
+constexpr int kScanThreads = 32 * kScanBlocks;  // one warp per block
+constexpr int kMaxGroups = 20;                  // 16 depth-4 groups + one partial group per other depth
+constexpr int kWordPitch = 2 * kScanBlocks + 1; // u32 words per staged row (odd: conflict-free)
+constexpr int kMaxSlots = 288;                  // padded channel slots over all groups
+
+template <int T>
+struct Depth {
+  static constexpr int cap = 32 / T;                  // channels per group
+  static constexpr int pitch = (cap + 3) / 4 * 4;     // slots per group, multiple of 4
+};
+
+__host__ __device__ constexpr int slot_pitch(int t) {
+  return t == 4 ? 8 : t == 3 ? 12 : t == 2 ? 16 : 32;
+}
+__host__ __device__ constexpr int group_cap(int t) { return 32 / t; }
+
+// Bit position of field m of a depth-t group inside the shifted word it is read
+// from (x << 1 when the field ends at or below bit 21, x >> 9 otherwise), so
+// that the field sits in [1, 23) under the exponent of 2^23.
+__host__ __device__ constexpr int field_pos(int t, int m) {
+  return (m * t + t <= 22) ? m * t + 1 : m * t - 9;
+}
+
+template <int GP>
+struct ScanSmem {
+  uint32_t words[kMaxGroups * 32 * kWordPitch];     // staged plane half-words
+  float u[kScanBlocks * kMaxSlots * GP];            // [block][group slots][head][slot]
+  float w[kMaxSlots * GP];                          // q 2^(4 - t - pos), [group slots][head][slot]
+  float sc[kMaxSlots * kScanBlocks];                // block scales, [slot][block]
+  int16_t row_of_lane[kMaxGroups * 32];             // j * 4 + p, or -1
+  int16_t slot_ch[kMaxSlots];                       // channel of each slot, or -1
+  int8_t grp_t[kMaxGroups];
+  int16_t grp_base[kMaxGroups];                     // first slot of each group
+  int8_t grp_cnt[kMaxGroups];                       // channels in each group
+  int cnt_t[5];
+  int warp_cnt[4][5];
+  int n_groups, n_slots;
+};
+
+// 32 x 32 bit transpose across the warp: on return bit r of lane l's word is
+// bit l of lane r's input word.
+__device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, const uint32_t (&keep)[5],
+                                                     const uint32_t (&rot)[5]) {
+#pragma unroll
+  for (int s = 0; s < 5; ++s) {
+    const int j = 16 >> s;
+    const uint32_t p = __shfl_xor_sync(0xffffffffu, x, j);
+    const uint32_t r = __funnelshift_l(p, p, rot[s]);
+    x = (x & keep[s]) | (r & ~keep[s]);
+  }
+  return x;
+}
+
+__device__ __forceinline__ unsigned long long pack2(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+__device__ __forceinline__ void unpack2(unsigned long long v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b,
+                                                    unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// e (scaled by 2^pos) of field m of a depth-T group, from the shifted words.
+template <int T, int M>
+__device__ __forceinline__ float field_value(uint32_t xa, uint32_t xb) {
+  constexpr int pos = field_pos(T, M);
+  constexpr uint32_t mask = ((1u << T) - 1u) << pos;
+  constexpr bool use_a = (M * T + T <= 22);
+  const uint32_t src = use_a ? xa : xb;
+  const float f = __uint_as_float((src & mask) | 0x4B000000u);     // 2^23 + c 2^pos
+  constexpr float K = 8388608.f + ((float)(1 << (T - 1)) - 0.5f) * (float)(1u << pos);
+  return f - K;                                                    // (c - 2^(T-1) + 1/2) 2^pos, exact
+}
+
+// Accumulate the fields M and M+1 of one group into the head accumulators of
+// the two tokens of this lane.  acc*[h] hold (even-field, odd-field) partial sums.
+template <int T, int M, int GP>
+__device__ __forceinline__ void field_pair(uint32_t xa0, uint32_t xb0, uint32_t xa1, uint32_t xb1,
+                                           const float* __restrict__ ug, unsigned long long (&acc0)[GP],
+                                           unsigned long long (&acc1)[GP]) {
+  constexpr int P = Depth<T>::pitch;
+  const float e0a = field_value<T, M>(xa0, xb0);
+  const float e1a = field_value<T, M>(xa1, xb1);
+  float e0b = 0.f, e1b = 0.f;
+  if constexpr (M + 1 < Depth<T>::cap) {
+    e0b = field_value<T, M + 1>(xa0, xb0);
+    e1b = field_value<T, M + 1>(xa1, xb1);
+  }
+  const unsigned long long E0 = pack2(e0a, e0b), E1 = pack2(e1a, e1b);
+#pragma unroll
+  for (int h = 0; h < GP; ++h) {
+    const float2 uu = *reinterpret_cast<const float2*>(ug + h * P + M);
+    const unsigned long long U = pack2(uu.x, uu.y);
+    acc0[h] = ffma2(U, E0, acc0[h]);
+    acc1[h] = ffma2(U, E1, acc1[h]);
+  }
+}
+
+template <int T, int GP, int M = 0>
+__device__ __forceinline__ void group_fields(int cnt, uint32_t xa0, uint32_t xb0, uint32_t xa1, uint32_t xb1,
+                                             const float* __restrict__ ug, unsigned long long (&acc0)[GP],
+                                             unsigned long long (&acc1)[GP]) {
+  if constexpr (M < Depth<T>::cap) {
+    if (M < cnt) {
+      field_pair<T, M, GP>(xa0, xb0, xa1, xb1, ug, acc0, acc1);
+      group_fields<T, GP, M + 2>(cnt, xa0, xb0, xa1, xb1, ug, acc0, acc1);
+    }
+  }
+}
+
+// Transpose constants of this lane (see warp_transpose32).
+__device__ __forceinline__ void transpose_consts(int lane, uint32_t (&keep)[5], uint32_t (&rot)[5]) {
+#pragma unroll
+  for (int st = 0; st < 5; ++st) {
+    const int j = 16 >> st;
+    const uint32_t M = st == 0 ? 0x0000FFFFu : st == 1 ? 0x00FF00FFu : st == 2 ? 0x0F0F0F0Fu
+                     : st == 3 ? 0x33333333u : 0x55555555u;
+    const bool hi = (lane & j) != 0;
+    keep[st] = hi ? ~M : M;
+    rot[st] = hi ? (uint32_t)(32 - j) : (uint32_t)j;
+  }
+}
+
+// Channel groups and per-query weights.  Threads 0..127 pass their channel's
+// depth t and q values; blockDim.x must be kScanThreads.
+template <int GP>
+__device__ void scan_setup(ScanSmem<GP>& S, int t, const float (&qv)[GP]) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int rank = 0;
+  if (tid < kD) {
+#pragma unroll
+    for (int d = 1; d <= 4; ++d) {
+      const uint32_t b = __ballot_sync(0xffffffffu, t == d);
+      if (t == d) rank = __popc(b & ((1u << lane) - 1u));
+      if (lane == 0) S.warp_cnt[warp][d] = __popc(b);
+    }
+  }
+  for (int e = tid; e < kMaxGroups * 32; e += kScanThreads) S.row_of_lane[e] = -1;
+  for (int e = tid; e < kMaxSlots; e += kScanThreads) S.slot_ch[e] = -1;
+  __syncthreads();
+  if (tid == 0) {
+    int g = 0, slot = 0;
+    for (int d = 4; d >= 1; --d) {
+      int c = 0;
+      for (int w = 0; w < 4; ++w) c += S.warp_cnt[w][d];
+      S.cnt_t[d] = c;
+      for (int first = 0; first < c; first += group_cap(d), ++g) {
+        S.grp_t[g] = (int8_t)d;
+        S.grp_base[g] = (int16_t)slot;
+        S.grp_cnt[g] = (int8_t)min(group_cap(d), c - first);
+        slot += slot_pitch(d);
+      }
+    }
+    S.n_groups = g;
+    S.n_slots = slot;
+  }
+  __syncthreads();
+  if (tid < kD && t > 0) {
+    for (int w = 0; w < warp; ++w) rank += S.warp_cnt[w][t];
+    // group index: groups of deeper channels come first
+    int g = 0;
+    for (int d = 4; d > t; --d) g += (S.cnt_t[d] + group_cap(d) - 1) / group_cap(d);
+    g += rank / group_cap(t);
+    const int m = rank % group_cap(t);
+    S.slot_ch[S.grp_base[g] + m] = (int16_t)tid;
+    for (int p = 0; p < t; ++p) S.row_of_lane[g * 32 + m * t + (t - 1 - p)] = (int16_t)(tid * 4 + p);
+    // w = q 2^(4 - t - pos) per head, laid out [group][head][slot]
+    const int P = slot_pitch(t);
+    const int base = S.grp_base[g];
+#pragma unroll
+    for (int hh = 0; hh < GP; ++hh) S.w[base * GP + hh * P + m] = ldexpf(qv[hh], 4 - t - field_pos(t, m));
+  }
+  __syncthreads();
+  // unused slots of partial groups weigh 0
+  for (int g = 0; g < S.n_groups; ++g) {
+    const int d = S.grp_t[g], P = slot_pitch(d), base = S.grp_base[g], cnt = S.grp_cnt[g];
+    for (int e = tid; e < P * GP; e += kScanThreads) {
+      if (e % P >= cnt) S.w[base * GP + e] = 0.f;
+    }
+  }
+  __syncthreads();
+}
+
+// Stage the plane words and scales of nbl (<= kScanBlocks) blocks starting at
+// pl / sp (the unit's arrays offset by the first block) and form u = s w.
+template <int GP>
+__device__ void scan_stage(ScanSmem<GP>& S, const uint64_t* __restrict__ pl, const uint16_t* __restrict__ sp,
+                           int64_t nb_cap, int nbl) {
+  const int tid = threadIdx.x;
+  const int n_groups = S.n_groups, n_slots = S.n_slots;
+  __syncthreads();  // the previous chunk's compute is done with words and u
+  for (int e = tid; e < n_groups * 32 * kScanBlocks; e += kScanThreads) {
+    const int r = e / kScanBlocks, lb = e % kScanBlocks;
+    const int row = S.row_of_lane[r];
+    if (row >= 0 && lb < nbl) {
+      const uint64_t w = pl[(int64_t)row * nb_cap + lb];
+      S.words[r * kWordPitch + 2 * lb] = (uint32_t)w;
+      S.words[r * kWordPitch + 2 * lb + 1] = (uint32_t)(w >> 32);
+    }
+  }
+  for (int e = tid; e < kScanBlocks * n_slots; e += kScanThreads) {
+    const int lb = e % kScanBlocks, slot = e / kScanBlocks;
+    const int ch = S.slot_ch[slot];
+    S.sc[e] = (ch >= 0 && lb < nbl) ? fp16_bits_to_float(sp[(int64_t)ch * nb_cap + lb]) : 0.f;
+  }
+  __syncthreads();
+  for (int e = tid; e < kScanBlocks * n_slots; e += kScanThreads) {
+    const int lb = e % kScanBlocks, slot = e / kScanBlocks;
+    const float sc = S.sc[e];
+    int g = 0;
+    while (g + 1 < n_groups && S.grp_base[g + 1] <= slot) ++g;
+    const int base = S.grp_base[g], m = slot - base, P = slot_pitch(S.grp_t[g]);
+    float* ud = S.u + (lb * n_slots + base) * GP;
+#pragma unroll
+    for (int hh = 0; hh < GP; ++hh) ud[hh * P + m] = sc * S.w[base * GP + hh * P + m];
+  }
+  __syncthreads();
+}
+
+// Score the staged blocks: warp w takes block w (w < nbl).  Scores of head g
+// for the chunk's token x go to out[g * ld + x], for x < n_valid.
+template <int GP>
+__device__ void scan_compute(const ScanSmem<GP>& S, int nbl, int G, float* out, int64_t ld, int64_t n_valid) {
+  const int lane = threadIdx.x & 31, lb = threadIdx.x >> 5;
+  if (lb >= nbl) return;
+  uint32_t keep[5], rot[5];
+  transpose_consts(lane, keep, rot);
+  unsigned long long acc0[GP], acc1[GP];
+#pragma unroll
+  for (int hh = 0; hh < GP; ++hh) acc0[hh] = acc1[hh] = 0ull;
+  const int n_groups = S.n_groups, n_slots = S.n_slots;
+  for (int g = 0; g < n_groups; ++g) {
+    const int d = S.grp_t[g], cnt = S.grp_cnt[g];
+    const uint32_t* wr = S.words + (g * 32 + lane) * kWordPitch + 2 * lb;
+    const uint32_t x0 = warp_transpose32(wr[0], keep, rot);
+    const uint32_t x1 = warp_transpose32(wr[1], keep, rot);
+    const uint32_t xa0 = x0 << 1, xb0 = x0 >> 9, xa1 = x1 << 1, xb1 = x1 >> 9;
+    const float* ug = S.u + (lb * n_slots + S.grp_base[g]) * GP;
+    switch (d) {
+      case 4: group_fields<4, GP>(cnt, xa0, xb0, xa1, xb1, ug, acc0, acc1); break;
+      case 3: group_fields<3, GP>(cnt, xa0, xb0, xa1, xb1, ug, acc0, acc1); break;
+      case 2: group_fields<2, GP>(cnt, xa0, xb0, xa1, xb1, ug, acc0, acc1); break;
+      default: group_fields<1, GP>(cnt, xa0, xb0, xa1, xb1, ug, acc0, acc1); break;
+    }
+  }
+  const int64_t x0 = (int64_t)lb * kBlock + lane;
+#pragma unroll
+  for (int hh = 0; hh < GP; ++hh) {
+    if (hh >= G) break;
+    float p0, p1, r0, r1;
+    unpack2(acc0[hh], p0, p1);
+    unpack2(acc1[hh], r0, r1);
+    if (x0 < n_valid) out[hh * ld + x0] = p0 + p1;
+    if (x0 + 32 < n_valid) out[hh * ld + x0 + 32] = r0 + r1;
+  }
+}
+
+}  // namespace bpkv

@@ -61,6 +61,7 @@ constexpr int kHistBits = 11;
 constexpr int kHistBins = 1 << kHistBits;
 constexpr int kCandCap = 4096;       // candidates kept from the threshold bucket
 constexpr int kSelCap = 8192;        // selected indices (k <= 8192)
+constexpr int kSelBatch = 8;         // independent score loads in flight per thread
 
 struct TopkSmem {
   uint32_t hist[kHistBins];
@@ -103,6 +104,7 @@ __device__ __forceinline__ int pow2_at_least(int x) {
 }
 
 __global__ void __launch_bounds__(kSelThreads) k_topk(TopkArgs a) {
+  pdl_enter();
   extern __shared__ __align__(16) unsigned char topk_raw[];
   TopkSmem& S = *reinterpret_cast<TopkSmem*>(topk_raw);
   const int row = blockIdx.x;
@@ -137,9 +139,19 @@ __global__ void __launch_bounds__(kSelThreads) k_topk(TopkArgs a) {
       const int shift = shifts[lvl], nb = 1 << widths[lvl];
       for (int b = tid; b < nb; b += kSelThreads) S.hist[b] = 0;
       __syncthreads();
-      for (int64_t i = lo + tid; i < hi; i += kSelThreads) {
-        const uint32_t u = ordered_key(sc[i]);
-        if ((u & pmask) == pref) atomicAdd(&S.hist[(u >> shift) & (nb - 1)], 1u);
+      for (int64_t base = lo; base < hi; base += kSelBatch * kSelThreads) {
+        float v[kSelBatch];
+#pragma unroll
+        for (int b = 0; b < kSelBatch; ++b) {
+          const int64_t i = base + b * kSelThreads + tid;
+          v[b] = i < hi ? sc[i] : 0.f;
+        }
+#pragma unroll
+        for (int b = 0; b < kSelBatch; ++b) {
+          const int64_t i = base + b * kSelThreads + tid;
+          const uint32_t u = ordered_key(v[b]);
+          if (i < hi && (u & pmask) == pref) atomicAdd(&S.hist[(u >> shift) & (nb - 1)], 1u);
+        }
       }
       __syncthreads();
       if (tid < 32) {
@@ -179,14 +191,25 @@ __global__ void __launch_bounds__(kSelThreads) k_topk(TopkArgs a) {
     const uint32_t above = pref | ~pmask;
     const bool exact = pmask == 0xFFFFFFFFu && S.hist[pref & (kHistBins / 2 - 1)] > (uint32_t)kCandCap;
     if (!exact) {
-      for (int64_t i = lo + tid; i < hi; i += kSelThreads) {
-        const uint32_t u = ordered_key(sc[i]);
-        if (u > above) {
-          sel_push(S, (int32_t)i);
-        } else if ((u & pmask) == pref) {
-          const uint32_t c = atomicAdd(&S.n_cand, 1u);
-          if (c < (uint32_t)kCandCap)
-            S.cand[c] = ((unsigned long long)u << 32) | (0xFFFFFFFFu - (uint32_t)i);
+      for (int64_t base = lo; base < hi; base += kSelBatch * kSelThreads) {
+        float v[kSelBatch];
+#pragma unroll
+        for (int b = 0; b < kSelBatch; ++b) {
+          const int64_t i = base + b * kSelThreads + tid;
+          v[b] = i < hi ? sc[i] : 0.f;
+        }
+#pragma unroll
+        for (int b = 0; b < kSelBatch; ++b) {
+          const int64_t i = base + b * kSelThreads + tid;
+          if (i >= hi) continue;
+          const uint32_t u = ordered_key(v[b]);
+          if (u > above) {
+            sel_push(S, (int32_t)i);
+          } else if ((u & pmask) == pref) {
+            const uint32_t c = atomicAdd(&S.n_cand, 1u);
+            if (c < (uint32_t)kCandCap)
+              S.cand[c] = ((unsigned long long)u << 32) | (0xFFFFFFFFu - (uint32_t)i);
+          }
         }
       }
       __syncthreads();
@@ -233,8 +256,7 @@ cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, in
   const int smem = (int)sizeof(TopkSmem);
   cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k_topk<<<c.n_seq * c.n_kv_heads * c.group, kSelThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_topk, dim3(c.n_seq * c.n_kv_heads * c.group), dim3(kSelThreads), smem, st, a);
 }
 
 // ---------------------------------------------------------------- union
@@ -268,6 +290,7 @@ __device__ __forceinline__ int upper_bound_i32(const int32_t* v, int n, int32_t 
 }
 
 __global__ void __launch_bounds__(kSelThreads) k_union(UnionArgs a) {
+  pdl_enter();
   extern __shared__ __align__(16) int32_t usm[];
   const int G = a.group, k = a.k;
   int32_t* L = usm;              // [G][k] lists
@@ -342,8 +365,7 @@ cudaError_t launch_union(const bpkv_cache& c, const int32_t* idx, int32_t k, int
     if (e != cudaSuccess) return e;
   }
   UnionArgs a{idx, uidx, umask, ucount, c.group, k};
-  k_union<<<c.n_seq * c.n_kv_heads, kSelThreads, sm, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_union, dim3(c.n_seq * c.n_kv_heads), dim3(kSelThreads), sm, st, a);
 }
 
 }  // namespace bpkv

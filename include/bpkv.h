@@ -252,10 +252,25 @@ typedef struct bpkv_step_args {
   void *const *stage_events;/* optional [L][BPKV_STAGE_EVENTS] cudaEvent_t, NULL to skip:
                                recorded on `stream` (as external events, so they also
                                time graph replays) before encode, depths, scan, top-k,
-                               union, attention and after attention */
+                               union, attention and after attention; on the fused path
+                               the first five stages are the fused kernel and the
+                               last one the sequence-length update */
+  int32_t flags;            /* BPKV_STEP_* */
 } bpkv_step_args;
 
 #define BPKV_STAGE_EVENTS 7
+#define BPKV_STEP_FUSED 1       /* use the fused cluster kernel when bpkv_step_fused allows it */
+
+/*
+ * 1 when bpkv_decode_step, given BPKV_STEP_FUSED, can run a layer of this cache
+ * as one fused kernel per pass (a thread-block cluster per (sequence, KV head)
+ * doing append, depths, scan, top-k, union and attention in shared and
+ * distributed shared memory), 0 when it runs the per-stage kernels.  Fused needs: not dense, G <= 8, at most
+ * 40960 tokens after the append (5120 per CTA), k - n_sink - n_recent <= 988,
+ * and the shared memory the group size implies.  Results are identical to the
+ * per-stage path's up to float rounding of the attention.
+ */
+int bpkv_step_fused(const bpkv_cache *c, int32_t k, int32_t n_sink, int32_t n_recent, int32_t depth_rule);
 
 /*
  * One decode step over n_layers layers (each its own bpkv_cache, same shapes):

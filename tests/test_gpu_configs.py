@@ -18,23 +18,26 @@ def pk():
     return m
 
 
-def test_tiny_all_units(pk, orc):
+@pytest.mark.parametrize("flags", [1, 0], ids=["fused", "per_stage"])
+def test_tiny_all_units(pk, orc, flags):
     from workload import CONFIGS, gen_layer
     cfg = CONFIGS["tiny"]
     inp = gen_layer(cfg, 0, device="cpu")
-    cache, d, idx, out = decode_one_layer(inp, cfg)
+    cache, d, idx, out = decode_one_layer(inp, cfg, flags=flags)
     same, _ = check_unit(orc, cfg, inp, cache, d, idx, out, 0, 0, what="tiny")
     assert same >= 3
 
 
+@pytest.mark.parametrize("flags", [1, 0], ids=["fused", "per_stage"])
 @pytest.mark.parametrize("budget", [68, 92, 136])
-def test_qwen3_layer_all_units(pk, orc, budget):
+def test_qwen3_layer_all_units(pk, orc, budget, flags):
     from workload import CONFIGS, gen_layer
     cfg = CONFIGS["qwen3_8b_layer"]
     inp = gen_layer(cfg, 0, device="cuda")
     inp.k, inp.v = inp.k.cpu(), inp.v.cpu()
     b = torch.full((cfg.n_seq,), budget, dtype=torch.int32)
-    cache, d, idx, out = decode_one_layer(inp, cfg, budgets=b)
+    cache, d, idx, out = decode_one_layer(inp, cfg, budgets=b, flags=flags)
+    assert pk.bpkv_step_fused(cache.c, cfg.k, cfg.n_sink, cfg.n_recent, 0)
     same_total, found = 0, 0
     for h in range(cfg.n_kv_heads):
         same, _ = check_unit(orc, cfg, inp, cache, d, idx, out, 0, h, budget_bits=budget, what=f"b{budget} h{h}")
@@ -82,3 +85,38 @@ def test_multi_session_sampled(pk, orc):
     for s in range(cfg.n_seq):
         for h in range(cfg.n_kv_heads):
             assert depth_quarter_bits(dd[s, h]) <= 4 * int(inp.budgets[s])
+
+
+@pytest.mark.parametrize("wl,n_tok,rule,fixed", [("qwen3_8b_layer", 32768, 0, (0, 0)),
+                                                 ("qwen3_8b_layer", 20000 + 13, 1, (32, 4)),
+                                                 ("qwen3_8b_layer", 1000, 1, (128, 2)),
+                                                 ("tiny", 4096, 0, (0, 0)),
+                                                 ("tiny", 100, 0, (0, 0))])
+def test_fused_matches_per_stage(pk, wl, n_tok, rule, fixed):
+    """The fused cluster kernel and the per-stage kernels share the scan
+    arithmetic: same depths, same selections; attention within float rounding."""
+    from workload import CONFIGS, gen_layer
+    cfg = CONFIGS[wl]
+    inp = gen_layer(cfg, 3, device="cuda", n_tokens=n_tok)
+    r_f = decode_one_layer(inp, cfg, depth_rule=rule, fixed=fixed, flags=1)
+    r_s = decode_one_layer(inp, cfg, depth_rule=rule, fixed=fixed, flags=0)
+    assert pk.bpkv_step_fused(r_f[0].c, cfg.k, cfg.n_sink, cfg.n_recent, rule)
+    assert torch.equal(r_f[1], r_s[1])
+    assert torch.equal(r_f[2], r_s[2])
+    assert torch.max(torch.abs(r_f[3] - r_s[3])).item() < 1e-4
+    nb = (n_tok + 63) // 64  # words past the last block are never written
+    assert torch.equal(r_f[0].planes[..., :nb], r_s[0].planes[..., :nb])
+    assert torch.equal(r_f[0].scales[..., :nb], r_s[0].scales[..., :nb])
+    assert torch.equal(r_f[0].seq_len, r_s[0].seq_len)
+
+
+def test_fused_eligibility(pk):
+    from bit_plane_kv_encode_gb300 import Cache
+    small = Cache(1, 8, 4, 33280)
+    small.c.n_max = 32767
+    assert pk.bpkv_step_fused(small.c, 512, 4, 32, 0)
+    assert not pk.bpkv_step_fused(small.c, 512, 4, 32, 2)       # dense
+    assert not pk.bpkv_step_fused(small.c, 2048, 4, 32, 0)      # k too large for the merge buffers
+    big = Cache(1, 1, 4, 131584)
+    big.c.n_max = 131071
+    assert not pk.bpkv_step_fused(big.c, 512, 4, 32, 0)         # 16384 tokens per CTA
