@@ -48,6 +48,7 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--fused", action="store_true", help="one fused cluster kernel per pass where eligible")
+    p.add_argument("--tail", action="store_true", help="one cluster kernel for top-k, union and attention")
     p.add_argument("--budget", type=int, default=0, help="run this budget only (bits/token)")
     return p.parse_args()
 
@@ -242,7 +243,8 @@ def bench_ours(args, cfg, rank, world, local):
     import __graft_entry__
     __graft_entry__.build()
     budgets = [args.budget] if args.budget else None
-    inp, passes, ws, io = make_workload(cfg, args.steps, args.warmup, dev, 1 if args.fused else 0, budgets)
+    inp, passes, ws, io = make_workload(cfg, args.steps, args.warmup, dev,
+                                       (1 if args.fused else 0) | (2 if args.tail else 0), budgets)
     N, H, n, D = cfg.n_seq, cfg.n_kv_heads, cfg.n_tokens, cfg.head_dim
     G, L = cfg.group, cfg.n_layers
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)

@@ -19,7 +19,7 @@ HEAD_DIM = 128
 WS_SCAN_TOPK, WS_ATTEND, WS_DENSE, WS_STEP = 1, 2, 4, 8
 DEPTH_WATERFILL, DEPTH_FIXED, DEPTH_DENSE = 0, 1, 2
 DEV_OVERFLOW, DEV_SELECT = 1, 2
-STEP_FUSED = 1
+STEP_FUSED, STEP_TAIL = 1, 2
 
 
 class Cache:

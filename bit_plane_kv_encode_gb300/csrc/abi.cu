@@ -23,6 +23,9 @@ cudaError_t launch_attend(const bpkv_cache& c, const float* q, const int32_t* ui
 size_t attend_part_bytes(const bpkv_cache& c, int64_t rows, bool dense);
 cudaError_t launch_bump_len(const bpkv_cache& c, int32_t t_new, cudaStream_t st);
 bool fused_eligible(const bpkv_cache& c, int32_t k, int32_t n_sink, int32_t n_recent, int32_t depth_rule);
+bool tail_eligible(const bpkv_cache& c, int32_t k, int32_t n_sink, int32_t n_recent);
+cudaError_t launch_select_attend(const bpkv_cache& c, const float* scores, int64_t ld, const float* q, int32_t k,
+                                 int32_t n_sink, int32_t n_recent, float* out, int32_t* idx_out, cudaStream_t st);
 cudaError_t launch_decode_fused(const bpkv_cache& c, const uint16_t* k_new, const uint16_t* v_new, const float* q,
                                 const float* sigma2, const int32_t* budget_q, int32_t depth_rule,
                                 int32_t fixed_channels, int32_t fixed_depth, int32_t k, int32_t n_sink,
@@ -325,6 +328,13 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
     BPKV_TRY(mark(l, 2));
     BPKV_TRY(cuda_status(launch_scan(c, q, depths, scores, c.cap_tokens, st)));
     BPKV_TRY(mark(l, 3));
+    if ((a->flags & BPKV_STEP_TAIL) && tail_eligible(c, a->k, a->n_sink, a->n_recent)) {
+      int32_t* iout = a->idx_out ? a->idx_out + (size_t)l * NH * G * a->k : nullptr;
+      BPKV_TRY(cuda_status(
+          launch_select_attend(c, scores, c.cap_tokens, q, a->k, a->n_sink, a->n_recent, out, iout, st)));
+      for (int e = 4; e <= 6; ++e) BPKV_TRY(mark(l, e));
+      continue;
+    }
     BPKV_TRY(cuda_status(launch_topk(c, scores, c.cap_tokens, a->k, a->n_sink, a->n_recent, idx, status, st)));
     BPKV_TRY(mark(l, 4));
     BPKV_TRY(cuda_status(launch_union(c, idx, a->k, uidx, umask, ucount, st)));

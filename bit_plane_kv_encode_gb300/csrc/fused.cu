@@ -26,6 +26,7 @@
 // The sequence length is advanced by a separate kernel afterwards.
 #include <cooperative_groups.h>
 
+#include "cluster_core.cuh"
 #include "depths_core.cuh"
 #include "encode_core.cuh"
 #include "scan_core.cuh"
@@ -38,10 +39,7 @@ constexpr int kFuseCS = 8;                 // CTAs per cluster
 constexpr int kFuseThreads = kScanThreads; // 256
 constexpr int kFuseMaxBlocks = 80;         // blocks per CTA (5120 tokens)
 constexpr int kFuseMaxTok = kFuseMaxBlocks * kBlock;
-constexpr int kFuseBins = 2048;
-constexpr int kFuseCand = 2048;            // threshold-bin candidates kept before falling back to a full sort
-constexpr int kFuseSortCap = 8192;         // entries of the full-sort fallback
-constexpr int kFuseMaxTop = 988;           // k - n_sink - n_recent at most (k <= 1024)
+constexpr int kFuseMaxTop = kClMaxTop;
 
 struct FusedArgs {
   uint64_t* planes;
@@ -71,17 +69,11 @@ union FusedScratch {
   uint16_t kb[kBlock][kD];
   DepthSmem dep;
   ScanSmem<GP> scan;
-  struct {
-    uint32_t hist[kFuseBins];
-    unsigned long long buf[kFuseSortCap];   // candidates, or every entry for the full sort
-    unsigned long long win[kFuseMaxTop + 4];
-    uint32_t warp_red[32];
-    uint32_t n_buf, n_win, bin, rem, lo_key, hi_key, n_over;
-  } sel;
+  SelScratch sel;
   struct {
     int32_t rows[kFuseMaxTok];
-    float m[8][BPKV_MAX_GROUP], l[8][BPKV_MAX_GROUP];
-    float o[8][BPKV_MAX_GROUP][kD];
+    uint8_t rmask[kFuseMaxTok];
+    AttScratch a;
     uint32_t warp_red[32];
     uint32_t n_rows;
   } att;
@@ -98,155 +90,6 @@ struct FusedSmem {
   FusedScratch<GP> x;
   // followed by the merge buffer of merge_cap 64-bit entries
 };
-
-__device__ __forceinline__ unsigned long long sel_entry(uint32_t key, uint32_t tok) {
-  return ((unsigned long long)key << 32) | (0xFFFFFFFFu - tok);  // larger = earlier
-}
-__device__ __forceinline__ uint32_t entry_tok(unsigned long long e) { return 0xFFFFFFFFu - (uint32_t)e; }
-
-__device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, uint32_t* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  uint32_t s = 0;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w];
-  __syncthreads();
-  return s;
-}
-
-__device__ __forceinline__ uint32_t block_min_max(uint32_t v, bool is_max, uint32_t* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const uint32_t y = __shfl_xor_sync(0xffffffffu, v, o);
-    v = is_max ? max(v, y) : min(v, y);
-  }
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  uint32_t s = red[0];
-  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) s = is_max ? max(s, red[w]) : min(s, red[w]);
-  __syncthreads();
-  return s;
-}
-
-template <typename T>
-__device__ void cta_bitonic(T* v, int n2, bool desc) {
-  for (int size = 2; size <= n2; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int t = threadIdx.x; t < n2 / 2; t += blockDim.x) {
-        const int i = 2 * t - (t & (stride - 1));
-        const int j = i + stride;
-        const bool d = ((i & size) == 0) == desc;
-        const T a = v[i], b = v[j];
-        if ((a < b) == d) {
-          v[i] = b;
-          v[j] = a;
-        }
-      }
-      __syncthreads();
-    }
-  }
-}
-
-__device__ __forceinline__ int pow2_ge(int x) {
-  int p = 1;
-  while (p < x) p <<= 1;
-  return p;
-}
-
-// Exact top-m of cnt entries (u64: key << 32 | ~token; larger first) given by
-// get(e).  Winners are handed to emit(entry) (each exactly once).  Scratch S.
-template <int GP, typename Get, typename Emit>
-__device__ void cta_select(FusedScratch<GP>& X, int cnt, int m, Get get, Emit emit) {
-  auto& S = X.sel;
-  const int tid = threadIdx.x;
-  if (m <= 0 || cnt <= 0) return;
-  if (cnt <= m) {
-    for (int e = tid; e < cnt; e += blockDim.x) emit(get(e));
-    __syncthreads();
-    return;
-  }
-  // key range
-  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
-  for (int e = tid; e < cnt; e += blockDim.x) {
-    const uint32_t k = (uint32_t)(get(e) >> 32);
-    lo = min(lo, k);
-    hi = max(hi, k);
-  }
-  lo = block_min_max(lo, false, S.warp_red);
-  hi = block_min_max(hi, true, S.warp_red);
-  // monotone bin map (any non-decreasing map of the key works for selection)
-  const float scale = (float)kFuseBins / ((float)(hi - lo) + 1.f);
-  auto bin_of = [&](uint32_t k) -> int { return min((int)((float)(k - lo) * scale), kFuseBins - 1); };
-  for (int b = tid; b < kFuseBins; b += blockDim.x) S.hist[b] = 0;
-  if (tid == 0) {
-    S.n_buf = 0;
-    S.n_over = 0;
-  }
-  __syncthreads();
-  for (int e = tid; e < cnt; e += blockDim.x) atomicAdd(&S.hist[bin_of((uint32_t)(get(e) >> 32))], 1u);
-  __syncthreads();
-  // threshold bin: the bin holding the m-th largest key, scanned from the top
-  if (tid < 32) {
-    const int per = kFuseBins / 32;
-    const int top = kFuseBins - 1 - tid * per;
-    uint32_t loc = 0;
-    for (int q = 0; q < per; ++q) loc += S.hist[top - q];
-    uint32_t incl = loc;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (tid >= o) incl += y;
-    }
-    const uint32_t excl = incl - loc;
-    if (excl < (uint32_t)m && (uint32_t)m <= incl) {
-      uint32_t cum = excl;
-      int d = top;
-      for (int q = 0; q < per; ++q, --d) {
-        if (cum + S.hist[d] >= (uint32_t)m) break;
-        cum += S.hist[d];
-      }
-      S.bin = (uint32_t)d;
-      S.rem = (uint32_t)m - cum;
-    }
-  }
-  __syncthreads();
-  const int tb = (int)S.bin;
-  const uint32_t rem = S.rem;
-  const bool crowded = S.hist[tb] > (uint32_t)kFuseCand;
-  __syncthreads();
-  if (!crowded) {
-    for (int e = tid; e < cnt; e += blockDim.x) {
-      const unsigned long long v = get(e);
-      const int b = bin_of((uint32_t)(v >> 32));
-      if (b > tb) {
-        emit(v);
-      } else if (b == tb) {
-        const uint32_t c = atomicAdd(&S.n_buf, 1u);
-        S.buf[c] = v;
-      }
-    }
-    __syncthreads();
-    const int nb = (int)S.n_buf;
-    const int n2 = pow2_ge(max(nb, 2));
-    for (int e = nb + tid; e < n2; e += blockDim.x) S.buf[e] = 0ull;
-    __syncthreads();
-    cta_bitonic(S.buf, n2, true);
-    for (int e = tid; e < (int)rem; e += blockDim.x) emit(S.buf[e]);
-  } else {
-    // many keys in one bin: sort every entry (exact, slower)
-    const int n2 = pow2_ge(max(cnt, 2));
-    for (int e = tid; e < n2; e += blockDim.x) S.buf[e] = e < cnt ? get(e) : 0ull;
-    __syncthreads();
-    cta_bitonic(S.buf, n2, true);
-    for (int e = tid; e < m; e += blockDim.x) emit(S.buf[e]);
-  }
-  __syncthreads();
-}
 
 template <int GP>
 __global__ void __launch_bounds__(kFuseThreads) k_decode_fused(FusedArgs a) {
@@ -333,8 +176,8 @@ __global__ void __launch_bounds__(kFuseThreads) k_decode_fused(FusedArgs a) {
       const float* sg = S.scores + g * T;
       if (tid == 0) S.x.sel.n_win = 0;
       __syncthreads();
-      cta_select<GP>(
-          S.x, cb - ca, n_top,
+      cta_select(
+          S.x.sel, cb - ca, n_top,
           [&](int e) -> unsigned long long {
             return sel_entry(ordered_key(sg[ca + e]), (uint32_t)(t_begin + ca + e));
           },
@@ -357,8 +200,8 @@ __global__ void __launch_bounds__(kFuseThreads) k_decode_fused(FusedArgs a) {
   if (!take_all && n_top > 0 && rank < G) {
     const int g = rank;
     const int cnt = (int)min(S.merge_n[g], (uint32_t)a.merge_cap);
-    cta_select<GP>(
-        S.x, cnt, n_top, [&](int e) -> unsigned long long { return merge[e]; },
+    cta_select(
+        S.x.sel, cnt, n_top, [&](int e) -> unsigned long long { return merge[e]; },
         [&](unsigned long long v) {
           const uint32_t tok = entry_tok(v);
           const int owner = (int)(tok / (uint32_t)T);
@@ -402,7 +245,6 @@ __global__ void __launch_bounds__(kFuseThreads) k_decode_fused(FusedArgs a) {
       }
     }
     // ordered compaction of this CTA's selected tokens, all heads per 256-token tile
-    uint32_t* wred = S.x.att.warp_red;  // [8 warps][4 heads] packed below
     __shared__ uint32_t tile_cnt[8][BPKV_MAX_GROUP];
     for (int x0 = 0; x0 < n_own; x0 += kFuseThreads) {
       const int x = x0 + tid;
@@ -425,7 +267,6 @@ __global__ void __launch_bounds__(kFuseThreads) k_decode_fused(FusedArgs a) {
       }
       __syncthreads();
     }
-    (void)wred;
     if (rank == kFuseCS - 1)
       for (int g = 0; g < G; ++g)
         for (int p = (int)total[g] + tid; p < a.k; p += kFuseThreads) a.idx_out[(unit * G + g) * a.k + p] = -1;
@@ -438,133 +279,25 @@ __global__ void __launch_bounds__(kFuseThreads) k_decode_fused(FusedArgs a) {
     __syncthreads();
     for (int x0 = 0; x0 < n_own; x0 += kFuseThreads) {
       const int x = x0 + tid;
-      const uint32_t f = (x < n_own) ? ((S.mask[x >> 2] >> (8 * (x & 3))) & 0xffu) != 0 : 0u;
-      const uint32_t bal = __ballot_sync(0xffffffffu, f);
+      const uint32_t mk = (x < n_own) ? ((S.mask[x >> 2] >> (8 * (x & 3))) & 0xffu) : 0u;
+      const uint32_t bal = __ballot_sync(0xffffffffu, mk != 0u);
       uint32_t wbase = 0;
       if (lane == 0 && bal) wbase = atomicAdd(&A.n_rows, (uint32_t)__popc(bal));
       wbase = __shfl_sync(0xffffffffu, wbase, 0);
-      if (f) A.rows[wbase + __popc(bal & ((1u << lane) - 1u))] = x;
+      if (mk) {
+        const uint32_t r = wbase + __popc(bal & ((1u << lane) - 1u));
+        A.rows[r] = x;
+        A.rmask[r] = (uint8_t)mk;
+      }
     }
     __syncthreads();
-    const int nrows = (int)A.n_rows;
-    const float qscale = 0.08838834764831845f * 1.4426950408889634f;
-    float qr[GP][4];
-#pragma unroll
-    for (int g = 0; g < GP; ++g)
-#pragma unroll
-      for (int d = 0; d < 4; ++d) qr[g][d] = (g < G) ? qp[g * kD + lane * 4 + d] * qscale : 0.f;
-    float m[GP], l[GP], o[GP][4];
-#pragma unroll
-    for (int g = 0; g < GP; ++g) {
-      m[g] = -INFINITY;
-      l[g] = 0.f;
-#pragma unroll
-      for (int d = 0; d < 4; ++d) o[g][d] = 0.f;
-    }
-    const uint16_t* kb = a.k_rows + U.row_base(unit) + t_begin * kD + lane * 4;
-    const uint16_t* vb = a.v_rows + U.row_base(unit) + t_begin * kD + lane * 4;
-    constexpr int RB = 4;
-    for (int rb = warp; rb < nrows; rb += 8 * RB) {
-      uint2 kw[RB], vw[RB];
-      uint32_t mk[RB];
-#pragma unroll
-      for (int b = 0; b < RB; ++b) {
-        const int r = rb + b * 8;
-        mk[b] = 0;
-        if (r < nrows) {
-          const int x = A.rows[r];
-          mk[b] = (S.mask[x >> 2] >> (8 * (x & 3))) & 0xffu;
-          kw[b] = *reinterpret_cast<const uint2*>(kb + (int64_t)x * kD);
-          vw[b] = *reinterpret_cast<const uint2*>(vb + (int64_t)x * kD);
-        }
-      }
-#pragma unroll
-      for (int b = 0; b < RB; ++b) {
-        if (mk[b] == 0) continue;
-        const float kf[4] = {__uint_as_float(kw[b].x << 16), __uint_as_float(kw[b].x & 0xffff0000u),
-                             __uint_as_float(kw[b].y << 16), __uint_as_float(kw[b].y & 0xffff0000u)};
-        const float vf[4] = {__uint_as_float(vw[b].x << 16), __uint_as_float(vw[b].x & 0xffff0000u),
-                             __uint_as_float(vw[b].y << 16), __uint_as_float(vw[b].y & 0xffff0000u)};
-#pragma unroll
-        for (int g = 0; g < GP; ++g) {
-          if (g >= G || !((mk[b] >> g) & 1u)) continue;
-          float dot = qr[g][0] * kf[0];
-          dot = fmaf(qr[g][1], kf[1], dot);
-          dot = fmaf(qr[g][2], kf[2], dot);
-          dot = fmaf(qr[g][3], kf[3], dot);
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-          const float mn = fmaxf(m[g], dot);
-          const float corr = exp2f(m[g] - mn);
-          const float p = exp2f(dot - mn);
-          l[g] = l[g] * corr + p;
-#pragma unroll
-          for (int d = 0; d < 4; ++d) o[g][d] = fmaf(o[g][d], corr, p * vf[d]);
-          m[g] = mn;
-        }
-      }
-    }
-#pragma unroll
-    for (int g = 0; g < GP; ++g) {
-      if (lane == 0) {
-        A.m[warp][g] = m[g];
-        A.l[warp][g] = l[g];
-      }
-#pragma unroll
-      for (int d = 0; d < 4; ++d) A.o[warp][g][lane * 4 + d] = o[g][d];
-    }
-    __syncthreads();
-    for (int e = tid; e < GP * kD; e += kFuseThreads) {
-      const int g = e / kD, d = e % kD;
-      float M = -INFINITY;
-      for (int w = 0; w < 8; ++w)
-        if (A.l[w][g] > 0.f) M = fmaxf(M, A.m[w][g]);
-      float L = 0.f, O = 0.f;
-      if (M != -INFINITY) {
-        for (int w = 0; w < 8; ++w) {
-          if (!(A.l[w][g] > 0.f)) continue;
-          const float f = exp2f(A.m[w][g] - M);
-          L += A.l[w][g] * f;
-          O += A.o[w][g][d] * f;
-        }
-      }
-      S.part[g][d] = O;
-      if (d == 0) {
-        S.part[g][kD] = M;
-        S.part[g][kD + 1] = L;
-      }
-    }
+    attend_rows<GP>(A.a, A.rows, A.rmask, (int)A.n_rows, a.k_rows + U.row_base(unit) + t_begin * kD,
+                    a.v_rows + U.row_base(unit) + t_begin * kD, qp, G, S.part);
   }
   cluster.sync();
 
   // ---- 6. leaders merge their head's partials
-  if (rank < G) {
-    const int g = rank;
-    const int d = tid;
-    if (d < kD) {
-      float mr[kFuseCS], lr[kFuseCS];
-      float M = -INFINITY;
-#pragma unroll
-      for (int r = 0; r < kFuseCS; ++r) {
-        const float* pr = cluster.map_shared_rank(&S.part[g][0], r);
-        mr[r] = pr[kD];
-        lr[r] = pr[kD + 1];
-        if (lr[r] > 0.f) M = fmaxf(M, mr[r]);
-      }
-      float L = 0.f, O = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int r = 0; r < kFuseCS; ++r) {
-          if (!(lr[r] > 0.f)) continue;
-          const float* pr = cluster.map_shared_rank(&S.part[g][0], r);
-          const float f = exp2f(mr[r] - M);
-          L += lr[r] * f;
-          O += pr[d] * f;
-        }
-      }
-      a.out[(unit * G + g) * kD + d] = (L > 0.f) ? O / L : 0.f;
-    }
-  }
+  if (rank < G) merge_partials<kFuseCS>(cluster, S.part, rank, a.out + (unit * G + rank) * kD);
   cluster.sync();
 }
 

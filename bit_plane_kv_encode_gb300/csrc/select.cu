@@ -1,14 +1,16 @@
 // Selection (Fathom page, section 2, "Top-k decoding") and the GQA union of
 // winner rows (section 1 / section 3.1: k_U <= G k distinct rows per KV head).
 //
-// Top-k: one CTA per query head.  Scores map to order-preserving 32-bit keys.
-// A histogram of the top 11 key bits over the candidates (tokens that are
-// neither sinks nor recent) locates the bucket holding the
-// (k - n_sink - n_recent)-th largest key; if that bucket is crowded the next 11
-// bits (then the last 10) refine it.  One more pass takes every key above the
-// bucket and gathers the bucket's keys, which a shared-memory bitonic sort by
-// (key desc, index asc) cuts at the exact count: ties go to the lower index.
-// Sinks, recent tokens and the winners are finally sorted ascending.
+// Top-k: one CTA per query head.  Scores map to order-preserving 32-bit keys
+// (staged in shared memory when the row's candidates fit).  A linear histogram
+// over the candidates' key range [min, max] locates the bucket holding the
+// (k - n_sink - n_recent)-th largest key (bins follow the data, so no bin takes
+// most of the atomics); a crowded bucket is refined the same way over its own
+// exact key range.  One more pass takes every key above the bucket and gathers
+// the bucket's keys, which a shared-memory bitonic sort by (key desc, index
+// asc) cuts at the exact count: ties go to the lower index, with an ordered
+// scan when more than kCandCap keys equal the threshold key.  Sinks, recent
+// tokens and the winners are finally sorted ascending.
 //
 // Union: one CTA per KV head.  Each sorted list entry's rank in the merge of
 // the G lists is its own position plus binary-search counts in the other
@@ -57,22 +59,24 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* warp_t
   return r;
 }
 
-constexpr int kHistBits = 11;
-constexpr int kHistBins = 1 << kHistBits;
-constexpr int kCandCap = 4096;       // candidates kept from the threshold bucket
+constexpr int kHistBins = 2048;
+constexpr int kCandCap = 4096;       // keys of the threshold bucket kept for the exact sort
 constexpr int kSelCap = 8192;        // selected indices (k <= 8192)
 constexpr int kSelBatch = 8;         // independent score loads in flight per thread
+constexpr int kStageKeys = 32768;    // candidates staged in shared memory when they fit
 
 struct TopkSmem {
+  uint32_t keys[kStageKeys];           // staged order-preserving keys of the candidates
   uint32_t hist[kHistBins];
   unsigned long long cand[kCandCap];   // (key << 32) | ~index: larger = earlier
   int32_t sel[kSelCap];
   uint32_t warp_tot[32];
-  uint32_t n_cand, n_sel, digit, rem, tot;
+  uint32_t red[2][32];
+  uint32_t n_cand, n_sel, tb, rem, tot, b_lo, b_hi;
 };
 
-// Bitonic sort of v[0..n2) (n2 a power of two) by the whole 64-bit value;
-// descending when desc, else ascending.  Called by the whole block.
+// Bitonic sort of v[0..n2) (n2 a power of two) by the whole value; descending
+// when desc, else ascending.  Called by the whole block.
 template <typename T>
 __device__ void block_bitonic(T* v, int n2, bool desc) {
   for (int size = 2; size <= n2; size <<= 1) {
@@ -103,6 +107,52 @@ __device__ __forceinline__ int pow2_at_least(int x) {
   return p;
 }
 
+// Block-wide min and max of (lo, hi) pairs.
+__device__ __forceinline__ void block_range(uint32_t& lo, uint32_t& hi, TopkSmem& S) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  if (lane == 0) {
+    S.red[0][warp] = lo;
+    S.red[1][warp] = hi;
+  }
+  __syncthreads();
+  lo = S.red[0][0];
+  hi = S.red[1][0];
+  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
+    lo = min(lo, S.red[0][w]);
+    hi = max(hi, S.red[1][w]);
+  }
+  __syncthreads();
+}
+
+// Visit the order-preserving keys of candidates [0, cnt) (staged in shared
+// memory, or read from the scores kSelBatch at a time): f(index, key).
+template <typename F>
+__device__ __forceinline__ void for_keys(const TopkSmem& S, bool staged, const float* sc, int64_t lo, int64_t cnt,
+                                         F f) {
+  if (staged) {
+    for (int64_t e = threadIdx.x; e < cnt; e += kSelThreads) f(e, S.keys[e]);
+    return;
+  }
+  for (int64_t e0 = threadIdx.x; e0 < cnt; e0 += (int64_t)kSelBatch * kSelThreads) {
+    float v[kSelBatch];
+#pragma unroll
+    for (int b = 0; b < kSelBatch; ++b) {
+      const int64_t e = e0 + (int64_t)b * kSelThreads;
+      v[b] = e < cnt ? sc[lo + e] : 0.f;
+    }
+#pragma unroll
+    for (int b = 0; b < kSelBatch; ++b) {
+      const int64_t e = e0 + (int64_t)b * kSelThreads;
+      if (e < cnt) f(e, ordered_key(v[b]));
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kSelThreads) k_topk(TopkArgs a) {
   pdl_enter();
   extern __shared__ __align__(16) unsigned char topk_raw[];
@@ -114,6 +164,7 @@ __global__ void __launch_bounds__(kSelThreads) k_topk(TopkArgs a) {
   int32_t* out = a.idx + (int64_t)row * a.k;
   const int64_t lo = min64(a.n_sink, n);
   const int64_t hi = max64(n - a.n_recent, lo);
+  const int64_t cnt = hi - lo;
   const int64_t n_top = max(a.k - a.n_sink - a.n_recent, 0);
   const int tid = threadIdx.x;
 
@@ -126,92 +177,91 @@ __global__ void __launch_bounds__(kSelThreads) k_topk(TopkArgs a) {
   for (int64_t i = tid; i < lo; i += kSelThreads) sel_push(S, (int32_t)i);
   for (int64_t i = hi + tid; i < n; i += kSelThreads) sel_push(S, (int32_t)i);
 
-  if (hi - lo <= n_top) {
+  if (cnt <= n_top) {
     for (int64_t i = lo + tid; i < hi; i += kSelThreads) sel_push(S, (int32_t)i);
   } else if (n_top > 0) {
-    // Threshold bucket: up to three levels (11, 11, 10 bits), stopping once the
-    // bucket holding the n_top-th largest key has at most kCandCap keys.
-    uint32_t pref = 0, pmask = 0;
-    uint32_t rem = (uint32_t)n_top;
-    const int shifts[3] = {21, 10, 0};
-    const int widths[3] = {11, 11, 10};
-    for (int lvl = 0; lvl < 3; ++lvl) {
-      const int shift = shifts[lvl], nb = 1 << widths[lvl];
-      for (int b = tid; b < nb; b += kSelThreads) S.hist[b] = 0;
-      __syncthreads();
-      for (int64_t base = lo; base < hi; base += kSelBatch * kSelThreads) {
+    const bool staged = cnt <= kStageKeys;
+    // key range of the candidates (staging them when they fit)
+    uint32_t klo = 0xFFFFFFFFu, khi = 0u;
+    if (staged) {
+      for (int e0 = tid; e0 < cnt; e0 += kSelBatch * kSelThreads) {
         float v[kSelBatch];
 #pragma unroll
         for (int b = 0; b < kSelBatch; ++b) {
-          const int64_t i = base + b * kSelThreads + tid;
-          v[b] = i < hi ? sc[i] : 0.f;
+          const int e = e0 + b * kSelThreads;
+          v[b] = e < cnt ? sc[lo + e] : 0.f;
         }
 #pragma unroll
         for (int b = 0; b < kSelBatch; ++b) {
-          const int64_t i = base + b * kSelThreads + tid;
-          const uint32_t u = ordered_key(v[b]);
-          if (i < hi && (u & pmask) == pref) atomicAdd(&S.hist[(u >> shift) & (nb - 1)], 1u);
-        }
-      }
-      __syncthreads();
-      if (tid < 32) {
-        // lane l owns bins [nb - (l+1) nb/32, nb - l nb/32), scanned from the top
-        const int per = nb / 32;
-        const int top = nb - 1 - tid * per;
-        uint32_t loc = 0;
-        for (int q = 0; q < per; ++q) loc += S.hist[top - q];
-        uint32_t incl = loc;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (tid >= o) incl += y;
-        }
-        const uint32_t excl = incl - loc;
-        if (excl < rem && rem <= incl) {
-          uint32_t cum = excl;
-          int d = top;
-          for (int q = 0; q < per; ++q, --d) {
-            if (cum + S.hist[d] >= rem) break;
-            cum += S.hist[d];
+          const int e = e0 + b * kSelThreads;
+          if (e < cnt) {
+            const uint32_t k = ordered_key(v[b]);
+            S.keys[e] = k;
+            klo = min(klo, k);
+            khi = max(khi, k);
           }
-          S.digit = (uint32_t)d;
-          S.rem = rem - cum;
         }
       }
-      __syncthreads();
-      const uint32_t dgt = S.digit;
-      rem = S.rem;
-      pref |= dgt << shift;
-      pmask |= (uint32_t)(nb - 1) << shift;
-      const bool done = S.hist[dgt] <= (uint32_t)kCandCap;
-      __syncthreads();
-      if (done) break;
+    } else {
+      for_keys(S, false, sc, lo, cnt, [&](int64_t, uint32_t k) {
+        klo = min(klo, k);
+        khi = max(khi, k);
+      });
     }
-    // keys above the bucket are selected; keys in it are candidates
-    const uint32_t above = pref | ~pmask;
-    const bool exact = pmask == 0xFFFFFFFFu && S.hist[pref & (kHistBins / 2 - 1)] > (uint32_t)kCandCap;
-    if (!exact) {
-      for (int64_t base = lo; base < hi; base += kSelBatch * kSelThreads) {
-        float v[kSelBatch];
-#pragma unroll
-        for (int b = 0; b < kSelBatch; ++b) {
-          const int64_t i = base + b * kSelThreads + tid;
-          v[b] = i < hi ? sc[i] : 0.f;
-        }
-#pragma unroll
-        for (int b = 0; b < kSelBatch; ++b) {
-          const int64_t i = base + b * kSelThreads + tid;
-          if (i >= hi) continue;
-          const uint32_t u = ordered_key(v[b]);
-          if (u > above) {
-            sel_push(S, (int32_t)i);
-          } else if ((u & pmask) == pref) {
-            const uint32_t c = atomicAdd(&S.n_cand, 1u);
-            if (c < (uint32_t)kCandCap)
-              S.cand[c] = ((unsigned long long)u << 32) | (0xFFFFFFFFu - (uint32_t)i);
-          }
-        }
+    block_range(klo, khi, S);
+    // Threshold bucket: a linear histogram over the active key range [klo, khi]
+    // locates the bucket holding the rem-th largest active key; a crowded
+    // bucket becomes the next active range (its exact min and max keys).
+    uint32_t rem = (uint32_t)n_top, b_lo = klo, b_hi = khi, bucket_n = 0;
+    for (int lvl = 0; lvl < 3; ++lvl) {
+      const float scale = (float)kHistBins / ((float)(khi - klo) + 1.f);
+      auto bin_of = [&](uint32_t k) { return min((int)((float)(k - klo) * scale), kHistBins - 1); };
+      for (int b = tid; b < kHistBins; b += kSelThreads) S.hist[b] = 0;
+      __syncthreads();
+      for_keys(S, staged, sc, lo, cnt, [&](int64_t, uint32_t k) {
+        if (k >= klo && k <= khi) atomicAdd(&S.hist[bin_of(k)], 1u);
+      });
+      __syncthreads();
+      // thread t owns bins 2047 - 2t and 2046 - 2t (descending); block scan
+      const uint32_t h0 = S.hist[kHistBins - 1 - 2 * tid], h1 = S.hist[kHistBins - 2 - 2 * tid];
+      const uint32_t ex = block_excl_scan(h0 + h1, S.warp_tot, &S.tot);
+      if (ex < rem && rem <= ex + h0) {
+        S.tb = kHistBins - 1 - 2 * tid;
+        S.rem = rem - ex;
+      } else if (ex + h0 < rem && rem <= ex + h0 + h1) {
+        S.tb = kHistBins - 2 - 2 * tid;
+        S.rem = rem - ex - h0;
       }
+      __syncthreads();
+      const int tb = (int)S.tb;
+      rem = S.rem;
+      bucket_n = S.hist[tb];
+      // exact key range of the bucket
+      uint32_t blo = 0xFFFFFFFFu, bhi = 0u;
+      for_keys(S, staged, sc, lo, cnt, [&](int64_t, uint32_t k) {
+        if (k >= klo && k <= khi && bin_of(k) == tb) {
+          blo = min(blo, k);
+          bhi = max(bhi, k);
+        }
+      });
+      block_range(blo, bhi, S);
+      b_lo = blo;
+      b_hi = bhi;
+      if (bucket_n <= (uint32_t)kCandCap || b_lo == b_hi) break;
+      klo = b_lo;
+      khi = b_hi;
+    }
+    if (bucket_n <= (uint32_t)kCandCap) {
+      // keys above the bucket are selected; the bucket's keys are sorted exactly
+      for_keys(S, staged, sc, lo, cnt, [&](int64_t e, uint32_t k) {
+        if (k > b_hi) {
+          sel_push(S, (int32_t)(lo + e));
+        } else if (k >= b_lo) {
+          const uint32_t c = atomicAdd(&S.n_cand, 1u);
+          if (c < (uint32_t)kCandCap)
+            S.cand[c] = ((unsigned long long)k << 32) | (0xFFFFFFFFu - (uint32_t)(lo + e));
+        }
+      });
       __syncthreads();
       const int nc = (int)min(S.n_cand, (uint32_t)kCandCap);
       const int nc2 = pow2_at_least(max(nc, 2));
@@ -221,19 +271,19 @@ __global__ void __launch_bounds__(kSelThreads) k_topk(TopkArgs a) {
       for (int e = tid; e < (int)rem && e < nc; e += kSelThreads)
         sel_push(S, (int32_t)(0xFFFFFFFFu - (uint32_t)S.cand[e]));
     } else {
-      // more than kCandCap keys equal the threshold key: take the rem of them
-      // with the lowest indices by an ordered scan over the candidates
+      // more than kCandCap keys equal the threshold key (b_lo == b_hi): take
+      // the rem of them with the lowest indices by an ordered scan
       uint32_t carry = 0;
-      for (int64_t base = lo; base < hi; base += kSelThreads) {
-        const int64_t i = base + tid;
+      for (int64_t base = 0; base < cnt; base += kSelThreads) {
+        const int64_t e = base + tid;
         uint32_t tie = 0;
-        if (i < hi) {
-          const uint32_t u = ordered_key(sc[i]);
-          if (u > above) sel_push(S, (int32_t)i);
-          else if (u == pref) tie = 1;
+        if (e < cnt) {
+          const uint32_t k = staged ? S.keys[e] : ordered_key(sc[lo + e]);
+          if (k > b_hi) sel_push(S, (int32_t)(lo + e));
+          else if (k == b_lo) tie = 1;
         }
         const uint32_t ex = block_excl_scan(tie, S.warp_tot, &S.tot) + carry;
-        if (tie && ex < rem) sel_push(S, (int32_t)i);
+        if (tie && ex < rem) sel_push(S, (int32_t)(lo + e));
         carry += S.tot;
         __syncthreads();
       }
@@ -242,12 +292,12 @@ __global__ void __launch_bounds__(kSelThreads) k_topk(TopkArgs a) {
   __syncthreads();
   const int ns = (int)S.n_sel;
   if (ns > a.k && tid == 0) set_status(a.status, BPKV_DEV_SELECT);
-  const int cnt = min(ns, a.k);
-  const int n2 = pow2_at_least(max(cnt, 2));
-  for (int e = cnt + tid; e < n2; e += kSelThreads) S.sel[e] = 0x7FFFFFFF;
+  const int cnt_out = min(ns, a.k);
+  const int n2 = pow2_at_least(max(cnt_out, 2));
+  for (int e = cnt_out + tid; e < n2; e += kSelThreads) S.sel[e] = 0x7FFFFFFF;
   __syncthreads();
   block_bitonic(S.sel, n2, false);
-  for (int e = tid; e < a.k; e += kSelThreads) out[e] = e < cnt ? S.sel[e] : -1;
+  for (int e = tid; e < a.k; e += kSelThreads) out[e] = e < cnt_out ? S.sel[e] : -1;
 }
 
 cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,

@@ -260,6 +260,8 @@ typedef struct bpkv_step_args {
 
 #define BPKV_STAGE_EVENTS 7
 #define BPKV_STEP_FUSED 1       /* use the fused cluster kernel when bpkv_step_fused allows it */
+#define BPKV_STEP_TAIL 2        /* after the scan, one cluster kernel for top-k, union and
+                                   attention instead of three separate kernels */
 
 /*
  * 1 when bpkv_decode_step, given BPKV_STEP_FUSED, can run a layer of this cache
@@ -276,7 +278,10 @@ int bpkv_step_fused(const bpkv_cache *c, int32_t k, int32_t n_sink, int32_t n_re
  * One decode step over n_layers layers (each its own bpkv_cache, same shapes):
  * append the new token (encode), choose depths, scan + top-k, union, sparse
  * attention (or dense attention for BPKV_DEPTH_DENSE).  Every layer's n_max is
- * raised by one.  Needs workspace BPKV_WS_STEP.
+ * raised by one.  Needs workspace BPKV_WS_STEP.  With BPKV_STEP_TAIL, selection,
+ * union and attention after the scan run as one kernel with a thread-block
+ * cluster per (sequence, KV head) when k - n_sink - n_recent <= 988 and G <= 8;
+ * the selections are the same either way.
  */
 int bpkv_decode_step(bpkv_cache *layers, int32_t n_layers, const bpkv_step_args *a, void *ws,
                      size_t ws_bytes, void *stream);

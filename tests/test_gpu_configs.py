@@ -18,7 +18,7 @@ def pk():
     return m
 
 
-@pytest.mark.parametrize("flags", [1, 0], ids=["fused", "per_stage"])
+@pytest.mark.parametrize("flags", [1, 2, 0], ids=["fused", "tail", "split"])
 def test_tiny_all_units(pk, orc, flags):
     from workload import CONFIGS, gen_layer
     cfg = CONFIGS["tiny"]
@@ -28,7 +28,7 @@ def test_tiny_all_units(pk, orc, flags):
     assert same >= 3
 
 
-@pytest.mark.parametrize("flags", [1, 0], ids=["fused", "per_stage"])
+@pytest.mark.parametrize("flags", [1, 2, 0], ids=["fused", "tail", "split"])
 @pytest.mark.parametrize("budget", [68, 92, 136])
 def test_qwen3_layer_all_units(pk, orc, budget, flags):
     from workload import CONFIGS, gen_layer
@@ -120,3 +120,19 @@ def test_fused_eligibility(pk):
     big = Cache(1, 1, 4, 131584)
     big.c.n_max = 131071
     assert not pk.bpkv_step_fused(big.c, 512, 4, 32, 0)         # 16384 tokens per CTA
+
+
+@pytest.mark.parametrize("wl,n_tok,budget", [("qwen3_8b_layer", 32768, 92), ("full_step", 131072, 136),
+                                             ("multi_session", 65536, None), ("tiny", 300, 68)])
+def test_tail_matches_split(pk, wl, n_tok, budget):
+    """The cluster tail (selection + union + attention in one kernel) and the
+    separate top-k / union / attention kernels select the same sets."""
+    from workload import CONFIGS, gen_layer
+    cfg = CONFIGS[wl]
+    inp = gen_layer(cfg, 7, device="cuda", n_tokens=n_tok, n_seq=min(cfg.n_seq, 4))
+    b = None if budget is None else torch.full((inp.k.shape[0],), budget, dtype=torch.int32)
+    r_t = decode_one_layer(inp, cfg, budgets=b, flags=2)
+    r_s = decode_one_layer(inp, cfg, budgets=b, flags=0)
+    assert torch.equal(r_t[1], r_s[1])
+    assert torch.equal(r_t[2], r_s[2])
+    assert torch.max(torch.abs(r_t[3] - r_s[3])).item() < 1e-4
