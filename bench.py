@@ -33,7 +33,15 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 STAGES = ["encode", "depths", "scan", "topk", "union", "attend"]
-LAUNCHES_PER_PASS = {"encode": 2, "depths": 1, "scan": 1, "topk": 1, "union": 1, "attend": 2}
+
+
+def launches_per_pass(p, args) -> int:
+    """Kernels bpkv_decode_step launches per layer on the path this pass takes."""
+    if p["fused"]:
+        return 2          # fused cluster kernel + length update
+    if args.tail:
+        return 5          # encode + length update, depths, scan, cluster tail
+    return 6              # encode + length update, depths, scan, top-k, range attention
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -372,7 +380,7 @@ def bench_ours(args, cfg, rank, world, local):
                            "union_rows": union_rows},
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": args.steps * L * sum(2 if p["fused"] else sum(LAUNCHES_PER_PASS.values()) for p in passes),
+        "gpu_launches": args.steps * L * sum(launches_per_pass(p, args) for p in passes),
         "clocks": clk,
         "wall_s_timed": round(wall, 3),
     }

@@ -8,9 +8,13 @@ namespace bpkv {
 cudaError_t launch_encode_append(const bpkv_cache& c, const uint16_t* k_new, const uint16_t* v_new, int32_t t_new,
                                  cudaStream_t st);
 cudaError_t launch_alloc_depths(const bpkv_cache& c, const float* q, const float* sigma2, const int32_t* budget_q,
-                                uint8_t* depths, cudaStream_t st);
+                                uint8_t* depths, cudaStream_t st, uint32_t* tickets = nullptr);
 cudaError_t launch_fixed_depths(const bpkv_cache& c, const float* q, int32_t n_channels, int32_t depth,
-                                uint8_t* depths, cudaStream_t st);
+                                uint8_t* depths, cudaStream_t st, uint32_t* tickets = nullptr);
+size_t attend_ranges_part_bytes(const bpkv_cache& c);
+bool attend_ranges_eligible(const bpkv_cache& c, int32_t k);
+cudaError_t launch_attend_ranges(const bpkv_cache& c, const float* q, const int32_t* idx, int32_t k, float* part,
+                                 uint32_t* tickets, float* out, cudaStream_t st);
 cudaError_t launch_scan(const bpkv_cache& c, const float* q, const uint8_t* depths, float* scores, int64_t ld,
                         cudaStream_t st);
 cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
@@ -70,7 +74,7 @@ int check_k(int32_t k, int32_t n_sink, int32_t n_recent) {
 
 // Workspace layout: status word, then the buffers each call family needs.
 struct Layout {
-  size_t scores = 0, part = 0, depths = 0, idx = 0, uidx = 0, umask = 0, ucount = 0, total = 0;
+  size_t scores = 0, part = 0, depths = 0, idx = 0, uidx = 0, umask = 0, ucount = 0, tickets = 0, total = 0;
 };
 
 Layout layout(const bpkv_cache& c, int32_t k, int32_t what) {
@@ -87,6 +91,10 @@ Layout layout(const bpkv_cache& c, int32_t k, int32_t what) {
     const size_t pd = attend_part_bytes(c, c.cap_tokens, true);
     if (pd > part) part = pd;
   }
+  if (what & BPKV_WS_STEP) {
+    const size_t pr = attend_ranges_part_bytes(c);
+    if (pr > part) part = pr;
+  }
   if (part) {
     L.part = off;
     off = align_up(off + part);
@@ -102,6 +110,8 @@ Layout layout(const bpkv_cache& c, int32_t k, int32_t what) {
     off = align_up(off + NH * c.group * (size_t)k);
     L.ucount = off;
     off = align_up(off + NH * sizeof(int32_t));
+    L.tickets = off;
+    off = align_up(off + NH * sizeof(uint32_t));
   }
   L.total = off;
   return L;
@@ -318,12 +328,13 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
     int32_t* uidx = reinterpret_cast<int32_t*>(at(ws, L.uidx));
     uint8_t* umask = at(ws, L.umask);
     int32_t* ucount = reinterpret_cast<int32_t*>(at(ws, L.ucount));
+    uint32_t* tickets = reinterpret_cast<uint32_t*>(at(ws, L.tickets));
     BPKV_TRY(mark(l, 1));
     if (a->depth_rule == BPKV_DEPTH_WATERFILL) {
       BPKV_TRY(cuda_status(
-          launch_alloc_depths(c, q, a->sigma2 + (size_t)l * NH * kD, a->budget_q, depths, st)));
+          launch_alloc_depths(c, q, a->sigma2 + (size_t)l * NH * kD, a->budget_q, depths, st, tickets)));
     } else {
-      BPKV_TRY(cuda_status(launch_fixed_depths(c, q, a->fixed_channels, a->fixed_depth, depths, st)));
+      BPKV_TRY(cuda_status(launch_fixed_depths(c, q, a->fixed_channels, a->fixed_depth, depths, st, tickets)));
     }
     BPKV_TRY(mark(l, 2));
     BPKV_TRY(cuda_status(launch_scan(c, q, depths, scores, c.cap_tokens, st)));
@@ -337,6 +348,13 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
     }
     BPKV_TRY(cuda_status(launch_topk(c, scores, c.cap_tokens, a->k, a->n_sink, a->n_recent, idx, status, st)));
     BPKV_TRY(mark(l, 4));
+    if (attend_ranges_eligible(c, a->k)) {
+      // union formed inside the attention kernel, per token range
+      BPKV_TRY(mark(l, 5));
+      BPKV_TRY(cuda_status(launch_attend_ranges(c, q, idx, a->k, part, tickets, out, st)));
+      BPKV_TRY(mark(l, 6));
+      continue;
+    }
     BPKV_TRY(cuda_status(launch_union(c, idx, a->k, uidx, umask, ucount, st)));
     BPKV_TRY(mark(l, 5));
     BPKV_TRY(cuda_status(launch_attend(c, q, uidx, umask, ucount, (int32_t)(G * a->k), part, out, false, st)));

@@ -222,6 +222,384 @@ __global__ void __launch_bounds__(kD) k_attend_combine(AttnArgs a, float* out) {
   out[(int64_t)row * kD + d] = (L > 0.f) ? O / L : 0.f;
 }
 
+// ---------------------------------------------------------------------------
+// Decode-step attention straight from the per-head selections.  One CTA per
+// (token range, KV head, sequence): it binary-searches each head's ascending
+// index list for the tokens of its range, merges those pieces into the range's
+// union rows with head masks (ranks by binary search in the other pieces), and
+// attends in two phases: logits with one thread per row (a whole 128-channel
+// dot product per thread, no shuffles), then V accumulation with one thread per
+// channel.  The partial (max, sum, output) of every head goes to the
+// workspace; the last CTA of the unit to finish (ticket counter, zeroed by the
+// depth kernel earlier in the step) merges them by log-sum-exp and resets it.
+constexpr int kRangeThreads = 128;
+constexpr int kRangeMaxEnt = 4096;    // selected (token, head) entries in one range (<= G k)
+constexpr int kRangeMaxRows = 2048;   // union rows of one range (<= min(range tokens, G k))
+constexpr int kRangeMaxRanges = 16;   // ranges per unit
+
+struct RangeArgs {
+  const uint16_t* k_rows;
+  const uint16_t* v_rows;
+  const int64_t* seq_len;
+  const float* q;
+  const int32_t* idx;     // [N][H][G][k], ascending, -1 padded
+  int32_t k;
+  int64_t cap;
+  int32_t n_heads, group;
+  int64_t range_tok;      // tokens per range
+  int32_t n_ranges;
+  float* part;            // [N][H][n_ranges][G][D + 2]
+  uint32_t* tickets;      // [N][H], zero on entry
+  float* out;             // [N][H][G][D]
+};
+
+struct RangeSmem {
+  int32_t sub[kRangeMaxEnt];           // the heads' pieces of their lists, one after another
+  int32_t rows[kRangeMaxEnt];
+  uint8_t rmask[kRangeMaxEnt];
+  float logit[kRangeMaxRows][BPKV_MAX_GROUP];
+  float q[BPKV_MAX_GROUP][kD];
+  int sa[BPKV_MAX_GROUP], sn[BPKV_MAX_GROUP], soff[BPKV_MAX_GROUP];
+  float red[BPKV_MAX_GROUP][kRangeThreads / 32];
+  float m[BPKV_MAX_GROUP], l[BPKV_MAX_GROUP];
+  uint32_t n_rows, is_last;
+};
+
+__device__ __forceinline__ int valid_count(const int32_t* v, int k) {
+  int lo = 0, hi = k;  // entries >= 0 come first
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (v[mid] >= 0) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ int lower_bound_g(const int32_t* v, int n, int64_t x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if ((int64_t)v[mid] < x) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(kRangeThreads) k_attend_ranges(RangeArgs a) {
+  pdl_enter();
+  extern __shared__ __align__(16) unsigned char range_raw[];
+  RangeSmem& S = *reinterpret_cast<RangeSmem*>(range_raw);
+  const int rg = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+  const int64_t unit = (int64_t)s * a.n_heads + h;
+  const int G = a.group;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t n = a.seq_len[s];
+  const int64_t t0 = (int64_t)rg * a.range_tok, t1 = min64(t0 + a.range_tok, n);
+  const int32_t* li = a.idx + unit * G * a.k;
+  const float qscale = 0.08838834764831845f * 1.4426950408889634f;
+
+  for (int e = tid; e < G * kD; e += kRangeThreads) S.q[e / kD][e % kD] = a.q[unit * G * kD + e] * qscale;
+  // the heads' lists, staged with one coalesced pass (rows[] is free until the merge)
+  int32_t* lst = S.rows;
+  for (int e = tid; e < G * a.k; e += kRangeThreads) lst[e] = li[e];
+  __syncthreads();
+  if (tid < G) {
+    const int32_t* lg = lst + tid * a.k;
+    const int cnt = valid_count(lg, a.k);
+    const int lo = t0 < t1 ? lower_bound_g(lg, cnt, t0) : 0;
+    const int hi = t0 < t1 ? lower_bound_g(lg, cnt, t1) : 0;
+    S.sa[tid] = lo;
+    S.sn[tid] = hi - lo;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int off = 0;
+    for (int g = 0; g < G; ++g) {
+      S.soff[g] = off;
+      off += S.sn[g];
+    }
+    S.n_rows = (uint32_t)off;  // entries before merging
+  }
+  __syncthreads();
+  const int n_ent = (int)S.n_rows;
+  for (int g = 0; g < G; ++g)
+    for (int i = tid; i < S.sn[g]; i += kRangeThreads) S.sub[S.soff[g] + i] = lst[g * a.k + S.sa[g] + i];
+  __syncthreads();
+  // merge rank of every entry; duplicates (same token, several heads) are ordered by head
+  for (int e = tid; e < n_ent; e += kRangeThreads) {
+    int g = 0;
+    while (g + 1 < G && S.soff[g + 1] <= e) ++g;
+    const int32_t x = S.sub[e];
+    int pos = e - S.soff[g];
+    for (int g2 = 0; g2 < G; ++g2) {
+      if (g2 == g) continue;
+      const int32_t* v = S.sub + S.soff[g2];
+      const int nn = S.sn[g2];
+      int lo = 0, hi = nn;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (g2 < g ? v[mid] <= x : v[mid] < x) lo = mid + 1;
+        else hi = mid;
+      }
+      pos += lo;
+    }
+    S.rows[pos] = x;
+    S.rmask[pos] = (uint8_t)g;  // head of the entry for now
+  }
+  __syncthreads();
+  // collapse equal tokens: the first entry of each run keeps the OR of the heads
+  uint32_t first = 0, bits = 0;
+  int32_t tok = -1;
+  if (tid == 0) S.n_rows = 0;
+  __syncthreads();
+  for (int base = 0; base < n_ent; base += kRangeThreads) {
+    const int e = base + tid;
+    first = 0;
+    if (e < n_ent) {
+      tok = S.rows[e];
+      first = (e == 0 || S.rows[e - 1] != tok) ? 1u : 0u;
+      bits = 0;
+      if (first)
+        for (int j = e; j < n_ent && S.rows[j] == tok; ++j) bits |= 1u << S.rmask[j];
+    }
+    __syncthreads();
+    const uint32_t bal = __ballot_sync(0xffffffffu, first);
+    __shared__ uint32_t wcnt[kRangeThreads / 32];
+    if (lane == 0) wcnt[warp] = __popc(bal);
+    __syncthreads();
+    uint32_t off = S.n_rows;
+    for (int w = 0; w < warp; ++w) off += wcnt[w];
+    off += __popc(bal & ((1u << lane) - 1u));
+    uint32_t tile = 0;
+    for (int w = 0; w < kRangeThreads / 32; ++w) tile += wcnt[w];
+    __syncthreads();
+    if (first) {
+      S.rows[off] = tok;  // off <= e: writes land on entries already read
+      S.rmask[off] = (uint8_t)bits;
+    }
+    if (tid == 0) S.n_rows += tile;
+    __syncthreads();
+  }
+  const int nrows = (int)S.n_rows;
+
+  const uint16_t* kb = a.k_rows + unit * a.cap * kD;
+  const uint16_t* vb = a.v_rows + unit * a.cap * kD;
+  // phase 1: logits, four threads per row (32 channels each).  The loop bound
+  // is the same for every thread, so all lanes reach the shuffles.
+  const int n_items = nrows * 4;
+  for (int t0 = 0; t0 < n_items; t0 += kRangeThreads) {
+    const int t = t0 + tid;
+    const bool valid = t < n_items;
+    const int r = t >> 2, part4 = t & 3;
+    uint4 w[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) w[c] = make_uint4(0u, 0u, 0u, 0u);
+    if (valid) {
+      const uint4* kr = reinterpret_cast<const uint4*>(kb + (int64_t)S.rows[r] * kD + part4 * 32);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) w[c] = kr[c];
+    }
+    float acc[BPKV_MAX_GROUP];
+#pragma unroll
+    for (int g = 0; g < BPKV_MAX_GROUP; ++g) acc[g] = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t wv[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float lo = __uint_as_float(wv[e] << 16), hi = __uint_as_float(wv[e] & 0xffff0000u);
+        const int ch = part4 * 32 + c * 8 + 2 * e;
+#pragma unroll
+        for (int g = 0; g < BPKV_MAX_GROUP; ++g) {
+          if (g >= G) break;
+          acc[g] = fmaf(S.q[g][ch], lo, acc[g]);
+          acc[g] = fmaf(S.q[g][ch + 1], hi, acc[g]);
+        }
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < BPKV_MAX_GROUP; ++g) {
+      acc[g] += __shfl_xor_sync(0xffffffffu, acc[g], 1);
+      acc[g] += __shfl_xor_sync(0xffffffffu, acc[g], 2);
+    }
+    if (valid && part4 == 0) {
+      const uint32_t mk = S.rmask[r];
+#pragma unroll
+      for (int g = 0; g < BPKV_MAX_GROUP; ++g)
+        if (g < G) S.logit[r][g] = ((mk >> g) & 1u) ? acc[g] : -INFINITY;
+    }
+  }
+  __syncthreads();
+  // phase 2: per-head max and sum
+  for (int g = 0; g < G; ++g) {
+    float mx = -INFINITY;
+    for (int r = tid; r < nrows; r += kRangeThreads) mx = fmaxf(mx, S.logit[r][g]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) S.red[g][warp] = mx;
+  }
+  __syncthreads();
+  if (tid < G) {
+    float mx = S.red[tid][0];
+    for (int w = 1; w < kRangeThreads / 32; ++w) mx = fmaxf(mx, S.red[tid][w]);
+    S.m[tid] = mx;
+  }
+  __syncthreads();
+  for (int g = 0; g < G; ++g) {
+    float sum = 0.f;
+    const float mg = S.m[g];
+    for (int r = tid; r < nrows; r += kRangeThreads) {
+      const float p = (S.logit[r][g] == -INFINITY) ? 0.f : exp2f(S.logit[r][g] - mg);
+      S.logit[r][g] = p;
+      sum += p;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) S.red[g][warp] = sum;
+  }
+  __syncthreads();
+  if (tid < G) {
+    float sum = 0.f;
+    for (int w = 0; w < kRangeThreads / 32; ++w) sum += S.red[tid][w];
+    S.l[tid] = sum;
+  }
+  __syncthreads();
+  // phase 3: V accumulation: thread = (row slot rs of 4, channels 4 c4 .. 4 c4 + 3),
+  // rows rs, rs + 4, ... with eight 8-byte loads in flight; slots merged in order
+  {
+    const int rs = tid >> 5, c4 = tid & 31;
+    float o[BPKV_MAX_GROUP][4];
+#pragma unroll
+    for (int g = 0; g < BPKV_MAX_GROUP; ++g)
+#pragma unroll
+      for (int d = 0; d < 4; ++d) o[g][d] = 0.f;
+    for (int r0 = rs; r0 < nrows; r0 += 4 * 8) {
+      uint2 vw[8];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        const int r = r0 + 4 * b;
+        vw[b] = r < nrows ? *reinterpret_cast<const uint2*>(vb + (int64_t)S.rows[r] * kD + 4 * c4)
+                          : make_uint2(0u, 0u);
+      }
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        const int r = r0 + 4 * b;
+        if (r >= nrows) break;
+        const float vf[4] = {__uint_as_float(vw[b].x << 16), __uint_as_float(vw[b].x & 0xffff0000u),
+                             __uint_as_float(vw[b].y << 16), __uint_as_float(vw[b].y & 0xffff0000u)};
+#pragma unroll
+        for (int g = 0; g < BPKV_MAX_GROUP; ++g) {
+          if (g >= G) break;
+          const float p = S.logit[r][g];
+#pragma unroll
+          for (int d = 0; d < 4; ++d) o[g][d] = fmaf(p, vf[d], o[g][d]);
+        }
+      }
+    }
+    // merge the four row slots in order through shared memory: the upper half of
+    // the logit buffer is free once every weight has been used
+    __syncthreads();
+    float* acc = &S.logit[kRangeMaxRows / 2][0];  // [slot][head][128]: 4 * 8 * 128 floats
+#pragma unroll
+    for (int g = 0; g < BPKV_MAX_GROUP; ++g) {
+      if (g >= G) break;
+#pragma unroll
+      for (int d = 0; d < 4; ++d) acc[(rs * BPKV_MAX_GROUP + g) * kD + 4 * c4 + d] = o[g][d];
+    }
+    __syncthreads();
+    const int d = tid;
+    float* pp = a.part + ((unit * a.n_ranges + rg) * G) * kPartStride;
+    for (int g = 0; g < G; ++g) {
+      float v = 0.f;
+#pragma unroll
+      for (int r4 = 0; r4 < 4; ++r4) v += acc[(r4 * BPKV_MAX_GROUP + g) * kD + d];
+      pp[g * kPartStride + d] = v;
+      if (d == 0) {
+        pp[g * kPartStride + kD] = S.m[g];
+        pp[g * kPartStride + kD + 1] = S.l[g];
+      }
+    }
+  }
+  // ticket: the last CTA of the unit merges every range's partial
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) S.is_last = (atomicAdd(&a.tickets[unit], 1u) == (uint32_t)(a.n_ranges - 1)) ? 1u : 0u;
+  __syncthreads();
+  if (!S.is_last) return;
+  __threadfence();
+  const float* pu = a.part + unit * a.n_ranges * G * kPartStride;
+  // every range's (max, sum) at once, then weights, then the outputs with
+  // eight independent loads in flight per thread
+  float* wgt = &S.logit[0][0];  // [n_ranges][G] weights (the logits are no longer needed)
+  for (int e = tid; e < a.n_ranges * G; e += kRangeThreads) {
+    const float lc = __ldcg(pu + e * kPartStride + kD + 1);
+    wgt[e] = lc > 0.f ? __ldcg(pu + e * kPartStride + kD) : -INFINITY;
+  }
+  __syncthreads();
+  if (tid < G) {
+    float M = -INFINITY;
+    for (int c = 0; c < a.n_ranges; ++c) M = fmaxf(M, wgt[c * G + tid]);
+    S.m[tid] = M;
+  }
+  __syncthreads();
+  for (int e = tid; e < a.n_ranges * G; e += kRangeThreads) {
+    const float mc = wgt[e];
+    wgt[e] = (mc == -INFINITY) ? 0.f : exp2f(mc - S.m[e % G]);
+  }
+  __syncthreads();
+  if (tid < G) {
+    float L = 0.f;
+    for (int c = 0; c < a.n_ranges; ++c) L += wgt[c * G + tid] * __ldcg(pu + (c * G + tid) * kPartStride + kD + 1);
+    S.l[tid] = L;
+  }
+  __syncthreads();
+  for (int g = 0; g < G; ++g) {
+    float O = 0.f;
+    int c = 0;
+    for (; c + 8 <= a.n_ranges; c += 8) {
+      float ov[8];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) ov[b] = __ldcg(pu + ((c + b) * G + g) * kPartStride + tid);
+#pragma unroll
+      for (int b = 0; b < 8; ++b) O = fmaf(wgt[(c + b) * G + g], ov[b], O);
+    }
+    for (; c < a.n_ranges; ++c) O = fmaf(wgt[c * G + g], __ldcg(pu + (c * G + g) * kPartStride + tid), O);
+    a.out[(unit * G + g) * kD + tid] = (S.l[g] > 0.f) ? O / S.l[g] : 0.f;
+  }
+  if (tid == 0) a.tickets[unit] = 0u;
+}
+
+// Tokens per range: at least 512, at most kRangeMaxRanges ranges per unit.
+int64_t range_tokens(int64_t n_max) {
+  int64_t rt = (n_max + kRangeMaxRanges - 1) / kRangeMaxRanges;
+  rt = (rt + 63) / 64 * 64;
+  return rt < 512 ? 512 : rt;
+}
+
+size_t attend_ranges_part_bytes(const bpkv_cache& c) {
+  return (size_t)c.n_seq * c.n_kv_heads * kRangeMaxRanges * c.group * kPartStride * sizeof(float);
+}
+
+// The range kernel needs every range's entries and union rows to fit its buffers.
+bool attend_ranges_eligible(const bpkv_cache& c, int32_t k) {
+  const int64_t ent = (int64_t)c.group * k;
+  const int64_t rows = min64(range_tokens(c.n_max), ent);
+  return ent <= kRangeMaxEnt && rows <= kRangeMaxRows;
+}
+
+cudaError_t launch_attend_ranges(const bpkv_cache& c, const float* q, const int32_t* idx, int32_t k, float* part,
+                                 uint32_t* tickets, float* out, cudaStream_t st) {
+  const int64_t rt = range_tokens(c.n_max);
+  const int32_t nr = (int32_t)((c.n_max + rt - 1) / rt);
+  if (nr == 0) return cudaSuccess;
+  RangeArgs a{c.k_rows, c.v_rows, c.seq_len, q, idx, k, c.cap_tokens, c.n_kv_heads, c.group, rt, nr, part, tickets,
+              out};
+  const int smem = (int)sizeof(RangeSmem);
+  cudaError_t e = cudaFuncSetAttribute(k_attend_ranges, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_attend_ranges, dim3(nr, c.n_kv_heads, c.n_seq), dim3(kRangeThreads), (size_t)smem, st, a);
+}
+
 int attend_chunks(int64_t rows, bool dense) {
   const int rpc = dense ? kDenseRows : kSparseRows;
   return (int)((rows + rpc - 1) / rpc);

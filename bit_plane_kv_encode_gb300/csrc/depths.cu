@@ -19,6 +19,7 @@ struct DepthArgs {
   uint8_t* depths;
   int32_t n_heads;
   int32_t group;
+  uint32_t* tickets;  // optional [N][H]: zeroed for the attention of this step
 };
 
 __global__ void __launch_bounds__(256) k_alloc_depths(DepthArgs a) {
@@ -26,28 +27,30 @@ __global__ void __launch_bounds__(256) k_alloc_depths(DepthArgs a) {
   __shared__ DepthSmem S;
   const int unit = blockIdx.x;
   const int s = unit / a.n_heads;
+  if (a.tickets && threadIdx.x == 0) a.tickets[unit] = 0u;
   alloc_depths_cta(S, a.q + (int64_t)unit * a.group * kD, a.sigma2 + (int64_t)unit * kD, a.group, a.budget_q[s],
                    a.depths + (int64_t)unit * kD);
 }
 
 __global__ void __launch_bounds__(128) k_fixed_depths(const float* q, uint8_t* depths, int group, int n_channels,
-                                                      int t) {
+                                                      int t, uint32_t* tickets) {
   pdl_enter();
   __shared__ DepthSmem S;
   const int unit = blockIdx.x;
+  if (tickets && threadIdx.x == 0) tickets[unit] = 0u;
   fixed_depths_cta(S, q + (int64_t)unit * group * kD, group, n_channels, t, depths + (int64_t)unit * kD);
 }
 
 cudaError_t launch_alloc_depths(const bpkv_cache& c, const float* q, const float* sigma2, const int32_t* budget_q,
-                                uint8_t* depths, cudaStream_t st) {
-  DepthArgs a{q, sigma2, budget_q, depths, c.n_kv_heads, c.group};
+                                uint8_t* depths, cudaStream_t st, uint32_t* tickets) {
+  DepthArgs a{q, sigma2, budget_q, depths, c.n_kv_heads, c.group, tickets};
   return launch_pdl(k_alloc_depths, dim3(c.n_seq * c.n_kv_heads), dim3(256), 0, st, a);
 }
 
 cudaError_t launch_fixed_depths(const bpkv_cache& c, const float* q, int32_t n_channels, int32_t depth,
-                                uint8_t* depths, cudaStream_t st) {
+                                uint8_t* depths, cudaStream_t st, uint32_t* tickets) {
   return launch_pdl(k_fixed_depths, dim3(c.n_seq * c.n_kv_heads), dim3(128), 0, st, q, depths, (int)c.group,
-                    (int)n_channels, (int)depth);
+                    (int)n_channels, (int)depth, tickets);
 }
 
 }  // namespace bpkv

@@ -213,6 +213,8 @@ __global__ void __launch_bounds__(kSelThreads) k_topk(TopkArgs a) {
     // locates the bucket holding the rem-th largest active key; a crowded
     // bucket becomes the next active range (its exact min and max keys).
     uint32_t rem = (uint32_t)n_top, b_lo = klo, b_hi = khi, bucket_n = 0;
+    int tb_final = -1;
+    float scale_final = 0.f;
     for (int lvl = 0; lvl < 3; ++lvl) {
       const float scale = (float)kHistBins / ((float)(khi - klo) + 1.f);
       auto bin_of = [&](uint32_t k) { return min((int)((float)(k - klo) * scale), kHistBins - 1); };
@@ -236,7 +238,13 @@ __global__ void __launch_bounds__(kSelThreads) k_topk(TopkArgs a) {
       const int tb = (int)S.tb;
       rem = S.rem;
       bucket_n = S.hist[tb];
-      // exact key range of the bucket
+      if (bucket_n <= (uint32_t)kCandCap) {
+        // small bucket: keys are classified by their bin under this level's map
+        tb_final = tb;
+        scale_final = scale;
+        break;
+      }
+      // crowded bucket: its exact key range becomes the next level's range
       uint32_t blo = 0xFFFFFFFFu, bhi = 0u;
       for_keys(S, staged, sc, lo, cnt, [&](int64_t, uint32_t k) {
         if (k >= klo && k <= khi && bin_of(k) == tb) {
@@ -247,16 +255,23 @@ __global__ void __launch_bounds__(kSelThreads) k_topk(TopkArgs a) {
       block_range(blo, bhi, S);
       b_lo = blo;
       b_hi = bhi;
-      if (bucket_n <= (uint32_t)kCandCap || b_lo == b_hi) break;
+      if (b_lo == b_hi) break;
       klo = b_lo;
       khi = b_hi;
     }
-    if (bucket_n <= (uint32_t)kCandCap) {
-      // keys above the bucket are selected; the bucket's keys are sorted exactly
+    if (tb_final >= 0) {
+      // keys in higher bins are selected; the bucket's keys are ranked exactly
+      const uint32_t klo_f = klo, khi_f = khi;
+      auto bin_f = [&](uint32_t k) { return min((int)((float)(k - klo_f) * scale_final), kHistBins - 1); };
       for_keys(S, staged, sc, lo, cnt, [&](int64_t e, uint32_t k) {
-        if (k > b_hi) {
+        if (k < klo_f || k > khi_f) {
+          if (k > khi_f) sel_push(S, (int32_t)(lo + e));
+          return;
+        }
+        const int b = bin_f(k);
+        if (b > tb_final) {
           sel_push(S, (int32_t)(lo + e));
-        } else if (k >= b_lo) {
+        } else if (b == tb_final) {
           const uint32_t c = atomicAdd(&S.n_cand, 1u);
           if (c < (uint32_t)kCandCap)
             S.cand[c] = ((unsigned long long)k << 32) | (0xFFFFFFFFu - (uint32_t)(lo + e));
@@ -264,12 +279,22 @@ __global__ void __launch_bounds__(kSelThreads) k_topk(TopkArgs a) {
       });
       __syncthreads();
       const int nc = (int)min(S.n_cand, (uint32_t)kCandCap);
-      const int nc2 = pow2_at_least(max(nc, 2));
-      for (int e = nc + tid; e < nc2; e += kSelThreads) S.cand[e] = 0ull;
-      __syncthreads();
-      block_bitonic(S.cand, nc2, true);
-      for (int e = tid; e < (int)rem && e < nc; e += kSelThreads)
-        sel_push(S, (int32_t)(0xFFFFFFFFu - (uint32_t)S.cand[e]));
+      if (nc <= kSelThreads) {
+        // rank of each candidate among the bucket (distinct entries): no barriers
+        if (tid < nc) {
+          const unsigned long long mine = S.cand[tid];
+          int rank = 0;
+          for (int j = 0; j < nc; ++j) rank += S.cand[j] > mine;
+          if (rank < (int)rem) sel_push(S, (int32_t)(0xFFFFFFFFu - (uint32_t)mine));
+        }
+      } else {
+        const int nc2 = pow2_at_least(nc);
+        for (int e = nc + tid; e < nc2; e += kSelThreads) S.cand[e] = 0ull;
+        __syncthreads();
+        block_bitonic(S.cand, nc2, true);
+        for (int e = tid; e < (int)rem && e < nc; e += kSelThreads)
+          sel_push(S, (int32_t)(0xFFFFFFFFu - (uint32_t)S.cand[e]));
+      }
     } else {
       // more than kCandCap keys equal the threshold key (b_lo == b_hi): take
       // the rem of them with the lowest indices by an ordered scan
@@ -293,6 +318,17 @@ __global__ void __launch_bounds__(kSelThreads) k_topk(TopkArgs a) {
   const int ns = (int)S.n_sel;
   if (ns > a.k && tid == 0) set_status(a.status, BPKV_DEV_SELECT);
   const int cnt_out = min(ns, a.k);
+  if (cnt_out <= kSelThreads) {
+    // ascending order by rank (the indices are distinct): no barriers
+    if (tid < cnt_out) {
+      const int32_t mine = S.sel[tid];
+      int rank = 0;
+      for (int j = 0; j < cnt_out; ++j) rank += S.sel[j] < mine;
+      out[rank] = mine;
+    }
+    for (int e = cnt_out + tid; e < a.k; e += kSelThreads) out[e] = -1;
+    return;
+  }
   const int n2 = pow2_at_least(max(cnt_out, 2));
   for (int e = cnt_out + tid; e < n2; e += kSelThreads) S.sel[e] = 0x7FFFFFFF;
   __syncthreads();
