@@ -8,15 +8,17 @@ namespace bpkv {
 cudaError_t launch_encode_append(const bpkv_cache& c, const uint16_t* k_new, const uint16_t* v_new, int32_t t_new,
                                  cudaStream_t st);
 cudaError_t launch_alloc_depths(const bpkv_cache& c, const float* q, const float* sigma2, const int32_t* budget_q,
-                                uint8_t* depths, cudaStream_t st, uint32_t* tickets = nullptr);
+                                uint8_t* depths, cudaStream_t st, uint32_t* tickets = nullptr,
+                                void* plan = nullptr);
 cudaError_t launch_fixed_depths(const bpkv_cache& c, const float* q, int32_t n_channels, int32_t depth,
-                                uint8_t* depths, cudaStream_t st, uint32_t* tickets = nullptr);
+                                uint8_t* depths, cudaStream_t st, uint32_t* tickets = nullptr, void* plan = nullptr);
+size_t scan_plan_bytes(int group);
 size_t attend_ranges_part_bytes(const bpkv_cache& c);
 bool attend_ranges_eligible(const bpkv_cache& c, int32_t k);
 cudaError_t launch_attend_ranges(const bpkv_cache& c, const float* q, const int32_t* idx, int32_t k, float* part,
                                  uint32_t* tickets, float* out, cudaStream_t st);
 cudaError_t launch_scan(const bpkv_cache& c, const float* q, const uint8_t* depths, float* scores, int64_t ld,
-                        cudaStream_t st);
+                        cudaStream_t st, const void* plan = nullptr);
 cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
                         int32_t n_recent, int32_t* idx, int32_t* status, cudaStream_t st);
 cudaError_t launch_union(const bpkv_cache& c, const int32_t* idx, int32_t k, int32_t* uidx, uint8_t* umask,
@@ -74,7 +76,8 @@ int check_k(int32_t k, int32_t n_sink, int32_t n_recent) {
 
 // Workspace layout: status word, then the buffers each call family needs.
 struct Layout {
-  size_t scores = 0, part = 0, depths = 0, idx = 0, uidx = 0, umask = 0, ucount = 0, tickets = 0, total = 0;
+  size_t scores = 0, part = 0, depths = 0, idx = 0, uidx = 0, umask = 0, ucount = 0, tickets = 0, plan = 0,
+         total = 0;
 };
 
 Layout layout(const bpkv_cache& c, int32_t k, int32_t what) {
@@ -112,6 +115,8 @@ Layout layout(const bpkv_cache& c, int32_t k, int32_t what) {
     off = align_up(off + NH * sizeof(int32_t));
     L.tickets = off;
     off = align_up(off + NH * sizeof(uint32_t));
+    L.plan = off;
+    off = align_up(off + NH * scan_plan_bytes(c.group));
   }
   L.total = off;
   return L;
@@ -329,15 +334,17 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
     uint8_t* umask = at(ws, L.umask);
     int32_t* ucount = reinterpret_cast<int32_t*>(at(ws, L.ucount));
     uint32_t* tickets = reinterpret_cast<uint32_t*>(at(ws, L.tickets));
+    void* plan = at(ws, L.plan);
     BPKV_TRY(mark(l, 1));
     if (a->depth_rule == BPKV_DEPTH_WATERFILL) {
       BPKV_TRY(cuda_status(
-          launch_alloc_depths(c, q, a->sigma2 + (size_t)l * NH * kD, a->budget_q, depths, st, tickets)));
+          launch_alloc_depths(c, q, a->sigma2 + (size_t)l * NH * kD, a->budget_q, depths, st, tickets, plan)));
     } else {
-      BPKV_TRY(cuda_status(launch_fixed_depths(c, q, a->fixed_channels, a->fixed_depth, depths, st, tickets)));
+      BPKV_TRY(
+          cuda_status(launch_fixed_depths(c, q, a->fixed_channels, a->fixed_depth, depths, st, tickets, plan)));
     }
     BPKV_TRY(mark(l, 2));
-    BPKV_TRY(cuda_status(launch_scan(c, q, depths, scores, c.cap_tokens, st)));
+    BPKV_TRY(cuda_status(launch_scan(c, q, depths, scores, c.cap_tokens, st, plan)));
     BPKV_TRY(mark(l, 3));
     if ((a->flags & BPKV_STEP_TAIL) && tail_eligible(c, a->k, a->n_sink, a->n_recent)) {
       int32_t* iout = a->idx_out ? a->idx_out + (size_t)l * NH * G * a->k : nullptr;

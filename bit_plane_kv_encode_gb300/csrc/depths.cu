@@ -8,7 +8,14 @@
 // (5 for a channel's first bit: 4 for the plane + 1 for its fp16 scale; 4 after)
 // and the items before the first one that does not fit, or is worthless, are
 // taken.  This is the greedy heap's result computed as a single water level.
+//
+// In a decode step the same CTA also builds the unit's scan plan (channel
+// groups, plane rows, weights q 2^(4-t-pos)) once, so that every scan CTA of
+// the unit copies it instead of deriving it again from the depths.
 #include "depths_core.cuh"
+#include "scan_core.cuh"
+
+#include <type_traits>
 
 namespace bpkv {
 
@@ -20,37 +27,85 @@ struct DepthArgs {
   int32_t n_heads;
   int32_t group;
   uint32_t* tickets;  // optional [N][H]: zeroed for the attention of this step
+  void* plan;         // optional [N][H] ScanPlan<GP>
+  int32_t n_channels; // fixed sets only
+  int32_t depth;      // fixed sets only
 };
 
-__global__ void __launch_bounds__(256) k_alloc_depths(DepthArgs a) {
+// Build the scan plan of this unit from the depths the CTA just wrote (each
+// thread j < D reads back its own depth) and store it.
+template <int GP>
+__device__ void emit_plan(const DepthArgs& a, int64_t unit, const uint8_t* dep) {
+  __shared__ ScanPlan<GP> P;
+  __shared__ PlanScratch X;
+  const int tid = threadIdx.x;
+  int t = 0;
+  float qv[GP];
+  if (tid < kD) {
+    t = dep[tid];
+    const float* qp = a.q + unit * a.group * kD;
+#pragma unroll
+    for (int hh = 0; hh < GP; ++hh) qv[hh] = hh < a.group ? qp[hh * kD + tid] : 0.f;
+  }
+  scan_setup<GP>(P, X, t, qv);
+  scan_store_plan<GP>(P, reinterpret_cast<ScanPlan<GP>*>(a.plan) + unit);
+}
+
+template <int GP>
+__global__ void __launch_bounds__(kScanThreads) k_alloc_depths(DepthArgs a) {
   pdl_enter();
   __shared__ DepthSmem S;
   const int unit = blockIdx.x;
   const int s = unit / a.n_heads;
   if (a.tickets && threadIdx.x == 0) a.tickets[unit] = 0u;
+  uint8_t* dep = a.depths + (int64_t)unit * kD;
   alloc_depths_cta(S, a.q + (int64_t)unit * a.group * kD, a.sigma2 + (int64_t)unit * kD, a.group, a.budget_q[s],
-                   a.depths + (int64_t)unit * kD);
+                   dep);
+  if (a.plan) emit_plan<GP>(a, unit, dep);
 }
 
-__global__ void __launch_bounds__(128) k_fixed_depths(const float* q, uint8_t* depths, int group, int n_channels,
-                                                      int t, uint32_t* tickets) {
+template <int GP>
+__global__ void __launch_bounds__(kScanThreads) k_fixed_depths(DepthArgs a) {
   pdl_enter();
   __shared__ DepthSmem S;
   const int unit = blockIdx.x;
-  if (tickets && threadIdx.x == 0) tickets[unit] = 0u;
-  fixed_depths_cta(S, q + (int64_t)unit * group * kD, group, n_channels, t, depths + (int64_t)unit * kD);
+  if (a.tickets && threadIdx.x == 0) a.tickets[unit] = 0u;
+  uint8_t* dep = a.depths + (int64_t)unit * kD;
+  fixed_depths_cta(S, a.q + (int64_t)unit * a.group * kD, a.group, a.n_channels, a.depth, dep);
+  if (a.plan) emit_plan<GP>(a, unit, dep);
+}
+
+template <typename F>
+cudaError_t launch_depths_gp(int group, F&& launch) {
+  if (group <= 1) return launch(std::integral_constant<int, 1>{});
+  if (group <= 2) return launch(std::integral_constant<int, 2>{});
+  if (group <= 4) return launch(std::integral_constant<int, 4>{});
+  return launch(std::integral_constant<int, 8>{});
+}
+
+size_t scan_plan_bytes(int group) {
+  if (group <= 1) return sizeof(ScanPlan<1>);
+  if (group <= 2) return sizeof(ScanPlan<2>);
+  if (group <= 4) return sizeof(ScanPlan<4>);
+  return sizeof(ScanPlan<8>);
 }
 
 cudaError_t launch_alloc_depths(const bpkv_cache& c, const float* q, const float* sigma2, const int32_t* budget_q,
-                                uint8_t* depths, cudaStream_t st, uint32_t* tickets) {
-  DepthArgs a{q, sigma2, budget_q, depths, c.n_kv_heads, c.group, tickets};
-  return launch_pdl(k_alloc_depths, dim3(c.n_seq * c.n_kv_heads), dim3(256), 0, st, a);
+                                uint8_t* depths, cudaStream_t st, uint32_t* tickets, void* plan) {
+  DepthArgs a{q, sigma2, budget_q, depths, c.n_kv_heads, c.group, tickets, plan, 0, 0};
+  return launch_depths_gp(c.group, [&](auto gp) {
+    return launch_pdl(k_alloc_depths<decltype(gp)::value>, dim3(c.n_seq * c.n_kv_heads), dim3(kScanThreads), 0, st,
+                      a);
+  });
 }
 
 cudaError_t launch_fixed_depths(const bpkv_cache& c, const float* q, int32_t n_channels, int32_t depth,
-                                uint8_t* depths, cudaStream_t st, uint32_t* tickets) {
-  return launch_pdl(k_fixed_depths, dim3(c.n_seq * c.n_kv_heads), dim3(128), 0, st, q, depths, (int)c.group,
-                    (int)n_channels, (int)depth, tickets);
+                                uint8_t* depths, cudaStream_t st, uint32_t* tickets, void* plan) {
+  DepthArgs a{q, nullptr, nullptr, depths, c.n_kv_heads, c.group, tickets, plan, n_channels, depth};
+  return launch_depths_gp(c.group, [&](auto gp) {
+    return launch_pdl(k_fixed_depths<decltype(gp)::value>, dim3(c.n_seq * c.n_kv_heads), dim3(kScanThreads), 0, st,
+                      a);
+  });
 }
 
 }  // namespace bpkv

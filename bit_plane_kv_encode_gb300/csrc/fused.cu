@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(kFuseThreads) k_decode_fused(FusedArgs a) {
 #pragma unroll
       for (int hh = 0; hh < GP; ++hh) qv[hh] = hh < G ? qp[hh * kD + tid] : 0.f;
     }
-    scan_setup<GP>(S.x.scan, t, qv);
+    scan_setup<GP>(S.x.scan.P, S.x.scan.X, t, qv);
     const int64_t b_begin = t_begin / kBlock;
     for (int c0 = 0; c0 * kBlock < n_own; c0 += kScanBlocks) {
       const int nbl = (int)min64(kScanBlocks, (n_own - (int64_t)c0 * kBlock + kBlock - 1) / kBlock);

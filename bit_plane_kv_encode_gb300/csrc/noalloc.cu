@@ -15,7 +15,7 @@
 
 namespace bpkv {
 cudaError_t launch_scan(const bpkv_cache& c, const float* q, const uint8_t* depths, float* scores, int64_t ld,
-                        cudaStream_t st);
+                        cudaStream_t st, const void* plan = nullptr);
 cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
                         int32_t n_recent, int32_t* idx, int32_t* status, cudaStream_t st);
 }  // namespace bpkv

@@ -23,6 +23,7 @@
 namespace bpkv {
 
 struct ScanArgs {
+  const void* plan;          // optional per-unit ScanPlan<GP> built by the depth kernel
   const uint64_t* planes;
   const uint16_t* scales;
   const int64_t* seq_len;
@@ -49,15 +50,19 @@ __global__ void __launch_bounds__(kScanThreads) k_scan(ScanArgs a) {
   const int nbl = (int)min64(kScanBlocks, nb_valid - b0);
   const int tid = threadIdx.x;
   const int G = a.group;
-  int t = 0;
-  float qv[GP];
-  if (tid < kD) {
-    t = a.depths[unit * kD + tid];
-    const float* qp = a.q + unit * G * kD;
+  if (a.plan) {
+    scan_load_plan<GP>(S.P, reinterpret_cast<const ScanPlan<GP>*>(a.plan) + unit);
+  } else {
+    int t = 0;
+    float qv[GP];
+    if (tid < kD) {
+      t = a.depths[unit * kD + tid];
+      const float* qp = a.q + unit * G * kD;
 #pragma unroll
-    for (int hh = 0; hh < GP; ++hh) qv[hh] = hh < G ? qp[hh * kD + tid] : 0.f;
+      for (int hh = 0; hh < GP; ++hh) qv[hh] = hh < G ? qp[hh * kD + tid] : 0.f;
+    }
+    scan_setup<GP>(S.P, S.X, t, qv);
   }
-  scan_setup<GP>(S, t, qv);
   scan_stage<GP>(S, a.planes + unit * kD * kPlanes * a.nb_cap + b0, a.scales + unit * kD * a.nb_cap + b0, a.nb_cap,
                  nbl);
   scan_compute<GP>(S, nbl, G, a.scores + unit * G * a.ld + b0 * kBlock, a.ld, n - b0 * kBlock);
@@ -72,8 +77,9 @@ cudaError_t launch_scan_gp(const ScanArgs& a, dim3 grid, cudaStream_t st) {
 }
 
 cudaError_t launch_scan(const bpkv_cache& c, const float* q, const uint8_t* depths, float* scores, int64_t ld,
-                        cudaStream_t st) {
-  ScanArgs a{c.planes, c.scales, c.seq_len, q, depths, scores, ld, c.cap_tokens / kBlock, c.n_kv_heads, c.group};
+                        cudaStream_t st, const void* plan) {
+  ScanArgs a{plan, c.planes, c.scales, c.seq_len, q, depths, scores, ld, c.cap_tokens / kBlock, c.n_kv_heads,
+             c.group};
   const int64_t chunks = (c.n_max + kScanBlocks * kBlock - 1) / (kScanBlocks * kBlock);
   if (chunks == 0) return cudaSuccess;
   dim3 grid((unsigned)chunks, c.n_kv_heads, c.n_seq);

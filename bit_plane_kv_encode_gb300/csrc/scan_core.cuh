@@ -30,20 +30,32 @@ __host__ __device__ constexpr int field_pos(int t, int m) {
   return (m * t + t <= 22) ? m * t + 1 : m * t - 9;
 }
 
+// What a CTA needs to scan one unit, derived from its depth vector and query:
+// the channel groups, the plane row of every (group, lane), the channel and
+// group of every slot, and the weights w = q 2^(4 - t - pos).
+template <int GP>
+struct __align__(16) ScanPlan {
+  float w[kMaxSlots * GP];                          // [group slots][head][slot]
+  int16_t row_of_lane[kMaxGroups * 32];             // j * 4 + p, or -1
+  int16_t slot_ch[kMaxSlots];                       // channel of each slot, or -1
+  int8_t slot_grp[kMaxSlots];                       // group of each slot
+  int8_t grp_t[kMaxGroups];
+  int16_t grp_base[kMaxGroups];                     // first slot of each group
+  int8_t grp_cnt[kMaxGroups];                       // channels in each group
+  int n_groups, n_slots;
+};
+
+struct PlanScratch {
+  int cnt_t[5];
+  int warp_cnt[4][5];
+};
+
 template <int GP>
 struct ScanSmem {
   uint32_t words[kMaxGroups * 32 * kWordPitch];     // staged plane half-words
   float u[kScanBlocks * kMaxSlots * GP];            // [block][group slots][head][slot]
-  float w[kMaxSlots * GP];                          // q 2^(4 - t - pos), [group slots][head][slot]
-  float sc[kMaxSlots * kScanBlocks];                // block scales, [slot][block]
-  int16_t row_of_lane[kMaxGroups * 32];             // j * 4 + p, or -1
-  int16_t slot_ch[kMaxSlots];                       // channel of each slot, or -1
-  int8_t grp_t[kMaxGroups];
-  int16_t grp_base[kMaxGroups];                     // first slot of each group
-  int8_t grp_cnt[kMaxGroups];                       // channels in each group
-  int cnt_t[5];
-  int warp_cnt[4][5];
-  int n_groups, n_slots;
+  ScanPlan<GP> P;
+  PlanScratch X;
 };
 
 // 32 x 32 bit transpose across the warp: on return bit r of lane l's word is
@@ -141,7 +153,7 @@ __device__ __forceinline__ void transpose_consts(int lane, uint32_t (&keep)[5], 
 // Channel groups and per-query weights.  Threads 0..127 pass their channel's
 // depth t and q values; blockDim.x must be kScanThreads.
 template <int GP>
-__device__ void scan_setup(ScanSmem<GP>& S, int t, const float (&qv)[GP]) {
+__device__ void scan_setup(ScanPlan<GP>& S, PlanScratch& X, int t, const float (&qv)[GP]) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int rank = 0;
   if (tid < kD) {
@@ -149,18 +161,21 @@ __device__ void scan_setup(ScanSmem<GP>& S, int t, const float (&qv)[GP]) {
     for (int d = 1; d <= 4; ++d) {
       const uint32_t b = __ballot_sync(0xffffffffu, t == d);
       if (t == d) rank = __popc(b & ((1u << lane) - 1u));
-      if (lane == 0) S.warp_cnt[warp][d] = __popc(b);
+      if (lane == 0) X.warp_cnt[warp][d] = __popc(b);
     }
   }
   for (int e = tid; e < kMaxGroups * 32; e += kScanThreads) S.row_of_lane[e] = -1;
-  for (int e = tid; e < kMaxSlots; e += kScanThreads) S.slot_ch[e] = -1;
+  for (int e = tid; e < kMaxSlots; e += kScanThreads) {
+    S.slot_ch[e] = -1;
+    S.slot_grp[e] = 0;
+  }
   __syncthreads();
   if (tid == 0) {
     int g = 0, slot = 0;
     for (int d = 4; d >= 1; --d) {
       int c = 0;
-      for (int w = 0; w < 4; ++w) c += S.warp_cnt[w][d];
-      S.cnt_t[d] = c;
+      for (int w = 0; w < 4; ++w) c += X.warp_cnt[w][d];
+      X.cnt_t[d] = c;
       for (int first = 0; first < c; first += group_cap(d), ++g) {
         S.grp_t[g] = (int8_t)d;
         S.grp_base[g] = (int16_t)slot;
@@ -173,10 +188,10 @@ __device__ void scan_setup(ScanSmem<GP>& S, int t, const float (&qv)[GP]) {
   }
   __syncthreads();
   if (tid < kD && t > 0) {
-    for (int w = 0; w < warp; ++w) rank += S.warp_cnt[w][t];
+    for (int w = 0; w < warp; ++w) rank += X.warp_cnt[w][t];
     // group index: groups of deeper channels come first
     int g = 0;
-    for (int d = 4; d > t; --d) g += (S.cnt_t[d] + group_cap(d) - 1) / group_cap(d);
+    for (int d = 4; d > t; --d) g += (X.cnt_t[d] + group_cap(d) - 1) / group_cap(d);
     g += rank / group_cap(t);
     const int m = rank % group_cap(t);
     S.slot_ch[S.grp_base[g] + m] = (int16_t)tid;
@@ -188,14 +203,33 @@ __device__ void scan_setup(ScanSmem<GP>& S, int t, const float (&qv)[GP]) {
     for (int hh = 0; hh < GP; ++hh) S.w[base * GP + hh * P + m] = ldexpf(qv[hh], 4 - t - field_pos(t, m));
   }
   __syncthreads();
-  // unused slots of partial groups weigh 0
+  // unused slots of partial groups weigh 0; slot -> group map
   for (int g = 0; g < S.n_groups; ++g) {
     const int d = S.grp_t[g], P = slot_pitch(d), base = S.grp_base[g], cnt = S.grp_cnt[g];
     for (int e = tid; e < P * GP; e += kScanThreads) {
       if (e % P >= cnt) S.w[base * GP + e] = 0.f;
     }
+    for (int m = tid; m < P; m += kScanThreads) S.slot_grp[base + m] = (int8_t)g;
   }
   __syncthreads();
+}
+
+// Copy a plan built by scan_setup elsewhere (global memory) into shared memory.
+template <int GP>
+__device__ void scan_load_plan(ScanPlan<GP>& S, const ScanPlan<GP>* __restrict__ src) {
+  static_assert(sizeof(ScanPlan<GP>) % 16 == 0, "plan copied in 16-byte pieces");
+  const uint4* g = reinterpret_cast<const uint4*>(src);
+  uint4* d = reinterpret_cast<uint4*>(&S);
+  for (int e = threadIdx.x; e < (int)(sizeof(ScanPlan<GP>) / 16); e += blockDim.x) d[e] = g[e];
+  __syncthreads();
+}
+
+// Store the plan (shared memory) to global memory.
+template <int GP>
+__device__ void scan_store_plan(const ScanPlan<GP>& S, ScanPlan<GP>* __restrict__ dst) {
+  const uint4* s = reinterpret_cast<const uint4*>(&S);
+  uint4* g = reinterpret_cast<uint4*>(dst);
+  for (int e = threadIdx.x; e < (int)(sizeof(ScanPlan<GP>) / 16); e += blockDim.x) g[e] = s[e];
 }
 
 // Stage the plane words and scales of nbl (<= kScanBlocks) blocks starting at
@@ -204,11 +238,12 @@ template <int GP>
 __device__ void scan_stage(ScanSmem<GP>& S, const uint64_t* __restrict__ pl, const uint16_t* __restrict__ sp,
                            int64_t nb_cap, int nbl) {
   const int tid = threadIdx.x;
-  const int n_groups = S.n_groups, n_slots = S.n_slots;
+  const ScanPlan<GP>& P = S.P;
+  const int n_groups = P.n_groups, n_slots = P.n_slots;
   __syncthreads();  // the previous chunk's compute is done with words and u
   for (int e = tid; e < n_groups * 32 * kScanBlocks; e += kScanThreads) {
     const int r = e / kScanBlocks, lb = e % kScanBlocks;
-    const int row = S.row_of_lane[r];
+    const int row = P.row_of_lane[r];
     if (row >= 0 && lb < nbl) {
       const uint64_t w = pl[(int64_t)row * nb_cap + lb];
       S.words[r * kWordPitch + 2 * lb] = (uint32_t)w;
@@ -217,19 +252,13 @@ __device__ void scan_stage(ScanSmem<GP>& S, const uint64_t* __restrict__ pl, con
   }
   for (int e = tid; e < kScanBlocks * n_slots; e += kScanThreads) {
     const int lb = e % kScanBlocks, slot = e / kScanBlocks;
-    const int ch = S.slot_ch[slot];
-    S.sc[e] = (ch >= 0 && lb < nbl) ? fp16_bits_to_float(sp[(int64_t)ch * nb_cap + lb]) : 0.f;
-  }
-  __syncthreads();
-  for (int e = tid; e < kScanBlocks * n_slots; e += kScanThreads) {
-    const int lb = e % kScanBlocks, slot = e / kScanBlocks;
-    const float sc = S.sc[e];
-    int g = 0;
-    while (g + 1 < n_groups && S.grp_base[g + 1] <= slot) ++g;
-    const int base = S.grp_base[g], m = slot - base, P = slot_pitch(S.grp_t[g]);
+    const int ch = P.slot_ch[slot];
+    const float sc = (ch >= 0 && lb < nbl) ? fp16_bits_to_float(sp[(int64_t)ch * nb_cap + lb]) : 0.f;
+    const int g = P.slot_grp[slot];
+    const int base = P.grp_base[g], m = slot - base, pitch = slot_pitch(P.grp_t[g]);
     float* ud = S.u + (lb * n_slots + base) * GP;
 #pragma unroll
-    for (int hh = 0; hh < GP; ++hh) ud[hh * P + m] = sc * S.w[base * GP + hh * P + m];
+    for (int hh = 0; hh < GP; ++hh) ud[hh * pitch + m] = sc * P.w[base * GP + hh * pitch + m];
   }
   __syncthreads();
 }
@@ -245,14 +274,15 @@ __device__ void scan_compute(const ScanSmem<GP>& S, int nbl, int G, float* out, 
   unsigned long long acc0[GP], acc1[GP];
 #pragma unroll
   for (int hh = 0; hh < GP; ++hh) acc0[hh] = acc1[hh] = 0ull;
-  const int n_groups = S.n_groups, n_slots = S.n_slots;
+  const ScanPlan<GP>& P = S.P;
+  const int n_groups = P.n_groups, n_slots = P.n_slots;
   for (int g = 0; g < n_groups; ++g) {
-    const int d = S.grp_t[g], cnt = S.grp_cnt[g];
+    const int d = P.grp_t[g], cnt = P.grp_cnt[g];
     const uint32_t* wr = S.words + (g * 32 + lane) * kWordPitch + 2 * lb;
     const uint32_t x0 = warp_transpose32(wr[0], keep, rot);
     const uint32_t x1 = warp_transpose32(wr[1], keep, rot);
     const uint32_t xa0 = x0 << 1, xb0 = x0 >> 9, xa1 = x1 << 1, xb1 = x1 >> 9;
-    const float* ug = S.u + (lb * n_slots + S.grp_base[g]) * GP;
+    const float* ug = S.u + (lb * n_slots + P.grp_base[g]) * GP;
     switch (d) {
       case 4: group_fields<4, GP>(cnt, xa0, xb0, xa1, xb1, ug, acc0, acc1); break;
       case 3: group_fields<3, GP>(cnt, xa0, xb0, xa1, xb1, ug, acc0, acc1); break;
