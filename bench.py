@@ -149,7 +149,8 @@ def make_workload(cfg, steps: int, warmup: int, dev, step_flags: int = 0, budget
     from workload import gen_layer
 
     L, N, H, G, D, n = cfg.n_layers, cfg.n_seq, cfg.n_kv_heads, cfg.group, cfg.head_dim, cfg.n_tokens
-    cap = ((n + warmup + steps + 64 + 511) // 512) * 512
+    # room for every step the bench runs: warm-up, timed, breakdown, list and e2e steps
+    cap = ((n + warmup + 2 * steps + 128 + 511) // 512) * 512
     budgets = list(budgets or cfg.budgets)
     host = cfg.residency == "host"
     caches = {b: [] for b in budgets}
@@ -195,7 +196,11 @@ def make_workload(cfg, steps: int, warmup: int, dev, step_flags: int = 0, budget
         p["arr"] = pk.cache_array(caches[b])
         common = (io["k_new"].data_ptr(), io["v_new"].data_ptr(), io["q"].data_ptr(), io["sigma2"].data_ptr(),
                   p["budget_q"].data_ptr(), pk.DEPTH_WATERFILL, 0, 0, cfg.k, cfg.n_sink, cfg.n_recent,
-                  p["out"].data_ptr(), p["depths"].data_ptr(), p["idx"].data_ptr())
+                  p["out"].data_ptr(), p["depths"].data_ptr())
+        # timed steps write no index lists (the attention reads the selection cuts);
+        # one untimed step with lists afterwards gives the union sizes for the byte count
+        p["args_lists"] = pk.bpkv_step_args(*common, p["idx"].data_ptr(), None, step_flags)
+        common = common + (None,)
         # timed graph: no event nodes (each costs about 2 us inside a graph)
         p["args"] = pk.bpkv_step_args(*common, None, step_flags)
         # breakdown graph: events at every stage boundary
@@ -207,14 +212,15 @@ def make_workload(cfg, steps: int, warmup: int, dev, step_flags: int = 0, budget
     return inp0, passes, ws, io
 
 
-def run_step(passes, ws, events=False):
+def run_step(passes, ws, events=False, lists=False):
     import bit_plane_kv_encode_gb300 as pk
     for p in passes:
         # n_max is the launch-sizing bound: the capacity, so that graph replays stay
         # valid while the sequences grow by one token per replay
         for layer in p["arr"]:
             layer.n_max = p["cap"] - 1
-        pk.bpkv_decode_step(p["arr"], p["L"], p["args_ev"] if events else p["args"], ws, ws.numel())
+        a = p["args_lists"] if lists else (p["args_ev"] if events else p["args"])
+        pk.bpkv_decode_step(p["arr"], p["L"], a, ws, ws.numel())
 
 
 def stage_times_ms(passes):
@@ -313,6 +319,8 @@ def bench_ours(args, cfg, rank, world, local):
         for s, v in stage_times_ms(passes).items():
             stage_ms[s].append(v)
 
+    run_step(passes, ws, lists=True)  # untimed: index lists for the union sizes below
+    torch.cuda.synchronize()
     total_ms = all_max(sum(step_ms), world)
     ms_per_step = total_ms / args.steps
     keys_per_step = len(passes) * L * N * H * n

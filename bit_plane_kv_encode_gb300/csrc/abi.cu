@@ -9,18 +9,23 @@ cudaError_t launch_encode_append(const bpkv_cache& c, const uint16_t* k_new, con
                                  cudaStream_t st);
 cudaError_t launch_alloc_depths(const bpkv_cache& c, const float* q, const float* sigma2, const int32_t* budget_q,
                                 uint8_t* depths, cudaStream_t st, uint32_t* tickets = nullptr,
-                                void* plan = nullptr);
+                                void* plan = nullptr, uint32_t* hist = nullptr, uint32_t* ctr = nullptr);
 cudaError_t launch_fixed_depths(const bpkv_cache& c, const float* q, int32_t n_channels, int32_t depth,
-                                uint8_t* depths, cudaStream_t st, uint32_t* tickets = nullptr, void* plan = nullptr);
+                                uint8_t* depths, cudaStream_t st, uint32_t* tickets = nullptr, void* plan = nullptr,
+                                uint32_t* hist = nullptr, uint32_t* ctr = nullptr);
 size_t scan_plan_bytes(int group);
 size_t attend_ranges_part_bytes(const bpkv_cache& c);
 bool attend_ranges_eligible(const bpkv_cache& c, int32_t k);
-cudaError_t launch_attend_ranges(const bpkv_cache& c, const float* q, const int32_t* idx, int32_t k, float* part,
+cudaError_t launch_attend_ranges(const bpkv_cache& c, const float* q, const float* scores, int64_t ld,
+                                 const unsigned long long* cut, int32_t n_sink, int32_t n_recent, float* part,
                                  uint32_t* tickets, float* out, cudaStream_t st);
 cudaError_t launch_scan(const bpkv_cache& c, const float* q, const uint8_t* depths, float* scores, int64_t ld,
-                        cudaStream_t st, const void* plan = nullptr);
+                        cudaStream_t st, const void* plan = nullptr, uint32_t* hist = nullptr,
+                        int32_t n_sink = 0, int32_t n_recent = 0);
 cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
-                        int32_t n_recent, int32_t* idx, int32_t* status, cudaStream_t st);
+                        int32_t n_recent, const SelBufs& b, HistState hs, int32_t* idx, int32_t* status,
+                        cudaStream_t st);
+bool cut_counts_hist(const bpkv_cache& c);
 cudaError_t launch_union(const bpkv_cache& c, const int32_t* idx, int32_t k, int32_t* uidx, uint8_t* umask,
                          int32_t* ucount, cudaStream_t st);
 cudaError_t launch_attend(const bpkv_cache& c, const float* q, const int32_t* uidx, const uint8_t* umask,
@@ -76,8 +81,8 @@ int check_k(int32_t k, int32_t n_sink, int32_t n_recent) {
 
 // Workspace layout: status word, then the buffers each call family needs.
 struct Layout {
-  size_t scores = 0, part = 0, depths = 0, idx = 0, uidx = 0, umask = 0, ucount = 0, tickets = 0, plan = 0,
-         total = 0;
+  size_t scores = 0, hist = 0, ctr = 0, cand = 0, cut = 0, part = 0, depths = 0, idx = 0, uidx = 0, umask = 0,
+         ucount = 0, tickets = 0, plan = 0, total = 0;
 };
 
 Layout layout(const bpkv_cache& c, int32_t k, int32_t what) {
@@ -87,6 +92,15 @@ Layout layout(const bpkv_cache& c, int32_t k, int32_t what) {
   if (what & (BPKV_WS_SCAN_TOPK | BPKV_WS_STEP)) {
     L.scores = off;
     off = align_up(off + NH * c.group * (size_t)c.cap_tokens * sizeof(float));
+    // selection scratch; ctr directly follows hist (one memset clears both)
+    const size_t rows = NH * c.group;
+    L.hist = off;
+    L.ctr = off + rows * kTopkBins * sizeof(uint32_t);
+    off = align_up(L.ctr + rows * kSelCounters * sizeof(uint32_t));
+    L.cand = off;
+    off = align_up(off + rows * 1024 * sizeof(unsigned long long));
+    L.cut = off;
+    off = align_up(off + rows * sizeof(unsigned long long));
   }
   size_t part = 0;
   if (what & (BPKV_WS_ATTEND | BPKV_WS_STEP)) part = attend_part_bytes(c, (int64_t)c.group * k, false);
@@ -120,6 +134,12 @@ Layout layout(const bpkv_cache& c, int32_t k, int32_t what) {
   }
   L.total = off;
   return L;
+}
+
+SelBufs sel_bufs(void* ws, const Layout& L) {
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  return SelBufs{reinterpret_cast<uint32_t*>(w + L.hist), reinterpret_cast<uint32_t*>(w + L.ctr),
+                 reinterpret_cast<unsigned long long*>(w + L.cand), reinterpret_cast<unsigned long long*>(w + L.cut)};
 }
 
 int check_ws(const bpkv_cache& c, int32_t k, int32_t what, void* ws, size_t ws_bytes) {
@@ -212,9 +232,10 @@ int bpkv_topk(const bpkv_cache* c, const float* scores, int64_t ld_scores, int32
   BPKV_TRY(check_cache(c));
   BPKV_TRY(check_k(k, n_sink, n_recent));
   if (!scores || !idx || ld_scores < c->n_max) return BPKV_EINVAL;
-  if (!ws || !aligned(ws, kAlign) || ws_bytes < kAlign) return BPKV_ENOWORKSPACE;
-  return cuda_status(launch_topk(*c, scores, ld_scores, k, n_sink, n_recent, idx, static_cast<int32_t*>(ws),
-                                 as_stream(stream)));
+  BPKV_TRY(check_ws(*c, k, BPKV_WS_SCAN_TOPK, ws, ws_bytes));
+  const Layout L = layout(*c, k, BPKV_WS_SCAN_TOPK);
+  return cuda_status(launch_topk(*c, scores, ld_scores, k, n_sink, n_recent, sel_bufs(ws, L), HistState::kDirty, idx,
+                                 static_cast<int32_t*>(ws), as_stream(stream)));
 }
 
 int bpkv_scan_topk(const bpkv_cache* c, const float* q, const uint8_t* depths, int32_t k, int32_t n_sink,
@@ -225,10 +246,17 @@ int bpkv_scan_topk(const bpkv_cache* c, const float* q, const uint8_t* depths, i
   BPKV_TRY(check_ws(*c, k, BPKV_WS_SCAN_TOPK, ws, ws_bytes));
   const Layout L = layout(*c, k, BPKV_WS_SCAN_TOPK);
   float* scores = reinterpret_cast<float*>(at(ws, L.scores));
+  const SelBufs b = sel_bufs(ws, L);
   cudaStream_t st = as_stream(stream);
-  BPKV_TRY(cuda_status(launch_scan(*c, q, depths, scores, c->cap_tokens, st)));
-  return cuda_status(
-      launch_topk(*c, scores, c->cap_tokens, k, n_sink, n_recent, idx, static_cast<int32_t*>(ws), st));
+  const size_t rows = (size_t)c->n_seq * c->n_kv_heads * c->group;
+  BPKV_TRY(cuda_status(cudaMemsetAsync(b.hist, 0, rows * (kTopkBins + kSelCounters) * sizeof(uint32_t), st)));
+  // the level-0 histograms: counted by the cut kernel when it can, else by the scan
+  const bool cut_counts = cut_counts_hist(*c);
+  BPKV_TRY(cuda_status(launch_scan(*c, q, depths, scores, c->cap_tokens, st, nullptr, cut_counts ? nullptr : b.hist,
+                                   n_sink, n_recent)));
+  return cuda_status(launch_topk(*c, scores, c->cap_tokens, k, n_sink, n_recent, b,
+                                 cut_counts ? HistState::kZero : HistState::kCounted, idx, static_cast<int32_t*>(ws),
+                                 st));
 }
 
 int bpkv_union(const bpkv_cache* c, const int32_t* idx, int32_t k, int32_t* uidx, uint8_t* umask, int32_t* ucount,
@@ -335,16 +363,21 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
     int32_t* ucount = reinterpret_cast<int32_t*>(at(ws, L.ucount));
     uint32_t* tickets = reinterpret_cast<uint32_t*>(at(ws, L.tickets));
     void* plan = at(ws, L.plan);
+    const SelBufs sb = sel_bufs(ws, L);
     BPKV_TRY(mark(l, 1));
     if (a->depth_rule == BPKV_DEPTH_WATERFILL) {
-      BPKV_TRY(cuda_status(
-          launch_alloc_depths(c, q, a->sigma2 + (size_t)l * NH * kD, a->budget_q, depths, st, tickets, plan)));
+      BPKV_TRY(cuda_status(launch_alloc_depths(c, q, a->sigma2 + (size_t)l * NH * kD, a->budget_q, depths, st,
+                                               tickets, plan, sb.hist, sb.ctr)));
     } else {
-      BPKV_TRY(
-          cuda_status(launch_fixed_depths(c, q, a->fixed_channels, a->fixed_depth, depths, st, tickets, plan)));
+      BPKV_TRY(cuda_status(launch_fixed_depths(c, q, a->fixed_channels, a->fixed_depth, depths, st, tickets, plan,
+                                               sb.hist, sb.ctr)));
     }
     BPKV_TRY(mark(l, 2));
-    BPKV_TRY(cuda_status(launch_scan(c, q, depths, scores, c.cap_tokens, st, plan)));
+    // the level-0 histograms (zeroed by the depth kernel): counted by the cut kernel when it can, else by the scan
+    const bool cut_counts = cut_counts_hist(c);
+    const HistState hs = cut_counts ? HistState::kZero : HistState::kCounted;
+    BPKV_TRY(cuda_status(launch_scan(c, q, depths, scores, c.cap_tokens, st, plan, cut_counts ? nullptr : sb.hist,
+                                     a->n_sink, a->n_recent)));
     BPKV_TRY(mark(l, 3));
     if ((a->flags & BPKV_STEP_TAIL) && tail_eligible(c, a->k, a->n_sink, a->n_recent)) {
       int32_t* iout = a->idx_out ? a->idx_out + (size_t)l * NH * G * a->k : nullptr;
@@ -353,15 +386,21 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
       for (int e = 4; e <= 6; ++e) BPKV_TRY(mark(l, e));
       continue;
     }
-    BPKV_TRY(cuda_status(launch_topk(c, scores, c.cap_tokens, a->k, a->n_sink, a->n_recent, idx, status, st)));
-    BPKV_TRY(mark(l, 4));
     if (attend_ranges_eligible(c, a->k)) {
-      // union formed inside the attention kernel, per token range
+      // cuts only (lists when asked for); the attention selects by cut and forms the union per token range
+      int32_t* iout = a->idx_out ? a->idx_out + (size_t)l * NH * G * a->k : nullptr;
+      BPKV_TRY(cuda_status(
+          launch_topk(c, scores, c.cap_tokens, a->k, a->n_sink, a->n_recent, sb, hs, iout, status, st)));
+      BPKV_TRY(mark(l, 4));
       BPKV_TRY(mark(l, 5));
-      BPKV_TRY(cuda_status(launch_attend_ranges(c, q, idx, a->k, part, tickets, out, st)));
+      BPKV_TRY(cuda_status(launch_attend_ranges(c, q, scores, c.cap_tokens, sb.cut, a->n_sink, a->n_recent, part,
+                                                tickets, out, st)));
       BPKV_TRY(mark(l, 6));
       continue;
     }
+    BPKV_TRY(
+        cuda_status(launch_topk(c, scores, c.cap_tokens, a->k, a->n_sink, a->n_recent, sb, hs, idx, status, st)));
+    BPKV_TRY(mark(l, 4));
     BPKV_TRY(cuda_status(launch_union(c, idx, a->k, uidx, umask, ucount, st)));
     BPKV_TRY(mark(l, 5));
     BPKV_TRY(cuda_status(launch_attend(c, q, uidx, umask, ucount, (int32_t)(G * a->k), part, out, false, st)));

@@ -17,7 +17,7 @@ constexpr int kAttnThreads = 128;
 constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kSparseRows = 64;    // union rows per CTA
 constexpr int kDenseRows = 512;    // tokens per CTA (dense)
-constexpr int kPartStride = kD + 2;  // o[D], m, l
+constexpr int kPartStride = kD + 4;  // o[D], m, l, 2 pad (rows 16-byte aligned)
 
 struct AttnArgs {
   const uint16_t* k_rows;
@@ -223,69 +223,63 @@ __global__ void __launch_bounds__(kD) k_attend_combine(AttnArgs a, float* out) {
 }
 
 // ---------------------------------------------------------------------------
-// Decode-step attention straight from the per-head selections.  One CTA per
-// (token range, KV head, sequence): it binary-searches each head's ascending
-// index list for the tokens of its range, merges those pieces into the range's
-// union rows with head masks (ranks by binary search in the other pieces), and
-// attends in two phases: logits with one thread per row (a whole 128-channel
-// dot product per thread, no shuffles), then V accumulation with one thread per
-// channel.  The partial (max, sum, output) of every head goes to the
-// workspace; the last CTA of the unit to finish (ticket counter, zeroed by the
-// depth kernel earlier in the step) merges them by log-sum-exp and resets it.
-constexpr int kRangeThreads = 128;
-constexpr int kRangeMaxEnt = 4096;    // selected (token, head) entries in one range (<= G k)
+// Decode-step attention straight from the selection cuts.  One CTA per (token
+// range, KV head, sequence).  Every token of the range is marked with the query
+// heads that chose it: sinks and recent tokens by all, middle tokens by the
+// heads whose cut their (score key, ~index) reaches.  An ordered compaction
+// (block scan) lists the range's union rows ascending with their head masks.  Attention then runs in two
+// phases: logits with four threads per row, then V accumulation.  The partial
+// (max, sum, output) of every head goes to the workspace; the last CTA of the
+// unit to finish (ticket counter, zeroed by the depth kernel earlier in the
+// step) merges them by log-sum-exp and resets it.
+constexpr int kRangeThreads = 256;
 constexpr int kRangeMaxRows = 2048;   // union rows of one range (<= min(range tokens, G k))
-constexpr int kRangeMaxRanges = 16;   // ranges per unit
+constexpr int kRangeMaxRanges = 24;   // ranges per unit (the merge holds all of a unit's in registers)
+constexpr int kRangeAlign = 512;      // range sizes are multiples of this
+constexpr int kRangeWin = 2048;       // selection window (its scores fill the logit buffer at G = 8)
+constexpr int kQPitch = 36;           // floats per (head, quarter) row of q in shared memory
+// (range, head) partials the merge stages at once: 3 kRangeMaxRanges G floats of
+// weights and n kD floats of outputs within the kRangeMaxRows G float logit buffer
+constexpr int kMergeEntries = (kRangeMaxRows * BPKV_MAX_GROUP - 3 * kRangeMaxRanges * BPKV_MAX_GROUP) / kD;
 
 struct RangeArgs {
   const uint16_t* k_rows;
   const uint16_t* v_rows;
   const int64_t* seq_len;
   const float* q;
-  const int32_t* idx;     // [N][H][G][k], ascending, -1 padded
-  int32_t k;
+  const float* scores;             // [N][H][G][ld]
+  int64_t ld;
+  const unsigned long long* cut;   // [N][H][G]
+  int32_t n_sink, n_recent;
   int64_t cap;
   int32_t n_heads, group;
-  int64_t range_tok;      // tokens per range
+  int64_t range_tok;               // tokens per range, a multiple of kRangeAlign
   int32_t n_ranges;
-  float* part;            // [N][H][n_ranges][G][D + 2]
-  uint32_t* tickets;      // [N][H], zero on entry
-  float* out;             // [N][H][G][D]
+  float* part;                     // [N][H][n_ranges][G][D + 2]
+  uint32_t* tickets;               // [N][H], zero on entry
+  float* out;                      // [N][H][G][D]
 };
 
 struct RangeSmem {
-  int32_t sub[kRangeMaxEnt];           // the heads' pieces of their lists, one after another
-  int32_t rows[kRangeMaxEnt];
-  uint8_t rmask[kRangeMaxEnt];
+  int32_t rows[kRangeMaxRows];
+  uint8_t rmask[kRangeMaxRows];
   float logit[kRangeMaxRows][BPKV_MAX_GROUP];
-  float q[BPKV_MAX_GROUP][kD];
-  int sa[BPKV_MAX_GROUP], sn[BPKV_MAX_GROUP], soff[BPKV_MAX_GROUP];
-  float red[BPKV_MAX_GROUP][kRangeThreads / 32];
-  float m[BPKV_MAX_GROUP], l[BPKV_MAX_GROUP];
+  float q[BPKV_MAX_GROUP * 4 * kQPitch];  // [head][quarter][kQPitch], 32 used
+  __align__(16) uint8_t wbits[kRangeWin];
+  uint32_t ck[BPKV_MAX_GROUP], ci[BPKV_MAX_GROUP];
+  uint32_t mkey[BPKV_MAX_GROUP];          // order-preserving key of each head's largest logit
+  uint32_t warp_tot[kRangeThreads / 32];
+  float lslot[kRangeThreads / 32][BPKV_MAX_GROUP];
   uint32_t n_rows, is_last;
 };
 
-__device__ __forceinline__ int valid_count(const int32_t* v, int k) {
-  int lo = 0, hi = k;  // entries >= 0 come first
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (v[mid] >= 0) lo = mid + 1;
-    else hi = mid;
-  }
-  return lo;
+// Inverse of ordered_key.
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-__device__ __forceinline__ int lower_bound_g(const int32_t* v, int n, int64_t x) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if ((int64_t)v[mid] < x) lo = mid + 1;
-    else hi = mid;
-  }
-  return lo;
-}
-
-__global__ void __launch_bounds__(kRangeThreads) k_attend_ranges(RangeArgs a) {
+template <int GP>
+__global__ void __launch_bounds__(kRangeThreads, 512 / kRangeThreads) k_attend_ranges(RangeArgs a) {
   pdl_enter();
   extern __shared__ __align__(16) unsigned char range_raw[];
   RangeSmem& S = *reinterpret_cast<RangeSmem*>(range_raw);
@@ -295,309 +289,357 @@ __global__ void __launch_bounds__(kRangeThreads) k_attend_ranges(RangeArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t n = a.seq_len[s];
   const int64_t t0 = (int64_t)rg * a.range_tok, t1 = min64(t0 + a.range_tok, n);
-  const int32_t* li = a.idx + unit * G * a.k;
+  const int64_t lo = min64(a.n_sink, n), hi = max64(n - a.n_recent, lo);
   const float qscale = 0.08838834764831845f * 1.4426950408889634f;
 
-  for (int e = tid; e < G * kD; e += kRangeThreads) S.q[e / kD][e % kD] = a.q[unit * G * kD + e] * qscale;
-  // the heads' lists, staged with one coalesced pass (rows[] is free until the merge)
-  int32_t* lst = S.rows;
-  for (int e = tid; e < G * a.k; e += kRangeThreads) lst[e] = li[e];
-  __syncthreads();
+  for (int e = tid; e < G * kD; e += kRangeThreads)
+    S.q[(e / 32) * kQPitch + e % 32] = a.q[unit * G * kD + e] * qscale;
   if (tid < G) {
-    const int32_t* lg = lst + tid * a.k;
-    const int cnt = valid_count(lg, a.k);
-    const int lo = t0 < t1 ? lower_bound_g(lg, cnt, t0) : 0;
-    const int hi = t0 < t1 ? lower_bound_g(lg, cnt, t1) : 0;
-    S.sa[tid] = lo;
-    S.sn[tid] = hi - lo;
+    const unsigned long long c = a.cut[unit * G + tid];
+    S.ck[tid] = (uint32_t)(c >> 32);
+    S.ci[tid] = 0xFFFFFFFFu - (uint32_t)c;
+    S.mkey[tid] = 0u;
   }
   __syncthreads();
-  if (tid == 0) {
-    int off = 0;
-    for (int g = 0; g < G; ++g) {
-      S.soff[g] = off;
-      off += S.sn[g];
-    }
-    S.n_rows = (uint32_t)off;  // entries before merging
-  }
-  __syncthreads();
-  const int n_ent = (int)S.n_rows;
-  for (int g = 0; g < G; ++g)
-    for (int i = tid; i < S.sn[g]; i += kRangeThreads) S.sub[S.soff[g] + i] = lst[g * a.k + S.sa[g] + i];
-  __syncthreads();
-  // merge rank of every entry; duplicates (same token, several heads) are ordered by head
-  for (int e = tid; e < n_ent; e += kRangeThreads) {
-    int g = 0;
-    while (g + 1 < G && S.soff[g + 1] <= e) ++g;
-    const int32_t x = S.sub[e];
-    int pos = e - S.soff[g];
-    for (int g2 = 0; g2 < G; ++g2) {
-      if (g2 == g) continue;
-      const int32_t* v = S.sub + S.soff[g2];
-      const int nn = S.sn[g2];
-      int lo = 0, hi = nn;
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (g2 < g ? v[mid] <= x : v[mid] < x) lo = mid + 1;
-        else hi = mid;
+  // selection, in windows of kRangeWin tokens: thread = 4-token quads, all
+  // heads' scores of a quad loaded at once (two quads in flight); the quads'
+  // head masks go to shared memory, then each thread compacts a run of
+  // consecutive tokens in order.
+  const float* sc = a.scores + unit * G * a.ld;
+  const uint32_t all = (1u << G) - 1u;
+  uint32_t carry = 0;
+  for (int64_t w0 = t0; w0 < t1; w0 += kRangeWin) {
+    const int wl = (int)min64(kRangeWin, t1 - w0);
+    const int wq = (wl + 3) / 4;  // score rows hold whole quads (their length is a multiple of 4)
+    __syncthreads();              // the previous window is done
+    for (int q0 = tid; q0 < wq; q0 += 2 * kRangeThreads) {
+      float4 v[2][GP];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int qd = min(q0 + u * kRangeThreads, wq - 1);  // unconditional loads
+#pragma unroll
+        for (int g = 0; g < GP; ++g)
+          if (g < G) v[u][g] = *reinterpret_cast<const float4*>(sc + g * a.ld + w0 + 4 * qd);
       }
-      pos += lo;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int qd = q0 + u * kRangeThreads;
+        if (qd >= wq) break;
+        uint32_t packed = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int64_t x = w0 + 4 * qd + j;
+          uint32_t bits = 0u;
+          if (x < t1) {
+            if (x < lo || x >= hi) {
+              bits = all;
+            } else {
+#pragma unroll
+              for (int g = 0; g < GP; ++g) {
+                if (g >= G) break;
+                const float f = j == 0 ? v[u][g].x : (j == 1 ? v[u][g].y : (j == 2 ? v[u][g].z : v[u][g].w));
+                const uint32_t key = ordered_key(f);
+                if (key > S.ck[g] || (key == S.ck[g] && (uint32_t)x <= S.ci[g])) bits |= 1u << g;
+              }
+            }
+          }
+          packed |= bits << (8 * j);
+        }
+        reinterpret_cast<uint32_t*>(S.wbits)[qd] = packed;
+      }
     }
-    S.rows[pos] = x;
-    S.rmask[pos] = (uint8_t)g;  // head of the entry for now
+    __syncthreads();
+    const int run = (wl + kRangeThreads - 1) / kRangeThreads, j0 = tid * run;
+    uint32_t c_sel = 0;
+    for (int j = 0; j < run; ++j) c_sel += (j0 + j < wl && S.wbits[j0 + j] != 0);
+    uint32_t x = c_sel;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) S.warp_tot[warp] = x;
+    __syncthreads();
+    uint32_t pos = carry + x - c_sel, total = 0;
+#pragma unroll
+    for (int w = 0; w < kRangeThreads / 32; ++w) {
+      const uint32_t t = S.warp_tot[w];
+      pos += w < warp ? t : 0u;
+      total += t;
+    }
+    for (int j = 0; j < run; ++j) {
+      if (j0 + j < wl && S.wbits[j0 + j] != 0) {
+        if (pos < (uint32_t)kRangeMaxRows) {
+          S.rows[pos] = (int32_t)(w0 + j0 + j);
+          S.rmask[pos] = S.wbits[j0 + j];
+        }
+        ++pos;
+      }
+    }
+    carry += total;
   }
+  if (tid == 0) S.n_rows = min(carry, (uint32_t)kRangeMaxRows);
   __syncthreads();
-  // collapse equal tokens: the first entry of each run keeps the OR of the heads
-  uint32_t first = 0, bits = 0;
-  int32_t tok = -1;
-  if (tid == 0) S.n_rows = 0;
-  __syncthreads();
-  for (int base = 0; base < n_ent; base += kRangeThreads) {
-    const int e = base + tid;
-    first = 0;
-    if (e < n_ent) {
-      tok = S.rows[e];
-      first = (e == 0 || S.rows[e - 1] != tok) ? 1u : 0u;
-      bits = 0;
-      if (first)
-        for (int j = e; j < n_ent && S.rows[j] == tok; ++j) bits |= 1u << S.rmask[j];
-    }
-    __syncthreads();
-    const uint32_t bal = __ballot_sync(0xffffffffu, first);
-    __shared__ uint32_t wcnt[kRangeThreads / 32];
-    if (lane == 0) wcnt[warp] = __popc(bal);
-    __syncthreads();
-    uint32_t off = S.n_rows;
-    for (int w = 0; w < warp; ++w) off += wcnt[w];
-    off += __popc(bal & ((1u << lane) - 1u));
-    uint32_t tile = 0;
-    for (int w = 0; w < kRangeThreads / 32; ++w) tile += wcnt[w];
-    __syncthreads();
-    if (first) {
-      S.rows[off] = tok;  // off <= e: writes land on entries already read
-      S.rmask[off] = (uint8_t)bits;
-    }
-    if (tid == 0) S.n_rows += tile;
-    __syncthreads();
-  }
   const int nrows = (int)S.n_rows;
-
   const uint16_t* kb = a.k_rows + unit * a.cap * kD;
   const uint16_t* vb = a.v_rows + unit * a.cap * kD;
-  // phase 1: logits, four threads per row (32 channels each).  The loop bound
-  // is the same for every thread, so all lanes reach the shuffles.
+
+  // V rows of this thread's slot, loaded now: they do not depend on the logits.
+  // thread = (row slot rs, channels 4 c4 .. 4 c4 + 3); slot rs takes rows
+  // rs, rs + kSlots, ...
+  constexpr int kSlots = kRangeThreads / 32;
+  constexpr int kVPre = 16;
+  const int rs = warp, c4 = lane;
+  uint2 vpre[kVPre];
+  if (nrows > 0) {
+#pragma unroll
+    for (int b = 0; b < kVPre; ++b) {
+      const int r = min(rs + kSlots * b, nrows - 1);
+      vpre[b] = *reinterpret_cast<const uint2*>(vb + (int64_t)S.rows[r] * kD + 4 * c4);
+    }
+  }
+
+  // phase 1: logits, four threads per row (32 channels each), two items per
+  // thread in flight; the loop bound is the same for every thread, so all
+  // lanes reach the shuffles.  q is read as float4 from rows of kQPitch floats
+  // per (head, quarter): the four quarters of a warp's rows fall in different
+  // banks.  Each head's largest logit goes to S.mkey.
   const int n_items = nrows * 4;
-  for (int t0 = 0; t0 < n_items; t0 += kRangeThreads) {
-    const int t = t0 + tid;
-    const bool valid = t < n_items;
-    const int r = t >> 2, part4 = t & 3;
-    uint4 w[4];
+  constexpr int kItemsPer = 1;  // logit items per thread in flight
+  float mx[GP];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) w[c] = make_uint4(0u, 0u, 0u, 0u);
-    if (valid) {
-      const uint4* kr = reinterpret_cast<const uint4*>(kb + (int64_t)S.rows[r] * kD + part4 * 32);
+  for (int g = 0; g < GP; ++g) mx[g] = -INFINITY;
+  for (int it0 = 0; it0 < n_items; it0 += kItemsPer * kRangeThreads) {
+    uint4 w[kItemsPer][4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) w[c] = kr[c];
+    for (int u = 0; u < kItemsPer; ++u) {
+      const int t = min(it0 + u * kRangeThreads + tid, n_items - 1);
+      const uint4* kr = reinterpret_cast<const uint4*>(kb + (int64_t)S.rows[t >> 2] * kD + (t & 3) * 32);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) w[u][c] = kr[c];
     }
-    float acc[BPKV_MAX_GROUP];
 #pragma unroll
-    for (int g = 0; g < BPKV_MAX_GROUP; ++g) acc[g] = 0.f;
+    for (int u = 0; u < kItemsPer; ++u) {
+      const int t = it0 + u * kRangeThreads + tid;
+      const bool valid = t < n_items;
+      const int r = t >> 2, part4 = t & 3;
+      float acc[GP];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint32_t wv[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
+      for (int g = 0; g < GP; ++g) acc[g] = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float lo = __uint_as_float(wv[e] << 16), hi = __uint_as_float(wv[e] & 0xffff0000u);
-        const int ch = part4 * 32 + c * 8 + 2 * e;
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t wv[4] = {w[u][c].x, w[u][c].y, w[u][c].z, w[u][c].w};
 #pragma unroll
-        for (int g = 0; g < BPKV_MAX_GROUP; ++g) {
-          if (g >= G) break;
-          acc[g] = fmaf(S.q[g][ch], lo, acc[g]);
-          acc[g] = fmaf(S.q[g][ch + 1], hi, acc[g]);
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const float k0 = __uint_as_float(wv[2 * e2] << 16), k1 = __uint_as_float(wv[2 * e2] & 0xffff0000u);
+          const float k2 = __uint_as_float(wv[2 * e2 + 1] << 16);
+          const float k3 = __uint_as_float(wv[2 * e2 + 1] & 0xffff0000u);
+#pragma unroll
+          for (int g = 0; g < GP; ++g) {
+            const float4 qv = *reinterpret_cast<const float4*>(&S.q[(g * 4 + part4) * kQPitch + c * 8 + 4 * e2]);
+            acc[g] = fmaf(qv.x, k0, acc[g]);
+            acc[g] = fmaf(qv.y, k1, acc[g]);
+            acc[g] = fmaf(qv.z, k2, acc[g]);
+            acc[g] = fmaf(qv.w, k3, acc[g]);
+          }
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        acc[g] += __shfl_xor_sync(0xffffffffu, acc[g], 1);
+        acc[g] += __shfl_xor_sync(0xffffffffu, acc[g], 2);
+      }
+      if (valid && part4 == 0) {
+        const uint32_t mk = S.rmask[r];
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+          if (g < G) {
+            const float lg = ((mk >> g) & 1u) ? acc[g] : -INFINITY;
+            S.logit[r][g] = lg;
+            mx[g] = fmaxf(mx[g], lg);
+          }
         }
       }
     }
+  }
 #pragma unroll
-    for (int g = 0; g < BPKV_MAX_GROUP; ++g) {
-      acc[g] += __shfl_xor_sync(0xffffffffu, acc[g], 1);
-      acc[g] += __shfl_xor_sync(0xffffffffu, acc[g], 2);
-    }
-    if (valid && part4 == 0) {
-      const uint32_t mk = S.rmask[r];
+  for (int g = 0; g < GP; ++g) {
 #pragma unroll
-      for (int g = 0; g < BPKV_MAX_GROUP; ++g)
-        if (g < G) S.logit[r][g] = ((mk >> g) & 1u) ? acc[g] : -INFINITY;
-    }
+    for (int o = 16; o > 0; o >>= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], o));
+    if (lane == 0 && g < G && mx[g] != -INFINITY) atomicMax(&S.mkey[g], ordered_key(mx[g]));
   }
   __syncthreads();
-  // phase 2: per-head max and sum
-  for (int g = 0; g < G; ++g) {
-    float mx = -INFINITY;
-    for (int r = tid; r < nrows; r += kRangeThreads) mx = fmaxf(mx, S.logit[r][g]);
+  float M[GP];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) S.red[g][warp] = mx;
+  for (int g = 0; g < GP; ++g) M[g] = (g < G && S.mkey[g] != 0u) ? key_to_float(S.mkey[g]) : -INFINITY;
+
+  // phase 2: V accumulation with p = 2^(logit - M) formed on the fly and the
+  // sums of p per slot; slots are then added in slot order
+  float o[GP][4], lsum[GP];
+#pragma unroll
+  for (int g = 0; g < GP; ++g) {
+    lsum[g] = 0.f;
+#pragma unroll
+    for (int d = 0; d < 4; ++d) o[g][d] = 0.f;
   }
-  __syncthreads();
-  if (tid < G) {
-    float mx = S.red[tid][0];
-    for (int w = 1; w < kRangeThreads / 32; ++w) mx = fmaxf(mx, S.red[tid][w]);
-    S.m[tid] = mx;
-  }
-  __syncthreads();
-  for (int g = 0; g < G; ++g) {
-    float sum = 0.f;
-    const float mg = S.m[g];
-    for (int r = tid; r < nrows; r += kRangeThreads) {
-      const float p = (S.logit[r][g] == -INFINITY) ? 0.f : exp2f(S.logit[r][g] - mg);
-      S.logit[r][g] = p;
-      sum += p;
-    }
+  auto accumulate = [&](uint2 vw, int r) {
+    const float vf[4] = {__uint_as_float(vw.x << 16), __uint_as_float(vw.x & 0xffff0000u),
+                         __uint_as_float(vw.y << 16), __uint_as_float(vw.y & 0xffff0000u)};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane == 0) S.red[g][warp] = sum;
-  }
-  __syncthreads();
-  if (tid < G) {
-    float sum = 0.f;
-    for (int w = 0; w < kRangeThreads / 32; ++w) sum += S.red[tid][w];
-    S.l[tid] = sum;
-  }
-  __syncthreads();
-  // phase 3: V accumulation: thread = (row slot rs of 4, channels 4 c4 .. 4 c4 + 3),
-  // rows rs, rs + 4, ... with eight 8-byte loads in flight; slots merged in order
-  {
-    const int rs = tid >> 5, c4 = tid & 31;
-    float o[BPKV_MAX_GROUP][4];
-#pragma unroll
-    for (int g = 0; g < BPKV_MAX_GROUP; ++g)
-#pragma unroll
-      for (int d = 0; d < 4; ++d) o[g][d] = 0.f;
-    for (int r0 = rs; r0 < nrows; r0 += 4 * 8) {
-      uint2 vw[8];
-#pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        const int r = r0 + 4 * b;
-        vw[b] = r < nrows ? *reinterpret_cast<const uint2*>(vb + (int64_t)S.rows[r] * kD + 4 * c4)
-                          : make_uint2(0u, 0u);
-      }
-#pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        const int r = r0 + 4 * b;
-        if (r >= nrows) break;
-        const float vf[4] = {__uint_as_float(vw[b].x << 16), __uint_as_float(vw[b].x & 0xffff0000u),
-                             __uint_as_float(vw[b].y << 16), __uint_as_float(vw[b].y & 0xffff0000u)};
-#pragma unroll
-        for (int g = 0; g < BPKV_MAX_GROUP; ++g) {
-          if (g >= G) break;
-          const float p = S.logit[r][g];
-#pragma unroll
-          for (int d = 0; d < 4; ++d) o[g][d] = fmaf(p, vf[d], o[g][d]);
-        }
-      }
-    }
-    // merge the four row slots in order through shared memory: the upper half of
-    // the logit buffer is free once every weight has been used
-    __syncthreads();
-    float* acc = &S.logit[kRangeMaxRows / 2][0];  // [slot][head][128]: 4 * 8 * 128 floats
-#pragma unroll
-    for (int g = 0; g < BPKV_MAX_GROUP; ++g) {
+    for (int g = 0; g < GP; ++g) {
       if (g >= G) break;
+      const float lg = S.logit[r][g];
+      const float p = (lg == -INFINITY) ? 0.f : exp2f(lg - M[g]);
+      lsum[g] += p;
 #pragma unroll
-      for (int d = 0; d < 4; ++d) acc[(rs * BPKV_MAX_GROUP + g) * kD + 4 * c4 + d] = o[g][d];
+      for (int d = 0; d < 4; ++d) o[g][d] = fmaf(p, vf[d], o[g][d]);
     }
-    __syncthreads();
-    const int d = tid;
-    float* pp = a.part + ((unit * a.n_ranges + rg) * G) * kPartStride;
-    for (int g = 0; g < G; ++g) {
-      float v = 0.f;
+  };
 #pragma unroll
-      for (int r4 = 0; r4 < 4; ++r4) v += acc[(r4 * BPKV_MAX_GROUP + g) * kD + d];
-      pp[g * kPartStride + d] = v;
-      if (d == 0) {
-        pp[g * kPartStride + kD] = S.m[g];
-        pp[g * kPartStride + kD + 1] = S.l[g];
-      }
+  for (int b = 0; b < kVPre; ++b) {
+    const int r = rs + kSlots * b;
+    if (r < nrows) accumulate(vpre[b], r);
+  }
+  for (int r0 = rs + kSlots * kVPre; r0 < nrows; r0 += kSlots * 8) {
+    uint2 vw[8];
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const int r = min(r0 + kSlots * b, nrows - 1);
+      vw[b] = *reinterpret_cast<const uint2*>(vb + (int64_t)S.rows[r] * kD + 4 * c4);
+    }
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const int r = r0 + kSlots * b;
+      if (r < nrows) accumulate(vw[b], r);
     }
   }
-  // ticket: the last CTA of the unit merges every range's partial
-  __threadfence();
+  __syncthreads();  // every logit has been read: the logit buffer takes the slot sums
+  float* acc = &S.logit[0][0];  // [slot][head][128]
+#pragma unroll
+  for (int g = 0; g < GP; ++g) {
+    if (g >= G) break;
+    *reinterpret_cast<float4*>(&acc[(rs * GP + g) * kD + 4 * c4]) = make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
+    if (lane == 0) S.lslot[rs][g] = lsum[g];
+  }
   __syncthreads();
-  if (tid == 0) S.is_last = (atomicAdd(&a.tickets[unit], 1u) == (uint32_t)(a.n_ranges - 1)) ? 1u : 0u;
+  float* pp = a.part + ((unit * a.n_ranges + rg) * G) * kPartStride;
+  for (int e = tid; e < G * kD; e += kRangeThreads) {
+    const int g = e / kD, d = e % kD;
+    float v = 0.f;
+#pragma unroll
+    for (int r4 = 0; r4 < kSlots; ++r4) v += acc[(r4 * GP + g) * kD + d];
+    pp[g * kPartStride + d] = v;
+    if (d == 0) {
+      float L = 0.f;
+#pragma unroll
+      for (int r4 = 0; r4 < kSlots; ++r4) L += S.lslot[r4][g];
+      pp[g * kPartStride + kD] = M[g];
+      pp[g * kPartStride + kD + 1] = L;
+    }
+  }
+  // ticket: the last CTA of the unit merges every range's partial (the
+  // barrier orders the CTA's writes before thread 0's cumulative fence)
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    S.is_last = (atomicAdd(&a.tickets[unit], 1u) == (uint32_t)(a.n_ranges - 1)) ? 1u : 0u;
+    if (S.is_last) __threadfence();
+  }
   __syncthreads();
   if (!S.is_last) return;
-  __threadfence();
+  // merge: thread = (head, two channels) with its outputs of every range in
+  // flight; warp g < G meanwhile reduces head g's (max, sum) pairs across the
+  // ranges (lane = range) into weights 2^(m_c - M) and L (a fixed-order warp
+  // scan); the outputs are summed in range order
   const float* pu = a.part + unit * a.n_ranges * G * kPartStride;
-  // every range's (max, sum) at once, then weights, then the outputs with
-  // eight independent loads in flight per thread
-  float* wgt = &S.logit[0][0];  // [n_ranges][G] weights (the logits are no longer needed)
-  for (int e = tid; e < a.n_ranges * G; e += kRangeThreads) {
-    const float lc = __ldcg(pu + e * kPartStride + kD + 1);
-    wgt[e] = lc > 0.f ? __ldcg(pu + e * kPartStride + kD) : -INFINITY;
-  }
-  __syncthreads();
-  if (tid < G) {
-    float M = -INFINITY;
-    for (int c = 0; c < a.n_ranges; ++c) M = fmaxf(M, wgt[c * G + tid]);
-    S.m[tid] = M;
-  }
-  __syncthreads();
-  for (int e = tid; e < a.n_ranges * G; e += kRangeThreads) {
-    const float mc = wgt[e];
-    wgt[e] = (mc == -INFINITY) ? 0.f : exp2f(mc - S.m[e % G]);
-  }
-  __syncthreads();
-  if (tid < G) {
-    float L = 0.f;
-    for (int c = 0; c < a.n_ranges; ++c) L += wgt[c * G + tid] * __ldcg(pu + (c * G + tid) * kPartStride + kD + 1);
-    S.l[tid] = L;
-  }
-  __syncthreads();
-  for (int g = 0; g < G; ++g) {
-    float O = 0.f;
-    int c = 0;
-    for (; c + 8 <= a.n_ranges; c += 8) {
-      float ov[8];
+  float* pw = &S.logit[0][0];  // [n_ranges][G] weights
+  static_assert(kRangeMaxRanges <= 32, "one lane per range");
+  for (int e0 = 0; e0 < G * (kD / 2); e0 += kRangeThreads) {
+    const int e = e0 + tid;
+    const int g = min(e, G * (kD / 2) - 1) / (kD / 2), d2 = e % (kD / 2);
+    float2 ov[kRangeMaxRanges];
 #pragma unroll
-      for (int b = 0; b < 8; ++b) ov[b] = __ldcg(pu + ((c + b) * G + g) * kPartStride + tid);
+    for (int c = 0; c < kRangeMaxRanges; ++c)  // unconditional loads
+      ov[c] = __ldcg(reinterpret_cast<const float2*>(pu + (min(c, a.n_ranges - 1) * G + g) * kPartStride) + d2);
+    if (e0 == 0) {
+      if (warp < G) {
+        const int gw = warp, c = lane;
+        const bool in = c < a.n_ranges;
+        const float* pc = pu + (min(c, a.n_ranges - 1) * G + gw) * kPartStride;
+        const float mc = __ldcg(pc + kD), lc = __ldcg(pc + kD + 1);
+        const bool live = in && lc > 0.f;
+        float Mx = live ? mc : -INFINITY;
 #pragma unroll
-      for (int b = 0; b < 8; ++b) O = fmaf(wgt[(c + b) * G + g], ov[b], O);
+        for (int o = 16; o > 0; o >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
+        const float wc = live ? exp2f(mc - Mx) : 0.f;
+        // L: inclusive scan over the lanes, the last lane holds the total
+        float x = wc * lc;
+        if (!live) x = 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        if (in) pw[c * G + gw] = wc;
+        if (lane == 31) S.lslot[0][gw] = x;
+      }
+      __syncthreads();
     }
-    for (; c < a.n_ranges; ++c) O = fmaf(wgt[c * G + g], __ldcg(pu + (c * G + g) * kPartStride + tid), O);
-    a.out[(unit * G + g) * kD + tid] = (S.l[g] > 0.f) ? O / S.l[g] : 0.f;
+    float O0 = 0.f, O1 = 0.f;
+#pragma unroll
+    for (int c = 0; c < kRangeMaxRanges; ++c) {
+      if (c < a.n_ranges) {
+        const float wc = pw[c * G + g];
+        O0 = fmaf(wc, ov[c].x, O0);
+        O1 = fmaf(wc, ov[c].y, O1);
+      }
+    }
+    const float L = S.lslot[0][g];
+    if (e < G * (kD / 2))
+      reinterpret_cast<float2*>(a.out + (unit * G + g) * kD)[d2] =
+          L > 0.f ? make_float2(O0 / L, O1 / L) : make_float2(0.f, 0.f);
   }
   if (tid == 0) a.tickets[unit] = 0u;
 }
 
-// Tokens per range: at least 512, at most kRangeMaxRanges ranges per unit.
-int64_t range_tokens(int64_t n_max) {
-  int64_t rt = (n_max + kRangeMaxRanges - 1) / kRangeMaxRanges;
-  rt = (rt + 63) / 64 * 64;
-  return rt < 512 ? 512 : rt;
+// Tokens per range: a multiple of kRangeAlign, with at most kRangeMaxRanges ranges
+// per unit and at most kMergeEntries (range, head) partials (the merge stages
+// them all in the logit buffer).
+int64_t range_tokens(int64_t n_max, int group) {
+  const int64_t max_ranges = min64(kRangeMaxRanges, kMergeEntries / group);
+  int64_t rt = (n_max + max_ranges - 1) / max_ranges;
+  rt = (rt + kRangeAlign - 1) / kRangeAlign * kRangeAlign;
+  return rt < kRangeAlign ? kRangeAlign : rt;
 }
 
 size_t attend_ranges_part_bytes(const bpkv_cache& c) {
   return (size_t)c.n_seq * c.n_kv_heads * kRangeMaxRanges * c.group * kPartStride * sizeof(float);
 }
 
-// The range kernel needs every range's entries and union rows to fit its buffers.
+// A range's union rows (at most its tokens, and at most G k) must fit the row buffers.
 bool attend_ranges_eligible(const bpkv_cache& c, int32_t k) {
-  const int64_t ent = (int64_t)c.group * k;
-  const int64_t rows = min64(range_tokens(c.n_max), ent);
-  return ent <= kRangeMaxEnt && rows <= kRangeMaxRows;
+  const int64_t rows = min64(range_tokens(c.n_max, c.group), (int64_t)c.group * k);
+  return rows <= kRangeMaxRows;
 }
 
-cudaError_t launch_attend_ranges(const bpkv_cache& c, const float* q, const int32_t* idx, int32_t k, float* part,
+cudaError_t launch_attend_ranges(const bpkv_cache& c, const float* q, const float* scores, int64_t ld,
+                                 const unsigned long long* cut, int32_t n_sink, int32_t n_recent, float* part,
                                  uint32_t* tickets, float* out, cudaStream_t st) {
-  const int64_t rt = range_tokens(c.n_max);
+  const int64_t rt = range_tokens(c.n_max, c.group);
   const int32_t nr = (int32_t)((c.n_max + rt - 1) / rt);
   if (nr == 0) return cudaSuccess;
-  RangeArgs a{c.k_rows, c.v_rows, c.seq_len, q, idx, k, c.cap_tokens, c.n_kv_heads, c.group, rt, nr, part, tickets,
-              out};
+  RangeArgs a{c.k_rows, c.v_rows, c.seq_len,     q,       scores, ld,      cut,    n_sink, n_recent,
+              c.cap_tokens, c.n_kv_heads, c.group, rt, nr, part, tickets, out};
   const int smem = (int)sizeof(RangeSmem);
-  cudaError_t e = cudaFuncSetAttribute(k_attend_ranges, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(k_attend_ranges, dim3(nr, c.n_kv_heads, c.n_seq), dim3(kRangeThreads), (size_t)smem, st, a);
+  auto go = [&](auto kern) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kern, dim3(nr, c.n_kv_heads, c.n_seq), dim3(kRangeThreads), (size_t)smem, st, a);
+  };
+  if (c.group <= 1) return go(k_attend_ranges<1>);
+  if (c.group <= 2) return go(k_attend_ranges<2>);
+  if (c.group <= 4) return go(k_attend_ranges<4>);
+  return go(k_attend_ranges<8>);
 }
 
 int attend_chunks(int64_t rows, bool dense) {

@@ -36,6 +36,27 @@ __device__ __forceinline__ float fp16_bits_to_float(uint16_t b) {
 
 // Order-preserving map float -> uint32 (larger float -> larger key); -0 and +0
 // get the same key, as they compare equal.
+constexpr int kTopkBins = 4096;  // level-0 histogram: top 12 bits of the ordered key
+
+constexpr int kSelCounters = 4;  // per row: candidates gathered, CTAs done, CTAs at the barrier, spare
+
+// Selection scratch for rows = N H G query heads.  hist and ctr must be zero
+// when the selection starts (ctr is left zero by it); hist is followed
+// directly by ctr, so one memset clears both.
+// State of SelBufs::hist and ::ctr when a selection starts.
+enum class HistState {
+  kCounted,  // histograms counted (by the scan), counters zero
+  kZero,     // histograms and counters zero
+  kDirty,    // anything: cleared by the selection
+};
+
+struct SelBufs {
+  uint32_t* hist;            // [rows][kTopkBins]
+  uint32_t* ctr;             // [rows][kSelCounters]
+  unsigned long long* cand;  // [rows][1024]
+  unsigned long long* cut;   // [rows]
+};
+
 __device__ __forceinline__ uint32_t ordered_key(float f) {
   uint32_t u = __float_as_uint(f == 0.f ? 0.f : f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
@@ -70,5 +91,29 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
+
+// Cooperative launch (every CTA of the grid resident at once, so that CTAs
+// may wait for one another) with programmatic dependent launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_coop_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// Spin limit of in-kernel waits for other CTAs (each round sleeps ~100 ns):
+// well above any real wait, then the waiter records BPKV_DEV_TIMEOUT and goes on.
+constexpr uint32_t kSpinLimit = 1u << 21;
 
 }  // namespace bpkv

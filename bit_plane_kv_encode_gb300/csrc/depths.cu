@@ -30,7 +30,16 @@ struct DepthArgs {
   void* plan;         // optional [N][H] ScanPlan<GP>
   int32_t n_channels; // fixed sets only
   int32_t depth;      // fixed sets only
+  uint32_t* hist;     // optional [N][H][G][kTopkBins]: zeroed for the scan of this step
+  uint32_t* ctr;      // optional [N][H][G][kSelCounters] selection counters: zeroed with hist
 };
+
+// Zero this unit's selection histograms (G kTopkBins words).
+__device__ __forceinline__ void zero_hist(const DepthArgs& a, int64_t unit) {
+  uint4* h = reinterpret_cast<uint4*>(a.hist + unit * a.group * kTopkBins);
+  for (int e = threadIdx.x; e < a.group * kTopkBins / 4; e += blockDim.x) h[e] = make_uint4(0u, 0u, 0u, 0u);
+  if (a.ctr && (int)threadIdx.x < kSelCounters * a.group) a.ctr[unit * kSelCounters * a.group + threadIdx.x] = 0u;
+}
 
 // Build the scan plan of this unit from the depths the CTA just wrote (each
 // thread j < D reads back its own depth) and store it.
@@ -58,6 +67,7 @@ __global__ void __launch_bounds__(kScanThreads) k_alloc_depths(DepthArgs a) {
   const int unit = blockIdx.x;
   const int s = unit / a.n_heads;
   if (a.tickets && threadIdx.x == 0) a.tickets[unit] = 0u;
+  if (a.hist) zero_hist(a, unit);
   uint8_t* dep = a.depths + (int64_t)unit * kD;
   alloc_depths_cta(S, a.q + (int64_t)unit * a.group * kD, a.sigma2 + (int64_t)unit * kD, a.group, a.budget_q[s],
                    dep);
@@ -70,6 +80,7 @@ __global__ void __launch_bounds__(kScanThreads) k_fixed_depths(DepthArgs a) {
   __shared__ DepthSmem S;
   const int unit = blockIdx.x;
   if (a.tickets && threadIdx.x == 0) a.tickets[unit] = 0u;
+  if (a.hist) zero_hist(a, unit);
   uint8_t* dep = a.depths + (int64_t)unit * kD;
   fixed_depths_cta(S, a.q + (int64_t)unit * a.group * kD, a.group, a.n_channels, a.depth, dep);
   if (a.plan) emit_plan<GP>(a, unit, dep);
@@ -91,8 +102,9 @@ size_t scan_plan_bytes(int group) {
 }
 
 cudaError_t launch_alloc_depths(const bpkv_cache& c, const float* q, const float* sigma2, const int32_t* budget_q,
-                                uint8_t* depths, cudaStream_t st, uint32_t* tickets, void* plan) {
-  DepthArgs a{q, sigma2, budget_q, depths, c.n_kv_heads, c.group, tickets, plan, 0, 0};
+                                uint8_t* depths, cudaStream_t st, uint32_t* tickets, void* plan, uint32_t* hist,
+                                uint32_t* ctr) {
+  DepthArgs a{q, sigma2, budget_q, depths, c.n_kv_heads, c.group, tickets, plan, 0, 0, hist, ctr};
   return launch_depths_gp(c.group, [&](auto gp) {
     return launch_pdl(k_alloc_depths<decltype(gp)::value>, dim3(c.n_seq * c.n_kv_heads), dim3(kScanThreads), 0, st,
                       a);
@@ -100,8 +112,9 @@ cudaError_t launch_alloc_depths(const bpkv_cache& c, const float* q, const float
 }
 
 cudaError_t launch_fixed_depths(const bpkv_cache& c, const float* q, int32_t n_channels, int32_t depth,
-                                uint8_t* depths, cudaStream_t st, uint32_t* tickets, void* plan) {
-  DepthArgs a{q, nullptr, nullptr, depths, c.n_kv_heads, c.group, tickets, plan, n_channels, depth};
+                                uint8_t* depths, cudaStream_t st, uint32_t* tickets, void* plan, uint32_t* hist,
+                                uint32_t* ctr) {
+  DepthArgs a{q, nullptr, nullptr, depths, c.n_kv_heads, c.group, tickets, plan, n_channels, depth, hist, ctr};
   return launch_depths_gp(c.group, [&](auto gp) {
     return launch_pdl(k_fixed_depths<decltype(gp)::value>, dim3(c.n_seq * c.n_kv_heads), dim3(kScanThreads), 0, st,
                       a);

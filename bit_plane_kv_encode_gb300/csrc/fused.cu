@@ -147,9 +147,10 @@ __global__ void __launch_bounds__(kFuseThreads) k_decode_fused(FusedArgs a) {
     const int64_t b_begin = t_begin / kBlock;
     for (int c0 = 0; c0 * kBlock < n_own; c0 += kScanBlocks) {
       const int nbl = (int)min64(kScanBlocks, (n_own - (int64_t)c0 * kBlock + kBlock - 1) / kBlock);
-      scan_stage<GP>(S.x.scan, a.planes + U.plane_base(unit) + b_begin + c0,
-                     a.scales + U.scale_base(unit) + b_begin + c0, a.nb_cap, nbl);
-      scan_compute<GP>(S.x.scan, nbl, G, S.scores + c0 * kBlock, T, n_own - (int64_t)c0 * kBlock);
+      float v0[GP], v1[GP];
+      scan_chunk<GP>(S.x.scan, a.planes + U.plane_base(unit) + b_begin + c0,
+                     a.scales + U.scale_base(unit) + b_begin + c0, a.nb_cap, nbl, G, S.scores + c0 * kBlock, T,
+                     n_own - (int64_t)c0 * kBlock, v0, v1);
     }
     __syncthreads();
   }

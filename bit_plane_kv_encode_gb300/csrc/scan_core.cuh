@@ -6,11 +6,17 @@
 
 namespace bpkv {
 
-constexpr int kScanBlocks = 8;                  // 64-token blocks per CTA
+constexpr int kScanBlocks = 8;                  // 64-token blocks per chunk
+constexpr int kStageBatch = 8;                  // independent global loads in flight per thread while staging
 constexpr int kScanThreads = 32 * kScanBlocks;  // one warp per block
 constexpr int kMaxGroups = 20;                  // 16 depth-4 groups + one partial group per other depth
 constexpr int kWordPitch = 2 * kScanBlocks + 1; // u32 words per staged row (odd: conflict-free)
 constexpr int kMaxSlots = 288;                  // padded channel slots over all groups
+// Groups are staged and scored in passes of at most kPassGroups groups and
+// kPassSlots slots (one pass for every budget up to about 300 bits per token).
+constexpr int kPassGroups = 10;
+constexpr int kPassSlots = 144;
+constexpr int kMaxPasses = 8;
 
 template <int T>
 struct Depth {
@@ -42,7 +48,8 @@ struct __align__(16) ScanPlan {
   int8_t grp_t[kMaxGroups];
   int16_t grp_base[kMaxGroups];                     // first slot of each group
   int8_t grp_cnt[kMaxGroups];                       // channels in each group
-  int n_groups, n_slots;
+  int8_t pass_g[kMaxPasses + 1];                    // first group of each pass, then n_groups
+  int n_groups, n_slots, n_passes;
 };
 
 struct PlanScratch {
@@ -52,8 +59,8 @@ struct PlanScratch {
 
 template <int GP>
 struct ScanSmem {
-  uint32_t words[kMaxGroups * 32 * kWordPitch];     // staged plane half-words
-  float u[kScanBlocks * kMaxSlots * GP];            // [block][group slots][head][slot]
+  uint32_t words[kPassGroups * 32 * kWordPitch];    // staged plane half-words of one pass
+  float u[kScanBlocks * kPassSlots * GP];           // [block][pass slots: group slots][head][slot]
   ScanPlan<GP> P;
   PlanScratch X;
 };
@@ -185,6 +192,17 @@ __device__ void scan_setup(ScanPlan<GP>& S, PlanScratch& X, int t, const float (
     }
     S.n_groups = g;
     S.n_slots = slot;
+    // passes: runs of groups within kPassGroups groups and kPassSlots slots
+    int np = 0, g0 = 0;
+    while (g0 < g && np < kMaxPasses) {
+      int g1 = g0, sl = 0;
+      while (g1 < g && g1 - g0 < kPassGroups && sl + slot_pitch(S.grp_t[g1]) <= kPassSlots)
+        sl += slot_pitch(S.grp_t[g1++]);
+      S.pass_g[np++] = (int8_t)g0;
+      g0 = g1;
+    }
+    S.pass_g[np] = (int8_t)g;
+    S.n_passes = np;
   }
   __syncthreads();
   if (tid < kD && t > 0) {
@@ -232,57 +250,80 @@ __device__ void scan_store_plan(const ScanPlan<GP>& S, ScanPlan<GP>* __restrict_
   for (int e = threadIdx.x; e < (int)(sizeof(ScanPlan<GP>) / 16); e += blockDim.x) g[e] = s[e];
 }
 
-// Stage the plane words and scales of nbl (<= kScanBlocks) blocks starting at
-// pl / sp (the unit's arrays offset by the first block) and form u = s w.
+// Stage the plane words and block scales of groups [g0, g1) (slots [s0, s1))
+// for nbl (<= kScanBlocks) blocks starting at pl / sp (the unit's arrays
+// offset by the first block) and form u = s w for those slots.
 template <int GP>
-__device__ void scan_stage(ScanSmem<GP>& S, const uint64_t* __restrict__ pl, const uint16_t* __restrict__ sp,
-                           int64_t nb_cap, int nbl) {
+__device__ void scan_stage_pass(ScanSmem<GP>& S, const uint64_t* __restrict__ pl,
+                                const uint16_t* __restrict__ sp, int64_t nb_cap, int nbl, int g0, int g1) {
   const int tid = threadIdx.x;
   const ScanPlan<GP>& P = S.P;
-  const int n_groups = P.n_groups, n_slots = P.n_slots;
-  __syncthreads();  // the previous chunk's compute is done with words and u
-  for (int e = tid; e < n_groups * 32 * kScanBlocks; e += kScanThreads) {
-    const int r = e / kScanBlocks, lb = e % kScanBlocks;
-    const int row = P.row_of_lane[r];
-    if (row >= 0 && lb < nbl) {
-      const uint64_t w = pl[(int64_t)row * nb_cap + lb];
-      S.words[r * kWordPitch + 2 * lb] = (uint32_t)w;
-      S.words[r * kWordPitch + 2 * lb + 1] = (uint32_t)(w >> 32);
+  const int s0 = P.grp_base[g0], s1 = g1 < P.n_groups ? (int)P.grp_base[g1] : P.n_slots;
+  const int ps = s1 - s0;
+  __syncthreads();  // the previous compute is done with words and u
+  // plane words, kStageBatch independent loads in flight per thread
+  const int n_w = (g1 - g0) * 32 * kScanBlocks;
+  for (int e0 = tid; e0 < n_w; e0 += kStageBatch * kScanThreads) {
+    uint64_t w[kStageBatch];
+#pragma unroll
+    for (int b = 0; b < kStageBatch; ++b) {
+      const int e = e0 + b * kScanThreads, r = e / kScanBlocks, lb = e % kScanBlocks;
+      const int row = e < n_w ? P.row_of_lane[g0 * 32 + r] : -1;
+      w[b] = (row >= 0 && lb < nbl) ? pl[(int64_t)row * nb_cap + lb] : 0ull;
+    }
+#pragma unroll
+    for (int b = 0; b < kStageBatch; ++b) {
+      const int e = e0 + b * kScanThreads, r = e / kScanBlocks, lb = e % kScanBlocks;
+      if (e < n_w) {
+        S.words[r * kWordPitch + 2 * lb] = (uint32_t)w[b];
+        S.words[r * kWordPitch + 2 * lb + 1] = (uint32_t)(w[b] >> 32);
+      }
     }
   }
-  for (int e = tid; e < kScanBlocks * n_slots; e += kScanThreads) {
-    const int lb = e % kScanBlocks, slot = e / kScanBlocks;
-    const int ch = P.slot_ch[slot];
-    const float sc = (ch >= 0 && lb < nbl) ? fp16_bits_to_float(sp[(int64_t)ch * nb_cap + lb]) : 0.f;
-    const int g = P.slot_grp[slot];
-    const int base = P.grp_base[g], m = slot - base, pitch = slot_pitch(P.grp_t[g]);
-    float* ud = S.u + (lb * n_slots + base) * GP;
+  // block scales times the slot weights: u = s w
+  const int n_u = kScanBlocks * ps;
+  for (int e0 = tid; e0 < n_u; e0 += kStageBatch * kScanThreads) {
+    uint16_t sb[kStageBatch];
 #pragma unroll
-    for (int hh = 0; hh < GP; ++hh) ud[hh * pitch + m] = sc * P.w[base * GP + hh * pitch + m];
+    for (int b = 0; b < kStageBatch; ++b) {
+      const int e = e0 + b * kScanThreads, lb = e % kScanBlocks, slot = s0 + e / kScanBlocks;
+      const int ch = e < n_u ? P.slot_ch[slot] : -1;
+      sb[b] = (ch >= 0 && lb < nbl) ? sp[(int64_t)ch * nb_cap + lb] : (uint16_t)0;
+    }
+#pragma unroll
+    for (int b = 0; b < kStageBatch; ++b) {
+      const int e = e0 + b * kScanThreads, lb = e % kScanBlocks, slot = s0 + e / kScanBlocks;
+      if (e < n_u) {
+        const float sc = fp16_bits_to_float(sb[b]);
+        const int g = P.slot_grp[slot];
+        const int base = P.grp_base[g], m = slot - base, pitch = slot_pitch(P.grp_t[g]);
+        float* ud = S.u + (lb * ps + (base - s0)) * GP;
+#pragma unroll
+        for (int hh = 0; hh < GP; ++hh) ud[hh * pitch + m] = sc * P.w[base * GP + hh * pitch + m];
+      }
+    }
   }
   __syncthreads();
 }
 
-// Score the staged blocks: warp w takes block w (w < nbl).  Scores of head g
-// for the chunk's token x go to out[g * ld + x], for x < n_valid.
+// Add groups [g0, g1) of the staged pass to this lane's accumulators: warp w
+// takes block w (w < nbl), lane the tokens lane and lane + 32 of it.
 template <int GP>
-__device__ void scan_compute(const ScanSmem<GP>& S, int nbl, int G, float* out, int64_t ld, int64_t n_valid) {
+__device__ __forceinline__ void scan_compute_pass(const ScanSmem<GP>& S, int g0, int g1,
+                                                  unsigned long long (&acc0)[GP], unsigned long long (&acc1)[GP]) {
   const int lane = threadIdx.x & 31, lb = threadIdx.x >> 5;
-  if (lb >= nbl) return;
   uint32_t keep[5], rot[5];
   transpose_consts(lane, keep, rot);
-  unsigned long long acc0[GP], acc1[GP];
-#pragma unroll
-  for (int hh = 0; hh < GP; ++hh) acc0[hh] = acc1[hh] = 0ull;
   const ScanPlan<GP>& P = S.P;
-  const int n_groups = P.n_groups, n_slots = P.n_slots;
-  for (int g = 0; g < n_groups; ++g) {
+  const int s0 = P.grp_base[g0], s1 = g1 < P.n_groups ? (int)P.grp_base[g1] : P.n_slots;
+  const int ps = s1 - s0;
+  for (int g = g0; g < g1; ++g) {
     const int d = P.grp_t[g], cnt = P.grp_cnt[g];
-    const uint32_t* wr = S.words + (g * 32 + lane) * kWordPitch + 2 * lb;
+    const uint32_t* wr = S.words + ((g - g0) * 32 + lane) * kWordPitch + 2 * lb;
     const uint32_t x0 = warp_transpose32(wr[0], keep, rot);
     const uint32_t x1 = warp_transpose32(wr[1], keep, rot);
     const uint32_t xa0 = x0 << 1, xb0 = x0 >> 9, xa1 = x1 << 1, xb1 = x1 >> 9;
-    const float* ug = S.u + (lb * n_slots + P.grp_base[g]) * GP;
+    const float* ug = S.u + (lb * ps + (P.grp_base[g] - s0)) * GP;
     switch (d) {
       case 4: group_fields<4, GP>(cnt, xa0, xb0, xa1, xb1, ug, acc0, acc1); break;
       case 3: group_fields<3, GP>(cnt, xa0, xb0, xa1, xb1, ug, acc0, acc1); break;
@@ -290,6 +331,29 @@ __device__ void scan_compute(const ScanSmem<GP>& S, int nbl, int G, float* out, 
       default: group_fields<1, GP>(cnt, xa0, xb0, xa1, xb1, ug, acc0, acc1); break;
     }
   }
+}
+
+// Score one chunk of nbl (<= kScanBlocks) blocks starting at pl / sp: every
+// pass is staged and added in turn.  Scores of head g for the chunk's token x
+// go to out[g * ld + x], for x < n_valid; they are also left in v0 (token x)
+// and v1 (token x + 32).  Returns false for warps without a block.  The plan
+// must be in S.P.
+template <int GP>
+__device__ bool scan_chunk(ScanSmem<GP>& S, const uint64_t* __restrict__ pl, const uint16_t* __restrict__ sp,
+                           int64_t nb_cap, int nbl, int G, float* out, int64_t ld, int64_t n_valid,
+                           float (&v0)[GP], float (&v1)[GP]) {
+  const int lane = threadIdx.x & 31, lb = threadIdx.x >> 5;
+  const bool act = lb < nbl;
+  unsigned long long acc0[GP], acc1[GP];
+#pragma unroll
+  for (int hh = 0; hh < GP; ++hh) acc0[hh] = acc1[hh] = 0ull;
+  const int n_passes = S.P.n_passes;
+  for (int ps = 0; ps < n_passes; ++ps) {
+    const int g0 = S.P.pass_g[ps], g1 = S.P.pass_g[ps + 1];
+    scan_stage_pass<GP>(S, pl, sp, nb_cap, nbl, g0, g1);
+    if (act) scan_compute_pass<GP>(S, g0, g1, acc0, acc1);
+  }
+  if (!act) return false;
   const int64_t x0 = (int64_t)lb * kBlock + lane;
 #pragma unroll
   for (int hh = 0; hh < GP; ++hh) {
@@ -297,8 +361,33 @@ __device__ void scan_compute(const ScanSmem<GP>& S, int nbl, int G, float* out, 
     float p0, p1, r0, r1;
     unpack2(acc0[hh], p0, p1);
     unpack2(acc1[hh], r0, r1);
-    if (x0 < n_valid) out[hh * ld + x0] = p0 + p1;
-    if (x0 + 32 < n_valid) out[hh * ld + x0 + 32] = r0 + r1;
+    v0[hh] = p0 + p1;
+    v1[hh] = r0 + r1;
+    if (x0 < n_valid) out[hh * ld + x0] = v0[hh];
+    if (x0 + 32 < n_valid) out[hh * ld + x0 + 32] = v1[hh];
+  }
+  return true;
+}
+
+// Level-0 selection histogram of one warp's block (top 12 bits of the
+// order-preserving key), for tokens x0 + lane and x0 + lane + 32 in [lo, hi),
+// added to hist [G][kTopkBins]: lanes with equal (head, bin) are counted by
+// one atomic of their leader.  Called by whole warps.
+template <int GP>
+__device__ __forceinline__ void warp_hist(int G, int64_t x0, int64_t lo, int64_t hi, const float (&v0)[GP],
+                                          const float (&v1)[GP], uint32_t* __restrict__ hist) {
+  const int lane = threadIdx.x & 31;
+  const bool in0 = x0 >= lo && x0 < hi, in1 = x0 + 32 >= lo && x0 + 32 < hi;
+#pragma unroll
+  for (int hh = 0; hh < GP; ++hh) {
+    if (hh >= G) break;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const bool in = half ? in1 : in0;
+      const uint32_t b = in ? (ordered_key(half ? v1[hh] : v0[hh]) >> 20) : 0xFFFFu;
+      const uint32_t peers = __match_any_sync(0xffffffffu, b);
+      if (in && lane == __ffs(peers) - 1) atomicAdd(hist + hh * kTopkBins + b, (uint32_t)__popc(peers));
+    }
   }
 }
 

@@ -1,16 +1,23 @@
 // Selection (Fathom page, section 2, "Top-k decoding") and the GQA union of
 // winner rows (section 1 / section 3.1: k_U <= G k distinct rows per KV head).
 //
-// Top-k: one CTA per query head.  Scores map to order-preserving 32-bit keys
-// (staged in shared memory when the row's candidates fit).  A linear histogram
-// over the candidates' key range [min, max] locates the bucket holding the
-// (k - n_sink - n_recent)-th largest key (bins follow the data, so no bin takes
-// most of the atomics); a crowded bucket is refined the same way over its own
-// exact key range.  One more pass takes every key above the bucket and gathers
-// the bucket's keys, which a shared-memory bitonic sort by (key desc, index
-// asc) cuts at the exact count: ties go to the lower index, with an ordered
-// scan when more than kCandCap keys equal the threshold key.  Sinks, recent
-// tokens and the winners are finally sorted ascending.
+// Top-k, as an exact radix selection over order-preserving 32-bit score keys.
+// Each row (query head) keeps its sinks [0, n_sink), its recent tokens
+// [n - n_recent, n) and the m = k - n_sink - n_recent largest middle keys,
+// ties to the lower index.  Ordering the middle tokens by (key desc, index
+// asc), the chosen ones are exactly those whose 64-bit value (key, ~index) is
+// at least the m-th largest such value: the row's "cut".
+//   1. A 4096-bin histogram of the middle keys' top 12 bits (counted by the
+//      scan kernel as it writes the scores, or by k_hist) locates the bucket
+//      holding the m-th largest key.
+//   2. k_cut: CTAs over 4096-key chunks of the row append the bucket's keys to
+//      the row's candidate list; the last CTA to finish ranks them and stores
+//      the cut.  A bucket of more than 1024 keys is refined by that CTA on the
+//      next 12, then 8, key bits; a bucket that is a single key value repeated
+//      more than 1024 times is cut at the right occurrence in index order.
+//   3. k_lists (when index lists are wanted): an ordered compaction writes the
+//      sinks, the chosen middle tokens and the recent tokens ascending.
+// The decode step's attention reads the cuts directly.
 //
 // Union: one CTA per KV head.  Each sorted list entry's rank in the merge of
 // the G lists is its own position plus binary-search counts in the other
@@ -18,22 +25,20 @@
 // ORs the heads that chose it.
 #include "common.cuh"
 
+#include <mutex>
+
 namespace bpkv {
 
-constexpr int kSelThreads = 1024;
+constexpr int kSelThreads = 1024;  // k_lists and k_union
+constexpr int kCutThreads = 256;   // k_hist and k_cut
+constexpr int kCutChunk = 4096;    // middle keys per k_hist / k_cut CTA
+constexpr int kSelBatch = 16;      // independent score loads in flight per thread
+constexpr int kTileKeys = 32768;   // keys staged in shared memory per k_lists tile
 
-struct TopkArgs {
-  const float* scores;
-  int64_t ld;
-  const int64_t* seq_len;
-  int32_t* idx;
-  int32_t* status;
-  int32_t n_heads, group, k, n_sink, n_recent;
-};
-
-// Block-wide exclusive scan of one 32-bit value per thread (blockDim = 1024).
+// Block-wide exclusive scan of one 32-bit value per thread (any block size that
+// is a multiple of 32, up to 1024).
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* warp_tot, uint32_t* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
   uint32_t x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -43,7 +48,7 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* warp_t
   if (lane == 31) warp_tot[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    uint32_t w = warp_tot[lane];
+    const uint32_t w = lane < n_warps ? warp_tot[lane] : 0u;
     uint32_t incl = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -59,290 +64,525 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* warp_t
   return r;
 }
 
-constexpr int kHistBins = 2048;
-constexpr int kCandCap = 4096;       // keys of the threshold bucket kept for the exact sort
-constexpr int kSelCap = 8192;        // selected indices (k <= 8192)
-constexpr int kSelBatch = 8;         // independent score loads in flight per thread
-constexpr int kStageKeys = 32768;    // candidates staged in shared memory when they fit
-
-struct TopkSmem {
-  uint32_t keys[kStageKeys];           // staged order-preserving keys of the candidates
-  uint32_t hist[kHistBins];
-  unsigned long long cand[kCandCap];   // (key << 32) | ~index: larger = earlier
-  int32_t sel[kSelCap];
-  uint32_t warp_tot[32];
-  uint32_t red[2][32];
-  uint32_t n_cand, n_sel, tb, rem, tot, b_lo, b_hi;
+// The middle range [lo, hi) of a row and the number m of its keys to choose.
+struct RowRange {
+  int64_t n, lo, hi, cnt, m;
 };
 
-// Bitonic sort of v[0..n2) (n2 a power of two) by the whole value; descending
-// when desc, else ascending.  Called by the whole block.
-template <typename T>
-__device__ void block_bitonic(T* v, int n2, bool desc) {
-  for (int size = 2; size <= n2; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int t = threadIdx.x; t < n2 / 2; t += blockDim.x) {
-        const int i = 2 * t - (t & (stride - 1));
-        const int j = i + stride;
-        const bool d = ((i & size) == 0) == desc;
-        const T x = v[i], y = v[j];
-        if ((x < y) == d) {
-          v[i] = y;
-          v[j] = x;
-        }
-      }
-      __syncthreads();
-    }
-  }
+__device__ __forceinline__ RowRange row_range(int64_t n, int32_t k, int32_t n_sink, int32_t n_recent) {
+  RowRange r;
+  r.n = n;
+  r.lo = min64(n_sink, n);
+  r.hi = max64(n - n_recent, r.lo);
+  r.cnt = r.hi - r.lo;
+  r.m = max(k - n_sink - n_recent, 0);
+  return r;
 }
 
-__device__ __forceinline__ void sel_push(TopkSmem& S, int32_t i) {
-  const uint32_t p = atomicAdd(&S.n_sel, 1u);
-  if (p < (uint32_t)kSelCap) S.sel[p] = i;
-}
-
-__device__ __forceinline__ int pow2_at_least(int x) {
-  int p = 1;
-  while (p < x) p <<= 1;
-  return p;
-}
-
-// Block-wide min and max of (lo, hi) pairs.
-__device__ __forceinline__ void block_range(uint32_t& lo, uint32_t& hi, TopkSmem& S) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-  }
-  if (lane == 0) {
-    S.red[0][warp] = lo;
-    S.red[1][warp] = hi;
-  }
-  __syncthreads();
-  lo = S.red[0][0];
-  hi = S.red[1][0];
-  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
-    lo = min(lo, S.red[0][w]);
-    hi = max(hi, S.red[1][w]);
-  }
-  __syncthreads();
-}
-
-// Visit the order-preserving keys of candidates [0, cnt) (staged in shared
-// memory, or read from the scores kSelBatch at a time): f(index, key).
+// f(e, key) for the middle keys e in [e_begin, e_end) of a row (scores sc,
+// middle starting at lo), kSelBatch independent loads in flight per thread.
 template <typename F>
-__device__ __forceinline__ void for_keys(const TopkSmem& S, bool staged, const float* sc, int64_t lo, int64_t cnt,
-                                         F f) {
-  if (staged) {
-    for (int64_t e = threadIdx.x; e < cnt; e += kSelThreads) f(e, S.keys[e]);
-    return;
-  }
-  for (int64_t e0 = threadIdx.x; e0 < cnt; e0 += (int64_t)kSelBatch * kSelThreads) {
+__device__ __forceinline__ void for_row_keys(const float* __restrict__ sc, int64_t lo, int64_t e_begin,
+                                             int64_t e_end, F f) {
+  const int nt = blockDim.x;
+  for (int64_t e0 = e_begin + threadIdx.x; e0 < e_end; e0 += (int64_t)kSelBatch * nt) {
     float v[kSelBatch];
 #pragma unroll
-    for (int b = 0; b < kSelBatch; ++b) {
-      const int64_t e = e0 + (int64_t)b * kSelThreads;
-      v[b] = e < cnt ? sc[lo + e] : 0.f;
-    }
+    for (int b = 0; b < kSelBatch; ++b) v[b] = sc[lo + min64(e0 + (int64_t)b * nt, e_end - 1)];  // unconditional
 #pragma unroll
     for (int b = 0; b < kSelBatch; ++b) {
-      const int64_t e = e0 + (int64_t)b * kSelThreads;
-      if (e < cnt) f(e, ordered_key(v[b]));
+      const int64_t e = e0 + (int64_t)b * nt;
+      if (e < e_end) f(e, ordered_key(v[b]));
     }
   }
 }
 
-__global__ void __launch_bounds__(kSelThreads) k_topk(TopkArgs a) {
+// ------------------------------------------------------------------ k_hist
+
+struct HistArgs {
+  const float* scores;
+  int64_t ld;
+  const int64_t* seq_len;
+  uint32_t* hist;  // [rows][kTopkBins], zero on entry
+  int32_t rows_per_seq, k, n_sink, n_recent;
+};
+
+// Level-0 histogram of one chunk of one row's middle keys.  Grid (chunks, rows).
+__global__ void __launch_bounds__(kCutThreads) k_hist(HistArgs a) {
   pdl_enter();
-  extern __shared__ __align__(16) unsigned char topk_raw[];
-  TopkSmem& S = *reinterpret_cast<TopkSmem*>(topk_raw);
-  const int row = blockIdx.x;
-  const int s = row / (a.n_heads * a.group);
-  const int64_t n = a.seq_len[s];
-  const float* sc = a.scores + (int64_t)row * a.ld;
-  int32_t* out = a.idx + (int64_t)row * a.k;
-  const int64_t lo = min64(a.n_sink, n);
-  const int64_t hi = max64(n - a.n_recent, lo);
-  const int64_t cnt = hi - lo;
-  const int64_t n_top = max(a.k - a.n_sink - a.n_recent, 0);
+  __shared__ uint32_t H[kTopkBins];
+  const int row = blockIdx.y;
+  const RowRange r = row_range(a.seq_len[row / a.rows_per_seq], a.k, a.n_sink, a.n_recent);
+  const int64_t c0 = (int64_t)blockIdx.x * kCutChunk, c1 = min64(c0 + kCutChunk, r.cnt);
+  if (r.cnt <= r.m || r.m == 0 || c0 >= c1) return;
+  for (int b = threadIdx.x; b < kTopkBins; b += kCutThreads) H[b] = 0u;
+  __syncthreads();
+  for_row_keys(a.scores + (int64_t)row * a.ld, r.lo, c0, c1,
+               [&](int64_t, uint32_t key) { atomicAdd(&H[key >> 20], 1u); });
+  __syncthreads();
+  uint32_t* g = a.hist + (int64_t)row * kTopkBins;
+  for (int b = threadIdx.x; b < kTopkBins; b += kCutThreads)
+    if (H[b]) atomicAdd(g + b, H[b]);
+}
+
+// ------------------------------------------------------------------ k_cut
+
+constexpr int kRankCap = 1024;  // bucket size ranked directly
+
+struct CutArgs {
+  const float* scores;
+  int64_t ld;
+  const int64_t* seq_len;
+  uint32_t* hist;              // [rows][kTopkBins] level-0 histograms of the middle keys
+  unsigned long long* cand;    // [rows][kRankCap] candidate (key, ~index) values
+  uint32_t* ctr;               // [rows][kSelCounters]: zero on entry, left zero
+  unsigned long long* cut;     // [rows] out
+  int32_t* status;
+  int32_t rows_per_seq, k, n_sink, n_recent;
+  int32_t build_hist;          // count hist here (zero on entry; cooperative launch) instead of reading it
+};
+
+struct __align__(16) CutSmem {
+  uint32_t hist[kTopkBins];
+  unsigned long long cand[kRankCap + 2];
+  uint32_t warp_tot[32];
+  uint32_t tot, tb, rem, nb, n_cand, is_last;
+  unsigned long long cut;
+};
+
+// Radix levels over the 32-bit key: 12, 12 and 8 bits.
+__device__ __forceinline__ int level_shift(int l) { return l == 0 ? 20 : (l == 1 ? 8 : 0); }
+__device__ __forceinline__ int level_bins(int l) { return l == 2 ? 256 : kTopkBins; }
+
+constexpr int kBinsPerThread = kTopkBins / kCutThreads;  // 16
+
+// Descending bucket search.  Thread t holds the counts of bins top - r,
+// r < kBinsPerThread, in h[r] (top = nbins - 1 - kBinsPerThread t; bins below
+// 0 hold 0).  Finds the bin holding the rem-th largest key and the rank left
+// within it: whole block (kCutThreads); writes S.tb, S.rem, S.nb.
+__device__ void find_bucket(CutSmem& S, const uint32_t (&h)[kBinsPerThread], int top, uint32_t rem) {
+  if (threadIdx.x == 0) {
+    S.tb = 0u;
+    S.rem = 0u;
+    S.nb = 0u;
+  }
+  uint32_t sum = 0;
+#pragma unroll
+  for (int r = 0; r < kBinsPerThread; ++r) sum += h[r];
+  uint32_t ex = block_excl_scan(sum, S.warp_tot, &S.tot);
+#pragma unroll
+  for (int r = 0; r < kBinsPerThread; ++r) {
+    if (ex < rem && rem <= ex + h[r]) {
+      S.tb = (uint32_t)(top - r);
+      S.rem = rem - ex;
+      S.nb = h[r];
+    }
+    ex += h[r];
+  }
+  __syncthreads();
+}
+
+// The counts of this thread's bins (descending) from a histogram whose bins
+// [0, nbins) are 16-byte aligned words.
+__device__ __forceinline__ int bins_of_thread(const uint32_t* hist, int nbins, uint32_t (&h)[kBinsPerThread]) {
+  const int top = nbins - 1 - kBinsPerThread * (int)threadIdx.x;
+  const int base = top - (kBinsPerThread - 1);
+  if (base < 0) {
+#pragma unroll
+    for (int r = 0; r < kBinsPerThread; ++r) h[r] = 0u;
+    return top;
+  }
+  const uint4* p = reinterpret_cast<const uint4*>(hist + base);
+#pragma unroll
+  for (int i = 0; i < kBinsPerThread / 4; ++i) {
+    const uint4 v = p[i];
+    h[kBinsPerThread - 1 - 4 * i] = v.x;
+    h[kBinsPerThread - 2 - 4 * i] = v.y;
+    h[kBinsPerThread - 3 - 4 * i] = v.z;
+    h[kBinsPerThread - 4 - 4 * i] = v.w;
+  }
+  return top;
+}
+
+// Rank S.cand[0..nc) by value and set S.cut to the rem-th largest.  S.cand is
+// zero-padded to an even count (0 ranks below every candidate).
+__device__ __forceinline__ void rank_cut(CutSmem& S, int nc, uint32_t rem) {
+  const int nc2 = (nc + 1) & ~1;
+  for (int e = threadIdx.x; e < nc; e += blockDim.x) {
+    const unsigned long long mine = S.cand[e];
+    uint32_t r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+    int j = 0;
+    for (; j + 4 <= nc2; j += 4) {
+      const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(&S.cand[j]);
+      const ulonglong2 b = *reinterpret_cast<const ulonglong2*>(&S.cand[j + 2]);
+      r0 += a.x > mine;
+      r1 += a.y > mine;
+      r2 += b.x > mine;
+      r3 += b.y > mine;
+    }
+    for (; j < nc2; ++j) r0 += S.cand[j] > mine;
+    if (r0 + r1 + r2 + r3 + 1 == rem) S.cut = mine;
+  }
+}
+
+// The cut of a row whose level-0 bucket (S.tb, S.nb keys) holds more than
+// kRankCap keys, by one CTA streaming the row's middle keys.
+__device__ void cut_refine(CutSmem& S, const float* __restrict__ sc, int64_t lo, int64_t cnt, uint32_t rem) {
   const int tid = threadIdx.x;
-
-  if (tid == 0) {
-    S.n_cand = 0;
-    S.n_sel = 0;
+  uint32_t prefix = S.tb;
+  int lvl = 0;
+  while (lvl < 2 && S.nb > (uint32_t)kRankCap) {
+    const int nl = lvl + 1, pre_sh = level_shift(lvl), sh = level_shift(nl);
+    const uint32_t bmask = (uint32_t)level_bins(nl) - 1u;
+    __syncthreads();  // every thread has read S.nb
+    for (int b = tid; b < kTopkBins; b += blockDim.x) S.hist[b] = 0u;
+    __syncthreads();
+    for_row_keys(sc, lo, 0, cnt, [&](int64_t, uint32_t key) {
+      if ((key >> pre_sh) == prefix) atomicAdd(&S.hist[(key >> sh) & bmask], 1u);
+    });
+    __syncthreads();
+    uint32_t h[kBinsPerThread];
+    const int top = bins_of_thread(S.hist, level_bins(nl), h);
+    find_bucket(S, h, top, rem);
+    rem = S.rem;
+    prefix = (prefix << (nl == 1 ? 12 : 8)) | S.tb;
+    lvl = nl;
   }
-  __syncthreads();
-  // fixed tokens
-  for (int64_t i = tid; i < lo; i += kSelThreads) sel_push(S, (int32_t)i);
-  for (int64_t i = hi + tid; i < n; i += kSelThreads) sel_push(S, (int32_t)i);
-
-  if (cnt <= n_top) {
-    for (int64_t i = lo + tid; i < hi; i += kSelThreads) sel_push(S, (int32_t)i);
-  } else if (n_top > 0) {
-    const bool staged = cnt <= kStageKeys;
-    // key range of the candidates (staging them when they fit)
-    uint32_t klo = 0xFFFFFFFFu, khi = 0u;
-    if (staged) {
-      for (int e0 = tid; e0 < cnt; e0 += kSelBatch * kSelThreads) {
-        float v[kSelBatch];
-#pragma unroll
-        for (int b = 0; b < kSelBatch; ++b) {
-          const int e = e0 + b * kSelThreads;
-          v[b] = e < cnt ? sc[lo + e] : 0.f;
-        }
-#pragma unroll
-        for (int b = 0; b < kSelBatch; ++b) {
-          const int e = e0 + b * kSelThreads;
-          if (e < cnt) {
-            const uint32_t k = ordered_key(v[b]);
-            S.keys[e] = k;
-            klo = min(klo, k);
-            khi = max(khi, k);
-          }
-        }
+  const int sh = level_shift(lvl);
+  if (S.nb <= (uint32_t)kRankCap) {
+    if (tid == 0) S.n_cand = 0;
+    __syncthreads();
+    for_row_keys(sc, lo, 0, cnt, [&](int64_t e, uint32_t key) {
+      if ((key >> sh) == prefix) {
+        const uint32_t c = atomicAdd(&S.n_cand, 1u);
+        if (c < (uint32_t)kRankCap)
+          S.cand[c] = ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)(lo + e));
       }
-    } else {
-      for_keys(S, false, sc, lo, cnt, [&](int64_t, uint32_t k) {
-        klo = min(klo, k);
-        khi = max(khi, k);
-      });
-    }
-    block_range(klo, khi, S);
-    // Threshold bucket: a linear histogram over the active key range [klo, khi]
-    // locates the bucket holding the rem-th largest active key; a crowded
-    // bucket becomes the next active range (its exact min and max keys).
-    uint32_t rem = (uint32_t)n_top, b_lo = klo, b_hi = khi, bucket_n = 0;
-    int tb_final = -1;
-    float scale_final = 0.f;
-    for (int lvl = 0; lvl < 3; ++lvl) {
-      const float scale = (float)kHistBins / ((float)(khi - klo) + 1.f);
-      auto bin_of = [&](uint32_t k) { return min((int)((float)(k - klo) * scale), kHistBins - 1); };
-      for (int b = tid; b < kHistBins; b += kSelThreads) S.hist[b] = 0;
-      __syncthreads();
-      for_keys(S, staged, sc, lo, cnt, [&](int64_t, uint32_t k) {
-        if (k >= klo && k <= khi) atomicAdd(&S.hist[bin_of(k)], 1u);
-      });
-      __syncthreads();
-      // thread t owns bins 2047 - 2t and 2046 - 2t (descending); block scan
-      const uint32_t h0 = S.hist[kHistBins - 1 - 2 * tid], h1 = S.hist[kHistBins - 2 - 2 * tid];
-      const uint32_t ex = block_excl_scan(h0 + h1, S.warp_tot, &S.tot);
-      if (ex < rem && rem <= ex + h0) {
-        S.tb = kHistBins - 1 - 2 * tid;
-        S.rem = rem - ex;
-      } else if (ex + h0 < rem && rem <= ex + h0 + h1) {
-        S.tb = kHistBins - 2 - 2 * tid;
-        S.rem = rem - ex - h0;
-      }
-      __syncthreads();
-      const int tb = (int)S.tb;
-      rem = S.rem;
-      bucket_n = S.hist[tb];
-      if (bucket_n <= (uint32_t)kCandCap) {
-        // small bucket: keys are classified by their bin under this level's map
-        tb_final = tb;
-        scale_final = scale;
-        break;
-      }
-      // crowded bucket: its exact key range becomes the next level's range
-      uint32_t blo = 0xFFFFFFFFu, bhi = 0u;
-      for_keys(S, staged, sc, lo, cnt, [&](int64_t, uint32_t k) {
-        if (k >= klo && k <= khi && bin_of(k) == tb) {
-          blo = min(blo, k);
-          bhi = max(bhi, k);
-        }
-      });
-      block_range(blo, bhi, S);
-      b_lo = blo;
-      b_hi = bhi;
-      if (b_lo == b_hi) break;
-      klo = b_lo;
-      khi = b_hi;
-    }
-    if (tb_final >= 0) {
-      // keys in higher bins are selected; the bucket's keys are ranked exactly
-      const uint32_t klo_f = klo, khi_f = khi;
-      auto bin_f = [&](uint32_t k) { return min((int)((float)(k - klo_f) * scale_final), kHistBins - 1); };
-      for_keys(S, staged, sc, lo, cnt, [&](int64_t e, uint32_t k) {
-        if (k < klo_f || k > khi_f) {
-          if (k > khi_f) sel_push(S, (int32_t)(lo + e));
-          return;
-        }
-        const int b = bin_f(k);
-        if (b > tb_final) {
-          sel_push(S, (int32_t)(lo + e));
-        } else if (b == tb_final) {
-          const uint32_t c = atomicAdd(&S.n_cand, 1u);
-          if (c < (uint32_t)kCandCap)
-            S.cand[c] = ((unsigned long long)k << 32) | (0xFFFFFFFFu - (uint32_t)(lo + e));
-        }
-      });
-      __syncthreads();
-      const int nc = (int)min(S.n_cand, (uint32_t)kCandCap);
-      if (nc <= kSelThreads) {
-        // rank of each candidate among the bucket (distinct entries): no barriers
-        if (tid < nc) {
-          const unsigned long long mine = S.cand[tid];
-          int rank = 0;
-          for (int j = 0; j < nc; ++j) rank += S.cand[j] > mine;
-          if (rank < (int)rem) sel_push(S, (int32_t)(0xFFFFFFFFu - (uint32_t)mine));
-        }
-      } else {
-        const int nc2 = pow2_at_least(nc);
-        for (int e = nc + tid; e < nc2; e += kSelThreads) S.cand[e] = 0ull;
-        __syncthreads();
-        block_bitonic(S.cand, nc2, true);
-        for (int e = tid; e < (int)rem && e < nc; e += kSelThreads)
-          sel_push(S, (int32_t)(0xFFFFFFFFu - (uint32_t)S.cand[e]));
-      }
-    } else {
-      // more than kCandCap keys equal the threshold key (b_lo == b_hi): take
-      // the rem of them with the lowest indices by an ordered scan
-      uint32_t carry = 0;
-      for (int64_t base = 0; base < cnt; base += kSelThreads) {
-        const int64_t e = base + tid;
-        uint32_t tie = 0;
-        if (e < cnt) {
-          const uint32_t k = staged ? S.keys[e] : ordered_key(sc[lo + e]);
-          if (k > b_hi) sel_push(S, (int32_t)(lo + e));
-          else if (k == b_lo) tie = 1;
-        }
-        const uint32_t ex = block_excl_scan(tie, S.warp_tot, &S.tot) + carry;
-        if (tie && ex < rem) sel_push(S, (int32_t)(lo + e));
-        carry += S.tot;
-        __syncthreads();
-      }
-    }
-  }
-  __syncthreads();
-  const int ns = (int)S.n_sel;
-  if (ns > a.k && tid == 0) set_status(a.status, BPKV_DEV_SELECT);
-  const int cnt_out = min(ns, a.k);
-  if (cnt_out <= kSelThreads) {
-    // ascending order by rank (the indices are distinct): no barriers
-    if (tid < cnt_out) {
-      const int32_t mine = S.sel[tid];
-      int rank = 0;
-      for (int j = 0; j < cnt_out; ++j) rank += S.sel[j] < mine;
-      out[rank] = mine;
-    }
-    for (int e = cnt_out + tid; e < a.k; e += kSelThreads) out[e] = -1;
+    });
+    __syncthreads();
+    const int nc = (int)min(S.n_cand, (uint32_t)kRankCap);
+    if (tid == 0) S.cand[nc] = 0ull;
+    __syncthreads();
+    rank_cut(S, nc, rem);
     return;
   }
-  const int n2 = pow2_at_least(max(cnt_out, 2));
-  for (int e = cnt_out + tid; e < n2; e += kSelThreads) S.sel[e] = 0x7FFFFFFF;
-  __syncthreads();
-  block_bitonic(S.sel, n2, false);
-  for (int e = tid; e < a.k; e += kSelThreads) out[e] = e < cnt_out ? S.sel[e] : -1;
+  // a single key value tk repeated more than kRankCap times: its rem-th
+  // occurrence in index order, 16 consecutive keys per thread
+  const uint32_t tk = prefix;
+  constexpr int kSeg = 16;
+  uint32_t carry = 0;
+  for (int64_t base = 0; base < cnt && carry < rem; base += (int64_t)kSeg * blockDim.x) {
+    const int64_t e0 = base + (int64_t)tid * kSeg;
+    uint32_t c = 0;
+#pragma unroll
+    for (int j = 0; j < kSeg; ++j)
+      if (e0 + j < cnt && ordered_key(sc[lo + e0 + j]) == tk) ++c;
+    const uint32_t ex = block_excl_scan(c, S.warp_tot, &S.tot) + carry;
+    if (ex < rem && rem <= ex + c) {
+      uint32_t need = rem - ex;
+      for (int j = 0; j < kSeg && e0 + j < cnt; ++j) {
+        if (ordered_key(sc[lo + e0 + j]) == tk && --need == 0) {
+          S.cut = ((unsigned long long)tk << 32) | (0xFFFFFFFFu - (uint32_t)(lo + e0 + j));
+          break;
+        }
+      }
+    }
+    carry += S.tot;
+  }
 }
 
-cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
-                        int32_t n_recent, int32_t* idx, int32_t* status, cudaStream_t st) {
-  TopkArgs a{scores, ld, c.seq_len, idx, status, c.n_kv_heads, c.group, k, n_sink, n_recent};
-  const int smem = (int)sizeof(TopkSmem);
-  cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+// Wait until `count` CTAs have arrived at *bar (thread 0 of each CTA arrives
+// once); bounded, records BPKV_DEV_TIMEOUT if it gives up.  Whole block.
+__device__ __forceinline__ void row_barrier(uint32_t* bar, uint32_t count, int32_t* status) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(bar, 1u);
+    uint32_t it = 0;
+    while (*reinterpret_cast<volatile uint32_t*>(bar) < count) {
+      if (++it > kSpinLimit) {
+        set_status(status, BPKV_DEV_TIMEOUT);
+        break;
+      }
+      __nanosleep(100);
+    }
+    __threadfence();
+  }
+  __syncthreads();
+}
+
+// Grid (chunks of kCutChunk middle keys, rows).  Each thread holds
+// kCutChunk / kCutThreads keys of its CTA's chunk in registers throughout.
+__global__ void __launch_bounds__(kCutThreads, 2) k_cut(CutArgs a) {
+  pdl_enter();
+  __shared__ CutSmem S;
+  const int row = blockIdx.y, tid = threadIdx.x, lane = tid & 31;
+  static_assert(kCutChunk == kSelBatch * kCutThreads, "one batch of loads per thread");
+  uint32_t h[kBinsPerThread];
+  int top = 0;
+  if (!a.build_hist) top = bins_of_thread(a.hist + (int64_t)row * kTopkBins, kTopkBins, h);  // before seq_len
+  const RowRange r = row_range(a.seq_len[row / a.rows_per_seq], a.k, a.n_sink, a.n_recent);
+  if (r.cnt <= r.m || r.m == 0) {
+    // every middle key, or none
+    if (blockIdx.x == 0 && tid == 0) a.cut[row] = r.cnt <= r.m ? 0ull : ~0ull;
+    return;
+  }
+  const float* sc = a.scores + (int64_t)row * a.ld;
+  uint32_t* ctr = a.ctr + (int64_t)kSelCounters * row;
+  unsigned long long* cand = a.cand + (int64_t)row * kRankCap;
+  // this CTA's keys, all loads in flight
+  const int64_t c0 = (int64_t)blockIdx.x * kCutChunk, c1 = min64(c0 + kCutChunk, r.cnt);
+  uint32_t keys[kSelBatch], valid = 0;
+  if (c0 < c1) {
+    float v[kSelBatch];
+#pragma unroll
+    for (int b = 0; b < kSelBatch; ++b) v[b] = sc[r.lo + min64(c0 + tid + (int64_t)b * kCutThreads, c1 - 1)];
+#pragma unroll
+    for (int b = 0; b < kSelBatch; ++b) {
+      keys[b] = ordered_key(v[b]);
+      if (c0 + tid + (int64_t)b * kCutThreads < c1) valid |= 1u << b;
+    }
+  }
+  if (a.build_hist) {
+    // level-0 histogram: counted per CTA in shared memory, added to the row's
+    // with one atomic per non-empty bin, then every CTA of the row waits for
+    // the others (the grid is launched cooperatively)
+    for (int b = tid; b < kTopkBins; b += kCutThreads) S.hist[b] = 0u;
+    __syncthreads();
+#pragma unroll
+    for (int b = 0; b < kSelBatch; ++b)
+      if ((valid >> b) & 1u) atomicAdd(&S.hist[keys[b] >> 20], 1u);
+    __syncthreads();
+    uint32_t* gh = a.hist + (int64_t)row * kTopkBins;
+    for (int b = tid; b < kTopkBins; b += kCutThreads)
+      if (S.hist[b]) atomicAdd(gh + b, S.hist[b]);
+    row_barrier(ctr + 2, gridDim.x, a.status);
+    top = bins_of_thread(reinterpret_cast<const uint32_t*>(gh), kTopkBins, h);
+  }
+  if (tid == 0) S.cut = ~0ull;
+  find_bucket(S, h, top, (uint32_t)r.m);
+  const uint32_t tb = S.tb, nb = S.nb, rem = S.rem;
+  if (nb <= (uint32_t)kRankCap) {
+    // this CTA's bucket keys: one returning atomic per warp for the warp's matches
+    uint32_t match = 0;
+#pragma unroll
+    for (int b = 0; b < kSelBatch; ++b)
+      if (((valid >> b) & 1u) && (keys[b] >> 20) == tb) match |= 1u << b;
+    const uint32_t cnt = __popc(match);
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const uint32_t warp_total = __shfl_sync(0xffffffffu, incl, 31);
+    uint32_t base = 0;
+    if (lane == 31 && warp_total) base = atomicAdd(ctr, warp_total);
+    base = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
+#pragma unroll
+    for (int b = 0; b < kSelBatch; ++b) {
+      if ((match >> b) & 1u) {
+        if (base < (uint32_t)kRankCap)
+          cand[base] = ((unsigned long long)keys[b] << 32) |
+                       (0xFFFFFFFFu - (uint32_t)(r.lo + c0 + tid + (int64_t)b * kCutThreads));
+        ++base;
+      }
+    }
+  }
+  // the last CTA of the row to finish decides the cut (the barrier orders the
+  // CTA's writes before thread 0's cumulative fence)
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    S.is_last = (atomicAdd(ctr + 1, 1u) == gridDim.x - 1) ? 1u : 0u;
+    if (S.is_last) __threadfence();
+  }
+  __syncthreads();
+  if (!S.is_last) return;
+  if (nb <= (uint32_t)kRankCap) {
+    const int nc = (int)min(__ldcg(ctr), (uint32_t)kRankCap);
+    for (int e = tid; e < nc; e += kCutThreads) S.cand[e] = __ldcg(cand + e);
+    if (tid == 0) S.cand[nc] = 0ull;
+    __syncthreads();
+    rank_cut(S, nc, rem);
+  } else {
+    // refine in the shared histogram buffer
+    if (tid == 0) {
+      S.nb = nb;
+      S.tb = tb;
+    }
+    __syncthreads();
+    cut_refine(S, sc, r.lo, r.cnt, rem);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    a.cut[row] = S.cut;
+    if (S.cut == ~0ull) set_status(a.status, BPKV_DEV_SELECT);  // histogram and keys disagree
+#pragma unroll
+    for (int i = 0; i < kSelCounters; ++i) ctr[i] = 0u;  // every CTA of the row is past its waits
+  }
+}
+
+// ------------------------------------------------------------------ k_lists
+
+struct ListArgs {
+  const float* scores;
+  int64_t ld;
+  const int64_t* seq_len;
+  const unsigned long long* cut;
+  int32_t* idx;  // [rows][k]
+  int32_t* status;
+  int32_t rows_per_seq, k, n_sink, n_recent;
+};
+
+struct ListSmem {
+  uint32_t keys[kTileKeys];
+  uint32_t warp_tot[32];
+  uint32_t tot;
+};
+
+// Index lists from the cuts: sinks, the chosen middle tokens, the recent
+// tokens, ascending, -1 padded.  One CTA (kSelThreads) per row.
+__global__ void __launch_bounds__(kSelThreads) k_lists(ListArgs a) {
+  pdl_enter();
+  extern __shared__ __align__(16) unsigned char list_raw[];
+  ListSmem& S = *reinterpret_cast<ListSmem*>(list_raw);
+  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+  const RowRange r = row_range(a.seq_len[row / a.rows_per_seq], a.k, a.n_sink, a.n_recent);
+  const float* sc = a.scores + (int64_t)row * a.ld;
+  int32_t* out = a.idx + (int64_t)row * a.k;
+  const int64_t n_mid = r.cnt <= r.m ? r.cnt : r.m;
+  for (int64_t i = tid; i < r.lo; i += kSelThreads) out[i] = (int32_t)i;
+  for (int64_t e = tid; e < r.n - r.hi; e += kSelThreads) out[r.lo + n_mid + e] = (int32_t)(r.hi + e);
+  for (int64_t e = r.lo + n_mid + (r.n - r.hi) + tid; e < a.k; e += kSelThreads) out[e] = -1;
+  if (r.cnt <= r.m) {
+    for (int64_t e = tid; e < r.cnt; e += kSelThreads) out[r.lo + e] = (int32_t)(r.lo + e);
+    return;
+  }
+  if (r.m == 0) return;
+  const unsigned long long cut = a.cut[row];
+  const uint32_t ck = (uint32_t)(cut >> 32), ci = 0xFFFFFFFFu - (uint32_t)cut;
+  uint32_t carry = 0;
+  for (int64_t t0 = 0; t0 < r.cnt; t0 += kTileKeys) {
+    const int len = (int)min64(kTileKeys, r.cnt - t0);
+    __syncthreads();  // the previous tile's readers are done
+    for_row_keys(sc, r.lo + t0, 0, len, [&](int64_t e, uint32_t key) { S.keys[e] = key; });
+    __syncthreads();
+    // thread = segment of seg consecutive keys, read rotated by lane (no bank conflicts)
+    const int seg = (len + kSelThreads - 1) / kSelThreads, start = tid * seg;
+    uint32_t mask = 0;
+    for (int j = 0; j < seg; ++j) {
+      int jj = j + lane % seg;
+      if (jj >= seg) jj -= seg;
+      const int e = start + jj;
+      if (e < len) {
+        const uint32_t key = S.keys[e];
+        const uint32_t i = (uint32_t)(r.lo + t0 + e);
+        if (key > ck || (key == ck && i <= ci)) mask |= 1u << jj;
+      }
+    }
+    const uint32_t ex = block_excl_scan((uint32_t)__popc(mask), S.warp_tot, &S.tot) + carry;
+    int32_t* o = out + r.lo + ex;
+    int64_t room = n_mid - ex;
+    while (mask && room-- > 0) {
+      const int b = __ffs(mask) - 1;
+      mask &= mask - 1u;
+      *o++ = (int32_t)(r.lo + t0 + start + b);
+    }
+    carry += S.tot;
+  }
+  if (carry != (uint32_t)n_mid) {
+    if (tid == 0) set_status(a.status, BPKV_DEV_SELECT);
+    for (int64_t e = min64(carry, n_mid) + tid; e < n_mid; e += kSelThreads) out[r.lo + e] = -1;
+  }
+}
+
+// ------------------------------------------------------------------ launchers
+
+int64_t cut_chunks(const bpkv_cache& c) {
+  const int64_t ch = (c.n_max + kCutChunk - 1) / kCutChunk;
+  return ch < 1 ? 1 : ch;
+}
+
+size_t cut_scratch_bytes(const bpkv_cache& c) {
+  const size_t rows = (size_t)c.n_seq * c.n_kv_heads * c.group;
+  return rows * ((size_t)kRankCap * 8 + kSelCounters * 4 + 8);
+}
+
+cudaError_t launch_hist(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
+                        int32_t n_recent, uint32_t* hist, cudaStream_t st) {
+  HistArgs a{scores, ld, c.seq_len, hist, c.n_kv_heads * c.group, k, n_sink, n_recent};
+  const dim3 grid((unsigned)cut_chunks(c), (unsigned)(c.n_seq * c.n_kv_heads * c.group));
+  return launch_pdl(k_hist, grid, dim3(kCutThreads), 0, st, a);
+}
+
+// Whether the cut kernel can count the level-0 histograms itself: its whole
+// grid must be resident at once (cooperative launch).
+bool cut_counts_hist(const bpkv_cache& c) {
+  constexpr int kDevs = 64;
+  static int slots[kDevs] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return false;
+  int n = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (slots[dev] == 0) {
+      int sms = 0, per_sm = 0, coop = 0;
+      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+      if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop) return false;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_cut, kCutThreads, 0) != cudaSuccess) return false;
+      slots[dev] = sms * per_sm > 0 ? sms * per_sm : -1;
+    }
+    n = slots[dev];
+  }
+  const int64_t grid = cut_chunks(c) * (int64_t)c.n_seq * c.n_kv_heads * c.group;
+  return n > 0 && grid <= n;
+}
+
+cudaError_t launch_cut(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
+                       int32_t n_recent, const SelBufs& b, bool build_hist, int32_t* status, cudaStream_t st) {
+  CutArgs a{scores, ld, c.seq_len, b.hist, b.cand, b.ctr, b.cut, status, c.n_kv_heads * c.group, k, n_sink, n_recent,
+            build_hist ? 1 : 0};
+  const dim3 grid((unsigned)cut_chunks(c), (unsigned)(c.n_seq * c.n_kv_heads * c.group));
+  if (build_hist) return launch_coop_pdl(k_cut, grid, dim3(kCutThreads), 0, st, a);
+  return launch_pdl(k_cut, grid, dim3(kCutThreads), 0, st, a);
+}
+
+cudaError_t launch_lists(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
+                         int32_t n_recent, const unsigned long long* cut, int32_t* idx, int32_t* status,
+                         cudaStream_t st) {
+  ListArgs a{scores, ld, c.seq_len, cut, idx, status, c.n_kv_heads * c.group, k, n_sink, n_recent};
+  const int smem = (int)sizeof(ListSmem);
+  cudaError_t e = cudaFuncSetAttribute(k_lists, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_topk, dim3(c.n_seq * c.n_kv_heads * c.group), dim3(kSelThreads), smem, st, a);
+  return launch_pdl(k_lists, dim3(c.n_seq * c.n_kv_heads * c.group), dim3(kSelThreads), smem, st, a);
+}
+
+// Top-k of every row: the cuts into b.cut and, when idx is given, the index
+// lists.  Histograms still to be counted are counted by the cut kernel itself
+// (cooperative launch) or, when its grid cannot be resident at once, by k_hist
+// first.
+cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
+                        int32_t n_recent, const SelBufs& b, HistState hs, int32_t* idx, int32_t* status,
+                        cudaStream_t st) {
+  cudaError_t e;
+  bool build = false;
+  if (hs == HistState::kDirty) {
+    const size_t rows = (size_t)c.n_seq * c.n_kv_heads * c.group;
+    e = cudaMemsetAsync(b.hist, 0, rows * (kTopkBins + kSelCounters) * sizeof(uint32_t), st);
+    if (e != cudaSuccess) return e;
+  }
+  if (hs != HistState::kCounted) {
+    build = cut_counts_hist(c);
+    if (!build) {
+      e = launch_hist(c, scores, ld, k, n_sink, n_recent, b.hist, st);
+      if (e != cudaSuccess) return e;
+    }
+  }
+  e = launch_cut(c, scores, ld, k, n_sink, n_recent, b, build, status, st);
+  if (e != cudaSuccess || !idx) return e;
+  return launch_lists(c, scores, ld, k, n_sink, n_recent, b.cut, idx, status, st);
 }
 
 // ---------------------------------------------------------------- union

@@ -52,6 +52,7 @@ extern "C" {
 /* device status word bits (bpkv_read_status) */
 #define BPKV_DEV_OVERFLOW 1    /* append would pass cap_tokens; nothing written */
 #define BPKV_DEV_SELECT 2      /* a selection produced more rows than its output holds */
+#define BPKV_DEV_TIMEOUT 4     /* a wait inside a kernel for the other CTAs of its grid gave up */
 
 #define BPKV_MAX_GROUP 8
 #define BPKV_HEAD_DIM 128
@@ -177,7 +178,9 @@ int bpkv_scan(const bpkv_cache *c, const float *q, const uint8_t *depths, float 
 int bpkv_topk(const bpkv_cache *c, const float *scores, int64_t ld_scores, int32_t k, int32_t n_sink,
               int32_t n_recent, int32_t *idx, void *ws, size_t ws_bytes, void *stream);
 
-/* bpkv_scan into the workspace followed by bpkv_topk. */
+/* bpkv_scan into the workspace followed by bpkv_topk.  The scan also counts
+ * each row's first-level selection histogram into the workspace (cleared by an
+ * enqueued memset first), which the top-k then reads instead of counting it. */
 int bpkv_scan_topk(const bpkv_cache *c, const float *q, const uint8_t *depths, int32_t k, int32_t n_sink,
                    int32_t n_recent, int32_t *idx, void *ws, size_t ws_bytes, void *stream);
 
@@ -187,11 +190,13 @@ int bpkv_scan_topk(const bpkv_cache *c, const float *q, const uint8_t *depths, i
  * GPU's memory, or a loop that must not pay the device-wide synchronisation a
  * cudaMalloc/cudaFree can cause.  The Fathom page has no counterpart of this
  * call; its results are identical to bpkv_scan_topk's.
- * The score scratch is a fixed 16 MiB array built into the library, held on
- * every GPU that loads the library until the process exits; requests needing
- * more (N * H * G * round_up(n_max, 64) * 4 bytes > 16 MiB) return
- * BPKV_ENOWORKSPACE.  The call allocates nothing (no cudaMalloc, cudaFree or
- * allocating library routine).  Its first call on a device looks up the
+ * The scratch (scores and selection buffers) is a fixed 16 MiB array built
+ * into the library, held on every GPU that loads the library until the
+ * process exits; requests needing more (rows = N * H * G; rows *
+ * (4 * round_up(n_max, 64) + 24600) bytes plus under 1 KiB of alignment
+ * > 16 MiB) return BPKV_ENOWORKSPACE.  The call allocates nothing (no
+ * cudaMalloc, cudaFree or allocating library routine); it enqueues a memset of
+ * the selection counters.  Its first call on a device looks up the
  * array's device address once (with that device current); make that first
  * call before any stream capture.  All calls on a device share the one array,
  * so calls whose work overlaps on the GPU (other streams, other threads) race

@@ -77,10 +77,12 @@ def check_topk_sets(gpu_idx: np.ndarray, ref_idx: np.ndarray, ref_score: np.ndar
     return len(diff)
 
 
-def decode_one_layer(inp, cfg, depth_rule=0, fixed=(0, 0), budgets=None, residency="hbm", dev="cuda", flags=0):
+def decode_one_layer(inp, cfg, depth_rule=0, fixed=(0, 0), budgets=None, residency="hbm", dev="cuda", flags=0,
+                     lists=True):
     """Prefill n-1 tokens of a generated layer, then one bpkv_decode_step (appends
     token n-1 and runs the whole path).  Returns (cache, depths, idx, out) with
-    depths [N][H][D], idx [N][H][G][k], out [N][H][G][D] on the device."""
+    depths [N][H][D], idx [N][H][G][k], out [N][H][G][D] on the device; with
+    lists=False the step writes no index lists (idx stays zero)."""
     import bit_plane_kv_encode_gb300 as pk
     N, H, n, D = inp.k.shape
     G = cfg.group
@@ -98,7 +100,7 @@ def decode_one_layer(inp, cfg, depth_rule=0, fixed=(0, 0), budgets=None, residen
     v_new = v_all[:, :, n - 1][None].contiguous()
     a = pk.bpkv_step_args(k_new.data_ptr(), v_new.data_ptr(), q.data_ptr(), sigma2.data_ptr(), budget_q.data_ptr(),
                           depth_rule, fixed[0], fixed[1], cfg.k, cfg.n_sink, cfg.n_recent, out.data_ptr(),
-                          depths.data_ptr(), idx.data_ptr(), None, flags)
+                          depths.data_ptr(), idx.data_ptr() if lists else None, None, flags)
     arr = pk.cache_array([cache])
     pk.bpkv_clear_status(ws)
     pk.bpkv_decode_step(arr, 1, a, ws, ws.numel())

@@ -136,3 +136,23 @@ def test_tail_matches_split(pk, wl, n_tok, budget):
     assert torch.equal(r_t[1], r_s[1])
     assert torch.equal(r_t[2], r_s[2])
     assert torch.max(torch.abs(r_t[3] - r_s[3])).item() < 1e-4
+
+
+@pytest.mark.parametrize("wl,n_tok,rule,fixed,budget", [("qwen3_8b_layer", 32768, 0, (0, 0), 92),
+                                                        ("full_step", 131072, 1, (32, 4), None),
+                                                        ("multi_session", 65536, 0, (0, 0), None),
+                                                        ("qwen3_8b_layer", 20000 + 13, 1, (1, 1), None),
+                                                        ("tiny", 4096, 0, (0, 0), 0),
+                                                        ("tiny", 37, 0, (0, 0), 136)])
+def test_step_without_lists_matches(pk, wl, n_tok, rule, fixed, budget):
+    """A step that writes no index lists (the attention reads only the selection
+    cuts) gives bit-identical outputs to one that writes them."""
+    from workload import CONFIGS, gen_layer
+    cfg = CONFIGS[wl]
+    inp = gen_layer(cfg, 5, device="cuda", n_tokens=n_tok, n_seq=min(cfg.n_seq, 4))
+    b = None if budget is None else torch.full((inp.k.shape[0],), budget, dtype=torch.int32)
+    r_l = decode_one_layer(inp, cfg, depth_rule=rule, fixed=fixed, budgets=b, lists=True)
+    r_n = decode_one_layer(inp, cfg, depth_rule=rule, fixed=fixed, budgets=b, lists=False)
+    assert torch.equal(r_l[1], r_n[1])
+    assert torch.equal(r_l[3], r_n[3])
+    assert (r_n[2] == 0).all()  # no lists were written

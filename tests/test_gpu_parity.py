@@ -269,3 +269,77 @@ def test_topk_massive_ties(pk, orc, n_ties, n_above):
     for q in range(G):
         want = orc.topk(sc[0, 0, q].numpy().astype(np.float64), k)
         assert np.array_equal(idx[0, 0, q].cpu().numpy(), want), q
+
+
+def _topk_rows(pk, c, sc, k, n_sink=4, n_recent=32):
+    """bpkv_topk on given scores [N][H][G][n] (the kernel counts its own histogram)."""
+    N, H, G, n = sc.shape
+    ld = c.c.cap_tokens
+    buf = torch.zeros((N, H, G, ld), device="cuda")
+    buf[..., :n] = sc.cuda()
+    idx = torch.zeros((N, H, G, k), dtype=torch.int32, device="cuda")
+    ws = c.workspace(k, pk.WS_SCAN_TOPK)
+    pk.bpkv_clear_status(ws)
+    pk.bpkv_topk(c.c, buf, ld, k, n_sink, n_recent, idx, ws, ws.numel())
+    assert pk.bpkv_read_status(ws) == 0
+    return idx.cpu().numpy()
+
+
+@pytest.mark.parametrize("n,k,ties", [(70000, 512, 0.3), (100003, 2048, 0.0), (32772, 512, 0.0),
+                                      (32805, 100, 0.95)])
+def test_topk_long_rows(pk, orc, n, k, ties):
+    """Rows longer than one staged tile of 32768 keys: every pass runs tile by tile."""
+    from workload.gen import random_scores
+    N, H, G = 1, 1, 2
+    kk, vv = _rand_kv(N, H, n, seed=11)
+    c = build_cache(kk, vv, G)
+    sc = random_scores(N * H * G, n, seed=n + 7 * k, tie_frac=ties).reshape(N, H, G, n)
+    got = _topk_rows(pk, c, sc, k)
+    for g in range(G):
+        want = orc.topk(sc[0, 0, g].numpy().astype(np.float64), k)
+        assert np.array_equal(got[0, 0, g], want), g
+
+
+@pytest.mark.parametrize("n,spread", [(20000, 3000), (20000, 40), (70000, 0), (20000, 0), (50000, 200000)])
+def test_topk_refinement_levels(pk, orc, n, spread):
+    """Scores packed into a few ulps of 1.0: the first-level bucket holds most
+    keys, so the second and third radix levels (and, at spread 0 or with long
+    runs of equal keys, the ordered tie cut) decide the set."""
+    N, H, G, k = 1, 1, 2, 512
+    kk, vv = _rand_kv(N, H, n, seed=12)
+    c = build_cache(kk, vv, G)
+    g = torch.Generator(device="cpu").manual_seed(n + spread)
+    steps = torch.randint(0, max(spread, 1), (N, H, G, n), generator=g) if spread else torch.zeros(
+        (N, H, G, n), dtype=torch.int64)
+    sc = (1.0 + steps.double() * 2.0 ** -23).float()
+    got = _topk_rows(pk, c, sc, k)
+    for q in range(G):
+        want = orc.topk(sc[0, 0, q].numpy().astype(np.float64), k)
+        assert np.array_equal(got[0, 0, q], want), q
+
+
+@pytest.mark.parametrize("n,G,budget", [(3000, 4, 136), (40000, 2, 92), (700, 8, 68), (37, 4, 136)])
+def test_scan_topk_histogram_matches_topk(pk, n, G, budget):
+    """bpkv_scan_topk (histogram counted by the scan) gives the same indices as
+    bpkv_scan followed by bpkv_topk (histogram counted by the top-k kernel)."""
+    N, H, k = 2, 2, 256
+    kk, vv = _rand_kv(N, H, n, seed=13)
+    c = build_cache(kk, vv, G)
+    gq = torch.Generator(device="cpu").manual_seed(n + G)
+    q = torch.randn((N, H, G, 128), generator=gq).cuda()
+    s2 = torch.ones((N, H, 128), device="cuda")
+    bq = torch.full((N,), budget * 4, dtype=torch.int32, device="cuda")
+    depths = torch.zeros((N, H, 128), dtype=torch.uint8, device="cuda")
+    pk.bpkv_alloc_depths(c.c, q, s2, bq, depths)
+    ws = c.workspace(k, pk.WS_SCAN_TOPK)
+    idx_a = torch.zeros((N, H, G, k), dtype=torch.int32, device="cuda")
+    pk.bpkv_clear_status(ws)
+    pk.bpkv_scan_topk(c.c, q, depths, k, 4, 32, idx_a, ws, ws.numel())
+    assert pk.bpkv_read_status(ws) == 0
+    ld = c.c.cap_tokens
+    scores = torch.zeros((N, H, G, ld), device="cuda")
+    pk.bpkv_scan(c.c, q, depths, scores, ld)
+    idx_b = torch.zeros_like(idx_a)
+    pk.bpkv_topk(c.c, scores, ld, k, 4, 32, idx_b, ws, ws.numel())
+    assert pk.bpkv_read_status(ws) == 0
+    assert torch.equal(idx_a, idx_b)

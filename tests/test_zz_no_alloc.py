@@ -51,7 +51,7 @@ def test_noalloc_matches_workspace_call_twice(pk):
 
 
 def test_noalloc_refuses_oversized_request(pk):
-    # N H G round_up(n, 64) 4 bytes = 1 x 16 x 4 x 65536 x 4 = 16 MiB + 0 -> fits; 65600 tokens does not
+    # rows (4 round_up(n, 64) + 24600) bytes with rows = N H G = 64: 64 x (262400 + 24600) > 16 MiB
     cache, g = _case(pk, 65600, 16, seed=22)
     q = torch.randn((1, 16, 4, 128), generator=g).cuda()
     depths = torch.full((1, 16, 128), 1, dtype=torch.uint8, device="cuda")
