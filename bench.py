@@ -41,7 +41,7 @@ def launches_per_pass(p, args) -> int:
         return 2          # fused cluster kernel + length update
     if args.tail:
         return 5          # encode + length update, depths, scan, cluster tail
-    return 6              # encode + length update, depths, scan, top-k, range attention
+    return 4              # front (append beside depths and plan), scan, cut, range attention
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -382,8 +382,10 @@ def bench_ours(args, cfg, rank, world, local):
         "fused_kernel": all(p["fused"] for p in passes),
         "stages_us_per_step": {s: round(v * 1e3, 2) for s, v in stage_mean.items()},
         "stages_note": ("from separate replays with event nodes at every stage boundary "
-                        f"({statistics.mean(ev_ms) * 1e3:.1f} us/step with them); on the fused path "
-                        "'encode' holds the whole fused kernel and 'attend' the length update"),
+                        f"({statistics.mean(ev_ms) * 1e3:.1f} us/step with them); on the default path "
+                        "'encode' holds the front kernel (append beside depths and plan), 'topk' the cut "
+                        "kernel and 'attend' the range attention; on the fused path 'encode' holds the "
+                        "whole fused kernel and 'attend' the length update"),
         "bytes_per_step": {"scan": round(scan_bytes), "rows": round(rows_bytes), "scores_overhead": round(score_bytes),
                            "union_rows": union_rows},
         "roofline": roofline,

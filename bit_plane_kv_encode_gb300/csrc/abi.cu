@@ -18,13 +18,18 @@ size_t attend_ranges_part_bytes(const bpkv_cache& c);
 bool attend_ranges_eligible(const bpkv_cache& c, int32_t k);
 cudaError_t launch_attend_ranges(const bpkv_cache& c, const float* q, const float* scores, int64_t ld,
                                  const unsigned long long* cut, int32_t n_sink, int32_t n_recent, float* part,
-                                 uint32_t* tickets, float* out, cudaStream_t st);
+                                 uint32_t* tickets, float* out, int32_t pending, uint32_t* seq_tick,
+                                 cudaStream_t st);
 cudaError_t launch_scan(const bpkv_cache& c, const float* q, const uint8_t* depths, float* scores, int64_t ld,
                         cudaStream_t st, const void* plan = nullptr, uint32_t* hist = nullptr,
-                        int32_t n_sink = 0, int32_t n_recent = 0);
+                        int32_t n_sink = 0, int32_t n_recent = 0, int32_t pending = 0);
 cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
                         int32_t n_recent, const SelBufs& b, HistState hs, int32_t* idx, int32_t* status,
-                        cudaStream_t st);
+                        cudaStream_t st, int32_t pending = 0);
+cudaError_t launch_front(const bpkv_cache& c, const uint16_t* k_new, const uint16_t* v_new, int32_t t_new,
+                         const float* q, const float* sigma2, const int32_t* budget_q, int32_t depth_rule,
+                         int32_t n_channels, int32_t depth, uint8_t* depths, void* plan, uint32_t* hist,
+                         uint32_t* ctr, uint32_t* tickets, uint32_t* seq_tick, cudaStream_t st);
 bool cut_counts_hist(const bpkv_cache& c);
 cudaError_t launch_union(const bpkv_cache& c, const int32_t* idx, int32_t k, int32_t* uidx, uint8_t* umask,
                          int32_t* ucount, cudaStream_t st);
@@ -82,7 +87,7 @@ int check_k(int32_t k, int32_t n_sink, int32_t n_recent) {
 // Workspace layout: status word, then the buffers each call family needs.
 struct Layout {
   size_t scores = 0, hist = 0, ctr = 0, cand = 0, cut = 0, part = 0, depths = 0, idx = 0, uidx = 0, umask = 0,
-         ucount = 0, tickets = 0, plan = 0, total = 0;
+         ucount = 0, tickets = 0, seq_tick = 0, plan = 0, total = 0;
 };
 
 Layout layout(const bpkv_cache& c, int32_t k, int32_t what) {
@@ -129,6 +134,8 @@ Layout layout(const bpkv_cache& c, int32_t k, int32_t what) {
     off = align_up(off + NH * sizeof(int32_t));
     L.tickets = off;
     off = align_up(off + NH * sizeof(uint32_t));
+    L.seq_tick = off;
+    off = align_up(off + (size_t)c.n_seq * sizeof(uint32_t));
     L.plan = off;
     off = align_up(off + NH * scan_plan_bytes(c.group));
   }
@@ -348,61 +355,74 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
       c.n_max += 1;
       continue;
     }
-    BPKV_TRY(cuda_status(launch_encode_append(c, kn, vn, 1, st)));
-    c.n_max += 1;
-    if (dense) {
-      for (int e = 1; e <= 5; ++e) BPKV_TRY(mark(l, e));
-      BPKV_TRY(cuda_status(launch_attend(c, q, nullptr, nullptr, nullptr, 1, part, out, true, st)));
-      BPKV_TRY(mark(l, 6));
-      continue;
-    }
     uint8_t* depths = a->depths_out ? a->depths_out + (size_t)l * NH * kD : at(ws, L.depths);
     int32_t* idx = a->idx_out ? a->idx_out + (size_t)l * NH * G * a->k : reinterpret_cast<int32_t*>(at(ws, L.idx));
     int32_t* uidx = reinterpret_cast<int32_t*>(at(ws, L.uidx));
     uint8_t* umask = at(ws, L.umask);
     int32_t* ucount = reinterpret_cast<int32_t*>(at(ws, L.ucount));
     uint32_t* tickets = reinterpret_cast<uint32_t*>(at(ws, L.tickets));
+    uint32_t* seq_tick = reinterpret_cast<uint32_t*>(at(ws, L.seq_tick));
     void* plan = at(ws, L.plan);
     const SelBufs sb = sel_bufs(ws, L);
-    BPKV_TRY(mark(l, 1));
-    if (a->depth_rule == BPKV_DEPTH_WATERFILL) {
-      BPKV_TRY(cuda_status(launch_alloc_depths(c, q, a->sigma2 + (size_t)l * NH * kD, a->budget_q, depths, st,
-                                               tickets, plan, sb.hist, sb.ctr)));
-    } else {
-      BPKV_TRY(cuda_status(launch_fixed_depths(c, q, a->fixed_channels, a->fixed_depth, depths, st, tickets, plan,
-                                               sb.hist, sb.ctr)));
-    }
-    BPKV_TRY(mark(l, 2));
-    // the level-0 histograms (zeroed by the depth kernel): counted by the cut kernel when it can, else by the scan
-    const bool cut_counts = cut_counts_hist(c);
-    const HistState hs = cut_counts ? HistState::kZero : HistState::kCounted;
-    BPKV_TRY(cuda_status(launch_scan(c, q, depths, scores, c.cap_tokens, st, plan, cut_counts ? nullptr : sb.hist,
-                                     a->n_sink, a->n_recent)));
-    BPKV_TRY(mark(l, 3));
-    if ((a->flags & BPKV_STEP_TAIL) && tail_eligible(c, a->k, a->n_sink, a->n_recent)) {
+    const float* s2 = a->sigma2 ? a->sigma2 + (size_t)l * NH * kD : nullptr;
+    const bool tail = !dense && (a->flags & BPKV_STEP_TAIL) && tail_eligible(c, a->k, a->n_sink, a->n_recent);
+    if (dense || tail) {
+      // append (and length update) first, then the stages one by one
+      BPKV_TRY(cuda_status(launch_encode_append(c, kn, vn, 1, st)));
+      c.n_max += 1;
+      if (dense) {
+        for (int e = 1; e <= 5; ++e) BPKV_TRY(mark(l, e));
+        BPKV_TRY(cuda_status(launch_attend(c, q, nullptr, nullptr, nullptr, 1, part, out, true, st)));
+        BPKV_TRY(mark(l, 6));
+        continue;
+      }
+      BPKV_TRY(mark(l, 1));
+      if (a->depth_rule == BPKV_DEPTH_WATERFILL)
+        BPKV_TRY(cuda_status(launch_alloc_depths(c, q, s2, a->budget_q, depths, st, tickets, plan, sb.hist, sb.ctr)));
+      else
+        BPKV_TRY(cuda_status(launch_fixed_depths(c, q, a->fixed_channels, a->fixed_depth, depths, st, tickets, plan,
+                                                 sb.hist, sb.ctr)));
+      BPKV_TRY(mark(l, 2));
+      BPKV_TRY(cuda_status(launch_scan(c, q, depths, scores, c.cap_tokens, st, plan)));
+      BPKV_TRY(mark(l, 3));
       int32_t* iout = a->idx_out ? a->idx_out + (size_t)l * NH * G * a->k : nullptr;
       BPKV_TRY(cuda_status(
           launch_select_attend(c, scores, c.cap_tokens, q, a->k, a->n_sink, a->n_recent, out, iout, st)));
       for (int e = 4; e <= 6; ++e) BPKV_TRY(mark(l, e));
       continue;
     }
+    // append beside depths and plan in one launch; the new token counts in
+    // seq_len only from the end of the layer (pending = 1 until then)
+    BPKV_TRY(cuda_status(launch_front(c, kn, vn, 1, q, s2, a->budget_q, a->depth_rule, a->fixed_channels,
+                                      a->fixed_depth, depths, plan, sb.hist, sb.ctr, tickets, seq_tick, st)));
+    c.n_max += 1;
+    BPKV_TRY(mark(l, 1));
+    BPKV_TRY(mark(l, 2));
+    // the level-0 histograms (zeroed by the front kernel): counted by the cut kernel when it can, else by the scan
+    const bool cut_counts = cut_counts_hist(c);
+    const HistState hs = cut_counts ? HistState::kZero : HistState::kCounted;
+    BPKV_TRY(cuda_status(launch_scan(c, q, depths, scores, c.cap_tokens, st, plan, cut_counts ? nullptr : sb.hist,
+                                     a->n_sink, a->n_recent, 1)));
+    BPKV_TRY(mark(l, 3));
     if (attend_ranges_eligible(c, a->k)) {
-      // cuts only (lists when asked for); the attention selects by cut and forms the union per token range
+      // cuts only (lists when asked for); the attention selects by cut, forms
+      // the union per token range and finally raises seq_len
       int32_t* iout = a->idx_out ? a->idx_out + (size_t)l * NH * G * a->k : nullptr;
       BPKV_TRY(cuda_status(
-          launch_topk(c, scores, c.cap_tokens, a->k, a->n_sink, a->n_recent, sb, hs, iout, status, st)));
+          launch_topk(c, scores, c.cap_tokens, a->k, a->n_sink, a->n_recent, sb, hs, iout, status, st, 1)));
       BPKV_TRY(mark(l, 4));
       BPKV_TRY(mark(l, 5));
       BPKV_TRY(cuda_status(launch_attend_ranges(c, q, scores, c.cap_tokens, sb.cut, a->n_sink, a->n_recent, part,
-                                                tickets, out, st)));
+                                                tickets, out, 1, seq_tick, st)));
       BPKV_TRY(mark(l, 6));
       continue;
     }
     BPKV_TRY(
-        cuda_status(launch_topk(c, scores, c.cap_tokens, a->k, a->n_sink, a->n_recent, sb, hs, idx, status, st)));
+        cuda_status(launch_topk(c, scores, c.cap_tokens, a->k, a->n_sink, a->n_recent, sb, hs, idx, status, st, 1)));
     BPKV_TRY(mark(l, 4));
     BPKV_TRY(cuda_status(launch_union(c, idx, a->k, uidx, umask, ucount, st)));
     BPKV_TRY(mark(l, 5));
+    BPKV_TRY(cuda_status(launch_bump_len(c, 1, st)));  // the union's rows are final: count the new token
     BPKV_TRY(cuda_status(launch_attend(c, q, uidx, umask, ucount, (int32_t)(G * a->k), part, out, false, st)));
     BPKV_TRY(mark(l, 6));
   }

@@ -258,6 +258,9 @@ struct RangeArgs {
   float* part;                     // [N][H][n_ranges][G][D + 2]
   uint32_t* tickets;               // [N][H], zero on entry
   float* out;                      // [N][H][G][D]
+  int32_t pending;                 // tokens appended in this step but not yet in seq_len
+  int64_t* seq_len_out;            // with pending: seq_len, raised by pending once every unit is done
+  uint32_t* seq_tick;              // [N], zero on entry (with pending)
 };
 
 struct RangeSmem {
@@ -287,7 +290,7 @@ __global__ void __launch_bounds__(kRangeThreads, 512 / kRangeThreads) k_attend_r
   const int64_t unit = (int64_t)s * a.n_heads + h;
   const int G = a.group;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t n = a.seq_len[s];
+  const int64_t n = a.seq_len[s] + a.pending;
   const int64_t t0 = (int64_t)rg * a.range_tok, t1 = min64(t0 + a.range_tok, n);
   const int64_t lo = min64(a.n_sink, n), hi = max64(n - a.n_recent, lo);
   const float qscale = 0.08838834764831845f * 1.4426950408889634f;
@@ -599,7 +602,15 @@ __global__ void __launch_bounds__(kRangeThreads, 512 / kRangeThreads) k_attend_r
       reinterpret_cast<float2*>(a.out + (unit * G + g) * kD)[d2] =
           L > 0.f ? make_float2(O0 / L, O1 / L) : make_float2(0.f, 0.f);
   }
-  if (tid == 0) a.tickets[unit] = 0u;
+  if (tid == 0) {
+    a.tickets[unit] = 0u;
+    // every CTA of this unit has read seq_len; the last unit of the sequence
+    // to finish raises it by the tokens appended in this step
+    if (a.pending && atomicAdd(&a.seq_tick[s], 1u) == (uint32_t)(a.n_heads - 1)) {
+      a.seq_len_out[s] += a.pending;
+      a.seq_tick[s] = 0u;
+    }
+  }
 }
 
 // Tokens per range: a multiple of kRangeAlign, with at most kRangeMaxRanges ranges
@@ -624,12 +635,13 @@ bool attend_ranges_eligible(const bpkv_cache& c, int32_t k) {
 
 cudaError_t launch_attend_ranges(const bpkv_cache& c, const float* q, const float* scores, int64_t ld,
                                  const unsigned long long* cut, int32_t n_sink, int32_t n_recent, float* part,
-                                 uint32_t* tickets, float* out, cudaStream_t st) {
+                                 uint32_t* tickets, float* out, int32_t pending, uint32_t* seq_tick,
+                                 cudaStream_t st) {
   const int64_t rt = range_tokens(c.n_max, c.group);
   const int32_t nr = (int32_t)((c.n_max + rt - 1) / rt);
   if (nr == 0) return cudaSuccess;
   RangeArgs a{c.k_rows, c.v_rows, c.seq_len,     q,       scores, ld,      cut,    n_sink, n_recent,
-              c.cap_tokens, c.n_kv_heads, c.group, rt, nr, part, tickets, out};
+              c.cap_tokens, c.n_kv_heads, c.group, rt, nr, part, tickets, out, pending, c.seq_len, seq_tick};
   const int smem = (int)sizeof(RangeSmem);
   auto go = [&](auto kern) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

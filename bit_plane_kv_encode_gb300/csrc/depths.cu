@@ -12,7 +12,13 @@
 // In a decode step the same CTA also builds the unit's scan plan (channel
 // groups, plane rows, weights q 2^(4-t-pos)) once, so that every scan CTA of
 // the unit copies it instead of deriving it again from the depths.
+//
+// k_front runs a decode step's first work in one launch: per unit, the
+// append and re-encode of the new tokens' block(s) (which also clear the
+// unit's selection histograms and counters) beside the depth allocation and
+// plan; the two do not depend on each other.
 #include "depths_core.cuh"
+#include "encode_core.cuh"
 #include "scan_core.cuh"
 
 #include <type_traits>
@@ -99,6 +105,90 @@ size_t scan_plan_bytes(int group) {
   if (group <= 2) return sizeof(ScanPlan<2>);
   if (group <= 4) return sizeof(ScanPlan<4>);
   return sizeof(ScanPlan<8>);
+}
+
+struct FrontArgs {
+  DepthArgs d;
+  int32_t depth_rule;       // BPKV_DEPTH_WATERFILL or BPKV_DEPTH_FIXED
+  uint32_t* seq_tick;       // [N]: zeroed for the attention of this step
+  // append
+  uint64_t* planes;
+  uint16_t* scales;
+  uint16_t* k_rows;
+  uint16_t* v_rows;
+  const int64_t* seq_len;
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  int32_t t_new;
+  int32_t enc_ctas;         // append CTAs per unit (blocks the new tokens can touch)
+  int64_t cap;
+};
+
+// Grid (enc_ctas + 1, H, N), kScanThreads threads: x < enc_ctas appends, x ==
+// enc_ctas allocates depths and emits the plan.
+template <int GP>
+__global__ void __launch_bounds__(kScanThreads) k_front(FrontArgs a) {
+  pdl_enter();
+  const int s = blockIdx.z, h = blockIdx.y, x = blockIdx.x;
+  const int64_t unit = (int64_t)s * a.d.n_heads + h;
+  const int G = a.d.group;
+  if (x < a.enc_ctas) {
+    // this CTA's slice of the unit's histograms and counters
+    {
+      const int n4 = G * kTopkBins / 4;
+      uint4* hz = reinterpret_cast<uint4*>(a.d.hist + unit * G * kTopkBins);
+      const int e0 = n4 * x / a.enc_ctas, e1 = n4 * (x + 1) / a.enc_ctas;
+      for (int e = e0 + threadIdx.x; e < e1; e += blockDim.x) hz[e] = make_uint4(0u, 0u, 0u, 0u);
+      if (x == 0 && (int)threadIdx.x < kSelCounters * G) a.d.ctr[unit * kSelCounters * G + threadIdx.x] = 0u;
+    }
+    const int64_t n_old = a.seq_len[s];
+    const int64_t n_new = n_old + a.t_new;
+    const int64_t blk = n_old / kBlock + x;
+    const int64_t t0 = blk * kBlock;
+    if (t0 >= n_new || n_new > a.cap) return;
+    const int cnt = (int)min64(kBlock, n_new - t0);
+    const Unit U{a.cap / kBlock, a.cap};
+    __shared__ __align__(16) uint16_t kb[kBlock][kD];
+    encode_block_cta<2>(kb, a.k_rows + U.row_base(unit), a.v_rows + U.row_base(unit),
+                        a.k_new + unit * a.t_new * kD, a.v_new + unit * a.t_new * kD, n_old, t0, cnt,
+                        a.planes + U.plane_base(unit), a.scales + U.scale_base(unit), a.cap / kBlock, blk);
+    return;
+  }
+  __shared__ DepthSmem S;
+  if (threadIdx.x == 0) {
+    a.d.tickets[unit] = 0u;
+    if (h == 0) a.seq_tick[s] = 0u;
+  }
+  uint8_t* dep = a.d.depths + unit * kD;
+  if (a.depth_rule == BPKV_DEPTH_WATERFILL)
+    alloc_depths_cta(S, a.d.q + unit * G * kD, a.d.sigma2 + unit * kD, G, a.d.budget_q[s], dep);
+  else
+    fixed_depths_cta(S, a.d.q + unit * G * kD, G, a.d.n_channels, a.d.depth, dep);
+  emit_plan<GP>(a.d, unit, dep);
+}
+
+cudaError_t launch_front(const bpkv_cache& c, const uint16_t* k_new, const uint16_t* v_new, int32_t t_new,
+                         const float* q, const float* sigma2, const int32_t* budget_q, int32_t depth_rule,
+                         int32_t n_channels, int32_t depth, uint8_t* depths, void* plan, uint32_t* hist,
+                         uint32_t* ctr, uint32_t* tickets, uint32_t* seq_tick, cudaStream_t st) {
+  FrontArgs a;
+  a.d = DepthArgs{q, sigma2, budget_q, depths, c.n_kv_heads, c.group, tickets, plan, n_channels, depth, hist, ctr};
+  a.depth_rule = depth_rule;
+  a.seq_tick = seq_tick;
+  a.planes = c.planes;
+  a.scales = c.scales;
+  a.k_rows = c.k_rows;
+  a.v_rows = c.v_rows;
+  a.seq_len = c.seq_len;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.t_new = t_new;
+  a.enc_ctas = (t_new + kBlock - 1) / kBlock + 1;
+  a.cap = c.cap_tokens;
+  const dim3 grid((unsigned)(a.enc_ctas + 1), (unsigned)c.n_kv_heads, (unsigned)c.n_seq);
+  return launch_depths_gp(c.group, [&](auto gp) {
+    return launch_pdl(k_front<decltype(gp)::value>, grid, dim3(kScanThreads), 0, st, a);
+  });
 }
 
 cudaError_t launch_alloc_depths(const bpkv_cache& c, const float* q, const float* sigma2, const int32_t* budget_q,

@@ -16,19 +16,33 @@ __device__ void encode_block_cta(uint16_t (*kb)[kD], uint16_t* krow, uint16_t* v
                                  const uint16_t* vnew, int64_t n_old, int64_t t0, int cnt, uint64_t* pw_base,
                                  uint16_t* scale_base, int64_t nb_cap, int64_t blk) {
   constexpr int TOK = kBlock / PARTS;
-  for (int v = threadIdx.x; v < cnt * 16; v += blockDim.x) {
-    const int r = v >> 4, c8 = (v & 15) * 8;
-    const int64_t tok = t0 + r;
-    uint4 val;
-    if (tok < n_old) {
-      val = *reinterpret_cast<const uint4*>(krow + tok * kD + c8);
-    } else {
-      const int64_t src = (tok - n_old) * kD + c8;
-      val = *reinterpret_cast<const uint4*>(knew + src);
-      *reinterpret_cast<uint4*>(krow + tok * kD + c8) = val;
-      *reinterpret_cast<uint4*>(vrow + tok * kD + c8) = *reinterpret_cast<const uint4*>(vnew + src);
+  constexpr int kBatch = 4;  // independent 16-byte loads in flight per thread
+  for (int v0 = threadIdx.x; v0 < cnt * 16; v0 += kBatch * blockDim.x) {
+    uint4 val[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int v = v0 + b * blockDim.x;
+      if (v < cnt * 16) {
+        const int r = v >> 4, c8 = (v & 15) * 8;
+        const int64_t tok = t0 + r;
+        val[b] = tok < n_old ? *reinterpret_cast<const uint4*>(krow + tok * kD + c8)
+                             : *reinterpret_cast<const uint4*>(knew + (tok - n_old) * kD + c8);
+      }
     }
-    *reinterpret_cast<uint4*>(&kb[r][c8]) = val;
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int v = v0 + b * blockDim.x;
+      if (v < cnt * 16) {
+        const int r = v >> 4, c8 = (v & 15) * 8;
+        const int64_t tok = t0 + r;
+        if (tok >= n_old) {
+          const int64_t src = (tok - n_old) * kD + c8;
+          *reinterpret_cast<uint4*>(krow + tok * kD + c8) = val[b];
+          *reinterpret_cast<uint4*>(vrow + tok * kD + c8) = *reinterpret_cast<const uint4*>(vnew + src);
+        }
+        *reinterpret_cast<uint4*>(&kb[r][c8]) = val[b];
+      }
+    }
   }
   __syncthreads();
   // thread = (channel j, part qd): tokens TOK qd .. TOK qd + TOK - 1; the parts

@@ -18,10 +18,10 @@
 namespace bpkv {
 cudaError_t launch_scan(const bpkv_cache& c, const float* q, const uint8_t* depths, float* scores, int64_t ld,
                         cudaStream_t st, const void* plan = nullptr, uint32_t* hist = nullptr,
-                        int32_t n_sink = 0, int32_t n_recent = 0);
+                        int32_t n_sink = 0, int32_t n_recent = 0, int32_t pending = 0);
 cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
                         int32_t n_recent, const SelBufs& b, HistState hs, int32_t* idx, int32_t* status,
-                        cudaStream_t st);
+                        cudaStream_t st, int32_t pending = 0);
 bool cut_counts_hist(const bpkv_cache& c);
 }  // namespace bpkv
 

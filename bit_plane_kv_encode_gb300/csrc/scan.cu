@@ -40,6 +40,7 @@ struct ScanArgs {
   uint32_t* hist;  // optional [N][H][G][kTopkBins] level-0 selection histogram (zeroed by the caller)
   int32_t n_sink, n_recent;
   int64_t chunks_per_cta;
+  int32_t pending;  // tokens appended in this step but not yet in seq_len
 };
 
 template <int GP>
@@ -49,7 +50,7 @@ __global__ void __launch_bounds__(kScanThreads, GP >= 8 ? 2 : 4) k_scan(ScanArgs
   ScanSmem<GP>& S = *reinterpret_cast<ScanSmem<GP>*>(smem_raw);
   const int s = blockIdx.z, h = blockIdx.y;
   const int64_t unit = (int64_t)s * a.n_heads + h;
-  const int64_t n = a.seq_len[s];
+  const int64_t n = a.seq_len[s] + a.pending;
   const int64_t c_begin = (int64_t)blockIdx.x * a.chunks_per_cta;
   if (c_begin * kScanBlocks * kBlock >= n) return;
   const int64_t nb_valid = (n + kBlock - 1) / kBlock;
@@ -119,9 +120,10 @@ cudaError_t launch_scan_gp(ScanArgs a, int64_t chunks, int64_t units, cudaStream
 }
 
 cudaError_t launch_scan(const bpkv_cache& c, const float* q, const uint8_t* depths, float* scores, int64_t ld,
-                        cudaStream_t st, const void* plan, uint32_t* hist, int32_t n_sink, int32_t n_recent) {
-  ScanArgs a{plan,    c.planes, c.scales, c.seq_len, q, depths, scores, ld, c.cap_tokens / kBlock,
-             c.n_kv_heads, c.group, hist,   n_sink,   n_recent, 1};
+                        cudaStream_t st, const void* plan, uint32_t* hist, int32_t n_sink, int32_t n_recent,
+                        int32_t pending) {
+  ScanArgs a{plan,         c.planes, c.scales, c.seq_len, q,        depths, scores, ld, c.cap_tokens / kBlock,
+             c.n_kv_heads, c.group,  hist,     n_sink,    n_recent, 1,      pending};
   const int64_t chunks = (c.n_max + kScanBlocks * kBlock - 1) / (kScanBlocks * kBlock);
   if (chunks == 0) return cudaSuccess;
   const int64_t units = (int64_t)c.n_seq * c.n_kv_heads;

@@ -105,6 +105,7 @@ struct HistArgs {
   const int64_t* seq_len;
   uint32_t* hist;  // [rows][kTopkBins], zero on entry
   int32_t rows_per_seq, k, n_sink, n_recent;
+  int32_t pending;  // tokens appended in this step but not yet in seq_len
 };
 
 // Level-0 histogram of one chunk of one row's middle keys.  Grid (chunks, rows).
@@ -112,7 +113,7 @@ __global__ void __launch_bounds__(kCutThreads) k_hist(HistArgs a) {
   pdl_enter();
   __shared__ uint32_t H[kTopkBins];
   const int row = blockIdx.y;
-  const RowRange r = row_range(a.seq_len[row / a.rows_per_seq], a.k, a.n_sink, a.n_recent);
+  const RowRange r = row_range(a.seq_len[row / a.rows_per_seq] + a.pending, a.k, a.n_sink, a.n_recent);
   const int64_t c0 = (int64_t)blockIdx.x * kCutChunk, c1 = min64(c0 + kCutChunk, r.cnt);
   if (r.cnt <= r.m || r.m == 0 || c0 >= c1) return;
   for (int b = threadIdx.x; b < kTopkBins; b += kCutThreads) H[b] = 0u;
@@ -140,6 +141,7 @@ struct CutArgs {
   int32_t* status;
   int32_t rows_per_seq, k, n_sink, n_recent;
   int32_t build_hist;          // count hist here (zero on entry; cooperative launch) instead of reading it
+  int32_t pending;             // tokens appended in this step but not yet in seq_len
 };
 
 struct __align__(16) CutSmem {
@@ -321,7 +323,7 @@ __global__ void __launch_bounds__(kCutThreads, 2) k_cut(CutArgs a) {
   uint32_t h[kBinsPerThread];
   int top = 0;
   if (!a.build_hist) top = bins_of_thread(a.hist + (int64_t)row * kTopkBins, kTopkBins, h);  // before seq_len
-  const RowRange r = row_range(a.seq_len[row / a.rows_per_seq], a.k, a.n_sink, a.n_recent);
+  const RowRange r = row_range(a.seq_len[row / a.rows_per_seq] + a.pending, a.k, a.n_sink, a.n_recent);
   if (r.cnt <= r.m || r.m == 0) {
     // every middle key, or none
     if (blockIdx.x == 0 && tid == 0) a.cut[row] = r.cnt <= r.m ? 0ull : ~0ull;
@@ -433,6 +435,7 @@ struct ListArgs {
   int32_t* idx;  // [rows][k]
   int32_t* status;
   int32_t rows_per_seq, k, n_sink, n_recent;
+  int32_t pending;  // tokens appended in this step but not yet in seq_len
 };
 
 struct ListSmem {
@@ -448,7 +451,7 @@ __global__ void __launch_bounds__(kSelThreads) k_lists(ListArgs a) {
   extern __shared__ __align__(16) unsigned char list_raw[];
   ListSmem& S = *reinterpret_cast<ListSmem*>(list_raw);
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
-  const RowRange r = row_range(a.seq_len[row / a.rows_per_seq], a.k, a.n_sink, a.n_recent);
+  const RowRange r = row_range(a.seq_len[row / a.rows_per_seq] + a.pending, a.k, a.n_sink, a.n_recent);
   const float* sc = a.scores + (int64_t)row * a.ld;
   int32_t* out = a.idx + (int64_t)row * a.k;
   const int64_t n_mid = r.cnt <= r.m ? r.cnt : r.m;
@@ -510,8 +513,8 @@ size_t cut_scratch_bytes(const bpkv_cache& c) {
 }
 
 cudaError_t launch_hist(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
-                        int32_t n_recent, uint32_t* hist, cudaStream_t st) {
-  HistArgs a{scores, ld, c.seq_len, hist, c.n_kv_heads * c.group, k, n_sink, n_recent};
+                        int32_t n_recent, uint32_t* hist, int32_t pending, cudaStream_t st) {
+  HistArgs a{scores, ld, c.seq_len, hist, c.n_kv_heads * c.group, k, n_sink, n_recent, pending};
   const dim3 grid((unsigned)cut_chunks(c), (unsigned)(c.n_seq * c.n_kv_heads * c.group));
   return launch_pdl(k_hist, grid, dim3(kCutThreads), 0, st, a);
 }
@@ -541,9 +544,10 @@ bool cut_counts_hist(const bpkv_cache& c) {
 }
 
 cudaError_t launch_cut(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
-                       int32_t n_recent, const SelBufs& b, bool build_hist, int32_t* status, cudaStream_t st) {
-  CutArgs a{scores, ld, c.seq_len, b.hist, b.cand, b.ctr, b.cut, status, c.n_kv_heads * c.group, k, n_sink, n_recent,
-            build_hist ? 1 : 0};
+                       int32_t n_recent, const SelBufs& b, bool build_hist, int32_t pending, int32_t* status,
+                       cudaStream_t st) {
+  CutArgs a{scores,   ld,     c.seq_len,  b.hist, b.cand, b.ctr, b.cut, status, c.n_kv_heads * c.group, k, n_sink,
+            n_recent, build_hist ? 1 : 0, pending};
   const dim3 grid((unsigned)cut_chunks(c), (unsigned)(c.n_seq * c.n_kv_heads * c.group));
   if (build_hist) return launch_coop_pdl(k_cut, grid, dim3(kCutThreads), 0, st, a);
   return launch_pdl(k_cut, grid, dim3(kCutThreads), 0, st, a);
@@ -551,8 +555,8 @@ cudaError_t launch_cut(const bpkv_cache& c, const float* scores, int64_t ld, int
 
 cudaError_t launch_lists(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
                          int32_t n_recent, const unsigned long long* cut, int32_t* idx, int32_t* status,
-                         cudaStream_t st) {
-  ListArgs a{scores, ld, c.seq_len, cut, idx, status, c.n_kv_heads * c.group, k, n_sink, n_recent};
+                         int32_t pending, cudaStream_t st) {
+  ListArgs a{scores, ld, c.seq_len, cut, idx, status, c.n_kv_heads * c.group, k, n_sink, n_recent, pending};
   const int smem = (int)sizeof(ListSmem);
   cudaError_t e = cudaFuncSetAttribute(k_lists, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -565,7 +569,7 @@ cudaError_t launch_lists(const bpkv_cache& c, const float* scores, int64_t ld, i
 // first.
 cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
                         int32_t n_recent, const SelBufs& b, HistState hs, int32_t* idx, int32_t* status,
-                        cudaStream_t st) {
+                        cudaStream_t st, int32_t pending) {
   cudaError_t e;
   bool build = false;
   if (hs == HistState::kDirty) {
@@ -576,13 +580,13 @@ cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, in
   if (hs != HistState::kCounted) {
     build = cut_counts_hist(c);
     if (!build) {
-      e = launch_hist(c, scores, ld, k, n_sink, n_recent, b.hist, st);
+      e = launch_hist(c, scores, ld, k, n_sink, n_recent, b.hist, pending, st);
       if (e != cudaSuccess) return e;
     }
   }
-  e = launch_cut(c, scores, ld, k, n_sink, n_recent, b, build, status, st);
+  e = launch_cut(c, scores, ld, k, n_sink, n_recent, b, build, pending, status, st);
   if (e != cudaSuccess || !idx) return e;
-  return launch_lists(c, scores, ld, k, n_sink, n_recent, b.cut, idx, status, st);
+  return launch_lists(c, scores, ld, k, n_sink, n_recent, b.cut, idx, status, pending, st);
 }
 
 // ---------------------------------------------------------------- union
