@@ -120,7 +120,7 @@ struct FrontArgs {
   const uint16_t* k_new;
   const uint16_t* v_new;
   int32_t t_new;
-  int32_t enc_ctas;         // append CTAs per unit (blocks the new tokens can touch)
+  int32_t enc_ctas;         // append CTAs per unit: two (channel halves) per block the new tokens can touch
   int64_t cap;
 };
 
@@ -141,17 +141,19 @@ __global__ void __launch_bounds__(kScanThreads) k_front(FrontArgs a) {
       for (int e = e0 + threadIdx.x; e < e1; e += blockDim.x) hz[e] = make_uint4(0u, 0u, 0u, 0u);
       if (x == 0 && (int)threadIdx.x < kSelCounters * G) a.d.ctr[unit * kSelCounters * G + threadIdx.x] = 0u;
     }
+    // CTA x: block n_old / 64 + x / 2, channels 64 (x % 2) ..
     const int64_t n_old = a.seq_len[s];
     const int64_t n_new = n_old + a.t_new;
-    const int64_t blk = n_old / kBlock + x;
+    const int64_t blk = n_old / kBlock + x / 2;
     const int64_t t0 = blk * kBlock;
     if (t0 >= n_new || n_new > a.cap) return;
     const int cnt = (int)min64(kBlock, n_new - t0);
     const Unit U{a.cap / kBlock, a.cap};
     __shared__ __align__(16) uint16_t kb[kBlock][kD];
-    encode_block_cta<2>(kb, a.k_rows + U.row_base(unit), a.v_rows + U.row_base(unit),
+    encode_block_cta<4>(kb, a.k_rows + U.row_base(unit), a.v_rows + U.row_base(unit),
                         a.k_new + unit * a.t_new * kD, a.v_new + unit * a.t_new * kD, n_old, t0, cnt,
-                        a.planes + U.plane_base(unit), a.scales + U.scale_base(unit), a.cap / kBlock, blk);
+                        a.planes + U.plane_base(unit), a.scales + U.scale_base(unit), a.cap / kBlock, blk,
+                        (x % 2) * (kD / 2));
     return;
   }
   __shared__ DepthSmem S;
@@ -183,7 +185,7 @@ cudaError_t launch_front(const bpkv_cache& c, const uint16_t* k_new, const uint1
   a.k_new = k_new;
   a.v_new = v_new;
   a.t_new = t_new;
-  a.enc_ctas = (t_new + kBlock - 1) / kBlock + 1;
+  a.enc_ctas = 2 * ((t_new + kBlock - 1) / kBlock + 1);
   a.cap = c.cap_tokens;
   const dim3 grid((unsigned)(a.enc_ctas + 1), (unsigned)c.n_kv_heads, (unsigned)c.n_seq);
   return launch_depths_gp(c.group, [&](auto gp) {

@@ -43,7 +43,9 @@ static __device__ void alloc_depths_cta(DepthSmem& S, const float* __restrict__ 
   if (tid == 0) S.cut = kItems;
   __syncthreads();
   // Bitonic sort, descending.
+#pragma unroll
   for (int size = 2; size <= kItems; size <<= 1) {
+#pragma unroll
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       const int i = 2 * tid - (tid & (stride - 1));
       const int j = i + stride;

@@ -6,24 +6,26 @@
 
 namespace bpkv {
 
-// Append the tokens of one 64-token block of one unit and re-encode the block.
-// Rows t0 .. t0 + cnt - 1 are the block's tokens; those below n_old come from
-// the stored rows, the others from knew/vnew (row r of the new tokens is
-// token n_old + r), which are also copied into the row store.  Threads:
-// PARTS per channel (blockDim.x == PARTS * 128), 64 / PARTS tokens each.
+// Append the tokens of one 64-token block of one unit and re-encode the block,
+// for channels c_lo .. c_lo + blockDim.x / PARTS - 1.  Rows t0 .. t0 + cnt - 1
+// are the block's tokens; those below n_old come from the stored rows, the
+// others from knew/vnew (row r of the new tokens is token n_old + r), which are
+// also copied into the row store (these channels of them).  Threads: PARTS per
+// channel, 64 / PARTS tokens each.
 template <int PARTS>
 __device__ void encode_block_cta(uint16_t (*kb)[kD], uint16_t* krow, uint16_t* vrow, const uint16_t* knew,
                                  const uint16_t* vnew, int64_t n_old, int64_t t0, int cnt, uint64_t* pw_base,
-                                 uint16_t* scale_base, int64_t nb_cap, int64_t blk) {
+                                 uint16_t* scale_base, int64_t nb_cap, int64_t blk, int c_lo = 0) {
   constexpr int TOK = kBlock / PARTS;
   constexpr int kBatch = 4;  // independent 16-byte loads in flight per thread
-  for (int v0 = threadIdx.x; v0 < cnt * 16; v0 += kBatch * blockDim.x) {
+  const int n8 = (int)(blockDim.x / PARTS) / 8;  // 16-byte pieces of a row in this CTA's channels
+  for (int v0 = threadIdx.x; v0 < cnt * n8; v0 += kBatch * blockDim.x) {
     uint4 val[kBatch];
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int v = v0 + b * blockDim.x;
-      if (v < cnt * 16) {
-        const int r = v >> 4, c8 = (v & 15) * 8;
+      if (v < cnt * n8) {
+        const int r = v / n8, c8 = c_lo + (v % n8) * 8;
         const int64_t tok = t0 + r;
         val[b] = tok < n_old ? *reinterpret_cast<const uint4*>(krow + tok * kD + c8)
                              : *reinterpret_cast<const uint4*>(knew + (tok - n_old) * kD + c8);
@@ -32,8 +34,8 @@ __device__ void encode_block_cta(uint16_t (*kb)[kD], uint16_t* krow, uint16_t* v
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int v = v0 + b * blockDim.x;
-      if (v < cnt * 16) {
-        const int r = v >> 4, c8 = (v & 15) * 8;
+      if (v < cnt * n8) {
+        const int r = v / n8, c8 = c_lo + (v % n8) * 8;
         const int64_t tok = t0 + r;
         if (tok >= n_old) {
           const int64_t src = (tok - n_old) * kD + c8;
@@ -47,7 +49,7 @@ __device__ void encode_block_cta(uint16_t (*kb)[kD], uint16_t* krow, uint16_t* v
   __syncthreads();
   // thread = (channel j, part qd): tokens TOK qd .. TOK qd + TOK - 1; the parts
   // of a channel are adjacent lanes.
-  const int j = threadIdx.x / PARTS, qd = threadIdx.x % PARTS;
+  const int j = c_lo + threadIdx.x / PARTS, qd = threadIdx.x % PARTS;
   const int r0 = TOK * qd, r1 = min(r0 + TOK, cnt);
   float amax = 0.f;
   for (int r = r0; r < r1; ++r) amax = fmaxf(amax, fabsf(bf16_bits_to_float(kb[r][j])));

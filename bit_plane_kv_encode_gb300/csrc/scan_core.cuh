@@ -158,7 +158,10 @@ __device__ __forceinline__ void transpose_consts(int lane, uint32_t (&keep)[5], 
 }
 
 // Channel groups and per-query weights.  Threads 0..127 pass their channel's
-// depth t and q values; blockDim.x must be kScanThreads.
+// depth t and q values; blockDim.x must be kScanThreads.  The groups of depth
+// 4 come first, then 3, 2, 1; within a depth, groups of group_cap(t) channels
+// in channel order.  Every layout figure follows in closed form from the four
+// per-depth channel counts.
 template <int GP>
 __device__ void scan_setup(ScanPlan<GP>& S, PlanScratch& X, int t, const float (&qv)[GP]) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -172,62 +175,79 @@ __device__ void scan_setup(ScanPlan<GP>& S, PlanScratch& X, int t, const float (
     }
   }
   for (int e = tid; e < kMaxGroups * 32; e += kScanThreads) S.row_of_lane[e] = -1;
-  for (int e = tid; e < kMaxSlots; e += kScanThreads) {
-    S.slot_ch[e] = -1;
-    S.slot_grp[e] = 0;
-  }
+  for (int e = tid; e < kMaxSlots * GP; e += kScanThreads) S.w[e] = 0.f;
   __syncthreads();
-  if (tid == 0) {
-    int g = 0, slot = 0;
+  // per depth d: channels, groups, first group and first slot
+  int cnt[5], ng[5], goff[5], soff[5];
+  int n_groups = 0, n_slots = 0;
+#pragma unroll
+  for (int d = 4; d >= 1; --d) {
+    cnt[d] = X.warp_cnt[0][d] + X.warp_cnt[1][d] + X.warp_cnt[2][d] + X.warp_cnt[3][d];
+    ng[d] = (cnt[d] + group_cap(d) - 1) / group_cap(d);
+    goff[d] = n_groups;
+    soff[d] = n_slots;
+    n_groups += ng[d];
+    n_slots += ng[d] * slot_pitch(d);
+  }
+  if (tid < n_groups) {
+#pragma unroll
     for (int d = 4; d >= 1; --d) {
-      int c = 0;
-      for (int w = 0; w < 4; ++w) c += X.warp_cnt[w][d];
-      X.cnt_t[d] = c;
-      for (int first = 0; first < c; first += group_cap(d), ++g) {
-        S.grp_t[g] = (int8_t)d;
-        S.grp_base[g] = (int16_t)slot;
-        S.grp_cnt[g] = (int8_t)min(group_cap(d), c - first);
-        slot += slot_pitch(d);
+      if (tid >= goff[d] && tid < goff[d] + ng[d]) {
+        const int i = tid - goff[d];
+        S.grp_t[tid] = (int8_t)d;
+        S.grp_base[tid] = (int16_t)(soff[d] + i * slot_pitch(d));
+        S.grp_cnt[tid] = (int8_t)min(group_cap(d), cnt[d] - i * group_cap(d));
       }
     }
-    S.n_groups = g;
-    S.n_slots = slot;
-    // passes: runs of groups within kPassGroups groups and kPassSlots slots
-    int np = 0, g0 = 0;
-    while (g0 < g && np < kMaxPasses) {
-      int g1 = g0, sl = 0;
-      while (g1 < g && g1 - g0 < kPassGroups && sl + slot_pitch(S.grp_t[g1]) <= kPassSlots)
-        sl += slot_pitch(S.grp_t[g1++]);
-      S.pass_g[np++] = (int8_t)g0;
-      g0 = g1;
+  }
+  for (int e = tid; e < kMaxSlots; e += kScanThreads) {
+    S.slot_ch[e] = -1;
+    int g = 0;
+#pragma unroll
+    for (int d = 4; d >= 1; --d)
+      if (e >= soff[d] && e < soff[d] + ng[d] * slot_pitch(d)) g = goff[d] + (e - soff[d]) / slot_pitch(d);
+    S.slot_grp[e] = (int8_t)g;
+  }
+  if (tid == 0) {
+    S.n_groups = n_groups;
+    S.n_slots = n_slots;
+    // passes: greedy runs of groups within kPassGroups groups and kPassSlots
+    // slots (at most 4 runs for any depth vector: the slots total <= 288)
+    int np = 0, run_g = 0, run_s = 0;
+    for (int d = 4; d >= 1; --d) {
+      for (int i = 0; i < ng[d]; ++i) {
+        const int pt = slot_pitch(d);
+        if (run_g == 0 || run_g == kPassGroups || run_s + pt > kPassSlots) {
+          if (np < kMaxPasses) S.pass_g[np] = (int8_t)(goff[d] + i);
+          ++np;
+          run_g = 0;
+          run_s = 0;
+        }
+        ++run_g;
+        run_s += pt;
+      }
     }
-    S.pass_g[np] = (int8_t)g;
+    np = min(np, kMaxPasses);
+    S.pass_g[np] = (int8_t)n_groups;
     S.n_passes = np;
   }
-  __syncthreads();
   if (tid < kD && t > 0) {
     for (int w = 0; w < warp; ++w) rank += X.warp_cnt[w][t];
-    // group index: groups of deeper channels come first
-    int g = 0;
-    for (int d = 4; d > t; --d) g += (X.cnt_t[d] + group_cap(d) - 1) / group_cap(d);
-    g += rank / group_cap(t);
-    const int m = rank % group_cap(t);
-    S.slot_ch[S.grp_base[g] + m] = (int16_t)tid;
+    int goff_t = 0, soff_t = 0;  // selected without dynamic indexing (keeps the arrays in registers)
+#pragma unroll
+    for (int d = 1; d <= 4; ++d) {
+      if (d == t) {
+        goff_t = goff[d];
+        soff_t = soff[d];
+      }
+    }
+    const int gi = rank / group_cap(t), m = rank % group_cap(t);
+    const int g = goff_t + gi, base = soff_t + gi * slot_pitch(t), P = slot_pitch(t);
+    S.slot_ch[base + m] = (int16_t)tid;
     for (int p = 0; p < t; ++p) S.row_of_lane[g * 32 + m * t + (t - 1 - p)] = (int16_t)(tid * 4 + p);
-    // w = q 2^(4 - t - pos) per head, laid out [group][head][slot]
-    const int P = slot_pitch(t);
-    const int base = S.grp_base[g];
+    // w = q 2^(4 - t - pos) per head, laid out [group][head][slot]; other slots stay 0
 #pragma unroll
     for (int hh = 0; hh < GP; ++hh) S.w[base * GP + hh * P + m] = ldexpf(qv[hh], 4 - t - field_pos(t, m));
-  }
-  __syncthreads();
-  // unused slots of partial groups weigh 0; slot -> group map
-  for (int g = 0; g < S.n_groups; ++g) {
-    const int d = S.grp_t[g], P = slot_pitch(d), base = S.grp_base[g], cnt = S.grp_cnt[g];
-    for (int e = tid; e < P * GP; e += kScanThreads) {
-      if (e % P >= cnt) S.w[base * GP + e] = 0.f;
-    }
-    for (int m = tid; m < P; m += kScanThreads) S.slot_grp[base + m] = (int8_t)g;
   }
   __syncthreads();
 }

@@ -118,7 +118,7 @@ def check_unit(orc, cfg, inp, cache, depths, idx, out, s, h, depth_rule=0, fixed
     kb, vb = bits16(inp.k[s, h]), bits16(inp.v[s, h])
     b = int(inp.budgets[s]) if budget_bits is None else budget_bits
     ref = orc.decode_unit(kb, vb, inp.q[s, h].numpy(), inp.sigma2[s, h].numpy(), b, cfg.k, cfg.n_sink,
-                          cfg.n_recent, nb_cap=cfg.cap_tokens // 64,
+                          cfg.n_recent, nb_cap=cache.c.cap_tokens // 64,
                           fixed=fixed if depth_rule == 1 else None)
     nb = (n + 63) // 64
     assert np.array_equal(bits64(cache.planes[s, h])[:, :, :nb], ref["planes"][:, :, :nb]), f"{what} planes"
