@@ -86,7 +86,8 @@ def all_max(x: float, world: int) -> float:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -358,7 +359,8 @@ def bench_ours(args, cfg, rank, world, local):
         hbm, peak_src, bound = link, "of measured (pinned host-to-device copy, 1 GiB)", "host_link"
     achieved = kbytes / (kms / 1e3) / 1e9
     traffic = load_traffic(dom)
-    roofline = {"bound": bound, "kernel": dom, "achieved": round(achieved, 1), "peak": round(hbm, 1),
+    kernel_name = {"scan": "k_scan", "topk": "k_cut", "attend": "k_attend_ranges"}.get(dom, dom)
+    roofline = {"bound": bound, "kernel": kernel_name, "achieved": round(achieved, 1), "peak": round(hbm, 1),
                 "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_source": peak_src,
                 "traffic": traffic, "algorithmic_bytes_per_launch": round(kbytes / n_launch),
                 "launch_us": round(kms * 1e3 / n_launch, 2)}
