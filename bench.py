@@ -358,7 +358,7 @@ def bench_ours(args, cfg, rank, world, local):
         link = link_h2d_gbs(dev)
         hbm, peak_src, bound = link, "of measured (pinned host-to-device copy, 1 GiB)", "host_link"
     achieved = kbytes / (kms / 1e3) / 1e9
-    traffic = load_traffic(dom)
+    traffic = load_traffic(dom, cfg.name, [p["budget"] for p in passes])
     kernel_name = {"scan": "k_scan", "topk": "k_cut", "attend": "k_attend_ranges"}.get(dom, dom)
     roofline = {"bound": bound, "kernel": kernel_name, "achieved": round(achieved, 1), "peak": round(hbm, 1),
                 "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_source": peak_src,
@@ -443,14 +443,16 @@ def bench_e2e(args, passes, io, ws, flush, dev, keys_per_step, world):
             "d2h_bytes_per_step": bo, "ms_per_step": round(ms, 5), "steps": n_e2e}
 
 
-def load_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it still matches
-    the kernel source it was taken from."""
+def load_traffic(kernel: str, workload: str, budgets):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    this workload and budgets and still matches the kernel source."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         d = json.load(open(path))[kernel]
     except Exception:
+        return None
+    if d.get("workload") != workload or list(d.get("budgets_bits", [])) != list(budgets):
         return None
     src = os.path.join(ROOT, "bit_plane_kv_encode_gb300", "csrc", d["source"])
     h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]

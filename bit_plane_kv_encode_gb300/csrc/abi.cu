@@ -29,7 +29,7 @@ cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, in
 cudaError_t launch_front(const bpkv_cache& c, const uint16_t* k_new, const uint16_t* v_new, int32_t t_new,
                          const float* q, const float* sigma2, const int32_t* budget_q, int32_t depth_rule,
                          int32_t n_channels, int32_t depth, uint8_t* depths, void* plan, uint32_t* hist,
-                         uint32_t* ctr, uint32_t* tickets, uint32_t* seq_tick, cudaStream_t st);
+                         uint32_t* hist1, uint32_t* ctr, uint32_t* tickets, uint32_t* seq_tick, cudaStream_t st);
 bool cut_counts_hist(const bpkv_cache& c);
 cudaError_t launch_union(const bpkv_cache& c, const int32_t* idx, int32_t k, int32_t* uidx, uint8_t* umask,
                          int32_t* ucount, cudaStream_t st);
@@ -86,7 +86,7 @@ int check_k(int32_t k, int32_t n_sink, int32_t n_recent) {
 
 // Workspace layout: status word, then the buffers each call family needs.
 struct Layout {
-  size_t scores = 0, hist = 0, ctr = 0, cand = 0, cut = 0, part = 0, depths = 0, idx = 0, uidx = 0, umask = 0,
+  size_t scores = 0, hist = 0, hist1 = 0, ctr = 0, cand = 0, cut = 0, part = 0, depths = 0, idx = 0, uidx = 0, umask = 0,
          ucount = 0, tickets = 0, seq_tick = 0, plan = 0, total = 0;
 };
 
@@ -100,7 +100,8 @@ Layout layout(const bpkv_cache& c, int32_t k, int32_t what) {
     // selection scratch; ctr directly follows hist (one memset clears both)
     const size_t rows = NH * c.group;
     L.hist = off;
-    L.ctr = off + rows * kTopkBins * sizeof(uint32_t);
+    L.hist1 = L.hist + rows * kTopkBins * sizeof(uint32_t);
+    L.ctr = L.hist1 + rows * kTopkBins * sizeof(uint32_t);
     off = align_up(L.ctr + rows * kSelCounters * sizeof(uint32_t));
     L.cand = off;
     off = align_up(off + rows * 1024 * sizeof(unsigned long long));
@@ -145,8 +146,9 @@ Layout layout(const bpkv_cache& c, int32_t k, int32_t what) {
 
 SelBufs sel_bufs(void* ws, const Layout& L) {
   unsigned char* w = static_cast<unsigned char*>(ws);
-  return SelBufs{reinterpret_cast<uint32_t*>(w + L.hist), reinterpret_cast<uint32_t*>(w + L.ctr),
-                 reinterpret_cast<unsigned long long*>(w + L.cand), reinterpret_cast<unsigned long long*>(w + L.cut)};
+  return SelBufs{reinterpret_cast<uint32_t*>(w + L.hist), reinterpret_cast<uint32_t*>(w + L.hist1),
+                 reinterpret_cast<uint32_t*>(w + L.ctr), reinterpret_cast<unsigned long long*>(w + L.cand),
+                 reinterpret_cast<unsigned long long*>(w + L.cut)};
 }
 
 int check_ws(const bpkv_cache& c, int32_t k, int32_t what, void* ws, size_t ws_bytes) {
@@ -256,7 +258,7 @@ int bpkv_scan_topk(const bpkv_cache* c, const float* q, const uint8_t* depths, i
   const SelBufs b = sel_bufs(ws, L);
   cudaStream_t st = as_stream(stream);
   const size_t rows = (size_t)c->n_seq * c->n_kv_heads * c->group;
-  BPKV_TRY(cuda_status(cudaMemsetAsync(b.hist, 0, rows * (kTopkBins + kSelCounters) * sizeof(uint32_t), st)));
+  BPKV_TRY(cuda_status(cudaMemsetAsync(b.hist, 0, rows * (2 * kTopkBins + kSelCounters) * sizeof(uint32_t), st)));
   // the level-0 histograms: counted by the cut kernel when it can, else by the scan
   const bool cut_counts = cut_counts_hist(*c);
   BPKV_TRY(cuda_status(launch_scan(*c, q, depths, scores, c->cap_tokens, st, nullptr, cut_counts ? nullptr : b.hist,
@@ -393,8 +395,11 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
     }
     // append beside depths and plan in one launch; the new token counts in
     // seq_len only from the end of the layer (pending = 1 until then)
+    // long rows (as the cut will see them, with the new token) use the level-1 histograms too
+    const bool l1 = c.n_max + 1 >= kLongRowTokens;
     BPKV_TRY(cuda_status(launch_front(c, kn, vn, 1, q, s2, a->budget_q, a->depth_rule, a->fixed_channels,
-                                      a->fixed_depth, depths, plan, sb.hist, sb.ctr, tickets, seq_tick, st)));
+                                      a->fixed_depth, depths, plan, sb.hist, l1 ? sb.hist1 : nullptr, sb.ctr,
+                                      tickets, seq_tick, st)));
     c.n_max += 1;
     BPKV_TRY(mark(l, 1));
     BPKV_TRY(mark(l, 2));

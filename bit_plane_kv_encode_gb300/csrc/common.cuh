@@ -39,10 +39,11 @@ __device__ __forceinline__ float fp16_bits_to_float(uint16_t b) {
 constexpr int kTopkBins = 4096;  // level-0 histogram: top 12 bits of the ordered key
 
 constexpr int kSelCounters = 4;  // per row: candidates gathered, CTAs done, CTAs at the barrier, spare
+constexpr int64_t kLongRowTokens = 131072;  // rows this long get a parallel level-1 histogram
 
-// Selection scratch for rows = N H G query heads.  hist and ctr must be zero
-// when the selection starts (ctr is left zero by it); hist is followed
-// directly by ctr, so one memset clears both.
+// Selection scratch for rows = N H G query heads.  hist, hist1 and ctr must
+// be zero when the selection starts (ctr is left zero by it); they are
+// contiguous, so one memset clears all three.
 // State of SelBufs::hist and ::ctr when a selection starts.
 enum class HistState {
   kCounted,  // histograms counted (by the scan), counters zero
@@ -51,7 +52,8 @@ enum class HistState {
 };
 
 struct SelBufs {
-  uint32_t* hist;            // [rows][kTopkBins]
+  uint32_t* hist;            // [rows][kTopkBins] level 0: top 12 key bits
+  uint32_t* hist1;           // [rows][kTopkBins] level 1 (next 12 bits) of long rows' bucket keys
   uint32_t* ctr;             // [rows][kSelCounters]
   unsigned long long* cand;  // [rows][1024]
   unsigned long long* cut;   // [rows]

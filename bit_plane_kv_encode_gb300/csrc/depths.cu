@@ -111,6 +111,7 @@ struct FrontArgs {
   DepthArgs d;
   int32_t depth_rule;       // BPKV_DEPTH_WATERFILL or BPKV_DEPTH_FIXED
   uint32_t* seq_tick;       // [N]: zeroed for the attention of this step
+  uint32_t* hist1;          // optional [N][H][G][kTopkBins]: zeroed with the level-0 histograms
   // append
   uint64_t* planes;
   uint16_t* scales;
@@ -139,6 +140,10 @@ __global__ void __launch_bounds__(kScanThreads) k_front(FrontArgs a) {
       uint4* hz = reinterpret_cast<uint4*>(a.d.hist + unit * G * kTopkBins);
       const int e0 = n4 * x / a.enc_ctas, e1 = n4 * (x + 1) / a.enc_ctas;
       for (int e = e0 + threadIdx.x; e < e1; e += blockDim.x) hz[e] = make_uint4(0u, 0u, 0u, 0u);
+      if (a.hist1) {
+        uint4* hz1 = reinterpret_cast<uint4*>(a.hist1 + unit * G * kTopkBins);
+        for (int e = e0 + threadIdx.x; e < e1; e += blockDim.x) hz1[e] = make_uint4(0u, 0u, 0u, 0u);
+      }
       if (x == 0 && (int)threadIdx.x < kSelCounters * G) a.d.ctr[unit * kSelCounters * G + threadIdx.x] = 0u;
     }
     // CTA x: block n_old / 64 + x / 2, channels 64 (x % 2) ..
@@ -172,11 +177,12 @@ __global__ void __launch_bounds__(kScanThreads) k_front(FrontArgs a) {
 cudaError_t launch_front(const bpkv_cache& c, const uint16_t* k_new, const uint16_t* v_new, int32_t t_new,
                          const float* q, const float* sigma2, const int32_t* budget_q, int32_t depth_rule,
                          int32_t n_channels, int32_t depth, uint8_t* depths, void* plan, uint32_t* hist,
-                         uint32_t* ctr, uint32_t* tickets, uint32_t* seq_tick, cudaStream_t st) {
+                         uint32_t* hist1, uint32_t* ctr, uint32_t* tickets, uint32_t* seq_tick, cudaStream_t st) {
   FrontArgs a;
   a.d = DepthArgs{q, sigma2, budget_q, depths, c.n_kv_heads, c.group, tickets, plan, n_channels, depth, hist, ctr};
   a.depth_rule = depth_rule;
   a.seq_tick = seq_tick;
+  a.hist1 = hist1;
   a.planes = c.planes;
   a.scales = c.scales;
   a.k_rows = c.k_rows;

@@ -69,11 +69,11 @@ extern "C" int bpkv_scan_topk_noalloc(const bpkv_cache* c, const float* q, const
   if (!is_aligned(c->planes, 16) || !is_aligned(c->scales, 16) || !is_aligned(c->seq_len, 8)) return BPKV_EINVAL;
   if (n_sink < 0 || n_recent < 0 || k < 1 || k > 8192 || (int64_t)n_sink + n_recent > k) return BPKV_EINVAL;
   // scores [rows][ld] with ld = n_max rounded up to 64 floats, then per row a
-  // level-0 histogram and its counters, 1024 candidates and the cut
+  // level-0 and level-1 histogram and its counters, 1024 candidates and the cut
   const size_t rows = (size_t)c->n_seq * c->n_kv_heads * c->group;
   const int64_t ld = (c->n_max + 63) / 64 * 64;
   const size_t off_hist = round256(rows * (size_t)ld * sizeof(float));
-  const size_t off_cand = round256(off_hist + rows * (kTopkBins + kSelCounters) * sizeof(uint32_t));
+  const size_t off_cand = round256(off_hist + rows * (2 * kTopkBins + kSelCounters) * sizeof(uint32_t));
   const size_t off_cut = round256(off_cand + rows * 1024 * sizeof(unsigned long long));
   const size_t need = off_cut + rows * sizeof(unsigned long long);
   if (need > kNoallocScratchBytes) return BPKV_ENOWORKSPACE;
@@ -84,9 +84,10 @@ extern "C" int bpkv_scan_topk_noalloc(const bpkv_cache* c, const float* q, const
   float* scores = reinterpret_cast<float*>(base);
   SelBufs b{reinterpret_cast<uint32_t*>(base + off_hist),
             reinterpret_cast<uint32_t*>(base + off_hist + rows * kTopkBins * sizeof(uint32_t)),
+            reinterpret_cast<uint32_t*>(base + off_hist + 2 * rows * kTopkBins * sizeof(uint32_t)),
             reinterpret_cast<unsigned long long*>(base + off_cand), reinterpret_cast<unsigned long long*>(base + off_cut)};
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(b.hist, 0, rows * (kTopkBins + kSelCounters) * sizeof(uint32_t), st) != cudaSuccess)
+  if (cudaMemsetAsync(b.hist, 0, rows * (2 * kTopkBins + kSelCounters) * sizeof(uint32_t), st) != cudaSuccess)
     return BPKV_ECUDA;
   const bool cut_counts = cut_counts_hist(*c);
   if (ld > 0 &&

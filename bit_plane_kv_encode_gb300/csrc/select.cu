@@ -135,6 +135,7 @@ struct CutArgs {
   int64_t ld;
   const int64_t* seq_len;
   uint32_t* hist;              // [rows][kTopkBins] level-0 histograms of the middle keys
+  const uint32_t* hist1;       // optional [rows][kTopkBins] level-1 histograms of the level-0 bucket
   unsigned long long* cand;    // [rows][kRankCap] candidate (key, ~index) values
   uint32_t* ctr;               // [rows][kSelCounters]: zero on entry, left zero
   unsigned long long* cut;     // [rows] out
@@ -227,12 +228,11 @@ __device__ __forceinline__ void rank_cut(CutSmem& S, int nc, uint32_t rem) {
   }
 }
 
-// The cut of a row whose level-0 bucket (S.tb, S.nb keys) holds more than
-// kRankCap keys, by one CTA streaming the row's middle keys.
-__device__ void cut_refine(CutSmem& S, const float* __restrict__ sc, int64_t lo, int64_t cnt, uint32_t rem) {
+// The cut of a row whose bucket (key bits prefix at level lvl, S.nb keys)
+// holds more than kRankCap keys, by one CTA streaming the row's middle keys.
+__device__ void cut_refine(CutSmem& S, const float* __restrict__ sc, int64_t lo, int64_t cnt, uint32_t rem,
+                           uint32_t prefix, int lvl) {
   const int tid = threadIdx.x;
-  uint32_t prefix = S.tb;
-  int lvl = 0;
   while (lvl < 2 && S.nb > (uint32_t)kRankCap) {
     const int nl = lvl + 1, pre_sh = level_shift(lvl), sh = level_shift(nl);
     const uint32_t bmask = (uint32_t)level_bins(nl) - 1u;
@@ -363,13 +363,24 @@ __global__ void __launch_bounds__(kCutThreads, 2) k_cut(CutArgs a) {
   }
   if (tid == 0) S.cut = ~0ull;
   find_bucket(S, h, top, (uint32_t)r.m);
-  const uint32_t tb = S.tb, nb = S.nb, rem = S.rem;
+  uint32_t prefix = S.tb, nb = S.nb, rem = S.rem;
+  int lvl = 0;
+  if (nb > (uint32_t)kRankCap && a.hist1) {
+    // the level-1 histogram of this bucket (counted by k_hist1) narrows it
+    const int top1 = bins_of_thread(a.hist1 + (int64_t)row * kTopkBins, kTopkBins, h);
+    find_bucket(S, h, top1, rem);
+    prefix = (prefix << 12) | S.tb;
+    nb = S.nb;
+    rem = S.rem;
+    lvl = 1;
+  }
+  const int sh = level_shift(lvl);
   if (nb <= (uint32_t)kRankCap) {
     // this CTA's bucket keys: one returning atomic per warp for the warp's matches
     uint32_t match = 0;
 #pragma unroll
     for (int b = 0; b < kSelBatch; ++b)
-      if (((valid >> b) & 1u) && (keys[b] >> 20) == tb) match |= 1u << b;
+      if (((valid >> b) & 1u) && (keys[b] >> sh) == prefix) match |= 1u << b;
     const uint32_t cnt = __popc(match);
     uint32_t incl = cnt;
 #pragma unroll
@@ -409,12 +420,9 @@ __global__ void __launch_bounds__(kCutThreads, 2) k_cut(CutArgs a) {
     rank_cut(S, nc, rem);
   } else {
     // refine in the shared histogram buffer
-    if (tid == 0) {
-      S.nb = nb;
-      S.tb = tb;
-    }
+    if (tid == 0) S.nb = nb;
     __syncthreads();
-    cut_refine(S, sc, r.lo, r.cnt, rem);
+    cut_refine(S, sc, r.lo, r.cnt, rem, prefix, lvl);
   }
   __syncthreads();
   if (tid == 0) {
@@ -423,6 +431,40 @@ __global__ void __launch_bounds__(kCutThreads, 2) k_cut(CutArgs a) {
 #pragma unroll
     for (int i = 0; i < kSelCounters; ++i) ctr[i] = 0u;  // every CTA of the row is past its waits
   }
+}
+
+// ------------------------------------------------------------------ k_hist1
+
+// Level-1 histogram (key bits 19..8) of the keys in each long row's level-0
+// bucket, counted by all chunk CTAs of the row.  Grid (chunks, rows); rows
+// whose bucket needs no refinement return at once.
+__global__ void __launch_bounds__(kCutThreads, 2) k_hist1(CutArgs a) {
+  pdl_enter();
+  __shared__ CutSmem S;
+  const int row = blockIdx.y, tid = threadIdx.x;
+  uint32_t h[kBinsPerThread];
+  const int top = bins_of_thread(a.hist + (int64_t)row * kTopkBins, kTopkBins, h);
+  const RowRange r = row_range(a.seq_len[row / a.rows_per_seq] + a.pending, a.k, a.n_sink, a.n_recent);
+  const int64_t c0 = (int64_t)blockIdx.x * kCutChunk, c1 = min64(c0 + kCutChunk, r.cnt);
+  if (r.cnt <= r.m || r.m == 0 || c0 >= c1) return;
+  find_bucket(S, h, top, (uint32_t)r.m);
+  const uint32_t tb = S.tb;
+  if (S.nb <= (uint32_t)kRankCap) return;
+  const float* sc = a.scores + (int64_t)row * a.ld;
+  float v[kSelBatch];
+#pragma unroll
+  for (int b = 0; b < kSelBatch; ++b) v[b] = sc[r.lo + min64(c0 + tid + (int64_t)b * kCutThreads, c1 - 1)];
+  for (int b = tid; b < kTopkBins; b += kCutThreads) S.hist[b] = 0u;
+  __syncthreads();
+#pragma unroll
+  for (int b = 0; b < kSelBatch; ++b) {
+    const uint32_t key = ordered_key(v[b]);
+    if (c0 + tid + (int64_t)b * kCutThreads < c1 && (key >> 20) == tb) atomicAdd(&S.hist[(key >> 8) & 0xFFFu], 1u);
+  }
+  __syncthreads();
+  uint32_t* g1 = const_cast<uint32_t*>(a.hist1) + (int64_t)row * kTopkBins;
+  for (int b = tid; b < kTopkBins; b += kCutThreads)
+    if (S.hist[b]) atomicAdd(g1 + b, S.hist[b]);
 }
 
 // ------------------------------------------------------------------ k_lists
@@ -543,13 +585,22 @@ bool cut_counts_hist(const bpkv_cache& c) {
   return n > 0 && grid <= n;
 }
 
+// Rows long enough that the level-0 bucket usually exceeds kRankCap keys get
+// a parallel level-1 histogram (k_hist1) before the cut.
+bool long_rows(const bpkv_cache& c) { return c.n_max >= kLongRowTokens; }
+
 cudaError_t launch_cut(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
                        int32_t n_recent, const SelBufs& b, bool build_hist, int32_t pending, int32_t* status,
                        cudaStream_t st) {
-  CutArgs a{scores,   ld,     c.seq_len,  b.hist, b.cand, b.ctr, b.cut, status, c.n_kv_heads * c.group, k, n_sink,
-            n_recent, build_hist ? 1 : 0, pending};
+  const bool l1 = !build_hist && long_rows(c);
+  CutArgs a{scores,   ld,           c.seq_len, b.hist, l1 ? b.hist1 : nullptr, b.cand, b.ctr, b.cut, status,
+            c.n_kv_heads * c.group, k, n_sink, n_recent, build_hist ? 1 : 0, pending};
   const dim3 grid((unsigned)cut_chunks(c), (unsigned)(c.n_seq * c.n_kv_heads * c.group));
   if (build_hist) return launch_coop_pdl(k_cut, grid, dim3(kCutThreads), 0, st, a);
+  if (l1) {
+    const cudaError_t e = launch_pdl(k_hist1, grid, dim3(kCutThreads), 0, st, a);
+    if (e != cudaSuccess) return e;
+  }
   return launch_pdl(k_cut, grid, dim3(kCutThreads), 0, st, a);
 }
 
@@ -574,7 +625,7 @@ cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, in
   bool build = false;
   if (hs == HistState::kDirty) {
     const size_t rows = (size_t)c.n_seq * c.n_kv_heads * c.group;
-    e = cudaMemsetAsync(b.hist, 0, rows * (kTopkBins + kSelCounters) * sizeof(uint32_t), st);
+    e = cudaMemsetAsync(b.hist, 0, rows * (2 * kTopkBins + kSelCounters) * sizeof(uint32_t), st);
     if (e != cudaSuccess) return e;
   }
   if (hs != HistState::kCounted) {

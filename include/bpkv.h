@@ -193,7 +193,7 @@ int bpkv_scan_topk(const bpkv_cache *c, const float *q, const uint8_t *depths, i
  * The scratch (scores and selection buffers) is a fixed 16 MiB array built
  * into the library, held on every GPU that loads the library until the
  * process exits; requests needing more (rows = N * H * G; rows *
- * (4 * round_up(n_max, 64) + 24600) bytes plus under 1 KiB of alignment
+ * (4 * round_up(n_max, 64) + 40984) bytes plus under 1 KiB of alignment
  * > 16 MiB) return BPKV_ENOWORKSPACE.  The call allocates nothing (no
  * cudaMalloc, cudaFree or allocating library routine); it enqueues a memset of
  * the selection counters.  Its first call on a device looks up the

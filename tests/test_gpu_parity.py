@@ -343,3 +343,19 @@ def test_scan_topk_histogram_matches_topk(pk, n, G, budget):
     pk.bpkv_topk(c.c, scores, ld, k, 4, 32, idx_b, ws, ws.numel())
     assert pk.bpkv_read_status(ws) == 0
     assert torch.equal(idx_a, idx_b)
+
+
+@pytest.mark.parametrize("n,ties", [(140000, 0.0), (150001, 0.9)])
+def test_topk_long_rows_level1(pk, orc, n, ties):
+    """Rows of at least 131072 keys over a grid too large to run cooperatively:
+    the level-1 histogram (k_hist1) narrows the level-0 bucket before the cut."""
+    from workload.gen import random_scores
+    N, H, G, k = 1, 4, 4, 512
+    kk, vv = _rand_kv(N, H, n, seed=14)
+    c = build_cache(kk, vv, G)
+    sc = random_scores(N * H * G, n, seed=n, tie_frac=ties).reshape(N, H, G, n)
+    got = _topk_rows(pk, c, sc, k)
+    for h in range(H):
+        for g in range(G):
+            want = orc.topk(sc[0, h, g].numpy().astype(np.float64), k)
+            assert np.array_equal(got[0, h, g], want), (h, g)

@@ -51,7 +51,7 @@ def test_noalloc_matches_workspace_call_twice(pk):
 
 
 def test_noalloc_refuses_oversized_request(pk):
-    # rows (4 round_up(n, 64) + 24600) bytes with rows = N H G = 64: 64 x (262400 + 24600) > 16 MiB
+    # rows (4 round_up(n, 64) + 40984) bytes with rows = N H G = 64: 64 x (262400 + 40984) > 16 MiB
     cache, g = _case(pk, 65600, 16, seed=22)
     q = torch.randn((1, 16, 4, 128), generator=g).cuda()
     depths = torch.full((1, 16, 128), 1, dtype=torch.uint8, device="cuda")
