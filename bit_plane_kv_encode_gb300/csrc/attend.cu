@@ -11,6 +11,8 @@
 // Dense: the same with rows = all stored tokens and every head selected.
 #include "common.cuh"
 
+#include <algorithm>
+
 namespace bpkv {
 
 constexpr int kAttnThreads = 128;
@@ -234,13 +236,15 @@ __global__ void __launch_bounds__(kD) k_attend_combine(AttnArgs a, float* out) {
 // step) merges them by log-sum-exp and resets it.
 constexpr int kRangeThreads = 256;
 constexpr int kRangeMaxRows = 2048;   // union rows of one range (<= min(range tokens, G k))
-constexpr int kRangeMaxRanges = 24;   // ranges per unit (the merge holds all of a unit's in registers)
+constexpr int kRangeMaxRanges = 64;   // ranges per unit (long sequences; 24 up to 24 x 4096 tokens)
+constexpr int kMergeBlock = 24;       // ranges whose partial outputs the merge holds in registers at once
 constexpr int kRangeAlign = 512;      // range sizes are multiples of this
-constexpr int kRangeWin = 2048;       // selection window (its scores fill the logit buffer at G = 8)
+constexpr int kRangeWin = 4096;       // selection window
+constexpr int kWinQuads = kRangeWin / 4 / kRangeThreads;  // 4-token quads per thread and window
+// quads whose scores a thread loads at once (fewer with more heads: registers)
+template <int GP>
+__host__ __device__ constexpr int win_batch() { return GP >= 8 ? kWinQuads / 2 : kWinQuads; }
 constexpr int kQPitch = 36;           // floats per (head, quarter) row of q in shared memory
-// (range, head) partials the merge stages at once: 3 kRangeMaxRanges G floats of
-// weights and n kD floats of outputs within the kRangeMaxRows G float logit buffer
-constexpr int kMergeEntries = (kRangeMaxRows * BPKV_MAX_GROUP - 3 * kRangeMaxRanges * BPKV_MAX_GROUP) / kD;
 
 struct RangeArgs {
   const uint16_t* k_rows;
@@ -305,7 +309,7 @@ __global__ void __launch_bounds__(kRangeThreads, 512 / kRangeThreads) k_attend_r
   }
   __syncthreads();
   // selection, in windows of kRangeWin tokens: thread = 4-token quads, all
-  // heads' scores of a quad loaded at once (two quads in flight); the quads'
+  // heads' scores of a quad loaded at once (kWinQuads quads in flight); the quads'
   // head masks go to shared memory, then each thread compacts a run of
   // consecutive tokens in order.
   const float* sc = a.scores + unit * G * a.ld;
@@ -315,17 +319,18 @@ __global__ void __launch_bounds__(kRangeThreads, 512 / kRangeThreads) k_attend_r
     const int wl = (int)min64(kRangeWin, t1 - w0);
     const int wq = (wl + 3) / 4;  // score rows hold whole quads (their length is a multiple of 4)
     __syncthreads();              // the previous window is done
-    for (int q0 = tid; q0 < wq; q0 += 2 * kRangeThreads) {
-      float4 v[2][GP];
+    constexpr int WB = win_batch<GP>();
+    for (int q0 = tid; q0 < wq; q0 += WB * kRangeThreads) {
+      float4 v[WB][GP];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < WB; ++u) {
         const int qd = min(q0 + u * kRangeThreads, wq - 1);  // unconditional loads
 #pragma unroll
         for (int g = 0; g < GP; ++g)
           if (g < G) v[u][g] = *reinterpret_cast<const float4*>(sc + g * a.ld + w0 + 4 * qd);
       }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < WB; ++u) {
         const int qd = q0 + u * kRangeThreads;
         if (qd >= wq) break;
         uint32_t packed = 0;
@@ -550,51 +555,63 @@ __global__ void __launch_bounds__(kRangeThreads, 512 / kRangeThreads) k_attend_r
   }
   __syncthreads();
   if (!S.is_last) return;
-  // merge: thread = (head, two channels) with its outputs of every range in
-  // flight; warp g < G meanwhile reduces head g's (max, sum) pairs across the
-  // ranges (lane = range) into weights 2^(m_c - M) and L (a fixed-order warp
-  // scan); the outputs are summed in range order
+  // merge: thread = (head, two channels) with its outputs of kMergeBlock
+  // ranges in flight at a time; warp g < G meanwhile reduces head g's (max,
+  // sum) pairs across the ranges (lane = range mod 32) into weights
+  // 2^(m_c - M) and L (fixed-order sums); the outputs are summed in range order
   const float* pu = a.part + unit * a.n_ranges * G * kPartStride;
   float* pw = &S.logit[0][0];  // [n_ranges][G] weights
-  static_assert(kRangeMaxRanges <= 32, "one lane per range");
+  static_assert(kRangeMaxRanges <= 64, "two ranges per lane");
   for (int e0 = 0; e0 < G * (kD / 2); e0 += kRangeThreads) {
     const int e = e0 + tid;
     const int g = min(e, G * (kD / 2) - 1) / (kD / 2), d2 = e % (kD / 2);
-    float2 ov[kRangeMaxRanges];
-#pragma unroll
-    for (int c = 0; c < kRangeMaxRanges; ++c)  // unconditional loads
-      ov[c] = __ldcg(reinterpret_cast<const float2*>(pu + (min(c, a.n_ranges - 1) * G + g) * kPartStride) + d2);
-    if (e0 == 0) {
-      if (warp < G) {
-        const int gw = warp, c = lane;
-        const bool in = c < a.n_ranges;
-        const float* pc = pu + (min(c, a.n_ranges - 1) * G + gw) * kPartStride;
-        const float mc = __ldcg(pc + kD), lc = __ldcg(pc + kD + 1);
-        const bool live = in && lc > 0.f;
-        float Mx = live ? mc : -INFINITY;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
-        const float wc = live ? exp2f(mc - Mx) : 0.f;
-        // L: inclusive scan over the lanes, the last lane holds the total
-        float x = wc * lc;
-        if (!live) x = 0.f;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y = __shfl_up_sync(0xffffffffu, x, o);
-          if (lane >= o) x += y;
-        }
-        if (in) pw[c * G + gw] = wc;
-        if (lane == 31) S.lslot[0][gw] = x;
-      }
-      __syncthreads();
-    }
     float O0 = 0.f, O1 = 0.f;
+    for (int cb = 0; cb < a.n_ranges; cb += kMergeBlock) {
+      float2 ov[kMergeBlock];
 #pragma unroll
-    for (int c = 0; c < kRangeMaxRanges; ++c) {
-      if (c < a.n_ranges) {
-        const float wc = pw[c * G + g];
-        O0 = fmaf(wc, ov[c].x, O0);
-        O1 = fmaf(wc, ov[c].y, O1);
+      for (int c = 0; c < kMergeBlock; ++c)  // unconditional loads
+        ov[c] = __ldcg(reinterpret_cast<const float2*>(pu + (min(cb + c, a.n_ranges - 1) * G + g) * kPartStride) + d2);
+      if (e0 == 0 && cb == 0) {
+        if (warp < G) {
+          const int gw = warp;
+          float mc[2], lc[2];
+          bool live[2];
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int c = lane + 32 * i;
+            const float* pc = pu + (min(c, a.n_ranges - 1) * G + gw) * kPartStride;
+            mc[i] = __ldcg(pc + kD);
+            lc[i] = __ldcg(pc + kD + 1);
+            live[i] = c < a.n_ranges && lc[i] > 0.f;
+          }
+          float Mx = fmaxf(live[0] ? mc[0] : -INFINITY, live[1] ? mc[1] : -INFINITY);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
+          float x = 0.f;
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int c = lane + 32 * i;
+            const float wc = live[i] ? exp2f(mc[i] - Mx) : 0.f;
+            if (live[i]) x += wc * lc[i];
+            if (c < a.n_ranges) pw[c * G + gw] = wc;
+          }
+          // L: inclusive scan over the lanes, the last lane holds the total
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+          }
+          if (lane == 31) S.lslot[0][gw] = x;
+        }
+        __syncthreads();
+      }
+#pragma unroll
+      for (int c = 0; c < kMergeBlock; ++c) {
+        if (cb + c < a.n_ranges) {
+          const float wc = pw[(cb + c) * G + g];
+          O0 = fmaf(wc, ov[c].x, O0);
+          O1 = fmaf(wc, ov[c].y, O1);
+        }
       }
     }
     const float L = S.lslot[0][g];
@@ -613,14 +630,18 @@ __global__ void __launch_bounds__(kRangeThreads, 512 / kRangeThreads) k_attend_r
   }
 }
 
-// Tokens per range: a multiple of kRangeAlign, with at most kRangeMaxRanges ranges
-// per unit and at most kMergeEntries (range, head) partials (the merge stages
-// them all in the logit buffer).
+// Tokens per range: a multiple of kRangeAlign; up to kMergeBlock ranges per
+// unit while a range stays within one selection window, up to
+// kRangeMaxRanges for longer sequences.
 int64_t range_tokens(int64_t n_max, int group) {
-  const int64_t max_ranges = min64(kRangeMaxRanges, kMergeEntries / group);
-  int64_t rt = (n_max + max_ranges - 1) / max_ranges;
-  rt = (rt + kRangeAlign - 1) / kRangeAlign * kRangeAlign;
-  return rt < kRangeAlign ? kRangeAlign : rt;
+  (void)group;
+  auto size_for = [&](int64_t ranges) {
+    int64_t rt = (n_max + ranges - 1) / ranges;
+    rt = (rt + kRangeAlign - 1) / kRangeAlign * kRangeAlign;
+    return rt < kRangeAlign ? (int64_t)kRangeAlign : rt;
+  };
+  const int64_t rt = size_for(kMergeBlock);
+  return rt <= kRangeWin ? rt : std::max<int64_t>(kRangeWin, size_for(kRangeMaxRanges));
 }
 
 size_t attend_ranges_part_bytes(const bpkv_cache& c) {

@@ -105,16 +105,19 @@ struct HistArgs {
   const int64_t* seq_len;
   uint32_t* hist;  // [rows][kTopkBins], zero on entry
   int32_t rows_per_seq, k, n_sink, n_recent;
-  int32_t pending;  // tokens appended in this step but not yet in seq_len
+  int32_t pending;         // tokens appended in this step but not yet in seq_len
+  int32_t chunks_per_cta;  // consecutive chunks of kCutChunk keys per CTA
 };
 
-// Level-0 histogram of one chunk of one row's middle keys.  Grid (chunks, rows).
+// Level-0 histogram of a run of chunks of one row's middle keys, counted in
+// shared memory and added to the row's once.  Grid (runs, rows).
 __global__ void __launch_bounds__(kCutThreads) k_hist(HistArgs a) {
   pdl_enter();
   __shared__ uint32_t H[kTopkBins];
   const int row = blockIdx.y;
   const RowRange r = row_range(a.seq_len[row / a.rows_per_seq] + a.pending, a.k, a.n_sink, a.n_recent);
-  const int64_t c0 = (int64_t)blockIdx.x * kCutChunk, c1 = min64(c0 + kCutChunk, r.cnt);
+  const int64_t c0 = (int64_t)blockIdx.x * a.chunks_per_cta * kCutChunk;
+  const int64_t c1 = min64(c0 + (int64_t)a.chunks_per_cta * kCutChunk, r.cnt);
   if (r.cnt <= r.m || r.m == 0 || c0 >= c1) return;
   for (int b = threadIdx.x; b < kTopkBins; b += kCutThreads) H[b] = 0u;
   __syncthreads();
@@ -143,6 +146,7 @@ struct CutArgs {
   int32_t rows_per_seq, k, n_sink, n_recent;
   int32_t build_hist;          // count hist here (zero on entry; cooperative launch) instead of reading it
   int32_t pending;             // tokens appended in this step but not yet in seq_len
+  int32_t chunks_per_cta;      // consecutive chunks of kCutChunk keys per CTA (1 when build_hist)
 };
 
 struct __align__(16) CutSmem {
@@ -164,6 +168,7 @@ constexpr int kBinsPerThread = kTopkBins / kCutThreads;  // 16
 // 0 hold 0).  Finds the bin holding the rem-th largest key and the rank left
 // within it: whole block (kCutThreads); writes S.tb, S.rem, S.nb.
 __device__ void find_bucket(CutSmem& S, const uint32_t (&h)[kBinsPerThread], int top, uint32_t rem) {
+  __syncthreads();  // every thread has read the previous call's S.tb, S.rem, S.nb
   if (threadIdx.x == 0) {
     S.tb = 0u;
     S.rem = 0u;
@@ -332,10 +337,13 @@ __global__ void __launch_bounds__(kCutThreads, 2) k_cut(CutArgs a) {
   const float* sc = a.scores + (int64_t)row * a.ld;
   uint32_t* ctr = a.ctr + (int64_t)kSelCounters * row;
   unsigned long long* cand = a.cand + (int64_t)row * kRankCap;
-  // this CTA's keys, all loads in flight
-  const int64_t c0 = (int64_t)blockIdx.x * kCutChunk, c1 = min64(c0 + kCutChunk, r.cnt);
+  // this CTA's run of chunks; a chunk's keys, all loads in flight
+  const int64_t run0 = (int64_t)blockIdx.x * a.chunks_per_cta;
   uint32_t keys[kSelBatch], valid = 0;
-  if (c0 < c1) {
+  auto load_chunk = [&](int64_t ch) {
+    const int64_t c0 = ch * kCutChunk, c1 = min64(c0 + kCutChunk, r.cnt);
+    valid = 0;
+    if (c0 >= c1) return;
     float v[kSelBatch];
 #pragma unroll
     for (int b = 0; b < kSelBatch; ++b) v[b] = sc[r.lo + min64(c0 + tid + (int64_t)b * kCutThreads, c1 - 1)];
@@ -344,11 +352,12 @@ __global__ void __launch_bounds__(kCutThreads, 2) k_cut(CutArgs a) {
       keys[b] = ordered_key(v[b]);
       if (c0 + tid + (int64_t)b * kCutThreads < c1) valid |= 1u << b;
     }
-  }
+  };
   if (a.build_hist) {
-    // level-0 histogram: counted per CTA in shared memory, added to the row's
-    // with one atomic per non-empty bin, then every CTA of the row waits for
-    // the others (the grid is launched cooperatively)
+    // level-0 histogram (one chunk per CTA): counted per CTA in shared memory,
+    // added to the row's with one atomic per non-empty bin, then every CTA of
+    // the row waits for the others (the grid is launched cooperatively)
+    load_chunk(run0);
     for (int b = tid; b < kTopkBins; b += kCutThreads) S.hist[b] = 0u;
     __syncthreads();
 #pragma unroll
@@ -376,29 +385,34 @@ __global__ void __launch_bounds__(kCutThreads, 2) k_cut(CutArgs a) {
   }
   const int sh = level_shift(lvl);
   if (nb <= (uint32_t)kRankCap) {
-    // this CTA's bucket keys: one returning atomic per warp for the warp's matches
-    uint32_t match = 0;
+    // the run's bucket keys: one returning atomic per warp and chunk for the warp's matches
+    for (int64_t ch = run0; ch < run0 + a.chunks_per_cta; ++ch) {
+      if (!a.build_hist) load_chunk(ch);
+      const int64_t c0 = ch * kCutChunk;
+      uint32_t match = 0;
 #pragma unroll
-    for (int b = 0; b < kSelBatch; ++b)
-      if (((valid >> b) & 1u) && (keys[b] >> sh) == prefix) match |= 1u << b;
-    const uint32_t cnt = __popc(match);
-    uint32_t incl = cnt;
+      for (int b = 0; b < kSelBatch; ++b)
+        if (((valid >> b) & 1u) && (keys[b] >> sh) == prefix) match |= 1u << b;
+      const uint32_t cnt = __popc(match);
+      uint32_t incl = cnt;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const uint32_t warp_total = __shfl_sync(0xffffffffu, incl, 31);
-    uint32_t base = 0;
-    if (lane == 31 && warp_total) base = atomicAdd(ctr, warp_total);
-    base = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t warp_total = __shfl_sync(0xffffffffu, incl, 31);
+      if (warp_total == 0u) continue;  // uniform across the warp
+      uint32_t base = 0;
+      if (lane == 31) base = atomicAdd(ctr, warp_total);
+      base = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
 #pragma unroll
-    for (int b = 0; b < kSelBatch; ++b) {
-      if ((match >> b) & 1u) {
-        if (base < (uint32_t)kRankCap)
-          cand[base] = ((unsigned long long)keys[b] << 32) |
-                       (0xFFFFFFFFu - (uint32_t)(r.lo + c0 + tid + (int64_t)b * kCutThreads));
-        ++base;
+      for (int b = 0; b < kSelBatch; ++b) {
+        if ((match >> b) & 1u) {
+          if (base < (uint32_t)kRankCap)
+            cand[base] = ((unsigned long long)keys[b] << 32) |
+                         (0xFFFFFFFFu - (uint32_t)(r.lo + c0 + tid + (int64_t)b * kCutThreads));
+          ++base;
+        }
       }
     }
   }
@@ -436,8 +450,8 @@ __global__ void __launch_bounds__(kCutThreads, 2) k_cut(CutArgs a) {
 // ------------------------------------------------------------------ k_hist1
 
 // Level-1 histogram (key bits 19..8) of the keys in each long row's level-0
-// bucket, counted by all chunk CTAs of the row.  Grid (chunks, rows); rows
-// whose bucket needs no refinement return at once.
+// bucket, counted by all CTAs of the row over their runs of chunks.  Grid
+// (runs, rows); rows whose bucket needs no refinement return at once.
 __global__ void __launch_bounds__(kCutThreads, 2) k_hist1(CutArgs a) {
   pdl_enter();
   __shared__ CutSmem S;
@@ -445,22 +459,17 @@ __global__ void __launch_bounds__(kCutThreads, 2) k_hist1(CutArgs a) {
   uint32_t h[kBinsPerThread];
   const int top = bins_of_thread(a.hist + (int64_t)row * kTopkBins, kTopkBins, h);
   const RowRange r = row_range(a.seq_len[row / a.rows_per_seq] + a.pending, a.k, a.n_sink, a.n_recent);
-  const int64_t c0 = (int64_t)blockIdx.x * kCutChunk, c1 = min64(c0 + kCutChunk, r.cnt);
-  if (r.cnt <= r.m || r.m == 0 || c0 >= c1) return;
+  const int64_t e0 = (int64_t)blockIdx.x * a.chunks_per_cta * kCutChunk;
+  const int64_t e1 = min64(e0 + (int64_t)a.chunks_per_cta * kCutChunk, r.cnt);
+  if (r.cnt <= r.m || r.m == 0 || e0 >= e1) return;
   find_bucket(S, h, top, (uint32_t)r.m);
   const uint32_t tb = S.tb;
   if (S.nb <= (uint32_t)kRankCap) return;
-  const float* sc = a.scores + (int64_t)row * a.ld;
-  float v[kSelBatch];
-#pragma unroll
-  for (int b = 0; b < kSelBatch; ++b) v[b] = sc[r.lo + min64(c0 + tid + (int64_t)b * kCutThreads, c1 - 1)];
   for (int b = tid; b < kTopkBins; b += kCutThreads) S.hist[b] = 0u;
   __syncthreads();
-#pragma unroll
-  for (int b = 0; b < kSelBatch; ++b) {
-    const uint32_t key = ordered_key(v[b]);
-    if (c0 + tid + (int64_t)b * kCutThreads < c1 && (key >> 20) == tb) atomicAdd(&S.hist[(key >> 8) & 0xFFFu], 1u);
-  }
+  for_row_keys(a.scores + (int64_t)row * a.ld, r.lo, e0, e1, [&](int64_t, uint32_t key) {
+    if ((key >> 20) == tb) atomicAdd(&S.hist[(key >> 8) & 0xFFFu], 1u);
+  });
   __syncthreads();
   uint32_t* g1 = const_cast<uint32_t*>(a.hist1) + (int64_t)row * kTopkBins;
   for (int b = tid; b < kTopkBins; b += kCutThreads)
@@ -554,33 +563,47 @@ size_t cut_scratch_bytes(const bpkv_cache& c) {
   return rows * ((size_t)kRankCap * 8 + kSelCounters * 4 + 8);
 }
 
-cudaError_t launch_hist(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
-                        int32_t n_recent, uint32_t* hist, int32_t pending, cudaStream_t st) {
-  HistArgs a{scores, ld, c.seq_len, hist, c.n_kv_heads * c.group, k, n_sink, n_recent, pending};
-  const dim3 grid((unsigned)cut_chunks(c), (unsigned)(c.n_seq * c.n_kv_heads * c.group));
-  return launch_pdl(k_hist, grid, dim3(kCutThreads), 0, st, a);
-}
-
-// Whether the cut kernel can count the level-0 histograms itself: its whole
-// grid must be resident at once (cooperative launch).
-bool cut_counts_hist(const bpkv_cache& c) {
+// Resident CTAs of k_cut on the current device (looked up once per device); 0 if unknown.
+int cut_slots() {
   constexpr int kDevs = 64;
   static int slots[kDevs] = {};
   static std::mutex mu;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return false;
-  int n = 0;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (slots[dev] == 0) {
-      int sms = 0, per_sm = 0, coop = 0;
-      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
-      if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop) return false;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_cut, kCutThreads, 0) != cudaSuccess) return false;
-      slots[dev] = sms * per_sm > 0 ? sms * per_sm : -1;
-    }
-    n = slots[dev];
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (slots[dev] == 0) {
+    int sms = 0, per_sm = 0, coop = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_cut, kCutThreads, 0) != cudaSuccess) return 0;
+    slots[dev] = (coop && sms * per_sm > 0) ? sms * per_sm : -1;
   }
+  return slots[dev] > 0 ? slots[dev] : 0;
+}
+
+// Chunks per CTA so that the (runs, rows) grid fits in about one wave.
+int32_t chunks_per_cta(const bpkv_cache& c) {
+  const int64_t rows = (int64_t)c.n_seq * c.n_kv_heads * c.group, chunks = cut_chunks(c);
+  const int64_t slots = cut_slots() > 0 ? cut_slots() : 2 * 152;
+  const int64_t cpc = (chunks * rows + slots - 1) / slots;
+  return (int32_t)(cpc < 1 ? 1 : cpc);
+}
+
+dim3 run_grid(const bpkv_cache& c, int32_t cpc) {
+  return dim3((unsigned)((cut_chunks(c) + cpc - 1) / cpc), (unsigned)(c.n_seq * c.n_kv_heads * c.group));
+}
+
+cudaError_t launch_hist(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
+                        int32_t n_recent, uint32_t* hist, int32_t pending, cudaStream_t st) {
+  const int32_t cpc = chunks_per_cta(c);
+  HistArgs a{scores, ld, c.seq_len, hist, c.n_kv_heads * c.group, k, n_sink, n_recent, pending, cpc};
+  return launch_pdl(k_hist, run_grid(c, cpc), dim3(kCutThreads), 0, st, a);
+}
+
+// Whether the cut kernel can count the level-0 histograms itself: its grid
+// (one CTA per chunk and row) must be resident at once (cooperative launch).
+bool cut_counts_hist(const bpkv_cache& c) {
+  const int n = cut_slots();
   const int64_t grid = cut_chunks(c) * (int64_t)c.n_seq * c.n_kv_heads * c.group;
   return n > 0 && grid <= n;
 }
@@ -593,9 +616,10 @@ cudaError_t launch_cut(const bpkv_cache& c, const float* scores, int64_t ld, int
                        int32_t n_recent, const SelBufs& b, bool build_hist, int32_t pending, int32_t* status,
                        cudaStream_t st) {
   const bool l1 = !build_hist && long_rows(c);
+  const int32_t cpc = build_hist ? 1 : chunks_per_cta(c);
   CutArgs a{scores,   ld,           c.seq_len, b.hist, l1 ? b.hist1 : nullptr, b.cand, b.ctr, b.cut, status,
-            c.n_kv_heads * c.group, k, n_sink, n_recent, build_hist ? 1 : 0, pending};
-  const dim3 grid((unsigned)cut_chunks(c), (unsigned)(c.n_seq * c.n_kv_heads * c.group));
+            c.n_kv_heads * c.group, k, n_sink, n_recent, build_hist ? 1 : 0, pending, cpc};
+  const dim3 grid = run_grid(c, cpc);
   if (build_hist) return launch_coop_pdl(k_cut, grid, dim3(kCutThreads), 0, st, a);
   if (l1) {
     const cudaError_t e = launch_pdl(k_hist1, grid, dim3(kCutThreads), 0, st, a);
