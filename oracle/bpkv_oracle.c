@@ -21,7 +21,9 @@
  *   - section 2 ("Top-k decoding"): first 4 and last 32 tokens always kept, the
  *     other k-36 are each query head's top scores, exact attention
  *     softmax(q K^T / sqrt(D)) V over the selected set;
- *   - section 2 ("SparQ"): fixed channel sets by summed |q| over the group.
+ *   - section 2 ("SparQ"): fixed channel sets by summed |q| over the group;
+ *   - section 2 ("Double Sparsity"): channel sets chosen offline from
+ *     calibration statistics (mean |q| times mean |k| per channel).
  * Readings where the page is silent (bit order inside a word, zero and
  * overflowing scales, tie rules, stop rule of the allocator) are stated at each
  * function.
@@ -239,6 +241,39 @@ void or_fixed_depths(int32_t D, int32_t G, const float *q, int32_t r, int32_t t,
     if (rank < r) depth[j] = (uint8_t)t;
   }
   free(a);
+}
+
+/* Offline-calibrated channel sets (section 2, "Double Sparsity"): a channel's
+ * calibration statistic is the mean of |q_j| over the m_q calibration queries
+ * and the G query heads of the unit, times the mean of |k_j| over the m_k
+ * calibration keys.  The c channels with the largest statistic (ties to the
+ * lower index) are read at depth t, the others not at all.  Reading: the page
+ * fixes the statistic and c = 32 for a 136-bit read; the precision is ours.
+ * Each sum runs in double in storage order (queries, then heads within a
+ * query; keys in order), each mean divides its sum once and the product is one
+ * double multiplication.  q_cal float [m_q][G][D], k_cal bf16 [m_k][D]. */
+void or_calibrate_channels(int32_t D, int32_t G, int64_t m_q, const float *q_cal, int64_t m_k,
+                           const uint16_t *k_cal, int32_t c, int32_t t, uint8_t *depth) {
+  double *st = (double *)malloc(sizeof(double) * (size_t)D);
+  for (int32_t j = 0; j < D; ++j) {
+    double a = 0.0, b = 0.0;
+    for (int64_t m = 0; m < m_q; ++m)
+      for (int32_t h = 0; h < G; ++h) {
+        double v = (double)q_cal[(m * G + h) * D + j];
+        a = a + ((OR_MUTANT == 12) ? v * v : fabs(v));
+      }
+    for (int64_t m = 0; m < m_k; ++m) b = b + fabs(or_bf16_value(k_cal[m * D + j]));
+    const double qa = a / (double)(m_q * G), kb = b / (double)m_k;
+    st[j] = (OR_MUTANT == 11) ? qa : qa * kb;
+    depth[j] = 0;
+  }
+  for (int32_t j = 0; j < D; ++j) {
+    int32_t rank = 0; /* channels ordered before j */
+    for (int32_t i = 0; i < D; ++i)
+      if (st[i] > st[j] || (st[i] == st[j] && i < j)) ++rank;
+    if (rank < c) depth[j] = (uint8_t)t;
+  }
+  free(st);
 }
 
 /* ---------------------------------------------------------------- scores */

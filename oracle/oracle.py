@@ -12,6 +12,7 @@ them in the order of one decode step.
 from __future__ import annotations
 
 import ctypes
+import hashlib
 import os
 import platform
 import subprocess
@@ -31,8 +32,8 @@ def lib_path() -> str:
 
 def build(force: bool = False, cflags=None) -> str:
     """Compile the oracle with gcc (plain C11, IEEE arithmetic, no contraction)."""
-    out = lib_path() if cflags is None else os.path.join(
-        _HERE, f"liboracle_{platform.machine()}_{abs(hash(tuple(cflags)))}.so")
+    tag = hashlib.sha1(" ".join(cflags).encode()).hexdigest()[:12] if cflags is not None else ""
+    out = lib_path() if cflags is None else os.path.join(_HERE, f"liboracle_{platform.machine()}_{tag}.so")
     if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(_SRC):
         cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
                "-shared", "-o", out, _SRC, "-lm"] + list(cflags or [])
@@ -56,6 +57,8 @@ def _bind(path: str) -> ctypes.CDLL:
     L.or_alloc_depths.restype = i32
     L.or_fixed_depths.argtypes = [i32, i32, P, i32, i32, P]
     L.or_fixed_depths.restype = None
+    L.or_calibrate_channels.argtypes = [i32, i32, i64, P, i64, P, i32, i32, P]
+    L.or_calibrate_channels.restype = None
     L.or_scores.argtypes = [i64, i32, i32, P, P, i64, P, P, P]
     L.or_scores.restype = None
     L.or_topk.argtypes = [i64, P, i32, i32, i32, P]
@@ -129,6 +132,16 @@ class Oracle:
         G, D = q.shape
         depth = np.zeros(D, dtype=np.uint8)
         self.L.or_fixed_depths(D, G, _p(q), int(r), int(t), _p(depth))
+        return depth
+
+    def calibrate_channels(self, q_cal: np.ndarray, k_cal_bits: np.ndarray, c: int, t: int) -> np.ndarray:
+        """q_cal float [m_q][G][D], k_cal_bits bf16 patterns [m_k][D] -> depths [D]."""
+        q_cal = _c(q_cal, np.float32)
+        k_cal_bits = _c(k_cal_bits, np.uint16)
+        m_q, G, D = q_cal.shape
+        depth = np.zeros(D, dtype=np.uint8)
+        self.L.or_calibrate_channels(D, G, m_q, _p(q_cal), k_cal_bits.shape[0], _p(k_cal_bits), int(c), int(t),
+                                     _p(depth))
         return depth
 
     def scores(self, n: int, scales: np.ndarray, planes: np.ndarray, depth: np.ndarray,

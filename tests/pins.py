@@ -334,6 +334,80 @@ def pin_fixed_depths(o):
         assert depth_bits(d) == bits
 
 
+def _dyadic_calibration(rng, m_q, G, m_k, D):
+    """Calibration data whose sums, means and products are exact in double:
+    |q| multiples of 1/4 in [0, 8], |k| multiples of 1/8 in [0, 4] (exact in
+    bf16), random signs, m_q G and m_k powers of two."""
+    q = rng.integers(0, 33, (m_q, G, D)) / 4.0 * rng.choice([-1.0, 1.0], (m_q, G, D))
+    k = rng.integers(0, 33, (m_k, D)) / 8.0 * rng.choice([-1.0, 1.0], (m_k, D))
+    return q.astype(np.float32), k
+
+
+def _calibration_order(q, k):
+    """Channels by (mean|q| mean|k| desc, index asc), in exact rational arithmetic."""
+    from fractions import Fraction
+    m_q, G, D = q.shape
+    st = []
+    for j in range(D):
+        a = sum(Fraction(float(abs(x))) for x in q[:, :, j].ravel()) / (m_q * G)
+        b = sum(Fraction(float(abs(x))) for x in k[:, j]) / k.shape[0]
+        st.append(a * b)
+    return sorted(range(D), key=lambda j: (-st[j], j)), st
+
+
+def pin_calibrated_channels(o):
+    from workload.bytes_model import depth_bits
+    rng = np.random.default_rng(20)
+    D, G, m_q, m_k = 32, 4, 8, 16
+    q, k = _dyadic_calibration(rng, m_q, G, m_k, D)
+    # an exact tie of equal columns, and one of equal products from different
+    # factors (twice the queries, half the keys): both go to the lower index
+    q[:, :, 9], k[:, 9] = q[:, :, 4], k[:, 4]
+    q[:, :, 12], k[:, 12] = 2 * q[:, :, 6], k[:, 6] / 2
+    # a channel with the largest queries and near-zero keys, one with the
+    # largest keys and small queries: neither statistic alone decides
+    q[:, :, 0], k[:, 0] = 8.0, 0.125
+    q[:, :, 1], k[:, 1] = 0.25, 4.0
+    # heads differ: the mean runs over every head of the group
+    q[:, 1:, 2] = 0.0
+    q[:, 0, 2] = 8.0
+    k[:, 2] = 2.0
+    order, st = _calibration_order(q, k)
+    assert st[9] == st[4] and st[12] == st[6]
+    kb = bf16_bits_of(k)
+    for c, t in [(8, 4), (16, 2), (32, 1), (0, 4), (40, 3)]:
+        d = o.calibrate_channels(q, kb, c, t)
+        want = np.zeros(D, np.uint8)
+        want[order[:c]] = t
+        assert np.array_equal(d, want), (c, t, list(d), list(want))
+    # storage order of the calibration tokens does not matter (exact sums)
+    pq, pk = rng.permutation(m_q), rng.permutation(m_k)
+    assert np.array_equal(o.calibrate_channels(q[pq], kb[pk], 8, 4), o.calibrate_channels(q, kb, 8, 4))
+    # one calibration query and keys of equal magnitude: the SparQ set of that query
+    q1 = rng.standard_normal((1, 4, 128)).astype(np.float32)
+    k1 = bf16_bits_of(np.where(rng.random((8, 128)) < 0.5, -1.5, 1.5))
+    a = np.zeros(128, np.float64)
+    for h in range(4):
+        a = a + np.abs(q1[0, h]).astype(np.float64)
+    sparq = sorted(range(128), key=lambda j: (-a[j], j))
+    d = o.calibrate_channels(q1, k1, 32, 4)
+    want = np.zeros(128, np.uint8)
+    want[sparq[:32]] = 4
+    assert np.array_equal(d, want)
+    assert depth_bits(d) == 136  # 32 channels x 4 bits + their scales
+    # a channel permutation permutes the set (tie-free random data)
+    qr = rng.standard_normal((16, 4, 128)).astype(np.float32)
+    kr = bf16_bits_of(rng.standard_normal((64, 128)) * np.exp(0.75 * rng.standard_normal(128)))
+    perm = rng.permutation(128)
+    d0 = o.calibrate_channels(qr, kr, 32, 4)
+    assert np.array_equal(o.calibrate_channels(qr[:, :, perm], kr[:, perm], 32, 4), d0[perm])
+    # and matches means formed by numpy's own reductions
+    stat = np.abs(qr.astype(np.float64)).mean(axis=(0, 1)) * np.abs(bf16_value(kr)).mean(axis=0)
+    want = np.zeros(128, np.uint8)
+    want[np.argsort(-stat, kind="stable")[:32]] = 4
+    assert np.array_equal(d0, want)
+
+
 # ------------------------------------------------------------------ selection
 
 def _topk_brute(score, k, n_sink=4, n_recent=32):
@@ -409,5 +483,5 @@ def pin_attention(o):
 
 
 ALL_PINS = [pin_fp16, pin_codes_exact, pin_prefix_quantiser, pin_special_values, pin_bit_order_golden,
-            pin_scores, pin_alloc_bruteforce, pin_alloc_golden, pin_fixed_depths, pin_topk, pin_union,
-            pin_attention]
+            pin_scores, pin_alloc_bruteforce, pin_alloc_golden, pin_fixed_depths, pin_calibrated_channels,
+            pin_topk, pin_union, pin_attention]
