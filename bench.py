@@ -150,16 +150,28 @@ def make_workload(cfg, steps: int, warmup: int, dev, step_flags: int = 0, budget
     from workload import gen_layer
 
     L, N, H, G, D, n = cfg.n_layers, cfg.n_seq, cfg.n_kv_heads, cfg.group, cfg.head_dim, cfg.n_tokens
-    # room for every step the bench runs: warm-up, timed, breakdown, list and e2e steps
-    cap = ((n + warmup + 2 * steps + 128 + 511) // 512) * 512
     budgets = list(budgets or cfg.budgets)
     host = cfg.residency == "host"
+    # one cache per (budget, layer) unless they would not fit in device memory;
+    # then every budget's pass decodes into the same caches (each pass appends
+    # its own token), which only happens for multi-layer configs whose planes do
+    # not survive in L2 from one pass to the next
+    share = (not host and len(budgets) > 1 and
+             len(budgets) * L * cache_bytes(cfg, n) > 0.45 * torch.cuda.get_device_properties(dev).total_memory)
+    # room for every step the bench runs: warm-up, timed, breakdown, list and e2e
+    # steps of every pass that appends to a cache, then the baseline arms
+    per_pass = warmup + steps + min(steps, 20) + 1 + 2 + max(3, min(steps, 50))
+    cap = n + (len(budgets) if share else 1) * per_pass + len(BASELINE_ARMS) * (3 + baseline_steps(steps)) + 64
+    cap = (cap + 511) // 512 * 512
     caches = {b: [] for b in budgets}
     q, s2, kn, vn = [], [], [], []
     inp0 = None
     for l in range(L):
         inp = gen_layer(cfg, l, device=dev)
         for b in budgets:
+            if share and b != budgets[0]:
+                caches[b].append(caches[budgets[0]][-1])
+                continue
             c = pk.Cache(N, H, G, cap, device=dev)
             c.append(inp.k[:, :, : n - 1].contiguous(), inp.v[:, :, : n - 1].contiguous())
             if host:
@@ -210,7 +222,24 @@ def make_workload(cfg, steps: int, warmup: int, dev, step_flags: int = 0, budget
                                                                              cfg.n_recent, pk.DEPTH_WATERFILL)
         passes.append(p)
     torch.cuda.synchronize()
+    passes[0]["shared_caches"] = share
     return inp0, passes, ws, io
+
+
+def cache_bytes(cfg, n: int) -> int:
+    """Device bytes of one layer's cache at n tokens (rows, planes, scales)."""
+    nh, D = cfg.n_seq * cfg.n_kv_heads, cfg.head_dim
+    return nh * (2 * n * D * 2 + D * (n // 64 + 1) * (4 * 8 + 2))
+
+
+# baselines through the same entry point (Fathom page, section 2): the SparQ
+# channel rule with 32 channels at full depth (136 bits/token), the 2-bit
+# thumbnail (all channels at 2 planes, 288 bits/token) and dense attention
+BASELINE_ARMS = {"fixed_136": ("fixed", 32, 4), "thumbnail_288": ("fixed", 128, 2), "dense_bf16": ("dense", 0, 0)}
+
+
+def baseline_steps(steps: int) -> int:
+    return max(3, min(steps, 20))
 
 
 def run_step(passes, ws, events=False, lists=False):
@@ -367,6 +396,7 @@ def bench_ours(args, cfg, rank, world, local):
 
     # end to end through host buffers: inputs copied in, outputs copied out, inside the timed region
     e2e = bench_e2e(args, passes, io, ws, flush, dev, keys_per_step, world)
+    baselines = bench_baselines(args, cfg, passes, io, ws, flush, dev, world)
 
     line = {
         "metric": "keys scored/s", "value": round(value), "unit": "keys/s", "n_gpus": world,
@@ -378,7 +408,9 @@ def bench_ours(args, cfg, rank, world, local):
                    "n_sink": cfg.n_sink,
                    "n_recent": cfg.n_recent, "residency": cfg.residency,
                    "l2": "flushed before every timed step (256 MiB write, outside the events)",
-                   "cuda_graph": graph is not None, "parallelism": f"replicas x{world}"},
+                   "cuda_graph": graph is not None, "parallelism": f"replicas x{world}",
+                   "caches": ("one per layer, shared by the budget passes (each pass appends its token)"
+                              if passes[0].get("shared_caches") else "one per (budget, layer)")},
         "decode_step_us_per_layer": round(ms_per_step * 1e3 / n_launch, 2),
         "achieved_gbs_step": round((scan_bytes + rows_bytes) / (ms_per_step / 1e3) / 1e9, 1),
         "fused_kernel": all(p["fused"] for p in passes),
@@ -392,6 +424,10 @@ def bench_ours(args, cfg, rank, world, local):
                            "union_rows": union_rows},
         "roofline": roofline,
         "e2e": e2e,
+        "baselines": baselines,
+        "baselines_note": ("same entry point, same caches and step structure: SparQ channel rule at 32 channels "
+                           "x 4 planes (136 bits/token), all channels at 2 planes (288 bits/token), dense bf16 "
+                           "attention over every row; read bytes are the plane prefixes (or rows for dense)"),
         "gpu_launches": args.steps * L * sum(launches_per_pass(p, args) for p in passes),
         "clocks": clk,
         "wall_s_timed": round(wall, 3),
@@ -401,6 +437,58 @@ def bench_ours(args, cfg, rank, world, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, inp, args.cpu_seconds, [p["budget"] for p in passes])
     return line
+
+
+def bench_baselines(args, cfg, passes, io, ws, flush, dev, world):
+    """The baseline arms, each one decode pass over the first pass's caches through
+    bpkv_decode_step, captured in a CUDA graph; L2 flushed before every timed step."""
+    import ctypes
+    import torch
+    import bit_plane_kv_encode_gb300 as pk
+    from workload.bytes_model import row_bytes
+    p0 = passes[0]
+    L, N, H, D, n = cfg.n_layers, cfg.n_seq, cfg.n_kv_heads, cfg.head_dim, cfg.n_tokens
+    keys = L * N * H * n
+    out = {}
+    for name, (rule, r, t) in BASELINE_ARMS.items():
+        rule_id = pk.DEPTH_FIXED if rule == "fixed" else pk.DEPTH_DENSE
+        a = pk.bpkv_step_args(io["k_new"].data_ptr(), io["v_new"].data_ptr(), io["q"].data_ptr(), None, None,
+                              rule_id, r, t, cfg.k, cfg.n_sink, cfg.n_recent, p0["out"].data_ptr(), None, None,
+                              None, 0)
+
+        def run():
+            for layer in p0["arr"]:
+                layer.n_max = p0["cap"] - 1
+            pk.bpkv_decode_step(p0["arr"], L, a, ws, ws.numel())
+
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=torch.cuda.Stream(device=dev)):
+            run()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        times = []
+        for _ in range(baseline_steps(args.steps)):
+            flush.zero_()
+            e0.record()
+            graph.replay()
+            e1.record()
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        if pk.bpkv_read_status(ws) != 0:
+            raise RuntimeError(f"device status {pk.bpkv_read_status(ws)} after the {name} arm")
+        ms = all_max(statistics.mean(times), world)
+        if rule == "dense":
+            nbytes = L * N * H * n * row_bytes(D)
+        else:
+            nbytes = L * N * H * n * (r * t + r * 16 / 64) / 8
+        out[name] = {"ms_per_step": round(ms, 5), "us_per_layer": round(ms * 1e3 / L, 2),
+                     "keys_per_s": round(world * keys / (ms / 1e3)),
+                     "bits_per_token": None if rule == "dense" else r * t + r // 4,
+                     "read_bytes_per_step": round(nbytes), "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
+                     "steps": len(times)}
+    return out
 
 
 def bench_e2e(args, passes, io, ws, flush, dev, keys_per_step, world):

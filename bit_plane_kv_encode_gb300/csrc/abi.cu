@@ -22,15 +22,17 @@ cudaError_t launch_attend_ranges(const bpkv_cache& c, const float* q, const floa
                                  cudaStream_t st);
 cudaError_t launch_scan(const bpkv_cache& c, const float* q, const uint8_t* depths, float* scores, int64_t ld,
                         cudaStream_t st, const void* plan = nullptr, uint32_t* hist = nullptr,
-                        int32_t n_sink = 0, int32_t n_recent = 0, int32_t pending = 0);
+                        int32_t n_sink = 0, int32_t n_recent = 0, int32_t pending = 0,
+                        int32_t* status = nullptr, uint32_t* work = nullptr);
 cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
                         int32_t n_recent, const SelBufs& b, HistState hs, int32_t* idx, int32_t* status,
                         cudaStream_t st, int32_t pending = 0);
 cudaError_t launch_front(const bpkv_cache& c, const uint16_t* k_new, const uint16_t* v_new, int32_t t_new,
                          const float* q, const float* sigma2, const int32_t* budget_q, int32_t depth_rule,
                          int32_t n_channels, int32_t depth, uint8_t* depths, void* plan, uint32_t* hist,
-                         uint32_t* hist1, uint32_t* ctr, uint32_t* tickets, uint32_t* seq_tick, cudaStream_t st);
-bool cut_counts_hist(const bpkv_cache& c);
+                         uint32_t* hist1, uint32_t* ctr, uint32_t* tickets, uint32_t* seq_tick, uint32_t* scan_work,
+                         cudaStream_t st);
+bool scan_counts_hist(const bpkv_cache& c);
 cudaError_t launch_union(const bpkv_cache& c, const int32_t* idx, int32_t k, int32_t* uidx, uint8_t* umask,
                          int32_t* ucount, cudaStream_t st);
 cudaError_t launch_attend(const bpkv_cache& c, const float* q, const int32_t* uidx, const uint8_t* umask,
@@ -102,7 +104,7 @@ Layout layout(const bpkv_cache& c, int32_t k, int32_t what) {
     L.hist = off;
     L.hist1 = L.hist + rows * kTopkBins * sizeof(uint32_t);
     L.ctr = L.hist1 + rows * kTopkBins * sizeof(uint32_t);
-    off = align_up(L.ctr + rows * kSelCounters * sizeof(uint32_t));
+    off = align_up(L.ctr + rows * kSelCounters * sizeof(uint32_t) + sizeof(uint32_t));  // + the scan work counter
     L.cand = off;
     off = align_up(off + rows * 1024 * sizeof(unsigned long long));
     L.cut = off;
@@ -148,7 +150,9 @@ SelBufs sel_bufs(void* ws, const Layout& L) {
   unsigned char* w = static_cast<unsigned char*>(ws);
   return SelBufs{reinterpret_cast<uint32_t*>(w + L.hist), reinterpret_cast<uint32_t*>(w + L.hist1),
                  reinterpret_cast<uint32_t*>(w + L.ctr), reinterpret_cast<unsigned long long*>(w + L.cand),
-                 reinterpret_cast<unsigned long long*>(w + L.cut)};
+                 reinterpret_cast<unsigned long long*>(w + L.cut),
+                 reinterpret_cast<uint32_t*>(w + L.ctr) + (L.hist1 - L.hist) / sizeof(uint32_t) / kTopkBins *
+                                                              kSelCounters};
 }
 
 int check_ws(const bpkv_cache& c, int32_t k, int32_t what, void* ws, size_t ws_bytes) {
@@ -258,13 +262,14 @@ int bpkv_scan_topk(const bpkv_cache* c, const float* q, const uint8_t* depths, i
   const SelBufs b = sel_bufs(ws, L);
   cudaStream_t st = as_stream(stream);
   const size_t rows = (size_t)c->n_seq * c->n_kv_heads * c->group;
-  BPKV_TRY(cuda_status(cudaMemsetAsync(b.hist, 0, rows * (2 * kTopkBins + kSelCounters) * sizeof(uint32_t), st)));
+  BPKV_TRY(cuda_status(
+      cudaMemsetAsync(b.hist, 0, rows * (2 * kTopkBins + kSelCounters) * sizeof(uint32_t) + sizeof(uint32_t), st)));
   // the level-0 histograms: counted by the cut kernel when it can, else by the scan
-  const bool cut_counts = cut_counts_hist(*c);
-  BPKV_TRY(cuda_status(launch_scan(*c, q, depths, scores, c->cap_tokens, st, nullptr, cut_counts ? nullptr : b.hist,
-                                   n_sink, n_recent)));
+  const bool scan_counts = scan_counts_hist(*c);
+  BPKV_TRY(cuda_status(launch_scan(*c, q, depths, scores, c->cap_tokens, st, nullptr, scan_counts ? b.hist : nullptr,
+                                   n_sink, n_recent, 0, static_cast<int32_t*>(ws), b.scan_work)));
   return cuda_status(launch_topk(*c, scores, c->cap_tokens, k, n_sink, n_recent, b,
-                                 cut_counts ? HistState::kZero : HistState::kCounted, idx, static_cast<int32_t*>(ws),
+                                 scan_counts ? HistState::kCounted : HistState::kZero, idx, static_cast<int32_t*>(ws),
                                  st));
 }
 
@@ -385,7 +390,7 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
         BPKV_TRY(cuda_status(launch_fixed_depths(c, q, a->fixed_channels, a->fixed_depth, depths, st, tickets, plan,
                                                  sb.hist, sb.ctr)));
       BPKV_TRY(mark(l, 2));
-      BPKV_TRY(cuda_status(launch_scan(c, q, depths, scores, c.cap_tokens, st, plan)));
+      BPKV_TRY(cuda_status(launch_scan(c, q, depths, scores, c.cap_tokens, st, plan, nullptr, 0, 0, 0, status)));
       BPKV_TRY(mark(l, 3));
       int32_t* iout = a->idx_out ? a->idx_out + (size_t)l * NH * G * a->k : nullptr;
       BPKV_TRY(cuda_status(
@@ -399,15 +404,15 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
     const bool l1 = c.n_max + 1 >= kLongRowTokens;
     BPKV_TRY(cuda_status(launch_front(c, kn, vn, 1, q, s2, a->budget_q, a->depth_rule, a->fixed_channels,
                                       a->fixed_depth, depths, plan, sb.hist, l1 ? sb.hist1 : nullptr, sb.ctr,
-                                      tickets, seq_tick, st)));
+                                      tickets, seq_tick, sb.scan_work, st)));
     c.n_max += 1;
     BPKV_TRY(mark(l, 1));
     BPKV_TRY(mark(l, 2));
     // the level-0 histograms (zeroed by the front kernel): counted by the cut kernel when it can, else by the scan
-    const bool cut_counts = cut_counts_hist(c);
-    const HistState hs = cut_counts ? HistState::kZero : HistState::kCounted;
-    BPKV_TRY(cuda_status(launch_scan(c, q, depths, scores, c.cap_tokens, st, plan, cut_counts ? nullptr : sb.hist,
-                                     a->n_sink, a->n_recent, 1)));
+    const bool scan_counts = scan_counts_hist(c);
+    const HistState hs = scan_counts ? HistState::kCounted : HistState::kZero;
+    BPKV_TRY(cuda_status(launch_scan(c, q, depths, scores, c.cap_tokens, st, plan, scan_counts ? sb.hist : nullptr,
+                                     a->n_sink, a->n_recent, 1, status, sb.scan_work)));
     BPKV_TRY(mark(l, 3));
     if (attend_ranges_eligible(c, a->k)) {
       // cuts only (lists when asked for); the attention selects by cut, forms

@@ -57,6 +57,7 @@ struct SelBufs {
   uint32_t* ctr;             // [rows][kSelCounters]
   unsigned long long* cand;  // [rows][1024]
   unsigned long long* cut;   // [rows]
+  uint32_t* scan_work;       // one counter right after ctr: the scan's shared work items (zeroed with ctr)
 };
 
 __device__ __forceinline__ uint32_t ordered_key(float f) {
@@ -117,5 +118,17 @@ cudaError_t launch_coop_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_
 // Spin limit of in-kernel waits for other CTAs (each round sleeps ~100 ns):
 // well above any real wait, then the waiter records BPKV_DEV_TIMEOUT and goes on.
 constexpr uint32_t kSpinLimit = 1u << 21;
+
+// ---- asynchronous 16-byte copies global -> shared (this thread's groups) ----
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// Both addresses 16-byte aligned; cached in L2 only.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until every copy this thread committed has landed.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 }  // namespace bpkv

@@ -22,6 +22,7 @@
 #include "scan_core.cuh"
 
 #include <mutex>
+#include <type_traits>
 
 namespace bpkv {
 
@@ -41,6 +42,10 @@ struct ScanArgs {
   int32_t n_sink, n_recent;
   int64_t chunks_per_cta;
   int32_t pending;  // tokens appended in this step but not yet in seq_len
+  int32_t* status;  // optional device status word (unused by the scan kernels today)
+  int64_t chunks;   // chunks per unit (from the host bound on the sequence lengths)
+  int64_t units;    // sequences x KV heads
+  uint32_t* work;   // optional zeroed counter: the second half of the work is handed out in small items
 };
 
 template <int GP>
@@ -84,9 +89,141 @@ __global__ void __launch_bounds__(kScanThreads, GP >= 8 ? 2 : 4) k_scan(ScanArgs
   }
 }
 
+// Device-resident caches.  The grid is one wave of CTAs over the units'
+// chunks laid end to end (unit-major); each CTA takes an equal share of that
+// sequence and scores it unit by unit.  Within a unit the steps (chunk, pass)
+// go through two stage buffers: once step i has landed and every warp is past
+// step i - 1, all threads start the copies of step i + 1 into the other
+// buffer, then each warp forms u = s w for its block and scores step i.
 template <int GP>
+__device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& S, int64_t unit, int64_t c_begin,
+                                               int64_t c_want) {
+  const int s = (int)(unit / a.n_heads);
+  const int64_t n = min64(a.seq_len[s] + a.pending, a.nb_cap * kBlock);
+  const int64_t nb_valid = (n + kBlock - 1) / kBlock;
+  const int64_t c_end = min64(c_want, (nb_valid + kScanBlocks - 1) / kScanBlocks);
+  if (c_begin >= c_end) return;
+  const int tid = threadIdx.x, lane = tid & 31, lb = tid >> 5;
+  const int G = a.group;
+  __syncthreads();  // every warp is done with the previous unit's plan and stage buffers
+  if (a.plan) {
+    scan_load_plan<GP>(S.P, reinterpret_cast<const ScanPlan<GP>*>(a.plan) + unit);
+  } else {
+    int t = 0;
+    float qv[GP];
+    if (tid < kD) {
+      t = a.depths[unit * kD + tid];
+      const float* qp = a.q + unit * G * kD;
+#pragma unroll
+      for (int hh = 0; hh < GP; ++hh) qv[hh] = hh < G ? qp[hh * kD + tid] : 0.f;
+    }
+    scan_setup<GP>(S.P, S.X, t, qv);
+  }
+  const uint64_t* pl = a.planes + unit * kD * kPlanes * a.nb_cap;
+  const uint16_t* sp = a.scales + unit * kD * a.nb_cap;
+  float* out = a.scores + unit * G * a.ld;
+  uint32_t* hist = a.hist ? a.hist + unit * G * kTopkBins : nullptr;
+  const int64_t lo = min64(a.n_sink, n), hi = max64(n - a.n_recent, lo);
+  const int n_passes = S.P.n_passes;
+  const int64_t steps = (c_end - c_begin) * n_passes;
+  Acc<GP> A;
+  acc_zero<GP>(A);
+  uint32_t keep[5], rot[5];
+  transpose_consts(lane, keep, rot);
+  // scores of chunk ch from the accumulators (zeros when no channel is read)
+  auto finish_chunk = [&](int64_t ch) {
+    const int64_t b0 = ch * kScanBlocks;
+    const int nbl = (int)min64(kScanBlocks, nb_valid - b0);
+    if (lb < nbl) {
+      const int64_t x0 = b0 * kBlock + (int64_t)lb * kBlock + lane;
+      float v0[GP], v1[GP];
+#pragma unroll
+      for (int hh = 0; hh < GP; ++hh) {
+        acc_scores<GP>(A, hh, v0[hh], v1[hh]);
+        if (hh < G) {
+          if (x0 < n) out[hh * a.ld + x0] = v0[hh];
+          if (x0 + 32 < n) out[hh * a.ld + x0 + 32] = v1[hh];
+        }
+      }
+      if (hist) warp_hist<GP>(G, x0, lo, hi, v0, v1, hist);
+    }
+    acc_zero<GP>(A);
+  };
+  if (steps == 0) {
+    for (int64_t ch = c_begin; ch < c_end; ++ch) finish_chunk(ch);
+    return;
+  }
+  scan_issue<GP>(S, 0, pl, sp, a.nb_cap, c_begin * kScanBlocks, S.P.pass_g[0], S.P.pass_g[1]);
+  int64_t ch = c_begin;  // chunk and pass of step i
+  int ps = 0;
+  for (int64_t i = 0; i < steps; ++i) {
+    const int b = (int)(i & 1);
+    cp_async_wait_all();
+    __syncthreads();  // step i visible to all; every warp is done with step i - 1 (the other buffer)
+    if (i + 1 < steps) {
+      const int ps1 = ps + 1 == n_passes ? 0 : ps + 1;
+      const int64_t ch1 = ps1 == 0 ? ch + 1 : ch;
+      scan_issue<GP>(S, b ^ 1, pl, sp, a.nb_cap, ch1 * kScanBlocks, S.P.pass_g[ps1], S.P.pass_g[ps1 + 1]);
+    }
+    const int g0 = S.P.pass_g[ps], g1 = S.P.pass_g[ps + 1];
+    const int s0 = S.P.grp_base[g0], s1 = g1 < S.P.n_groups ? (int)S.P.grp_base[g1] : S.P.n_slots;
+    scan_form_u<GP>(S, b, s0, s1, lb);
+    __syncwarp();
+    const int nbl = (int)min64(kScanBlocks, nb_valid - ch * kScanBlocks);
+    if (lb < nbl) scan_compute_pipe<GP>(S, b, g0, g1, s0, lb, keep, rot, A);
+    if (++ps == n_passes) {
+      finish_chunk(ch);
+      ps = 0;
+      ++ch;
+    }
+  }
+}
+
+template <int GP>
+__global__ void __launch_bounds__(kScanThreads, 2) k_scan_pipe(ScanArgs a) {
+  pdl_enter();
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  PipeSmem<GP>& S = *reinterpret_cast<PipeSmem<GP>*>(smem_raw);
+  // raw scales of slots no copy writes must be finite: start from zeros
+  constexpr int kScWords = kPassSlots * kScanBlocks / 2;
+  for (int e = threadIdx.x; e < 2 * kScWords; e += kScanThreads)
+    reinterpret_cast<uint32_t*>(S.st[e / kScWords].sc)[e % kScWords] = 0u;
+  // chunks [f0, f1) of the units' chunks laid end to end
+  auto run = [&](int64_t f0, int64_t f1) {
+    for (int64_t f = f0; f < f1;) {
+      const int64_t unit = f / a.chunks, c0 = f % a.chunks;
+      const int64_t c1 = min64(a.chunks, c0 + (f1 - f));
+      scan_unit_pipe<GP>(a, S, unit, c0, c1);
+      f += c1 - c0;
+    }
+  };
+  // units differ in cost (their depth vectors): with a counter, each CTA takes
+  // an equal share of the first half and then items of the rest until none is left
+  const int64_t total = a.units * a.chunks;
+  const int64_t stat = a.work ? total / 2 : total;
+  run(stat * blockIdx.x / gridDim.x, stat * (blockIdx.x + 1) / gridDim.x);
+  if (a.work) {
+    constexpr int64_t kItem = 4;  // chunks per item
+    const int64_t items = (total - stat + kItem - 1) / kItem;
+    for (;;) {
+      __syncthreads();  // every thread has read the previous item
+      if (threadIdx.x == 0) S.item = atomicAdd(a.work, 1u);
+      __syncthreads();
+      const int64_t j = S.item;
+      if (j >= items) break;
+      run(stat + j * kItem, min64(total, stat + (j + 1) * kItem));
+    }
+  }
+}
+
+template <int GP, bool Pipe>
 cudaError_t launch_scan_gp(ScanArgs a, int64_t chunks, int64_t units, cudaStream_t st) {
-  const int smem = (int)sizeof(ScanSmem<GP>);
+  int smem = 0;
+  if constexpr (Pipe) smem = (int)sizeof(PipeSmem<GP>);
+  else smem = (int)sizeof(ScanSmem<GP>);
+  void (*kernel)(ScanArgs) = nullptr;
+  if constexpr (Pipe) kernel = k_scan_pipe<GP>;
+  else kernel = k_scan<GP>;
   // resident CTAs per device, looked up once per device
   constexpr int kDevs = 64;
   static int slots[kDevs] = {};
@@ -99,38 +236,54 @@ cudaError_t launch_scan_gp(ScanArgs a, int64_t chunks, int64_t units, cudaStream
   {
     std::lock_guard<std::mutex> lock(mu);
     if (slots[dev] == 0) {
-      e = cudaFuncSetAttribute(k_scan<GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
       int sms = 0, per_sm = 0;
       e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
       if (e != cudaSuccess) return e;
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_scan<GP>, kScanThreads, smem);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kScanThreads, smem);
       if (e != cudaSuccess) return e;
       slots[dev] = sms * (per_sm > 0 ? per_sm : 1);
     }
     occ_slots = slots[dev];
   }
-  // enough chunks per CTA for the grid to fit in one wave of resident CTAs
   const int64_t total = chunks * units;
+  a.chunks = chunks;
+  a.units = units;
+  if constexpr (Pipe) {
+    // one wave; each CTA an equal share of all units' chunks laid end to end
+    // (half of them when work items are handed out: only for at least 8 chunks per CTA)
+    const unsigned ctas = (unsigned)min64(total, (int64_t)occ_slots);
+    if (total < 8 * (int64_t)ctas) a.work = nullptr;
+    return launch_pdl(kernel, dim3(ctas), dim3(kScanThreads), (size_t)smem, st, a);
+  }
+  // enough chunks per CTA for the grid to fit in one wave of resident CTAs
   a.chunks_per_cta = (total + occ_slots - 1) / occ_slots;
   if (a.chunks_per_cta < 1) a.chunks_per_cta = 1;
   const dim3 grid((unsigned)((chunks + a.chunks_per_cta - 1) / a.chunks_per_cta), (unsigned)a.n_heads,
                   (unsigned)(units / a.n_heads));
-  return launch_pdl(k_scan<GP>, grid, dim3(kScanThreads), (size_t)smem, st, a);
+  return launch_pdl(kernel, grid, dim3(kScanThreads), (size_t)smem, st, a);
 }
 
+// Device-resident caches take the pipelined kernel (asynchronous copies into
+// shared memory); pinned host caches the direct one (plain loads over the link).
 cudaError_t launch_scan(const bpkv_cache& c, const float* q, const uint8_t* depths, float* scores, int64_t ld,
                         cudaStream_t st, const void* plan, uint32_t* hist, int32_t n_sink, int32_t n_recent,
-                        int32_t pending) {
-  ScanArgs a{plan,         c.planes, c.scales, c.seq_len, q,        depths, scores, ld, c.cap_tokens / kBlock,
-             c.n_kv_heads, c.group,  hist,     n_sink,    n_recent, 1,      pending};
+                        int32_t pending, int32_t* status, uint32_t* work) {
+  ScanArgs a{plan,         c.planes, c.scales, c.seq_len, q,        depths, scores,  ld,    c.cap_tokens / kBlock,
+             c.n_kv_heads, c.group,  hist,     n_sink,    n_recent, 1,      pending, status, 0, 0, work};
   const int64_t chunks = (c.n_max + kScanBlocks * kBlock - 1) / (kScanBlocks * kBlock);
   if (chunks == 0) return cudaSuccess;
   const int64_t units = (int64_t)c.n_seq * c.n_kv_heads;
-  if (c.group <= 1) return launch_scan_gp<1>(a, chunks, units, st);
-  if (c.group <= 2) return launch_scan_gp<2>(a, chunks, units, st);
-  if (c.group <= 4) return launch_scan_gp<4>(a, chunks, units, st);
-  return launch_scan_gp<8>(a, chunks, units, st);
+  const bool pipe = c.residency == 0;
+  auto go = [&](auto gp) {
+    constexpr int GP = decltype(gp)::value;
+    return pipe ? launch_scan_gp<GP, true>(a, chunks, units, st) : launch_scan_gp<GP, false>(a, chunks, units, st);
+  };
+  if (c.group <= 1) return go(std::integral_constant<int, 1>{});
+  if (c.group <= 2) return go(std::integral_constant<int, 2>{});
+  if (c.group <= 4) return go(std::integral_constant<int, 4>{});
+  return go(std::integral_constant<int, 8>{});
 }
 
 }  // namespace bpkv

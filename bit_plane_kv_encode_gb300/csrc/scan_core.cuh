@@ -41,7 +41,7 @@ __host__ __device__ constexpr int field_pos(int t, int m) {
 // group of every slot, and the weights w = q 2^(4 - t - pos).
 template <int GP>
 struct __align__(16) ScanPlan {
-  float w[kMaxSlots * GP];                          // [group slots][head][slot]
+  float w[kMaxSlots * GP];                          // [slot][head]
   int16_t row_of_lane[kMaxGroups * 32];             // j * 4 + p, or -1
   int16_t slot_ch[kMaxSlots];                       // channel of each slot, or -1
   int8_t slot_grp[kMaxSlots];                       // group of each slot
@@ -247,7 +247,7 @@ __device__ void scan_setup(ScanPlan<GP>& S, PlanScratch& X, int t, const float (
     for (int p = 0; p < t; ++p) S.row_of_lane[g * 32 + m * t + (t - 1 - p)] = (int16_t)(tid * 4 + p);
     // w = q 2^(4 - t - pos) per head, laid out [group][head][slot]; other slots stay 0
 #pragma unroll
-    for (int hh = 0; hh < GP; ++hh) S.w[base * GP + hh * P + m] = ldexpf(qv[hh], 4 - t - field_pos(t, m));
+    for (int hh = 0; hh < GP; ++hh) S.w[(base + m) * GP + hh] = ldexpf(qv[hh], 4 - t - field_pos(t, m));
   }
   __syncthreads();
 }
@@ -319,7 +319,7 @@ __device__ void scan_stage_pass(ScanSmem<GP>& S, const uint64_t* __restrict__ pl
         const int base = P.grp_base[g], m = slot - base, pitch = slot_pitch(P.grp_t[g]);
         float* ud = S.u + (lb * ps + (base - s0)) * GP;
 #pragma unroll
-        for (int hh = 0; hh < GP; ++hh) ud[hh * pitch + m] = sc * P.w[base * GP + hh * pitch + m];
+        for (int hh = 0; hh < GP; ++hh) ud[hh * pitch + m] = sc * P.w[(base + m) * GP + hh];
       }
     }
   }
@@ -387,6 +387,232 @@ __device__ bool scan_chunk(ScanSmem<GP>& S, const uint64_t* __restrict__ pl, con
     if (x0 + 32 < n_valid) out[hh * ld + x0 + 32] = v1[hh];
   }
   return true;
+}
+
+// ---------------------------------------------------------------------------
+// Pipelined form (device-resident caches): the plane words and raw block
+// scales of one (chunk, pass) step are fetched by asynchronous 16-byte copies
+// into one of two stage buffers while the warps score the other.
+
+constexpr int kRowPitch = 20;                 // u32 words per staged plane row: 64 B + 16 B (16-byte aligned rows)
+constexpr int kStageRows = kPassGroups * 32;
+
+struct __align__(16) ScanStage {
+  uint32_t words[kStageRows * kRowPitch];     // the chunk's 8 words of each row of the pass: row (g - g0) * 32 + lane
+  uint16_t sc[kPassSlots * kScanBlocks];      // raw block scales of the pass's slots, [slot - s0][block]
+};
+
+template <int GP>
+struct __align__(16) PipeSmem {
+  ScanStage st[2];
+  float u[kScanBlocks][kPassSlots * GP];      // per warp (block): u = s w, [slot - s0][head]
+  ScanPlan<GP> P;
+  PlanScratch X;
+  uint32_t item;                              // the work item this CTA took last
+};
+
+__device__ __forceinline__ unsigned long long fadd2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Packed accumulators of one lane: for each of its two tokens, the heads in
+// pairs (one head, the two tokens, when GP = 1); even and odd fields apart.
+template <int GP>
+struct Acc {
+  static constexpr int HP = GP == 1 ? 1 : GP / 2;
+  unsigned long long t0[2][HP];  // [field parity][head pair]: token lane (GP = 1: both tokens)
+  unsigned long long t1[2][HP];  // token lane + 32 (unused when GP = 1)
+};
+
+// Field M of a depth-T group for this lane's two tokens.  xa / xb are the
+// transposed words shifted (see field_pos) with the exponent of 2^23 already
+// in bits 23..30, so one AND keeps the field and the exponent: the float is
+// 2^23 + c 2^pos, and one packed subtraction of the offset gives both tokens'
+// e 2^pos (exact).  Each pair of heads then takes one packed FMA per token
+// with e broadcast.
+template <int T, int M, int GP>
+__device__ __forceinline__ void field_heads(uint32_t xa0, uint32_t xb0, uint32_t xa1, uint32_t xb1,
+                                            const float* __restrict__ ud, Acc<GP>& A) {
+  constexpr int pos = field_pos(T, M);
+  constexpr uint32_t keep = (((1u << T) - 1u) << pos) | 0xFF800000u;
+  constexpr float K = 8388608.f + ((float)(1 << (T - 1)) - 0.5f) * (float)(1u << pos);
+  constexpr bool use_a = (M * T + T <= 22);
+  constexpr int par = M & 1;
+  const uint32_t s0 = use_a ? xa0 : xb0, s1 = use_a ? xa1 : xb1;
+  const unsigned long long E = fadd2(pack2(__uint_as_float(s0 & keep), __uint_as_float(s1 & keep)), pack2(-K, -K));
+  const float* up = ud + M * GP;
+  if constexpr (GP == 1) {
+    A.t0[par][0] = ffma2(pack2(up[0], up[0]), E, A.t0[par][0]);
+  } else {
+    float e0, e1;
+    unpack2(E, e0, e1);
+    const unsigned long long E0 = pack2(e0, e0), E1 = pack2(e1, e1);
+    if constexpr (GP == 2) {
+      const float2 uu = *reinterpret_cast<const float2*>(up);
+      const unsigned long long U = pack2(uu.x, uu.y);
+      A.t0[par][0] = ffma2(U, E0, A.t0[par][0]);
+      A.t1[par][0] = ffma2(U, E1, A.t1[par][0]);
+    } else {
+#pragma unroll
+      for (int q = 0; q < GP / 4; ++q) {
+        const float4 uu = *reinterpret_cast<const float4*>(up + 4 * q);
+        const unsigned long long Ua = pack2(uu.x, uu.y), Ub = pack2(uu.z, uu.w);
+        A.t0[par][2 * q] = ffma2(Ua, E0, A.t0[par][2 * q]);
+        A.t0[par][2 * q + 1] = ffma2(Ub, E0, A.t0[par][2 * q + 1]);
+        A.t1[par][2 * q] = ffma2(Ua, E1, A.t1[par][2 * q]);
+        A.t1[par][2 * q + 1] = ffma2(Ub, E1, A.t1[par][2 * q + 1]);
+      }
+    }
+  }
+}
+
+// Fields 4 B .. 4 B + 3 of a depth-T group (those below the group's capacity).
+// Slots past the group's channel count have u = 0, so their fields add 0.
+template <int T, int B, int GP>
+__device__ __forceinline__ void field_block(uint32_t xa0, uint32_t xb0, uint32_t xa1, uint32_t xb1,
+                                            const float* __restrict__ ud, Acc<GP>& A) {
+  constexpr int C = Depth<T>::cap;
+  if constexpr (4 * B < C) field_heads<T, 4 * B, GP>(xa0, xb0, xa1, xb1, ud, A);
+  if constexpr (4 * B + 1 < C) field_heads<T, 4 * B + 1, GP>(xa0, xb0, xa1, xb1, ud, A);
+  if constexpr (4 * B + 2 < C) field_heads<T, 4 * B + 2, GP>(xa0, xb0, xa1, xb1, ud, A);
+  if constexpr (4 * B + 3 < C) field_heads<T, 4 * B + 3, GP>(xa0, xb0, xa1, xb1, ud, A);
+}
+
+// The fields of one group in blocks of four: one jump to the group's last
+// block, then straight-line code down to block 0 (no test per field).
+template <int T, int GP>
+__device__ __forceinline__ void group_fields_heads(int cnt, uint32_t xa0, uint32_t xb0, uint32_t xa1, uint32_t xb1,
+                                                   const float* __restrict__ ud, Acc<GP>& A) {
+  constexpr int NB = (Depth<T>::cap + 3) / 4;
+  static_assert(NB <= 8, "at most 32 fields per group");
+#define BPKV_FIELD_BLOCK(b)                                                                    \
+  case (b) + 1:                                                                                \
+    if constexpr ((b) < NB) field_block<T, (b), GP>(xa0, xb0, xa1, xb1, ud, A); \
+    [[fallthrough]];
+  switch ((cnt + 3) >> 2) {
+    BPKV_FIELD_BLOCK(7)
+    BPKV_FIELD_BLOCK(6)
+    BPKV_FIELD_BLOCK(5)
+    BPKV_FIELD_BLOCK(4)
+    BPKV_FIELD_BLOCK(3)
+    BPKV_FIELD_BLOCK(2)
+    BPKV_FIELD_BLOCK(1)
+    case 1:
+      field_block<T, 0, GP>(xa0, xb0, xa1, xb1, ud, A);
+      [[fallthrough]];
+    default:
+      break;
+  }
+#undef BPKV_FIELD_BLOCK
+}
+
+// This lane's scores of head hh for its two tokens.
+template <int GP>
+__device__ __forceinline__ void acc_scores(const Acc<GP>& A, int hh, float& v0, float& v1) {
+  float a, b, c, d;
+  if constexpr (GP == 1) {
+    unpack2(A.t0[0][0], a, b);
+    unpack2(A.t0[1][0], c, d);
+    v0 = a + c;
+    v1 = b + d;
+  } else {
+    unpack2(A.t0[0][hh >> 1], a, b);
+    unpack2(A.t0[1][hh >> 1], c, d);
+    v0 = (hh & 1) ? b + d : a + c;
+    unpack2(A.t1[0][hh >> 1], a, b);
+    unpack2(A.t1[1][hh >> 1], c, d);
+    v1 = (hh & 1) ? b + d : a + c;
+  }
+}
+
+template <int GP>
+__device__ __forceinline__ void acc_zero(Acc<GP>& A) {
+#pragma unroll
+  for (int p = 0; p < 2; ++p)
+#pragma unroll
+    for (int i = 0; i < Acc<GP>::HP; ++i) A.t0[p][i] = A.t1[p][i] = 0ull;
+}
+
+// All threads: start the copies of step (chunk at block b0, groups [g0, g1))
+// into stage buffer b: per used plane row its chunk's 8 words (four 16-byte
+// pieces), per used slot its chunk's 8 block scales (one piece); then commit
+// them as this thread's newest group.  pl / sp are the unit's planes and
+// scales; b0 + 8 <= nb_cap.
+template <int GP>
+__device__ __forceinline__ void scan_issue(PipeSmem<GP>& S, int b, const uint64_t* pl, const uint16_t* sp,
+                                           int64_t nb_cap, int64_t b0, int g0, int g1) {
+  const ScanPlan<GP>& P = S.P;
+  const int n_row = (g1 - g0) * 32;
+  const int s0 = P.grp_base[g0], s1 = g1 < P.n_groups ? (int)P.grp_base[g1] : P.n_slots;
+  const int n_all = n_row + (s1 - s0);
+  for (int e = threadIdx.x; e < n_all; e += kScanThreads) {
+    if (e < n_row) {
+      const int row = P.row_of_lane[g0 * 32 + e];
+      if (row >= 0) {
+        const uint64_t* src = pl + (int64_t)row * nb_cap + b0;
+        uint32_t* dst = &S.st[b].words[e * kRowPitch];
+#pragma unroll
+        for (int piece = 0; piece < 4; ++piece) cp_async16(dst + 4 * piece, src + 2 * piece);
+      }
+    } else {
+      const int sl = s0 + e - n_row;
+      const int ch = P.slot_ch[sl];
+      if (ch >= 0) cp_async16(&S.st[b].sc[(sl - s0) * kScanBlocks], sp + (int64_t)ch * nb_cap + b0);
+    }
+  }
+  cp_async_commit();
+}
+
+// This warp's u = s w for the slots [s0, s1) of a landed stage (block lb):
+// one slot per lane at a time, all heads with vector loads and stores.
+template <int GP>
+__device__ __forceinline__ void scan_form_u(PipeSmem<GP>& S, int b, int s0, int s1, int lb) {
+  const int lane = threadIdx.x & 31;
+  const uint16_t* sc = S.st[b].sc + lb;
+  const float* w = S.P.w + s0 * GP;
+  float* ud = S.u[lb];
+  for (int rel = lane; rel < s1 - s0; rel += 32) {
+    const float sv = fp16_bits_to_float(sc[rel * kScanBlocks]);
+    if constexpr (GP == 1) {
+      ud[rel] = sv * w[rel];
+    } else if constexpr (GP == 2) {
+      const float2 wv = *reinterpret_cast<const float2*>(w + 2 * rel);
+      *reinterpret_cast<float2*>(ud + 2 * rel) = make_float2(sv * wv.x, sv * wv.y);
+    } else {
+#pragma unroll
+      for (int q = 0; q < GP / 4; ++q) {
+        const float4 wv = *reinterpret_cast<const float4*>(w + GP * rel + 4 * q);
+        *reinterpret_cast<float4*>(ud + GP * rel + 4 * q) = make_float4(sv * wv.x, sv * wv.y, sv * wv.z, sv * wv.w);
+      }
+    }
+  }
+}
+
+// Add groups [g0, g1) of a landed stage to this lane's accumulators (warp lb:
+// block lb of the chunk, tokens lane and lane + 32).  u must be formed.
+template <int GP>
+__device__ __forceinline__ void scan_compute_pipe(const PipeSmem<GP>& S, int b, int g0, int g1, int s0, int lb,
+                                                  const uint32_t (&keep)[5], const uint32_t (&rot)[5], Acc<GP>& A) {
+  const int lane = threadIdx.x & 31;
+  const ScanPlan<GP>& P = S.P;
+  for (int g = g0; g < g1; ++g) {
+    const int d = P.grp_t[g], cnt = P.grp_cnt[g];
+    const uint2 wv = *reinterpret_cast<const uint2*>(&S.st[b].words[((g - g0) * 32 + lane) * kRowPitch + 2 * lb]);
+    const uint32_t x0 = warp_transpose32(wv.x, keep, rot);
+    const uint32_t x1 = warp_transpose32(wv.y, keep, rot);
+    // the exponent of 2^23 over bits 23..30 of both shifted forms
+    const uint32_t xa0 = ((x0 << 1) & 0x007FFFFFu) | 0x4B000000u, xb0 = (x0 >> 9) | 0x4B000000u;
+    const uint32_t xa1 = ((x1 << 1) & 0x007FFFFFu) | 0x4B000000u, xb1 = (x1 >> 9) | 0x4B000000u;
+    const float* ud = S.u[lb] + (P.grp_base[g] - s0) * GP;
+    switch (d) {
+      case 4: group_fields_heads<4, GP>(cnt, xa0, xb0, xa1, xb1, ud, A); break;
+      case 3: group_fields_heads<3, GP>(cnt, xa0, xb0, xa1, xb1, ud, A); break;
+      case 2: group_fields_heads<2, GP>(cnt, xa0, xb0, xa1, xb1, ud, A); break;
+      default: group_fields_heads<1, GP>(cnt, xa0, xb0, xa1, xb1, ud, A); break;
+    }
+  }
 }
 
 // Level-0 selection histogram of one warp's block (top 12 bits of the
