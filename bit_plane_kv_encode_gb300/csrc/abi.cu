@@ -23,15 +23,14 @@ cudaError_t launch_attend_ranges(const bpkv_cache& c, const float* q, const floa
 cudaError_t launch_scan(const bpkv_cache& c, const float* q, const uint8_t* depths, float* scores, int64_t ld,
                         cudaStream_t st, const void* plan = nullptr, uint32_t* hist = nullptr,
                         int32_t n_sink = 0, int32_t n_recent = 0, int32_t pending = 0,
-                        int32_t* status = nullptr, uint32_t* work = nullptr);
+                        int32_t* status = nullptr);
 cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
                         int32_t n_recent, const SelBufs& b, HistState hs, int32_t* idx, int32_t* status,
                         cudaStream_t st, int32_t pending = 0);
 cudaError_t launch_front(const bpkv_cache& c, const uint16_t* k_new, const uint16_t* v_new, int32_t t_new,
                          const float* q, const float* sigma2, const int32_t* budget_q, int32_t depth_rule,
                          int32_t n_channels, int32_t depth, uint8_t* depths, void* plan, uint32_t* hist,
-                         uint32_t* hist1, uint32_t* ctr, uint32_t* tickets, uint32_t* seq_tick, uint32_t* scan_work,
-                         cudaStream_t st);
+                         uint32_t* hist1, uint32_t* ctr, uint32_t* tickets, uint32_t* seq_tick, cudaStream_t st);
 bool scan_counts_hist(const bpkv_cache& c);
 cudaError_t launch_union(const bpkv_cache& c, const int32_t* idx, int32_t k, int32_t* uidx, uint8_t* umask,
                          int32_t* ucount, cudaStream_t st);
@@ -104,7 +103,7 @@ Layout layout(const bpkv_cache& c, int32_t k, int32_t what) {
     L.hist = off;
     L.hist1 = L.hist + rows * kTopkBins * sizeof(uint32_t);
     L.ctr = L.hist1 + rows * kTopkBins * sizeof(uint32_t);
-    off = align_up(L.ctr + rows * kSelCounters * sizeof(uint32_t) + sizeof(uint32_t));  // + the scan work counter
+    off = align_up(L.ctr + rows * kSelCounters * sizeof(uint32_t));
     L.cand = off;
     off = align_up(off + rows * 1024 * sizeof(unsigned long long));
     L.cut = off;
@@ -150,9 +149,7 @@ SelBufs sel_bufs(void* ws, const Layout& L) {
   unsigned char* w = static_cast<unsigned char*>(ws);
   return SelBufs{reinterpret_cast<uint32_t*>(w + L.hist), reinterpret_cast<uint32_t*>(w + L.hist1),
                  reinterpret_cast<uint32_t*>(w + L.ctr), reinterpret_cast<unsigned long long*>(w + L.cand),
-                 reinterpret_cast<unsigned long long*>(w + L.cut),
-                 reinterpret_cast<uint32_t*>(w + L.ctr) + (L.hist1 - L.hist) / sizeof(uint32_t) / kTopkBins *
-                                                              kSelCounters};
+                 reinterpret_cast<unsigned long long*>(w + L.cut)};
 }
 
 int check_ws(const bpkv_cache& c, int32_t k, int32_t what, void* ws, size_t ws_bytes) {
@@ -262,12 +259,11 @@ int bpkv_scan_topk(const bpkv_cache* c, const float* q, const uint8_t* depths, i
   const SelBufs b = sel_bufs(ws, L);
   cudaStream_t st = as_stream(stream);
   const size_t rows = (size_t)c->n_seq * c->n_kv_heads * c->group;
-  BPKV_TRY(cuda_status(
-      cudaMemsetAsync(b.hist, 0, rows * (2 * kTopkBins + kSelCounters) * sizeof(uint32_t) + sizeof(uint32_t), st)));
+  BPKV_TRY(cuda_status(cudaMemsetAsync(b.hist, 0, rows * (2 * kTopkBins + kSelCounters) * sizeof(uint32_t), st)));
   // the level-0 histograms: counted by the cut kernel when it can, else by the scan
   const bool scan_counts = scan_counts_hist(*c);
   BPKV_TRY(cuda_status(launch_scan(*c, q, depths, scores, c->cap_tokens, st, nullptr, scan_counts ? b.hist : nullptr,
-                                   n_sink, n_recent, 0, static_cast<int32_t*>(ws), b.scan_work)));
+                                   n_sink, n_recent, 0, static_cast<int32_t*>(ws))));
   return cuda_status(launch_topk(*c, scores, c->cap_tokens, k, n_sink, n_recent, b,
                                  scan_counts ? HistState::kCounted : HistState::kZero, idx, static_cast<int32_t*>(ws),
                                  st));
@@ -404,7 +400,7 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
     const bool l1 = c.n_max + 1 >= kLongRowTokens;
     BPKV_TRY(cuda_status(launch_front(c, kn, vn, 1, q, s2, a->budget_q, a->depth_rule, a->fixed_channels,
                                       a->fixed_depth, depths, plan, sb.hist, l1 ? sb.hist1 : nullptr, sb.ctr,
-                                      tickets, seq_tick, sb.scan_work, st)));
+                                      tickets, seq_tick, st)));
     c.n_max += 1;
     BPKV_TRY(mark(l, 1));
     BPKV_TRY(mark(l, 2));
@@ -412,7 +408,7 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
     const bool scan_counts = scan_counts_hist(c);
     const HistState hs = scan_counts ? HistState::kCounted : HistState::kZero;
     BPKV_TRY(cuda_status(launch_scan(c, q, depths, scores, c.cap_tokens, st, plan, scan_counts ? sb.hist : nullptr,
-                                     a->n_sink, a->n_recent, 1, status, sb.scan_work)));
+                                     a->n_sink, a->n_recent, 1, status)));
     BPKV_TRY(mark(l, 3));
     if (attend_ranges_eligible(c, a->k)) {
       // cuts only (lists when asked for); the attention selects by cut, forms

@@ -57,7 +57,6 @@ struct SelBufs {
   uint32_t* ctr;             // [rows][kSelCounters]
   unsigned long long* cand;  // [rows][1024]
   unsigned long long* cut;   // [rows]
-  uint32_t* scan_work;       // one counter right after ctr: the scan's shared work items (zeroed with ctr)
 };
 
 __device__ __forceinline__ uint32_t ordered_key(float f) {

@@ -111,7 +111,6 @@ struct FrontArgs {
   DepthArgs d;
   int32_t depth_rule;       // BPKV_DEPTH_WATERFILL or BPKV_DEPTH_FIXED
   uint32_t* seq_tick;       // [N]: zeroed for the attention of this step
-  uint32_t* scan_work;      // optional: the scan's work-item counter, zeroed for the scan of this step
   uint32_t* hist1;          // optional [N][H][G][kTopkBins]: zeroed with the level-0 histograms
   // append
   uint64_t* planes;
@@ -166,7 +165,6 @@ __global__ void __launch_bounds__(kScanThreads) k_front(FrontArgs a) {
   if (threadIdx.x == 0) {
     a.d.tickets[unit] = 0u;
     if (h == 0) a.seq_tick[s] = 0u;
-    if (unit == 0 && a.scan_work) *a.scan_work = 0u;
   }
   uint8_t* dep = a.d.depths + unit * kD;
   if (a.depth_rule == BPKV_DEPTH_WATERFILL)
@@ -179,13 +177,11 @@ __global__ void __launch_bounds__(kScanThreads) k_front(FrontArgs a) {
 cudaError_t launch_front(const bpkv_cache& c, const uint16_t* k_new, const uint16_t* v_new, int32_t t_new,
                          const float* q, const float* sigma2, const int32_t* budget_q, int32_t depth_rule,
                          int32_t n_channels, int32_t depth, uint8_t* depths, void* plan, uint32_t* hist,
-                         uint32_t* hist1, uint32_t* ctr, uint32_t* tickets, uint32_t* seq_tick, uint32_t* scan_work,
-                         cudaStream_t st) {
+                         uint32_t* hist1, uint32_t* ctr, uint32_t* tickets, uint32_t* seq_tick, cudaStream_t st) {
   FrontArgs a;
   a.d = DepthArgs{q, sigma2, budget_q, depths, c.n_kv_heads, c.group, tickets, plan, n_channels, depth, hist, ctr};
   a.depth_rule = depth_rule;
   a.seq_tick = seq_tick;
-  a.scan_work = scan_work;
   a.hist1 = hist1;
   a.planes = c.planes;
   a.scales = c.scales;

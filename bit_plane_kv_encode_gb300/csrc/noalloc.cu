@@ -19,7 +19,7 @@ namespace bpkv {
 cudaError_t launch_scan(const bpkv_cache& c, const float* q, const uint8_t* depths, float* scores, int64_t ld,
                         cudaStream_t st, const void* plan = nullptr, uint32_t* hist = nullptr,
                         int32_t n_sink = 0, int32_t n_recent = 0, int32_t pending = 0,
-                        int32_t* status = nullptr, uint32_t* work = nullptr);
+                        int32_t* status = nullptr);
 cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
                         int32_t n_recent, const SelBufs& b, HistState hs, int32_t* idx, int32_t* status,
                         cudaStream_t st, int32_t pending = 0);
@@ -74,7 +74,7 @@ extern "C" int bpkv_scan_topk_noalloc(const bpkv_cache* c, const float* q, const
   const size_t rows = (size_t)c->n_seq * c->n_kv_heads * c->group;
   const int64_t ld = (c->n_max + 63) / 64 * 64;
   const size_t off_hist = round256(rows * (size_t)ld * sizeof(float));
-  const size_t off_cand = round256(off_hist + rows * (2 * kTopkBins + kSelCounters) * sizeof(uint32_t) + sizeof(uint32_t));
+  const size_t off_cand = round256(off_hist + rows * (2 * kTopkBins + kSelCounters) * sizeof(uint32_t));
   const size_t off_cut = round256(off_cand + rows * 1024 * sizeof(unsigned long long));
   const size_t need = off_cut + rows * sizeof(unsigned long long);
   if (need > kNoallocScratchBytes) return BPKV_ENOWORKSPACE;
@@ -86,16 +86,14 @@ extern "C" int bpkv_scan_topk_noalloc(const bpkv_cache* c, const float* q, const
   SelBufs b{reinterpret_cast<uint32_t*>(base + off_hist),
             reinterpret_cast<uint32_t*>(base + off_hist + rows * kTopkBins * sizeof(uint32_t)),
             reinterpret_cast<uint32_t*>(base + off_hist + 2 * rows * kTopkBins * sizeof(uint32_t)),
-            reinterpret_cast<unsigned long long*>(base + off_cand), reinterpret_cast<unsigned long long*>(base + off_cut),
-            reinterpret_cast<uint32_t*>(base + off_hist + rows * (2 * kTopkBins + kSelCounters) * sizeof(uint32_t))};
+            reinterpret_cast<unsigned long long*>(base + off_cand), reinterpret_cast<unsigned long long*>(base + off_cut)};
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(b.hist, 0, rows * (2 * kTopkBins + kSelCounters) * sizeof(uint32_t) + sizeof(uint32_t), st) !=
-      cudaSuccess)
+  if (cudaMemsetAsync(b.hist, 0, rows * (2 * kTopkBins + kSelCounters) * sizeof(uint32_t), st) != cudaSuccess)
     return BPKV_ECUDA;
   const bool scan_counts = scan_counts_hist(*c);
   if (ld > 0 &&
-      launch_scan(*c, q, depths, scores, ld, st, nullptr, scan_counts ? b.hist : nullptr, n_sink, n_recent, 0, nullptr,
-                  b.scan_work) != cudaSuccess)
+      launch_scan(*c, q, depths, scores, ld, st, nullptr, scan_counts ? b.hist : nullptr, n_sink, n_recent) !=
+          cudaSuccess)
     return BPKV_ECUDA;
   if (launch_topk(*c, scores, ld > 0 ? ld : 1, k, n_sink, n_recent, b,
                   scan_counts ? HistState::kCounted : HistState::kZero, idx, nullptr, st) != cudaSuccess)

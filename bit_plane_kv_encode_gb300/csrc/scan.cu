@@ -45,7 +45,6 @@ struct ScanArgs {
   int32_t* status;  // optional device status word (unused by the scan kernels today)
   int64_t chunks;   // chunks per unit (from the host bound on the sequence lengths)
   int64_t units;    // sequences x KV heads
-  uint32_t* work;   // optional zeroed counter: the second half of the work is handed out in small items
 };
 
 template <int GP>
@@ -126,6 +125,13 @@ __device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& 
   const int64_t lo = min64(a.n_sink, n), hi = max64(n - a.n_recent, lo);
   const int n_passes = S.P.n_passes;
   const int64_t steps = (c_end - c_begin) * n_passes;
+  constexpr bool kSmemHist = pipe_counts_hist<GP>();
+  if constexpr (kSmemHist) {
+    if (hist) {
+      for (int e = tid; e < G * kTopkBins / 2; e += kScanThreads) S.hist[e] = 0u;
+      __syncthreads();
+    }
+  }
   Acc<GP> A;
   acc_zero<GP>(A);
   uint32_t keep[5], rot[5];
@@ -143,14 +149,45 @@ __device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& 
         if (hh < G) {
           if (x0 < n) out[hh * a.ld + x0] = v0[hh];
           if (x0 + 32 < n) out[hh * a.ld + x0 + 32] = v1[hh];
+          if constexpr (kSmemHist) {
+            if (hist) {
+              uint32_t* H = S.hist + hh * (kTopkBins / 2);
+              if (x0 >= lo && x0 < hi) {
+                const uint32_t bin = ordered_key(v0[hh]) >> 20;
+                atomicAdd(H + (bin >> 1), 1u << ((bin & 1u) * 16));
+              }
+              if (x0 + 32 >= lo && x0 + 32 < hi) {
+                const uint32_t bin = ordered_key(v1[hh]) >> 20;
+                atomicAdd(H + (bin >> 1), 1u << ((bin & 1u) * 16));
+              }
+            }
+          }
         }
       }
-      if (hist) warp_hist<GP>(G, x0, lo, hi, v0, v1, hist);
+      if constexpr (!kSmemHist) {
+        if (hist) warp_hist<GP>(G, x0, lo, hi, v0, v1, hist);
+      }
     }
     acc_zero<GP>(A);
   };
+  // the unit's shared-memory histograms added to its global ones
+  auto flush_hist = [&]() {
+    if constexpr (kSmemHist) {
+      if (hist) {
+        __syncthreads();
+        for (int e = tid; e < G * kTopkBins / 2; e += kScanThreads) {
+          const uint32_t v = S.hist[e];
+          if (v == 0u) continue;
+          uint32_t* g = hist + (e / (kTopkBins / 2)) * kTopkBins + 2 * (e % (kTopkBins / 2));
+          if (v & 0xFFFFu) atomicAdd(g, v & 0xFFFFu);
+          if (v >> 16) atomicAdd(g + 1, v >> 16);
+        }
+      }
+    }
+  };
   if (steps == 0) {
     for (int64_t ch = c_begin; ch < c_end; ++ch) finish_chunk(ch);
+    flush_hist();
     return;
   }
   scan_issue<GP>(S, 0, pl, sp, a.nb_cap, c_begin * kScanBlocks, S.P.pass_g[0], S.P.pass_g[1]);
@@ -177,6 +214,7 @@ __device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& 
       ++ch;
     }
   }
+  flush_hist();
 }
 
 template <int GP>
@@ -184,35 +222,14 @@ __global__ void __launch_bounds__(kScanThreads, 2) k_scan_pipe(ScanArgs a) {
   pdl_enter();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   PipeSmem<GP>& S = *reinterpret_cast<PipeSmem<GP>*>(smem_raw);
-  // raw scales of slots no copy writes must be finite: start from zeros
-  constexpr int kScWords = kPassSlots * kScanBlocks / 2;
-  for (int e = threadIdx.x; e < 2 * kScWords; e += kScanThreads)
-    reinterpret_cast<uint32_t*>(S.st[e / kScWords].sc)[e % kScWords] = 0u;
-  // chunks [f0, f1) of the units' chunks laid end to end
-  auto run = [&](int64_t f0, int64_t f1) {
-    for (int64_t f = f0; f < f1;) {
-      const int64_t unit = f / a.chunks, c0 = f % a.chunks;
-      const int64_t c1 = min64(a.chunks, c0 + (f1 - f));
-      scan_unit_pipe<GP>(a, S, unit, c0, c1);
-      f += c1 - c0;
-    }
-  };
-  // units differ in cost (their depth vectors): with a counter, each CTA takes
-  // an equal share of the first half and then items of the rest until none is left
+  // an equal share of all units' chunks laid end to end, unit by unit
   const int64_t total = a.units * a.chunks;
-  const int64_t stat = a.work ? total / 2 : total;
-  run(stat * blockIdx.x / gridDim.x, stat * (blockIdx.x + 1) / gridDim.x);
-  if (a.work) {
-    constexpr int64_t kItem = 4;  // chunks per item
-    const int64_t items = (total - stat + kItem - 1) / kItem;
-    for (;;) {
-      __syncthreads();  // every thread has read the previous item
-      if (threadIdx.x == 0) S.item = atomicAdd(a.work, 1u);
-      __syncthreads();
-      const int64_t j = S.item;
-      if (j >= items) break;
-      run(stat + j * kItem, min64(total, stat + (j + 1) * kItem));
-    }
+  const int64_t f1 = total * (blockIdx.x + 1) / gridDim.x;
+  for (int64_t f = total * blockIdx.x / gridDim.x; f < f1;) {
+    const int64_t unit = f / a.chunks, c0 = f % a.chunks;
+    const int64_t c1 = min64(a.chunks, c0 + (f1 - f));
+    scan_unit_pipe<GP>(a, S, unit, c0, c1);
+    f += c1 - c0;
   }
 }
 
@@ -251,10 +268,8 @@ cudaError_t launch_scan_gp(ScanArgs a, int64_t chunks, int64_t units, cudaStream
   a.chunks = chunks;
   a.units = units;
   if constexpr (Pipe) {
-    // one wave; each CTA an equal share of all units' chunks laid end to end
-    // (half of them when work items are handed out: only for at least 8 chunks per CTA)
+    // one wave; each CTA an equal share of the work (see k_scan_pipe)
     const unsigned ctas = (unsigned)min64(total, (int64_t)occ_slots);
-    if (total < 8 * (int64_t)ctas) a.work = nullptr;
     return launch_pdl(kernel, dim3(ctas), dim3(kScanThreads), (size_t)smem, st, a);
   }
   // enough chunks per CTA for the grid to fit in one wave of resident CTAs
@@ -269,9 +284,9 @@ cudaError_t launch_scan_gp(ScanArgs a, int64_t chunks, int64_t units, cudaStream
 // shared memory); pinned host caches the direct one (plain loads over the link).
 cudaError_t launch_scan(const bpkv_cache& c, const float* q, const uint8_t* depths, float* scores, int64_t ld,
                         cudaStream_t st, const void* plan, uint32_t* hist, int32_t n_sink, int32_t n_recent,
-                        int32_t pending, int32_t* status, uint32_t* work) {
+                        int32_t pending, int32_t* status) {
   ScanArgs a{plan,         c.planes, c.scales, c.seq_len, q,        depths, scores,  ld,    c.cap_tokens / kBlock,
-             c.n_kv_heads, c.group,  hist,     n_sink,    n_recent, 1,      pending, status, 0, 0, work};
+             c.n_kv_heads, c.group,  hist,     n_sink,    n_recent, 1,      pending, status, 0, 0};
   const int64_t chunks = (c.n_max + kScanBlocks * kBlock - 1) / (kScanBlocks * kBlock);
   if (chunks == 0) return cudaSuccess;
   const int64_t units = (int64_t)c.n_seq * c.n_kv_heads;

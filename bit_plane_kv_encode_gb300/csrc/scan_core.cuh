@@ -174,8 +174,10 @@ __device__ void scan_setup(ScanPlan<GP>& S, PlanScratch& X, int t, const float (
       if (lane == 0) X.warp_cnt[warp][d] = __popc(b);
     }
   }
+  // defaults of every entry, before any thread writes its channel's entries
   for (int e = tid; e < kMaxGroups * 32; e += kScanThreads) S.row_of_lane[e] = -1;
   for (int e = tid; e < kMaxSlots * GP; e += kScanThreads) S.w[e] = 0.f;
+  for (int e = tid; e < kMaxSlots; e += kScanThreads) S.slot_ch[e] = -1;
   __syncthreads();
   // per depth d: channels, groups, first group and first slot
   int cnt[5], ng[5], goff[5], soff[5];
@@ -201,7 +203,6 @@ __device__ void scan_setup(ScanPlan<GP>& S, PlanScratch& X, int t, const float (
     }
   }
   for (int e = tid; e < kMaxSlots; e += kScanThreads) {
-    S.slot_ch[e] = -1;
     int g = 0;
 #pragma unroll
     for (int d = 4; d >= 1; --d)
@@ -408,8 +409,14 @@ struct __align__(16) PipeSmem {
   float u[kScanBlocks][kPassSlots * GP];      // per warp (block): u = s w, [slot - s0][head]
   ScanPlan<GP> P;
   PlanScratch X;
-  uint32_t item;                              // the work item this CTA took last
+  // level-0 selection histograms of the unit being scored, two 16-bit counts
+  // per word (bins 2i and 2i + 1 of head h at word h * kTopkBins / 2 + i)
+  uint32_t hist[GP <= 4 ? GP * kTopkBins / 2 : 1];
 };
+
+// Whether the pipelined scan counts the level-0 histograms in shared memory.
+template <int GP>
+__host__ __device__ constexpr bool pipe_counts_hist() { return GP <= 4; }
 
 __device__ __forceinline__ unsigned long long fadd2(unsigned long long a, unsigned long long b) {
   unsigned long long d;
@@ -565,6 +572,11 @@ __device__ __forceinline__ void scan_issue(PipeSmem<GP>& S, int b, const uint64_
   cp_async_commit();
 }
 
+// s w, or 0 where the weight is 0: a slot that no channel uses has w = 0 and
+// whatever raw scale an earlier step left in the stage buffer (possibly one
+// of a block past the end of a unit's cache, which is not a number).
+__device__ __forceinline__ float sw(float s, float w) { return w != 0.f ? s * w : 0.f; }
+
 // This warp's u = s w for the slots [s0, s1) of a landed stage (block lb):
 // one slot per lane at a time, all heads with vector loads and stores.
 template <int GP>
@@ -576,15 +588,16 @@ __device__ __forceinline__ void scan_form_u(PipeSmem<GP>& S, int b, int s0, int 
   for (int rel = lane; rel < s1 - s0; rel += 32) {
     const float sv = fp16_bits_to_float(sc[rel * kScanBlocks]);
     if constexpr (GP == 1) {
-      ud[rel] = sv * w[rel];
+      ud[rel] = sw(sv, w[rel]);
     } else if constexpr (GP == 2) {
       const float2 wv = *reinterpret_cast<const float2*>(w + 2 * rel);
-      *reinterpret_cast<float2*>(ud + 2 * rel) = make_float2(sv * wv.x, sv * wv.y);
+      *reinterpret_cast<float2*>(ud + 2 * rel) = make_float2(sw(sv, wv.x), sw(sv, wv.y));
     } else {
 #pragma unroll
       for (int q = 0; q < GP / 4; ++q) {
         const float4 wv = *reinterpret_cast<const float4*>(w + GP * rel + 4 * q);
-        *reinterpret_cast<float4*>(ud + GP * rel + 4 * q) = make_float4(sv * wv.x, sv * wv.y, sv * wv.z, sv * wv.w);
+        *reinterpret_cast<float4*>(ud + GP * rel + 4 * q) =
+            make_float4(sw(sv, wv.x), sw(sv, wv.y), sw(sv, wv.z), sw(sv, wv.w));
       }
     }
   }

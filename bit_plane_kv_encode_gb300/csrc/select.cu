@@ -609,10 +609,10 @@ bool cut_counts_hist(const bpkv_cache& c) {
 }
 
 // Whether the scan kernel should count the level-0 histograms as it writes
-// the scores: only when the cut cannot and the scan reads a pinned host cache
-// (its link-bound loop hides the atomics); otherwise k_hist counts them from
-// the scores, which costs far less than atomics inside a device-side scan.
-bool scan_counts_hist(const bpkv_cache& c) { return c.residency == 1 && !cut_counts_hist(c); }
+// the scores (when the cut cannot): the pinned-host scan (its link-bound loop
+// hides the atomics) and the device-side scan for groups of up to 4 query
+// heads (in shared memory); otherwise k_hist counts them from the scores.
+bool scan_counts_hist(const bpkv_cache& c) { return !cut_counts_hist(c) && (c.residency == 1 || c.group <= 4); }
 
 // Rows long enough that the level-0 bucket usually exceeds kRankCap keys get
 // a parallel level-1 histogram (k_hist1) before the cut.

@@ -345,6 +345,46 @@ def test_scan_topk_histogram_matches_topk(pk, n, G, budget):
     assert torch.equal(idx_a, idx_b)
 
 
+@pytest.mark.parametrize("N,H,G,n", [(2, 8, 4, 70001), (1, 8, 8, 70001), (1, 4, 2, 300000)])
+def test_scan_topk_grid_too_large_for_cut(pk, orc, N, H, G, n):
+    """Grids too large for the cut to count its own histograms: the scan counts
+    them (in shared memory for up to 4 query heads; k_hist for more).  Same
+    indices as bpkv_scan + bpkv_topk, and sampled rows equal the oracle's top-k
+    of the oracle's scores."""
+    k = 512
+    kk, vv = _rand_kv(N, H, n, seed=23)
+    c = build_cache(kk, vv, G)
+    gq = torch.Generator(device="cpu").manual_seed(n + G + 7)
+    q = torch.randn((N, H, G, 128), generator=gq).cuda()
+    s2 = torch.ones((N, H, 128), device="cuda")
+    bq = torch.full((N,), 92 * 4, dtype=torch.int32, device="cuda")
+    depths = torch.zeros((N, H, 128), dtype=torch.uint8, device="cuda")
+    pk.bpkv_alloc_depths(c.c, q, s2, bq, depths)
+    ws = c.workspace(k, pk.WS_SCAN_TOPK)
+    idx_a = torch.zeros((N, H, G, k), dtype=torch.int32, device="cuda")
+    pk.bpkv_clear_status(ws)
+    pk.bpkv_scan_topk(c.c, q, depths, k, 4, 32, idx_a, ws, ws.numel())
+    assert pk.bpkv_read_status(ws) == 0
+    ld = c.c.cap_tokens
+    scores = torch.zeros((N, H, G, ld), device="cuda")
+    pk.bpkv_scan(c.c, q, depths, scores, ld)
+    idx_b = torch.zeros_like(idx_a)
+    pk.bpkv_topk(c.c, scores, ld, k, 4, 32, idx_b, ws, ws.numel())
+    assert pk.bpkv_read_status(ws) == 0
+    differ = [tuple(int(x) for x in r) for r in (idx_a != idx_b).any(dim=-1).nonzero().cpu()]
+    assert not differ, f"rows (seq, head, query head) whose lists differ: {differ[:8]}"
+    # one sampled unit against the oracle (scores and top-k sets within the bar)
+    s, h = N - 1, H - 1
+    kb = bits16(kk[s, h])
+    scales, planes = orc.encode(kb, c.c.cap_tokens // 64)
+    d = depths[s, h].cpu().numpy()
+    qq = q[s, h].cpu().numpy()
+    ref = orc.scores(n, scales, planes, d, qq)
+    check_scores(scores[s, h, :, :n].cpu().numpy(), ref, abs_score_scale(qq, kb, d), "large-grid scan")
+    for g in range(G):
+        check_topk_sets(idx_a[s, h, g].cpu().numpy(), orc.topk(ref[g], k), ref[g], k, what=f"head {g}")
+
+
 @pytest.mark.parametrize("n,ties", [(140000, 0.0), (150001, 0.9)])
 def test_topk_long_rows_level1(pk, orc, n, ties):
     """Rows of at least 131072 keys over a grid too large to run cooperatively:
