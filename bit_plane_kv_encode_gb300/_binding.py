@@ -40,6 +40,7 @@ class bpkv_step_args(ctypes.Structure):
         ("depth_rule", i32), ("fixed_channels", i32), ("fixed_depth", i32),
         ("k", i32), ("n_sink", i32), ("n_recent", i32),
         ("out", P), ("depths_out", P), ("idx_out", P), ("stage_events", P), ("flags", i32),
+        ("depths_in", P),
     ]
 
 
@@ -52,6 +53,7 @@ _SIGS = {
     "bpkv_encode_append": ([P, P, P, i32, P], ctypes.c_int),
     "bpkv_alloc_depths": ([P, P, P, P, P, P], ctypes.c_int),
     "bpkv_fixed_depths": ([P, P, i32, i32, P, P], ctypes.c_int),
+    "bpkv_calibrate_channels": ([P, P, i32, i32, i64, i64, i32, i32, P, P], ctypes.c_int),
     "bpkv_scan": ([P, P, P, P, i64, P], ctypes.c_int),
     "bpkv_topk": ([P, P, i64, i32, i32, i32, P, P, sz, P], ctypes.c_int),
     "bpkv_scan_topk": ([P, P, P, i32, i32, i32, P, P, sz, P], ctypes.c_int),
@@ -160,6 +162,14 @@ def bpkv_fixed_depths(cache, q, n_channels: int, depth: int, depths, stream=None
     return _check("bpkv_fixed_depths",
                   load().bpkv_fixed_depths(ctypes.byref(cache), _ptr(q), int(n_channels), int(depth),
                                            _ptr(depths), _stream(stream)))
+
+
+def bpkv_calibrate_channels(q_cal, k_cal, n_units: int, group: int, m_q: int, m_k: int, n_channels: int,
+                            depth: int, depths, stream=None):
+    return _check("bpkv_calibrate_channels",
+                  load().bpkv_calibrate_channels(_ptr(q_cal), _ptr(k_cal), int(n_units), int(group), int(m_q),
+                                                 int(m_k), int(n_channels), int(depth), _ptr(depths),
+                                                 _stream(stream)))
 
 
 def bpkv_scan(cache, q, depths, scores, ld_scores: int, stream=None):

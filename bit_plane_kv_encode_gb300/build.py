@@ -12,7 +12,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
-SOURCES = ["encode.cu", "depths.cu", "scan.cu", "select.cu", "attend.cu", "abi.cu", "noalloc.cu", "fused.cu", "tail.cu"]
+SOURCES = ["encode.cu", "depths.cu", "scan.cu", "select.cu", "attend.cu", "abi.cu", "noalloc.cu", "fused.cu", "tail.cu",
+           "calibrate.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 

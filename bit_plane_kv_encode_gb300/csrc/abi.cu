@@ -30,7 +30,8 @@ cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, in
 cudaError_t launch_front(const bpkv_cache& c, const uint16_t* k_new, const uint16_t* v_new, int32_t t_new,
                          const float* q, const float* sigma2, const int32_t* budget_q, int32_t depth_rule,
                          int32_t n_channels, int32_t depth, uint8_t* depths, void* plan, uint32_t* hist,
-                         uint32_t* hist1, uint32_t* ctr, uint32_t* tickets, uint32_t* seq_tick, cudaStream_t st);
+                         uint32_t* hist1, uint32_t* ctr, uint32_t* tickets, uint32_t* seq_tick, cudaStream_t st,
+                         const uint8_t* depths_in);
 bool scan_counts_hist(const bpkv_cache& c);
 cudaError_t launch_union(const bpkv_cache& c, const int32_t* idx, int32_t k, int32_t* uidx, uint8_t* umask,
                          int32_t* ucount, cudaStream_t st);
@@ -318,7 +319,8 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
   if (a->depth_rule == BPKV_DEPTH_WATERFILL && (!a->sigma2 || !a->budget_q)) return BPKV_EINVAL;
   if (a->depth_rule == BPKV_DEPTH_FIXED && (a->fixed_channels < 0 || a->fixed_depth < 0 || a->fixed_depth > 4))
     return BPKV_EINVAL;
-  if (a->depth_rule < 0 || a->depth_rule > 2) return BPKV_EINVAL;
+  if (a->depth_rule < 0 || a->depth_rule > 3) return BPKV_EINVAL;
+  if (a->depth_rule == BPKV_DEPTH_GIVEN && !a->depths_in) return BPKV_EINVAL;
   if (!dense) {
     BPKV_TRY(check_k(a->k, a->n_sink, a->n_recent));
     if ((int64_t)a->k * layers[0].group > kMaxUnion) return BPKV_EINVAL;
@@ -368,7 +370,8 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
     void* plan = at(ws, L.plan);
     const SelBufs sb = sel_bufs(ws, L);
     const float* s2 = a->sigma2 ? a->sigma2 + (size_t)l * NH * kD : nullptr;
-    const bool tail = !dense && (a->flags & BPKV_STEP_TAIL) && tail_eligible(c, a->k, a->n_sink, a->n_recent);
+    const bool tail = !dense && a->depth_rule != BPKV_DEPTH_GIVEN && (a->flags & BPKV_STEP_TAIL) &&
+                      tail_eligible(c, a->k, a->n_sink, a->n_recent);
     if (dense || tail) {
       // append (and length update) first, then the stages one by one
       BPKV_TRY(cuda_status(launch_encode_append(c, kn, vn, 1, st)));
@@ -400,7 +403,7 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
     const bool l1 = c.n_max + 1 >= kLongRowTokens;
     BPKV_TRY(cuda_status(launch_front(c, kn, vn, 1, q, s2, a->budget_q, a->depth_rule, a->fixed_channels,
                                       a->fixed_depth, depths, plan, sb.hist, l1 ? sb.hist1 : nullptr, sb.ctr,
-                                      tickets, seq_tick, st)));
+                                      tickets, seq_tick, st, a->depths_in)));
     c.n_max += 1;
     BPKV_TRY(mark(l, 1));
     BPKV_TRY(mark(l, 2));

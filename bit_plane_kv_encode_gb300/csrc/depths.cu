@@ -109,7 +109,8 @@ size_t scan_plan_bytes(int group) {
 
 struct FrontArgs {
   DepthArgs d;
-  int32_t depth_rule;       // BPKV_DEPTH_WATERFILL or BPKV_DEPTH_FIXED
+  int32_t depth_rule;       // BPKV_DEPTH_WATERFILL, BPKV_DEPTH_FIXED or BPKV_DEPTH_GIVEN
+  const uint8_t* depths_in; // BPKV_DEPTH_GIVEN: [N][H][D] the caller's depths
   uint32_t* seq_tick;       // [N]: zeroed for the attention of this step
   uint32_t* hist1;          // optional [N][H][G][kTopkBins]: zeroed with the level-0 histograms
   // append
@@ -167,20 +168,26 @@ __global__ void __launch_bounds__(kScanThreads) k_front(FrontArgs a) {
     if (h == 0) a.seq_tick[s] = 0u;
   }
   uint8_t* dep = a.d.depths + unit * kD;
-  if (a.depth_rule == BPKV_DEPTH_WATERFILL)
+  if (a.depth_rule == BPKV_DEPTH_WATERFILL) {
     alloc_depths_cta(S, a.d.q + unit * G * kD, a.d.sigma2 + unit * kD, G, a.d.budget_q[s], dep);
-  else
+  } else if (a.depth_rule == BPKV_DEPTH_GIVEN) {
+    // each thread writes the entry it reads back in emit_plan
+    if (threadIdx.x < kD) dep[threadIdx.x] = (uint8_t)min((int)a.depths_in[unit * kD + threadIdx.x], 4);
+  } else {
     fixed_depths_cta(S, a.d.q + unit * G * kD, G, a.d.n_channels, a.d.depth, dep);
+  }
   emit_plan<GP>(a.d, unit, dep);
 }
 
 cudaError_t launch_front(const bpkv_cache& c, const uint16_t* k_new, const uint16_t* v_new, int32_t t_new,
                          const float* q, const float* sigma2, const int32_t* budget_q, int32_t depth_rule,
                          int32_t n_channels, int32_t depth, uint8_t* depths, void* plan, uint32_t* hist,
-                         uint32_t* hist1, uint32_t* ctr, uint32_t* tickets, uint32_t* seq_tick, cudaStream_t st) {
+                         uint32_t* hist1, uint32_t* ctr, uint32_t* tickets, uint32_t* seq_tick, cudaStream_t st,
+                         const uint8_t* depths_in) {
   FrontArgs a;
   a.d = DepthArgs{q, sigma2, budget_q, depths, c.n_kv_heads, c.group, tickets, plan, n_channels, depth, hist, ctr};
   a.depth_rule = depth_rule;
+  a.depths_in = depths_in;
   a.seq_tick = seq_tick;
   a.hist1 = hist1;
   a.planes = c.planes;

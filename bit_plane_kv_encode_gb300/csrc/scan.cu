@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(kScanThreads, GP >= 8 ? 2 : 4) k_scan(ScanArgs
     int t = 0;
     float qv[GP];
     if (tid < kD) {
-      t = a.depths[unit * kD + tid];
+      t = min((int)a.depths[unit * kD + tid], 4);  // depth values above 4 read as 4
       const float* qp = a.q + unit * G * kD;
 #pragma unroll
       for (int hh = 0; hh < GP; ++hh) qv[hh] = hh < G ? qp[hh * kD + tid] : 0.f;
@@ -111,7 +111,7 @@ __device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& 
     int t = 0;
     float qv[GP];
     if (tid < kD) {
-      t = a.depths[unit * kD + tid];
+      t = min((int)a.depths[unit * kD + tid], 4);  // depth values above 4 read as 4
       const float* qp = a.q + unit * G * kD;
 #pragma unroll
       for (int hh = 0; hh < GP; ++hh) qv[hh] = hh < G ? qp[hh * kD + tid] : 0.f;

@@ -155,12 +155,34 @@ int bpkv_alloc_depths(const bpkv_cache *c, const float *q, const float *sigma2, 
 int bpkv_fixed_depths(const bpkv_cache *c, const float *q, int32_t n_channels, int32_t depth,
                       uint8_t *depths, void *stream);
 
+/*
+ * Fathom page section 2 ("Double Sparsity"): a channel set chosen offline from
+ * calibration statistics.  For each of n_units units (e.g. every (layer, KV
+ * head), or every (sequence, KV head) of one layer), the statistic of channel j
+ * is mean|q_j| over the unit's calibration queries and its `group` query heads
+ * times mean|k_j| over its calibration keys; the n_channels channels with the
+ * largest statistic (ties to the lower index) get depth `depth`, the others 0
+ * (32 channels at depth 4 read 136 bits per token).  Sums run in double in
+ * storage order (queries, then heads; keys in order), each mean divides its sum
+ * once and the product is one double multiplication, so the choice matches a
+ * plain CPU evaluation exactly.  Inputs must be finite.
+ *   q_cal   float [n_units][m_q][group][D]   calibration queries (device)
+ *   k_cal   bf16  [n_units][m_k][D]          calibration keys (device)
+ *   depths  uint8 [n_units][D]               out (device); pass to bpkv_decode_step
+ *                                             with BPKV_DEPTH_GIVEN or to the scans
+ * BPKV_EINVAL for n_units, group, m_q or m_k below 1, group above
+ * BPKV_MAX_GROUP, n_channels below 0 or depth outside 0..4.
+ */
+int bpkv_calibrate_channels(const float *q_cal, const uint16_t *k_cal, int32_t n_units, int32_t group, int64_t m_q,
+                            int64_t m_k, int32_t n_channels, int32_t depth, uint8_t *depths, void *stream);
+
 /* ------------------------------------------------------------- scan (F3, F7) */
 /*
  * Fathom page sections 1 and 3.1.  score[i][h][g][x] = sum_j q_gj khat_xj(t_j)
  * for every token x < seq_len[i], where for t = depths[i][h][j] > 0
  * khat = s ((c_t + 1/2) 2^(4-t) - 8), c_t the first t planes of the code and
- * s the block scale; channels with t = 0 are not read.  No 1/sqrt(D) factor.
+ * s the block scale; channels with t = 0 are not read (depth values above 4
+ * are read as 4).  No 1/sqrt(D) factor.
  *   scores float [N][H][G][ld_scores], ld_scores >= n_max; entries past
  *   seq_len[i] are not written.
  */
@@ -240,6 +262,7 @@ int bpkv_dense_attend(const bpkv_cache *c, const float *q, float *out, void *ws,
 #define BPKV_DEPTH_WATERFILL 0  /* bpkv_alloc_depths with sigma2 and budget_q */
 #define BPKV_DEPTH_FIXED 1      /* bpkv_fixed_depths(fixed_channels, fixed_depth) */
 #define BPKV_DEPTH_DENSE 2      /* no scan: dense attention over all rows */
+#define BPKV_DEPTH_GIVEN 3      /* the caller's depths_in (e.g. from bpkv_calibrate_channels) */
 
 typedef struct bpkv_step_args {
   const uint16_t *k_new;    /* [L][N][H][D] bf16: the one new token per sequence and layer */
@@ -261,6 +284,8 @@ typedef struct bpkv_step_args {
                                the first five stages are the fused kernel and the
                                last one the sequence-length update */
   int32_t flags;            /* BPKV_STEP_* */
+  const uint8_t *depths_in; /* [L][N][H][D] BPKV_DEPTH_GIVEN: depth of every channel (values above
+                               4 read as 4; depths_out, if given, receives them as read) */
 } bpkv_step_args;
 
 #define BPKV_STAGE_EVENTS 7

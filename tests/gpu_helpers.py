@@ -78,7 +78,7 @@ def check_topk_sets(gpu_idx: np.ndarray, ref_idx: np.ndarray, ref_score: np.ndar
 
 
 def decode_one_layer(inp, cfg, depth_rule=0, fixed=(0, 0), budgets=None, residency="hbm", dev="cuda", flags=0,
-                     lists=True):
+                     lists=True, depths_in=None):
     """Prefill n-1 tokens of a generated layer, then one bpkv_decode_step (appends
     token n-1 and runs the whole path).  Returns (cache, depths, idx, out) with
     depths [N][H][D], idx [N][H][G][k], out [N][H][G][D] on the device; with
@@ -100,7 +100,8 @@ def decode_one_layer(inp, cfg, depth_rule=0, fixed=(0, 0), budgets=None, residen
     v_new = v_all[:, :, n - 1][None].contiguous()
     a = pk.bpkv_step_args(k_new.data_ptr(), v_new.data_ptr(), q.data_ptr(), sigma2.data_ptr(), budget_q.data_ptr(),
                           depth_rule, fixed[0], fixed[1], cfg.k, cfg.n_sink, cfg.n_recent, out.data_ptr(),
-                          depths.data_ptr(), idx.data_ptr() if lists else None, None, flags)
+                          depths.data_ptr(), idx.data_ptr() if lists else None, None, flags,
+                          depths_in.data_ptr() if depths_in is not None else None)
     arr = pk.cache_array([cache])
     pk.bpkv_clear_status(ws)
     pk.bpkv_decode_step(arr, 1, a, ws, ws.numel())
@@ -111,7 +112,7 @@ def decode_one_layer(inp, cfg, depth_rule=0, fixed=(0, 0), budgets=None, residen
 
 
 def check_unit(orc, cfg, inp, cache, depths, idx, out, s, h, depth_rule=0, fixed=(0, 0), budget_bits=None,
-               what=""):
+               what="", depth=None):
     """Oracle decode of unit (s, h) vs the GPU results; returns the number of
     heads whose sets matched exactly (their outputs are checked too)."""
     n = inp.k.shape[2]
@@ -119,7 +120,7 @@ def check_unit(orc, cfg, inp, cache, depths, idx, out, s, h, depth_rule=0, fixed
     b = int(inp.budgets[s]) if budget_bits is None else budget_bits
     ref = orc.decode_unit(kb, vb, inp.q[s, h].numpy(), inp.sigma2[s, h].numpy(), b, cfg.k, cfg.n_sink,
                           cfg.n_recent, nb_cap=cache.c.cap_tokens // 64,
-                          fixed=fixed if depth_rule == 1 else None)
+                          fixed=fixed if depth_rule == 1 else None, depth=depth)
     nb = (n + 63) // 64
     assert np.array_equal(bits64(cache.planes[s, h])[:, :, :nb], ref["planes"][:, :, :nb]), f"{what} planes"
     assert np.array_equal(bits16(cache.scales[s, h])[:, :nb], ref["scales"][:, :nb]), f"{what} scales"
