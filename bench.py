@@ -58,6 +58,10 @@ def parse():
     p.add_argument("--fused", action="store_true", help="one fused cluster kernel per pass where eligible")
     p.add_argument("--tail", action="store_true", help="one cluster kernel for top-k, union and attention")
     p.add_argument("--budget", type=int, default=0, help="run this budget only (bits/token)")
+    p.add_argument("--layers", type=int, default=0,
+                   help="profiling aid: decode only this many of the config's layers (reported in config)")
+    p.add_argument("--no-extras", action="store_true",
+                   help="profiling aid: skip the end-to-end and baseline measurements")
     return p.parse_args()
 
 
@@ -233,9 +237,12 @@ def cache_bytes(cfg, n: int) -> int:
 
 
 # baselines through the same entry point (Fathom page, section 2): the SparQ
-# channel rule with 32 channels at full depth (136 bits/token), the 2-bit
-# thumbnail (all channels at 2 planes, 288 bits/token) and dense attention
-BASELINE_ARMS = {"fixed_136": ("fixed", 32, 4), "thumbnail_288": ("fixed", 128, 2), "dense_bf16": ("dense", 0, 0)}
+# channel rule with 32 channels at full depth (136 bits/token), an offline
+# calibrated set of 32 channels at full depth (Double Sparsity's statistic over
+# each unit's first 2048 cached keys and 16 seeded calibration queries), the
+# 2-bit thumbnail (all channels at 2 planes, 288 bits/token) and dense attention
+BASELINE_ARMS = {"fixed_136": ("fixed", 32, 4), "calibrated_136": ("given", 32, 4), "thumbnail_288": ("fixed", 128, 2),
+                 "dense_bf16": ("dense", 0, 0)}
 
 
 def baseline_steps(steps: int) -> int:
@@ -395,8 +402,8 @@ def bench_ours(args, cfg, rank, world, local):
                 "launch_us": round(kms * 1e3 / n_launch, 2)}
 
     # end to end through host buffers: inputs copied in, outputs copied out, inside the timed region
-    e2e = bench_e2e(args, passes, io, ws, flush, dev, keys_per_step, world)
-    baselines = bench_baselines(args, cfg, passes, io, ws, flush, dev, world)
+    e2e = None if args.no_extras else bench_e2e(args, passes, io, ws, flush, dev, keys_per_step, world)
+    baselines = None if args.no_extras else bench_baselines(args, cfg, passes, io, ws, flush, dev, world)
 
     line = {
         "metric": "keys scored/s", "value": round(value), "unit": "keys/s", "n_gpus": world,
@@ -426,8 +433,9 @@ def bench_ours(args, cfg, rank, world, local):
         "e2e": e2e,
         "baselines": baselines,
         "baselines_note": ("same entry point, same caches and step structure: SparQ channel rule at 32 channels "
-                           "x 4 planes (136 bits/token), all channels at 2 planes (288 bits/token), dense bf16 "
-                           "attention over every row; read bytes are the plane prefixes (or rows for dense)"),
+                           "x 4 planes (136 bits/token), 32 offline-calibrated channels x 4 planes (136 bits/token), "
+                           "all channels at 2 planes (288 bits/token), dense bf16 attention over every row; read "
+                           "bytes are the plane prefixes (or rows for dense)"),
         "gpu_launches": args.steps * L * sum(launches_per_pass(p, args) for p in passes),
         "clocks": clk,
         "wall_s_timed": round(wall, 3),
@@ -450,11 +458,23 @@ def bench_baselines(args, cfg, passes, io, ws, flush, dev, world):
     L, N, H, D, n = cfg.n_layers, cfg.n_seq, cfg.n_kv_heads, cfg.head_dim, cfg.n_tokens
     keys = L * N * H * n
     out = {}
+    G = cfg.group
     for name, (rule, r, t) in BASELINE_ARMS.items():
-        rule_id = pk.DEPTH_FIXED if rule == "fixed" else pk.DEPTH_DENSE
+        rule_id = {"fixed": pk.DEPTH_FIXED, "given": pk.DEPTH_GIVEN, "dense": pk.DEPTH_DENSE}[rule]
+        depths_in = None
+        if rule == "given":
+            # offline calibration (not timed): per layer and unit, 16 seeded queries and the first 2048 keys
+            m_k = min(2048, n - 1)
+            gen = torch.Generator(device="cpu")
+            gen.manual_seed(cfg.seed * 1000 + 17)
+            depths_in = torch.zeros((L, N, H, D), dtype=torch.uint8, device=dev)
+            for li, c in enumerate(p0["caches"]):
+                q_cal = torch.randn((N * H, 16, G, D), generator=gen).to(dev)
+                k_cal = c.k_rows.view(N * H, -1, D)[:, :m_k].contiguous().to(dev)
+                pk.bpkv_calibrate_channels(q_cal, k_cal, N * H, G, 16, m_k, r, t, depths_in[li])
         a = pk.bpkv_step_args(io["k_new"].data_ptr(), io["v_new"].data_ptr(), io["q"].data_ptr(), None, None,
                               rule_id, r, t, cfg.k, cfg.n_sink, cfg.n_recent, p0["out"].data_ptr(), None, None,
-                              None, 0)
+                              None, 0, depths_in.data_ptr() if depths_in is not None else None)
 
         def run():
             for layer in p0["arr"]:
@@ -534,7 +554,6 @@ def bench_e2e(args, passes, io, ws, flush, dev, keys_per_step, world):
 def load_traffic(kernel: str, workload: str, budgets):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     this workload and budgets and still matches the kernel source."""
-    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         d = json.load(open(path))[kernel]
@@ -542,9 +561,16 @@ def load_traffic(kernel: str, workload: str, budgets):
         return None
     if d.get("workload") != workload or list(d.get("budgets_bits", [])) != list(budgets):
         return None
-    src = os.path.join(ROOT, "bit_plane_kv_encode_gb300", "csrc", d["source"])
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return d["dram_bytes_per_launch"] if h == d.get("source_sha256_16") else None
+    return d["dram_bytes_per_launch"] if source_hash(d["source"]) == d.get("source_sha256_16") else None
+
+
+def source_hash(files) -> str:
+    """First 16 hex digits of the SHA-256 of the kernel's source files, concatenated."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ([files] if isinstance(files, str) else files):
+        h.update(open(os.path.join(ROOT, "bit_plane_kv_encode_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -645,6 +671,9 @@ def main():
     args = parse()
     from workload import CONFIGS
     cfg = CONFIGS[args.workload]
+    if args.layers:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, n_layers=min(args.layers, cfg.n_layers))
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
         line = bench_reference(args, cfg, rank, args.gpus)
