@@ -23,7 +23,9 @@
  *     softmax(q K^T / sqrt(D)) V over the selected set;
  *   - section 2 ("SparQ"): fixed channel sets by summed |q| over the group;
  *   - section 2 ("Double Sparsity"): channel sets chosen offline from
- *     calibration statistics (mean |q| times mean |k| per channel).
+ *     calibration statistics (mean |q| times mean |k| per channel);
+ *   - contributions, basis rule: KLT planes (an orthogonal basis) for models
+ *     without QK norm, applied to keys and queries alike.
  * Readings where the page is silent (bit order inside a word, zero and
  * overflowing scales, tie rules, stop rule of the allocator) are stated at each
  * function.
@@ -274,6 +276,48 @@ void or_calibrate_channels(int32_t D, int32_t G, int64_t m_q, const float *q_cal
     if (rank < c) depth[j] = (uint8_t)t;
   }
   free(st);
+}
+
+/* ---------------------------------------------------------------- basis */
+
+/* A fixed orthogonal basis for the scanned key codes (Fathom page, section 1,
+ * contributions: KLT planes of the keys for models without QK norm; ReadKV
+ * page, section 5.1: the same Hadamard-sign transform on keys and queries keeps
+ * their inner products).  Reading: y_l = sum_j x_j R[j][l] with R [D][D], as a
+ * chain of float32 fused multiply-adds in order j = 0 .. D-1 starting from 0,
+ * one chain per output. */
+void or_rotate(int32_t D, int64_t rows, const float *x, const float *R, float *y) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int32_t l = 0; l < D; ++l) {
+      float acc = 0.0f;
+      for (int32_t j = 0; j < D; ++j) {
+        const float rv = (OR_MUTANT == 13) ? R[l * D + j] : R[j * D + l];
+        acc = fmaf(x[r * D + j], rv, acc);
+      }
+      y[r * D + l] = acc;
+    }
+}
+
+/* float32 to bf16 bit pattern, round to nearest even (finite values). */
+static uint16_t or_bf16_bits(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+/* Keys in the basis, rounded to bf16: the encoder codes these (the stored
+ * rows for exact attention stay in the original channels). */
+void or_rotate_keys(int32_t D, int64_t n, const uint16_t *k_bits, const float *R, uint16_t *out_bits) {
+  float *x = (float *)malloc(sizeof(float) * (size_t)D);
+  float *y = (float *)malloc(sizeof(float) * (size_t)D);
+  for (int64_t i = 0; i < n; ++i) {
+    for (int32_t j = 0; j < D; ++j) x[j] = (float)or_bf16_value(k_bits[i * D + j]);
+    or_rotate(D, 1, x, R, y);
+    for (int32_t l = 0; l < D; ++l) out_bits[i * D + l] = or_bf16_bits(y[l]);
+  }
+  free(x);
+  free(y);
 }
 
 /* ---------------------------------------------------------------- scores */

@@ -59,6 +59,10 @@ def _bind(path: str) -> ctypes.CDLL:
     L.or_fixed_depths.restype = None
     L.or_calibrate_channels.argtypes = [i32, i32, i64, P, i64, P, i32, i32, P]
     L.or_calibrate_channels.restype = None
+    L.or_rotate.argtypes = [i32, i64, P, P, P]
+    L.or_rotate.restype = None
+    L.or_rotate_keys.argtypes = [i32, i64, P, P, P]
+    L.or_rotate_keys.restype = None
     L.or_scores.argtypes = [i64, i32, i32, P, P, i64, P, P, P]
     L.or_scores.restype = None
     L.or_topk.argtypes = [i64, P, i32, i32, i32, P]
@@ -144,6 +148,24 @@ class Oracle:
                                      _p(depth))
         return depth
 
+    def rotate(self, x: np.ndarray, R: np.ndarray) -> np.ndarray:
+        """x float [rows][D] -> x R (float32 fused multiply-add chains)."""
+        x = _c(x, np.float32)
+        R = _c(R, np.float32)
+        rows, D = x.reshape(-1, x.shape[-1]).shape
+        y = np.zeros(x.shape, dtype=np.float32)
+        self.L.or_rotate(D, rows, _p(x), _p(R), _p(y))
+        return y
+
+    def rotate_keys(self, k_bits: np.ndarray, R: np.ndarray) -> np.ndarray:
+        """bf16 patterns [n][D] -> bf16 patterns of k R."""
+        k_bits = _c(k_bits, np.uint16)
+        R = _c(R, np.float32)
+        n, D = k_bits.shape
+        out = np.zeros((n, D), dtype=np.uint16)
+        self.L.or_rotate_keys(D, n, _p(k_bits), _p(R), _p(out))
+        return out
+
     def scores(self, n: int, scales: np.ndarray, planes: np.ndarray, depth: np.ndarray,
                q: np.ndarray) -> np.ndarray:
         scales = _c(scales, np.uint16)
@@ -192,18 +214,24 @@ class Oracle:
     def decode_unit(self, k_bits: np.ndarray, v_bits: np.ndarray, q: np.ndarray, sigma2: np.ndarray,
                     budget_bits: int | None, k: int, n_sink: int = 4, n_recent: int = 32,
                     nb_cap: int | None = None, depth: np.ndarray | None = None,
-                    fixed: tuple | None = None) -> dict:
+                    fixed: tuple | None = None, basis: np.ndarray | None = None) -> dict:
         """One decode step of one unit: encode the n rows, allocate depths (or
-        take ``depth`` / a ``fixed`` rule), score, select, union, attend."""
+        take ``depth`` / a ``fixed`` rule), score, select, union, attend.  With
+        a ``basis`` R the codes are those of the keys k R and the depths and
+        scores use q R (sigma2 is then the variance in that basis); the
+        attention uses the original q and rows."""
         n, D = k_bits.shape
         nb_cap = nb_cap if nb_cap is not None else (n + 63) // 64
-        scales, planes = self.encode(k_bits, nb_cap)
+        kq, qq = k_bits, q
+        if basis is not None:
+            kq, qq = self.rotate_keys(k_bits, basis), self.rotate(q, basis)
+        scales, planes = self.encode(kq, nb_cap)
         if depth is None:
             if fixed is not None:
-                depth = self.fixed_depths(q, fixed[0], fixed[1])
+                depth = self.fixed_depths(qq, fixed[0], fixed[1])
             else:
-                depth = self.alloc_depths(q, sigma2, 4 * int(budget_bits))
-        sc = self.scores(n, scales, planes, depth, q)
+                depth = self.alloc_depths(qq, sigma2, 4 * int(budget_bits))
+        sc = self.scores(n, scales, planes, depth, qq)
         G = q.shape[0]
         idx = np.stack([self.topk(sc[h], k, n_sink, n_recent) for h in range(G)])
         uidx, umask = self.union(idx)

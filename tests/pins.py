@@ -408,6 +408,86 @@ def pin_calibrated_channels(o):
     assert np.array_equal(d0, want)
 
 
+def _round_fp32(v):
+    """Nearest float32 to the rational v (ties to even), as a Fraction."""
+    from fractions import Fraction
+    if v == 0:
+        return Fraction(0)
+    sign = -1 if v < 0 else 1
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    e = max(e, -126)                      # subnormals share the lowest exponent
+    ulp = Fraction(2) ** (e - 23)
+    q, r = divmod(a / ulp, 1)
+    q = int(q)
+    if r > Fraction(1, 2) or (r == Fraction(1, 2) and q % 2 == 1):
+        q += 1
+    return sign * q * ulp
+
+
+def _bf16_of_fraction(v) -> int:
+    """bf16 pattern of a float32 value given as a Fraction (round to nearest even)."""
+    f = np.float32(float(v))              # exact: v is a float32 value
+    u = int(np.array([f], np.float32).view(np.uint32)[0])
+    u += 0x7FFF + ((u >> 16) & 1)
+    return (u >> 16) & 0xFFFF
+
+
+def pin_basis(o):
+    from fractions import Fraction
+    rng = np.random.default_rng(21)
+    D = 128
+    # exact: each output is a chain of float32 fused multiply-adds in channel order
+    x = (rng.standard_normal((2, D)) * np.exp(rng.standard_normal((2, D)))).astype(np.float32)
+    R = rng.standard_normal((D, D)).astype(np.float32)
+    y = o.rotate(x, R)
+    for r in range(2):
+        for l in range(0, D, 9):
+            acc = Fraction(0)
+            for j in range(D):
+                acc = _round_fp32(Fraction(float(x[r, j])) * Fraction(float(R[j, l])) + acc)
+            assert y[r, l] == np.float32(float(acc)), (r, l)
+    kb = bf16_bits_of(rng.standard_normal((3, D)) * 3)
+    yk = o.rotate_keys(kb, R)
+    xk = bf16_value(kb).astype(np.float32)
+    for r in range(3):
+        for l in range(0, D, 13):
+            acc = Fraction(0)
+            for j in range(D):
+                acc = _round_fp32(Fraction(float(xk[r, j])) * Fraction(float(R[j, l])) + acc)
+            assert int(yk[r, l]) == _bf16_of_fraction(acc), (r, l)
+    # identity and permutation bases move bits, nothing else
+    k = bf16_bits_of(rng.standard_normal((50, D)) * 2)
+    assert np.array_equal(o.rotate_keys(k, np.eye(D, dtype=np.float32)), k)
+    perm = rng.permutation(D)
+    P = np.zeros((D, D), np.float32)
+    P[perm, np.arange(D)] = 1.0
+    assert np.array_equal(o.rotate_keys(k, P), k[:, perm])
+    # an orthogonal basis (signed, normalised Hadamard) keeps inner products
+    H = np.array([[1.0]])
+    while H.shape[0] < D:
+        H = np.block([[H, H], [H, -H]])
+    Hs = (H * rng.choice([-1.0, 1.0], D)[:, None] / np.sqrt(D)).astype(np.float32)
+    q = rng.standard_normal((4, D)).astype(np.float32)
+    kk = rng.standard_normal((6, D)).astype(np.float32)
+    ref = q.astype(np.float64) @ kk.astype(np.float64).T
+    got = o.rotate(q, Hs).astype(np.float64) @ o.rotate(kk, Hs).astype(np.float64).T
+    assert np.allclose(got, ref, rtol=0, atol=1e-4 * np.abs(ref).max())
+    # the identity basis is a no-op for a whole decode of one unit
+    n = 300
+    kb2, vb2 = bf16_bits_of(rng.standard_normal((n, D)) * 2), bf16_bits_of(rng.standard_normal((n, D)))
+    q2 = rng.standard_normal((4, D)).astype(np.float32)
+    s2 = np.exp(rng.standard_normal(D)).astype(np.float32)
+    a = o.decode_unit(kb2, vb2, q2, s2, 92, 64)
+    b = o.decode_unit(kb2, vb2, q2, s2, 92, 64, basis=np.eye(D, dtype=np.float32))
+    for key in ("planes", "scales", "depth", "idx", "out"):
+        assert np.array_equal(a[key], b[key]), key
+
+
 # ------------------------------------------------------------------ selection
 
 def _topk_brute(score, k, n_sink=4, n_recent=32):
@@ -484,4 +564,4 @@ def pin_attention(o):
 
 ALL_PINS = [pin_fp16, pin_codes_exact, pin_prefix_quantiser, pin_special_values, pin_bit_order_golden,
             pin_scores, pin_alloc_bruteforce, pin_alloc_golden, pin_fixed_depths, pin_calibrated_channels,
-            pin_topk, pin_union, pin_attention]
+            pin_basis, pin_topk, pin_union, pin_attention]

@@ -2,8 +2,8 @@
 (-DOR_MUTANT=n, see the header of oracle/bpkv_oracle.c) must fail at least one
 pin.  The mistakes are plausible slips in reading the Fathom page: bit or plane
 order, floor vs round, the mid-rise half step, the scale's cost, q^2 vs |q|,
-tie rules, the 1/sqrt(D) factor, the union mask, stop vs skip and the
-calibration statistic."""
+tie rules, the 1/sqrt(D) factor, the union mask, stop vs skip, the
+calibration statistic and the basis orientation."""
 import pytest
 
 from pins import ALL_PINS
@@ -21,6 +21,7 @@ MUTANTS = {
     10: "allocator skips an unaffordable item instead of stopping",
     11: "calibrated channel sets rank by mean |q| alone",
     12: "calibrated channel sets average q^2 instead of |q|",
+    13: "basis applied transposed",
 }
 
 
