@@ -12,7 +12,7 @@ import ctypes
 
 from ._binding import (  # noqa: F401
     BpkvError, bpkv_alloc_depths, bpkv_cache, bpkv_calibrate_channels, bpkv_clear_status, bpkv_decode_step,
-    bpkv_dense_attend, bpkv_encode_append, bpkv_fixed_depths, bpkv_read_status, bpkv_scan, bpkv_scan_topk, bpkv_scan_topk_noalloc, bpkv_sparse_attend,
+    bpkv_dense_attend, bpkv_encode_append, bpkv_fixed_depths, bpkv_read_status, bpkv_rotate, bpkv_scan, bpkv_scan_topk, bpkv_scan_topk_noalloc, bpkv_sparse_attend,
     bpkv_status_string, bpkv_step_args, bpkv_step_fused, bpkv_topk, bpkv_union, bpkv_version, bpkv_workspace_size, header_symbols, load)
 
 HEAD_DIM = 128
@@ -48,9 +48,16 @@ class Cache:
         self.k_rows = buf((n_seq, n_kv_heads, cap_tokens, D), torch.bfloat16)
         self.v_rows = buf((n_seq, n_kv_heads, cap_tokens, D), torch.bfloat16)
         self.seq_len = torch.zeros(n_seq, dtype=torch.int64, device=self.device)
+        self.basis = None
         self.c = bpkv_cache(n_seq, n_kv_heads, group, D, cap_tokens, 0, 1 if host else 0, 0,
                             self.planes.data_ptr(), self.scales.data_ptr(), self.k_rows.data_ptr(),
-                            self.v_rows.data_ptr(), self.seq_len.data_ptr())
+                            self.v_rows.data_ptr(), self.seq_len.data_ptr(), None)
+
+    def set_basis(self, basis):
+        """Code the keys in an orthogonal basis R, float [H][D][D] on the device
+        (None: the raw channels); set it before the first append."""
+        self.basis = None if basis is None else basis.contiguous()
+        self.c.basis = None if basis is None else self.basis.data_ptr()
 
     @property
     def n_max(self) -> int:

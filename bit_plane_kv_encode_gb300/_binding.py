@@ -30,7 +30,7 @@ class bpkv_cache(ctypes.Structure):
     _fields_ = [
         ("n_seq", i32), ("n_kv_heads", i32), ("group", i32), ("head_dim", i32),
         ("cap_tokens", i64), ("n_max", i64), ("residency", i32), ("reserved", i32),
-        ("planes", P), ("scales", P), ("k_rows", P), ("v_rows", P), ("seq_len", P),
+        ("planes", P), ("scales", P), ("k_rows", P), ("v_rows", P), ("seq_len", P), ("basis", P),
     ]
 
 
@@ -54,6 +54,7 @@ _SIGS = {
     "bpkv_alloc_depths": ([P, P, P, P, P, P], ctypes.c_int),
     "bpkv_fixed_depths": ([P, P, i32, i32, P, P], ctypes.c_int),
     "bpkv_calibrate_channels": ([P, P, i32, i32, i64, i64, i32, i32, P, P], ctypes.c_int),
+    "bpkv_rotate": ([P, i32, i32, i64, P, P, P], ctypes.c_int),
     "bpkv_scan": ([P, P, P, P, i64, P], ctypes.c_int),
     "bpkv_topk": ([P, P, i64, i32, i32, i32, P, P, sz, P], ctypes.c_int),
     "bpkv_scan_topk": ([P, P, P, i32, i32, i32, P, P, sz, P], ctypes.c_int),
@@ -170,6 +171,11 @@ def bpkv_calibrate_channels(q_cal, k_cal, n_units: int, group: int, m_q: int, m_
                   load().bpkv_calibrate_channels(_ptr(q_cal), _ptr(k_cal), int(n_units), int(group), int(m_q),
                                                  int(m_k), int(n_channels), int(depth), _ptr(depths),
                                                  _stream(stream)))
+
+
+def bpkv_rotate(basis, n_seq: int, n_kv_heads: int, rows: int, x, y, stream=None):
+    return _check("bpkv_rotate", load().bpkv_rotate(_ptr(basis), int(n_seq), int(n_kv_heads), int(rows), _ptr(x),
+                                                    _ptr(y), _stream(stream)))
 
 
 def bpkv_scan(cache, q, depths, scores, ld_scores: int, stream=None):

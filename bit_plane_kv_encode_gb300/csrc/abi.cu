@@ -31,7 +31,7 @@ cudaError_t launch_front(const bpkv_cache& c, const uint16_t* k_new, const uint1
                          const float* q, const float* sigma2, const int32_t* budget_q, int32_t depth_rule,
                          int32_t n_channels, int32_t depth, uint8_t* depths, void* plan, uint32_t* hist,
                          uint32_t* hist1, uint32_t* ctr, uint32_t* tickets, uint32_t* seq_tick, cudaStream_t st,
-                         const uint8_t* depths_in);
+                         const uint8_t* depths_in, float* q_rot);
 bool scan_counts_hist(const bpkv_cache& c);
 cudaError_t launch_union(const bpkv_cache& c, const int32_t* idx, int32_t k, int32_t* uidx, uint8_t* umask,
                          int32_t* ucount, cudaStream_t st);
@@ -89,7 +89,7 @@ int check_k(int32_t k, int32_t n_sink, int32_t n_recent) {
 // Workspace layout: status word, then the buffers each call family needs.
 struct Layout {
   size_t scores = 0, hist = 0, hist1 = 0, ctr = 0, cand = 0, cut = 0, part = 0, depths = 0, idx = 0, uidx = 0, umask = 0,
-         ucount = 0, tickets = 0, seq_tick = 0, plan = 0, total = 0;
+         ucount = 0, tickets = 0, seq_tick = 0, plan = 0, q_rot = 0, total = 0;
 };
 
 Layout layout(const bpkv_cache& c, int32_t k, int32_t what) {
@@ -141,6 +141,8 @@ Layout layout(const bpkv_cache& c, int32_t k, int32_t what) {
     off = align_up(off + (size_t)c.n_seq * sizeof(uint32_t));
     L.plan = off;
     off = align_up(off + NH * scan_plan_bytes(c.group));
+    L.q_rot = off;  // q R when the cache has a basis
+    off = align_up(off + NH * c.group * kD * sizeof(float));
   }
   L.total = off;
   return L;
@@ -370,7 +372,7 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
     void* plan = at(ws, L.plan);
     const SelBufs sb = sel_bufs(ws, L);
     const float* s2 = a->sigma2 ? a->sigma2 + (size_t)l * NH * kD : nullptr;
-    const bool tail = !dense && a->depth_rule != BPKV_DEPTH_GIVEN && (a->flags & BPKV_STEP_TAIL) &&
+    const bool tail = !dense && a->depth_rule != BPKV_DEPTH_GIVEN && !c.basis && (a->flags & BPKV_STEP_TAIL) &&
                       tail_eligible(c, a->k, a->n_sink, a->n_recent);
     if (dense || tail) {
       // append (and length update) first, then the stages one by one
@@ -403,7 +405,8 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
     const bool l1 = c.n_max + 1 >= kLongRowTokens;
     BPKV_TRY(cuda_status(launch_front(c, kn, vn, 1, q, s2, a->budget_q, a->depth_rule, a->fixed_channels,
                                       a->fixed_depth, depths, plan, sb.hist, l1 ? sb.hist1 : nullptr, sb.ctr,
-                                      tickets, seq_tick, st, a->depths_in)));
+                                      tickets, seq_tick, st, a->depths_in,
+                                      reinterpret_cast<float*>(at(ws, L.q_rot)))));
     c.n_max += 1;
     BPKV_TRY(mark(l, 1));
     BPKV_TRY(mark(l, 2));

@@ -1,4 +1,6 @@
-// Offline-calibrated channel sets (Fathom page, section 2, "Double Sparsity"):
+// Offline choices for the scanned channels.
+//
+// Calibrated channel sets (Fathom page, section 2, "Double Sparsity"):
 // per unit, channel j's statistic is mean|q_j| over the calibration queries
 // and the unit's query heads times mean|k_j| over the calibration keys, and
 // the n_channels largest (ties to the lower index) are read at one depth.
@@ -7,6 +9,10 @@
 // column in double in storage order (coalesced across the CTA's threads), so
 // the sums, means and product are those of a plain sequential evaluation; the
 // ranks come from a comparison against every other channel's statistic.
+//
+// Bases (Fathom page, contributions: KLT planes; ReadKV page, section 5.1:
+// Hadamard-sign transform): bpkv_rotate takes queries into a cache's basis with
+// the same float32 fused multiply-add chains the decode step uses.
 #include "common.cuh"
 
 namespace bpkv {
@@ -42,7 +48,30 @@ __global__ void __launch_bounds__(kD) k_calibrate(CalArgs a) {
   a.depths[unit * kD + j] = (uint8_t)(rank < a.n_channels ? a.depth : 0);
 }
 
+// y = x R per KV head: grid (rows, H, N), one thread per output channel.
+__global__ void __launch_bounds__(kD) k_rotate(const float* basis, const float* x, float* y, int32_t n_heads,
+                                              int64_t rows) {
+  pdl_enter();
+  const int64_t h = blockIdx.y, row = ((int64_t)blockIdx.z * n_heads + h) * rows + blockIdx.x;
+  const float* R = basis + h * kD * kD;
+  const float* xr = x + row * kD;
+  const int l = threadIdx.x;
+  float acc = 0.f;
+  for (int i = 0; i < kD; ++i) acc = __fmaf_rn(xr[i], R[i * kD + l], acc);
+  y[row * kD + l] = acc;
+}
+
 }  // namespace bpkv
+
+extern "C" int bpkv_rotate(const float* basis, int32_t n_seq, int32_t n_kv_heads, int64_t rows, const float* x,
+                           float* y, void* stream) {
+  using namespace bpkv;
+  if (!basis || !x || !y || n_seq < 1 || n_kv_heads < 1 || rows < 1) return BPKV_EINVAL;
+  if (n_seq > 65535 || n_kv_heads > 65535 || rows > 0x7FFFFFFF) return BPKV_EUNSUPPORTED;
+  const cudaError_t e = launch_pdl(k_rotate, dim3((unsigned)rows, (unsigned)n_kv_heads, (unsigned)n_seq), dim3(kD), 0,
+                                   reinterpret_cast<cudaStream_t>(stream), basis, x, y, n_kv_heads, rows);
+  return e == cudaSuccess ? BPKV_OK : BPKV_ECUDA;
+}
 
 extern "C" int bpkv_calibrate_channels(const float* q_cal, const uint16_t* k_cal, int32_t n_units, int32_t group,
                                        int64_t m_q, int64_t m_k, int32_t n_channels, int32_t depth, uint8_t* depths,

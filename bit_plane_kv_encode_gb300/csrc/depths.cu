@@ -124,6 +124,8 @@ struct FrontArgs {
   int32_t t_new;
   int32_t enc_ctas;         // append CTAs per unit: two (channel halves) per block the new tokens can touch
   int64_t cap;
+  const float* basis;       // optional [H][D][D]: keys coded as k R, depths and plan from q R
+  float* q_rot;             // with a basis: [N][H][G][D] workspace for q R
 };
 
 // Grid (enc_ctas + 1, H, N), kScanThreads threads: x < enc_ctas appends, x ==
@@ -159,7 +161,7 @@ __global__ void __launch_bounds__(kScanThreads) k_front(FrontArgs a) {
     encode_block_cta<4>(kb, a.k_rows + U.row_base(unit), a.v_rows + U.row_base(unit),
                         a.k_new + unit * a.t_new * kD, a.v_new + unit * a.t_new * kD, n_old, t0, cnt,
                         a.planes + U.plane_base(unit), a.scales + U.scale_base(unit), a.cap / kBlock, blk,
-                        (x % 2) * (kD / 2));
+                        (x % 2) * (kD / 2), a.basis ? a.basis + (int64_t)h * kD * kD : nullptr);
     return;
   }
   __shared__ DepthSmem S;
@@ -168,22 +170,40 @@ __global__ void __launch_bounds__(kScanThreads) k_front(FrontArgs a) {
     if (h == 0) a.seq_tick[s] = 0u;
   }
   uint8_t* dep = a.d.depths + unit * kD;
+  // with a basis the depths and the plan come from q R (float32 fused
+  // multiply-add chains in channel order, one per output channel)
+  DepthArgs d = a.d;
+  if (a.basis) {
+    const float* R = a.basis + (int64_t)h * kD * kD;
+    const float* qs = a.d.q + unit * G * kD;
+    float* qr = a.q_rot + unit * G * kD;
+    if (threadIdx.x < kD) {
+      const int l = threadIdx.x;
+      for (int hh = 0; hh < G; ++hh) {
+        float acc = 0.f;
+        for (int i = 0; i < kD; ++i) acc = __fmaf_rn(qs[hh * kD + i], R[i * kD + l], acc);
+        qr[hh * kD + l] = acc;
+      }
+    }
+    __syncthreads();
+    d.q = a.q_rot;
+  }
   if (a.depth_rule == BPKV_DEPTH_WATERFILL) {
-    alloc_depths_cta(S, a.d.q + unit * G * kD, a.d.sigma2 + unit * kD, G, a.d.budget_q[s], dep);
+    alloc_depths_cta(S, d.q + unit * G * kD, a.d.sigma2 + unit * kD, G, a.d.budget_q[s], dep);
   } else if (a.depth_rule == BPKV_DEPTH_GIVEN) {
     // each thread writes the entry it reads back in emit_plan
     if (threadIdx.x < kD) dep[threadIdx.x] = (uint8_t)min((int)a.depths_in[unit * kD + threadIdx.x], 4);
   } else {
-    fixed_depths_cta(S, a.d.q + unit * G * kD, G, a.d.n_channels, a.d.depth, dep);
+    fixed_depths_cta(S, d.q + unit * G * kD, G, a.d.n_channels, a.d.depth, dep);
   }
-  emit_plan<GP>(a.d, unit, dep);
+  emit_plan<GP>(d, unit, dep);
 }
 
 cudaError_t launch_front(const bpkv_cache& c, const uint16_t* k_new, const uint16_t* v_new, int32_t t_new,
                          const float* q, const float* sigma2, const int32_t* budget_q, int32_t depth_rule,
                          int32_t n_channels, int32_t depth, uint8_t* depths, void* plan, uint32_t* hist,
                          uint32_t* hist1, uint32_t* ctr, uint32_t* tickets, uint32_t* seq_tick, cudaStream_t st,
-                         const uint8_t* depths_in) {
+                         const uint8_t* depths_in, float* q_rot) {
   FrontArgs a;
   a.d = DepthArgs{q, sigma2, budget_q, depths, c.n_kv_heads, c.group, tickets, plan, n_channels, depth, hist, ctr};
   a.depth_rule = depth_rule;
@@ -200,6 +220,8 @@ cudaError_t launch_front(const bpkv_cache& c, const uint16_t* k_new, const uint1
   a.t_new = t_new;
   a.enc_ctas = 2 * ((t_new + kBlock - 1) / kBlock + 1);
   a.cap = c.cap_tokens;
+  a.basis = c.basis;
+  a.q_rot = q_rot;
   const dim3 grid((unsigned)(a.enc_ctas + 1), (unsigned)c.n_kv_heads, (unsigned)c.n_seq);
   return launch_depths_gp(c.group, [&](auto gp) {
     return launch_pdl(k_front<decltype(gp)::value>, grid, dim3(kScanThreads), 0, st, a);

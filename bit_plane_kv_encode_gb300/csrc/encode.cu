@@ -22,6 +22,7 @@ struct EncodeArgs {
   int32_t t_new;
   int64_t cap;
   int64_t nb_cap;
+  const float* basis;  // optional [H][D][D]: code the keys k R
 };
 
 constexpr int kEncThreads = 4 * kD;  // four threads per channel, 16 tokens each
@@ -40,7 +41,8 @@ __global__ void __launch_bounds__(kEncThreads) k_encode_append(EncodeArgs a) {
   __shared__ __align__(16) uint16_t kb[kBlock][kD];
   encode_block_cta<4>(kb, a.k_rows + U.row_base(unit), a.v_rows + U.row_base(unit),
                       a.k_new + unit * a.t_new * kD, a.v_new + unit * a.t_new * kD, n_old, t0, cnt,
-                      a.planes + U.plane_base(unit), a.scales + U.scale_base(unit), a.nb_cap, blk);
+                      a.planes + U.plane_base(unit), a.scales + U.scale_base(unit), a.nb_cap, blk, 0,
+                      a.basis ? a.basis + (int64_t)h * kD * kD : nullptr);
 }
 
 __global__ void k_bump_len(int64_t* seq_len, int n_seq, int32_t t_new) {
@@ -67,6 +69,7 @@ cudaError_t launch_encode_append(const bpkv_cache& c, const uint16_t* k_new, con
   a.t_new = t_new;
   a.cap = c.cap_tokens;
   a.nb_cap = c.cap_tokens / kBlock;
+  a.basis = c.basis;
   dim3 grid((t_new + kBlock - 1) / kBlock + 1, c.n_kv_heads, c.n_seq);
   cudaError_t e = launch_pdl(k_encode_append, grid, dim3(kEncThreads), 0, st, a);
   if (e != cudaSuccess) return e;

@@ -333,7 +333,7 @@ cudaError_t launch_fused_gp(const FusedArgs& a, dim3 grid, cudaStream_t st) {
 // the cluster, each CTA's share of the tokens and its scores fit shared
 // memory, and k is small enough for the leaders' merge buffers.
 bool fused_eligible(const bpkv_cache& c, int32_t k, int32_t n_sink, int32_t n_recent, int32_t depth_rule) {
-  if (depth_rule == BPKV_DEPTH_DENSE || depth_rule == BPKV_DEPTH_GIVEN || c.group > kFuseCS) return false;
+  if (depth_rule == BPKV_DEPTH_DENSE || depth_rule == BPKV_DEPTH_GIVEN || c.basis || c.group > kFuseCS) return false;
   const int64_t nb = (c.n_max + 1 + kBlock - 1) / kBlock;
   const int64_t bpc = (nb + kFuseCS - 1) / kFuseCS;
   if (bpc < 1 || bpc > kFuseMaxBlocks) return false;

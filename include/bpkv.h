@@ -76,6 +76,16 @@ extern "C" {
  * place over the host link.  seq_len is always device memory.
  * n_max is host state: an upper bound of every seq_len[i], used to size
  * launches; bpkv_encode_append raises it.
+ * basis (optional, NULL: the raw channels) float [H][D][D] in device memory: an
+ * orthogonal basis per KV head for the coded keys (Fathom page, contributions:
+ * the keys' KLT planes for models without QK norm; ReadKV page, section 5.1:
+ * a Hadamard-sign transform).  The planes and scales then code the keys k R
+ * (channel l = sum_j k_j R[j][l], one float32 fused multiply-add chain in order
+ * j = 0 .. D-1, rounded to bf16); bpkv_decode_step allocates depths and scores
+ * with q R (sigma2 is then the variance in the basis), and the rows and the
+ * exact attention stay in the original channels.  The stand-alone depth, scan
+ * and top-k calls take q already in the basis (bpkv_rotate).  Set the basis
+ * before the first append; the fused and tail step paths do not support it.
  */
 typedef struct bpkv_cache {
   int32_t n_seq;
@@ -91,6 +101,7 @@ typedef struct bpkv_cache {
   uint16_t *k_rows;
   uint16_t *v_rows;
   int64_t *seq_len;
+  const float *basis;
 } bpkv_cache;
 
 /* ------------------------------------------------------------- workspace */
@@ -175,6 +186,15 @@ int bpkv_fixed_depths(const bpkv_cache *c, const float *q, int32_t n_channels, i
  */
 int bpkv_calibrate_channels(const float *q_cal, const uint16_t *k_cal, int32_t n_units, int32_t group, int64_t m_q,
                             int64_t m_k, int32_t n_channels, int32_t depth, uint8_t *depths, void *stream);
+
+/*
+ * y = x R per KV head: x, y float [n_seq][H][rows][D] (device), basis R float
+ * [H][D][D]; channel l of a row is one float32 fused multiply-add chain
+ * sum_j x_j R[j][l] in order j = 0 .. D-1 (the same arithmetic as the decode
+ * step's q R).  x and y may not overlap.
+ */
+int bpkv_rotate(const float *basis, int32_t n_seq, int32_t n_kv_heads, int64_t rows, const float *x, float *y,
+                void *stream);
 
 /* ------------------------------------------------------------- scan (F3, F7) */
 /*

@@ -21,12 +21,15 @@ def bits64(t: torch.Tensor) -> np.ndarray:
 
 
 def build_cache(k: torch.Tensor, v: torch.Tensor, group: int, cap: int | None = None, n_prefill: int | None = None,
-                residency: str = "hbm", chunks=None):
-    """Cache holding the first n_prefill (default all) rows of k/v [N][H][n][D]."""
+                residency: str = "hbm", chunks=None, basis=None):
+    """Cache holding the first n_prefill (default all) rows of k/v [N][H][n][D]
+    (keys coded in `basis`, float [H][D][D] on the device, when given)."""
     from bit_plane_kv_encode_gb300 import Cache
     N, H, n, _ = k.shape
     cap = cap if cap is not None else ((n + 511) // 512) * 512
     c = Cache(N, H, group, cap, device=k.device, residency=residency)
+    if basis is not None:
+        c.set_basis(basis)
     n_pre = n if n_prefill is None else n_prefill
     pos = 0
     for t in (chunks or [n_pre]):
@@ -78,7 +81,7 @@ def check_topk_sets(gpu_idx: np.ndarray, ref_idx: np.ndarray, ref_score: np.ndar
 
 
 def decode_one_layer(inp, cfg, depth_rule=0, fixed=(0, 0), budgets=None, residency="hbm", dev="cuda", flags=0,
-                     lists=True, depths_in=None):
+                     lists=True, depths_in=None, basis=None):
     """Prefill n-1 tokens of a generated layer, then one bpkv_decode_step (appends
     token n-1 and runs the whole path).  Returns (cache, depths, idx, out) with
     depths [N][H][D], idx [N][H][G][k], out [N][H][G][D] on the device; with
@@ -87,7 +90,7 @@ def decode_one_layer(inp, cfg, depth_rule=0, fixed=(0, 0), budgets=None, residen
     N, H, n, D = inp.k.shape
     G = cfg.group
     k_all, v_all = inp.k.to(dev), inp.v.to(dev)
-    cache = build_cache(k_all, v_all, G, cap=cfg.cap_tokens, n_prefill=n - 1, residency=residency)
+    cache = build_cache(k_all, v_all, G, cap=cfg.cap_tokens, n_prefill=n - 1, residency=residency, basis=basis)
     ws = cache.workspace(cfg.k, pk.WS_STEP)
     out = torch.zeros((1, N, H, G, D), dtype=torch.float32, device=dev)
     depths = torch.zeros((1, N, H, D), dtype=torch.uint8, device=dev)
@@ -112,7 +115,7 @@ def decode_one_layer(inp, cfg, depth_rule=0, fixed=(0, 0), budgets=None, residen
 
 
 def check_unit(orc, cfg, inp, cache, depths, idx, out, s, h, depth_rule=0, fixed=(0, 0), budget_bits=None,
-               what="", depth=None):
+               what="", depth=None, basis=None):
     """Oracle decode of unit (s, h) vs the GPU results; returns the number of
     heads whose sets matched exactly (their outputs are checked too)."""
     n = inp.k.shape[2]
@@ -120,7 +123,7 @@ def check_unit(orc, cfg, inp, cache, depths, idx, out, s, h, depth_rule=0, fixed
     b = int(inp.budgets[s]) if budget_bits is None else budget_bits
     ref = orc.decode_unit(kb, vb, inp.q[s, h].numpy(), inp.sigma2[s, h].numpy(), b, cfg.k, cfg.n_sink,
                           cfg.n_recent, nb_cap=cache.c.cap_tokens // 64,
-                          fixed=fixed if depth_rule == 1 else None, depth=depth)
+                          fixed=fixed if depth_rule == 1 else None, depth=depth, basis=basis)
     nb = (n + 63) // 64
     assert np.array_equal(bits64(cache.planes[s, h])[:, :, :nb], ref["planes"][:, :, :nb]), f"{what} planes"
     assert np.array_equal(bits16(cache.scales[s, h])[:, :nb], ref["scales"][:, :nb]), f"{what} scales"
