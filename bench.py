@@ -156,12 +156,14 @@ def make_workload(cfg, steps: int, warmup: int, dev, step_flags: int = 0, budget
     L, N, H, G, D, n = cfg.n_layers, cfg.n_seq, cfg.n_kv_heads, cfg.group, cfg.head_dim, cfg.n_tokens
     budgets = list(budgets or cfg.budgets)
     host = cfg.residency == "host"
-    # one cache per (budget, layer) unless they would not fit in device memory;
-    # then every budget's pass decodes into the same caches (each pass appends
-    # its own token), which only happens for multi-layer configs whose planes do
-    # not survive in L2 from one pass to the next
-    share = (not host and len(budgets) > 1 and
-             len(budgets) * L * cache_bytes(cfg, n) > 0.45 * torch.cuda.get_device_properties(dev).total_memory)
+    # one cache per (budget, layer) unless they would not fit in device memory
+    # (or, for host-resident caches, unless there are several budgets: pinned
+    # host memory is the scarcer resource); then every budget's pass decodes
+    # into the same caches (each pass appends its own token), which only
+    # happens for multi-layer configs whose planes do not survive in L2 from
+    # one pass to the next
+    share = len(budgets) > 1 and (host or len(budgets) * L * cache_bytes(cfg, n) >
+                                  0.45 * torch.cuda.get_device_properties(dev).total_memory)
     # room for every step the bench runs: warm-up, timed, breakdown, list and e2e
     # steps of every pass that appends to a cache, then the baseline arms
     per_pass = warmup + steps + min(steps, 20) + 1 + 2 + max(3, min(steps, 50))
@@ -395,7 +397,7 @@ def bench_ours(args, cfg, rank, world, local):
         hbm, peak_src, bound = link, "of measured (pinned host-to-device copy, 1 GiB)", "host_link"
     achieved = kbytes / (kms / 1e3) / 1e9
     traffic = load_traffic(dom, cfg.name, [p["budget"] for p in passes])
-    kernel_name = {"scan": "k_scan", "topk": "k_cut", "attend": "k_attend_ranges"}.get(dom, dom)
+    kernel_name = {"scan": "k_scan_pipe", "topk": "k_cut", "attend": "k_attend_ranges"}.get(dom, dom)
     roofline = {"bound": bound, "kernel": kernel_name, "achieved": round(achieved, 1), "peak": round(hbm, 1),
                 "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_source": peak_src,
                 "traffic": traffic, "algorithmic_bytes_per_launch": round(kbytes / n_launch),

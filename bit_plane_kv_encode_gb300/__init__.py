@@ -40,7 +40,15 @@ class Cache:
 
         def buf(shape, dtype):
             if host:
-                return torch.empty(shape, dtype=dtype, pin_memory=True)
+                # pinned host memory from a 256-byte boundary: the kernels' reads
+                # of it are not cached, so a row segment that starts inside a
+                # 32-byte sector moves one more sector over the link
+                n = dtype.itemsize
+                for e in shape:
+                    n *= e
+                raw = torch.empty(n + 256, dtype=torch.uint8, pin_memory=True)
+                off = (-raw.data_ptr()) % 256
+                return raw[off:off + n].view(dtype).view(shape)
             return torch.empty(shape, dtype=dtype, device=self.device)
 
         self.planes = buf((n_seq, n_kv_heads, D, 4, nb), torch.int64)

@@ -6,23 +6,24 @@
 //   score_g = sum_j u_gj e_j   with u_gj = s_j (q_gj 2^(4-t_j))  (one rounding),
 // e an exact half-integer, accumulated in float32 with fused multiply-adds.
 //
-// Work layout.  A CTA per (run of chunks of 8 blocks = 512 tokens, KV head,
-// sequence), the run as long as needed for the grid to fit in one wave of
-// resident CTAs; the unit's plan is loaded once per CTA.  The active channels are packed into "groups" of 32 plane rows,
+// Work layout.  Chunks are runs of 8 blocks (512 tokens) of one unit
+// (sequence, KV head).  One wave of resident CTAs splits all units' chunks,
+// laid end to end, into equal shares; a CTA loads the plan of each unit it
+// meets.  The active channels are packed into "groups" of 32 plane rows,
 // one depth per group (8 channels of depth 4, 10 of depth 3, 16 of depth 2,
 // 32 of depth 1), the planes of a channel placed so that, after a 32 x 32 bit
 // transpose, each token's code of each channel is a contiguous bit field with
-// its most significant bit highest.  The chunk's plane words are staged in
-// shared memory with coalesced loads; each warp takes one 64-token block, each
-// lane two tokens (i and i + 32).  Per group a lane reads one 32-bit word per
-// token half, the warp transposes them with five shuffle / funnel-shift /
-// select rounds, and every field becomes a float by OR-ing it under the
-// exponent of 2^23 and subtracting a constant (exact).  The products with u
-// (staged per block and channel) use packed fp32x2 FMAs over field pairs.
+// its most significant bit highest.  The plane words and block scales of each
+// step are staged in shared memory by asynchronous copies, double-buffered;
+// each warp takes one 64-token block, each lane two tokens (i and i + 32).
+// Per group a lane reads one 32-bit word per token half, the warp transposes
+// them with five shuffle / funnel-shift / select rounds, and every field
+// becomes a float by OR-ing it under the exponent of 2^23 and subtracting a
+// constant (exact).  The products with u = s w (formed per block and slot)
+// use packed fp32x2 FMAs over head pairs.
 #include "scan_core.cuh"
 
 #include <mutex>
-#include <type_traits>
 
 namespace bpkv {
 
@@ -40,60 +41,21 @@ struct ScanArgs {
   int32_t group;
   uint32_t* hist;  // optional [N][H][G][kTopkBins] level-0 selection histogram (zeroed by the caller)
   int32_t n_sink, n_recent;
-  int64_t chunks_per_cta;
   int32_t pending;  // tokens appended in this step but not yet in seq_len
   int32_t* status;  // optional device status word (unused by the scan kernels today)
   int64_t chunks;   // chunks per unit (from the host bound on the sequence lengths)
   int64_t units;    // sequences x KV heads
+  int32_t wide;     // whether the pipelined scan may take wide steps (host-resident caches)
 };
-
-template <int GP>
-__global__ void __launch_bounds__(kScanThreads, GP >= 8 ? 2 : 4) k_scan(ScanArgs a) {
-  pdl_enter();
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  ScanSmem<GP>& S = *reinterpret_cast<ScanSmem<GP>*>(smem_raw);
-  const int s = blockIdx.z, h = blockIdx.y;
-  const int64_t unit = (int64_t)s * a.n_heads + h;
-  const int64_t n = a.seq_len[s] + a.pending;
-  const int64_t c_begin = (int64_t)blockIdx.x * a.chunks_per_cta;
-  if (c_begin * kScanBlocks * kBlock >= n) return;
-  const int64_t nb_valid = (n + kBlock - 1) / kBlock;
-  const int64_t c_end = min64(c_begin + a.chunks_per_cta, (nb_valid + kScanBlocks - 1) / kScanBlocks);
-  const int tid = threadIdx.x;
-  const int G = a.group;
-  if (a.plan) {
-    scan_load_plan<GP>(S.P, reinterpret_cast<const ScanPlan<GP>*>(a.plan) + unit);
-  } else {
-    int t = 0;
-    float qv[GP];
-    if (tid < kD) {
-      t = min((int)a.depths[unit * kD + tid], 4);  // depth values above 4 read as 4
-      const float* qp = a.q + unit * G * kD;
-#pragma unroll
-      for (int hh = 0; hh < GP; ++hh) qv[hh] = hh < G ? qp[hh * kD + tid] : 0.f;
-    }
-    scan_setup<GP>(S.P, S.X, t, qv);
-  }
-  const int64_t lo = min64(a.n_sink, n), hi = max64(n - a.n_recent, lo);
-  for (int64_t ch = c_begin; ch < c_end; ++ch) {
-    const int64_t b0 = ch * kScanBlocks;
-    const int nbl = (int)min64(kScanBlocks, nb_valid - b0);
-    float v0[GP], v1[GP];
-    const bool act = scan_chunk<GP>(S, a.planes + unit * kD * kPlanes * a.nb_cap + b0,
-                                    a.scales + unit * kD * a.nb_cap + b0, a.nb_cap, nbl, G,
-                                    a.scores + unit * G * a.ld + b0 * kBlock, a.ld, n - b0 * kBlock, v0, v1);
-    if (a.hist && act)
-      warp_hist<GP>(G, b0 * kBlock + (threadIdx.x >> 5) * kBlock + (threadIdx.x & 31), lo, hi, v0, v1,
-                    a.hist + unit * G * kTopkBins);
-  }
-}
 
 // Device-resident caches.  The grid is one wave of CTAs over the units'
 // chunks laid end to end (unit-major); each CTA takes an equal share of that
-// sequence and scores it unit by unit.  Within a unit the steps (chunk, pass)
-// go through two stage buffers: once step i has landed and every warp is past
+// sequence and scores it unit by unit.  Within a unit the steps (one pass
+// over one chunk, or over kWideSub chunks when the unit's plan allows) go
+// through two stage buffers: once step i has landed and every warp is past
 // step i - 1, all threads start the copies of step i + 1 into the other
-// buffer, then each warp forms u = s w for its block and scores step i.
+// buffer, then each warp forms u = s w for its block of each chunk of the step
+// and scores it.
 template <int GP>
 __device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& S, int64_t unit, int64_t c_begin,
                                                int64_t c_want) {
@@ -124,7 +86,14 @@ __device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& 
   uint32_t* hist = a.hist ? a.hist + unit * G * kTopkBins : nullptr;
   const int64_t lo = min64(a.n_sink, n), hi = max64(n - a.n_recent, lo);
   const int n_passes = S.P.n_passes;
-  const int64_t steps = (c_end - c_begin) * n_passes;
+  // chunks per step: kWideSub when allowed and the plan is one pass that fits
+  // a wide step; wide steps start at even chunks (the first one may hold one
+  // chunk).  Device memory gains nothing from them (the L2 serves the second
+  // half of a scale sector) and they cost registers.
+  const int sub = (a.wide && n_passes == 1 && S.P.n_groups <= kWideGroups) ? kWideSub : 1;
+  auto span = [&](int64_t c) -> int {
+    return sub == 1 ? 1 : (int)min64((c & 1) ? 1 : kWideSub, c_end - c);
+  };
   constexpr bool kSmemHist = pipe_counts_hist<GP>();
   if constexpr (kSmemHist) {
     if (hist) {
@@ -185,34 +154,38 @@ __device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& 
       }
     }
   };
-  if (steps == 0) {
+  if (n_passes == 0) {
     for (int64_t ch = c_begin; ch < c_end; ++ch) finish_chunk(ch);
     flush_hist();
     return;
   }
-  scan_issue<GP>(S, 0, pl, sp, a.nb_cap, c_begin * kScanBlocks, S.P.pass_g[0], S.P.pass_g[1]);
-  int64_t ch = c_begin;  // chunk and pass of step i
-  int ps = 0;
-  for (int64_t i = 0; i < steps; ++i) {
+  // step i: chunks [ch, ch + n_sub), pass ps, in stage buffer i & 1
+  int64_t ch = c_begin;
+  int ps = 0, n_sub = span(c_begin);
+  scan_issue<GP>(S, 0, pl, sp, a.nb_cap, ch * kScanBlocks, S.P.pass_g[0], S.P.pass_g[1], sub, n_sub);
+  for (int64_t i = 0;; ++i) {
     const int b = (int)(i & 1);
     cp_async_wait_all();
     __syncthreads();  // step i visible to all; every warp is done with step i - 1 (the other buffer)
-    if (i + 1 < steps) {
-      const int ps1 = ps + 1 == n_passes ? 0 : ps + 1;
-      const int64_t ch1 = ps1 == 0 ? ch + 1 : ch;
-      scan_issue<GP>(S, b ^ 1, pl, sp, a.nb_cap, ch1 * kScanBlocks, S.P.pass_g[ps1], S.P.pass_g[ps1 + 1]);
-    }
+    const int ps1 = ps + 1 == n_passes ? 0 : ps + 1;
+    const int64_t ch1 = ps1 == 0 ? ch + n_sub : ch;
+    const int n_sub1 = ch1 < c_end ? span(ch1) : 0;
+    if (n_sub1 > 0)
+      scan_issue<GP>(S, b ^ 1, pl, sp, a.nb_cap, ch1 * kScanBlocks, S.P.pass_g[ps1], S.P.pass_g[ps1 + 1], sub, n_sub1);
     const int g0 = S.P.pass_g[ps], g1 = S.P.pass_g[ps + 1];
     const int s0 = S.P.grp_base[g0], s1 = g1 < S.P.n_groups ? (int)S.P.grp_base[g1] : S.P.n_slots;
-    scan_form_u<GP>(S, b, s0, s1, lb);
-    __syncwarp();
-    const int nbl = (int)min64(kScanBlocks, nb_valid - ch * kScanBlocks);
-    if (lb < nbl) scan_compute_pipe<GP>(S, b, g0, g1, s0, lb, keep, rot, A);
-    if (++ps == n_passes) {
-      finish_chunk(ch);
-      ps = 0;
-      ++ch;
+    for (int c = 0; c < n_sub; ++c) {
+      if (c > 0) __syncwarp();  // every lane is done reading the previous chunk's u
+      scan_form_u<GP>(S, b, s0, s1, lb, sub, c);
+      __syncwarp();
+      const int nbl = (int)min64(kScanBlocks, nb_valid - (ch + c) * kScanBlocks);
+      if (lb < nbl) scan_compute_pipe<GP>(S, b, g0, g1, s0, lb, sub, c, keep, rot, A);
+      if (ps + 1 == n_passes) finish_chunk(ch + c);
     }
+    if (n_sub1 == 0) break;
+    ch = ch1;
+    ps = ps1;
+    n_sub = n_sub1;
   }
   flush_hist();
 }
@@ -233,14 +206,10 @@ __global__ void __launch_bounds__(kScanThreads, 2) k_scan_pipe(ScanArgs a) {
   }
 }
 
-template <int GP, bool Pipe>
+template <int GP>
 cudaError_t launch_scan_gp(ScanArgs a, int64_t chunks, int64_t units, cudaStream_t st) {
-  int smem = 0;
-  if constexpr (Pipe) smem = (int)sizeof(PipeSmem<GP>);
-  else smem = (int)sizeof(ScanSmem<GP>);
-  void (*kernel)(ScanArgs) = nullptr;
-  if constexpr (Pipe) kernel = k_scan_pipe<GP>;
-  else kernel = k_scan<GP>;
+  const int smem = (int)sizeof(PipeSmem<GP>);
+  void (*kernel)(ScanArgs) = k_scan_pipe<GP>;
   // resident CTAs per device, looked up once per device
   constexpr int kDevs = 64;
   static int slots[kDevs] = {};
@@ -264,41 +233,28 @@ cudaError_t launch_scan_gp(ScanArgs a, int64_t chunks, int64_t units, cudaStream
     }
     occ_slots = slots[dev];
   }
-  const int64_t total = chunks * units;
   a.chunks = chunks;
   a.units = units;
-  if constexpr (Pipe) {
-    // one wave; each CTA an equal share of the work (see k_scan_pipe)
-    const unsigned ctas = (unsigned)min64(total, (int64_t)occ_slots);
-    return launch_pdl(kernel, dim3(ctas), dim3(kScanThreads), (size_t)smem, st, a);
-  }
-  // enough chunks per CTA for the grid to fit in one wave of resident CTAs
-  a.chunks_per_cta = (total + occ_slots - 1) / occ_slots;
-  if (a.chunks_per_cta < 1) a.chunks_per_cta = 1;
-  const dim3 grid((unsigned)((chunks + a.chunks_per_cta - 1) / a.chunks_per_cta), (unsigned)a.n_heads,
-                  (unsigned)(units / a.n_heads));
-  return launch_pdl(kernel, grid, dim3(kScanThreads), (size_t)smem, st, a);
+  // one wave; each CTA an equal share of the work (see k_scan_pipe)
+  const unsigned ctas = (unsigned)min64(chunks * units, (int64_t)occ_slots);
+  return launch_pdl(kernel, dim3(ctas), dim3(kScanThreads), (size_t)smem, st, a);
 }
 
-// Device-resident caches take the pipelined kernel (asynchronous copies into
-// shared memory); pinned host caches the direct one (plain loads over the link).
+// Device-resident and pinned host caches alike: asynchronous copies into
+// shared memory; host caches take wide steps.
 cudaError_t launch_scan(const bpkv_cache& c, const float* q, const uint8_t* depths, float* scores, int64_t ld,
                         cudaStream_t st, const void* plan, uint32_t* hist, int32_t n_sink, int32_t n_recent,
                         int32_t pending, int32_t* status) {
-  ScanArgs a{plan,         c.planes, c.scales, c.seq_len, q,        depths, scores,  ld,    c.cap_tokens / kBlock,
-             c.n_kv_heads, c.group,  hist,     n_sink,    n_recent, 1,      pending, status, 0, 0};
+  ScanArgs a{plan,         c.planes, c.scales, c.seq_len, q,        depths,  scores, ld, c.cap_tokens / kBlock,
+             c.n_kv_heads, c.group,  hist,     n_sink,    n_recent, pending, status, 0,  0,
+             c.residency == 1};
   const int64_t chunks = (c.n_max + kScanBlocks * kBlock - 1) / (kScanBlocks * kBlock);
   if (chunks == 0) return cudaSuccess;
   const int64_t units = (int64_t)c.n_seq * c.n_kv_heads;
-  const bool pipe = c.residency == 0;
-  auto go = [&](auto gp) {
-    constexpr int GP = decltype(gp)::value;
-    return pipe ? launch_scan_gp<GP, true>(a, chunks, units, st) : launch_scan_gp<GP, false>(a, chunks, units, st);
-  };
-  if (c.group <= 1) return go(std::integral_constant<int, 1>{});
-  if (c.group <= 2) return go(std::integral_constant<int, 2>{});
-  if (c.group <= 4) return go(std::integral_constant<int, 4>{});
-  return go(std::integral_constant<int, 8>{});
+  if (c.group <= 1) return launch_scan_gp<1>(a, chunks, units, st);
+  if (c.group <= 2) return launch_scan_gp<2>(a, chunks, units, st);
+  if (c.group <= 4) return launch_scan_gp<4>(a, chunks, units, st);
+  return launch_scan_gp<8>(a, chunks, units, st);
 }
 
 }  // namespace bpkv

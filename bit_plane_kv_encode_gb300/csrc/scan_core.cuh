@@ -391,17 +391,54 @@ __device__ bool scan_chunk(ScanSmem<GP>& S, const uint64_t* __restrict__ pl, con
 }
 
 // ---------------------------------------------------------------------------
-// Pipelined form (device-resident caches): the plane words and raw block
-// scales of one (chunk, pass) step are fetched by asynchronous 16-byte copies
-// into one of two stage buffers while the warps score the other.
+// Pipelined form: the plane words and raw block scales of one step are
+// fetched by asynchronous 16-byte copies into one of two stage buffers while
+// the warps score the other.  A step is one pass over one chunk, or, for a
+// unit whose plan is a single pass of at most kWideGroups groups, one pass
+// over kWideSub consecutive chunks starting at an even chunk: each slot's
+// block scales then come as one whole 32-byte sector instead of two halves
+// fetched in different steps (device memory serves the second half from L2;
+// reads of pinned host memory by these copies are not kept in L2, so there
+// every half sector crosses the link in full).
+//
+// Staged plane rows have no padding: a row of a step of `sub` chunks is 2 sub
+// 32-byte pieces (4 blocks each); piece k of row r sits at piece slot
+// k ^ swz_piece(r) of the row, with its two 16-byte halves swapped when
+// swz_half(r) is 1.  Every 32-byte sector read from memory so lands in one
+// aligned 32-byte slot (a copy whose sector halves land in different slots is
+// split and fetches the sector twice, which over the host link costs the
+// bytes in full), and the 8-byte reads of one block column by rows r .. r + 7
+// fall in eight different 16-byte bank groups.
 
-constexpr int kRowPitch = 20;                 // u32 words per staged plane row: 64 B + 16 B (16-byte aligned rows)
 constexpr int kStageRows = kPassGroups * 32;
+constexpr int kStageWords = kStageRows * 2 * kScanBlocks;  // one-chunk steps: 16 words per row
+constexpr int kWideSub = 2;                                 // chunks per step of a wide unit
+constexpr int kWideGroups = kStageWords / (32 * 2 * kScanBlocks * kWideSub);
+constexpr int kStageU32 = kStageWords + kPassSlots * kScanBlocks * kWideSub / 2;
+static_assert(kWideGroups >= 5, "a wide step must hold the single-pass plans of usual budgets");
 
+// u32 words per staged plane row for steps of `sub` chunks.
+__host__ __device__ constexpr int row_pitch(int sub) { return 2 * kScanBlocks * sub; }
+// Placement of the pieces of staged row r (see above).
+__device__ __forceinline__ int swz_piece(int r, int sub) { return sub == 1 ? (r >> 1) & 1 : r & 3; }
+__device__ __forceinline__ int swz_half(int r) { return (r >> 2) & 1; }
+// u32 word of 16-byte part q (0 .. 4 sub - 1) of staged row r
+__device__ __forceinline__ int staged_word(int r, int q, int sub) {
+  return r * row_pitch(sub) + 8 * ((q >> 1) ^ swz_piece(r, sub)) + 4 * ((q & 1) ^ swz_half(r));
+}
+
+// One stage buffer: the plane words (row (g - g0) * 32 + lane at
+// u32[row * row_pitch(sub)]), then from word kStageWords the raw block
+// scales, [slot - s0][sub chunks x 8 blocks].
 struct __align__(16) ScanStage {
-  uint32_t words[kStageRows * kRowPitch];     // the chunk's 8 words of each row of the pass: row (g - g0) * 32 + lane
-  uint16_t sc[kPassSlots * kScanBlocks];      // raw block scales of the pass's slots, [slot - s0][block]
+  uint32_t u32[kStageU32];
 };
+__device__ __forceinline__ uint16_t* stage_sc(ScanStage& st) {
+  return reinterpret_cast<uint16_t*>(st.u32 + kStageWords);
+}
+__device__ __forceinline__ const uint16_t* stage_sc(const ScanStage& st) {
+  return reinterpret_cast<const uint16_t*>(st.u32 + kStageWords);
+}
 
 template <int GP>
 struct __align__(16) PipeSmem {
@@ -542,31 +579,31 @@ __device__ __forceinline__ void acc_zero(Acc<GP>& A) {
     for (int i = 0; i < Acc<GP>::HP; ++i) A.t0[p][i] = A.t1[p][i] = 0ull;
 }
 
-// All threads: start the copies of step (chunk at block b0, groups [g0, g1))
-// into stage buffer b: per used plane row its chunk's 8 words (four 16-byte
-// pieces), per used slot its chunk's 8 block scales (one piece); then commit
-// them as this thread's newest group.  pl / sp are the unit's planes and
-// scales; b0 + 8 <= nb_cap.
+// All threads: start the copies of step (n_sub chunks from block b0, groups
+// [g0, g1)) into stage buffer b, laid out for steps of `sub` chunks: per used
+// plane row its n_sub x 8 words (16-byte pieces, consecutive pieces of a row
+// taken by consecutive threads so that each warp instruction copies whole row
+// segments), per used slot its n_sub x 8 block scales (one piece per chunk);
+// then commit them as this thread's newest group.  pl / sp are the unit's
+// planes and scales; b0 + 8 n_sub <= nb_cap.
 template <int GP>
 __device__ __forceinline__ void scan_issue(PipeSmem<GP>& S, int b, const uint64_t* pl, const uint16_t* sp,
-                                           int64_t nb_cap, int64_t b0, int g0, int g1) {
+                                           int64_t nb_cap, int64_t b0, int g0, int g1, int sub, int n_sub) {
   const ScanPlan<GP>& P = S.P;
-  const int n_row = (g1 - g0) * 32;
+  const int per_row = 4 * n_sub, sc_pitch = kScanBlocks * sub;
+  const int n_piece = (g1 - g0) * 32 * per_row;
   const int s0 = P.grp_base[g0], s1 = g1 < P.n_groups ? (int)P.grp_base[g1] : P.n_slots;
-  const int n_all = n_row + (s1 - s0);
+  const int n_all = n_piece + (s1 - s0) * n_sub;
   for (int e = threadIdx.x; e < n_all; e += kScanThreads) {
-    if (e < n_row) {
-      const int row = P.row_of_lane[g0 * 32 + e];
-      if (row >= 0) {
-        const uint64_t* src = pl + (int64_t)row * nb_cap + b0;
-        uint32_t* dst = &S.st[b].words[e * kRowPitch];
-#pragma unroll
-        for (int piece = 0; piece < 4; ++piece) cp_async16(dst + 4 * piece, src + 2 * piece);
-      }
+    if (e < n_piece) {
+      const int r = e / per_row, piece = e - r * per_row;
+      const int row = P.row_of_lane[g0 * 32 + r];
+      if (row >= 0)
+        cp_async16(&S.st[b].u32[staged_word(r, piece, sub)], pl + (int64_t)row * nb_cap + b0 + 2 * piece);
     } else {
-      const int sl = s0 + e - n_row;
-      const int ch = P.slot_ch[sl];
-      if (ch >= 0) cp_async16(&S.st[b].sc[(sl - s0) * kScanBlocks], sp + (int64_t)ch * nb_cap + b0);
+      const int f = e - n_piece, rel = f / n_sub, c = f - rel * n_sub;
+      const int ch = P.slot_ch[s0 + rel];
+      if (ch >= 0) cp_async16(stage_sc(S.st[b]) + rel * sc_pitch + kScanBlocks * c, sp + (int64_t)ch * nb_cap + b0 + kScanBlocks * c);
     }
   }
   cp_async_commit();
@@ -577,16 +614,18 @@ __device__ __forceinline__ void scan_issue(PipeSmem<GP>& S, int b, const uint64_
 // of a block past the end of a unit's cache, which is not a number).
 __device__ __forceinline__ float sw(float s, float w) { return w != 0.f ? s * w : 0.f; }
 
-// This warp's u = s w for the slots [s0, s1) of a landed stage (block lb):
-// one slot per lane at a time, all heads with vector loads and stores.
+// This warp's u = s w for the slots [s0, s1) of a landed stage (block lb of
+// chunk c of a step of `sub` chunks): one slot per lane at a time, all heads
+// with vector loads and stores.
 template <int GP>
-__device__ __forceinline__ void scan_form_u(PipeSmem<GP>& S, int b, int s0, int s1, int lb) {
+__device__ __forceinline__ void scan_form_u(PipeSmem<GP>& S, int b, int s0, int s1, int lb, int sub, int c) {
   const int lane = threadIdx.x & 31;
-  const uint16_t* sc = S.st[b].sc + lb;
+  const int sc_pitch = kScanBlocks * sub;
+  const uint16_t* sc = stage_sc(S.st[b]) + kScanBlocks * c + lb;
   const float* w = S.P.w + s0 * GP;
   float* ud = S.u[lb];
   for (int rel = lane; rel < s1 - s0; rel += 32) {
-    const float sv = fp16_bits_to_float(sc[rel * kScanBlocks]);
+    const float sv = fp16_bits_to_float(sc[rel * sc_pitch]);
     if constexpr (GP == 1) {
       ud[rel] = sw(sv, w[rel]);
     } else if constexpr (GP == 2) {
@@ -604,15 +643,21 @@ __device__ __forceinline__ void scan_form_u(PipeSmem<GP>& S, int b, int s0, int 
 }
 
 // Add groups [g0, g1) of a landed stage to this lane's accumulators (warp lb:
-// block lb of the chunk, tokens lane and lane + 32).  u must be formed.
+// block lb of chunk c of a step of `sub` chunks, tokens lane and lane + 32).
+// u must be formed.
 template <int GP>
 __device__ __forceinline__ void scan_compute_pipe(const PipeSmem<GP>& S, int b, int g0, int g1, int s0, int lb,
-                                                  const uint32_t (&keep)[5], const uint32_t (&rot)[5], Acc<GP>& A) {
+                                                  int sub, int c, const uint32_t (&keep)[5], const uint32_t (&rot)[5],
+                                                  Acc<GP>& A) {
   const int lane = threadIdx.x & 31;
   const ScanPlan<GP>& P = S.P;
+  // block lb of chunk c is word 2 (lb % 2) of 16-byte part 4 c + lb / 2 of
+  // row (g - g0) * 32 + lane (placed as row lane: 32 is a multiple of 8)
+  const uint32_t* wl = S.st[b].u32 + staged_word(lane, 4 * c + (lb >> 1), sub) + 2 * (lb & 1);
+  const int g_stride = 32 * row_pitch(sub);
   for (int g = g0; g < g1; ++g) {
     const int d = P.grp_t[g], cnt = P.grp_cnt[g];
-    const uint2 wv = *reinterpret_cast<const uint2*>(&S.st[b].words[((g - g0) * 32 + lane) * kRowPitch + 2 * lb]);
+    const uint2 wv = *reinterpret_cast<const uint2*>(wl + (g - g0) * g_stride);
     const uint32_t x0 = warp_transpose32(wv.x, keep, rot);
     const uint32_t x1 = warp_transpose32(wv.y, keep, rot);
     // the exponent of 2^23 over bits 23..30 of both shifted forms
