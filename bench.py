@@ -168,7 +168,7 @@ def make_workload(cfg, steps: int, warmup: int, dev, step_flags: int = 0, budget
     # steps of every pass that appends to a cache, then the baseline arms
     per_pass = warmup + steps + min(steps, 20) + 1 + 2 + max(3, min(steps, 50))
     cap = n + (len(budgets) if share else 1) * per_pass + len(BASELINE_ARMS) * (3 + baseline_steps(steps)) + 64
-    cap = (cap + 511) // 512 * 512
+    cap = (cap + 1023) // 1024 * 1024  # scale rows on 32-byte boundaries (see include/bpkv.h)
     caches = {b: [] for b in budgets}
     q, s2, kn, vn = [], [], [], []
     inp0 = None

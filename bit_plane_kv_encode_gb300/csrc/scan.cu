@@ -24,6 +24,7 @@
 #include "scan_core.cuh"
 
 #include <mutex>
+#include <type_traits>
 
 namespace bpkv {
 
@@ -45,7 +46,6 @@ struct ScanArgs {
   int32_t* status;  // optional device status word (unused by the scan kernels today)
   int64_t chunks;   // chunks per unit (from the host bound on the sequence lengths)
   int64_t units;    // sequences x KV heads
-  int32_t wide;     // whether the pipelined scan may take wide steps (host-resident caches)
 };
 
 // Device-resident caches.  The grid is one wave of CTAs over the units'
@@ -55,8 +55,9 @@ struct ScanArgs {
 // through two stage buffers: once step i has landed and every warp is past
 // step i - 1, all threads start the copies of step i + 1 into the other
 // buffer, then each warp forms u = s w for its block of each chunk of the step
-// and scores it.
-template <int GP>
+// and scores it.  kHost: the caches are in pinned host memory (wide steps
+// allowed, sector-coalesced copies).
+template <int GP, bool kHost>
 __device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& S, int64_t unit, int64_t c_begin,
                                                int64_t c_want) {
   const int s = (int)(unit / a.n_heads);
@@ -86,11 +87,11 @@ __device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& 
   uint32_t* hist = a.hist ? a.hist + unit * G * kTopkBins : nullptr;
   const int64_t lo = min64(a.n_sink, n), hi = max64(n - a.n_recent, lo);
   const int n_passes = S.P.n_passes;
-  // chunks per step: kWideSub when allowed and the plan is one pass that fits
-  // a wide step; wide steps start at even chunks (the first one may hold one
-  // chunk).  Device memory gains nothing from them (the L2 serves the second
-  // half of a scale sector) and they cost registers.
-  const int sub = (a.wide && n_passes == 1 && S.P.n_groups <= kWideGroups) ? kWideSub : 1;
+  // chunks per step: kWideSub for host caches whose plan is one pass that
+  // fits a wide step; wide steps start at even chunks (the first one may hold
+  // one chunk).  Device memory gains nothing from them (the L2 serves the
+  // second half of a scale sector).
+  const int sub = (kHost && n_passes == 1 && S.P.n_groups <= kWideGroups) ? kWideSub : 1;
   auto span = [&](int64_t c) -> int {
     return sub == 1 ? 1 : (int)min64((c & 1) ? 1 : kWideSub, c_end - c);
   };
@@ -162,7 +163,7 @@ __device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& 
   // step i: chunks [ch, ch + n_sub), pass ps, in stage buffer i & 1
   int64_t ch = c_begin;
   int ps = 0, n_sub = span(c_begin);
-  scan_issue<GP>(S, 0, pl, sp, a.nb_cap, ch * kScanBlocks, S.P.pass_g[0], S.P.pass_g[1], sub, n_sub);
+  scan_issue<GP>(S, 0, pl, sp, a.nb_cap, ch * kScanBlocks, S.P.pass_g[0], S.P.pass_g[1], sub, n_sub, kHost);
   for (int64_t i = 0;; ++i) {
     const int b = (int)(i & 1);
     cp_async_wait_all();
@@ -171,15 +172,15 @@ __device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& 
     const int64_t ch1 = ps1 == 0 ? ch + n_sub : ch;
     const int n_sub1 = ch1 < c_end ? span(ch1) : 0;
     if (n_sub1 > 0)
-      scan_issue<GP>(S, b ^ 1, pl, sp, a.nb_cap, ch1 * kScanBlocks, S.P.pass_g[ps1], S.P.pass_g[ps1 + 1], sub, n_sub1);
+      scan_issue<GP>(S, b ^ 1, pl, sp, a.nb_cap, ch1 * kScanBlocks, S.P.pass_g[ps1], S.P.pass_g[ps1 + 1], sub, n_sub1, kHost);
     const int g0 = S.P.pass_g[ps], g1 = S.P.pass_g[ps + 1];
     const int s0 = S.P.grp_base[g0], s1 = g1 < S.P.n_groups ? (int)S.P.grp_base[g1] : S.P.n_slots;
-    for (int c = 0; c < n_sub; ++c) {
+    for (int c = 0; c < (kHost ? n_sub : 1); ++c) {
       if (c > 0) __syncwarp();  // every lane is done reading the previous chunk's u
-      scan_form_u<GP>(S, b, s0, s1, lb, sub, c);
+      scan_form_u<GP>(S, b, s0, s1, lb, sub, c, kHost);
       __syncwarp();
       const int nbl = (int)min64(kScanBlocks, nb_valid - (ch + c) * kScanBlocks);
-      if (lb < nbl) scan_compute_pipe<GP>(S, b, g0, g1, s0, lb, sub, c, keep, rot, A);
+      if (lb < nbl) scan_compute_pipe<GP>(S, b, g0, g1, s0, lb, sub, c, kHost, keep, rot, A);
       if (ps + 1 == n_passes) finish_chunk(ch + c);
     }
     if (n_sub1 == 0) break;
@@ -190,7 +191,7 @@ __device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& 
   flush_hist();
 }
 
-template <int GP>
+template <int GP, bool kHost>
 __global__ void __launch_bounds__(kScanThreads, 2) k_scan_pipe(ScanArgs a) {
   pdl_enter();
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -201,15 +202,15 @@ __global__ void __launch_bounds__(kScanThreads, 2) k_scan_pipe(ScanArgs a) {
   for (int64_t f = total * blockIdx.x / gridDim.x; f < f1;) {
     const int64_t unit = f / a.chunks, c0 = f % a.chunks;
     const int64_t c1 = min64(a.chunks, c0 + (f1 - f));
-    scan_unit_pipe<GP>(a, S, unit, c0, c1);
+    scan_unit_pipe<GP, kHost>(a, S, unit, c0, c1);
     f += c1 - c0;
   }
 }
 
-template <int GP>
+template <int GP, bool kHost>
 cudaError_t launch_scan_gp(ScanArgs a, int64_t chunks, int64_t units, cudaStream_t st) {
   const int smem = (int)sizeof(PipeSmem<GP>);
-  void (*kernel)(ScanArgs) = k_scan_pipe<GP>;
+  void (*kernel)(ScanArgs) = k_scan_pipe<GP, kHost>;
   // resident CTAs per device, looked up once per device
   constexpr int kDevs = 64;
   static int slots[kDevs] = {};
@@ -246,15 +247,19 @@ cudaError_t launch_scan(const bpkv_cache& c, const float* q, const uint8_t* dept
                         cudaStream_t st, const void* plan, uint32_t* hist, int32_t n_sink, int32_t n_recent,
                         int32_t pending, int32_t* status) {
   ScanArgs a{plan,         c.planes, c.scales, c.seq_len, q,        depths,  scores, ld, c.cap_tokens / kBlock,
-             c.n_kv_heads, c.group,  hist,     n_sink,    n_recent, pending, status, 0,  0,
-             c.residency == 1};
+             c.n_kv_heads, c.group,  hist,     n_sink,    n_recent, pending, status, 0,  0};
   const int64_t chunks = (c.n_max + kScanBlocks * kBlock - 1) / (kScanBlocks * kBlock);
   if (chunks == 0) return cudaSuccess;
   const int64_t units = (int64_t)c.n_seq * c.n_kv_heads;
-  if (c.group <= 1) return launch_scan_gp<1>(a, chunks, units, st);
-  if (c.group <= 2) return launch_scan_gp<2>(a, chunks, units, st);
-  if (c.group <= 4) return launch_scan_gp<4>(a, chunks, units, st);
-  return launch_scan_gp<8>(a, chunks, units, st);
+  auto go = [&](auto gp) {
+    constexpr int GP = decltype(gp)::value;
+    return c.residency == 1 ? launch_scan_gp<GP, true>(a, chunks, units, st)
+                            : launch_scan_gp<GP, false>(a, chunks, units, st);
+  };
+  if (c.group <= 1) return go(std::integral_constant<int, 1>{});
+  if (c.group <= 2) return go(std::integral_constant<int, 2>{});
+  if (c.group <= 4) return go(std::integral_constant<int, 4>{});
+  return go(std::integral_constant<int, 8>{});
 }
 
 }  // namespace bpkv

@@ -401,43 +401,51 @@ __device__ bool scan_chunk(ScanSmem<GP>& S, const uint64_t* __restrict__ pl, con
 // reads of pinned host memory by these copies are not kept in L2, so there
 // every half sector crosses the link in full).
 //
-// Staged plane rows have no padding: a row of a step of `sub` chunks is 2 sub
-// 32-byte pieces (4 blocks each); piece k of row r sits at piece slot
-// k ^ swz_piece(r) of the row, with its two 16-byte halves swapped when
-// swz_half(r) is 1.  Every 32-byte sector read from memory so lands in one
-// aligned 32-byte slot (a copy whose sector halves land in different slots is
-// split and fetches the sector twice, which over the host link costs the
-// bytes in full), and the 8-byte reads of one block column by rows r .. r + 7
-// fall in eight different 16-byte bank groups.
+// Staged plane rows.  Device caches: one-chunk steps, each row's 16 words
+// followed by 4 words of padding (row pitch 20 words: the 8-byte reads of one
+// block column by rows r .. r + 7 fall in eight different 16-byte bank
+// groups).  Host caches: no padding; a row of a step of `sub` chunks is 2 sub
+// 32-byte pieces (4 blocks each), piece k of row r at piece slot
+// k ^ swz_piece(r) of the row with its two 16-byte halves swapped when
+// swz_half(r) is 1, which gives the reads the same eight bank groups while
+// every 32-byte sector read from memory lands in one aligned 32-byte slot (a
+// copy whose sector halves land in different slots is split and fetches the
+// sector twice; the L2 absorbs that for device memory, but over the host link
+// it costs the bytes in full).
 
 constexpr int kStageRows = kPassGroups * 32;
-constexpr int kStageWords = kStageRows * 2 * kScanBlocks;  // one-chunk steps: 16 words per row
+constexpr int kRowPitch = 2 * kScanBlocks + 4;              // device caches
+constexpr int kStageWords = kStageRows * kRowPitch;         // device caches
+constexpr int kHostStageWords = kStageRows * 2 * kScanBlocks;
 constexpr int kWideSub = 2;                                 // chunks per step of a wide unit
-constexpr int kWideGroups = kStageWords / (32 * 2 * kScanBlocks * kWideSub);
-constexpr int kStageU32 = kStageWords + kPassSlots * kScanBlocks * kWideSub / 2;
+constexpr int kWideGroups = kHostStageWords / (32 * 2 * kScanBlocks * kWideSub);
+constexpr int kStageU32 = kStageWords + kPassSlots * kScanBlocks / 2 > kHostStageWords + kPassSlots * kScanBlocks * kWideSub / 2
+                              ? kStageWords + kPassSlots * kScanBlocks / 2
+                              : kHostStageWords + kPassSlots * kScanBlocks * kWideSub / 2;
 static_assert(kWideGroups >= 5, "a wide step must hold the single-pass plans of usual budgets");
 
 // u32 words per staged plane row for steps of `sub` chunks.
-__host__ __device__ constexpr int row_pitch(int sub) { return 2 * kScanBlocks * sub; }
-// Placement of the pieces of staged row r (see above).
+__host__ __device__ constexpr int row_pitch(int sub, bool host) { return host ? 2 * kScanBlocks * sub : kRowPitch; }
+// Placement of the pieces of staged row r of a host cache (see above).
 __device__ __forceinline__ int swz_piece(int r, int sub) { return sub == 1 ? (r >> 1) & 1 : r & 3; }
 __device__ __forceinline__ int swz_half(int r) { return (r >> 2) & 1; }
 // u32 word of 16-byte part q (0 .. 4 sub - 1) of staged row r
-__device__ __forceinline__ int staged_word(int r, int q, int sub) {
-  return r * row_pitch(sub) + 8 * ((q >> 1) ^ swz_piece(r, sub)) + 4 * ((q & 1) ^ swz_half(r));
+__device__ __forceinline__ int staged_word(int r, int q, int sub, bool host) {
+  if (!host) return r * kRowPitch + 4 * q;
+  return r * row_pitch(sub, true) + ((4 * q) ^ (8 * swz_piece(r, sub) + 4 * swz_half(r)));
 }
 
 // One stage buffer: the plane words (row (g - g0) * 32 + lane at
-// u32[row * row_pitch(sub)]), then from word kStageWords the raw block
-// scales, [slot - s0][sub chunks x 8 blocks].
+// u32[row * row_pitch]), then the raw block scales, [slot - s0][sub chunks x
+// 8 blocks], from word kStageWords (device caches) or kHostStageWords.
 struct __align__(16) ScanStage {
   uint32_t u32[kStageU32];
 };
-__device__ __forceinline__ uint16_t* stage_sc(ScanStage& st) {
-  return reinterpret_cast<uint16_t*>(st.u32 + kStageWords);
+__device__ __forceinline__ uint16_t* stage_sc(ScanStage& st, bool host) {
+  return reinterpret_cast<uint16_t*>(st.u32 + (host ? kHostStageWords : kStageWords));
 }
-__device__ __forceinline__ const uint16_t* stage_sc(const ScanStage& st) {
-  return reinterpret_cast<const uint16_t*>(st.u32 + kStageWords);
+__device__ __forceinline__ const uint16_t* stage_sc(const ScanStage& st, bool host) {
+  return reinterpret_cast<const uint16_t*>(st.u32 + (host ? kHostStageWords : kStageWords));
 }
 
 template <int GP>
@@ -581,29 +589,55 @@ __device__ __forceinline__ void acc_zero(Acc<GP>& A) {
 
 // All threads: start the copies of step (n_sub chunks from block b0, groups
 // [g0, g1)) into stage buffer b, laid out for steps of `sub` chunks: per used
-// plane row its n_sub x 8 words (16-byte pieces, consecutive pieces of a row
-// taken by consecutive threads so that each warp instruction copies whole row
-// segments), per used slot its n_sub x 8 block scales (one piece per chunk);
-// then commit them as this thread's newest group.  pl / sp are the unit's
+// plane row its n_sub x 8 words (16-byte pieces), per used slot its n_sub x 8
+// block scales (one piece per chunk); then commit them as this thread's newest
+// group.  Host caches (`host`): consecutive pieces of a row are taken by
+// consecutive threads, so that each warp instruction copies whole sectors
+// (the halves of a sector copied by different instructions would each fetch
+// it over the link); device caches: each thread takes whole rows (fewer
+// instructions; the L2 serves the second half).  pl / sp are the unit's
 // planes and scales; b0 + 8 n_sub <= nb_cap.
 template <int GP>
 __device__ __forceinline__ void scan_issue(PipeSmem<GP>& S, int b, const uint64_t* pl, const uint16_t* sp,
-                                           int64_t nb_cap, int64_t b0, int g0, int g1, int sub, int n_sub) {
+                                           int64_t nb_cap, int64_t b0, int g0, int g1, int sub, int n_sub,
+                                           bool host) {
   const ScanPlan<GP>& P = S.P;
-  const int per_row = 4 * n_sub, sc_pitch = kScanBlocks * sub;
-  const int n_piece = (g1 - g0) * 32 * per_row;
+  const int sc_pitch = kScanBlocks * sub;
+  const int n_row = (g1 - g0) * 32;
   const int s0 = P.grp_base[g0], s1 = g1 < P.n_groups ? (int)P.grp_base[g1] : P.n_slots;
-  const int n_all = n_piece + (s1 - s0) * n_sub;
-  for (int e = threadIdx.x; e < n_all; e += kScanThreads) {
-    if (e < n_piece) {
-      const int r = e / per_row, piece = e - r * per_row;
-      const int row = P.row_of_lane[g0 * 32 + r];
-      if (row >= 0)
-        cp_async16(&S.st[b].u32[staged_word(r, piece, sub)], pl + (int64_t)row * nb_cap + b0 + 2 * piece);
-    } else {
-      const int f = e - n_piece, rel = f / n_sub, c = f - rel * n_sub;
-      const int ch = P.slot_ch[s0 + rel];
-      if (ch >= 0) cp_async16(stage_sc(S.st[b]) + rel * sc_pitch + kScanBlocks * c, sp + (int64_t)ch * nb_cap + b0 + kScanBlocks * c);
+  const int sh = n_sub - 1;  // n_sub is 1 or 2
+  const int n_sc = (s1 - s0) << sh;
+  if (host) {
+    const int n_piece = n_row << (2 + sh);
+    for (int e = threadIdx.x; e < n_piece + n_sc; e += kScanThreads) {
+      if (e < n_piece) {
+        const int r = e >> (2 + sh), piece = e & ((4 << sh) - 1);
+        const int row = P.row_of_lane[g0 * 32 + r];
+        if (row >= 0)
+          cp_async16(&S.st[b].u32[staged_word(r, piece, sub, true)], pl + (int64_t)row * nb_cap + b0 + 2 * piece);
+      } else {
+        const int f = e - n_piece, rel = f >> sh, c = f & sh;
+        const int ch = P.slot_ch[s0 + rel];
+        if (ch >= 0)
+          cp_async16(stage_sc(S.st[b], host) + rel * sc_pitch + kScanBlocks * c, sp + (int64_t)ch * nb_cap + b0 + kScanBlocks * c);
+      }
+    }
+  } else {
+    for (int e = threadIdx.x; e < n_row + n_sc; e += kScanThreads) {
+      if (e < n_row) {
+        const int row = P.row_of_lane[g0 * 32 + e];
+        if (row >= 0) {
+          const uint64_t* src = pl + (int64_t)row * nb_cap + b0;
+#pragma unroll 4
+          for (int piece = 0; piece < (4 << sh); ++piece)
+            cp_async16(&S.st[b].u32[staged_word(e, piece, sub, false)], src + 2 * piece);
+        }
+      } else {
+        const int f = e - n_row, rel = f >> sh, c = f & sh;
+        const int ch = P.slot_ch[s0 + rel];
+        if (ch >= 0)
+          cp_async16(stage_sc(S.st[b], host) + rel * sc_pitch + kScanBlocks * c, sp + (int64_t)ch * nb_cap + b0 + kScanBlocks * c);
+      }
     }
   }
   cp_async_commit();
@@ -615,13 +649,14 @@ __device__ __forceinline__ void scan_issue(PipeSmem<GP>& S, int b, const uint64_
 __device__ __forceinline__ float sw(float s, float w) { return w != 0.f ? s * w : 0.f; }
 
 // This warp's u = s w for the slots [s0, s1) of a landed stage (block lb of
-// chunk c of a step of `sub` chunks): one slot per lane at a time, all heads
-// with vector loads and stores.
+// chunk c of a step of `sub` chunks; `host`: the host-cache layout): one slot
+// per lane at a time, all heads with vector loads and stores.
 template <int GP>
-__device__ __forceinline__ void scan_form_u(PipeSmem<GP>& S, int b, int s0, int s1, int lb, int sub, int c) {
+__device__ __forceinline__ void scan_form_u(PipeSmem<GP>& S, int b, int s0, int s1, int lb, int sub, int c,
+                                            bool host) {
   const int lane = threadIdx.x & 31;
   const int sc_pitch = kScanBlocks * sub;
-  const uint16_t* sc = stage_sc(S.st[b]) + kScanBlocks * c + lb;
+  const uint16_t* sc = stage_sc(S.st[b], host) + kScanBlocks * c + lb;
   const float* w = S.P.w + s0 * GP;
   float* ud = S.u[lb];
   for (int rel = lane; rel < s1 - s0; rel += 32) {
@@ -643,18 +678,18 @@ __device__ __forceinline__ void scan_form_u(PipeSmem<GP>& S, int b, int s0, int 
 }
 
 // Add groups [g0, g1) of a landed stage to this lane's accumulators (warp lb:
-// block lb of chunk c of a step of `sub` chunks, tokens lane and lane + 32).
-// u must be formed.
+// block lb of chunk c of a step of `sub` chunks, tokens lane and lane + 32;
+// `host`: the host-cache layout).  u must be formed.
 template <int GP>
 __device__ __forceinline__ void scan_compute_pipe(const PipeSmem<GP>& S, int b, int g0, int g1, int s0, int lb,
-                                                  int sub, int c, const uint32_t (&keep)[5], const uint32_t (&rot)[5],
-                                                  Acc<GP>& A) {
+                                                  int sub, int c, bool host, const uint32_t (&keep)[5],
+                                                  const uint32_t (&rot)[5], Acc<GP>& A) {
   const int lane = threadIdx.x & 31;
   const ScanPlan<GP>& P = S.P;
   // block lb of chunk c is word 2 (lb % 2) of 16-byte part 4 c + lb / 2 of
   // row (g - g0) * 32 + lane (placed as row lane: 32 is a multiple of 8)
-  const uint32_t* wl = S.st[b].u32 + staged_word(lane, 4 * c + (lb >> 1), sub) + 2 * (lb & 1);
-  const int g_stride = 32 * row_pitch(sub);
+  const uint32_t* wl = S.st[b].u32 + staged_word(lane, 4 * c + (lb >> 1), sub, host) + 2 * (lb & 1);
+  const int g_stride = 32 * row_pitch(sub, host);
   for (int g = g0; g < g1; ++g) {
     const int d = P.grp_t[g], cnt = P.grp_cnt[g];
     const uint2 wv = *reinterpret_cast<const uint2*>(wl + (g - g0) * g_stride);

@@ -75,10 +75,11 @@ extern "C" {
  * or any memory on a system with address translation); kernels read them in
  * place over the host link.  seq_len is always device memory.
  * planes, scales and the rows must start on 16-byte boundaries (BPKV_EINVAL
- * otherwise); with cap_tokens a multiple of 512 and the four arrays on 256-byte
- * boundaries every plane row segment and row a kernel reads starts on a 32-byte
- * sector, which matters for host memory, whose reads L2 does not keep (a segment
- * that starts inside a sector moves one more sector over the link).
+ * otherwise); with cap_tokens a multiple of 1024 and the four arrays on 256-byte
+ * boundaries every plane row segment, scale segment and row a kernel reads
+ * starts on a 32-byte sector, which matters for host memory, whose reads L2 does
+ * not keep (a segment that starts inside a sector moves one more sector over the
+ * link).
  * n_max is host state: an upper bound of every seq_len[i], used to size
  * launches; bpkv_encode_append raises it.
  * basis (optional, NULL: the raw channels) float [H][D][D] in device memory: an
