@@ -163,16 +163,18 @@ __device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& 
   // step i: chunks [ch, ch + n_sub), pass ps, in stage buffer i & 1
   int64_t ch = c_begin;
   int ps = 0, n_sub = span(c_begin);
-  scan_issue<GP>(S, 0, pl, sp, a.nb_cap, ch * kScanBlocks, S.P.pass_g[0], S.P.pass_g[1], sub, n_sub, kHost);
+  scan_issue<GP>(S, 0, pl, sp, a.nb_cap, ch * kScanBlocks, S.P.pass_g[0], S.P.pass_g[1], sub,
+                 kHost ? n_sub : 1, kHost);
   for (int64_t i = 0;; ++i) {
     const int b = (int)(i & 1);
     cp_async_wait_all();
     __syncthreads();  // step i visible to all; every warp is done with step i - 1 (the other buffer)
     const int ps1 = ps + 1 == n_passes ? 0 : ps + 1;
-    const int64_t ch1 = ps1 == 0 ? ch + n_sub : ch;
+    const int64_t ch1 = ps1 == 0 ? ch + (kHost ? n_sub : 1) : ch;
     const int n_sub1 = ch1 < c_end ? span(ch1) : 0;
     if (n_sub1 > 0)
-      scan_issue<GP>(S, b ^ 1, pl, sp, a.nb_cap, ch1 * kScanBlocks, S.P.pass_g[ps1], S.P.pass_g[ps1 + 1], sub, n_sub1, kHost);
+      scan_issue<GP>(S, b ^ 1, pl, sp, a.nb_cap, ch1 * kScanBlocks, S.P.pass_g[ps1], S.P.pass_g[ps1 + 1], sub,
+                     kHost ? n_sub1 : 1, kHost);
     const int g0 = S.P.pass_g[ps], g1 = S.P.pass_g[ps + 1];
     const int s0 = S.P.grp_base[g0], s1 = g1 < S.P.n_groups ? (int)S.P.grp_base[g1] : S.P.n_slots;
     for (int c = 0; c < (kHost ? n_sub : 1); ++c) {
