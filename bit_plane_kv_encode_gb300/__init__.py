@@ -12,8 +12,7 @@ import ctypes
 
 from ._binding import (  # noqa: F401
     BpkvError, bpkv_alloc_depths, bpkv_cache, bpkv_calibrate_channels, bpkv_clear_status, bpkv_decode_step,
-    bpkv_dense_attend, bpkv_encode_append, bpkv_fixed_depths, bpkv_host_alloc, bpkv_host_free, bpkv_read_status,
-    bpkv_rotate, bpkv_scan, bpkv_scan_topk, bpkv_scan_topk_noalloc, bpkv_sparse_attend,
+    bpkv_dense_attend, bpkv_encode_append, bpkv_fixed_depths, bpkv_read_status, bpkv_rotate, bpkv_scan, bpkv_scan_topk, bpkv_scan_topk_noalloc, bpkv_sparse_attend,
     bpkv_status_string, bpkv_step_args, bpkv_step_fused, bpkv_topk, bpkv_union, bpkv_version, bpkv_workspace_size, header_symbols, load)
 
 HEAD_DIM = 128
@@ -23,28 +22,11 @@ DEV_OVERFLOW, DEV_SELECT = 1, 2
 STEP_FUSED, STEP_TAIL = 1, 2
 
 
-class HostBuffer:
-    """`nbytes` of host memory from bpkv_host_alloc, freed with the object."""
-
-    def __init__(self, nbytes: int):
-        import weakref
-        self.nbytes = int(nbytes)
-        self.ptr = bpkv_host_alloc(self.nbytes)
-        self._free = weakref.finalize(self, bpkv_host_free, self.ptr, self.nbytes)
-
-    def tensor(self, shape, dtype):
-        """A CPU tensor over the whole buffer (the buffer must outlive it)."""
-        import torch
-        raw = (ctypes.c_uint8 * self.nbytes).from_address(self.ptr)
-        return torch.frombuffer(raw, dtype=torch.uint8).view(dtype).view(shape)
-
-
 class Cache:
     """One layer's bit-plane K cache and bf16 K/V rows for N sequences x H KV heads.
 
     residency "hbm": all buffers in device memory.  "host": planes, scales and
-    rows in page-locked host memory (bpkv_host_alloc, owned by the cache), read
-    by the kernels in place over the host link.
+    rows in pinned host memory, read by the kernels in place over the host link.
     """
 
     def __init__(self, n_seq: int, n_kv_heads: int, group: int, cap_tokens: int, device="cuda",
@@ -56,20 +38,17 @@ class Cache:
         self.device = torch.device(device)
         host = residency == "host"
 
-        self._host_bufs = []
-
         def buf(shape, dtype):
             if host:
-                # page-locked host memory on huge pages (bpkv_host_alloc), which
-                # also starts on a sector boundary: the kernels' reads of it are
-                # not kept in L2, so a row segment that started inside a 32-byte
-                # sector would move one more sector over the link
+                # pinned host memory from a 256-byte boundary: the kernels' reads
+                # of it are not cached, so a row segment that starts inside a
+                # 32-byte sector moves one more sector over the link
                 n = dtype.itemsize
                 for e in shape:
                     n *= e
-                hb = HostBuffer(n)
-                self._host_bufs.append(hb)
-                return hb.tensor(shape, dtype)
+                raw = torch.empty(n + 256, dtype=torch.uint8, pin_memory=True)
+                off = (-raw.data_ptr()) % 256
+                return raw[off:off + n].view(dtype).view(shape)
             return torch.empty(shape, dtype=dtype, device=self.device)
 
         self.planes = buf((n_seq, n_kv_heads, D, 4, nb), torch.int64)
@@ -123,5 +102,5 @@ def sync_n_max(caches, arr):
         c.c.n_max = s.n_max
 
 
-__all__ = [n for n in dir() if n.startswith("bpkv_")] + ["Cache", "HostBuffer", "cache_array", "sync_n_max", "BpkvError"]
+__all__ = [n for n in dir() if n.startswith("bpkv_")] + ["Cache", "cache_array", "sync_n_max", "BpkvError"]
 _ = ctypes

@@ -64,8 +64,6 @@ _SIGS = {
     "bpkv_dense_attend": ([P, P, P, P, sz, P], ctypes.c_int),
     "bpkv_decode_step": ([P, i32, P, P, sz, P], ctypes.c_int),
     "bpkv_step_fused": ([P, i32, i32, i32, i32], ctypes.c_int),
-    "bpkv_host_alloc": ([sz, ctypes.POINTER(P)], ctypes.c_int),
-    "bpkv_host_free": ([P, sz], ctypes.c_int),
 }
 
 _lib = None
@@ -173,17 +171,6 @@ def bpkv_calibrate_channels(q_cal, k_cal, n_units: int, group: int, m_q: int, m_
                   load().bpkv_calibrate_channels(_ptr(q_cal), _ptr(k_cal), int(n_units), int(group), int(m_q),
                                                  int(m_k), int(n_channels), int(depth), _ptr(depths),
                                                  _stream(stream)))
-
-
-def bpkv_host_alloc(nbytes: int) -> int:
-    """Address of `nbytes` of page-locked, GPU-mapped host memory (see include/bpkv.h)."""
-    out = P()
-    _check("bpkv_host_alloc", load().bpkv_host_alloc(int(nbytes), ctypes.byref(out)))
-    return int(out.value)
-
-
-def bpkv_host_free(ptr: int, nbytes: int):
-    return _check("bpkv_host_free", load().bpkv_host_free(P(ptr), int(nbytes)))
 
 
 def bpkv_rotate(basis, n_seq: int, n_kv_heads: int, rows: int, x, y, stream=None):

@@ -1,8 +1,6 @@
 // extern "C" entry points of libbpkv (declared in include/bpkv.h): argument
-// checks, workspace layout and launch sequencing.  Nothing here allocates but
-// the host-memory helper bpkv_host_alloc.
+// checks, workspace layout and launch sequencing.  No allocation happens here.
 #include <stdio.h>
-#include <sys/mman.h>
 
 #include "common.cuh"
 
@@ -182,40 +180,6 @@ int cuda_status(cudaError_t e) {
 extern "C" {
 
 int32_t bpkv_version(void) { return 1; }
-
-int bpkv_host_alloc(size_t bytes, void** out) {
-  if (!out) return BPKV_EINVAL;
-  *out = nullptr;
-  if (bytes == 0) return BPKV_EINVAL;
-  constexpr size_t kHuge = size_t(1) << 29;  // the largest transparent huge page of common kernels
-  constexpr size_t kPage = size_t(1) << 16;  // a multiple of every base page size in use
-  const size_t len = (bytes + kPage - 1) / kPage * kPage;
-  void* raw = mmap(nullptr, len + kHuge, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
-  if (raw == MAP_FAILED) return BPKV_ECUDA;
-  const uintptr_t r0 = reinterpret_cast<uintptr_t>(raw);
-  const uintptr_t p = (r0 + kHuge - 1) / kHuge * kHuge;
-  // keep [p, p + len): give back the slack on both sides
-  if (p > r0) munmap(raw, p - r0);
-  if (r0 + len + kHuge > p + len) munmap(reinterpret_cast<void*>(p + len), r0 + len + kHuge - (p + len));
-  void* ptr = reinterpret_cast<void*>(p);
-  (void)madvise(ptr, len, MADV_HUGEPAGE);  // advice only
-  if (cudaHostRegister(ptr, len, cudaHostRegisterPortable | cudaHostRegisterMapped) != cudaSuccess) {
-    (void)cudaGetLastError();
-    munmap(ptr, len);
-    return BPKV_ECUDA;
-  }
-  *out = ptr;
-  return BPKV_OK;
-}
-
-int bpkv_host_free(void* ptr, size_t bytes) {
-  if (!ptr || bytes == 0) return BPKV_EINVAL;
-  constexpr size_t kPage = size_t(1) << 16;
-  const size_t len = (bytes + kPage - 1) / kPage * kPage;
-  const cudaError_t e = cudaHostUnregister(ptr);
-  munmap(ptr, len);
-  return e == cudaSuccess ? BPKV_OK : BPKV_ECUDA;
-}
 
 const char* bpkv_status_string(int status) {
   switch (status) {

@@ -131,20 +131,6 @@ int bpkv_read_status(const void *ws, int32_t *status, void *stream);
 const char *bpkv_status_string(int status);
 int32_t bpkv_version(void);
 
-/* Host memory for residency-1 caches (planes, scales, rows): `bytes` of
- * anonymous memory mapped at a 512 MiB boundary, advised for transparent huge
- * pages (best effort: the kernel decides), then page-locked and mapped for the
- * GPU (cudaHostRegister, portable and mapped; its device address equals the
- * host address on systems with unified addressing).  Huge pages cut the
- * address-translation misses of the kernels' scattered row reads over the host
- * link (measured: random 256-byte reads of a 16 GiB buffer took half the mean
- * time of cudaHostAlloc memory).  *out = the address, or NULL on error;
- * BPKV_EINVAL (out NULL or bytes 0) or BPKV_ECUDA (mapping or registration
- * failed; nothing is left allocated).  The memory is zero-filled.  Release it
- * with bpkv_host_free(ptr, bytes), same bytes. */
-int bpkv_host_alloc(size_t bytes, void **out);
-int bpkv_host_free(void *ptr, size_t bytes);
-
 /* ------------------------------------------------------------- encode (F1, F2) */
 /*
  * Fathom page section 3.2.  Append t_new tokens to every sequence: rows

@@ -73,7 +73,3 @@ def test_invalid_arguments_rejected_on_host(L):
     assert L.bpkv_dense_attend(ctypes.byref(c), fake, fake, fake, 10, None) == ENOWS
     assert L.bpkv_decode_step(None, 1, None, fake, 0, None) == EINVAL
     assert L.bpkv_status_string(-1) == b"invalid argument"
-    out = ctypes.c_void_p(1)
-    assert L.bpkv_host_alloc(0, ctypes.byref(out)) == EINVAL and not out.value
-    assert L.bpkv_host_alloc(1 << 20, None) == EINVAL
-    assert L.bpkv_host_free(None, 1 << 20) == EINVAL

@@ -1,7 +1,6 @@
 """Host-resident cache (Fathom page: KV cache and index in host memory, the
-scan's bytes crossing the interconnect): planes, scales and rows in
-page-locked host memory, read in place by the same kernels over the host
-link."""
+scan's bytes crossing the interconnect): planes, scales and rows in pinned
+host memory, read in place by the same kernels over the host link."""
 import numpy as np
 import pytest
 import torch
@@ -17,25 +16,6 @@ def pk():
     __graft_entry__.build()
     import bit_plane_kv_encode_gb300 as m
     return m
-
-
-def test_host_buffer(pk):
-    """bpkv_host_alloc: zero-filled, 512 MiB aligned, copies both ways, freed
-    with its owner (the kernels' reads of it: the host decode tests below)."""
-    n = (3 << 20) + 12345
-    hb = pk.HostBuffer(n)
-    assert hb.ptr % (1 << 29) == 0
-    t = hb.tensor((n,), torch.uint8)
-    assert int(t.sum()) == 0
-    src = torch.arange(n, device="cuda", dtype=torch.int64).remainder(251).to(torch.uint8)
-    t.copy_(src, non_blocking=True)
-    back = torch.empty_like(src)
-    back.copy_(t, non_blocking=True)
-    torch.cuda.synchronize()
-    assert torch.equal(back, src)
-    del t
-    hb._free()
-    assert not hb._free.alive
 
 
 def _decode(pk, cache, inp, cfg, flags=0):
