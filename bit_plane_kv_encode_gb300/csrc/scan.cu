@@ -160,35 +160,64 @@ __device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& 
     flush_hist();
     return;
   }
-  // step i: chunks [ch, ch + n_sub), pass ps, in stage buffer i & 1
-  int64_t ch = c_begin;
-  int ps = 0, n_sub = span(c_begin);
-  scan_issue<GP>(S, 0, pl, sp, a.nb_cap, ch * kScanBlocks, S.P.pass_g[0], S.P.pass_g[1], sub,
-                 kHost ? n_sub : 1, kHost);
-  for (int64_t i = 0;; ++i) {
-    const int b = (int)(i & 1);
-    cp_async_wait_all();
-    __syncthreads();  // step i visible to all; every warp is done with step i - 1 (the other buffer)
-    const int ps1 = ps + 1 == n_passes ? 0 : ps + 1;
-    const int64_t ch1 = ps1 == 0 ? ch + (kHost ? n_sub : 1) : ch;
-    const int n_sub1 = ch1 < c_end ? span(ch1) : 0;
-    if (n_sub1 > 0)
-      scan_issue<GP>(S, b ^ 1, pl, sp, a.nb_cap, ch1 * kScanBlocks, S.P.pass_g[ps1], S.P.pass_g[ps1 + 1], sub,
-                     kHost ? n_sub1 : 1, kHost);
-    const int g0 = S.P.pass_g[ps], g1 = S.P.pass_g[ps + 1];
-    const int s0 = S.P.grp_base[g0], s1 = g1 < S.P.n_groups ? (int)S.P.grp_base[g1] : S.P.n_slots;
-    for (int c = 0; c < (kHost ? n_sub : 1); ++c) {
-      if (c > 0) __syncwarp();  // every lane is done reading the previous chunk's u
-      scan_form_u<GP>(S, b, s0, s1, lb, sub, c, kHost);
+  if constexpr (!kHost) {
+    // device caches: steps (chunk, pass), one chunk each
+    const int64_t steps = (c_end - c_begin) * n_passes;
+    scan_issue<GP>(S, 0, pl, sp, a.nb_cap, c_begin * kScanBlocks, S.P.pass_g[0], S.P.pass_g[1], 1, 1, false);
+    int64_t ch = c_begin;  // chunk and pass of step i
+    int ps = 0;
+    for (int64_t i = 0; i < steps; ++i) {
+      const int b = (int)(i & 1);
+      cp_async_wait_all();
+      __syncthreads();  // step i visible to all; every warp is done with step i - 1 (the other buffer)
+      if (i + 1 < steps) {
+        const int ps1 = ps + 1 == n_passes ? 0 : ps + 1;
+        const int64_t ch1 = ps1 == 0 ? ch + 1 : ch;
+        scan_issue<GP>(S, b ^ 1, pl, sp, a.nb_cap, ch1 * kScanBlocks, S.P.pass_g[ps1], S.P.pass_g[ps1 + 1], 1, 1,
+                       false);
+      }
+      const int g0 = S.P.pass_g[ps], g1 = S.P.pass_g[ps + 1];
+      const int s0 = S.P.grp_base[g0], s1 = g1 < S.P.n_groups ? (int)S.P.grp_base[g1] : S.P.n_slots;
+      scan_form_u<GP>(S, b, s0, s1, lb, 1, 0, false);
       __syncwarp();
-      const int nbl = (int)min64(kScanBlocks, nb_valid - (ch + c) * kScanBlocks);
-      if (lb < nbl) scan_compute_pipe<GP>(S, b, g0, g1, s0, lb, sub, c, kHost, keep, rot, A);
-      if (ps + 1 == n_passes) finish_chunk(ch + c);
+      const int nbl = (int)min64(kScanBlocks, nb_valid - ch * kScanBlocks);
+      if (lb < nbl) scan_compute_pipe<GP>(S, b, g0, g1, s0, lb, 1, 0, false, keep, rot, A);
+      if (++ps == n_passes) {
+        finish_chunk(ch);
+        ps = 0;
+        ++ch;
+      }
     }
-    if (n_sub1 == 0) break;
-    ch = ch1;
-    ps = ps1;
-    n_sub = n_sub1;
+  } else {
+    // host caches: step i covers chunks [ch, ch + n_sub), pass ps
+    int64_t ch = c_begin;
+    int ps = 0, n_sub = span(c_begin);
+    scan_issue<GP>(S, 0, pl, sp, a.nb_cap, ch * kScanBlocks, S.P.pass_g[0], S.P.pass_g[1], sub, n_sub, true);
+    for (int64_t i = 0;; ++i) {
+      const int b = (int)(i & 1);
+      cp_async_wait_all();
+      __syncthreads();  // step i visible to all; every warp is done with step i - 1 (the other buffer)
+      const int ps1 = ps + 1 == n_passes ? 0 : ps + 1;
+      const int64_t ch1 = ps1 == 0 ? ch + n_sub : ch;
+      const int n_sub1 = ch1 < c_end ? span(ch1) : 0;
+      if (n_sub1 > 0)
+        scan_issue<GP>(S, b ^ 1, pl, sp, a.nb_cap, ch1 * kScanBlocks, S.P.pass_g[ps1], S.P.pass_g[ps1 + 1], sub,
+                       n_sub1, true);
+      const int g0 = S.P.pass_g[ps], g1 = S.P.pass_g[ps + 1];
+      const int s0 = S.P.grp_base[g0], s1 = g1 < S.P.n_groups ? (int)S.P.grp_base[g1] : S.P.n_slots;
+      for (int c = 0; c < n_sub; ++c) {
+        if (c > 0) __syncwarp();  // every lane is done reading the previous chunk's u
+        scan_form_u<GP>(S, b, s0, s1, lb, sub, c, true);
+        __syncwarp();
+        const int nbl = (int)min64(kScanBlocks, nb_valid - (ch + c) * kScanBlocks);
+        if (lb < nbl) scan_compute_pipe<GP>(S, b, g0, g1, s0, lb, sub, c, true, keep, rot, A);
+        if (ps + 1 == n_passes) finish_chunk(ch + c);
+      }
+      if (n_sub1 == 0) break;
+      ch = ch1;
+      ps = ps1;
+      n_sub = n_sub1;
+    }
   }
   flush_hist();
 }
