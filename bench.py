@@ -380,6 +380,21 @@ def bench_ours(args, cfg, rank, world, local):
                     rows_bytes += u * row_bytes(D)
         score_bytes += L * N * H * G * n * 4
     n_launch = len(passes) * L
+    # quality on the planted needles of layer 0 (positions of keys with a large
+    # q.k): the fraction inside the union of the KV head's selections, per budget
+    needle_recall = None
+    if getattr(inp, "needles", None) is not None:
+        needle_recall = {}
+        for p in passes:
+            idx0 = p["idx"][0].cpu().numpy()  # [N][H][G][k], layer 0
+            found = total = 0
+            for s in range(N):
+                for h in range(H):
+                    sel = set(idx0[s, h].ravel().tolist())
+                    pos = inp.needles[s, h].tolist()
+                    found += sum(int(x) in sel for x in pos)
+                    total += len(pos)
+            needle_recall[str(p["budget"])] = round(found / max(total, 1), 4)
     stage_mean = {s: statistics.mean(v) for s, v in stage_ms.items()}
     if all(p["fused"] for p in passes):
         # one fused kernel per pass: it reads the plane prefixes and the union rows
@@ -429,6 +444,7 @@ def bench_ours(args, cfg, rank, world, local):
                         "'encode' holds the front kernel (append beside depths and plan), 'topk' the cut "
                         "kernel and 'attend' the range attention; on the fused path 'encode' holds the "
                         "whole fused kernel and 'attend' the length update"),
+        "needle_recall_layer0": needle_recall,
         "bytes_per_step": {"scan": round(scan_bytes), "rows": round(rows_bytes), "scores_overhead": round(score_bytes),
                            "union_rows": union_rows},
         "roofline": roofline,
