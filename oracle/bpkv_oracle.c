@@ -26,6 +26,9 @@
  *     calibration statistics (mean |q| times mean |k| per channel);
  *   - contributions, basis rule: KLT planes (an orthogonal basis) for models
  *     without QK norm, applied to keys and queries alike.
+ * The value-side functions (or_v_*, or_attend_vdepth) follow the second read
+ * stage of "ReadKV" (the ReadKV page, sections 5.3 and 5.4): per-token value
+ * depths from the squared attention probabilities.
  * Readings where the page is silent (bit order inside a word, zero and
  * overflowing scales, tie rules, stop rule of the allocator) are stated at each
  * function.
@@ -479,4 +482,143 @@ void or_dense_attend(int64_t n, int32_t D, int32_t G, const float *q, const uint
     for (int32_t d = 0; d < D; ++d) out[h * D + d] /= z;
   }
   free(logit);
+}
+
+/* ------------------------------------------------- value-side depth (stage 2) */
+
+/*
+ * Second read stage of "ReadKV" (the ReadKV page, sections 5.3 and 5.4): after
+ * the keys decide the attention, each value row is read to a per-token depth,
+ * all channels of a token sharing it, and the depths go to the rows whose
+ * attention weight matters most.
+ *
+ * Value bit planes (readings: the page's value codes are progressive per
+ * token; the code is the same 4-bit mid-rise code as the keys, with the scale
+ * taken over the row instead of a block of a channel, since a row is what
+ * one depth covers): token i has one fp16 scale s_i = fp16(max_j |v_ij| / 8),
+ * codes c_ij = clip(floor(v_ij / s_i), -8, 7) + 8 (float32 division, as for the
+ * keys; a zero scale gives code 8), and plane p of token i is D / 64 words, bit
+ * b of word w = bit (3 - p) of the code of channel 64 w + b.  Layout: vscales
+ * [n], vplanes [n][4][D / 64].  D is a multiple of 64.
+ */
+void or_v_encode(int64_t n, int32_t D, const uint16_t *v, uint16_t *vscales, uint64_t *vplanes) {
+  const int32_t W = D / 64;
+  for (int64_t i = 0; i < n; ++i) {
+    double a = 0.0;
+    for (int32_t j = 0; j < D; ++j) {
+      double x = fabs(or_bf16_value(v[i * D + j]));
+      if (x > a) a = x;
+    }
+    uint16_t s16 = or_fp16_bits(a / 8.0);
+    float s = (float)or_fp16_value(s16);
+    vscales[i] = s16;
+    for (int64_t e = 0; e < 4 * (int64_t)W; ++e) vplanes[i * 4 * W + e] = 0;
+    for (int32_t j = 0; j < D; ++j) {
+      int c = 8;
+      if (s16 != 0) {
+        float qt = (float)or_bf16_value(v[i * D + j]) / s;
+        double f = floor((double)qt);
+        if (f < -8.0) f = -8.0;
+        if (f > 7.0) f = 7.0;
+        c = (int)f + 8;
+      }
+      int w = j / 64, b = (OR_MUTANT == 16) ? 63 - j % 64 : j % 64;
+      for (int p = 0; p < 4; ++p)
+        if ((c >> (3 - p)) & 1) vplanes[(i * 4 + p) * W + w] |= (uint64_t)1 << b;
+    }
+  }
+}
+
+/* Value row i read to depth t (0..4): vhat_j = s_i ((c_t + 1/2) 2^(4-t) - 8),
+ * the same mid-rise reconstruction as the keys; t = 0 reads nothing and gives
+ * the zero row. */
+void or_v_row(int32_t D, const uint16_t *vscales, const uint64_t *vplanes, int64_t i, int t, double *out) {
+  const int32_t W = D / 64;
+  double s = or_fp16_value(vscales[i]);
+  for (int32_t j = 0; j < D; ++j) {
+    int c = 0;
+    for (int p = 0; p < t; ++p) c = (c << 1) | (int)((vplanes[(i * 4 + p) * W + j / 64] >> (j % 64)) & 1);
+    out[j] = or_dequant(s, c, t);
+  }
+}
+
+/*
+ * Per-token value depths (the ReadKV page, section 5.4): greedy on the
+ * predicted error drop.  Items are (row r, next plane t_r) with value
+ * a_r 4^-t_r, the error of a mid-rise code in standardised units shrinking by
+ * 4 per plane; each item costs one plane (D bits per token, section 5.4), the
+ * budget is budget planes; the largest value goes first, ties to the lower
+ * row; allocation stops when the value is <= 0, the budget is spent or every
+ * row has 4 planes.  Row scales are read for rows with t_r > 0 and are not
+ * charged to the budget (the page counts value bits in planes).  Returns the
+ * planes used.
+ */
+int32_t or_v_alloc(int32_t n_rows, const double *a, int32_t budget, uint8_t *depth) {
+  for (int32_t r = 0; r < n_rows; ++r) depth[r] = 0;
+  int32_t left = budget;
+  while (left > 0) {
+    int32_t best = -1;
+    double bv = 0.0;
+    for (int32_t r = 0; r < n_rows; ++r) {
+      if (depth[r] >= 4) continue;
+      double v = a[r] * ldexp(1.0, -2 * depth[r]);
+      if (best < 0 || v > bv || (OR_MUTANT == 15 && v == bv)) { best = r; bv = v; }
+    }
+    if (best < 0 || !(bv > 0.0)) break;
+    depth[best] += 1;
+    left -= 1;
+  }
+  return budget - left;
+}
+
+/*
+ * Stage 2 over one KV head's union (rows uidx[0..n_u), ascending, with head
+ * masks umask: bit h set when query head h selected the row).  Head h attends
+ * over its own rows with exact bf16 keys: p_h(r) = softmax_r(q_h . k / sqrt(D)).
+ * The weight of a row is a_r = sum_h p_h(r)^2 (ReadKV page, section 5.3: squared
+ * attention probabilities summed over the query heads sharing the KV head, head
+ * scale coefficient 1), depths come from or_v_alloc, and
+ * o_h = sum_r p_h(r) vhat_r(t_r).  Everything in double.  Outputs: depth[n_u],
+ * weight[n_u] (a_r), out[G][D].
+ */
+void or_attend_vdepth(int32_t D, int32_t G, const float *q, const uint16_t *k_rows, const uint16_t *vscales,
+                      const uint64_t *vplanes, const int32_t *uidx, const uint8_t *umask, int32_t n_u,
+                      int32_t budget_v, uint8_t *depth, double *weight, double *out) {
+  const double scale = 1.0 / sqrt((double)D);
+  double *p = (double *)malloc(sizeof(double) * (size_t)(n_u > 0 ? n_u : 1) * (size_t)G);
+  double *row = (double *)malloc(sizeof(double) * (size_t)D);
+  for (int32_t h = 0; h < G; ++h) {
+    double m = -INFINITY;
+    for (int32_t r = 0; r < n_u; ++r) {
+      if (!((umask[r] >> h) & 1)) { p[h * n_u + r] = -INFINITY; continue; }
+      double acc = 0.0;
+      for (int32_t d = 0; d < D; ++d) acc += (double)q[h * D + d] * or_bf16_value(k_rows[(int64_t)uidx[r] * D + d]);
+      p[h * n_u + r] = acc * scale;
+      if (p[h * n_u + r] > m) m = p[h * n_u + r];
+    }
+    double z = 0.0;
+    for (int32_t r = 0; r < n_u; ++r) {
+      double e = ((umask[r] >> h) & 1) ? exp(p[h * n_u + r] - m) : 0.0;
+      p[h * n_u + r] = e;
+      z += e;
+    }
+    for (int32_t r = 0; r < n_u; ++r) p[h * n_u + r] = z > 0.0 ? p[h * n_u + r] / z : 0.0;
+  }
+  for (int32_t r = 0; r < n_u; ++r) {
+    double acc = 0.0;
+    for (int32_t h = 0; h < G; ++h) acc += (OR_MUTANT == 14) ? p[h * n_u + r] : p[h * n_u + r] * p[h * n_u + r];
+    weight[r] = acc;
+  }
+  or_v_alloc(n_u, weight, budget_v, depth);
+  for (int64_t e = 0; e < (int64_t)G * D; ++e) out[e] = 0.0;
+  for (int32_t r = 0; r < n_u; ++r) {
+    or_v_row(D, vscales, vplanes, uidx[r], depth[r], row);
+    for (int32_t h = 0; h < G; ++h) {
+      double w = p[h * n_u + r];
+      if (w == 0.0) continue;
+      for (int32_t d = 0; d < D; ++d) out[h * D + d] += w * row[d];
+    }
+  }
+  free(row);
+  free(p);
 }

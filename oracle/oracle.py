@@ -6,8 +6,9 @@ never imports it.
 
 Each function handles one unit, i.e. one (sequence, KV head) of one layer, and
 wraps the C function of the same name in ``bpkv_oracle.c`` (see that file for
-the passages of the Fathom page each one follows).  ``decode_unit`` chains
-them in the order of one decode step.
+the passages of the Fathom page each one follows; the ``v_*`` functions and
+``attend_vdepth`` follow the ReadKV page's second read stage).  ``decode_unit``
+chains them in the order of one decode step.
 """
 from __future__ import annotations
 
@@ -73,6 +74,14 @@ def _bind(path: str) -> ctypes.CDLL:
     L.or_attend.restype = None
     L.or_dense_attend.argtypes = [i64, i32, i32, P, P, P, P]
     L.or_dense_attend.restype = None
+    L.or_v_encode.argtypes = [i64, i32, P, P, P]
+    L.or_v_encode.restype = None
+    L.or_v_row.argtypes = [i32, P, P, i64, ctypes.c_int, P]
+    L.or_v_row.restype = None
+    L.or_v_alloc.argtypes = [i32, P, i32, P]
+    L.or_v_alloc.restype = i32
+    L.or_attend_vdepth.argtypes = [i32, i32, P, P, P, P, P, P, i32, i32, P, P, P]
+    L.or_attend_vdepth.restype = None
     return L
 
 
@@ -210,6 +219,50 @@ class Oracle:
         out = np.zeros((G, D), dtype=np.float64)
         self.L.or_dense_attend(int(n), D, G, _p(q), _p(k_rows), _p(v_rows), _p(out))
         return out
+
+    # -- value-side depth (ReadKV page, sections 5.3-5.4)
+    def v_encode(self, v_bits: np.ndarray):
+        """v_bits: bf16 patterns [n][D] -> (vscales [n] u16, vplanes [n][4][D/64] u64)."""
+        v_bits = _c(v_bits, np.uint16)
+        n, D = v_bits.shape
+        vscales = np.zeros(n, dtype=np.uint16)
+        vplanes = np.zeros((n, 4, D // 64), dtype=np.uint64)
+        self.L.or_v_encode(n, D, _p(v_bits), _p(vscales), _p(vplanes))
+        return vscales, vplanes
+
+    def v_row(self, vscales: np.ndarray, vplanes: np.ndarray, i: int, t: int) -> np.ndarray:
+        """Value row i read to depth t -> float64 [D]."""
+        vscales = _c(vscales, np.uint16)
+        vplanes = _c(vplanes, np.uint64)
+        D = vplanes.shape[2] * 64
+        out = np.zeros(D, dtype=np.float64)
+        self.L.or_v_row(D, _p(vscales), _p(vplanes), int(i), int(t), _p(out))
+        return out
+
+    def v_alloc(self, a: np.ndarray, budget: int):
+        """Row weights a [n_rows] (float64), budget in planes -> (depths [n_rows] u8, planes used)."""
+        a = _c(a, np.float64)
+        depth = np.zeros(a.shape[0], dtype=np.uint8)
+        used = self.L.or_v_alloc(a.shape[0], _p(a), int(budget), _p(depth))
+        return depth, int(used)
+
+    def attend_vdepth(self, q: np.ndarray, k_rows: np.ndarray, vscales: np.ndarray, vplanes: np.ndarray,
+                      uidx: np.ndarray, umask: np.ndarray, budget_v: int) -> dict:
+        """Stage 2 over one KV head's union: weights, value depths, output [G][D]."""
+        q = _c(q, np.float32)
+        k_rows = _c(k_rows, np.uint16)
+        vscales = _c(vscales, np.uint16)
+        vplanes = _c(vplanes, np.uint64)
+        uidx = _c(uidx, np.int32)
+        umask = _c(umask, np.uint8)
+        G, D = q.shape
+        n_u = uidx.shape[0]
+        depth = np.zeros(n_u, dtype=np.uint8)
+        weight = np.zeros(n_u, dtype=np.float64)
+        out = np.zeros((G, D), dtype=np.float64)
+        self.L.or_attend_vdepth(D, G, _p(q), _p(k_rows), _p(vscales), _p(vplanes), _p(uidx), _p(umask), n_u,
+                                int(budget_v), _p(depth), _p(weight), _p(out))
+        return dict(depth=depth, weight=weight, out=out)
 
     def decode_unit(self, k_bits: np.ndarray, v_bits: np.ndarray, q: np.ndarray, sigma2: np.ndarray,
                     budget_bits: int | None, k: int, n_sink: int = 4, n_recent: int = 32,

@@ -562,6 +562,148 @@ def pin_attention(o):
                        rtol=1e-13, atol=1e-13)
 
 
+# ------------------------------------------------------------------ value-side depth (ReadKV, stage 2)
+
+def exact_row_codes(v_bits: np.ndarray, t: int = 4) -> np.ndarray:
+    """Direct t-bit codes of value rows [n][D] with the row's scale
+    s = fp16(rowmax / 8) (numpy float16 rounding), exact rational floor."""
+    n, D = v_bits.shape
+    vv = bf16_value(v_bits)
+    out = np.zeros((n, D), dtype=np.int64)
+    if t == 0:
+        return out
+    half = 1 << (t - 1)
+    for i in range(n):
+        s = block_scale(float(np.max(np.abs(vv[i]))))
+        for j in range(D):
+            if s == 0.0:
+                out[i, j] = half
+                continue
+            f = math.floor(Fraction(vv[i, j]) / (Fraction(s) * (2 ** (4 - t))))
+            out[i, j] = min(max(f, -half), half - 1) + half
+    return out
+
+
+def unpack_row_codes(vplanes: np.ndarray, t: int = 4) -> np.ndarray:
+    """t-bit prefix codes [n][D] from token-major planes [n][4][D/64] (numpy
+    little-endian bit unpacking: bit b of word w = channel 64 w + b)."""
+    n, _, W = vplanes.shape
+    by = np.ascontiguousarray(vplanes).view(np.uint8).reshape(n, 4, W * 8)
+    bits = np.unpackbits(by, axis=-1, bitorder="little").astype(np.int64)  # [n][4][D]
+    c = np.zeros((n, W * 64), dtype=np.int64)
+    for p in range(t):
+        c = (c << 1) | bits[:, p, :]
+    return c
+
+
+def pin_value_codes(o):
+    rng = np.random.default_rng(21)
+    n, D = 9, 128
+    v = bf16_bits_of(rng.standard_normal((n, D)) * np.exp(rng.standard_normal((n, 1))))
+    v[2] = 0                                              # an all-zero row: scale 0, codes 8
+    adv = _adversarial_block(2)[:, 0]                     # values on and below every cell edge, s = 1
+    v[4, :64], v[4, 64:] = adv, adv
+    vscales, vplanes = o.v_encode(v)
+    for t in range(5):
+        got, want = unpack_row_codes(vplanes, t), exact_row_codes(v, t)
+        assert np.array_equal(got, want), (t, np.argwhere(got != want)[:5])
+    vv = bf16_value(v)
+    for i in range(n):
+        w = np.array([block_scale(float(np.max(np.abs(vv[i]))))], dtype=np.float16).view(np.uint16)[0]
+        assert vscales[i] == w, (i, hex(vscales[i]), hex(w))
+    # reconstruction: the mid-rise cell midpoint of the t-bit code, zero at t = 0
+    for i in (0, 4):
+        s = block_scale(float(np.max(np.abs(vv[i]))))
+        for t in range(5):
+            ct = exact_row_codes(v[i:i + 1], t)[0]
+            want = np.zeros(D) if t == 0 else s * ((ct + 0.5) * 2.0 ** (4 - t) - 8.0)
+            assert np.array_equal(o.v_row(vscales, vplanes, i, t), want), (i, t)
+    assert not o.v_row(vscales, vplanes, 2, 4).any()
+
+
+def pin_value_bit_order_golden(o):
+    g = json.load(open(os.path.join(GOLDEN, "value_plane_order.json")))
+    v = bf16_bits_of(np.array([[(j % 16) - 8 for j in range(128)]], dtype=np.float32))
+    vscales, vplanes = o.v_encode(v)
+    assert int(vscales[0]) == int(g["scale_fp16"], 16)
+    for p in range(4):
+        for w in range(2):
+            assert int(vplanes[0, p, w]) == int(g["planes"][p][w], 16), (p, w, hex(int(vplanes[0, p, w])))
+    depth, used = o.v_alloc(np.ones(3), 1)
+    assert list(depth) == [1, 0, 0] and used == 1
+
+
+def pin_value_alloc_bruteforce(o):
+    """The greedy depths minimise sum_r a_r 4^-t_r over every depth vector with
+    as many planes (a concave separable objective: greedy is optimal), use
+    min(budget, 4 n) planes when every weight is positive, and never read a
+    row of zero weight."""
+    n = 6
+    T = np.array(list(itertools.product(range(5), repeat=n)), dtype=np.int64)
+    used_all = T.sum(axis=1)
+    pw = 4.0 ** (-T.astype(np.float64))
+    rng = np.random.default_rng(22)
+    for trial in range(5):
+        a = rng.random(n) ** 3
+        if trial == 4:
+            a[1] = 0.0
+        obj = pw @ a
+        for B in range(0, 4 * n + 3):
+            t, used = o.v_alloc(a, B)
+            t = t.astype(np.int64)
+            assert used == int(t.sum()) <= B
+            if trial < 4:
+                assert used == min(B, 4 * n), (trial, B, used)
+            m = used_all <= used
+            mine = float(pw[np.ravel_multi_index(t, (5,) * n)] @ a)
+            assert mine <= obj[m].min() * (1 + 1e-12) + 1e-300, (trial, B, t)
+            if trial == 4:
+                assert t[1] == 0
+
+
+def pin_value_attention(o):
+    rng = np.random.default_rng(23)
+    n, D, G = 40, 128, 4
+    k = bf16_bits_of(rng.standard_normal((n, D)) * 1.5)
+    v = bf16_bits_of(rng.standard_normal((n, D)))
+    q = rng.standard_normal((G, D)).astype(np.float32)
+    vscales, vplanes = o.v_encode(v)
+    # a union of 25 rows; head h selects a subset, every row at least one head
+    uidx = np.sort(rng.choice(n, size=25, replace=False)).astype(np.int32)
+    umask = rng.integers(1, 16, size=25).astype(np.uint8)
+    kv = bf16_value(k)
+    p = np.zeros((G, 25))
+    for h in range(G):
+        sel = np.nonzero((umask >> h) & 1)[0]
+        lg = (q[h].astype(np.float64) @ kv[uidx[sel]].T) / math.sqrt(D)
+        w = np.exp(lg - lg.max())
+        p[h, sel] = w / w.sum()
+    weight = (p * p).sum(axis=0)
+    # full depth: textbook attention over each head's rows with the 4-bit values
+    full = o.attend_vdepth(q, k, vscales, vplanes, uidx, umask, 4 * 25)
+    assert np.all(full["depth"] == 4)
+    assert np.allclose(full["weight"], weight, rtol=1e-12, atol=1e-15)
+    c4 = exact_row_codes(v[uidx], 4)
+    s = np.array([block_scale(float(np.max(np.abs(bf16_value(v[i]))))) for i in uidx])
+    vhat4 = s[:, None] * (c4 - 7.5)
+    assert np.allclose(full["out"], p @ vhat4, rtol=1e-12, atol=1e-12)
+    # a partial budget: the depths are the greedy allocation of the weights,
+    # each row read through its own prefix
+    part = o.attend_vdepth(q, k, vscales, vplanes, uidx, umask, 37)
+    t = part["depth"].astype(np.int64)
+    assert int(t.sum()) == 37
+    assert np.array_equal(part["depth"], o.v_alloc(weight, 37)[0])
+    vhat = np.zeros((25, D))
+    for r in range(25):
+        if t[r]:
+            ct = exact_row_codes(v[uidx[r]:uidx[r] + 1], int(t[r]))[0]
+            vhat[r] = s[r] * ((ct + 0.5) * 2.0 ** (4 - t[r]) - 8.0)
+    assert np.allclose(part["out"], p @ vhat, rtol=1e-12, atol=1e-12)
+    # the heaviest row is read deepest
+    assert t[int(np.argmax(weight))] == t.max()
+
+
 ALL_PINS = [pin_fp16, pin_codes_exact, pin_prefix_quantiser, pin_special_values, pin_bit_order_golden,
             pin_scores, pin_alloc_bruteforce, pin_alloc_golden, pin_fixed_depths, pin_calibrated_channels,
-            pin_basis, pin_topk, pin_union, pin_attention]
+            pin_basis, pin_topk, pin_union, pin_attention, pin_value_codes, pin_value_bit_order_golden,
+            pin_value_alloc_bruteforce, pin_value_attention]

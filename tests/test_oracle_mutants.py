@@ -3,7 +3,9 @@
 pin.  The mistakes are plausible slips in reading the Fathom page: bit or plane
 order, floor vs round, the mid-rise half step, the scale's cost, q^2 vs |q|,
 tie rules, the 1/sqrt(D) factor, the union mask, stop vs skip, the
-calibration statistic and the basis orientation."""
+calibration statistic, the basis orientation, and in the ReadKV page's
+value stage the weight (squared probabilities), its tie rule and the
+channel order of a value plane."""
 import pytest
 
 from pins import ALL_PINS
@@ -22,6 +24,9 @@ MUTANTS = {
     11: "calibrated channel sets rank by mean |q| alone",
     12: "calibrated channel sets average q^2 instead of |q|",
     13: "basis applied transposed",
+    14: "value-row weights sum the attention probabilities, not their squares",
+    15: "value-depth ties go to the higher row",
+    16: "value planes hold the channels of a word in reverse order",
 }
 
 
