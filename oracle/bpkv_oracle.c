@@ -577,13 +577,14 @@ int32_t or_v_alloc(int32_t n_rows, const double *a, int32_t budget, uint8_t *dep
  * over its own rows with exact bf16 keys: p_h(r) = softmax_r(q_h . k / sqrt(D)).
  * The weight of a row is a_r = sum_h p_h(r)^2 (ReadKV page, section 5.3: squared
  * attention probabilities summed over the query heads sharing the KV head, head
- * scale coefficient 1), depths come from or_v_alloc, and
+ * scale coefficient 1), depths come from or_v_alloc (or are taken from
+ * depth_in when it is not NULL, to evaluate another allocation), and
  * o_h = sum_r p_h(r) vhat_r(t_r).  Everything in double.  Outputs: depth[n_u],
  * weight[n_u] (a_r), out[G][D].
  */
 void or_attend_vdepth(int32_t D, int32_t G, const float *q, const uint16_t *k_rows, const uint16_t *vscales,
                       const uint64_t *vplanes, const int32_t *uidx, const uint8_t *umask, int32_t n_u,
-                      int32_t budget_v, uint8_t *depth, double *weight, double *out) {
+                      int32_t budget_v, const uint8_t *depth_in, uint8_t *depth, double *weight, double *out) {
   const double scale = 1.0 / sqrt((double)D);
   double *p = (double *)malloc(sizeof(double) * (size_t)(n_u > 0 ? n_u : 1) * (size_t)G);
   double *row = (double *)malloc(sizeof(double) * (size_t)D);
@@ -609,7 +610,11 @@ void or_attend_vdepth(int32_t D, int32_t G, const float *q, const uint16_t *k_ro
     for (int32_t h = 0; h < G; ++h) acc += (OR_MUTANT == 14) ? p[h * n_u + r] : p[h * n_u + r] * p[h * n_u + r];
     weight[r] = acc;
   }
-  or_v_alloc(n_u, weight, budget_v, depth);
+  if (depth_in) {
+    for (int32_t r = 0; r < n_u; ++r) depth[r] = depth_in[r] > 4 ? 4 : depth_in[r];
+  } else {
+    or_v_alloc(n_u, weight, budget_v, depth);
+  }
   for (int64_t e = 0; e < (int64_t)G * D; ++e) out[e] = 0.0;
   for (int32_t r = 0; r < n_u; ++r) {
     or_v_row(D, vscales, vplanes, uidx[r], depth[r], row);

@@ -80,7 +80,7 @@ def _bind(path: str) -> ctypes.CDLL:
     L.or_v_row.restype = None
     L.or_v_alloc.argtypes = [i32, P, i32, P]
     L.or_v_alloc.restype = i32
-    L.or_attend_vdepth.argtypes = [i32, i32, P, P, P, P, P, P, i32, i32, P, P, P]
+    L.or_attend_vdepth.argtypes = [i32, i32, P, P, P, P, P, P, i32, i32, P, P, P, P]
     L.or_attend_vdepth.restype = None
     return L
 
@@ -247,8 +247,9 @@ class Oracle:
         return depth, int(used)
 
     def attend_vdepth(self, q: np.ndarray, k_rows: np.ndarray, vscales: np.ndarray, vplanes: np.ndarray,
-                      uidx: np.ndarray, umask: np.ndarray, budget_v: int) -> dict:
-        """Stage 2 over one KV head's union: weights, value depths, output [G][D]."""
+                      uidx: np.ndarray, umask: np.ndarray, budget_v: int, depth_in: np.ndarray | None = None) -> dict:
+        """Stage 2 over one KV head's union: weights, value depths (allocated, or
+        ``depth_in`` when given), output [G][D]."""
         q = _c(q, np.float32)
         k_rows = _c(k_rows, np.uint16)
         vscales = _c(vscales, np.uint16)
@@ -260,8 +261,9 @@ class Oracle:
         depth = np.zeros(n_u, dtype=np.uint8)
         weight = np.zeros(n_u, dtype=np.float64)
         out = np.zeros((G, D), dtype=np.float64)
+        din = None if depth_in is None else _c(depth_in, np.uint8)
         self.L.or_attend_vdepth(D, G, _p(q), _p(k_rows), _p(vscales), _p(vplanes), _p(uidx), _p(umask), n_u,
-                                int(budget_v), _p(depth), _p(weight), _p(out))
+                                int(budget_v), None if din is None else _p(din), _p(depth), _p(weight), _p(out))
         return dict(depth=depth, weight=weight, out=out)
 
     def decode_unit(self, k_bits: np.ndarray, v_bits: np.ndarray, q: np.ndarray, sigma2: np.ndarray,

@@ -701,6 +701,18 @@ def pin_value_attention(o):
     assert np.allclose(part["out"], p @ vhat, rtol=1e-12, atol=1e-12)
     # the heaviest row is read deepest
     assert t[int(np.argmax(weight))] == t.max()
+    # given depths: the same output as the allocation that produced them, and
+    # any other depth vector is read through each row's own prefix too
+    again = o.attend_vdepth(q, k, vscales, vplanes, uidx, umask, 0, depth_in=part["depth"])
+    assert np.array_equal(again["out"], part["out"]) and np.array_equal(again["depth"], part["depth"])
+    other = rng.integers(0, 5, size=25).astype(np.uint8)
+    got = o.attend_vdepth(q, k, vscales, vplanes, uidx, umask, 0, depth_in=other)
+    vo = np.zeros((25, D))
+    for r in range(25):
+        if other[r]:
+            ct = exact_row_codes(v[uidx[r]:uidx[r] + 1], int(other[r]))[0]
+            vo[r] = s[r] * ((ct + 0.5) * 2.0 ** (4 - int(other[r])) - 8.0)
+    assert np.allclose(got["out"], p @ vo, rtol=1e-12, atol=1e-12)
 
 
 ALL_PINS = [pin_fp16, pin_codes_exact, pin_prefix_quantiser, pin_special_values, pin_bit_order_golden,
