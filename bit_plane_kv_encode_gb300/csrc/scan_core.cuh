@@ -427,10 +427,10 @@ static_assert(kWideGroups >= 5, "a wide step must hold the single-pass plans of 
 // u32 words per staged plane row for steps of `sub` chunks.
 __host__ __device__ constexpr int row_pitch(int sub, bool host) { return host ? 2 * kScanBlocks * sub : kRowPitch; }
 // Placement of the pieces of staged row r of a host cache (see above).
-__device__ __forceinline__ int swz_piece(int r, int sub) { return sub == 1 ? (r >> 1) & 1 : r & 3; }
-__device__ __forceinline__ int swz_half(int r) { return (r >> 2) & 1; }
+__host__ __device__ __forceinline__ int swz_piece(int r, int sub) { return sub == 1 ? (r >> 1) & 1 : r & 3; }
+__host__ __device__ __forceinline__ int swz_half(int r) { return (r >> 2) & 1; }
 // u32 word of 16-byte part q (0 .. 4 sub - 1) of staged row r
-__device__ __forceinline__ int staged_word(int r, int q, int sub, bool host) {
+__host__ __device__ __forceinline__ int staged_word(int r, int q, int sub, bool host) {
   if (!host) return r * kRowPitch + 4 * q;
   return r * row_pitch(sub, true) + ((4 * q) ^ (8 * swz_piece(r, sub) + 4 * swz_half(r)));
 }
