@@ -327,13 +327,16 @@ void or_rotate_keys(int32_t D, int64_t n, const uint16_t *k_bits, const float *R
 
 /* score[h][i] = sum_j q_hj khat_ij(t_j) for every token i < n and query head h,
  * in double, channels in index order; no 1/sqrt(D) factor (it does not change
- * the ranking).  Reads only planes p < t_j and the scales of channels t_j > 0. */
+ * the ranking).  Reads only planes p < t_j and the scales of channels t_j > 0.
+ * A code has four planes, so a depth value above 4 is read as 4 (reading:
+ * the Fathom page's depth ranges over 0..4 bits; larger values read the
+ * whole code, never past it). */
 void or_scores(int64_t n, int32_t D, int32_t G, const uint16_t *scales, const uint64_t *planes,
                int64_t nb_cap, const uint8_t *depth, const float *q, double *score) {
   for (int64_t i = 0; i < n; ++i) {
     for (int32_t h = 0; h < G; ++h) score[(int64_t)h * n + i] = 0.0;
     for (int32_t j = 0; j < D; ++j) {
-      int t = depth[j];
+      int t = depth[j] > 4 ? 4 : depth[j];
       if (t == 0) continue;
       double s = or_fp16_value(scales[(int64_t)j * nb_cap + i / 64]);
       double kh = or_dequant(s, or_prefix_code(planes, nb_cap, j, t, i), t);

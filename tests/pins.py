@@ -244,6 +244,15 @@ def pin_scores(o):
     k2[:, 7] = bf16_bits_of(rng.standard_normal(n) * 50)
     s2, p2 = o.encode(k2, 3)
     assert np.array_equal(o.scores(n, scales, planes, depth, q), o.scores(n, s2, p2, depth, q))
+    # a code has four planes: depth values above 4 read the whole code (the
+    # full-depth closed form above), never the next channel's planes
+    for big in (5, 17, 255):
+        depth = rng.integers(0, 5, D).astype(np.uint8)
+        depth[rng.choice(D, 20, replace=False)] = big
+        got = o.scores(n, scales, planes, depth, q)
+        want = q.astype(np.float64) @ dequant_direct(k, np.minimum(depth, 4)).T
+        scale = np.abs(q).astype(np.float64) @ np.abs(dequant_direct(k, np.minimum(depth, 4))).T
+        assert np.all(np.abs(got - want) <= 1e-12 * (scale + 1e-300)), (big, np.max(np.abs(got - want)))
 
 
 # ------------------------------------------------------------------ depths
