@@ -12,14 +12,13 @@ import ctypes
 
 from ._binding import (  # noqa: F401
     BpkvError, bpkv_alloc_depths, bpkv_cache, bpkv_calibrate_channels, bpkv_clear_status, bpkv_decode_step,
-    bpkv_dense_attend, bpkv_encode_append, bpkv_fixed_depths, bpkv_read_status, bpkv_rotate, bpkv_scan, bpkv_scan_topk, bpkv_scan_topk_noalloc, bpkv_sparse_attend,
-    bpkv_status_string, bpkv_step_args, bpkv_step_fused, bpkv_topk, bpkv_union, bpkv_version, bpkv_workspace_size, header_symbols, load)
+    bpkv_dense_attend, bpkv_encode_append, bpkv_fixed_depths, bpkv_read_status, bpkv_rotate, bpkv_scan, bpkv_scan_topk, bpkv_scan_topk_noalloc, bpkv_selftest_wait, bpkv_sparse_attend,
+    bpkv_status_string, bpkv_step_args, bpkv_topk, bpkv_union, bpkv_version, bpkv_workspace_size, header_symbols, load)
 
 HEAD_DIM = 128
 WS_SCAN_TOPK, WS_ATTEND, WS_DENSE, WS_STEP = 1, 2, 4, 8
 DEPTH_WATERFILL, DEPTH_FIXED, DEPTH_DENSE, DEPTH_GIVEN = 0, 1, 2, 3
-DEV_OVERFLOW, DEV_SELECT = 1, 2
-STEP_FUSED, STEP_TAIL = 1, 2
+DEV_OVERFLOW, DEV_SELECT, DEV_TIMEOUT = 1, 2, 4
 
 
 class Cache:

@@ -50,6 +50,7 @@ _SIGS = {
     "bpkv_workspace_size": ([P, i32, i32], sz),
     "bpkv_clear_status": ([P, P], ctypes.c_int),
     "bpkv_read_status": ([P, P, P], ctypes.c_int),
+    "bpkv_selftest_wait": ([P, i32, i32, P], ctypes.c_int),
     "bpkv_encode_append": ([P, P, P, i32, P], ctypes.c_int),
     "bpkv_alloc_depths": ([P, P, P, P, P, P], ctypes.c_int),
     "bpkv_fixed_depths": ([P, P, i32, i32, P, P], ctypes.c_int),
@@ -63,7 +64,6 @@ _SIGS = {
     "bpkv_sparse_attend": ([P, P, P, P, P, i32, P, P, sz, P], ctypes.c_int),
     "bpkv_dense_attend": ([P, P, P, P, sz, P], ctypes.c_int),
     "bpkv_decode_step": ([P, i32, P, P, sz, P], ctypes.c_int),
-    "bpkv_step_fused": ([P, i32, i32, i32, i32], ctypes.c_int),
 }
 
 _lib = None
@@ -147,6 +147,11 @@ def bpkv_read_status(ws, stream=None) -> int:
     return int(st.value)
 
 
+def bpkv_selftest_wait(ws, arrivals: int, spin_limit: int, stream=None):
+    return _check("bpkv_selftest_wait", load().bpkv_selftest_wait(_ptr(ws), int(arrivals), int(spin_limit),
+                                                                  _stream(stream)))
+
+
 def bpkv_encode_append(cache, k_new, v_new, t_new: int, stream=None):
     return _check("bpkv_encode_append",
                   load().bpkv_encode_append(ctypes.byref(cache), _ptr(k_new), _ptr(v_new), int(t_new),
@@ -217,10 +222,6 @@ def bpkv_dense_attend(cache, q, out, ws, ws_bytes: int, stream=None):
     return _check("bpkv_dense_attend",
                   load().bpkv_dense_attend(ctypes.byref(cache), _ptr(q), _ptr(out), _ptr(ws), int(ws_bytes),
                                            _stream(stream)))
-
-
-def bpkv_step_fused(cache, k: int, n_sink: int, n_recent: int, depth_rule: int) -> bool:
-    return bool(load().bpkv_step_fused(ctypes.byref(cache), int(k), int(n_sink), int(n_recent), int(depth_rule)))
 
 
 def bpkv_decode_step(layers_array, n_layers: int, args, ws, ws_bytes: int, stream=None):

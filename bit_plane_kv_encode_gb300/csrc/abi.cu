@@ -40,30 +40,11 @@ cudaError_t launch_attend(const bpkv_cache& c, const float* q, const int32_t* ui
                           cudaStream_t st);
 size_t attend_part_bytes(const bpkv_cache& c, int64_t rows, bool dense);
 cudaError_t launch_bump_len(const bpkv_cache& c, int32_t t_new, cudaStream_t st);
-bool fused_eligible(const bpkv_cache& c, int32_t k, int32_t n_sink, int32_t n_recent, int32_t depth_rule);
-bool tail_eligible(const bpkv_cache& c, int32_t k, int32_t n_sink, int32_t n_recent);
-cudaError_t launch_select_attend(const bpkv_cache& c, const float* scores, int64_t ld, const float* q, int32_t k,
-                                 int32_t n_sink, int32_t n_recent, float* out, int32_t* idx_out, cudaStream_t st);
-cudaError_t launch_decode_fused(const bpkv_cache& c, const uint16_t* k_new, const uint16_t* v_new, const float* q,
-                                const float* sigma2, const int32_t* budget_q, int32_t depth_rule,
-                                int32_t fixed_channels, int32_t fixed_depth, int32_t k, int32_t n_sink,
-                                int32_t n_recent, float* out, uint8_t* depths_out, int32_t* idx_out,
-                                cudaStream_t st);
-}  // namespace bpkv
-
-using namespace bpkv;
+cudaError_t launch_selftest_wait(uint32_t* bar, uint32_t count, uint32_t limit, int32_t* status, cudaStream_t st);
 
 namespace {
-
-constexpr size_t kAlign = 256;
-constexpr int32_t kMaxK = 8192;
-constexpr int32_t kMaxUnion = 16384;
-
-size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
-
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+}  // namespace
 
 int check_cache(const bpkv_cache* c) {
   if (!c) return BPKV_EINVAL;
@@ -85,6 +66,19 @@ int check_k(int32_t k, int32_t n_sink, int32_t n_recent) {
   if ((int64_t)n_sink + n_recent > k) return BPKV_EINVAL;
   return BPKV_OK;
 }
+
+}  // namespace bpkv
+
+using namespace bpkv;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int32_t kMaxUnion = 16384;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 // Workspace layout: status word, then the buffers each call family needs.
 struct Layout {
@@ -210,6 +204,15 @@ int bpkv_read_status(const void* ws, int32_t* status, void* stream) {
   return *status ? BPKV_EDEVICE : BPKV_OK;
 }
 
+int bpkv_selftest_wait(void* ws, int32_t arrivals, int32_t spin_limit, void* stream) {
+  if (!ws || !aligned(ws, kAlign)) return BPKV_ENOWORKSPACE;
+  if (arrivals < 1 || arrivals > 1024 || spin_limit < 1 || (uint32_t)spin_limit > kSpinLimit) return BPKV_EINVAL;
+  // the barrier counter lives in the workspace's first 256 bytes, after the status word
+  uint32_t* bar = reinterpret_cast<uint32_t*>(at(ws, 64));
+  return cuda_status(launch_selftest_wait(bar, (uint32_t)arrivals, (uint32_t)spin_limit, static_cast<int32_t*>(ws),
+                                          as_stream(stream)));
+}
+
 int bpkv_encode_append(bpkv_cache* c, const uint16_t* k_new, const uint16_t* v_new, int32_t t_new, void* stream) {
   BPKV_TRY(check_cache(c));
   if (t_new < 1 || !k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)) return BPKV_EINVAL;
@@ -299,11 +302,6 @@ int bpkv_dense_attend(const bpkv_cache* c, const float* q, float* out, void* ws,
                                    out, true, as_stream(stream)));
 }
 
-int bpkv_step_fused(const bpkv_cache* c, int32_t k, int32_t n_sink, int32_t n_recent, int32_t depth_rule) {
-  if (check_cache(c) != BPKV_OK || check_k(k, n_sink, n_recent) != BPKV_OK) return 0;
-  return fused_eligible(*c, k, n_sink, n_recent, depth_rule) ? 1 : 0;
-}
-
 int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args* a, void* ws, size_t ws_bytes,
                      void* stream) {
   if (!layers || n_layers < 1 || !a) return BPKV_EINVAL;
@@ -315,7 +313,7 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
       return BPKV_EINVAL;
     if (x.n_max + 1 > x.cap_tokens) return BPKV_EINVAL;
   }
-  if (!a->k_new || !a->v_new || !a->q || !a->out) return BPKV_EINVAL;
+  if (!a->k_new || !a->v_new || !a->q || !a->out || a->flags != 0) return BPKV_EINVAL;
   if (!aligned(a->k_new, 16) || !aligned(a->v_new, 16)) return BPKV_EINVAL;
   const bool dense = a->depth_rule == BPKV_DEPTH_DENSE;
   if (a->depth_rule == BPKV_DEPTH_WATERFILL && (!a->sigma2 || !a->budget_q)) return BPKV_EINVAL;
@@ -349,19 +347,6 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
     const float* q = a->q + (size_t)l * NH * G * kD;
     float* out = a->out + (size_t)l * NH * G * kD;
     BPKV_TRY(mark(l, 0));
-    if (!dense && (a->flags & BPKV_STEP_FUSED) && fused_eligible(c, a->k, a->n_sink, a->n_recent, a->depth_rule)) {
-      uint8_t* dout = a->depths_out ? a->depths_out + (size_t)l * NH * kD : nullptr;
-      int32_t* iout = a->idx_out ? a->idx_out + (size_t)l * NH * G * a->k : nullptr;
-      const float* s2 = a->sigma2 ? a->sigma2 + (size_t)l * NH * kD : nullptr;
-      BPKV_TRY(cuda_status(launch_decode_fused(c, kn, vn, q, s2, a->budget_q, a->depth_rule, a->fixed_channels,
-                                               a->fixed_depth, a->k, a->n_sink, a->n_recent, out, dout, iout,
-                                               st)));
-      for (int e = 1; e <= 5; ++e) BPKV_TRY(mark(l, e));
-      BPKV_TRY(cuda_status(launch_bump_len(c, 1, st)));
-      BPKV_TRY(mark(l, 6));
-      c.n_max += 1;
-      continue;
-    }
     uint8_t* depths = a->depths_out ? a->depths_out + (size_t)l * NH * kD : at(ws, L.depths);
     int32_t* idx = a->idx_out ? a->idx_out + (size_t)l * NH * G * a->k : reinterpret_cast<int32_t*>(at(ws, L.idx));
     int32_t* uidx = reinterpret_cast<int32_t*>(at(ws, L.uidx));
@@ -372,31 +357,13 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
     void* plan = at(ws, L.plan);
     const SelBufs sb = sel_bufs(ws, L);
     const float* s2 = a->sigma2 ? a->sigma2 + (size_t)l * NH * kD : nullptr;
-    const bool tail = !dense && a->depth_rule != BPKV_DEPTH_GIVEN && !c.basis && (a->flags & BPKV_STEP_TAIL) &&
-                      tail_eligible(c, a->k, a->n_sink, a->n_recent);
-    if (dense || tail) {
-      // append (and length update) first, then the stages one by one
+    if (dense) {
+      // append (and length update) first, then attention over every row
       BPKV_TRY(cuda_status(launch_encode_append(c, kn, vn, 1, st)));
       c.n_max += 1;
-      if (dense) {
-        for (int e = 1; e <= 5; ++e) BPKV_TRY(mark(l, e));
-        BPKV_TRY(cuda_status(launch_attend(c, q, nullptr, nullptr, nullptr, 1, part, out, true, st)));
-        BPKV_TRY(mark(l, 6));
-        continue;
-      }
-      BPKV_TRY(mark(l, 1));
-      if (a->depth_rule == BPKV_DEPTH_WATERFILL)
-        BPKV_TRY(cuda_status(launch_alloc_depths(c, q, s2, a->budget_q, depths, st, tickets, plan, sb.hist, sb.ctr)));
-      else
-        BPKV_TRY(cuda_status(launch_fixed_depths(c, q, a->fixed_channels, a->fixed_depth, depths, st, tickets, plan,
-                                                 sb.hist, sb.ctr)));
-      BPKV_TRY(mark(l, 2));
-      BPKV_TRY(cuda_status(launch_scan(c, q, depths, scores, c.cap_tokens, st, plan, nullptr, 0, 0, 0, status)));
-      BPKV_TRY(mark(l, 3));
-      int32_t* iout = a->idx_out ? a->idx_out + (size_t)l * NH * G * a->k : nullptr;
-      BPKV_TRY(cuda_status(
-          launch_select_attend(c, scores, c.cap_tokens, q, a->k, a->n_sink, a->n_recent, out, iout, st)));
-      for (int e = 4; e <= 6; ++e) BPKV_TRY(mark(l, e));
+      for (int e = 1; e <= 5; ++e) BPKV_TRY(mark(l, e));
+      BPKV_TRY(cuda_status(launch_attend(c, q, nullptr, nullptr, nullptr, 1, part, out, true, st)));
+      BPKV_TRY(mark(l, 6));
       continue;
     }
     // append beside depths and plan in one launch; the new token counts in

@@ -13,6 +13,12 @@ namespace bpkv {
 constexpr int kD = BPKV_HEAD_DIM;   // channels per head
 constexpr int kBlock = 64;          // tokens per scale block / plane word
 constexpr int kPlanes = 4;          // bits per code
+constexpr int32_t kMaxK = 8192;     // largest per-head selection size
+
+// Host-side argument checks shared by the entry points (abi.cu): BPKV_OK or
+// the status an entry point returns before enqueueing anything.
+int check_cache(const bpkv_cache* c);
+int check_k(int32_t k, int32_t n_sink, int32_t n_recent);
 
 // Per-unit (sequence, KV head) base offsets of the cache arrays.
 struct Unit {

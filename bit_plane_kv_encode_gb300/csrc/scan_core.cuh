@@ -1,5 +1,5 @@
-// Device building blocks of the prefix-plane scan, shared by the stand-alone
-// scan kernel and the fused decode kernel.  See scan.cu for the method.
+// Device building blocks of the prefix-plane scan (the scan kernel and the
+// plan builder of the depth kernel).  See scan.cu for the method.
 #pragma once
 
 #include "common.cuh"
@@ -7,10 +7,8 @@
 namespace bpkv {
 
 constexpr int kScanBlocks = 8;                  // 64-token blocks per chunk
-constexpr int kStageBatch = 8;                  // independent global loads in flight per thread while staging
 constexpr int kScanThreads = 32 * kScanBlocks;  // one warp per block
 constexpr int kMaxGroups = 20;                  // 16 depth-4 groups + one partial group per other depth
-constexpr int kWordPitch = 2 * kScanBlocks + 1; // u32 words per staged row (odd: conflict-free)
 constexpr int kMaxSlots = 288;                  // padded channel slots over all groups
 // Groups are staged and scored in passes of at most kPassGroups groups and
 // kPassSlots slots (one pass for every budget up to about 300 bits per token).
@@ -57,14 +55,6 @@ struct PlanScratch {
   int warp_cnt[4][5];
 };
 
-template <int GP>
-struct ScanSmem {
-  uint32_t words[kPassGroups * 32 * kWordPitch];    // staged plane half-words of one pass
-  float u[kScanBlocks * kPassSlots * GP];           // [block][pass slots: group slots][head][slot]
-  ScanPlan<GP> P;
-  PlanScratch X;
-};
-
 // 32 x 32 bit transpose across the warp: on return bit r of lane l's word is
 // bit l of lane r's input word.
 __device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, const uint32_t (&keep)[5],
@@ -94,54 +84,6 @@ __device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsign
   unsigned long long d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
-}
-
-// e (scaled by 2^pos) of field m of a depth-T group, from the shifted words.
-template <int T, int M>
-__device__ __forceinline__ float field_value(uint32_t xa, uint32_t xb) {
-  constexpr int pos = field_pos(T, M);
-  constexpr uint32_t mask = ((1u << T) - 1u) << pos;
-  constexpr bool use_a = (M * T + T <= 22);
-  const uint32_t src = use_a ? xa : xb;
-  const float f = __uint_as_float((src & mask) | 0x4B000000u);     // 2^23 + c 2^pos
-  constexpr float K = 8388608.f + ((float)(1 << (T - 1)) - 0.5f) * (float)(1u << pos);
-  return f - K;                                                    // (c - 2^(T-1) + 1/2) 2^pos, exact
-}
-
-// Accumulate the fields M and M+1 of one group into the head accumulators of
-// the two tokens of this lane.  acc*[h] hold (even-field, odd-field) partial sums.
-template <int T, int M, int GP>
-__device__ __forceinline__ void field_pair(uint32_t xa0, uint32_t xb0, uint32_t xa1, uint32_t xb1,
-                                           const float* __restrict__ ug, unsigned long long (&acc0)[GP],
-                                           unsigned long long (&acc1)[GP]) {
-  constexpr int P = Depth<T>::pitch;
-  const float e0a = field_value<T, M>(xa0, xb0);
-  const float e1a = field_value<T, M>(xa1, xb1);
-  float e0b = 0.f, e1b = 0.f;
-  if constexpr (M + 1 < Depth<T>::cap) {
-    e0b = field_value<T, M + 1>(xa0, xb0);
-    e1b = field_value<T, M + 1>(xa1, xb1);
-  }
-  const unsigned long long E0 = pack2(e0a, e0b), E1 = pack2(e1a, e1b);
-#pragma unroll
-  for (int h = 0; h < GP; ++h) {
-    const float2 uu = *reinterpret_cast<const float2*>(ug + h * P + M);
-    const unsigned long long U = pack2(uu.x, uu.y);
-    acc0[h] = ffma2(U, E0, acc0[h]);
-    acc1[h] = ffma2(U, E1, acc1[h]);
-  }
-}
-
-template <int T, int GP, int M = 0>
-__device__ __forceinline__ void group_fields(int cnt, uint32_t xa0, uint32_t xb0, uint32_t xa1, uint32_t xb1,
-                                             const float* __restrict__ ug, unsigned long long (&acc0)[GP],
-                                             unsigned long long (&acc1)[GP]) {
-  if constexpr (M < Depth<T>::cap) {
-    if (M < cnt) {
-      field_pair<T, M, GP>(xa0, xb0, xa1, xb1, ug, acc0, acc1);
-      group_fields<T, GP, M + 2>(cnt, xa0, xb0, xa1, xb1, ug, acc0, acc1);
-    }
-  }
 }
 
 // Transpose constants of this lane (see warp_transpose32).
@@ -269,125 +211,6 @@ __device__ void scan_store_plan(const ScanPlan<GP>& S, ScanPlan<GP>* __restrict_
   const uint4* s = reinterpret_cast<const uint4*>(&S);
   uint4* g = reinterpret_cast<uint4*>(dst);
   for (int e = threadIdx.x; e < (int)(sizeof(ScanPlan<GP>) / 16); e += blockDim.x) g[e] = s[e];
-}
-
-// Stage the plane words and block scales of groups [g0, g1) (slots [s0, s1))
-// for nbl (<= kScanBlocks) blocks starting at pl / sp (the unit's arrays
-// offset by the first block) and form u = s w for those slots.
-template <int GP>
-__device__ void scan_stage_pass(ScanSmem<GP>& S, const uint64_t* __restrict__ pl,
-                                const uint16_t* __restrict__ sp, int64_t nb_cap, int nbl, int g0, int g1) {
-  const int tid = threadIdx.x;
-  const ScanPlan<GP>& P = S.P;
-  const int s0 = P.grp_base[g0], s1 = g1 < P.n_groups ? (int)P.grp_base[g1] : P.n_slots;
-  const int ps = s1 - s0;
-  __syncthreads();  // the previous compute is done with words and u
-  // plane words, kStageBatch independent loads in flight per thread
-  const int n_w = (g1 - g0) * 32 * kScanBlocks;
-  for (int e0 = tid; e0 < n_w; e0 += kStageBatch * kScanThreads) {
-    uint64_t w[kStageBatch];
-#pragma unroll
-    for (int b = 0; b < kStageBatch; ++b) {
-      const int e = e0 + b * kScanThreads, r = e / kScanBlocks, lb = e % kScanBlocks;
-      const int row = e < n_w ? P.row_of_lane[g0 * 32 + r] : -1;
-      w[b] = (row >= 0 && lb < nbl) ? pl[(int64_t)row * nb_cap + lb] : 0ull;
-    }
-#pragma unroll
-    for (int b = 0; b < kStageBatch; ++b) {
-      const int e = e0 + b * kScanThreads, r = e / kScanBlocks, lb = e % kScanBlocks;
-      if (e < n_w) {
-        S.words[r * kWordPitch + 2 * lb] = (uint32_t)w[b];
-        S.words[r * kWordPitch + 2 * lb + 1] = (uint32_t)(w[b] >> 32);
-      }
-    }
-  }
-  // block scales times the slot weights: u = s w
-  const int n_u = kScanBlocks * ps;
-  for (int e0 = tid; e0 < n_u; e0 += kStageBatch * kScanThreads) {
-    uint16_t sb[kStageBatch];
-#pragma unroll
-    for (int b = 0; b < kStageBatch; ++b) {
-      const int e = e0 + b * kScanThreads, lb = e % kScanBlocks, slot = s0 + e / kScanBlocks;
-      const int ch = e < n_u ? P.slot_ch[slot] : -1;
-      sb[b] = (ch >= 0 && lb < nbl) ? sp[(int64_t)ch * nb_cap + lb] : (uint16_t)0;
-    }
-#pragma unroll
-    for (int b = 0; b < kStageBatch; ++b) {
-      const int e = e0 + b * kScanThreads, lb = e % kScanBlocks, slot = s0 + e / kScanBlocks;
-      if (e < n_u) {
-        const float sc = fp16_bits_to_float(sb[b]);
-        const int g = P.slot_grp[slot];
-        const int base = P.grp_base[g], m = slot - base, pitch = slot_pitch(P.grp_t[g]);
-        float* ud = S.u + (lb * ps + (base - s0)) * GP;
-#pragma unroll
-        for (int hh = 0; hh < GP; ++hh) ud[hh * pitch + m] = sc * P.w[(base + m) * GP + hh];
-      }
-    }
-  }
-  __syncthreads();
-}
-
-// Add groups [g0, g1) of the staged pass to this lane's accumulators: warp w
-// takes block w (w < nbl), lane the tokens lane and lane + 32 of it.
-template <int GP>
-__device__ __forceinline__ void scan_compute_pass(const ScanSmem<GP>& S, int g0, int g1,
-                                                  unsigned long long (&acc0)[GP], unsigned long long (&acc1)[GP]) {
-  const int lane = threadIdx.x & 31, lb = threadIdx.x >> 5;
-  uint32_t keep[5], rot[5];
-  transpose_consts(lane, keep, rot);
-  const ScanPlan<GP>& P = S.P;
-  const int s0 = P.grp_base[g0], s1 = g1 < P.n_groups ? (int)P.grp_base[g1] : P.n_slots;
-  const int ps = s1 - s0;
-  for (int g = g0; g < g1; ++g) {
-    const int d = P.grp_t[g], cnt = P.grp_cnt[g];
-    const uint32_t* wr = S.words + ((g - g0) * 32 + lane) * kWordPitch + 2 * lb;
-    const uint32_t x0 = warp_transpose32(wr[0], keep, rot);
-    const uint32_t x1 = warp_transpose32(wr[1], keep, rot);
-    const uint32_t xa0 = x0 << 1, xb0 = x0 >> 9, xa1 = x1 << 1, xb1 = x1 >> 9;
-    const float* ug = S.u + (lb * ps + (P.grp_base[g] - s0)) * GP;
-    switch (d) {
-      case 4: group_fields<4, GP>(cnt, xa0, xb0, xa1, xb1, ug, acc0, acc1); break;
-      case 3: group_fields<3, GP>(cnt, xa0, xb0, xa1, xb1, ug, acc0, acc1); break;
-      case 2: group_fields<2, GP>(cnt, xa0, xb0, xa1, xb1, ug, acc0, acc1); break;
-      default: group_fields<1, GP>(cnt, xa0, xb0, xa1, xb1, ug, acc0, acc1); break;
-    }
-  }
-}
-
-// Score one chunk of nbl (<= kScanBlocks) blocks starting at pl / sp: every
-// pass is staged and added in turn.  Scores of head g for the chunk's token x
-// go to out[g * ld + x], for x < n_valid; they are also left in v0 (token x)
-// and v1 (token x + 32).  Returns false for warps without a block.  The plan
-// must be in S.P.
-template <int GP>
-__device__ bool scan_chunk(ScanSmem<GP>& S, const uint64_t* __restrict__ pl, const uint16_t* __restrict__ sp,
-                           int64_t nb_cap, int nbl, int G, float* out, int64_t ld, int64_t n_valid,
-                           float (&v0)[GP], float (&v1)[GP]) {
-  const int lane = threadIdx.x & 31, lb = threadIdx.x >> 5;
-  const bool act = lb < nbl;
-  unsigned long long acc0[GP], acc1[GP];
-#pragma unroll
-  for (int hh = 0; hh < GP; ++hh) acc0[hh] = acc1[hh] = 0ull;
-  const int n_passes = S.P.n_passes;
-  for (int ps = 0; ps < n_passes; ++ps) {
-    const int g0 = S.P.pass_g[ps], g1 = S.P.pass_g[ps + 1];
-    scan_stage_pass<GP>(S, pl, sp, nb_cap, nbl, g0, g1);
-    if (act) scan_compute_pass<GP>(S, g0, g1, acc0, acc1);
-  }
-  if (!act) return false;
-  const int64_t x0 = (int64_t)lb * kBlock + lane;
-#pragma unroll
-  for (int hh = 0; hh < GP; ++hh) {
-    if (hh >= G) break;
-    float p0, p1, r0, r1;
-    unpack2(acc0[hh], p0, p1);
-    unpack2(acc1[hh], r0, r1);
-    v0[hh] = p0 + p1;
-    v1[hh] = r0 + r1;
-    if (x0 < n_valid) out[hh * ld + x0] = v0[hh];
-    if (x0 + 32 < n_valid) out[hh * ld + x0 + 32] = v1[hh];
-  }
-  return true;
 }
 
 // ---------------------------------------------------------------------------

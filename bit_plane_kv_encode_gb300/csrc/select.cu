@@ -299,15 +299,17 @@ __device__ void cut_refine(CutSmem& S, const float* __restrict__ sc, int64_t lo,
 }
 
 // Wait until `count` CTAs have arrived at *bar (thread 0 of each CTA arrives
-// once); bounded, records BPKV_DEV_TIMEOUT if it gives up.  Whole block.
-__device__ __forceinline__ void row_barrier(uint32_t* bar, uint32_t count, int32_t* status) {
+// once); bounded by `limit` rounds of ~100 ns, records BPKV_DEV_TIMEOUT if it
+// gives up.  Whole block.
+__device__ __forceinline__ void row_barrier(uint32_t* bar, uint32_t count, int32_t* status,
+                                            uint32_t limit = kSpinLimit) {
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
     atomicAdd(bar, 1u);
     uint32_t it = 0;
     while (*reinterpret_cast<volatile uint32_t*>(bar) < count) {
-      if (++it > kSpinLimit) {
+      if (++it > limit) {
         set_status(status, BPKV_DEV_TIMEOUT);
         break;
       }
@@ -777,6 +779,21 @@ cudaError_t launch_union(const bpkv_cache& c, const int32_t* idx, int32_t k, int
   }
   UnionArgs a{idx, uidx, umask, ucount, c.group, k};
   return launch_pdl(k_union, dim3(c.n_seq * c.n_kv_heads), dim3(kSelThreads), sm, st, a);
+}
+
+
+// Self-test of the bounded wait: one CTA arrives at a fresh barrier that
+// expects `count` arrivals and waits there as the cut's CTAs do (nothing else
+// arrives when count > 1, so the wait runs out after `limit` rounds and
+// records BPKV_DEV_TIMEOUT).
+__global__ void k_selftest_wait(uint32_t* bar, uint32_t count, uint32_t limit, int32_t* status) {
+  if (threadIdx.x == 0) *bar = 0u;
+  row_barrier(bar, count, status, limit);
+}
+
+cudaError_t launch_selftest_wait(uint32_t* bar, uint32_t count, uint32_t limit, int32_t* status, cudaStream_t st) {
+  k_selftest_wait<<<1, 32, 0, st>>>(bar, count, limit, status);
+  return cudaGetLastError();
 }
 
 }  // namespace bpkv

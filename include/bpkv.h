@@ -91,7 +91,7 @@ extern "C" {
  * with q R (sigma2 is then the variance in the basis), and the rows and the
  * exact attention stay in the original channels.  The stand-alone depth, scan
  * and top-k calls take q already in the basis (bpkv_rotate).  Set the basis
- * before the first append; the fused and tail step paths do not support it.
+ * before the first append.
  */
 typedef struct bpkv_cache {
   int32_t n_seq;
@@ -129,6 +129,19 @@ int bpkv_clear_status(void *ws, void *stream);
 int bpkv_read_status(const void *ws, int32_t *status, void *stream);
 
 const char *bpkv_status_string(int status);
+
+/*
+ * Self-test of failure detection (the pages have no counterpart: this checks
+ * the library's own bounded waits).  One CTA waits, as the selection's CTAs
+ * do for one another, at a barrier that expects `arrivals` CTAs; only it
+ * arrives, so for arrivals > 1 the wait gives up after spin_limit rounds of
+ * about 100 ns (1 .. 2^21), records BPKV_DEV_TIMEOUT in the status word of
+ * `ws` (device memory, 256-byte aligned, at least 256 bytes; the barrier
+ * counter uses bytes 64..67) and returns, leaving the context usable.
+ * arrivals = 1 completes at once.  BPKV_EINVAL for arrivals outside 1..1024
+ * or spin_limit outside 1 .. 2^21.
+ */
+int bpkv_selftest_wait(void *ws, int32_t arrivals, int32_t spin_limit, void *stream);
 int32_t bpkv_version(void);
 
 /* ------------------------------------------------------------- encode (F1, F2) */
@@ -238,17 +251,21 @@ int bpkv_scan_topk(const bpkv_cache *c, const float *q, const uint8_t *depths, i
  * GPU's memory, or a loop that must not pay the device-wide synchronisation a
  * cudaMalloc/cudaFree can cause.  The Fathom page has no counterpart of this
  * call; its results are identical to bpkv_scan_topk's.
- * The scratch (scores and selection buffers) is a fixed 16 MiB array built
- * into the library, held on every GPU that loads the library until the
- * process exits; requests needing more (rows = N * H * G; rows *
- * (4 * round_up(n_max, 64) + 40984) bytes plus under 1 KiB of alignment
- * > 16 MiB) return BPKV_ENOWORKSPACE.  The call allocates nothing (no
- * cudaMalloc, cudaFree or allocating library routine); it enqueues a memset of
- * the selection counters.  Its first call on a device looks up the
- * array's device address once (with that device current); make that first
- * call before any stream capture.  All calls on a device share the one array,
- * so calls whose work overlaps on the GPU (other streams, other threads) race
- * and must be serialised by the caller.  No device status word is reported.
+ * The scratch (a status word, scores and selection buffers) is a fixed 16 MiB
+ * array built into the library, held on every GPU that loads the library
+ * until the process exits; requests needing more (rows = N * H * G; 256 +
+ * rows * (4 * round_up(n_max, 64) + 40984) bytes plus under 1 KiB of
+ * alignment > 16 MiB) return BPKV_ENOWORKSPACE.  The call allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library routine); it enqueues
+ * memsets of the status word and the selection counters.  Every call looks
+ * up the array's device address on the current device; the first call on a
+ * device also loads the library's kernels there, so make it before any
+ * stream capture.  After a device reset the next call finds the array again.
+ * All calls on a device share the one array, so calls whose work overlaps on
+ * the GPU (other streams, other threads) race and must be serialised by the
+ * caller.  No device status word is reported: if the selection's bounded wait
+ * for its other CTAs gives up (BPKV_DEV_TIMEOUT on the workspace call), idx
+ * can be wrong without any error returned.
  */
 int bpkv_scan_topk_noalloc(const bpkv_cache *c, const float *q, const uint8_t *depths, int32_t k,
                            int32_t n_sink, int32_t n_recent, int32_t *idx, void *stream);
@@ -306,38 +323,19 @@ typedef struct bpkv_step_args {
   void *const *stage_events;/* optional [L][BPKV_STAGE_EVENTS] cudaEvent_t, NULL to skip:
                                recorded on `stream` (as external events, so they also
                                time graph replays) before encode, depths, scan, top-k,
-                               union, attention and after attention; on the fused path
-                               the first five stages are the fused kernel and the
-                               last one the sequence-length update */
-  int32_t flags;            /* BPKV_STEP_* */
+                               union, attention and after attention */
+  int32_t flags;            /* reserved: 0 */
   const uint8_t *depths_in; /* [L][N][H][D] BPKV_DEPTH_GIVEN: depth of every channel (values above
                                4 read as 4; depths_out, if given, receives them as read) */
 } bpkv_step_args;
 
 #define BPKV_STAGE_EVENTS 7
-#define BPKV_STEP_FUSED 1       /* use the fused cluster kernel when bpkv_step_fused allows it */
-#define BPKV_STEP_TAIL 2        /* after the scan, one cluster kernel for top-k, union and
-                                   attention instead of three separate kernels */
-
-/*
- * 1 when bpkv_decode_step, given BPKV_STEP_FUSED, can run a layer of this cache
- * as one fused kernel per pass (a thread-block cluster per (sequence, KV head)
- * doing append, depths, scan, top-k, union and attention in shared and
- * distributed shared memory), 0 when it runs the per-stage kernels.  Fused needs: not dense, G <= 8, at most
- * 40960 tokens after the append (5120 per CTA), k - n_sink - n_recent <= 988,
- * and the shared memory the group size implies.  Results are identical to the
- * per-stage path's up to float rounding of the attention.
- */
-int bpkv_step_fused(const bpkv_cache *c, int32_t k, int32_t n_sink, int32_t n_recent, int32_t depth_rule);
 
 /*
  * One decode step over n_layers layers (each its own bpkv_cache, same shapes):
  * append the new token (encode), choose depths, scan + top-k, union, sparse
  * attention (or dense attention for BPKV_DEPTH_DENSE).  Every layer's n_max is
- * raised by one.  Needs workspace BPKV_WS_STEP.  With BPKV_STEP_TAIL, selection,
- * union and attention after the scan run as one kernel with a thread-block
- * cluster per (sequence, KV head) when k - n_sink - n_recent <= 988 and G <= 8;
- * the selections are the same either way.
+ * raised by one.  Needs workspace BPKV_WS_STEP.  BPKV_EINVAL when flags is not 0.
  */
 int bpkv_decode_step(bpkv_cache *layers, int32_t n_layers, const bpkv_step_args *a, void *ws,
                      size_t ws_bytes, void *stream);

@@ -73,3 +73,15 @@ def test_invalid_arguments_rejected_on_host(L):
     assert L.bpkv_dense_attend(ctypes.byref(c), fake, fake, fake, 10, None) == ENOWS
     assert L.bpkv_decode_step(None, 1, None, fake, 0, None) == EINVAL
     assert L.bpkv_status_string(-1) == b"invalid argument"
+    # the bounded-wait self-test: workspace and limits checked on the host
+    assert L.bpkv_selftest_wait(None, 2, 100, None) == ENOWS
+    assert L.bpkv_selftest_wait(ctypes.c_void_p((1 << 20) + 16), 2, 100, None) == ENOWS
+    assert L.bpkv_selftest_wait(fake, 0, 100, None) == EINVAL
+    assert L.bpkv_selftest_wait(fake, 2, 0, None) == EINVAL
+    assert L.bpkv_selftest_wait(fake, 2, (1 << 21) + 1, None) == EINVAL
+    # the step's reserved flags must be 0
+    from bit_plane_kv_encode_gb300 import bpkv_step_args
+    a = bpkv_step_args(fake.value, fake.value, fake.value, fake.value, fake.value, 0, 0, 0, 512, 4, 32, fake.value,
+                       None, None, None, 1, None)
+    arr = (type(c) * 1)(c)
+    assert L.bpkv_decode_step(arr, 1, ctypes.byref(a), fake, 1 << 30, None) == EINVAL

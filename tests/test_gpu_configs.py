@@ -18,26 +18,29 @@ def pk():
     return m
 
 
-@pytest.mark.parametrize("flags", [1, 2, 0], ids=["fused", "tail", "split"])
-def test_tiny_all_units(pk, orc, flags):
+@pytest.mark.parametrize("k", [64, 100], ids=["k64_fixed_included", "k100_literal"])
+def test_tiny_all_units(pk, orc, k):
+    """The tiny layer at k = 64 (the 36 sink and recent tokens counted in k)
+    and at the literal "64 per query head plus 4 sinks and 32 recent", k = 100."""
+    import dataclasses
     from workload import CONFIGS, gen_layer
-    cfg = CONFIGS["tiny"]
+    cfg = dataclasses.replace(CONFIGS["tiny"], k=k)
     inp = gen_layer(cfg, 0, device="cpu")
-    cache, d, idx, out = decode_one_layer(inp, cfg, flags=flags)
-    same, _ = check_unit(orc, cfg, inp, cache, d, idx, out, 0, 0, what="tiny")
+    cache, d, idx, out = decode_one_layer(inp, cfg)
+    same, _ = check_unit(orc, cfg, inp, cache, d, idx, out, 0, 0, what=f"tiny k{k}")
     assert same >= 3
+    # 36 fixed tokens plus k - 36 chosen ones per head
+    assert all(int((idx[0, 0, g] >= 0).sum()) == k for g in range(cfg.group))
 
 
-@pytest.mark.parametrize("flags", [1, 2, 0], ids=["fused", "tail", "split"])
 @pytest.mark.parametrize("budget", [68, 92, 136])
-def test_qwen3_layer_all_units(pk, orc, budget, flags):
+def test_qwen3_layer_all_units(pk, orc, budget):
     from workload import CONFIGS, gen_layer
     cfg = CONFIGS["qwen3_8b_layer"]
     inp = gen_layer(cfg, 0, device="cuda")
     inp.k, inp.v = inp.k.cpu(), inp.v.cpu()
     b = torch.full((cfg.n_seq,), budget, dtype=torch.int32)
-    cache, d, idx, out = decode_one_layer(inp, cfg, budgets=b, flags=flags)
-    assert pk.bpkv_step_fused(cache.c, cfg.k, cfg.n_sink, cfg.n_recent, 0)
+    cache, d, idx, out = decode_one_layer(inp, cfg, budgets=b)
     same_total, found = 0, 0
     for h in range(cfg.n_kv_heads):
         same, _ = check_unit(orc, cfg, inp, cache, d, idx, out, 0, h, budget_bits=budget, what=f"b{budget} h{h}")
@@ -85,57 +88,6 @@ def test_multi_session_sampled(pk, orc):
     for s in range(cfg.n_seq):
         for h in range(cfg.n_kv_heads):
             assert depth_quarter_bits(dd[s, h]) <= 4 * int(inp.budgets[s])
-
-
-@pytest.mark.parametrize("wl,n_tok,rule,fixed", [("qwen3_8b_layer", 32768, 0, (0, 0)),
-                                                 ("qwen3_8b_layer", 20000 + 13, 1, (32, 4)),
-                                                 ("qwen3_8b_layer", 1000, 1, (128, 2)),
-                                                 ("tiny", 4096, 0, (0, 0)),
-                                                 ("tiny", 100, 0, (0, 0))])
-def test_fused_matches_per_stage(pk, wl, n_tok, rule, fixed):
-    """The fused cluster kernel and the per-stage kernels share the scan
-    arithmetic: same depths, same selections; attention within float rounding."""
-    from workload import CONFIGS, gen_layer
-    cfg = CONFIGS[wl]
-    inp = gen_layer(cfg, 3, device="cuda", n_tokens=n_tok)
-    r_f = decode_one_layer(inp, cfg, depth_rule=rule, fixed=fixed, flags=1)
-    r_s = decode_one_layer(inp, cfg, depth_rule=rule, fixed=fixed, flags=0)
-    assert pk.bpkv_step_fused(r_f[0].c, cfg.k, cfg.n_sink, cfg.n_recent, rule)
-    assert torch.equal(r_f[1], r_s[1])
-    assert torch.equal(r_f[2], r_s[2])
-    assert torch.max(torch.abs(r_f[3] - r_s[3])).item() < 1e-4
-    nb = (n_tok + 63) // 64  # words past the last block are never written
-    assert torch.equal(r_f[0].planes[..., :nb], r_s[0].planes[..., :nb])
-    assert torch.equal(r_f[0].scales[..., :nb], r_s[0].scales[..., :nb])
-    assert torch.equal(r_f[0].seq_len, r_s[0].seq_len)
-
-
-def test_fused_eligibility(pk):
-    from bit_plane_kv_encode_gb300 import Cache
-    small = Cache(1, 8, 4, 33280)
-    small.c.n_max = 32767
-    assert pk.bpkv_step_fused(small.c, 512, 4, 32, 0)
-    assert not pk.bpkv_step_fused(small.c, 512, 4, 32, 2)       # dense
-    assert not pk.bpkv_step_fused(small.c, 2048, 4, 32, 0)      # k too large for the merge buffers
-    big = Cache(1, 1, 4, 131584)
-    big.c.n_max = 131071
-    assert not pk.bpkv_step_fused(big.c, 512, 4, 32, 0)         # 16384 tokens per CTA
-
-
-@pytest.mark.parametrize("wl,n_tok,budget", [("qwen3_8b_layer", 32768, 92), ("full_step", 131072, 136),
-                                             ("multi_session", 65536, None), ("tiny", 300, 68)])
-def test_tail_matches_split(pk, wl, n_tok, budget):
-    """The cluster tail (selection + union + attention in one kernel) and the
-    separate top-k / union / attention kernels select the same sets."""
-    from workload import CONFIGS, gen_layer
-    cfg = CONFIGS[wl]
-    inp = gen_layer(cfg, 7, device="cuda", n_tokens=n_tok, n_seq=min(cfg.n_seq, 4))
-    b = None if budget is None else torch.full((inp.k.shape[0],), budget, dtype=torch.int32)
-    r_t = decode_one_layer(inp, cfg, budgets=b, flags=2)
-    r_s = decode_one_layer(inp, cfg, budgets=b, flags=0)
-    assert torch.equal(r_t[1], r_s[1])
-    assert torch.equal(r_t[2], r_s[2])
-    assert torch.max(torch.abs(r_t[3] - r_s[3])).item() < 1e-4
 
 
 @pytest.mark.parametrize("wl,n_tok,rule,fixed,budget", [("qwen3_8b_layer", 32768, 0, (0, 0), 92),

@@ -26,19 +26,17 @@ def _case(pk, n, H, seed):
     sig = torch.exp(0.75 * torch.randn((N, H, 1, D), generator=g))
     k = (torch.randn((N, H, n, D), generator=g) * sig).to(torch.bfloat16).cuda()
     v = torch.randn((N, H, n, D), generator=g).to(torch.bfloat16).cuda()
-    cache = build_cache(k, v, G)
+    cache = build_cache(k, v, G, cap=max(512, (n + 511) // 512 * 512))
     return cache, g
 
 
-def test_noalloc_matches_workspace_call_twice(pk):
-    n, H, K = 32768, 8, 512
-    cache, g = _case(pk, n, H, seed=21)
+def _compare(pk, cache, g, H, K, budgets):
     N, G = 1, 4
     ws = cache.workspace(K, pk.WS_SCAN_TOPK)
-    for call in range(2):
+    for call, b in enumerate(budgets):
         q = torch.randn((N, H, G, 128), generator=g).cuda()
         s2 = torch.exp(torch.randn((N, H, 128), generator=g)).cuda()
-        budget = torch.tensor([4 * (68 + 24 * call)], dtype=torch.int32).cuda()
+        budget = torch.tensor([4 * b], dtype=torch.int32).cuda()
         depths = torch.zeros((N, H, 128), dtype=torch.uint8, device="cuda")
         pk.bpkv_alloc_depths(cache.c, q, s2, budget, depths)
         want = torch.full((N, H, G, K), -7, dtype=torch.int32, device="cuda")
@@ -46,12 +44,30 @@ def test_noalloc_matches_workspace_call_twice(pk):
         pk.bpkv_scan_topk(cache.c, q, depths, K, 4, 32, want, ws, ws.numel())
         pk.bpkv_scan_topk_noalloc(cache.c, q, depths, K, 4, 32, got)
         torch.cuda.synchronize()
+        assert pk.bpkv_read_status(ws) == 0
         assert (want >= -1).all()
         assert torch.equal(got, want), f"call {call}: {int((got != want).sum())} indices differ"
 
 
+# n = 32768: score rows as wide as the capacity; n = 70001: the array packs
+# rows at round_up(n, 64) = 70016 floats, narrower than the 70144-token
+# capacity the workspace call uses; n = 131073 on one KV head: long rows (the
+# selection's second histogram level); n = 0: nothing to scan, every list -1
+@pytest.mark.parametrize("n,H", [(32768, 8), (70001, 8), (131073, 1), (0, 8)])
+def test_noalloc_matches_workspace_call_twice(pk, n, H):
+    cache, g = _case(pk, n, H, seed=21 + n % 97)
+    _compare(pk, cache, g, H, 512, [68, 92])
+
+
+def test_noalloc_repeated_calls(pk):
+    # the same array reused by many calls in a row, with budgets and queries
+    # changing between calls: every call must still match the workspace call
+    cache, g = _case(pk, 70001, 8, seed=5)
+    _compare(pk, cache, g, 8, 512, [68, 92, 136, 32, 92, 68, 136, 44, 92, 104])
+
+
 def test_noalloc_refuses_oversized_request(pk):
-    # rows (4 round_up(n, 64) + 40984) bytes with rows = N H G = 64: 64 x (262400 + 40984) > 16 MiB
+    # 256 + rows (4 round_up(n, 64) + 40984) bytes with rows = N H G = 64: > 16 MiB
     cache, g = _case(pk, 65600, 16, seed=22)
     q = torch.randn((1, 16, 4, 128), generator=g).cuda()
     depths = torch.full((1, 16, 128), 1, dtype=torch.uint8, device="cuda")
