@@ -1,20 +1,26 @@
 #!/usr/bin/env python
 """Benchmark of the decode-time prefix-plane KV scan path on one GB300.
 
-A step is one decode pass of one Qwen3-8B-shaped layer (8 KV heads x 4 query
-heads, D = 128, batch 1, n = 32768 tokens, k = 512) at each of the budgets
-68, 92 and 136 bits/token: for each budget, bpkv_decode_step appends the new
-token (encode), allocates depths, scans the plane prefixes, selects top-k,
-forms the GQA union and runs sparse attention.  The step is captured once in a
-CUDA graph and replayed; the L2 cache is flushed (a 256 MiB write) before
-every timed step, outside the timed events.
+Default workload: the full decode step of a Qwen3-8B-shaped model (36 layers
+x 8 KV heads x 4 query heads, D = 128, batch 4, n = 131072 tokens per
+sequence, k = 512, caches in HBM) at each budget of the sweep 32, 44, ..., 136
+bits/token.  A bench step is one decode pass per budget: for each budget,
+bpkv_decode_step runs every layer (append and encode the new token, allocate
+depths, scan the plane prefixes, select top-k, form the GQA union, sparse
+attention).  The step is captured once in a CUDA graph and replayed; the L2
+cache is flushed (a 256 MiB write) before every timed step, outside the timed
+events.
 
-Metric: keys scored/s = (budgets x N x H x n) / step time.  The JSON line also
-carries decode-step us per layer, per-stage times, the roofline of the
-dominant kernel, the end-to-end number through host buffers, the CPU oracle
-baseline and the clocks seen while timing.
+Metric: keys scored/s = (budgets x layers x N x H x n) / step time.  The JSON
+line also carries decode-step us per layer, per-stage times, the roofline of
+the scan kernel (with its issue-slot and FMA-floor fractions), the other
+kernels' rates, the end-to-end number through host buffers, the fixed-depth
+and dense baselines, a host-resident sub-record (one layer of the
+million-token workload in pinned host memory, against the host-to-device
+copy rate measured in the same run), the CPU oracle baseline and the clocks
+seen while timing.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 """
 from __future__ import annotations
 
@@ -35,13 +41,22 @@ sys.path.insert(0, ROOT)
 STAGES = ["encode", "depths", "scan", "topk", "union", "attend"]
 
 
-def launches_per_pass(p, args) -> int:
-    """Kernels bpkv_decode_step launches per layer on the path this pass takes."""
-    if p["fused"]:
-        return 2          # fused cluster kernel + length update
-    if args.tail:
-        return 5          # encode + length update, depths, scan, cluster tail
-    return 4              # front (append beside depths and plan), scan, cut, range attention
+SM_COUNT = 152            # GB300 streaming multiprocessors
+ISSUE_PER_SM_CLK = 4      # warp instructions issued per SM per clock (one per scheduler)
+FMA_PER_SM_CLK = 128      # float32 fused multiply-adds per SM per clock
+
+
+def launches_per_pass(cap: int, rows: int) -> int:
+    """Kernels bpkv_decode_step launches per layer: the front kernel (append
+    beside depths and plan), the scan, the cut and the range attention, plus
+    the level-1 histogram kernel before the cut on rows of 131072 keys or more
+    when the cut's grid is not resident at once (the bench sizes launches by
+    the capacity)."""
+    long_rows = cap - 1 >= 131072
+    cut_ctas = rows * ((cap - 1 - 36 + 4095) // 4096)
+    return 4 + (1 if long_rows and cut_ctas > 2 * SM_COUNT else 0)
+
+
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -51,12 +66,12 @@ def parse():
     p.add_argument("--steps", type=int, default=100)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--workload", default="qwen3_8b_layer")
+    p.add_argument("--workload", default="full_step")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true")
-    p.add_argument("--fused", action="store_true", help="one fused cluster kernel per pass where eligible")
-    p.add_argument("--tail", action="store_true", help="one cluster kernel for top-k, union and attention")
+    p.add_argument("--no-host", action="store_true",
+                   help="skip the host-resident sub-record (one layer of the million-token workload)")
     p.add_argument("--budget", type=int, default=0, help="run this budget only (bits/token)")
     p.add_argument("--layers", type=int, default=0,
                    help="profiling aid: decode only this many of the config's layers (reported in config)")
@@ -144,7 +159,7 @@ class Clocks:
 
 # ------------------------------------------------------------------ workload
 
-def make_workload(cfg, steps: int, warmup: int, dev, step_flags: int = 0, budgets=None):
+def make_workload(cfg, steps: int, warmup: int, dev, budgets=None):
     """Caches and step inputs.  One pass per budget; each pass decodes all the
     config's layers (each layer its own cache).  Host-resident configs build each
     layer's cache in device memory and move it to pinned host memory."""
@@ -218,14 +233,12 @@ def make_workload(cfg, steps: int, warmup: int, dev, step_flags: int = 0, budget
                   p["out"].data_ptr(), p["depths"].data_ptr())
         # timed steps write no index lists (the attention reads the selection cuts);
         # one untimed step with lists afterwards gives the union sizes for the byte count
-        p["args_lists"] = pk.bpkv_step_args(*common, p["idx"].data_ptr(), None, step_flags)
+        p["args_lists"] = pk.bpkv_step_args(*common, p["idx"].data_ptr(), None, 0)
         common = common + (None,)
         # timed graph: no event nodes (each costs about 2 us inside a graph)
-        p["args"] = pk.bpkv_step_args(*common, None, step_flags)
+        p["args"] = pk.bpkv_step_args(*common, None, 0)
         # breakdown graph: events at every stage boundary
-        p["args_ev"] = pk.bpkv_step_args(*common, ctypes.cast(p["ev_arr"], ctypes.c_void_p), step_flags)
-        p["fused"] = bool(step_flags & pk.STEP_FUSED) and pk.bpkv_step_fused(caches[b][0].c, cfg.k, cfg.n_sink,
-                                                                             cfg.n_recent, pk.DEPTH_WATERFILL)
+        p["args_ev"] = pk.bpkv_step_args(*common, ctypes.cast(p["ev_arr"], ctypes.c_void_p), 0)
         passes.append(p)
     torch.cuda.synchronize()
     passes[0]["shared_caches"] = share
@@ -263,11 +276,14 @@ def run_step(passes, ws, events=False, lists=False):
 
 
 def stage_times_ms(passes):
-    out = {s: 0.0 for s in STAGES}
+    """Per pass, the time of each stage summed over the pass's layers (ms)."""
+    out = []
     for p in passes:
+        t = {st: 0.0 for st in STAGES}
         for ev in p["events"]:
-            for i, s in enumerate(STAGES):
-                out[s] += ev[i].elapsed_time(ev[i + 1])
+            for i, st in enumerate(STAGES):
+                t[st] += ev[i].elapsed_time(ev[i + 1])
+        out.append(t)
     return out
 
 
@@ -287,17 +303,56 @@ def link_h2d_gbs(dev) -> float:
     return best
 
 
+def time_graph(graph, flush, n: int) -> list:
+    """CUDA-event times (ms) of n replays, L2 flushed before each, outside the events."""
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    out = []
+    for _ in range(n):
+        flush.zero_()
+        e0.record()
+        graph.replay()
+        e1.record()
+        e1.synchronize()
+        out.append(e0.elapsed_time(e1))
+    return out
+
+
+def pass_bytes(cfg, passes):
+    """Algorithmic bytes per pass (Fathom page, section 3.1 Eq. 1 terms): plane
+    prefixes and scales read by the scan, union rows read by the attention,
+    and the active (token, channel) pairs the scan multiplies by G query heads.
+    Needs the index lists of an untimed step with lists."""
+    from workload.bytes_model import depth_bits, row_bytes
+    L, N, H, n, D = cfg.n_layers, cfg.n_seq, cfg.n_kv_heads, cfg.n_tokens, cfg.head_dim
+    out = []
+    for p in passes:
+        dd = p["depths"].cpu().numpy()
+        idx = p["idx"].cpu().numpy()
+        scan_b = rows_b = 0.0
+        union_rows = active = 0
+        for l in range(L):
+            for sq in range(N):
+                for h in range(H):
+                    scan_b += depth_bits(dd[l, sq, h]) * n / 8
+                    active += int((dd[l, sq, h] > 0).sum()) * n
+                    u = len(np.unique(idx[l, sq, h][idx[l, sq, h] >= 0]))
+                    union_rows += u
+                    rows_b += u * row_bytes(D)
+        out.append(dict(budget=p["budget"], scan=scan_b, rows=rows_b, union_rows=union_rows, active=active,
+                        scores=L * N * H * cfg.group * n * 4))
+    return out
+
+
 def bench_ours(args, cfg, rank, world, local):
     import torch
     import bit_plane_kv_encode_gb300 as pk
-    from workload.bytes_model import depth_bits, row_bytes
 
     dev = torch.device("cuda", local)
     import __graft_entry__
     __graft_entry__.build()
     budgets = [args.budget] if args.budget else None
-    inp, passes, ws, io = make_workload(cfg, args.steps, args.warmup, dev,
-                                       (1 if args.fused else 0) | (2 if args.tail else 0), budgets)
+    inp, passes, ws, io = make_workload(cfg, args.steps, args.warmup, dev, budgets)
     N, H, n, D = cfg.n_seq, cfg.n_kv_heads, cfg.n_tokens, cfg.head_dim
     G, L = cfg.group, cfg.n_layers
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -332,7 +387,7 @@ def bench_ours(args, cfg, rank, world, local):
     barrier(world)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    step_ms, stage_ms = [], {s: [] for s in STAGES}
+    step_ms = []
     t_wall = time.perf_counter()
     for _ in range(args.steps):
         flush.zero_()
@@ -346,8 +401,9 @@ def bench_ours(args, cfg, rank, world, local):
     wall = time.perf_counter() - t_wall
     clk = clocks.stop()
     assert pk.bpkv_read_status(ws) == 0
-    # stage breakdown (separate replays of the graph with event nodes)
-    ev_ms = []
+    # stage breakdown: separate replays of the graph with event nodes at every
+    # stage boundary (recorded on the stream the kernels are launched on)
+    ev_ms, per_pass = [], [{st: [] for st in STAGES} for _ in passes]
     for _ in range(min(args.steps, 20)):
         flush.zero_()
         e0.record()
@@ -355,8 +411,11 @@ def bench_ours(args, cfg, rank, world, local):
         e1.record()
         e1.synchronize()
         ev_ms.append(e0.elapsed_time(e1))
-        for s, v in stage_times_ms(passes).items():
-            stage_ms[s].append(v)
+        for i, t in enumerate(stage_times_ms(passes)):
+            for st, v in t.items():
+                per_pass[i][st].append(v)
+    stage_pass = [{st: statistics.mean(v) for st, v in pp.items()} for pp in per_pass]
+    stage_mean = {st: sum(sp[st] for sp in stage_pass) for st in STAGES}
 
     run_step(passes, ws, lists=True)  # untimed: index lists for the union sizes below
     torch.cuda.synchronize()
@@ -364,22 +423,14 @@ def bench_ours(args, cfg, rank, world, local):
     ms_per_step = total_ms / args.steps
     keys_per_step = len(passes) * L * N * H * n
     value = world * keys_per_step / (ms_per_step / 1e3)
+    pb = pass_bytes(cfg, passes)
+    scan_bytes = sum(b["scan"] for b in pb)
+    rows_bytes = sum(b["rows"] for b in pb)
+    score_bytes = sum(b["scores"] for b in pb)
+    union_rows = sum(b["union_rows"] for b in pb)
+    active = sum(b["active"] for b in pb)
+    n_launch = len(passes) * L  # launches of each kernel per step
 
-    # algorithmic bytes per pass (Fathom page, section 3.1 Eq. 1 terms)
-    scan_bytes, rows_bytes, score_bytes = 0.0, 0.0, 0.0
-    union_rows = 0
-    for p in passes:
-        dd = p["depths"].cpu().numpy()
-        idx = p["idx"].cpu().numpy()
-        for l in range(L):
-            for s in range(N):
-                for h in range(H):
-                    scan_bytes += depth_bits(dd[l, s, h]) * n / 8
-                    u = len(np.unique(idx[l, s, h][idx[l, s, h] >= 0]))
-                    union_rows += u
-                    rows_bytes += u * row_bytes(D)
-        score_bytes += L * N * H * G * n * 4
-    n_launch = len(passes) * L
     # quality on the planted needles of layer 0 (positions of keys with a large
     # q.k): the fraction inside the union of the KV head's selections, per budget
     needle_recall = None
@@ -388,81 +439,210 @@ def bench_ours(args, cfg, rank, world, local):
         for p in passes:
             idx0 = p["idx"][0].cpu().numpy()  # [N][H][G][k], layer 0
             found = total = 0
-            for s in range(N):
+            for sq in range(N):
                 for h in range(H):
-                    sel = set(idx0[s, h].ravel().tolist())
-                    pos = inp.needles[s, h].tolist()
+                    sel = set(idx0[sq, h].ravel().tolist())
+                    pos = inp.needles[sq, h].tolist()
                     found += sum(int(x) in sel for x in pos)
                     total += len(pos)
             needle_recall[str(p["budget"])] = round(found / max(total, 1), 4)
-    stage_mean = {s: statistics.mean(v) for s, v in stage_ms.items()}
-    if all(p["fused"] for p in passes):
-        # one fused kernel per pass: it reads the plane prefixes and the union rows
-        dom, kbytes, kms = "k_decode_fused", scan_bytes + rows_bytes, stage_mean["encode"]
-    else:
-        stage_bytes = {"scan": scan_bytes, "topk": score_bytes, "attend": rows_bytes}
-        dom = max(stage_bytes, key=lambda s: stage_mean[s])
-        kbytes, kms = stage_bytes[dom], stage_mean[dom]
+
+    # roofline of the scan (the method's dominant term, b n / 8 per unit)
     hbm, peak_src = peaks()
-    bound = "hbm"
-    link = None
-    if cfg.residency == "host":
-        # the scan and the row reads cross the host link: its measured copy rate is the peak
-        link = link_h2d_gbs(dev)
-        hbm, peak_src, bound = link, "of measured (pinned host-to-device copy, 1 GiB)", "host_link"
-    achieved = kbytes / (kms / 1e3) / 1e9
-    traffic = load_traffic(dom, cfg.name, [p["budget"] for p in passes])
-    kernel_name = {"scan": "k_scan_pipe", "topk": "k_cut", "attend": "k_attend_ranges"}.get(dom, dom)
-    roofline = {"bound": bound, "kernel": kernel_name, "achieved": round(achieved, 1), "peak": round(hbm, 1),
+    kms = stage_mean["scan"]
+    achieved = scan_bytes / (kms / 1e3) / 1e9
+    budgets_run = [p["budget"] for p in passes]
+    traffic = load_traffic("k_scan_pipe", cfg.name, budgets_run)
+    roofline = {"bound": "hbm", "kernel": "k_scan_pipe", "achieved": round(achieved, 1), "peak": round(hbm, 1),
                 "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_source": peak_src,
-                "traffic": traffic, "algorithmic_bytes_per_launch": round(kbytes / n_launch),
-                "launch_us": round(kms * 1e3 / n_launch, 2)}
+                "traffic": traffic, "algorithmic_bytes_per_launch": round(scan_bytes / n_launch),
+                "launch_us": round(kms * 1e3 / n_launch, 2),
+                "per_budget": {str(b["budget"]): {
+                    "launch_us": round(sp["scan"] * 1e3 / L, 2),
+                    "gbs": round(b["scan"] / (sp["scan"] / 1e3) / 1e9, 1),
+                    "frac": round(b["scan"] / (sp["scan"] / 1e3) / 1e9 / hbm, 4)} for b, sp in zip(pb, stage_pass)}}
+    # the scan's issue-slot fraction (instructions per launch from a committed
+    # ncu count of this source) and its FMA floor: G float32 fused multiply-adds
+    # per (token, active channel), 128 per SM per clock
+    f_sm = (clk.get("sm_mhz") or 0.0) * 1e6
+    scan_issue = {"fma_per_token_channel": G, "clock_mhz": clk.get("sm_mhz")}
+    if f_sm > 0:
+        fma_rate = SM_COUNT * FMA_PER_SM_CLK * f_sm
+        scan_issue["fma_floor_frac"] = round(active * G / (kms / 1e3) / fma_rate, 4)
+        scan_issue["fma_floor_gbs"] = round(scan_bytes / (active * G / fma_rate) / 1e9, 1)
+        inst = load_inst("k_scan_pipe", cfg.name, budgets_run)
+        if inst is not None:
+            scan_issue["inst_per_step"] = inst * L
+            scan_issue["issue_frac"] = round(inst * L / (kms / 1e3) / (SM_COUNT * ISSUE_PER_SM_CLK * f_sm), 4)
+            scan_issue["inst_source"] = "profiles/issue.json (ncu smsp__inst_executed.sum, one layer per budget)"
+        else:
+            scan_issue["issue_frac"] = None
+            scan_issue["inst_source"] = "no ncu instruction count for this source and workload"
+    # the other kernels, per launch
+    kernels = {
+        "k_front": {"us": round(stage_mean["encode"] * 1e3 / n_launch, 2)},
+        "k_scan_pipe": {"us": round(kms * 1e3 / n_launch, 2), "gbs": round(achieved, 1)},
+        "k_cut": {"us": round(stage_mean["topk"] * 1e3 / n_launch, 2),
+                  "score_gbs": round(score_bytes / (stage_mean["topk"] / 1e3) / 1e9, 1)},
+        "k_attend_ranges": {"us": round(stage_mean["attend"] * 1e3 / n_launch, 2),
+                            "rows_gbs": round(rows_bytes / (stage_mean["attend"] / 1e3) / 1e9, 1)},
+    }
 
     # end to end through host buffers: inputs copied in, outputs copied out, inside the timed region
     e2e = None if args.no_extras else bench_e2e(args, passes, io, ws, flush, dev, keys_per_step, world)
     baselines = None if args.no_extras else bench_baselines(args, cfg, passes, io, ws, flush, dev, world)
+    cap = passes[0]["cap"]
+    n_launches = args.steps * n_launch * launches_per_pass(cap, N * H * G)
 
     line = {
         "metric": "keys scored/s", "value": round(value), "unit": "keys/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded; K ~ N(0, sigma_j^2), sigma_j = exp(0.75 z), 8 planted needles/head)",
+        "data": "synthetic (seeded; K ~ N(0, sigma_j^2), sigma_j = exp(0.75 z), V ~ N(0, 1), q ~ N(0, 1))",
         "config": {"workload": cfg.name, "n_seq": N, "n_kv_heads": H, "group": G, "head_dim": D,
-                   "n_layers": L, "n_tokens": n, "budgets_bits": [p["budget"] for p in passes], "k": cfg.k,
-                   "n_sink": cfg.n_sink,
-                   "n_recent": cfg.n_recent, "residency": cfg.residency,
+                   "n_layers": L, "n_tokens": n, "budgets_bits": budgets_run, "k": cfg.k,
+                   "n_sink": cfg.n_sink, "n_recent": cfg.n_recent, "residency": cfg.residency,
+                   "step": "one decode pass over every layer at each budget of the sweep",
                    "l2": "flushed before every timed step (256 MiB write, outside the events)",
                    "cuda_graph": graph is not None, "parallelism": f"replicas x{world}",
                    "caches": ("one per layer, shared by the budget passes (each pass appends its token)"
                               if passes[0].get("shared_caches") else "one per (budget, layer)")},
         "decode_step_us_per_layer": round(ms_per_step * 1e3 / n_launch, 2),
         "achieved_gbs_step": round((scan_bytes + rows_bytes) / (ms_per_step / 1e3) / 1e9, 1),
-        "fused_kernel": all(p["fused"] for p in passes),
-        "stages_us_per_step": {s: round(v * 1e3, 2) for s, v in stage_mean.items()},
+        "stages_us_per_step": {st: round(v * 1e3, 2) for st, v in stage_mean.items()},
         "stages_note": ("from separate replays with event nodes at every stage boundary "
-                        f"({statistics.mean(ev_ms) * 1e3:.1f} us/step with them); on the default path "
-                        "'encode' holds the front kernel (append beside depths and plan), 'topk' the cut "
-                        "kernel and 'attend' the range attention; on the fused path 'encode' holds the "
-                        "whole fused kernel and 'attend' the length update"),
+                        f"({statistics.mean(ev_ms) * 1e3:.1f} us/step with them); 'encode' holds the front "
+                        "kernel (append beside depths and plan), 'topk' the level-1 histogram and cut kernels, "
+                        "'attend' the range attention"),
         "needle_recall_layer0": needle_recall,
         "bytes_per_step": {"scan": round(scan_bytes), "rows": round(rows_bytes), "scores_overhead": round(score_bytes),
-                           "union_rows": union_rows},
+                           "union_rows": union_rows, "active_token_channels": active},
         "roofline": roofline,
+        "scan_issue": scan_issue,
+        "kernels": kernels,
         "e2e": e2e,
         "baselines": baselines,
         "baselines_note": ("same entry point, same caches and step structure: SparQ channel rule at 32 channels "
                            "x 4 planes (136 bits/token), 32 offline-calibrated channels x 4 planes (136 bits/token), "
                            "all channels at 2 planes (288 bits/token), dense bf16 attention over every row; read "
                            "bytes are the plane prefixes (or rows for dense)"),
-        "gpu_launches": args.steps * L * sum(launches_per_pass(p, args) for p in passes),
+        "gpu_launches": n_launches,
         "clocks": clk,
         "wall_s_timed": round(wall, 3),
     }
-    if link is not None:
-        line["link_h2d_gbs"] = round(link, 1)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg, inp, args.cpu_seconds, [p["budget"] for p in passes])
+        line["cpu_baseline"] = cpu_baseline(cfg, inp, args.cpu_seconds, budgets_run)
+    if not args.no_extras and not args.no_host and cfg.residency != "host":
+        # free this workload before building the host-resident layer
+        del passes, ws, io, graph, graph_ev, flush
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        line["host_resident"] = bench_host(args, dev)
     return line
+
+
+def numa_info(ptr: int) -> dict:
+    """NUMA placement of the host page holding ptr (/proc/self/numa_maps) and
+    the NUMA node of the GPU's PCI function (sysfs), best effort."""
+    info = {}
+    try:
+        start = None
+        for line in open("/proc/self/maps"):
+            lo, hi = (int(x, 16) for x in line.split()[0].split("-"))
+            if lo <= ptr < hi:
+                start = lo
+                break
+        if start is not None:
+            for line in open("/proc/self/numa_maps"):
+                f = line.split()
+                if int(f[0], 16) == start:
+                    info["host_pages_by_node"] = {x.split("=")[0]: int(x.split("=")[1]) for x in f
+                                                  if x.startswith("N") and "=" in x}
+                    info["policy"] = f[1]
+                    break
+    except Exception as e:  # noqa: BLE001
+        info["host_pages_error"] = str(e)[:80]
+    try:
+        bus = subprocess.run(["nvidia-smi", "--query-gpu=pci.bus_id", "--format=csv,noheader", "-i", "0"],
+                             capture_output=True, text=True, timeout=10).stdout.strip().lower()
+        bus = bus[-12:] if len(bus) > 12 else bus
+        info["gpu_pci"] = bus
+        info["gpu_numa_node"] = int(open(f"/sys/bus/pci/devices/{bus}/numa_node").read().strip())
+    except Exception as e:  # noqa: BLE001
+        info["gpu_numa_error"] = str(e)[:80]
+    try:
+        cpus = sorted(os.sched_getaffinity(0))
+        nodes = set()
+        for d in os.listdir("/sys/devices/system/node"):
+            if d.startswith("node"):
+                lst = open(f"/sys/devices/system/node/{d}/cpulist").read().strip()
+                ids = set()
+                for part in lst.split(","):
+                    if "-" in part:
+                        x, y = part.split("-")
+                        ids.update(range(int(x), int(y) + 1))
+                    elif part:
+                        ids.add(int(part))
+                if ids & set(cpus):
+                    nodes.add(int(d[4:]))
+        info["process_cpu_nodes"] = sorted(nodes)
+    except Exception as e:  # noqa: BLE001
+        info["cpu_nodes_error"] = str(e)[:80]
+    return info
+
+
+def bench_host(args, dev) -> dict:
+    """One layer of the million-token workload with planes, scales and rows in
+    pinned host memory (cudaHostAlloc), one decode pass per budget 68, 92, 136:
+    the scan's plane-prefix rate and the attention's union-row rate against
+    the pinned host-to-device copy rate measured in the same run."""
+    import dataclasses
+    import torch
+    import bit_plane_kv_encode_gb300 as pk
+    from workload import CONFIGS
+    cfg = dataclasses.replace(CONFIGS["host_1m"], n_layers=1)
+    steps = max(3, min(args.steps, 10))
+    _, passes, ws, io = make_workload(cfg, steps, 3, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=torch.cuda.Stream(device=dev)):
+        run_step(passes, ws, events=True)
+    pk.bpkv_clear_status(ws)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    per_pass = [{st: [] for st in STAGES} for _ in passes]
+    for _ in range(steps):
+        time_graph(graph, flush, 1)
+        for i, t in enumerate(stage_times_ms(passes)):
+            for st, v in t.items():
+                per_pass[i][st].append(v)
+    if pk.bpkv_read_status(ws) != 0:
+        raise RuntimeError("device status after the host-resident passes")
+    run_step(passes, ws, lists=True)
+    torch.cuda.synchronize()
+    pb = pass_bytes(cfg, passes)
+    link = link_h2d_gbs(dev)
+    out = {"workload": "host_1m (1 of its 8 layers)", "n_tokens": cfg.n_tokens, "n_kv_heads": cfg.n_kv_heads,
+           "group": cfg.group, "k": cfg.k, "memory": "cudaHostAlloc (pinned, mapped), read in place over the host link",
+           "link_h2d_gbs": round(link, 1),
+           "link_note": "pinned host-to-device cudaMemcpyAsync of 1 GiB, best of 10, CUDA events, this run",
+           "numa": numa_info(passes[0]["caches"][0].planes.data_ptr()), "passes": {}}
+    for p, b, pp in zip(passes, pb, per_pass):
+        sc = statistics.mean(pp["scan"])
+        at = statistics.mean(pp["attend"])
+        tot = sum(statistics.mean(v) for v in pp.values())
+        out["passes"][str(p["budget"])] = {
+            "layer_us": round(tot * 1e3, 1),
+            "scan_us": round(sc * 1e3, 1), "scan_gbs": round(b["scan"] / (sc / 1e3) / 1e9, 1),
+            "scan_frac_of_link": round(b["scan"] / (sc / 1e3) / 1e9 / link, 4),
+            "attend_us": round(at * 1e3, 1), "union_rows": b["union_rows"],
+            "rows_gbs": round(b["rows"] / (at / 1e3) / 1e9, 1),
+            "rows_frac_of_link": round(b["rows"] / (at / 1e3) / 1e9 / link, 4)}
+    del passes, ws, io, graph
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
 
 
 def bench_baselines(args, cfg, passes, io, ws, flush, dev, world):
@@ -582,6 +762,23 @@ def load_traffic(kernel: str, workload: str, budgets):
     return d["dram_bytes_per_launch"] if source_hash(d["source"]) == d.get("source_sha256_16") else None
 
 
+def load_inst(kernel: str, workload: str, budgets):
+    """Warp instructions per launch summed over the passes of one step (one
+    layer each) from the committed ncu count, if it was taken on this workload
+    and budgets and still matches the kernel source."""
+    path = os.path.join(ROOT, "profiles", "issue.json")
+    try:
+        d = json.load(open(path))[kernel]
+    except Exception:
+        return None
+    if d.get("workload") != workload or source_hash(d["source"]) != d.get("source_sha256_16"):
+        return None
+    per = d.get("inst_per_launch", {})
+    if not all(str(b) in per for b in budgets):
+        return None
+    return sum(int(per[str(b)]) for b in budgets)
+
+
 def source_hash(files) -> str:
     """First 16 hex digits of the SHA-256 of the kernel's source files, concatenated."""
     import hashlib
@@ -653,12 +850,15 @@ def cpu_baseline(cfg, inp, seconds: float, budgets) -> dict:
 
 
 def bench_reference(args, cfg, rank, world):
-    """The reference arm: the CPU oracle as it stands, timed on the host cores."""
+    """The reference arm: the CPU oracle as it stands, timed on the host cores.
+    Each step is a bounded sample of the workload: one decode pass of the
+    first 8 (sequence, KV head) units of layer 0 at one budget, the budgets of
+    the sweep taken in turn from step to step."""
     import concurrent.futures as cf
     from workload import gen_layer
     if rank != 0:
         return None
-    inp = gen_layer(cfg, 0, device="cpu")
+    inp = gen_layer(cfg, 0, device="cpu", n_seq=1)
     inp.k, inp.v = inp.k[:1, :8], inp.v[:1, :8]
     budgets = [args.budget] if args.budget else list(cfg.budgets)
     o, units = _oracle_units(cfg, inp)
@@ -666,22 +866,24 @@ def bench_reference(args, cfg, rank, world):
     cores = os.cpu_count() or 1
     times = []
     with cf.ThreadPoolExecutor(max_workers=cores) as pool:
-        for _ in range(args.warmup):
-            _oracle_step(o, cfg, inp, units, pool, budgets)
-        for _ in range(args.steps):
+        for i in range(args.warmup):
+            _oracle_step(o, cfg, inp, units, pool, [budgets[i % len(budgets)]])
+        for i in range(args.steps):
             t0 = time.perf_counter()
-            _oracle_step(o, cfg, inp, units, pool, budgets)
+            _oracle_step(o, cfg, inp, units, pool, [budgets[i % len(budgets)]])
             times.append(time.perf_counter() - t0)
     ms = 1e3 * statistics.mean(times)
-    keys = len(budgets) * len(units) * n
+    keys = len(units) * n
     val = round(keys / (ms / 1e3))
     return {"impl": "reference", "metric": "keys scored/s", "value": val, "unit": "keys/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg.name, "n_tokens": n, "budgets_bits": budgets, "k": cfg.k},
+            "config": {"workload": cfg.name, "n_seq": cfg.n_seq, "n_kv_heads": cfg.n_kv_heads, "group": cfg.group,
+                       "head_dim": cfg.head_dim, "n_layers": cfg.n_layers, "n_tokens": n, "budgets_bits": budgets,
+                       "k": cfg.k, "n_sink": cfg.n_sink, "n_recent": cfg.n_recent, "residency": cfg.residency},
             "cpu_baseline": {"value": val, "unit": "keys/s", "cores": cores, "kind": "oracle",
-                             "sample": f"every step: {len(budgets)} budgets x {len(units)} (seq, KV head) units "
-                                       f"of layer 0 of {cfg.name} on the host cores"},
+                             "sample": f"every step: {len(units)} (seq, KV head) units of layer 0 of {cfg.name} at "
+                                       f"one budget (the sweep's budgets in turn), threads over units"},
             "e2e": {"value": val, "unit": "keys/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
