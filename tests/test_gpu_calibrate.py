@@ -102,3 +102,26 @@ def test_given_depths_above_four_read_as_four(pk):
     _, d_4, _, out_4 = decode_one_layer(inp, cfg, depth_rule=pk.DEPTH_GIVEN, depths_in=four.cuda())
     assert torch.equal(d_hi, four[0].cuda()) and torch.equal(d_4, four[0].cuda())
     assert torch.equal(out_hi, out_4)
+
+
+def test_given_depths_above_four_vs_oracle(pk, orc):
+    """A decode step given depth values 5, 17 and 255 against the oracle's
+    decode of the same raw depth vector (both read them as 4)."""
+    from gpu_helpers import ATTN_ATOL, check_topk_sets
+    from workload import CONFIGS, gen_layer
+    cfg = dataclasses.replace(CONFIGS["tiny"], n_tokens=3000)
+    inp = gen_layer(cfg, 2)
+    N, H, n, D = inp.k.shape
+    g = torch.Generator().manual_seed(11)
+    raw = torch.randint(0, 5, (1, N, H, D), generator=g).to(torch.uint8)
+    raw[..., 0:8], raw[..., 30:38], raw[..., 90:98] = 5, 17, 255
+    cache, depths, idx, out = decode_one_layer(inp, cfg, depth_rule=pk.DEPTH_GIVEN, depths_in=raw.cuda())
+    assert torch.equal(depths.cpu(), raw[0].clamp(max=4))
+    kb, vb = bits16(inp.k[0, 0]), bits16(inp.v[0, 0])
+    ref = orc.decode_unit(kb, vb, inp.q[0, 0].numpy(), inp.sigma2[0, 0].numpy(), None, cfg.k, cfg.n_sink,
+                          cfg.n_recent, nb_cap=cache.c.cap_tokens // 64, depth=raw[0, 0, 0].numpy())
+    for gg in range(cfg.group):
+        gi = idx[0, 0, gg].cpu().numpy()
+        d = check_topk_sets(gi, ref["idx"][gg], ref["scores"][gg], cfg.k, cfg.n_sink, cfg.n_recent, what=f"g{gg}")
+        want = ref["out"][gg] if d == 0 else orc.attend(inp.q[0, 0, gg:gg + 1].numpy(), kb, vb, gi[None])[0]
+        assert float(np.max(np.abs(out[0, 0, gg].cpu().numpy() - want))) <= ATTN_ATOL

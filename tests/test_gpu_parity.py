@@ -118,7 +118,8 @@ def test_fixed_depths_bitexact(pk, orc, r, t):
 # ------------------------------------------------------------------ scan
 
 @pytest.mark.parametrize("n,G,depth_kind", [(4096, 4, "water68"), (5000 + 17, 4, "random"), (777, 8, "full"),
-                                            (2048, 1, "thumb"), (130, 4, "water136"), (3, 2, "random")])
+                                            (2048, 1, "thumb"), (130, 4, "water136"), (3, 2, "random"),
+                                            (3000 + 5, 4, "above4")])
 def test_scan_scores(pk, orc, n, G, depth_kind):
     N, H = 2, 2
     k, v = _rand_kv(N, H, n, seed=n + G)
@@ -131,6 +132,11 @@ def test_scan_scores(pk, orc, n, G, depth_kind):
         d = torch.full((N, H, 128), 4, dtype=torch.uint8)
     elif depth_kind == "thumb":
         d = torch.full((N, H, 128), 2, dtype=torch.uint8)
+    elif depth_kind == "above4":
+        # depth values above 4 read the whole 4-plane code (never the next channel's planes)
+        d = torch.randint(0, 5, (N, H, 128), generator=g, dtype=torch.uint8)
+        for val, lo in ((5, 0), (17, 40), (255, 80)):
+            d[..., lo:lo + 12] = val
     else:
         b = int(depth_kind[5:])
         s2 = torch.exp(torch.randn((N, H, 128), generator=g))
@@ -145,7 +151,7 @@ def test_scan_scores(pk, orc, n, G, depth_kind):
             kb = bits16(k[s, h])
             sc, pl = orc.encode(kb, nb_cap)
             ref = orc.scores(n, sc, pl, d[s, h].numpy(), q[s, h].numpy())
-            scale = abs_score_scale(q[s, h].numpy(), kb, d[s, h].numpy())
+            scale = abs_score_scale(q[s, h].numpy(), kb, np.minimum(d[s, h].numpy(), 4))
             check_scores(got[s, h, :, :n], ref, scale, what=f"{depth_kind} s{s} h{h}")
             assert np.isnan(got[s, h, :, n:]).all()  # nothing written past seq_len
 
