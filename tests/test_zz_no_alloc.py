@@ -33,6 +33,7 @@ def _case(pk, n, H, seed):
 def _compare(pk, cache, g, H, K, budgets):
     N, G = 1, 4
     ws = cache.workspace(K, pk.WS_SCAN_TOPK)
+    pk.bpkv_clear_status(ws)
     for call, b in enumerate(budgets):
         q = torch.randn((N, H, G, 128), generator=g).cuda()
         s2 = torch.exp(torch.randn((N, H, 128), generator=g)).cuda()
