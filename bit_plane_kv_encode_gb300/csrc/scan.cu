@@ -106,27 +106,33 @@ __device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& 
   acc_zero<GP>(A);
   uint32_t keep[5], rot[5];
   transpose_consts(lane, keep, rot);
-  // scores of chunk ch from the accumulators (zeros when no channel is read)
+  // scores of chunk ch from the accumulators (zeros when no channel is read);
+  // positions relative to the chunk in 32-bit arithmetic (a chunk is 512 tokens)
   auto finish_chunk = [&](int64_t ch) {
-    const int64_t b0 = ch * kScanBlocks;
-    const int nbl = (int)min64(kScanBlocks, nb_valid - b0);
-    if (lb < nbl) {
-      const int64_t x0 = b0 * kBlock + (int64_t)lb * kBlock + lane;
+    const int64_t t0 = ch * (kScanBlocks * kBlock);
+    const int r0 = lb * kBlock + lane;  // this lane's first token within the chunk
+    const int lim = (int)min64(n - t0, kScanBlocks * kBlock);
+    if (lb * kBlock < lim) {  // whole warps (warp_hist needs them)
+      const int lo_r = (int)max64(min64(lo - t0, kScanBlocks * kBlock), -1);
+      const int hi_r = (int)max64(min64(hi - t0, kScanBlocks * kBlock), -1);
+      const bool w0 = r0 < lim, w1 = r0 + 32 < lim;
+      const bool in0 = r0 >= lo_r && r0 < hi_r, in1 = r0 + 32 >= lo_r && r0 + 32 < hi_r;
+      float* o = out + t0 + r0;
       float v0[GP], v1[GP];
 #pragma unroll
       for (int hh = 0; hh < GP; ++hh) {
         acc_scores<GP>(A, hh, v0[hh], v1[hh]);
         if (hh < G) {
-          if (x0 < n) out[hh * a.ld + x0] = v0[hh];
-          if (x0 + 32 < n) out[hh * a.ld + x0 + 32] = v1[hh];
+          if (w0) o[hh * a.ld] = v0[hh];
+          if (w1) o[hh * a.ld + 32] = v1[hh];
           if constexpr (kSmemHist) {
             if (hist) {
               uint32_t* H = S.hist + hh * (kTopkBins / 2);
-              if (x0 >= lo && x0 < hi) {
+              if (in0) {
                 const uint32_t bin = ordered_key(v0[hh]) >> 20;
                 atomicAdd(H + (bin >> 1), 1u << ((bin & 1u) * 16));
               }
-              if (x0 + 32 >= lo && x0 + 32 < hi) {
+              if (in1) {
                 const uint32_t bin = ordered_key(v1[hh]) >> 20;
                 atomicAdd(H + (bin >> 1), 1u << ((bin & 1u) * 16));
               }
@@ -135,7 +141,7 @@ __device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& 
         }
       }
       if constexpr (!kSmemHist) {
-        if (hist) warp_hist<GP>(G, x0, lo, hi, v0, v1, hist);
+        if (hist) warp_hist<GP>(G, t0 + r0, lo, hi, v0, v1, hist);
       }
     }
     acc_zero<GP>(A);

@@ -56,11 +56,15 @@ struct PlanScratch {
 };
 
 // 32 x 32 bit transpose across the warp: on return bit r of lane l's word is
-// bit l of lane r's input word.
+// bit l of lane r's input word.  Five exchange rounds with the lane at
+// distance 16, 8, 4, 2, 1; the byte-level rounds (16, 8) merge with one byte
+// permute (sel[0], sel[1] per lane), the others with a rotate and a select.
 __device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, const uint32_t (&keep)[5],
                                                      const uint32_t (&rot)[5]) {
+  x = __byte_perm(x, __shfl_xor_sync(0xffffffffu, x, 16), keep[0]);
+  x = __byte_perm(x, __shfl_xor_sync(0xffffffffu, x, 8), keep[1]);
 #pragma unroll
-  for (int s = 0; s < 5; ++s) {
+  for (int s = 2; s < 5; ++s) {
     const int j = 16 >> s;
     const uint32_t p = __shfl_xor_sync(0xffffffffu, x, j);
     const uint32_t r = __funnelshift_l(p, p, rot[s]);
@@ -86,13 +90,17 @@ __device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsign
   return d;
 }
 
-// Transpose constants of this lane (see warp_transpose32).
+// Transpose constants of this lane (see warp_transpose32): byte selectors of
+// the rounds at distance 16 and 8 (keep[0], keep[1]; rot unused), kept bits and
+// rotation of the others.
 __device__ __forceinline__ void transpose_consts(int lane, uint32_t (&keep)[5], uint32_t (&rot)[5]) {
+  keep[0] = (lane & 16) ? 0x3276u : 0x5410u;
+  keep[1] = (lane & 8) ? 0x3715u : 0x6240u;
+  rot[0] = rot[1] = 0u;
 #pragma unroll
-  for (int st = 0; st < 5; ++st) {
+  for (int st = 2; st < 5; ++st) {
     const int j = 16 >> st;
-    const uint32_t M = st == 0 ? 0x0000FFFFu : st == 1 ? 0x00FF00FFu : st == 2 ? 0x0F0F0F0Fu
-                     : st == 3 ? 0x33333333u : 0x55555555u;
+    const uint32_t M = st == 2 ? 0x0F0F0F0Fu : st == 3 ? 0x33333333u : 0x55555555u;
     const bool hi = (lane & j) != 0;
     keep[st] = hi ? ~M : M;
     rot[st] = hi ? (uint32_t)(32 - j) : (uint32_t)j;
@@ -441,8 +449,9 @@ __device__ __forceinline__ void scan_issue(PipeSmem<GP>& S, int b, const uint64_
       } else {
         const int f = e - n_piece, rel = f >> sh, c = f & sh;
         const int ch = P.slot_ch[s0 + rel];
-        if (ch >= 0)
-          cp_async16(stage_sc(S.st[b], host) + rel * sc_pitch + kScanBlocks * c, sp + (int64_t)ch * nb_cap + b0 + kScanBlocks * c);
+        uint16_t* dst = stage_sc(S.st[b], host) + rel * sc_pitch + kScanBlocks * c;
+        if (ch >= 0) cp_async16(dst, sp + (int64_t)ch * nb_cap + b0 + kScanBlocks * c);
+        else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);  // unused slot: scale 0
       }
     }
   } else {
@@ -458,18 +467,20 @@ __device__ __forceinline__ void scan_issue(PipeSmem<GP>& S, int b, const uint64_
       } else {
         const int f = e - n_row, rel = f >> sh, c = f & sh;
         const int ch = P.slot_ch[s0 + rel];
-        if (ch >= 0)
-          cp_async16(stage_sc(S.st[b], host) + rel * sc_pitch + kScanBlocks * c, sp + (int64_t)ch * nb_cap + b0 + kScanBlocks * c);
+        uint16_t* dst = stage_sc(S.st[b], host) + rel * sc_pitch + kScanBlocks * c;
+        if (ch >= 0) cp_async16(dst, sp + (int64_t)ch * nb_cap + b0 + kScanBlocks * c);
+        else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);  // unused slot: scale 0
       }
     }
   }
   cp_async_commit();
 }
 
-// s w, or 0 where the weight is 0: a slot that no channel uses has w = 0 and
-// whatever raw scale an earlier step left in the stage buffer (possibly one
-// of a block past the end of a unit's cache, which is not a number).
-__device__ __forceinline__ float sw(float s, float w) { return w != 0.f ? s * w : 0.f; }
+// s w.  A slot that no channel uses has w = 0 and a staged scale of 0 (its
+// copy writes zeros), so stale stage contents never reach a score; the
+// scales of blocks past the end of a unit's cache are whatever the cache
+// holds there, but they only reach tokens past the end, which are not written.
+__device__ __forceinline__ float sw(float s, float w) { return s * w; }
 
 // This warp's u = s w for the slots [s0, s1) of a landed stage (block lb of
 // chunk c of a step of `sub` chunks; `host`: the host-cache layout): one slot
