@@ -12,13 +12,14 @@ import ctypes
 
 from ._binding import (  # noqa: F401
     BpkvError, bpkv_alloc_depths, bpkv_cache, bpkv_calibrate_channels, bpkv_clear_status, bpkv_decode_step,
-    bpkv_dense_attend, bpkv_encode_append, bpkv_fixed_depths, bpkv_read_status, bpkv_rotate, bpkv_scan, bpkv_scan_topk, bpkv_scan_topk_noalloc, bpkv_selftest_wait, bpkv_sparse_attend,
+    bpkv_dense_attend, bpkv_encode_append, bpkv_fixed_depths, bpkv_read_status, bpkv_rotate, bpkv_scan, bpkv_scan_topk, bpkv_scan_topk_noalloc, bpkv_selftest_wait, bpkv_sparse_attend, bpkv_sparse_attend_vdepth,
     bpkv_status_string, bpkv_step_args, bpkv_topk, bpkv_union, bpkv_version, bpkv_workspace_size, header_symbols, load)
 
 HEAD_DIM = 128
 WS_SCAN_TOPK, WS_ATTEND, WS_DENSE, WS_STEP = 1, 2, 4, 8
 DEPTH_WATERFILL, DEPTH_FIXED, DEPTH_DENSE, DEPTH_GIVEN = 0, 1, 2, 3
 DEV_OVERFLOW, DEV_SELECT, DEV_TIMEOUT = 1, 2, 4
+STEP_VDEPTH = 1
 
 
 class Cache:
@@ -29,7 +30,7 @@ class Cache:
     """
 
     def __init__(self, n_seq: int, n_kv_heads: int, group: int, cap_tokens: int, device="cuda",
-                 residency: str = "hbm"):
+                 residency: str = "hbm", values: bool = False):
         import torch
         if cap_tokens % 512:
             raise ValueError("cap_tokens must be a multiple of 512")
@@ -56,9 +57,13 @@ class Cache:
         self.v_rows = buf((n_seq, n_kv_heads, cap_tokens, D), torch.bfloat16)
         self.seq_len = torch.zeros(n_seq, dtype=torch.int64, device=self.device)
         self.basis = None
+        # the value rows' own code (value-side read depth), when asked for
+        self.vplanes = buf((n_seq, n_kv_heads, cap_tokens, 4, D // 64), torch.int64) if values else None
+        self.vscales = buf((n_seq, n_kv_heads, cap_tokens), torch.int16) if values else None
         self.c = bpkv_cache(n_seq, n_kv_heads, group, D, cap_tokens, 0, 1 if host else 0, 0,
                             self.planes.data_ptr(), self.scales.data_ptr(), self.k_rows.data_ptr(),
-                            self.v_rows.data_ptr(), self.seq_len.data_ptr(), None)
+                            self.v_rows.data_ptr(), self.seq_len.data_ptr(), None,
+                            self.vplanes.data_ptr() if values else None, self.vscales.data_ptr() if values else None)
 
     def set_basis(self, basis):
         """Code the keys in an orthogonal basis R, float [H][D][D] on the device
@@ -77,8 +82,9 @@ class Cache:
     def copy_from(self, other: "Cache"):
         """Take over another cache's contents (same shapes), e.g. a host-resident
         copy of a cache built in device memory; copies run on the current stream."""
-        for name in ("planes", "scales", "k_rows", "v_rows", "seq_len"):
-            getattr(self, name).copy_(getattr(other, name), non_blocking=True)
+        for name in ("planes", "scales", "k_rows", "v_rows", "seq_len", "vplanes", "vscales"):
+            if getattr(self, name) is not None and getattr(other, name) is not None:
+                getattr(self, name).copy_(getattr(other, name), non_blocking=True)
         self.c.n_max = other.c.n_max
 
     def workspace(self, k: int, what: int):

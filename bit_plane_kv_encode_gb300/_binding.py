@@ -31,6 +31,7 @@ class bpkv_cache(ctypes.Structure):
         ("n_seq", i32), ("n_kv_heads", i32), ("group", i32), ("head_dim", i32),
         ("cap_tokens", i64), ("n_max", i64), ("residency", i32), ("reserved", i32),
         ("planes", P), ("scales", P), ("k_rows", P), ("v_rows", P), ("seq_len", P), ("basis", P),
+        ("vplanes", P), ("vscales", P),
     ]
 
 
@@ -40,7 +41,7 @@ class bpkv_step_args(ctypes.Structure):
         ("depth_rule", i32), ("fixed_channels", i32), ("fixed_depth", i32),
         ("k", i32), ("n_sink", i32), ("n_recent", i32),
         ("out", P), ("depths_out", P), ("idx_out", P), ("stage_events", P), ("flags", i32),
-        ("depths_in", P),
+        ("depths_in", P), ("budget_v", i32), ("vdepth_out", P),
     ]
 
 
@@ -63,6 +64,7 @@ _SIGS = {
     "bpkv_union": ([P, P, i32, P, P, P, P], ctypes.c_int),
     "bpkv_sparse_attend": ([P, P, P, P, P, i32, P, P, sz, P], ctypes.c_int),
     "bpkv_dense_attend": ([P, P, P, P, sz, P], ctypes.c_int),
+    "bpkv_sparse_attend_vdepth": ([P, P, P, P, P, i32, i32, P, P, P, P], ctypes.c_int),
     "bpkv_decode_step": ([P, i32, P, P, sz, P], ctypes.c_int),
 }
 
@@ -216,6 +218,14 @@ def bpkv_sparse_attend(cache, q, uidx, umask, ucount, u_cap: int, out, ws, ws_by
     return _check("bpkv_sparse_attend",
                   load().bpkv_sparse_attend(ctypes.byref(cache), _ptr(q), _ptr(uidx), _ptr(umask), _ptr(ucount),
                                             int(u_cap), _ptr(out), _ptr(ws), int(ws_bytes), _stream(stream)))
+
+
+def bpkv_sparse_attend_vdepth(cache, q, uidx, umask, ucount, u_cap: int, budget_v: int, out, vdepth=None,
+                              weight=None, stream=None):
+    return _check("bpkv_sparse_attend_vdepth",
+                  load().bpkv_sparse_attend_vdepth(ctypes.byref(cache), _ptr(q), _ptr(uidx), _ptr(umask), _ptr(ucount),
+                                                   int(u_cap), int(budget_v), _ptr(out), _ptr(vdepth), _ptr(weight),
+                                                   _stream(stream)))
 
 
 def bpkv_dense_attend(cache, q, out, ws, ws_bytes: int, stream=None):

@@ -13,7 +13,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 SOURCES = ["encode.cu", "depths.cu", "scan.cu", "select.cu", "attend.cu", "abi.cu", "noalloc.cu",
-           "calibrate.cu"]
+           "calibrate.cu", "vdepth.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 
@@ -36,7 +36,7 @@ def _cuda_lib_dir(nvcc: str) -> str:
 def build(force: bool = False, verbose: bool = False) -> str:
     out = lib_path()
     deps = [os.path.join(CSRC, s) for s in SOURCES] + [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "scan_core.cuh"), os.path.join(CSRC, "depths_core.cuh"),
-                                                       os.path.join(CSRC, "encode_core.cuh"),
+                                                       os.path.join(CSRC, "encode_core.cuh"), os.path.join(CSRC, "value_core.cuh"),
                                                        os.path.join(INCLUDE, "bpkv.h")]
     if not force and os.path.exists(out) and os.path.getmtime(out) >= max(os.path.getmtime(d) for d in deps):
         return out

@@ -41,6 +41,9 @@ cudaError_t launch_attend(const bpkv_cache& c, const float* q, const int32_t* ui
 size_t attend_part_bytes(const bpkv_cache& c, int64_t rows, bool dense);
 cudaError_t launch_bump_len(const bpkv_cache& c, int32_t t_new, cudaStream_t st);
 cudaError_t launch_selftest_wait(uint32_t* bar, uint32_t count, uint32_t limit, int32_t* status, cudaStream_t st);
+cudaError_t launch_attend_vdepth(const bpkv_cache& c, const float* q, const int32_t* uidx, const uint8_t* umask,
+                                 const int32_t* ucount, int32_t u_cap, int32_t budget_v, float* out,
+                                 uint8_t* vdepth, float* weight, cudaStream_t st);
 
 namespace {
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -58,6 +61,8 @@ int check_cache(const bpkv_cache* c) {
   if (!aligned(c->planes, 16) || !aligned(c->scales, 16) || !aligned(c->k_rows, 16) || !aligned(c->v_rows, 16) ||
       !aligned(c->seq_len, 8))
     return BPKV_EINVAL;
+  if ((c->vplanes == nullptr) != (c->vscales == nullptr)) return BPKV_EINVAL;
+  if (c->vplanes && (!aligned(c->vplanes, 16) || !aligned(c->vscales, 16))) return BPKV_EINVAL;
   return BPKV_OK;
 }
 
@@ -75,6 +80,7 @@ namespace {
 
 constexpr size_t kAlign = 256;
 constexpr int32_t kMaxUnion = 16384;
+constexpr int32_t kMaxVdepthRows = 2048;  // union rows the value-depth stage holds per unit
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -173,7 +179,7 @@ int cuda_status(cudaError_t e) {
 
 extern "C" {
 
-int32_t bpkv_version(void) { return 1; }
+int32_t bpkv_version(void) { return 2; }
 
 const char* bpkv_status_string(int status) {
   switch (status) {
@@ -293,6 +299,16 @@ int bpkv_sparse_attend(const bpkv_cache* c, const float* q, const int32_t* uidx,
                                    false, as_stream(stream)));
 }
 
+int bpkv_sparse_attend_vdepth(const bpkv_cache* c, const float* q, const int32_t* uidx, const uint8_t* umask,
+                              const int32_t* ucount, int32_t u_cap, int32_t budget_v, float* out, uint8_t* vdepth,
+                              float* weight, void* stream) {
+  BPKV_TRY(check_cache(c));
+  if (!c->vplanes || !q || !uidx || !umask || !ucount || !out) return BPKV_EINVAL;
+  if (u_cap < 1 || u_cap > kMaxVdepthRows || budget_v < 0) return BPKV_EINVAL;
+  return cuda_status(
+      launch_attend_vdepth(*c, q, uidx, umask, ucount, u_cap, budget_v, out, vdepth, weight, as_stream(stream)));
+}
+
 int bpkv_dense_attend(const bpkv_cache* c, const float* q, float* out, void* ws, size_t ws_bytes, void* stream) {
   BPKV_TRY(check_cache(c));
   if (!q || !out) return BPKV_EINVAL;
@@ -313,7 +329,8 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
       return BPKV_EINVAL;
     if (x.n_max + 1 > x.cap_tokens) return BPKV_EINVAL;
   }
-  if (!a->k_new || !a->v_new || !a->q || !a->out || a->flags != 0) return BPKV_EINVAL;
+  if (!a->k_new || !a->v_new || !a->q || !a->out || (a->flags & ~BPKV_STEP_VDEPTH) != 0) return BPKV_EINVAL;
+  const bool vdepth = (a->flags & BPKV_STEP_VDEPTH) != 0;
   if (!aligned(a->k_new, 16) || !aligned(a->v_new, 16)) return BPKV_EINVAL;
   const bool dense = a->depth_rule == BPKV_DEPTH_DENSE;
   if (a->depth_rule == BPKV_DEPTH_WATERFILL && (!a->sigma2 || !a->budget_q)) return BPKV_EINVAL;
@@ -324,6 +341,11 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
   if (!dense) {
     BPKV_TRY(check_k(a->k, a->n_sink, a->n_recent));
     if ((int64_t)a->k * layers[0].group > kMaxUnion) return BPKV_EINVAL;
+  }
+  if (vdepth) {
+    if (dense || a->budget_v < 0 || (int64_t)a->k * layers[0].group > kMaxVdepthRows) return BPKV_EINVAL;
+    for (int32_t l = 0; l < n_layers; ++l)
+      if (!layers[l].vplanes) return BPKV_EINVAL;
   }
   const int32_t k = dense ? 1 : a->k;
   BPKV_TRY(check_ws(layers[0], k, BPKV_WS_STEP, ws, ws_bytes));
@@ -383,6 +405,20 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
     BPKV_TRY(cuda_status(launch_scan(c, q, depths, scores, c.cap_tokens, st, plan, scan_counts ? sb.hist : nullptr,
                                      a->n_sink, a->n_recent, 1, status)));
     BPKV_TRY(mark(l, 3));
+    if (vdepth) {
+      // index lists, the union, then the value-side depth stage over it
+      BPKV_TRY(
+          cuda_status(launch_topk(c, scores, c.cap_tokens, a->k, a->n_sink, a->n_recent, sb, hs, idx, status, st, 1)));
+      BPKV_TRY(mark(l, 4));
+      BPKV_TRY(cuda_status(launch_union(c, idx, a->k, uidx, umask, ucount, st)));
+      BPKV_TRY(mark(l, 5));
+      BPKV_TRY(cuda_status(launch_bump_len(c, 1, st)));  // the union's rows are final: count the new token
+      uint8_t* vd = a->vdepth_out ? a->vdepth_out + (size_t)l * NH * G * a->k : nullptr;
+      BPKV_TRY(cuda_status(launch_attend_vdepth(c, q, uidx, umask, ucount, (int32_t)(G * a->k), a->budget_v, out, vd,
+                                                nullptr, st)));
+      BPKV_TRY(mark(l, 6));
+      continue;
+    }
     if (attend_ranges_eligible(c, a->k)) {
       // cuts only (lists when asked for); the attention selects by cut, forms
       // the union per token range and finally raises seq_len

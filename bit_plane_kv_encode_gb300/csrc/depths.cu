@@ -20,6 +20,7 @@
 #include "depths_core.cuh"
 #include "encode_core.cuh"
 #include "scan_core.cuh"
+#include "value_core.cuh"
 
 #include <type_traits>
 
@@ -126,6 +127,8 @@ struct FrontArgs {
   int64_t cap;
   const float* basis;       // optional [H][D][D]: keys coded as k R, depths and plan from q R
   float* q_rot;             // with a basis: [N][H][G][D] workspace for q R
+  uint64_t* vplanes;        // optional [N][H][cap][4][D/64]: the value rows' own code
+  uint16_t* vscales;        // optional [N][H][cap]
 };
 
 // Grid (enc_ctas + 1, H, N), kScanThreads threads: x < enc_ctas appends, x ==
@@ -162,6 +165,9 @@ __global__ void __launch_bounds__(kScanThreads) k_front(FrontArgs a) {
                         a.k_new + unit * a.t_new * kD, a.v_new + unit * a.t_new * kD, n_old, t0, cnt,
                         a.planes + U.plane_base(unit), a.scales + U.scale_base(unit), a.cap / kBlock, blk,
                         (x % 2) * (kD / 2), a.basis ? a.basis + (int64_t)h * kD * kD : nullptr);
+    if (a.vplanes && x % 2 == 0)
+      encode_value_rows(a.v_new + unit * a.t_new * kD, n_old, t0, cnt, a.vplanes + unit * a.cap * (kPlanes * kD / 64),
+                        a.vscales + unit * a.cap, 0, kScanThreads / 32);
     return;
   }
   __shared__ DepthSmem S;
@@ -222,6 +228,8 @@ cudaError_t launch_front(const bpkv_cache& c, const uint16_t* k_new, const uint1
   a.cap = c.cap_tokens;
   a.basis = c.basis;
   a.q_rot = q_rot;
+  a.vplanes = c.vplanes;
+  a.vscales = c.vscales;
   const dim3 grid((unsigned)(a.enc_ctas + 1), (unsigned)c.n_kv_heads, (unsigned)c.n_seq);
   return launch_depths_gp(c.group, [&](auto gp) {
     return launch_pdl(k_front<decltype(gp)::value>, grid, dim3(kScanThreads), 0, st, a);

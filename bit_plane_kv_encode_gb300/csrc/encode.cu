@@ -7,6 +7,7 @@
 // computes c = clip(floor(k / s), -8, 7) + 8 with IEEE float32 division and
 // packs bit (3 - p) of the 64 codes into plane word p (token i -> bit i).
 #include "encode_core.cuh"
+#include "value_core.cuh"
 
 namespace bpkv {
 
@@ -23,6 +24,8 @@ struct EncodeArgs {
   int64_t cap;
   int64_t nb_cap;
   const float* basis;  // optional [H][D][D]: code the keys k R
+  uint64_t* vplanes;   // optional [N][H][cap][4][D/64]: the value rows' own code
+  uint16_t* vscales;   // optional [N][H][cap]
 };
 
 constexpr int kEncThreads = 4 * kD;  // four threads per channel, 16 tokens each
@@ -43,6 +46,9 @@ __global__ void __launch_bounds__(kEncThreads) k_encode_append(EncodeArgs a) {
                       a.k_new + unit * a.t_new * kD, a.v_new + unit * a.t_new * kD, n_old, t0, cnt,
                       a.planes + U.plane_base(unit), a.scales + U.scale_base(unit), a.nb_cap, blk, 0,
                       a.basis ? a.basis + (int64_t)h * kD * kD : nullptr);
+  if (a.vplanes)
+    encode_value_rows(a.v_new + unit * a.t_new * kD, n_old, t0, cnt, a.vplanes + unit * a.cap * (kPlanes * kD / 64),
+                      a.vscales + unit * a.cap, 0, kEncThreads / 32);
 }
 
 __global__ void k_bump_len(int64_t* seq_len, int n_seq, int32_t t_new) {
@@ -70,6 +76,8 @@ cudaError_t launch_encode_append(const bpkv_cache& c, const uint16_t* k_new, con
   a.cap = c.cap_tokens;
   a.nb_cap = c.cap_tokens / kBlock;
   a.basis = c.basis;
+  a.vplanes = c.vplanes;
+  a.vscales = c.vscales;
   dim3 grid((t_new + kBlock - 1) / kBlock + 1, c.n_kv_heads, c.n_seq);
   cudaError_t e = launch_pdl(k_encode_append, grid, dim3(kEncThreads), 0, st, a);
   if (e != cudaSuccess) return e;

@@ -1,0 +1,307 @@
+// Value-side per-token read depth: the second read stage of ReadKV (the ReadKV
+// page, section 5.3 "approximate attention decides value-token depth" and
+// section 5.4, the allocator), over the exact key attention of the union rows.
+//
+// Value rows are coded with the keys' 4-bit mid-rise code, one fp16 scale per
+// row (s_i = fp16(max_j |v_ij| / 8)), as token-major bit planes: word (i, p, w)
+// bit b is bit (3 - p) of the code of channel 64 w + b, so the first t planes
+// of a row are its t-bit quantiser and a row read to depth t costs t x 16
+// bytes plus its scale.
+//
+// Stage 2 for one (sequence, KV head): each query head h attends over its own
+// union rows with the exact bf16 keys, p_h(r) = softmax_r(q_h . k_r / sqrt(D));
+// each row gets the weight a_r = sum_h p_h(r)^2; items (r, t), t = 0..3, with
+// value a_r 4^-t are taken greedily (largest value first, ties to the lower
+// row, then the lower t) up to the plane budget B_V, stopping at values <= 0;
+// row r is read to depth t_r = its items taken, and o_h = sum_r p_h(r) vhat_r(t_r)
+// with vhat = s ((c_t + 1/2) 2^(4-t) - 8) and vhat = 0 at t = 0.
+//
+// One CTA per unit.  The greedy order is one total order of 64-bit keys
+// (value bits, then the complemented item index), so the taken items are
+// exactly the B_V largest keys: a radix select over the key bits finds the
+// B_V-th largest key and every item at or above it is taken.
+#include "common.cuh"
+
+namespace bpkv {
+
+// ---------------------------------------------------------------- stage 2
+
+constexpr int kVdThreads = 512;
+constexpr int kVdWarps = kVdThreads / 32;
+constexpr int kVdMaxRows = 2048;  // union rows of one unit (G k)
+
+struct VdArgs {
+  const float* q;          // [N][H][G][D]
+  const uint16_t* k_rows;  // [N][H][cap][D]
+  const uint64_t* vplanes; // [N][H][cap][4][D/64]
+  const uint16_t* vscales; // [N][H][cap]
+  const int32_t* uidx;     // [N][H][u_cap]
+  const uint8_t* umask;    // [N][H][u_cap]
+  const int32_t* ucount;   // [N][H]
+  int32_t u_cap;
+  int32_t group;
+  int32_t budget_v;        // planes per unit
+  int64_t cap;
+  float* out;              // [N][H][G][D]
+  uint8_t* vdepth;         // optional [N][H][u_cap]
+  float* weight;           // optional [N][H][u_cap]
+};
+
+template <int GP>
+struct VdSmem {
+  float p[GP][kVdMaxRows];   // logits, then probabilities
+  float a[kVdMaxRows];       // a_r
+  uint8_t dep[kVdMaxRows];
+  float q[GP][kD];
+  float o[GP][kD];
+  float red[kVdWarps][GP];
+  uint32_t hist[256];
+  unsigned long long prefix;
+  uint32_t need;
+};
+
+__device__ __forceinline__ float vd_warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+__device__ __forceinline__ float vd_warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+// Key of item (r, t): the value a_r 4^-t (a positive float orders like its
+// bits), then the complemented item index 4 r + t (lower row, then lower t,
+// first).  Items of value <= 0 get key 0 and are never taken.
+__device__ __forceinline__ unsigned long long vd_key(float a, int r, int t) {
+  const float v = ldexpf(a, -2 * t);
+  if (!(v > 0.f)) return 0ull;
+  return ((unsigned long long)__float_as_uint(v) << 32) | (0xFFFFFFFFu - (uint32_t)(4 * r + t));
+}
+
+template <int GP>
+__global__ void __launch_bounds__(kVdThreads) k_attend_vdepth(VdArgs a) {
+  pdl_enter();
+  extern __shared__ __align__(16) unsigned char vd_raw[];
+  VdSmem<GP>& S = *reinterpret_cast<VdSmem<GP>*>(vd_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t unit = blockIdx.x;
+  const int G = a.group;
+  const int n_u = min(a.ucount[unit], min(a.u_cap, kVdMaxRows));
+  const int32_t* rows = a.uidx + unit * a.u_cap;
+  const uint8_t* masks = a.umask + unit * a.u_cap;
+  const uint16_t* kr = a.k_rows + unit * a.cap * kD;
+  for (int e = tid; e < GP * kD; e += kVdThreads) {
+    const int h = e / kD;
+    S.q[h][e % kD] = h < G ? a.q[(unit * G + h) * kD + e % kD] : 0.f;
+    S.o[h][e % kD] = 0.f;
+  }
+  __syncthreads();
+  // logits q_h . k_r / sqrt(D) of the heads that selected row r (warp per row,
+  // four channels per lane), -inf elsewhere
+  const float scale = rsqrtf((float)kD);
+  for (int r = warp; r < n_u; r += kVdWarps) {
+    const uint2 kv = *reinterpret_cast<const uint2*>(kr + (int64_t)rows[r] * kD + 4 * lane);
+    const float k0 = __uint_as_float(kv.x << 16), k1 = __uint_as_float(kv.x & 0xFFFF0000u);
+    const float k2 = __uint_as_float(kv.y << 16), k3 = __uint_as_float(kv.y & 0xFFFF0000u);
+    const uint32_t m = masks[r];
+#pragma unroll
+    for (int h = 0; h < GP; ++h) {
+      const float* qh = S.q[h] + 4 * lane;
+      float d = qh[0] * k0;
+      d = fmaf(qh[1], k1, d);
+      d = fmaf(qh[2], k2, d);
+      d = fmaf(qh[3], k3, d);
+      d = vd_warp_sum(d);
+      if (lane == 0) S.p[h][r] = (h < G && ((m >> h) & 1)) ? d * scale : -INFINITY;
+    }
+  }
+  __syncthreads();
+  // softmax per head: max, exponentials, sum, probabilities
+  float mx[GP], z[GP];
+#pragma unroll
+  for (int h = 0; h < GP; ++h) {
+    float v = -INFINITY;
+    for (int r = tid; r < n_u; r += kVdThreads) v = fmaxf(v, S.p[h][r]);
+    v = vd_warp_max(v);
+    if (lane == 0) S.red[warp][h] = v;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < GP; ++h) {
+    mx[h] = -INFINITY;
+    for (int w = 0; w < kVdWarps; ++w) mx[h] = fmaxf(mx[h], S.red[w][h]);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < GP; ++h) {
+    float v = 0.f;
+    for (int r = tid; r < n_u; r += kVdThreads) {
+      const float l = S.p[h][r];
+      const float e = l == -INFINITY ? 0.f : __expf(l - mx[h]);
+      S.p[h][r] = e;
+      v += e;
+    }
+    v = vd_warp_sum(v);
+    if (lane == 0) S.red[warp][h] = v;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < GP; ++h) {
+    z[h] = 0.f;
+    for (int w = 0; w < kVdWarps; ++w) z[h] += S.red[w][h];
+  }
+  // probabilities and row weights a_r = sum_h p_h(r)^2 (heads in order)
+  for (int r = tid; r < n_u; r += kVdThreads) {
+    float acc = 0.f;
+#pragma unroll
+    for (int h = 0; h < GP; ++h) {
+      const float pr = z[h] > 0.f ? S.p[h][r] / z[h] : 0.f;
+      S.p[h][r] = pr;
+      acc = fmaf(pr, pr, acc);
+    }
+    S.a[r] = acc;
+  }
+  if (tid == 0) {
+    S.prefix = 0ull;
+    S.need = (uint32_t)max(a.budget_v, 0);
+  }
+  __syncthreads();
+  // radix select, eight bits at a time from the top, of the need-th largest
+  // key among the 4 n_u items (the last one taken); fewer positive items than
+  // the budget: every positive item is taken (the cut falls to key 1)
+  unsigned long long cut = ~0ull;
+  if (S.need > 0) {
+    for (int shift = 56; shift >= 0; shift -= 8) {
+      for (int e = tid; e < 256; e += kVdThreads) S.hist[e] = 0u;
+      __syncthreads();
+      const unsigned long long pre = S.prefix;
+      const unsigned long long hi_mask = shift == 56 ? 0ull : (~0ull << (shift + 8));
+      for (int it = tid; it < 4 * n_u; it += kVdThreads) {
+        const unsigned long long k = vd_key(S.a[it >> 2], it >> 2, it & 3);
+        if (k != 0ull && (k & hi_mask) == pre) atomicAdd(&S.hist[(k >> shift) & 0xFF], 1u);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // bins from the top: the bin holding the need-th largest key
+        uint32_t need = S.need, acc = 0;
+        int sel = -1;
+        for (int base = 224; base >= 0 && sel < 0; base -= 32) {
+          const uint32_t c = S.hist[base + lane];
+          // inclusive sum from the top of this 32-bin slice (lane 31 highest)
+          uint32_t incl = c;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
+            if (lane + o < 32) incl += y;
+          }
+          const bool hit = acc + incl >= need && acc + incl - c < need;
+          const uint32_t hb = __ballot_sync(0xffffffffu, hit);
+          if (hb) {
+            const int l = 31 - __clz(hb);  // the one lane where the running count crosses need
+            const uint32_t before = __shfl_sync(0xffffffffu, acc + incl - c, l);
+            sel = base + l;
+            need -= before;
+          } else {
+            acc += __shfl_sync(0xffffffffu, incl, 0);
+          }
+        }
+        if (lane == 0) {
+          if (sel < 0) {
+            S.need = 0u;  // fewer positive items than the budget
+          } else {
+            S.prefix = pre | ((unsigned long long)sel << shift);
+            S.need = need;
+          }
+        }
+      }
+      __syncthreads();
+      if (S.need == 0u) break;
+    }
+    cut = S.need == 0u ? 1ull : S.prefix;
+  }
+  __syncthreads();
+  // depth of each row: its items at or above the cut
+  for (int r = tid; r < n_u; r += kVdThreads) {
+    int t = 0;
+    if (a.budget_v > 0) {
+#pragma unroll
+      for (int tt = 0; tt < 4; ++tt) t += vd_key(S.a[r], r, tt) >= cut ? 1 : 0;
+    }
+    S.dep[r] = (uint8_t)t;
+    if (a.vdepth) a.vdepth[unit * a.u_cap + r] = (uint8_t)t;
+    if (a.weight) a.weight[unit * a.u_cap + r] = S.a[r];
+  }
+  __syncthreads();
+  // o_h = sum_r p_h(r) vhat_r(t_r): warp per row, lane channels l, l + 32,
+  // l + 64, l + 96 (word 0 bits l and l + 32, word 1 bits l and l + 32)
+  float acc[GP][4];
+#pragma unroll
+  for (int h = 0; h < GP; ++h)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[h][i] = 0.f;
+  const uint64_t* vpu = a.vplanes + unit * a.cap * (kPlanes * kD / 64);
+  const uint16_t* vsu = a.vscales + unit * a.cap;
+  for (int r = warp; r < n_u; r += kVdWarps) {
+    const int t = S.dep[r];
+    if (t == 0) continue;
+    const int64_t tok = rows[r];
+    const float s = fp16_bits_to_float(vsu[tok]);
+    const uint64_t* w = vpu + tok * (kPlanes * kD / 64);
+    uint32_t c[4] = {0u, 0u, 0u, 0u};
+    for (int pl = 0; pl < t; ++pl) {
+      const uint64_t w0 = w[2 * pl], w1 = w[2 * pl + 1];
+      c[0] = (c[0] << 1) | (uint32_t)((w0 >> lane) & 1u);
+      c[1] = (c[1] << 1) | (uint32_t)((w0 >> (lane + 32)) & 1u);
+      c[2] = (c[2] << 1) | (uint32_t)((w1 >> lane) & 1u);
+      c[3] = (c[3] << 1) | (uint32_t)((w1 >> (lane + 32)) & 1u);
+    }
+    const float step = ldexpf(s, 4 - t);  // s 2^(4 - t)
+    float vh[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) vh[i] = fmaf((float)c[i] + 0.5f, step, -8.f * s);
+#pragma unroll
+    for (int h = 0; h < GP; ++h) {
+      const float pr = S.p[h][r];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[h][i] = fmaf(pr, vh[i], acc[h][i]);
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < GP; ++h)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) atomicAdd(&S.o[h][lane + 32 * i], acc[h][i]);
+  __syncthreads();
+  for (int e = tid; e < G * kD; e += kVdThreads) a.out[unit * G * kD + e] = S.o[e / kD][e % kD];
+}
+
+size_t vdepth_smem(int group) {
+  if (group <= 1) return sizeof(VdSmem<1>);
+  if (group <= 2) return sizeof(VdSmem<2>);
+  if (group <= 4) return sizeof(VdSmem<4>);
+  return sizeof(VdSmem<8>);
+}
+
+template <int GP>
+cudaError_t launch_vdepth_gp(const VdArgs& a, unsigned units, cudaStream_t st) {
+  const int smem = (int)sizeof(VdSmem<GP>);
+  cudaError_t e = cudaFuncSetAttribute(k_attend_vdepth<GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_attend_vdepth<GP>, dim3(units), dim3(kVdThreads), (size_t)smem, st, a);
+}
+
+cudaError_t launch_attend_vdepth(const bpkv_cache& c, const float* q, const int32_t* uidx, const uint8_t* umask,
+                                 const int32_t* ucount, int32_t u_cap, int32_t budget_v, float* out,
+                                 uint8_t* vdepth, float* weight, cudaStream_t st) {
+  VdArgs a{q, c.k_rows, c.vplanes, c.vscales, uidx, umask, ucount, u_cap, c.group, budget_v, c.cap_tokens,
+           out, vdepth, weight};
+  const unsigned units = (unsigned)(c.n_seq * c.n_kv_heads);
+  if (c.group <= 1) return launch_vdepth_gp<1>(a, units, st);
+  if (c.group <= 2) return launch_vdepth_gp<2>(a, units, st);
+  if (c.group <= 4) return launch_vdepth_gp<4>(a, units, st);
+  return launch_vdepth_gp<8>(a, units, st);
+}
+
+}  // namespace bpkv

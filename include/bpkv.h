@@ -92,6 +92,16 @@ extern "C" {
  * exact attention stay in the original channels.  The stand-alone depth, scan
  * and top-k calls take q already in the basis (bpkv_rotate).  Set the basis
  * before the first append.
+ * vplanes, vscales (optional, NULL: no value planes; both or neither) hold the
+ * values' own 4-bit code for the value-side read depth (ReadKV page,
+ * sections 5.3-5.4): one fp16 scale per row, token-major planes
+ *   vplanes uint64 [N][H][cap][4][D/64]  word (x, p, w): bit b is bit (3 - p) of
+ *                                        the code of channel 64 w + b of token x
+ *   vscales uint16 [N][H][cap]           fp16 bit pattern of s = max_j |v_xj| / 8
+ * with the keys' code, c = clip(floor(v / s), -8, 7) + 8 (all 8 when s rounds
+ * to 0), so the first t planes of a row are its t-bit mid-rise quantiser.
+ * bpkv_encode_append and bpkv_decode_step write them for every appended token
+ * when present (same residency as the rows; 16-byte aligned).
  */
 typedef struct bpkv_cache {
   int32_t n_seq;
@@ -108,6 +118,8 @@ typedef struct bpkv_cache {
   uint16_t *v_rows;
   int64_t *seq_len;
   const float *basis;
+  uint64_t *vplanes;
+  uint16_t *vscales;
 } bpkv_cache;
 
 /* ------------------------------------------------------------- workspace */
@@ -296,6 +308,30 @@ int bpkv_sparse_attend(const bpkv_cache *c, const float *q, const int32_t *uidx,
                        const int32_t *ucount, int32_t u_cap, float *out, void *ws, size_t ws_bytes,
                        void *stream);
 
+/*
+ * Value-side read depth (ReadKV page, section 5.3: the approximate attention
+ * decides each value row's depth; section 5.4: the allocator), over the union
+ * of each KV head's selections: head h's probabilities p_h(r) = softmax over
+ * its own rows of q_h . k_r / sqrt(D) with the exact bf16 keys; row weights
+ * a_r = sum_h p_h(r)^2 (float32); depths t_r by greedy on a_r 4^-t_r, one
+ * plane per item, largest first (ties to the lower row), at most budget_v
+ * planes per (sequence, KV head), items worth <= 0 never taken; then
+ * o_h = sum_r p_h(r) vhat_r(t_r) with each value row read to its depth from
+ * the cache's vplanes / vscales: vhat = s ((c_t + 1/2) 2^(4-t) - 8), the zero
+ * row at t = 0.  The depths are those of the float32 weights: where two
+ * weights are within float32 rounding the order may differ from an exact
+ * evaluation's.
+ *   uidx/umask/ucount, u_cap as bpkv_union writes them (u_cap <= 2048)
+ *   out    float [N][H][G][D]
+ *   vdepth uint8 [N][H][u_cap] (optional, NULL to skip): depth of each union row
+ *   weight float [N][H][u_cap] (optional, NULL to skip): a_r
+ * BPKV_EINVAL when the cache has no value planes, u_cap is outside 1..2048 or
+ * budget_v < 0.  No workspace.
+ */
+int bpkv_sparse_attend_vdepth(const bpkv_cache *c, const float *q, const int32_t *uidx, const uint8_t *umask,
+                              const int32_t *ucount, int32_t u_cap, int32_t budget_v, float *out, uint8_t *vdepth,
+                              float *weight, void *stream);
+
 /* Dense bf16 attention over every stored row (the dense baseline), same output
  * layout.  Needs workspace BPKV_WS_DENSE. */
 int bpkv_dense_attend(const bpkv_cache *c, const float *q, float *out, void *ws, size_t ws_bytes,
@@ -324,18 +360,26 @@ typedef struct bpkv_step_args {
                                recorded on `stream` (as external events, so they also
                                time graph replays) before encode, depths, scan, top-k,
                                union, attention and after attention */
-  int32_t flags;            /* reserved: 0 */
+  int32_t flags;            /* BPKV_STEP_* (0: keys only) */
   const uint8_t *depths_in; /* [L][N][H][D] BPKV_DEPTH_GIVEN: depth of every channel (values above
                                4 read as 4; depths_out, if given, receives them as read) */
+  int32_t budget_v;         /* BPKV_STEP_VDEPTH: value planes per (sequence, KV head) */
+  uint8_t *vdepth_out;      /* BPKV_STEP_VDEPTH, optional [L][N][H][G k]: depth of each union row */
 } bpkv_step_args;
 
 #define BPKV_STAGE_EVENTS 7
+#define BPKV_STEP_VDEPTH 1      /* read the value rows to per-row depths (bpkv_sparse_attend_vdepth)
+                                   instead of in full; the cache needs value planes */
 
 /*
  * One decode step over n_layers layers (each its own bpkv_cache, same shapes):
  * append the new token (encode), choose depths, scan + top-k, union, sparse
  * attention (or dense attention for BPKV_DEPTH_DENSE).  Every layer's n_max is
- * raised by one.  Needs workspace BPKV_WS_STEP.  BPKV_EINVAL when flags is not 0.
+ * raised by one.  Needs workspace BPKV_WS_STEP.  With BPKV_STEP_VDEPTH the
+ * step forms each KV head's union list and attends with value-side depths
+ * (bpkv_sparse_attend_vdepth, budget_v planes per sequence and KV head).
+ * BPKV_EINVAL for other flags, or BPKV_STEP_VDEPTH on a cache without value
+ * planes, with budget_v < 0 or with G k > 2048.
  */
 int bpkv_decode_step(bpkv_cache *layers, int32_t n_layers, const bpkv_step_args *a, void *ws,
                      size_t ws_bytes, void *stream);

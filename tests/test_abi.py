@@ -20,7 +20,7 @@ def test_exports_every_header_symbol(L):
     assert len(names) >= 15
     for n in names:
         assert hasattr(L, n), n
-    assert L.bpkv_version() == 1
+    assert L.bpkv_version() == 2
 
 
 def test_binding_names_match_header():
