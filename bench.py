@@ -46,7 +46,7 @@ ISSUE_PER_SM_CLK = 4      # warp instructions issued per SM per clock (one per s
 FMA_PER_SM_CLK = 128      # float32 fused multiply-adds per SM per clock
 
 
-def launches_per_pass(cap: int, rows: int) -> int:
+def launches_per_pass(cap: int, rows: int, group: int) -> int:
     """Kernels bpkv_decode_step launches per layer: the front kernel (append
     beside depths and plan), the scan, the cut and the range attention, plus
     the level-1 histogram kernel before the cut on rows of 131072 keys or more
@@ -70,6 +70,7 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--no-vdepth", action="store_true", help="skip the value-side depth sub-record")
     p.add_argument("--no-host", action="store_true",
                    help="skip the host-resident sub-record (one layer of the million-token workload)")
     p.add_argument("--budget", type=int, default=0, help="run this budget only (bits/token)")
@@ -159,7 +160,8 @@ class Clocks:
 
 # ------------------------------------------------------------------ workload
 
-def make_workload(cfg, steps: int, warmup: int, dev, budgets=None):
+def make_workload(cfg, steps: int, warmup: int, dev, budgets=None, values: bool = False, step_flags: int = 0,
+                  budget_v: int = 0):
     """Caches and step inputs.  One pass per budget; each pass decodes all the
     config's layers (each layer its own cache).  Host-resident configs build each
     layer's cache in device memory and move it to pinned host memory."""
@@ -193,7 +195,7 @@ def make_workload(cfg, steps: int, warmup: int, dev, budgets=None):
             if share and b != budgets[0]:
                 caches[b].append(caches[budgets[0]][-1])
                 continue
-            c = pk.Cache(N, H, G, cap, device=dev)
+            c = pk.Cache(N, H, G, cap, device=dev, values=values)
             c.append(inp.k[:, :, : n - 1].contiguous(), inp.v[:, :, : n - 1].contiguous())
             if host:
                 hc = pk.Cache(N, H, G, cap, device=dev, residency="host")
@@ -222,6 +224,7 @@ def make_workload(cfg, steps: int, warmup: int, dev, budgets=None):
         p["out"] = torch.zeros((L, N, H, G, D), dtype=torch.float32, device=dev)
         p["depths"] = torch.zeros((L, N, H, D), dtype=torch.uint8, device=dev)
         p["idx"] = torch.zeros((L, N, H, G, cfg.k), dtype=torch.int32, device=dev)
+        p["vdepth"] = torch.zeros((L, N, H, G * cfg.k), dtype=torch.uint8, device=dev) if values else None
         p["events"] = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(L)]
         for row in p["events"]:
             for e in row:
@@ -233,12 +236,13 @@ def make_workload(cfg, steps: int, warmup: int, dev, budgets=None):
                   p["out"].data_ptr(), p["depths"].data_ptr())
         # timed steps write no index lists (the attention reads the selection cuts);
         # one untimed step with lists afterwards gives the union sizes for the byte count
-        p["args_lists"] = pk.bpkv_step_args(*common, p["idx"].data_ptr(), None, 0)
+        vd = (None, budget_v, p["vdepth"].data_ptr()) if values else ()
+        p["args_lists"] = pk.bpkv_step_args(*common, p["idx"].data_ptr(), None, step_flags, *vd)
         common = common + (None,)
         # timed graph: no event nodes (each costs about 2 us inside a graph)
-        p["args"] = pk.bpkv_step_args(*common, None, 0)
+        p["args"] = pk.bpkv_step_args(*common, None, step_flags, *vd)
         # breakdown graph: events at every stage boundary
-        p["args_ev"] = pk.bpkv_step_args(*common, ctypes.cast(p["ev_arr"], ctypes.c_void_p), 0)
+        p["args_ev"] = pk.bpkv_step_args(*common, ctypes.cast(p["ev_arr"], ctypes.c_void_p), step_flags, *vd)
         passes.append(p)
     torch.cuda.synchronize()
     passes[0]["shared_caches"] = share
@@ -492,7 +496,7 @@ def bench_ours(args, cfg, rank, world, local):
     e2e = None if args.no_extras else bench_e2e(args, passes, io, ws, flush, dev, keys_per_step, world)
     baselines = None if args.no_extras else bench_baselines(args, cfg, passes, io, ws, flush, dev, world)
     cap = passes[0]["cap"]
-    n_launches = args.steps * n_launch * launches_per_pass(cap, N * H * G)
+    n_launches = args.steps * n_launch * launches_per_pass(cap, N * H * G, G)
 
     line = {
         "metric": "keys scored/s", "value": round(value), "unit": "keys/s", "n_gpus": world,
@@ -538,7 +542,69 @@ def bench_ours(args, cfg, rank, world, local):
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
         line["host_resident"] = bench_host(args, dev)
+    if not args.no_extras and not args.no_vdepth and cfg.residency != "host":
+        line["value_depth"] = bench_vdepth(args, dev)
     return line
+
+
+def bench_vdepth(args, dev) -> dict:
+    """One Qwen3-8B-shaped layer (8 KV heads, G = 4, n = 32768, k = 512) with
+    value planes: the decode step with value-side read depth (ReadKV page,
+    sections 5.3-5.4; value rows read to per-row depths, about two planes per
+    union row) beside the same step reading the value rows in full, budgets
+    68, 92, 136; per pass the stage times, the value bytes each reads and the
+    value stage's rate."""
+    import torch
+    import bit_plane_kv_encode_gb300 as pk
+    from workload import CONFIGS
+    cfg = CONFIGS["qwen3_8b_layer"]
+    steps = max(3, min(args.steps, 20))
+    budget_v = 2 * cfg.group * cfg.k  # planes per (sequence, KV head): ~2 per union row
+    out = {"workload": cfg.name, "budget_v_planes_per_unit": budget_v, "passes": {}}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for mode in ("vdepth", "full"):
+        _, passes, ws, io = make_workload(cfg, steps, 3, dev, values=True,
+                                          step_flags=pk.STEP_VDEPTH if mode == "vdepth" else 0, budget_v=budget_v)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=torch.cuda.Stream(device=dev)):
+            run_step(passes, ws, events=True)
+        pk.bpkv_clear_status(ws)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        per_pass = [{st: [] for st in STAGES} for _ in passes]
+        step_ms = []
+        for _ in range(steps):
+            step_ms += time_graph(graph, flush, 1)
+            for i, t in enumerate(stage_times_ms(passes)):
+                for st, v in t.items():
+                    per_pass[i][st].append(v)
+        if pk.bpkv_read_status(ws) != 0:
+            raise RuntimeError("device status after the value-depth passes")
+        run_step(passes, ws, lists=True)
+        torch.cuda.synchronize()
+        pb = pass_bytes(cfg, passes)
+        for p, b, pp in zip(passes, pb, per_pass):
+            at = statistics.mean(pp["attend"])
+            rec = {"layer_us": round(sum(statistics.mean(v) for v in pp.values()) * 1e3, 1),
+                   "attend_us": round(at * 1e3, 1), "union_rows": b["union_rows"],
+                   "v_full_bytes": b["union_rows"] * cfg.head_dim * 2}
+            if mode == "vdepth":
+                vd = p["vdepth"].to(torch.int64)
+                planes = int(vd.sum())
+                read = int((vd > 0).sum())
+                rec.update({"v_planes": planes, "v_bytes": planes * cfg.head_dim // 8 + 2 * read,
+                            "k_bytes": b["union_rows"] * cfg.head_dim * 2})
+                rec["v_bytes_frac_of_full"] = round(rec["v_bytes"] / rec["v_full_bytes"], 4)
+                rec["stage_gbs"] = round((rec["v_bytes"] + rec["k_bytes"]) / (at / 1e3) / 1e9, 1)
+            out["passes"].setdefault(str(p["budget"]), {})[mode] = rec
+        del passes, ws, io, graph
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    out["note"] = ("'vdepth': front, scan, cut with index lists, union, value-depth stage (one CTA per unit: exact-key "
+                   "softmax, row weights, plane allocation, value rows read to their depths); 'full': the default "
+                   "path (range attention over full bf16 rows); attend_us is the last stage of each")
+    return out
 
 
 def numa_info(ptr: int) -> dict:

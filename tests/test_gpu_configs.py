@@ -108,3 +108,20 @@ def test_step_without_lists_matches(pk, wl, n_tok, rule, fixed, budget):
     assert torch.equal(r_l[1], r_n[1])
     assert torch.equal(r_l[3], r_n[3])
     assert (r_n[2] == 0).all()  # no lists were written
+
+
+@pytest.mark.parametrize("n_tok,k,fixed", [(20000 + 3, 512, (0, 4)), (20000 + 3, 36, (32, 4)), (5000, 37, (32, 4)),
+                                           (200000 + 9, 512, (8, 1))])
+def test_step_selection_edges(pk, orc, n_tok, k, fixed):
+    """Decode steps whose selection is decided by the scan's candidates at the
+    edges: every score equal (no channel read: ties all the way, the lowest
+    indices win), no middle token kept (k = 36), one kept (k = 37), and rows
+    longer than one scan CTA's part with few distinct score values."""
+    import dataclasses
+    from workload import CONFIGS, gen_layer
+    cfg = dataclasses.replace(CONFIGS["qwen3_8b_layer"], k=k, n_tokens=n_tok)
+    inp = gen_layer(cfg, 9, device="cuda", n_tokens=n_tok)
+    cache, d, idx, out = decode_one_layer(inp, cfg, depth_rule=1, fixed=fixed)
+    inp.k, inp.v = inp.k.cpu(), inp.v.cpu()
+    for h in (0, 5):
+        check_unit(orc, cfg, inp, cache, d, idx, out, 0, h, depth_rule=1, fixed=fixed, what=f"n{n_tok} k{k} h{h}")
