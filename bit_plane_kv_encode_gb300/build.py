@@ -18,8 +18,12 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 
 
-def lib_path() -> str:
-    return os.path.join(HERE, f"libbpkv_{platform.machine()}.so")
+def lib_path(checks: bool | None = None) -> str:
+    """The library (checks: the bounds-checked build; None: as the
+    BPKV_CHECKS environment variable says)."""
+    if checks is None:
+        checks = os.environ.get("BPKV_CHECKS") == "1"
+    return os.path.join(HERE, f"libbpkv_{'checks_' if checks else ''}{platform.machine()}.so")
 
 
 def _nvcc() -> str:
@@ -33,20 +37,25 @@ def _cuda_lib_dir(nvcc: str) -> str:
     return os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc))), "lib64")
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    out = lib_path()
+def build(force: bool = False, verbose: bool = False, checks: bool | None = None) -> str:
+    """Compile and link the library; checks: the bounds-checked variant
+    (-DBPKV_CHECKS=1, its own objects and library file)."""
+    if checks is None:
+        checks = os.environ.get("BPKV_CHECKS") == "1"
+    out = lib_path(checks)
     deps = [os.path.join(CSRC, s) for s in SOURCES] + [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "scan_core.cuh"), os.path.join(CSRC, "depths_core.cuh"),
                                                        os.path.join(CSRC, "encode_core.cuh"), os.path.join(CSRC, "value_core.cuh"),
                                                        os.path.join(INCLUDE, "bpkv.h")]
     if not force and os.path.exists(out) and os.path.getmtime(out) >= max(os.path.getmtime(d) for d in deps):
         return out
     nvcc = _nvcc()
-    objdir = os.path.join(HERE, "_build", platform.machine())
+    objdir = os.path.join(HERE, "_build", platform.machine() + ("_checks" if checks else ""))
     os.makedirs(objdir, exist_ok=True)
 
     def compile_one(src: str) -> tuple:
         obj = os.path.join(objdir, src.replace(".cu", ".o"))
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *(["-DBPKV_CHECKS=1"] if checks else []), "-I", INCLUDE, "-c",
+               os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")

@@ -31,7 +31,7 @@ cudaError_t launch_front(const bpkv_cache& c, const uint16_t* k_new, const uint1
                          const float* q, const float* sigma2, const int32_t* budget_q, int32_t depth_rule,
                          int32_t n_channels, int32_t depth, uint8_t* depths, void* plan, uint32_t* hist,
                          uint32_t* hist1, uint32_t* ctr, uint32_t* tickets, uint32_t* seq_tick, cudaStream_t st,
-                         const uint8_t* depths_in, float* q_rot);
+                         const uint8_t* depths_in, float* q_rot, int32_t* status = nullptr);
 bool scan_counts_hist(const bpkv_cache& c);
 cudaError_t launch_union(const bpkv_cache& c, const int32_t* idx, int32_t k, int32_t* uidx, uint8_t* umask,
                          int32_t* ucount, cudaStream_t st);
@@ -395,7 +395,7 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
     BPKV_TRY(cuda_status(launch_front(c, kn, vn, 1, q, s2, a->budget_q, a->depth_rule, a->fixed_channels,
                                       a->fixed_depth, depths, plan, sb.hist, l1 ? sb.hist1 : nullptr, sb.ctr,
                                       tickets, seq_tick, st, a->depths_in,
-                                      reinterpret_cast<float*>(at(ws, L.q_rot)))));
+                                      reinterpret_cast<float*>(at(ws, L.q_rot)), status)));
     c.n_max += 1;
     BPKV_TRY(mark(l, 1));
     BPKV_TRY(mark(l, 2));

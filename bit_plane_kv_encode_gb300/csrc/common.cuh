@@ -74,6 +74,24 @@ __device__ __forceinline__ void set_status(int32_t* status, int32_t bit) {
   if (status) atomicOr(status, bit);
 }
 
+// Bounds-checked builds (compiled with -DBPKV_CHECKS=1, a separate library):
+// indices the kernels compute into shared and global arrays are checked;
+// one outside [0, n) is recorded as BPKV_DEV_BOUNDS in the status word (when
+// the call has one) and replaced by 0, so the access stays inside the array.
+// Regular builds compile the checks away.
+#ifdef BPKV_CHECKS
+__device__ __forceinline__ int64_t bpkv_checked(int64_t i, int64_t n, int32_t* status) {
+  if (i < 0 || i >= n) {
+    set_status(status, BPKV_DEV_BOUNDS);
+    return 0;
+  }
+  return i;
+}
+#define BPKV_CHK(i, n, st) bpkv_checked((int64_t)(i), (int64_t)(n), (st))
+#else
+#define BPKV_CHK(i, n, st) (i)
+#endif
+
 // Programmatic dependent launch: every kernel of the library lets the next
 // kernel on its stream start launching at once, then waits until the kernel
 // before it has completed and its writes are visible.  Launches without the

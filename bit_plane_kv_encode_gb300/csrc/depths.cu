@@ -39,6 +39,7 @@ struct DepthArgs {
   int32_t depth;      // fixed sets only
   uint32_t* hist;     // optional [N][H][G][kTopkBins]: zeroed for the scan of this step
   uint32_t* ctr;      // optional [N][H][G][kSelCounters] selection counters: zeroed with hist
+  int32_t* status;    // optional device status word (bounds-checked builds record in it)
 };
 
 // Zero this unit's selection histograms (G kTopkBins words).
@@ -63,7 +64,7 @@ __device__ void emit_plan(const DepthArgs& a, int64_t unit, const uint8_t* dep) 
 #pragma unroll
     for (int hh = 0; hh < GP; ++hh) qv[hh] = hh < a.group ? qp[hh * kD + tid] : 0.f;
   }
-  scan_setup<GP>(P, X, t, qv);
+  scan_setup<GP>(P, X, t, qv, a.status);
   scan_store_plan<GP>(P, reinterpret_cast<ScanPlan<GP>*>(a.plan) + unit);
 }
 
@@ -209,9 +210,10 @@ cudaError_t launch_front(const bpkv_cache& c, const uint16_t* k_new, const uint1
                          const float* q, const float* sigma2, const int32_t* budget_q, int32_t depth_rule,
                          int32_t n_channels, int32_t depth, uint8_t* depths, void* plan, uint32_t* hist,
                          uint32_t* hist1, uint32_t* ctr, uint32_t* tickets, uint32_t* seq_tick, cudaStream_t st,
-                         const uint8_t* depths_in, float* q_rot) {
+                         const uint8_t* depths_in, float* q_rot, int32_t* status) {
   FrontArgs a;
-  a.d = DepthArgs{q, sigma2, budget_q, depths, c.n_kv_heads, c.group, tickets, plan, n_channels, depth, hist, ctr};
+  a.d = DepthArgs{q, sigma2, budget_q, depths, c.n_kv_heads, c.group, tickets, plan, n_channels, depth, hist, ctr,
+                  status};
   a.depth_rule = depth_rule;
   a.depths_in = depths_in;
   a.seq_tick = seq_tick;
@@ -239,7 +241,7 @@ cudaError_t launch_front(const bpkv_cache& c, const uint16_t* k_new, const uint1
 cudaError_t launch_alloc_depths(const bpkv_cache& c, const float* q, const float* sigma2, const int32_t* budget_q,
                                 uint8_t* depths, cudaStream_t st, uint32_t* tickets, void* plan, uint32_t* hist,
                                 uint32_t* ctr) {
-  DepthArgs a{q, sigma2, budget_q, depths, c.n_kv_heads, c.group, tickets, plan, 0, 0, hist, ctr};
+  DepthArgs a{q, sigma2, budget_q, depths, c.n_kv_heads, c.group, tickets, plan, 0, 0, hist, ctr, nullptr};
   return launch_depths_gp(c.group, [&](auto gp) {
     return launch_pdl(k_alloc_depths<decltype(gp)::value>, dim3(c.n_seq * c.n_kv_heads), dim3(kScanThreads), 0, st,
                       a);
@@ -249,7 +251,8 @@ cudaError_t launch_alloc_depths(const bpkv_cache& c, const float* q, const float
 cudaError_t launch_fixed_depths(const bpkv_cache& c, const float* q, int32_t n_channels, int32_t depth,
                                 uint8_t* depths, cudaStream_t st, uint32_t* tickets, void* plan, uint32_t* hist,
                                 uint32_t* ctr) {
-  DepthArgs a{q, nullptr, nullptr, depths, c.n_kv_heads, c.group, tickets, plan, n_channels, depth, hist, ctr};
+  DepthArgs a{q, nullptr, nullptr, depths, c.n_kv_heads, c.group, tickets, plan, n_channels, depth, hist, ctr,
+              nullptr};
   return launch_depths_gp(c.group, [&](auto gp) {
     return launch_pdl(k_fixed_depths<decltype(gp)::value>, dim3(c.n_seq * c.n_kv_heads), dim3(kScanThreads), 0, st,
                       a);

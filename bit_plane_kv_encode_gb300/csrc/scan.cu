@@ -43,7 +43,7 @@ struct ScanArgs {
   uint32_t* hist;  // optional [N][H][G][kTopkBins] level-0 selection histogram (zeroed by the caller)
   int32_t n_sink, n_recent;
   int32_t pending;  // tokens appended in this step but not yet in seq_len
-  int32_t* status;  // optional device status word (unused by the scan kernels today)
+  int32_t* status;  // optional device status word (bounds-checked builds record in it)
   int64_t chunks;   // chunks per unit (from the host bound on the sequence lengths)
   int64_t units;    // sequences x KV heads
 };
@@ -79,7 +79,7 @@ __device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& 
 #pragma unroll
       for (int hh = 0; hh < GP; ++hh) qv[hh] = hh < G ? qp[hh * kD + tid] : 0.f;
     }
-    scan_setup<GP>(S.P, S.X, t, qv);
+    scan_setup<GP>(S.P, S.X, t, qv, a.status);
   }
   const uint64_t* pl = a.planes + unit * kD * kPlanes * a.nb_cap;
   const uint16_t* sp = a.scales + unit * kD * a.nb_cap;
@@ -169,7 +169,7 @@ __device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& 
   if constexpr (!kHost) {
     // device caches: steps (chunk, pass), one chunk each
     const int64_t steps = (c_end - c_begin) * n_passes;
-    scan_issue<GP>(S, 0, pl, sp, a.nb_cap, c_begin * kScanBlocks, S.P.pass_g[0], S.P.pass_g[1], 1, 1, false);
+    scan_issue<GP>(S, 0, pl, sp, a.nb_cap, c_begin * kScanBlocks, S.P.pass_g[0], S.P.pass_g[1], 1, 1, false, a.status);
     int64_t ch = c_begin;  // chunk and pass of step i
     int ps = 0;
     for (int64_t i = 0; i < steps; ++i) {
@@ -180,14 +180,14 @@ __device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& 
         const int ps1 = ps + 1 == n_passes ? 0 : ps + 1;
         const int64_t ch1 = ps1 == 0 ? ch + 1 : ch;
         scan_issue<GP>(S, b ^ 1, pl, sp, a.nb_cap, ch1 * kScanBlocks, S.P.pass_g[ps1], S.P.pass_g[ps1 + 1], 1, 1,
-                       false);
+                       false, a.status);
       }
       const int g0 = S.P.pass_g[ps], g1 = S.P.pass_g[ps + 1];
       const int s0 = S.P.grp_base[g0], s1 = g1 < S.P.n_groups ? (int)S.P.grp_base[g1] : S.P.n_slots;
-      scan_form_u<GP>(S, b, s0, s1, lb, 1, 0, false);
+      scan_form_u<GP>(S, b, s0, s1, lb, 1, 0, false, a.status);
       __syncwarp();
       const int nbl = (int)min64(kScanBlocks, nb_valid - ch * kScanBlocks);
-      if (lb < nbl) scan_compute_pipe<GP>(S, b, g0, g1, s0, lb, 1, 0, false, keep, rot, A);
+      if (lb < nbl) scan_compute_pipe<GP>(S, b, g0, g1, s0, lb, 1, 0, false, keep, rot, A, a.status);
       if (++ps == n_passes) {
         finish_chunk(ch);
         ps = 0;
@@ -198,7 +198,7 @@ __device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& 
     // host caches: step i covers chunks [ch, ch + n_sub), pass ps
     int64_t ch = c_begin;
     int ps = 0, n_sub = span(c_begin);
-    scan_issue<GP>(S, 0, pl, sp, a.nb_cap, ch * kScanBlocks, S.P.pass_g[0], S.P.pass_g[1], sub, n_sub, true);
+    scan_issue<GP>(S, 0, pl, sp, a.nb_cap, ch * kScanBlocks, S.P.pass_g[0], S.P.pass_g[1], sub, n_sub, true, a.status);
     for (int64_t i = 0;; ++i) {
       const int b = (int)(i & 1);
       cp_async_wait_all();
@@ -208,15 +208,15 @@ __device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& 
       const int n_sub1 = ch1 < c_end ? span(ch1) : 0;
       if (n_sub1 > 0)
         scan_issue<GP>(S, b ^ 1, pl, sp, a.nb_cap, ch1 * kScanBlocks, S.P.pass_g[ps1], S.P.pass_g[ps1 + 1], sub,
-                       n_sub1, true);
+                       n_sub1, true, a.status);
       const int g0 = S.P.pass_g[ps], g1 = S.P.pass_g[ps + 1];
       const int s0 = S.P.grp_base[g0], s1 = g1 < S.P.n_groups ? (int)S.P.grp_base[g1] : S.P.n_slots;
       for (int c = 0; c < n_sub; ++c) {
         if (c > 0) __syncwarp();  // every lane is done reading the previous chunk's u
-        scan_form_u<GP>(S, b, s0, s1, lb, sub, c, true);
+        scan_form_u<GP>(S, b, s0, s1, lb, sub, c, true, a.status);
         __syncwarp();
         const int nbl = (int)min64(kScanBlocks, nb_valid - (ch + c) * kScanBlocks);
-        if (lb < nbl) scan_compute_pipe<GP>(S, b, g0, g1, s0, lb, sub, c, true, keep, rot, A);
+        if (lb < nbl) scan_compute_pipe<GP>(S, b, g0, g1, s0, lb, sub, c, true, keep, rot, A, a.status);
         if (ps + 1 == n_passes) finish_chunk(ch + c);
       }
       if (n_sub1 == 0) break;

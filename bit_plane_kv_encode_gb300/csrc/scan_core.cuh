@@ -113,7 +113,8 @@ __device__ __forceinline__ void transpose_consts(int lane, uint32_t (&keep)[5], 
 // in channel order.  Every layout figure follows in closed form from the four
 // per-depth channel counts.
 template <int GP>
-__device__ void scan_setup(ScanPlan<GP>& S, PlanScratch& X, int t, const float (&qv)[GP]) {
+__device__ void scan_setup(ScanPlan<GP>& S, PlanScratch& X, int t, const float (&qv)[GP],
+                           int32_t* status = nullptr) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int rank = 0;
   if (tid < kD) {
@@ -142,13 +143,14 @@ __device__ void scan_setup(ScanPlan<GP>& S, PlanScratch& X, int t, const float (
     n_slots += ng[d] * slot_pitch(d);
   }
   if (tid < n_groups) {
+    const int gi = (int)BPKV_CHK(tid, kMaxGroups, status);
 #pragma unroll
     for (int d = 4; d >= 1; --d) {
       if (tid >= goff[d] && tid < goff[d] + ng[d]) {
         const int i = tid - goff[d];
-        S.grp_t[tid] = (int8_t)d;
-        S.grp_base[tid] = (int16_t)(soff[d] + i * slot_pitch(d));
-        S.grp_cnt[tid] = (int8_t)min(group_cap(d), cnt[d] - i * group_cap(d));
+        S.grp_t[gi] = (int8_t)d;
+        S.grp_base[gi] = (int16_t)(soff[d] + i * slot_pitch(d));
+        S.grp_cnt[gi] = (int8_t)min(group_cap(d), cnt[d] - i * group_cap(d));
       }
     }
   }
@@ -194,11 +196,13 @@ __device__ void scan_setup(ScanPlan<GP>& S, PlanScratch& X, int t, const float (
     }
     const int gi = rank / group_cap(t), m = rank % group_cap(t);
     const int g = goff_t + gi, base = soff_t + gi * slot_pitch(t), P = slot_pitch(t);
-    S.slot_ch[base + m] = (int16_t)tid;
-    for (int p = 0; p < t; ++p) S.row_of_lane[g * 32 + m * t + (t - 1 - p)] = (int16_t)(tid * 4 + p);
+    S.slot_ch[BPKV_CHK(base + m, kMaxSlots, status)] = (int16_t)tid;
+    for (int p = 0; p < t; ++p)
+      S.row_of_lane[BPKV_CHK(g * 32 + m * t + (t - 1 - p), kMaxGroups * 32, status)] = (int16_t)(tid * 4 + p);
     // w = q 2^(4 - t - pos) per head, laid out [group][head][slot]; other slots stay 0
 #pragma unroll
-    for (int hh = 0; hh < GP; ++hh) S.w[(base + m) * GP + hh] = ldexpf(qv[hh], 4 - t - field_pos(t, m));
+    for (int hh = 0; hh < GP; ++hh)
+      S.w[BPKV_CHK((base + m) * GP + hh, kMaxSlots * GP, status)] = ldexpf(qv[hh], 4 - t - field_pos(t, m));
   }
   __syncthreads();
 }
@@ -431,7 +435,7 @@ __device__ __forceinline__ void acc_zero(Acc<GP>& A) {
 template <int GP>
 __device__ __forceinline__ void scan_issue(PipeSmem<GP>& S, int b, const uint64_t* pl, const uint16_t* sp,
                                            int64_t nb_cap, int64_t b0, int g0, int g1, int sub, int n_sub,
-                                           bool host) {
+                                           bool host, int32_t* status = nullptr) {
   const ScanPlan<GP>& P = S.P;
   const int sc_pitch = kScanBlocks * sub;
   const int n_row = (g1 - g0) * 32;
@@ -443,32 +447,36 @@ __device__ __forceinline__ void scan_issue(PipeSmem<GP>& S, int b, const uint64_
     for (int e = threadIdx.x; e < n_piece + n_sc; e += kScanThreads) {
       if (e < n_piece) {
         const int r = e >> (2 + sh), piece = e & ((4 << sh) - 1);
-        const int row = P.row_of_lane[g0 * 32 + r];
+        const int row = P.row_of_lane[BPKV_CHK(g0 * 32 + r, kMaxGroups * 32, status)];
         if (row >= 0)
-          cp_async16(&S.st[b].u32[staged_word(r, piece, sub, true)], pl + (int64_t)row * nb_cap + b0 + 2 * piece);
+          cp_async16(&S.st[b].u32[BPKV_CHK(staged_word(r, piece, sub, true), kHostStageWords - 3, status)],
+                     pl + BPKV_CHK((int64_t)row * nb_cap + b0 + 2 * piece, kD * kPlanes * nb_cap - 1, status));
       } else {
         const int f = e - n_piece, rel = f >> sh, c = f & sh;
-        const int ch = P.slot_ch[s0 + rel];
-        uint16_t* dst = stage_sc(S.st[b], host) + rel * sc_pitch + kScanBlocks * c;
-        if (ch >= 0) cp_async16(dst, sp + (int64_t)ch * nb_cap + b0 + kScanBlocks * c);
+        const int ch = P.slot_ch[BPKV_CHK(s0 + rel, kMaxSlots, status)];
+        uint16_t* dst = stage_sc(S.st[b], host) +
+                        BPKV_CHK(rel * sc_pitch + kScanBlocks * c, 2 * (kStageU32 - kHostStageWords) - 7, status);
+        if (ch >= 0) cp_async16(dst, sp + BPKV_CHK((int64_t)ch * nb_cap + b0 + kScanBlocks * c, kD * nb_cap - 7, status));
         else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);  // unused slot: scale 0
       }
     }
   } else {
     for (int e = threadIdx.x; e < n_row + n_sc; e += kScanThreads) {
       if (e < n_row) {
-        const int row = P.row_of_lane[g0 * 32 + e];
+        const int row = P.row_of_lane[BPKV_CHK(g0 * 32 + e, kMaxGroups * 32, status)];
         if (row >= 0) {
-          const uint64_t* src = pl + (int64_t)row * nb_cap + b0;
+          const uint64_t* src = pl + BPKV_CHK((int64_t)row * nb_cap + b0, kD * kPlanes * nb_cap - 8 * (1 << sh) + 1, status);
 #pragma unroll 4
           for (int piece = 0; piece < (4 << sh); ++piece)
-            cp_async16(&S.st[b].u32[staged_word(e, piece, sub, false)], src + 2 * piece);
+            cp_async16(&S.st[b].u32[BPKV_CHK(staged_word(e, piece, sub, false), kStageWords - 3, status)],
+                       src + 2 * piece);
         }
       } else {
         const int f = e - n_row, rel = f >> sh, c = f & sh;
-        const int ch = P.slot_ch[s0 + rel];
-        uint16_t* dst = stage_sc(S.st[b], host) + rel * sc_pitch + kScanBlocks * c;
-        if (ch >= 0) cp_async16(dst, sp + (int64_t)ch * nb_cap + b0 + kScanBlocks * c);
+        const int ch = P.slot_ch[BPKV_CHK(s0 + rel, kMaxSlots, status)];
+        uint16_t* dst = stage_sc(S.st[b], host) +
+                        BPKV_CHK(rel * sc_pitch + kScanBlocks * c, 2 * (kStageU32 - kStageWords) - 7, status);
+        if (ch >= 0) cp_async16(dst, sp + BPKV_CHK((int64_t)ch * nb_cap + b0 + kScanBlocks * c, kD * nb_cap - 7, status));
         else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);  // unused slot: scale 0
       }
     }
@@ -487,12 +495,15 @@ __device__ __forceinline__ float sw(float s, float w) { return s * w; }
 // per lane at a time, all heads with vector loads and stores.
 template <int GP>
 __device__ __forceinline__ void scan_form_u(PipeSmem<GP>& S, int b, int s0, int s1, int lb, int sub, int c,
-                                            bool host) {
+                                            bool host, int32_t* status = nullptr) {
   const int lane = threadIdx.x & 31;
   const int sc_pitch = kScanBlocks * sub;
   const uint16_t* sc = stage_sc(S.st[b], host) + kScanBlocks * c + lb;
   const float* w = S.P.w + s0 * GP;
   float* ud = S.u[lb];
+#ifdef BPKV_CHECKS
+  if (lane == 0 && (s0 < 0 || s1 > kMaxSlots || s1 - s0 > kPassSlots)) set_status(status, BPKV_DEV_BOUNDS);
+#endif
   for (int rel = lane; rel < s1 - s0; rel += 32) {
     const float sv = fp16_bits_to_float(sc[rel * sc_pitch]);
     if constexpr (GP == 1) {
@@ -517,7 +528,7 @@ __device__ __forceinline__ void scan_form_u(PipeSmem<GP>& S, int b, int s0, int 
 template <int GP>
 __device__ __forceinline__ void scan_compute_pipe(const PipeSmem<GP>& S, int b, int g0, int g1, int s0, int lb,
                                                   int sub, int c, bool host, const uint32_t (&keep)[5],
-                                                  const uint32_t (&rot)[5], Acc<GP>& A) {
+                                                  const uint32_t (&rot)[5], Acc<GP>& A, int32_t* status = nullptr) {
   const int lane = threadIdx.x & 31;
   const ScanPlan<GP>& P = S.P;
   // block lb of chunk c is word 2 (lb % 2) of 16-byte part 4 c + lb / 2 of
@@ -526,6 +537,12 @@ __device__ __forceinline__ void scan_compute_pipe(const PipeSmem<GP>& S, int b, 
   const int g_stride = 32 * row_pitch(sub, host);
   for (int g = g0; g < g1; ++g) {
     const int d = P.grp_t[g], cnt = P.grp_cnt[g];
+#ifdef BPKV_CHECKS
+    // the group's rows inside the stage, its slots inside the pass's u
+    if (lane == 0 && ((g - g0 + 1) * g_stride > (host ? kHostStageWords : kStageWords) || d < 1 || d > 4 ||
+                      (P.grp_base[g] - s0 + slot_pitch(d)) > kPassSlots || P.grp_base[g] < s0))
+      set_status(status, BPKV_DEV_BOUNDS);
+#endif
     const uint2 wv = *reinterpret_cast<const uint2*>(wl + (g - g0) * g_stride);
     const uint32_t x0 = warp_transpose32(wv.x, keep, rot);
     const uint32_t x1 = warp_transpose32(wv.y, keep, rot);

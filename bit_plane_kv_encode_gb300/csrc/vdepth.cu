@@ -29,6 +29,7 @@ namespace bpkv {
 constexpr int kVdThreads = 512;
 constexpr int kVdWarps = kVdThreads / 32;
 constexpr int kVdMaxRows = 2048;  // union rows of one unit (G k)
+constexpr int kVdBatch = 4;       // rows a warp loads at once
 
 struct VdArgs {
   const float* q;          // [N][H][G][D]
@@ -101,21 +102,32 @@ __global__ void __launch_bounds__(kVdThreads) k_attend_vdepth(VdArgs a) {
   __syncthreads();
   // logits q_h . k_r / sqrt(D) of the heads that selected row r (warp per row,
   // four channels per lane), -inf elsewhere
+  // kVdBatch rows per warp at a time, their loads issued together
   const float scale = rsqrtf((float)kD);
-  for (int r = warp; r < n_u; r += kVdWarps) {
-    const uint2 kv = *reinterpret_cast<const uint2*>(kr + (int64_t)rows[r] * kD + 4 * lane);
-    const float k0 = __uint_as_float(kv.x << 16), k1 = __uint_as_float(kv.x & 0xFFFF0000u);
-    const float k2 = __uint_as_float(kv.y << 16), k3 = __uint_as_float(kv.y & 0xFFFF0000u);
-    const uint32_t m = masks[r];
+  for (int r0 = warp; r0 < n_u; r0 += kVdWarps * kVdBatch) {
+    uint2 kv[kVdBatch];
 #pragma unroll
-    for (int h = 0; h < GP; ++h) {
-      const float* qh = S.q[h] + 4 * lane;
-      float d = qh[0] * k0;
-      d = fmaf(qh[1], k1, d);
-      d = fmaf(qh[2], k2, d);
-      d = fmaf(qh[3], k3, d);
-      d = vd_warp_sum(d);
-      if (lane == 0) S.p[h][r] = (h < G && ((m >> h) & 1)) ? d * scale : -INFINITY;
+    for (int u = 0; u < kVdBatch; ++u) {
+      const int r = min(r0 + u * kVdWarps, n_u - 1);
+      kv[u] = *reinterpret_cast<const uint2*>(kr + (int64_t)rows[r] * kD + 4 * lane);
+    }
+#pragma unroll
+    for (int u = 0; u < kVdBatch; ++u) {
+      const int r = r0 + u * kVdWarps;
+      if (r >= n_u) break;  // uniform across the warp
+      const float k0 = __uint_as_float(kv[u].x << 16), k1 = __uint_as_float(kv[u].x & 0xFFFF0000u);
+      const float k2 = __uint_as_float(kv[u].y << 16), k3 = __uint_as_float(kv[u].y & 0xFFFF0000u);
+      const uint32_t m = masks[r];
+#pragma unroll
+      for (int h = 0; h < GP; ++h) {
+        const float* qh = S.q[h] + 4 * lane;
+        float d = qh[0] * k0;
+        d = fmaf(qh[1], k1, d);
+        d = fmaf(qh[2], k2, d);
+        d = fmaf(qh[3], k3, d);
+        d = vd_warp_sum(d);
+        if (lane == 0) S.p[h][r] = (h < G && ((m >> h) & 1)) ? d * scale : -INFINITY;
+      }
     }
   }
   __syncthreads();
@@ -244,29 +256,46 @@ __global__ void __launch_bounds__(kVdThreads) k_attend_vdepth(VdArgs a) {
     for (int i = 0; i < 4; ++i) acc[h][i] = 0.f;
   const uint64_t* vpu = a.vplanes + unit * a.cap * (kPlanes * kD / 64);
   const uint16_t* vsu = a.vscales + unit * a.cap;
-  for (int r = warp; r < n_u; r += kVdWarps) {
-    const int t = S.dep[r];
-    if (t == 0) continue;
-    const int64_t tok = rows[r];
-    const float s = fp16_bits_to_float(vsu[tok]);
-    const uint64_t* w = vpu + tok * (kPlanes * kD / 64);
-    uint32_t c[4] = {0u, 0u, 0u, 0u};
-    for (int pl = 0; pl < t; ++pl) {
-      const uint64_t w0 = w[2 * pl], w1 = w[2 * pl + 1];
-      c[0] = (c[0] << 1) | (uint32_t)((w0 >> lane) & 1u);
-      c[1] = (c[1] << 1) | (uint32_t)((w0 >> (lane + 32)) & 1u);
-      c[2] = (c[2] << 1) | (uint32_t)((w1 >> lane) & 1u);
-      c[3] = (c[3] << 1) | (uint32_t)((w1 >> (lane + 32)) & 1u);
+  // kVdBatch rows per warp at a time: each lane loads one of the rows' plane
+  // words (row u: words 2 p + w at lanes 8 u + 2 p + w) and their scales, the
+  // warp shares them by shuffles
+  for (int r0 = warp; r0 < n_u; r0 += kVdWarps * kVdBatch) {
+    uint64_t wl = 0ull;
+    uint16_t sl = 0;
+    {
+      const int u = lane >> 3, r = r0 + u * kVdWarps;
+      if (u < kVdBatch && r < n_u && (lane & 7) < 2 * S.dep[r]) {
+        const int64_t tok = rows[r];
+        wl = vpu[tok * (kPlanes * kD / 64) + (lane & 7)];
+        if ((lane & 7) == 0) sl = vsu[tok];
+      }
     }
-    const float step = ldexpf(s, 4 - t);  // s 2^(4 - t)
-    float vh[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) vh[i] = fmaf((float)c[i] + 0.5f, step, -8.f * s);
+    for (int u = 0; u < kVdBatch; ++u) {
+      const int r = r0 + u * kVdWarps;
+      if (r >= n_u) break;  // uniform across the warp
+      const int t = S.dep[r];
+      if (t == 0) continue;
+      const float s = fp16_bits_to_float((uint16_t)__shfl_sync(0xffffffffu, (uint32_t)sl, 8 * u));
+      uint32_t c[4] = {0u, 0u, 0u, 0u};
+      for (int pl = 0; pl < t; ++pl) {
+        const uint64_t w0 = __shfl_sync(0xffffffffu, wl, 8 * u + 2 * pl);
+        const uint64_t w1 = __shfl_sync(0xffffffffu, wl, 8 * u + 2 * pl + 1);
+        c[0] = (c[0] << 1) | (uint32_t)((w0 >> lane) & 1u);
+        c[1] = (c[1] << 1) | (uint32_t)((w0 >> (lane + 32)) & 1u);
+        c[2] = (c[2] << 1) | (uint32_t)((w1 >> lane) & 1u);
+        c[3] = (c[3] << 1) | (uint32_t)((w1 >> (lane + 32)) & 1u);
+      }
+      const float step = ldexpf(s, 4 - t);  // s 2^(4 - t)
+      float vh[4];
 #pragma unroll
-    for (int h = 0; h < GP; ++h) {
-      const float pr = S.p[h][r];
+      for (int i = 0; i < 4; ++i) vh[i] = fmaf((float)c[i] + 0.5f, step, -8.f * s);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[h][i] = fmaf(pr, vh[i], acc[h][i]);
+      for (int h = 0; h < GP; ++h) {
+        const float pr = S.p[h][r];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[h][i] = fmaf(pr, vh[i], acc[h][i]);
+      }
     }
   }
 #pragma unroll

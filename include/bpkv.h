@@ -53,6 +53,8 @@ extern "C" {
 #define BPKV_DEV_OVERFLOW 1    /* append would pass cap_tokens; nothing written */
 #define BPKV_DEV_SELECT 2      /* a selection produced more rows than its output holds */
 #define BPKV_DEV_TIMEOUT 4     /* a wait inside a kernel for the other CTAs of its grid gave up */
+#define BPKV_DEV_BOUNDS 8      /* bounds-checked builds only: a computed index was outside its array
+                                  (the access was redirected to element 0) */
 
 #define BPKV_MAX_GROUP 8
 #define BPKV_HEAD_DIM 128
