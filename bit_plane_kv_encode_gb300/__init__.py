@@ -12,7 +12,7 @@ import ctypes
 
 from ._binding import (  # noqa: F401
     BpkvError, bpkv_alloc_depths, bpkv_cache, bpkv_calibrate_channels, bpkv_clear_status, bpkv_decode_step,
-    bpkv_dense_attend, bpkv_encode_append, bpkv_fixed_depths, bpkv_read_status, bpkv_rotate, bpkv_scan, bpkv_scan_topk, bpkv_scan_topk_noalloc, bpkv_selftest_wait, bpkv_sparse_attend, bpkv_sparse_attend_vdepth,
+    bpkv_dense_attend, bpkv_encode_append, bpkv_fixed_depths, bpkv_read_status, bpkv_rotate, bpkv_row_cache_stats, bpkv_scan, bpkv_scan_topk, bpkv_scan_topk_noalloc, bpkv_selftest_wait, bpkv_sparse_attend, bpkv_sparse_attend_vdepth,
     bpkv_status_string, bpkv_step_args, bpkv_topk, bpkv_union, bpkv_version, bpkv_workspace_size, header_symbols, load)
 
 HEAD_DIM = 128
@@ -30,7 +30,7 @@ class Cache:
     """
 
     def __init__(self, n_seq: int, n_kv_heads: int, group: int, cap_tokens: int, device="cuda",
-                 residency: str = "hbm", values: bool = False):
+                 residency: str = "hbm", values: bool = False, rc_slots: int = 0):
         import torch
         if cap_tokens % 512:
             raise ValueError("cap_tokens must be a multiple of 512")
@@ -64,6 +64,14 @@ class Cache:
                             self.planes.data_ptr(), self.scales.data_ptr(), self.k_rows.data_ptr(),
                             self.v_rows.data_ptr(), self.seq_len.data_ptr(), None,
                             self.vplanes.data_ptr() if values else None, self.vscales.data_ptr() if values else None)
+        # device row cache of recently selected rows (host-resident caches)
+        self.rc_rows = self.rc_tok = None
+        if rc_slots:
+            self.rc_rows = torch.empty((n_seq, n_kv_heads, rc_slots, 2, D), dtype=torch.bfloat16, device=self.device)
+            self.rc_tok = torch.full((n_seq, n_kv_heads, rc_slots), -1, dtype=torch.int32, device=self.device)
+            self.c.rc_rows = self.rc_rows.data_ptr()
+            self.c.rc_tok = self.rc_tok.data_ptr()
+            self.c.rc_slots = rc_slots
 
     def set_basis(self, basis):
         """Code the keys in an orthogonal basis R, float [H][D][D] on the device

@@ -31,7 +31,7 @@ class bpkv_cache(ctypes.Structure):
         ("n_seq", i32), ("n_kv_heads", i32), ("group", i32), ("head_dim", i32),
         ("cap_tokens", i64), ("n_max", i64), ("residency", i32), ("reserved", i32),
         ("planes", P), ("scales", P), ("k_rows", P), ("v_rows", P), ("seq_len", P), ("basis", P),
-        ("vplanes", P), ("vscales", P),
+        ("vplanes", P), ("vscales", P), ("rc_rows", P), ("rc_tok", P), ("rc_slots", i32), ("rc_reserved", i32),
     ]
 
 
@@ -52,6 +52,7 @@ _SIGS = {
     "bpkv_clear_status": ([P, P], ctypes.c_int),
     "bpkv_read_status": ([P, P, P], ctypes.c_int),
     "bpkv_selftest_wait": ([P, i32, i32, P], ctypes.c_int),
+    "bpkv_row_cache_stats": ([P, i32, P, P, P], ctypes.c_int),
     "bpkv_encode_append": ([P, P, P, i32, P], ctypes.c_int),
     "bpkv_alloc_depths": ([P, P, P, P, P, P], ctypes.c_int),
     "bpkv_fixed_depths": ([P, P, i32, i32, P, P], ctypes.c_int),
@@ -147,6 +148,15 @@ def bpkv_read_status(ws, stream=None) -> int:
     if rc not in (0, -5):
         _check("bpkv_read_status", rc)
     return int(st.value)
+
+
+def bpkv_row_cache_stats(cache, k: int, ws, stream=None):
+    """(hits, misses) per (sequence, KV head) of the last step: numpy uint32 [N][H][2]."""
+    import numpy as np
+    out = np.zeros((cache.n_seq, cache.n_kv_heads, 2), dtype=np.uint32)
+    _check("bpkv_row_cache_stats", load().bpkv_row_cache_stats(ctypes.byref(cache), int(k), _ptr(ws),
+                                                                out.ctypes.data_as(ctypes.c_void_p), _stream(stream)))
+    return out
 
 
 def bpkv_selftest_wait(ws, arrivals: int, spin_limit: int, stream=None):

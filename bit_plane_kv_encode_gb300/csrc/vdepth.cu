@@ -26,10 +26,10 @@ namespace bpkv {
 
 // ---------------------------------------------------------------- stage 2
 
-constexpr int kVdThreads = 512;
+constexpr int kVdThreads = 768;
 constexpr int kVdWarps = kVdThreads / 32;
 constexpr int kVdMaxRows = 2048;  // union rows of one unit (G k)
-constexpr int kVdBatch = 4;       // rows a warp loads at once
+constexpr int kVdBatch = 4;       // rows a warp loads at once (the value phase: one row per 8 lanes)
 
 struct VdArgs {
   const float* q;          // [N][H][G][D]

@@ -104,6 +104,20 @@ extern "C" {
  * to 0), so the first t planes of a row are its t-bit mid-rise quantiser.
  * bpkv_encode_append and bpkv_decode_step write them for every appended token
  * when present (same residency as the rows; 16-byte aligned).
+ * rc_rows, rc_tok, rc_slots (optional, rc_slots = 0: none; host-resident
+ * caches only) are a device-memory cache of recently selected rows, so that
+ * rows selected again in later steps are read from HBM instead of over the
+ * host link (the KVDrive page's reuse of critical KV across steps; Fathom
+ * page, section 1: the winner rows' k_U R term):
+ *   rc_rows uint16 [N][H][rc_slots][2][D]  the bf16 K row, then the V row, held in each slot
+ *   rc_tok  int32  [N][H][rc_slots]        token held by each slot, -1 for none (the caller
+ *                                          fills it with -1 before the first step)
+ * rc_slots is a power of two from 64 to 2^20; token x can sit only in slot
+ * x mod rc_slots.  bpkv_decode_step reads a selected row from its slot when
+ * the slot holds that token, and after the attention places the rows it read
+ * over the link in their slots (of several such rows with one slot, the
+ * latest token wins).  Rows never change once appended, so a cached row is
+ * always the current one; results are identical with or without the cache.
  */
 typedef struct bpkv_cache {
   int32_t n_seq;
@@ -122,6 +136,10 @@ typedef struct bpkv_cache {
   const float *basis;
   uint64_t *vplanes;
   uint16_t *vscales;
+  uint16_t *rc_rows;
+  int32_t *rc_tok;
+  int32_t rc_slots;
+  int32_t rc_reserved;
 } bpkv_cache;
 
 /* ------------------------------------------------------------- workspace */
@@ -368,6 +386,15 @@ typedef struct bpkv_step_args {
   int32_t budget_v;         /* BPKV_STEP_VDEPTH: value planes per (sequence, KV head) */
   uint8_t *vdepth_out;      /* BPKV_STEP_VDEPTH, optional [L][N][H][G k]: depth of each union row */
 } bpkv_step_args;
+
+/*
+ * Hits and misses of the row cache in the last bpkv_decode_step that used
+ * this workspace (summed over its layers): synchronises `stream`, then
+ * out[2 (seq H + h)] = selected rows read from the row cache and out[... + 1]
+ * = rows read over the host link, for every (sequence, KV head) (host array
+ * of 2 N H).  The workspace must be the step's (same cache shape and k).
+ */
+int bpkv_row_cache_stats(const bpkv_cache *c, int32_t k, const void *ws, uint32_t *out, void *stream);
 
 #define BPKV_STAGE_EVENTS 7
 #define BPKV_STEP_VDEPTH 1      /* read the value rows to per-row depths (bpkv_sparse_attend_vdepth)

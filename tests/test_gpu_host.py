@@ -93,3 +93,54 @@ def test_host_1m_layer_sampled(pk, orc):
     inp.k, inp.v = inp.k.cpu(), inp.v.cpu()
     for h in (0, 5):
         check_unit(orc, cfg, inp, host_cache, d, idx, out, 0, h, what=f"host1m h{h}")
+
+
+def test_row_cache_identical_and_hits(pk):
+    """The device row cache of recently selected rows (host-resident caches):
+    over steps whose queries drift, outputs equal those of the same cache
+    without it bit for bit, the first step reads every row over the link and
+    later steps find most rows in the row cache."""
+    from workload import CONFIGS, gen_layer
+    cfg = CONFIGS["host_1m"]
+    n0, steps = 65536 - 8, 6
+    inp = gen_layer(cfg, 2, device="cuda", n_tokens=n0 + steps)
+    N, H, n_all, D = inp.k.shape
+    G = cfg.group
+    cap = (n_all + 1023) // 1024 * 1024
+    dev_cache = build_cache(inp.k, inp.v, G, cap=cap, n_prefill=n0)
+    plain = pk.Cache(N, H, G, cap, residency="host")
+    cached = pk.Cache(N, H, G, cap, residency="host", rc_slots=4096)
+    plain.copy_from(dev_cache)
+    cached.copy_from(dev_cache)
+    torch.cuda.synchronize()
+    g = torch.Generator().manual_seed(5)
+    drift = torch.randn(inp.q.shape, generator=g)
+    dev = torch.device("cuda")
+    outs = {}
+    stats = []
+    for name, cache in (("plain", plain), ("cached", cached)):
+        ws = cache.workspace(cfg.k, pk.WS_STEP)
+        arr = pk.cache_array([cache])
+        outs[name] = []
+        for t in range(steps):
+            q = (inp.q + 0.05 * t * drift).to(dev)[None].contiguous()
+            s2 = inp.sigma2.to(dev)[None].contiguous()
+            bq = (4 * inp.budgets).to(torch.int32).to(dev)
+            kn = inp.k[:, :, n0 + t][None].contiguous()
+            vn = inp.v[:, :, n0 + t][None].contiguous()
+            out = torch.zeros((1, N, H, G, D), device=dev)
+            a = pk.bpkv_step_args(kn.data_ptr(), vn.data_ptr(), q.data_ptr(), s2.data_ptr(), bq.data_ptr(), 0, 0, 0,
+                                  cfg.k, cfg.n_sink, cfg.n_recent, out.data_ptr(), None, None, None, 0)
+            pk.bpkv_clear_status(ws)
+            pk.bpkv_decode_step(arr, 1, a, ws, ws.numel())
+            torch.cuda.synchronize()
+            assert pk.bpkv_read_status(ws) == 0
+            outs[name].append(out.clone())
+            if name == "cached":
+                stats.append(pk.bpkv_row_cache_stats(arr[0], cfg.k, ws))
+        pk.sync_n_max([cache], arr)
+    for t in range(steps):
+        assert torch.equal(outs["plain"][t], outs["cached"][t]), f"step {t}"
+    assert (stats[0][..., 0] == 0).all() and (stats[0][..., 1] > 0).all()  # first step: all misses
+    later = np.stack(stats[1:])
+    assert later[..., 0].sum() > 0.5 * later.sum(), later.sum(axis=(1, 2))
