@@ -19,10 +19,7 @@ bool attend_ranges_eligible(const bpkv_cache& c, int32_t k);
 cudaError_t launch_attend_ranges(const bpkv_cache& c, const float* q, const float* scores, int64_t ld,
                                  const unsigned long long* cut, int32_t n_sink, int32_t n_recent, float* part,
                                  uint32_t* tickets, float* out, int32_t pending, uint32_t* seq_tick,
-                                 cudaStream_t st, int32_t* rc_miss = nullptr, uint32_t* rc_nmiss = nullptr,
-                                 uint32_t* rc_stats = nullptr, int32_t miss_cap = 0);
-cudaError_t launch_rc_fill(const bpkv_cache& c, const int32_t* rc_miss, uint32_t* rc_nmiss, int32_t miss_cap,
-                           cudaStream_t st);
+                                 cudaStream_t st, uint32_t* rc_stats = nullptr);
 cudaError_t launch_scan(const bpkv_cache& c, const float* q, const uint8_t* depths, float* scores, int64_t ld,
                         cudaStream_t st, const void* plan = nullptr, uint32_t* hist = nullptr,
                         int32_t n_sink = 0, int32_t n_recent = 0, int32_t pending = 0,
@@ -96,8 +93,7 @@ cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 // Workspace layout: status word, then the buffers each call family needs.
 struct Layout {
   size_t scores = 0, hist = 0, hist1 = 0, ctr = 0, cand = 0, cut = 0, part = 0, depths = 0, idx = 0, uidx = 0, umask = 0,
-         ucount = 0, tickets = 0, seq_tick = 0, plan = 0, q_rot = 0, rc_miss = 0, rc_nmiss = 0, rc_stats = 0,
-         total = 0;
+         ucount = 0, tickets = 0, seq_tick = 0, plan = 0, q_rot = 0, rc_stats = 0, total = 0;
 };
 
 Layout layout(const bpkv_cache& c, int32_t k, int32_t what) {
@@ -151,13 +147,9 @@ Layout layout(const bpkv_cache& c, int32_t k, int32_t what) {
     off = align_up(off + NH * scan_plan_bytes(c.group));
     L.q_rot = off;  // q R when the cache has a basis
     off = align_up(off + NH * c.group * kD * sizeof(float));
-    // the row cache's miss lists (tokens read over the link), their lengths
-    // and the step's hit and row counts; the lengths and counts adjoin
-    L.rc_miss = off;
-    off = align_up(off + NH * c.group * (size_t)k * sizeof(int32_t));
-    L.rc_nmiss = off;
-    L.rc_stats = off + NH * sizeof(uint32_t);
-    off = align_up(off + 3 * NH * sizeof(uint32_t));
+    // the row cache's counts of the step: rows found in it, rows
+    L.rc_stats = off;
+    off = align_up(off + 2 * NH * sizeof(uint32_t));
   }
   L.total = off;
   return L;
@@ -389,7 +381,7 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
     cudaEvent_t ev = static_cast<cudaEvent_t>(a->stage_events[(size_t)l * BPKV_STAGE_EVENTS + e]);
     return cuda_status(cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal));
   };
-  BPKV_TRY(cuda_status(cudaMemsetAsync(at(ws, L.rc_nmiss), 0, 3 * NH * sizeof(uint32_t), st)));
+  BPKV_TRY(cuda_status(cudaMemsetAsync(at(ws, L.rc_stats), 0, 2 * NH * sizeof(uint32_t), st)));
   for (int32_t l = 0; l < n_layers; ++l) {
     bpkv_cache& c = layers[l];
     const uint16_t* kn = a->k_new + (size_t)l * NH * kD;
@@ -455,14 +447,9 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
           launch_topk(c, scores, c.cap_tokens, a->k, a->n_sink, a->n_recent, sb, hs, iout, status, st, 1)));
       BPKV_TRY(mark(l, 4));
       BPKV_TRY(mark(l, 5));
-      const bool rc = c.residency == 1 && c.rc_slots > 0;
-      int32_t* rc_miss = reinterpret_cast<int32_t*>(at(ws, L.rc_miss));
-      uint32_t* rc_nmiss = reinterpret_cast<uint32_t*>(at(ws, L.rc_nmiss));
-      const int32_t miss_cap = (int32_t)(G * a->k);
       BPKV_TRY(cuda_status(launch_attend_ranges(c, q, scores, c.cap_tokens, sb.cut, a->n_sink, a->n_recent, part,
-                                                tickets, out, 1, seq_tick, st, rc ? rc_miss : nullptr, rc_nmiss,
-                                                reinterpret_cast<uint32_t*>(at(ws, L.rc_stats)), miss_cap)));
-      if (rc) BPKV_TRY(cuda_status(launch_rc_fill(c, rc_miss, rc_nmiss, miss_cap, st)));
+                                                tickets, out, 1, seq_tick, st,
+                                                reinterpret_cast<uint32_t*>(at(ws, L.rc_stats)))));
       BPKV_TRY(mark(l, 6));
       continue;
     }

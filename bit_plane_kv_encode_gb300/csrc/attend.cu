@@ -245,6 +245,7 @@ constexpr int kWinQuads = kRangeWin / 4 / kRangeThreads;  // 4-token quads per t
 template <int GP>
 __host__ __device__ constexpr int win_batch() { return GP >= 8 ? kWinQuads / 2 : kWinQuads; }
 constexpr int kQPitch = 36;           // floats per (head, quarter) row of q in shared memory
+constexpr int kRcMaxPart = 1024;      // row cache slots of one range
 
 struct RangeArgs {
   const uint16_t* k_rows;
@@ -265,21 +266,24 @@ struct RangeArgs {
   int32_t pending;                 // tokens appended in this step but not yet in seq_len
   int64_t* seq_len_out;            // with pending: seq_len, raised by pending once every unit is done
   uint32_t* seq_tick;              // [N], zero on entry (with pending)
-  // optional row cache (host-resident caches; see bpkv_cache): rows whose
-  // slot holds their token are read from it, the others over the link and
-  // listed for k_rc_fill
-  const uint16_t* rc_rows;         // [N][H][rc_slots][2][D]
-  const int32_t* rc_tok;           // [N][H][rc_slots]
+  // optional row cache (host-resident caches; see bpkv_cache).  Range rg
+  // owns slots [rg part, rg part + part) with part = rc_slots / n_ranges
+  // (at most kRcMaxPart), token x of the range lives only in slot
+  // rg part + x mod part: a row whose slot holds it is read from there; a row
+  // read over the link is written into its slot unless that slot serves a
+  // row read from it in this step or a later token of the range claims it
+  uint16_t* rc_rows;               // [N][H][rc_slots][2][D]
+  int32_t* rc_tok;                 // [N][H][rc_slots]
   int32_t rc_slots;                // 0: no row cache
-  int32_t miss_cap;                // entries of each unit's miss list
-  int32_t* rc_miss;                // [N][H][miss_cap] tokens read over the link
-  uint32_t* rc_nmiss;              // [N][H] entries in each list
-  uint32_t* rc_stats;              // [N][H][2] hits, misses (summed over the step's layers)
+  int32_t rc_part;                 // slots per range
+  uint32_t* rc_stats;              // [N][H][2] rows found, rows (summed over the step's layers)
 };
 
 struct RangeSmem {
   int32_t rows[kRangeMaxRows];
-  int32_t rsrc[kRangeMaxRows];  // row cache slot of each row, -1: read over the link
+  int32_t rsrc[kRangeMaxRows];  // row cache: slot of a row read from it; -2 - slot for a row read over
+                                // the link and then written there; -1 otherwise
+  int32_t claim[kRcMaxPart];    // row cache: the range's slots (INT32_MAX: serving a row this step)
   uint8_t rmask[kRangeMaxRows];
   float logit[kRangeMaxRows][BPKV_MAX_GROUP];
   float q[BPKV_MAX_GROUP * 4 * kQPitch];  // [head][quarter][kQPitch], 32 used
@@ -296,7 +300,7 @@ __device__ __forceinline__ float key_to_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-template <int GP>
+template <int GP, bool kRc>
 __global__ void __launch_bounds__(kRangeThreads, 512 / kRangeThreads) k_attend_ranges(RangeArgs a) {
   pdl_enter();
   extern __shared__ __align__(16) unsigned char range_raw[];
@@ -402,40 +406,55 @@ __global__ void __launch_bounds__(kRangeThreads, 512 / kRangeThreads) k_attend_r
   const int nrows = (int)S.n_rows;
   const uint16_t* kb = a.k_rows + unit * a.cap * kD;
   const uint16_t* vb = a.v_rows + unit * a.cap * kD;
-  const uint16_t* rcu = a.rc_slots ? a.rc_rows + unit * a.rc_slots * 2 * kD : nullptr;
-  if (a.rc_slots) {
-    // which rows the row cache holds; the others are listed for k_rc_fill
-    const int32_t* tok = a.rc_tok + unit * a.rc_slots;
+  uint16_t* rcu = kRc ? a.rc_rows + unit * a.rc_slots * 2 * kD : nullptr;
+  if (kRc) {
+    // the range's slots: rows found in the row cache keep theirs; of the rows
+    // read over the link, the latest token of each free slot will fill it
+    int32_t* tok = a.rc_tok + unit * a.rc_slots;
+    const int part = a.rc_part;
+    const int32_t sbase = rg * part;
+    for (int i = tid; i < part; i += kRangeThreads) S.claim[i] = -1;
+    __syncthreads();
     uint32_t hits = 0;
-    for (int r0 = 0; r0 < nrows; r0 += kRangeThreads) {  // whole warps (ballots)
-      const int r = r0 + tid;
-      const int32_t x = r < nrows ? S.rows[r] : -1;
-      const int32_t sl = x & (a.rc_slots - 1);
-      const bool hit = r < nrows && tok[sl] == x;
-      if (r < nrows) S.rsrc[r] = hit ? sl : -1;
+    for (int r = tid; r < nrows; r += kRangeThreads) {
+      const int32_t x = S.rows[r];
+      const int32_t i = (int32_t)(x % part);
+      const bool hit = tok[sbase + i] == x;
+      S.rsrc[r] = hit ? sbase + i : -1;
+      if (hit) S.claim[i] = INT32_MAX;
       hits += hit ? 1u : 0u;
-      const uint32_t miss = __ballot_sync(0xffffffffu, r < nrows && !hit);
-      if (miss) {
-        uint32_t base = 0;
-        if (lane == 0) base = atomicAdd(a.rc_nmiss + unit, (uint32_t)__popc(miss));
-        base = __shfl_sync(0xffffffffu, base, 0) + __popc(miss & ((1u << lane) - 1u));
-        if (r < nrows && !hit && base < (uint32_t)a.miss_cap) a.rc_miss[unit * a.miss_cap + base] = x;
-      }
+    }
+    __syncthreads();
+    for (int r = tid; r < nrows; r += kRangeThreads) {
+      const int32_t x = S.rows[r];
+      const int32_t i = (int32_t)(x % part);
+      if (S.rsrc[r] < 0 && S.claim[i] != INT32_MAX) atomicMax(&S.claim[i], x);
+    }
+    __syncthreads();
+    for (int r = tid; r < nrows; r += kRangeThreads) {
+      const int32_t x = S.rows[r];
+      const int32_t i = (int32_t)(x % part);
+      if (S.rsrc[r] < 0 && S.claim[i] == x) S.rsrc[r] = -2 - (sbase + i);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) hits += __shfl_xor_sync(0xffffffffu, hits, o);
     if (lane == 0) atomicAdd(a.rc_stats + 2 * unit, hits);
-    if (tid == 0) atomicAdd(a.rc_stats + 2 * unit + 1, (uint32_t)nrows);  // rows; misses = rows - hits later
+    if (tid == 0) atomicAdd(a.rc_stats + 2 * unit + 1, (uint32_t)nrows);
     __syncthreads();
   }
   // the K and V row of union row r: from the row cache or the cache's rows
   auto k_row = [&](int r) -> const uint16_t* {
-    const int sl = rcu ? S.rsrc[r] : -1;
+    const int sl = kRc ? S.rsrc[r] : -1;
     return sl >= 0 ? rcu + (int64_t)sl * 2 * kD : kb + (int64_t)S.rows[r] * kD;
   };
   auto v_row = [&](int r) -> const uint16_t* {
-    const int sl = rcu ? S.rsrc[r] : -1;
+    const int sl = kRc ? S.rsrc[r] : -1;
     return sl >= 0 ? rcu + (int64_t)sl * 2 * kD + kD : vb + (int64_t)S.rows[r] * kD;
+  };
+  // the row cache slot a row read over the link fills (nullptr: none)
+  auto fill_row = [&](int r) -> uint16_t* {
+    const int sl = kRc ? S.rsrc[r] : -1;
+    return sl <= -2 ? rcu + (int64_t)(-2 - sl) * 2 * kD : nullptr;
   };
 
   // V rows of this thread's slot, loaded now: they do not depend on the logits.
@@ -450,6 +469,14 @@ __global__ void __launch_bounds__(kRangeThreads, 512 / kRangeThreads) k_attend_r
     for (int b = 0; b < kVPre; ++b) {
       const int r = min(rs + kSlots * b, nrows - 1);
       vpre[b] = *reinterpret_cast<const uint2*>(v_row(r) + 4 * c4);
+    }
+    if (kRc) {
+#pragma unroll
+      for (int b = 0; b < kVPre; ++b) {
+        const int r = rs + kSlots * b;
+        uint16_t* f = r < nrows ? fill_row(r) : nullptr;
+        if (f) *reinterpret_cast<uint2*>(f + kD + 4 * c4) = vpre[b];
+      }
     }
   }
 
@@ -471,6 +498,14 @@ __global__ void __launch_bounds__(kRangeThreads, 512 / kRangeThreads) k_attend_r
       const uint4* kr = reinterpret_cast<const uint4*>(k_row(t >> 2) + (t & 3) * 32);
 #pragma unroll
       for (int c = 0; c < 4; ++c) w[u][c] = kr[c];
+      if (kRc && it0 + u * kRangeThreads + tid < n_items) {
+        uint16_t* f = fill_row(t >> 2);
+        if (f) {
+          uint4* fk = reinterpret_cast<uint4*>(f + (t & 3) * 32);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) fk[c] = w[u][c];
+        }
+      }
     }
 #pragma unroll
     for (int u = 0; u < kItemsPer; ++u) {
@@ -561,6 +596,14 @@ __global__ void __launch_bounds__(kRangeThreads, 512 / kRangeThreads) k_attend_r
       const int r = min(r0 + kSlots * b, nrows - 1);
       vw[b] = *reinterpret_cast<const uint2*>(v_row(r) + 4 * c4);
     }
+    if (kRc) {
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        const int r = r0 + kSlots * b;
+        uint16_t* f = r < nrows ? fill_row(r) : nullptr;
+        if (f) *reinterpret_cast<uint2*>(f + kD + 4 * c4) = vw[b];
+      }
+    }
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
       const int r = r0 + kSlots * b;
@@ -568,6 +611,14 @@ __global__ void __launch_bounds__(kRangeThreads, 512 / kRangeThreads) k_attend_r
     }
   }
   __syncthreads();  // every logit has been read: the logit buffer takes the slot sums
+  if (kRc) {
+    // the filled slots' rows are written (the barrier above): they now hold their tokens
+    int32_t* tok = a.rc_tok + unit * a.rc_slots;
+    for (int r = tid; r < nrows; r += kRangeThreads) {
+      const int sl = S.rsrc[r];
+      if (sl <= -2) tok[-2 - sl] = S.rows[r];
+    }
+  }
   float* acc = &S.logit[0][0];  // [slot][head][128]
 #pragma unroll
   for (int g = 0; g < GP; ++g) {
@@ -703,70 +754,32 @@ bool attend_ranges_eligible(const bpkv_cache& c, int32_t k) {
 cudaError_t launch_attend_ranges(const bpkv_cache& c, const float* q, const float* scores, int64_t ld,
                                  const unsigned long long* cut, int32_t n_sink, int32_t n_recent, float* part,
                                  uint32_t* tickets, float* out, int32_t pending, uint32_t* seq_tick,
-                                 cudaStream_t st, int32_t* rc_miss, uint32_t* rc_nmiss, uint32_t* rc_stats,
-                                 int32_t miss_cap) {
+                                 cudaStream_t st, uint32_t* rc_stats) {
   const int64_t rt = range_tokens(c.n_max, c.group);
   const int32_t nr = (int32_t)((c.n_max + rt - 1) / rt);
   if (nr == 0) return cudaSuccess;
-  const bool rc = c.residency == 1 && c.rc_slots > 0 && rc_miss;
+  const bool rc = c.residency == 1 && c.rc_slots > 0 && rc_stats;
+  const int32_t rc_part = rc ? std::min<int32_t>(c.rc_slots / nr, kRcMaxPart) : 0;
   RangeArgs a{c.k_rows, c.v_rows, c.seq_len,     q,       scores, ld,      cut,    n_sink, n_recent,
               c.cap_tokens, c.n_kv_heads, c.group, rt, nr, part, tickets, out, pending, c.seq_len, seq_tick,
-              rc ? c.rc_rows : nullptr, rc ? c.rc_tok : nullptr, rc ? c.rc_slots : 0, miss_cap, rc_miss, rc_nmiss,
-              rc_stats};
+              rc && rc_part > 0 ? c.rc_rows : nullptr, rc ? c.rc_tok : nullptr, rc && rc_part > 0 ? c.rc_slots : 0,
+              rc_part, rc_stats};
   const int smem = (int)sizeof(RangeSmem);
   auto go = [&](auto kern) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(nr, c.n_kv_heads, c.n_seq), dim3(kRangeThreads), (size_t)smem, st, a);
   };
-  if (c.group <= 1) return go(k_attend_ranges<1>);
-  if (c.group <= 2) return go(k_attend_ranges<2>);
-  if (c.group <= 4) return go(k_attend_ranges<4>);
-  return go(k_attend_ranges<8>);
-}
-
-// The row cache after a step's attention: the rows read over the link (each
-// unit's miss list) take their slots; of several with one slot the latest
-// token wins (slots of listed rows are emptied, then claimed by the largest
-// token, then filled).  One CTA per unit; empties the list.
-constexpr int kFillThreads = 256;
-
-__global__ void __launch_bounds__(kFillThreads) k_rc_fill(const uint16_t* __restrict__ k_rows,
-                                                         const uint16_t* __restrict__ v_rows, int64_t cap,
-                                                         uint16_t* rc_rows, int32_t* rc_tok, int32_t rc_slots,
-                                                         const int32_t* rc_miss, uint32_t* rc_nmiss,
-                                                         int32_t miss_cap) {
-  pdl_enter();
-  const int64_t unit = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n = (int)min((uint32_t)miss_cap, rc_nmiss[unit]);
-  const int32_t* list = rc_miss + unit * miss_cap;
-  int32_t* tok = rc_tok + unit * rc_slots;
-  for (int i = tid; i < n; i += kFillThreads) tok[list[i] & (rc_slots - 1)] = -1;
-  __syncthreads();
-  for (int i = tid; i < n; i += kFillThreads) atomicMax(tok + (list[i] & (rc_slots - 1)), list[i]);
-  __syncthreads();
-  // warp per row: lanes 0-15 copy the K row, 16-31 the V row (16 bytes each)
-  const uint16_t* kb = k_rows + unit * cap * kD;
-  const uint16_t* vb = v_rows + unit * cap * kD;
-  uint16_t* dst = rc_rows + unit * (int64_t)rc_slots * 2 * kD;
-  for (int i = warp; i < n; i += kFillThreads / 32) {
-    const int32_t x = list[i];
-    const int32_t sl = x & (rc_slots - 1);
-    if (tok[sl] != x) continue;  // uniform across the warp
-    const uint16_t* src = (lane < 16 ? kb : vb) + (int64_t)x * kD + 8 * (lane & 15);
-    *reinterpret_cast<uint4*>(dst + ((int64_t)sl * 2 + (lane >> 4)) * kD + 8 * (lane & 15)) =
-        *reinterpret_cast<const uint4*>(src);
+  if (a.rc_slots) {
+    if (c.group <= 1) return go(k_attend_ranges<1, true>);
+    if (c.group <= 2) return go(k_attend_ranges<2, true>);
+    if (c.group <= 4) return go(k_attend_ranges<4, true>);
+    return go(k_attend_ranges<8, true>);
   }
-  __syncthreads();
-  if (tid == 0) rc_nmiss[unit] = 0u;
-}
-
-cudaError_t launch_rc_fill(const bpkv_cache& c, const int32_t* rc_miss, uint32_t* rc_nmiss, int32_t miss_cap,
-                           cudaStream_t st) {
-  return launch_pdl(k_rc_fill, dim3((unsigned)(c.n_seq * c.n_kv_heads)), dim3(kFillThreads), 0, st, c.k_rows,
-                    c.v_rows, (int64_t)c.cap_tokens, c.rc_rows, c.rc_tok, (int32_t)c.rc_slots, rc_miss, rc_nmiss,
-                    miss_cap);
+  if (c.group <= 1) return go(k_attend_ranges<1, false>);
+  if (c.group <= 2) return go(k_attend_ranges<2, false>);
+  if (c.group <= 4) return go(k_attend_ranges<4, false>);
+  return go(k_attend_ranges<8, false>);
 }
 
 int attend_chunks(int64_t rows, bool dense) {

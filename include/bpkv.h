@@ -112,12 +112,15 @@ extern "C" {
  *   rc_rows uint16 [N][H][rc_slots][2][D]  the bf16 K row, then the V row, held in each slot
  *   rc_tok  int32  [N][H][rc_slots]        token held by each slot, -1 for none (the caller
  *                                          fills it with -1 before the first step)
- * rc_slots is a power of two from 64 to 2^20; token x can sit only in slot
- * x mod rc_slots.  bpkv_decode_step reads a selected row from its slot when
- * the slot holds that token, and after the attention places the rows it read
- * over the link in their slots (of several such rows with one slot, the
- * latest token wins).  Rows never change once appended, so a cached row is
- * always the current one; results are identical with or without the cache.
+ * rc_slots is a power of two from 64 to 2^20.  bpkv_decode_step splits a
+ * sequence's tokens into ranges (one attention CTA each) and gives range r
+ * the slots [r P, r P + P), P = min(rc_slots / ranges, 1024); token x of the
+ * range can sit only in slot r P + x mod P.  A selected row is read from its
+ * slot when the slot holds that token; a row read over the link is written
+ * into its slot by the same kernel, unless the slot serves another selected
+ * row in that step (of several with one free slot, the latest token wins).
+ * Rows never change once appended, so a cached row is always the current
+ * one; results are identical with or without the row cache.
  */
 typedef struct bpkv_cache {
   int32_t n_seq;
