@@ -43,9 +43,9 @@ def build(force: bool = False, verbose: bool = False, checks: bool | None = None
     if checks is None:
         checks = os.environ.get("BPKV_CHECKS") == "1"
     out = lib_path(checks)
-    deps = [os.path.join(CSRC, s) for s in SOURCES] + [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "scan_core.cuh"), os.path.join(CSRC, "depths_core.cuh"),
-                                                       os.path.join(CSRC, "encode_core.cuh"), os.path.join(CSRC, "value_core.cuh"),
-                                                       os.path.join(INCLUDE, "bpkv.h")]
+    deps = ([os.path.join(CSRC, s) for s in SOURCES] +
+            [os.path.join(CSRC, h) for h in sorted(os.listdir(CSRC)) if h.endswith(".cuh")] +
+            [os.path.join(INCLUDE, "bpkv.h")])
     if not force and os.path.exists(out) and os.path.getmtime(out) >= max(os.path.getmtime(d) for d in deps):
         return out
     nvcc = _nvcc()
