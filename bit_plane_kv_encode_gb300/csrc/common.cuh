@@ -44,8 +44,11 @@ __device__ __forceinline__ float fp16_bits_to_float(uint16_t b) {
 // get the same key, as they compare equal.
 constexpr int kTopkBins = 4096;  // level-0 histogram: top 12 bits of the ordered key
 
-constexpr int kSelCounters = 4;  // per row: candidates gathered, CTAs done, CTAs at the barrier, spare
-constexpr int64_t kLongRowTokens = 131072;  // rows this long get a parallel level-1 histogram
+// per row: candidates gathered, CTAs done, CTAs at the barrier, spare, then
+// the row's bucket as k_bucket found it (key prefix, rank left in it, keys in
+// it, spare)
+constexpr int kSelCounters = 8;
+constexpr int64_t kLongRowTokens = 262144;  // rows this long get a parallel level-1 histogram
 
 // Selection scratch for rows = N H G query heads.  hist, hist1 and ctr must
 // be zero when the selection starts (ctr is left zero by it); they are

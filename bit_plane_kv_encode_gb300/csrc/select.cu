@@ -213,8 +213,32 @@ __device__ __forceinline__ int bins_of_thread(const uint32_t* hist, int nbins, u
 }
 
 // Rank S.cand[0..nc) by value and set S.cut to the rem-th largest.  S.cand is
-// zero-padded to an even count (0 ranks below every candidate).
+// zero-padded to an even count (0 ranks below every candidate).  Small sets
+// are ranked by counting; larger ones sorted (bitonic, descending, padded with
+// zeros to a power of two: S.cand holds kRankCap + 2 entries).
 __device__ __forceinline__ void rank_cut(CutSmem& S, int nc, uint32_t rem) {
+  if (nc > 128) {
+    int P = 256;
+    while (P < nc) P <<= 1;
+    for (int e = nc + (int)threadIdx.x; e < P; e += blockDim.x) S.cand[e] = 0ull;
+    __syncthreads();
+    for (int kk = 2; kk <= P; kk <<= 1) {
+      for (int j = kk >> 1; j > 0; j >>= 1) {
+        for (int t = threadIdx.x; t < P / 2; t += blockDim.x) {
+          const int i = 2 * t - (t & (j - 1));  // lower element of the pair, partner i + j
+          const bool desc = (i & kk) == 0;
+          const unsigned long long x = S.cand[i], y = S.cand[i + j];
+          if ((x < y) == desc) {
+            S.cand[i] = y;
+            S.cand[i + j] = x;
+          }
+        }
+        __syncthreads();
+      }
+    }
+    if (threadIdx.x == 0 && rem >= 1 && (int)rem <= nc) S.cut = S.cand[rem - 1];
+    return;
+  }
   const int nc2 = (nc + 1) & ~1;
   for (int e = threadIdx.x; e < nc; e += blockDim.x) {
     const unsigned long long mine = S.cand[e];
@@ -320,106 +344,14 @@ __device__ __forceinline__ void row_barrier(uint32_t* bar, uint32_t count, int32
   __syncthreads();
 }
 
-// Grid (chunks of kCutChunk middle keys, rows).  Each thread holds
-// kCutChunk / kCutThreads keys of its CTA's chunk in registers throughout.
-__global__ void __launch_bounds__(kCutThreads, 2) k_cut(CutArgs a) {
-  pdl_enter();
-  __shared__ CutSmem S;
-  const int row = blockIdx.y, tid = threadIdx.x, lane = tid & 31;
-  static_assert(kCutChunk == kSelBatch * kCutThreads, "one batch of loads per thread");
-  uint32_t h[kBinsPerThread];
-  int top = 0;
-  if (!a.build_hist) top = bins_of_thread(a.hist + (int64_t)row * kTopkBins, kTopkBins, h);  // before seq_len
-  const RowRange r = row_range(a.seq_len[row / a.rows_per_seq] + a.pending, a.k, a.n_sink, a.n_recent);
-  if (r.cnt <= r.m || r.m == 0) {
-    // every middle key, or none
-    if (blockIdx.x == 0 && tid == 0) a.cut[row] = r.cnt <= r.m ? 0ull : ~0ull;
-    return;
-  }
-  const float* sc = a.scores + (int64_t)row * a.ld;
-  uint32_t* ctr = a.ctr + (int64_t)kSelCounters * row;
-  unsigned long long* cand = a.cand + (int64_t)row * kRankCap;
-  // this CTA's run of chunks; a chunk's keys, all loads in flight
-  const int64_t run0 = (int64_t)blockIdx.x * a.chunks_per_cta;
-  uint32_t keys[kSelBatch], valid = 0;
-  auto load_chunk = [&](int64_t ch) {
-    const int64_t c0 = ch * kCutChunk, c1 = min64(c0 + kCutChunk, r.cnt);
-    valid = 0;
-    if (c0 >= c1) return;
-    float v[kSelBatch];
-#pragma unroll
-    for (int b = 0; b < kSelBatch; ++b) v[b] = sc[r.lo + min64(c0 + tid + (int64_t)b * kCutThreads, c1 - 1)];
-#pragma unroll
-    for (int b = 0; b < kSelBatch; ++b) {
-      keys[b] = ordered_key(v[b]);
-      if (c0 + tid + (int64_t)b * kCutThreads < c1) valid |= 1u << b;
-    }
-  };
-  if (a.build_hist) {
-    // level-0 histogram (one chunk per CTA): counted per CTA in shared memory,
-    // added to the row's with one atomic per non-empty bin, then every CTA of
-    // the row waits for the others (the grid is launched cooperatively)
-    load_chunk(run0);
-    for (int b = tid; b < kTopkBins; b += kCutThreads) S.hist[b] = 0u;
-    __syncthreads();
-#pragma unroll
-    for (int b = 0; b < kSelBatch; ++b)
-      if ((valid >> b) & 1u) atomicAdd(&S.hist[keys[b] >> 20], 1u);
-    __syncthreads();
-    uint32_t* gh = a.hist + (int64_t)row * kTopkBins;
-    for (int b = tid; b < kTopkBins; b += kCutThreads)
-      if (S.hist[b]) atomicAdd(gh + b, S.hist[b]);
-    row_barrier(ctr + 2, gridDim.x, a.status);
-    top = bins_of_thread(reinterpret_cast<const uint32_t*>(gh), kTopkBins, h);
-  }
-  if (tid == 0) S.cut = ~0ull;
-  find_bucket(S, h, top, (uint32_t)r.m);
-  uint32_t prefix = S.tb, nb = S.nb, rem = S.rem;
-  int lvl = 0;
-  if (nb > (uint32_t)kRankCap && a.hist1) {
-    // the level-1 histogram of this bucket (counted by k_hist1) narrows it
-    const int top1 = bins_of_thread(a.hist1 + (int64_t)row * kTopkBins, kTopkBins, h);
-    find_bucket(S, h, top1, rem);
-    prefix = (prefix << 12) | S.tb;
-    nb = S.nb;
-    rem = S.rem;
-    lvl = 1;
-  }
-  const int sh = level_shift(lvl);
-  if (nb <= (uint32_t)kRankCap) {
-    // the run's bucket keys: one returning atomic per warp and chunk for the warp's matches
-    for (int64_t ch = run0; ch < run0 + a.chunks_per_cta; ++ch) {
-      if (!a.build_hist) load_chunk(ch);
-      const int64_t c0 = ch * kCutChunk;
-      uint32_t match = 0;
-#pragma unroll
-      for (int b = 0; b < kSelBatch; ++b)
-        if (((valid >> b) & 1u) && (keys[b] >> sh) == prefix) match |= 1u << b;
-      const uint32_t cnt = __popc(match);
-      uint32_t incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const uint32_t warp_total = __shfl_sync(0xffffffffu, incl, 31);
-      if (warp_total == 0u) continue;  // uniform across the warp
-      uint32_t base = 0;
-      if (lane == 31) base = atomicAdd(ctr, warp_total);
-      base = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
-#pragma unroll
-      for (int b = 0; b < kSelBatch; ++b) {
-        if ((match >> b) & 1u) {
-          if (base < (uint32_t)kRankCap)
-            cand[base] = ((unsigned long long)keys[b] << 32) |
-                         (0xFFFFFFFFu - (uint32_t)(r.lo + c0 + tid + (int64_t)b * kCutThreads));
-          ++base;
-        }
-      }
-    }
-  }
-  // the last CTA of the row to finish decides the cut (the barrier orders the
-  // CTA's writes before thread 0's cumulative fence)
+// The end of a row's cut: the last CTA of the row to finish (the barrier
+// orders the CTA's candidate writes before thread 0's cumulative fence) ranks
+// the candidates, or refines a bucket of more than kRankCap keys, and stores
+// the cut; it also clears the row's counters.  Whole block.
+__device__ void cut_finish(CutSmem& S, const CutArgs& a, int row, const RowRange& r, const float* __restrict__ sc,
+                           uint32_t* ctr, const unsigned long long* cand, uint32_t nb, uint32_t rem, uint32_t prefix,
+                           int lvl) {
+  const int tid = threadIdx.x;
   __syncthreads();
   if (tid == 0) {
     __threadfence();
@@ -428,6 +360,7 @@ __global__ void __launch_bounds__(kCutThreads, 2) k_cut(CutArgs a) {
   }
   __syncthreads();
   if (!S.is_last) return;
+  if (tid == 0) S.cut = ~0ull;
   if (nb <= (uint32_t)kRankCap) {
     const int nc = (int)min(__ldcg(ctr), (uint32_t)kRankCap);
     for (int e = tid; e < nc; e += kCutThreads) S.cand[e] = __ldcg(cand + e);
@@ -449,6 +382,212 @@ __global__ void __launch_bounds__(kCutThreads, 2) k_cut(CutArgs a) {
   }
 }
 
+// Append this warp's matching keys (bit b of `match`: key keys[b] of token
+// index idx0 + b * stride) to the row's candidate list: one returning atomic
+// per warp for the warp's matches.  Whole warps.
+__device__ __forceinline__ void append_matches(uint32_t match, const uint32_t (&keys)[kSelBatch], uint32_t idx0,
+                                               uint32_t stride, uint32_t* ctr, unsigned long long* cand) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t cnt = __popc(match);
+  uint32_t incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const uint32_t warp_total = __shfl_sync(0xffffffffu, incl, 31);
+  if (warp_total == 0u) return;  // uniform across the warp
+  uint32_t base = 0;
+  if (lane == 31) base = atomicAdd(ctr, warp_total);
+  base = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
+#pragma unroll
+  for (int b = 0; b < kSelBatch; ++b) {
+    if ((match >> b) & 1u) {
+      if (base < (uint32_t)kRankCap)
+        cand[base] = ((unsigned long long)keys[b] << 32) | (0xFFFFFFFFu - (idx0 + (uint32_t)b * stride));
+      ++base;
+    }
+  }
+}
+
+// Cooperative form (the row's CTAs count the level-0 histogram themselves):
+// grid (chunks of kCutChunk middle keys, rows), launched so that every CTA is
+// resident; each thread holds kCutChunk / kCutThreads keys of its CTA's chunk.
+__global__ void __launch_bounds__(kCutThreads, 2) k_cut(CutArgs a) {
+  pdl_enter();
+  __shared__ CutSmem S;
+  const int row = blockIdx.y, tid = threadIdx.x;
+  static_assert(kCutChunk == kSelBatch * kCutThreads, "one batch of loads per thread");
+  const RowRange r = row_range(a.seq_len[row / a.rows_per_seq] + a.pending, a.k, a.n_sink, a.n_recent);
+  if (r.cnt <= r.m || r.m == 0) {
+    // every middle key, or none
+    if (blockIdx.x == 0 && tid == 0) a.cut[row] = r.cnt <= r.m ? 0ull : ~0ull;
+    return;
+  }
+  const float* sc = a.scores + (int64_t)row * a.ld;
+  uint32_t* ctr = a.ctr + (int64_t)kSelCounters * row;
+  unsigned long long* cand = a.cand + (int64_t)row * kRankCap;
+  // this CTA's chunk; all loads in flight
+  const int64_t c0 = (int64_t)blockIdx.x * kCutChunk, c1 = min64(c0 + kCutChunk, r.cnt);
+  uint32_t keys[kSelBatch], valid = 0;
+  {
+    float v[kSelBatch];
+#pragma unroll
+    for (int b = 0; b < kSelBatch; ++b) v[b] = sc[r.lo + min64(c0 + tid + (int64_t)b * kCutThreads, c1 - 1)];
+#pragma unroll
+    for (int b = 0; b < kSelBatch; ++b) {
+      keys[b] = ordered_key(v[b]);
+      if (c0 + tid + (int64_t)b * kCutThreads < c1) valid |= 1u << b;
+    }
+  }
+  // level-0 histogram counted per CTA in shared memory, added to the row's
+  // with one atomic per non-empty bin, then every CTA of the row waits for
+  // the others (the grid is launched cooperatively)
+  for (int b = tid; b < kTopkBins; b += kCutThreads) S.hist[b] = 0u;
+  __syncthreads();
+#pragma unroll
+  for (int b = 0; b < kSelBatch; ++b)
+    if ((valid >> b) & 1u) atomicAdd(&S.hist[keys[b] >> 20], 1u);
+  __syncthreads();
+  uint32_t* gh = a.hist + (int64_t)row * kTopkBins;
+  for (int b = tid; b < kTopkBins; b += kCutThreads)
+    if (S.hist[b]) atomicAdd(gh + b, S.hist[b]);
+  row_barrier(ctr + 2, gridDim.x, a.status);
+  uint32_t h[kBinsPerThread];
+  const int top = bins_of_thread(reinterpret_cast<const uint32_t*>(gh), kTopkBins, h);
+  find_bucket(S, h, top, (uint32_t)r.m);
+  const uint32_t prefix = S.tb, nb = S.nb, rem = S.rem;
+  if (nb <= (uint32_t)kRankCap) {
+    uint32_t match = 0;
+#pragma unroll
+    for (int b = 0; b < kSelBatch; ++b)
+      if (((valid >> b) & 1u) && (keys[b] >> 20) == prefix) match |= 1u << b;
+    append_matches(match, keys, (uint32_t)(r.lo + c0 + tid), kCutThreads, ctr, cand);
+  }
+  cut_finish(S, a, row, r, sc, ctr, cand, nb, rem, prefix, 0);
+}
+
+// Streaming form (the row's bucket found by k_bucket, refined by k_hist1's
+// level-1 histogram on long rows): grid (chunks of kStreamChunk tokens in
+// absolute position, rows); each thread loads kStreamVec 16-byte groups of
+// scores (tokens 4 (t + 256 j) .. + 3 of the chunk) at once, then keeps the
+// middle tokens whose key is in the bucket and appends them.
+constexpr int kStreamVec = 8;                              // float4 loads per thread
+constexpr int kStreamChunk = 4 * kStreamVec * kCutThreads;  // 8192 tokens per CTA
+
+__global__ void __launch_bounds__(kCutThreads, 4) k_cut_stream(CutArgs a) {
+  pdl_enter();
+  __shared__ CutSmem S;
+  const int row = blockIdx.y, tid = threadIdx.x, lane = tid & 31;
+  const RowRange r = row_range(a.seq_len[row / a.rows_per_seq] + a.pending, a.k, a.n_sink, a.n_recent);
+  if (r.cnt <= r.m || r.m == 0) {
+    if (blockIdx.x == 0 && tid == 0) a.cut[row] = r.cnt <= r.m ? 0ull : ~0ull;
+    return;
+  }
+  const float* sc = a.scores + (int64_t)row * a.ld;
+  uint32_t* ctr = a.ctr + (int64_t)kSelCounters * row;
+  unsigned long long* cand = a.cand + (int64_t)row * kRankCap;
+  uint32_t prefix = ctr[4], rem = ctr[5], nb = ctr[6];  // the row's level-0 bucket (k_bucket)
+  int lvl = 0;
+  if (nb > (uint32_t)kRankCap && a.hist1) {
+    // the level-1 histogram of this bucket (counted by k_hist1) narrows it
+    uint32_t h[kBinsPerThread];
+    const int top1 = bins_of_thread(a.hist1 + (int64_t)row * kTopkBins, kTopkBins, h);
+    find_bucket(S, h, top1, rem);
+    prefix = (prefix << 12) | S.tb;
+    nb = S.nb;
+    rem = S.rem;
+    lvl = 1;
+  }
+  if (nb <= (uint32_t)kRankCap) {
+    // the bucket as an interval of floats: key(f) in [klo, khi] exactly when
+    // flo <= f <= fhi (the order-preserving key is monotone; -0 and +0 share
+    // a key, so a bucket ending just below +0's key ends at the negative
+    // float nearest 0)
+    const int sh = level_shift(lvl);
+    const uint32_t klo = prefix << sh, khi = klo | ((1u << sh) - 1u);
+    auto key_float = [](uint32_t k) {
+      return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+    };
+    const float flo = key_float(klo);
+    const float fhi = khi == 0x7FFFFFFFu ? __uint_as_float(0x80000001u) : key_float(khi);
+    const uint32_t x0 = (uint32_t)blockIdx.x * kStreamChunk;  // the chunk's first token
+    const uint32_t lo = (uint32_t)r.lo, hi = (uint32_t)r.hi, ld = (uint32_t)a.ld;
+    const float4* p = reinterpret_cast<const float4*>(sc + x0);
+    float4 v[kStreamVec];
+#pragma unroll
+    for (int j = 0; j < kStreamVec; ++j) {
+      const uint32_t x = x0 + 4 * (tid + kCutThreads * j);
+      v[j] = x < ld ? p[tid + kCutThreads * j] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    // bit 4 j + e: token x0 + 4 (tid + 256 j) + e is a middle token in the bucket
+    uint32_t match = 0;
+    const bool inner = x0 >= lo && x0 + kStreamChunk <= hi;  // every token of the chunk is a middle token
+#pragma unroll
+    for (int j = 0; j < kStreamVec; ++j) {
+      const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (f[e] >= flo && f[e] <= fhi) match |= 1u << (4 * j + e);
+    }
+    if (!inner) {
+#pragma unroll
+      for (int j = 0; j < kStreamVec; ++j) {
+        const uint32_t x = x0 + 4 * (tid + kCutThreads * j);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (x + e < lo || x + e >= hi) match &= ~(1u << (4 * j + e));
+      }
+    }
+    const uint32_t cnt = __popc(match);
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const uint32_t warp_total = __shfl_sync(0xffffffffu, incl, 31);
+    if (warp_total != 0u) {  // uniform across the warp
+      uint32_t base = 0;
+      if (lane == 31) base = atomicAdd(ctr, warp_total);
+      base = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
+      // the few matches, their scores read again (cached)
+      while (match) {
+        const int b = __ffs(match) - 1;
+        match &= match - 1u;
+        const uint32_t x = x0 + 4 * (tid + kCutThreads * (b >> 2)) + (b & 3);
+        if (base < (uint32_t)kRankCap) cand[base] = ((unsigned long long)ordered_key(sc[x]) << 32) | (0xFFFFFFFFu - x);
+        ++base;
+      }
+    }
+  }
+  cut_finish(S, a, row, r, sc, ctr, cand, nb, rem, prefix, lvl);
+}
+
+// ------------------------------------------------------------------ k_bucket
+
+// Per row (one CTA each): the level-0 bucket holding the m-th largest middle
+// key, from the row's counted histogram, stored in the row's counters
+// [4 .. 6] (key prefix, rank left in the bucket, keys in the bucket) for
+// k_hist1 and k_cut, so that their many CTAs need not each read and scan the
+// 4096 bins.
+__global__ void __launch_bounds__(kCutThreads) k_bucket(CutArgs a) {
+  pdl_enter();
+  __shared__ CutSmem S;
+  const int row = blockIdx.x;
+  uint32_t h[kBinsPerThread];
+  const int top = bins_of_thread(a.hist + (int64_t)row * kTopkBins, kTopkBins, h);
+  const RowRange r = row_range(a.seq_len[row / a.rows_per_seq] + a.pending, a.k, a.n_sink, a.n_recent);
+  if (r.cnt <= r.m || r.m == 0) return;  // k_cut decides these rows without a bucket
+  find_bucket(S, h, top, (uint32_t)r.m);
+  if (threadIdx.x == 0) {
+    uint32_t* ctr = a.ctr + (int64_t)kSelCounters * row;
+    ctr[4] = S.tb;
+    ctr[5] = S.rem;
+    ctr[6] = S.nb;
+  }
+}
+
 // ------------------------------------------------------------------ k_hist1
 
 // Level-1 histogram (key bits 19..8) of the keys in each long row's level-0
@@ -458,15 +597,13 @@ __global__ void __launch_bounds__(kCutThreads, 2) k_hist1(CutArgs a) {
   pdl_enter();
   __shared__ CutSmem S;
   const int row = blockIdx.y, tid = threadIdx.x;
-  uint32_t h[kBinsPerThread];
-  const int top = bins_of_thread(a.hist + (int64_t)row * kTopkBins, kTopkBins, h);
   const RowRange r = row_range(a.seq_len[row / a.rows_per_seq] + a.pending, a.k, a.n_sink, a.n_recent);
   const int64_t e0 = (int64_t)blockIdx.x * a.chunks_per_cta * kCutChunk;
   const int64_t e1 = min64(e0 + (int64_t)a.chunks_per_cta * kCutChunk, r.cnt);
   if (r.cnt <= r.m || r.m == 0 || e0 >= e1) return;
-  find_bucket(S, h, top, (uint32_t)r.m);
-  const uint32_t tb = S.tb;
-  if (S.nb <= (uint32_t)kRankCap) return;
+  const uint32_t* ctr = a.ctr + (int64_t)kSelCounters * row;  // the row's bucket (k_bucket)
+  const uint32_t tb = ctr[4];
+  if (ctr[6] <= (uint32_t)kRankCap) return;
   for (int b = tid; b < kTopkBins; b += kCutThreads) S.hist[b] = 0u;
   __syncthreads();
   for_row_keys(a.scores + (int64_t)row * a.ld, r.lo, e0, e1, [&](int64_t, uint32_t key) {
@@ -627,13 +764,17 @@ cudaError_t launch_cut(const bpkv_cache& c, const float* scores, int64_t ld, int
   const int32_t cpc = build_hist ? 1 : chunks_per_cta(c);
   CutArgs a{scores,   ld,           c.seq_len, b.hist, l1 ? b.hist1 : nullptr, b.cand, b.ctr, b.cut, status,
             c.n_kv_heads * c.group, k, n_sink, n_recent, build_hist ? 1 : 0, pending, cpc};
-  const dim3 grid = run_grid(c, cpc);
-  if (build_hist) return launch_coop_pdl(k_cut, grid, dim3(kCutThreads), 0, st, a);
+  if (build_hist) return launch_coop_pdl(k_cut, run_grid(c, 1), dim3(kCutThreads), 0, st, a);
+  // each row's bucket once, then (long rows) the level-1 histogram, then the
+  // cut, both over runs of chunks sized for about one wave
+  cudaError_t e = launch_pdl(k_bucket, dim3((unsigned)(c.n_seq * c.n_kv_heads * c.group)), dim3(kCutThreads), 0, st, a);
+  if (e != cudaSuccess) return e;
   if (l1) {
-    const cudaError_t e = launch_pdl(k_hist1, grid, dim3(kCutThreads), 0, st, a);
+    e = launch_pdl(k_hist1, run_grid(c, cpc), dim3(kCutThreads), 0, st, a);
     if (e != cudaSuccess) return e;
   }
-  return launch_pdl(k_cut, grid, dim3(kCutThreads), 0, st, a);
+  const dim3 grid((unsigned)((c.n_max + kStreamChunk - 1) / kStreamChunk), (unsigned)(c.n_seq * c.n_kv_heads * c.group));
+  return launch_pdl(k_cut_stream, grid, dim3(kCutThreads), 0, st, a);
 }
 
 cudaError_t launch_lists(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,

@@ -391,10 +391,12 @@ def test_scan_topk_grid_too_large_for_cut(pk, orc, N, H, G, n):
         check_topk_sets(idx_a[s, h, g].cpu().numpy(), orc.topk(ref[g], k), ref[g], k, what=f"head {g}")
 
 
-@pytest.mark.parametrize("n,ties", [(140000, 0.0), (150001, 0.9)])
+@pytest.mark.parametrize("n,ties", [(140000, 0.0), (150001, 0.9), (270000, 0.0), (300001, 0.9)])
 def test_topk_long_rows_level1(pk, orc, n, ties):
-    """Rows of at least 131072 keys over a grid too large to run cooperatively:
-    the level-1 histogram (k_hist1) narrows the level-0 bucket before the cut."""
+    """Rows over a grid too large to run cooperatively.  Of 262144 keys or
+    more: the level-1 histogram (k_hist1) narrows the level-0 bucket before
+    the cut.  Shorter: a bucket of more than 1024 keys (the heavy ties) is
+    refined by the row's last CTA."""
     from workload.gen import random_scores
     N, H, G, k = 1, 4, 4, 512
     kk, vv = _rand_kv(N, H, n, seed=14)
