@@ -289,6 +289,7 @@ struct RangeSmem {
   float q[BPKV_MAX_GROUP * 4 * kQPitch];  // [head][quarter][kQPitch], 32 used
   __align__(16) uint8_t wbits[kRangeWin];
   uint32_t ck[BPKV_MAX_GROUP], ci[BPKV_MAX_GROUP];
+  float fck[BPKV_MAX_GROUP];              // each head's cut key as a float
   uint32_t mkey[BPKV_MAX_GROUP];          // order-preserving key of each head's largest logit
   uint32_t warp_tot[kRangeThreads / 32];
   float lslot[kRangeThreads / 32][BPKV_MAX_GROUP];
@@ -320,6 +321,9 @@ __global__ void __launch_bounds__(kRangeThreads, 512 / kRangeThreads) k_attend_r
     const unsigned long long c = a.cut[unit * G + tid];
     S.ck[tid] = (uint32_t)(c >> 32);
     S.ci[tid] = 0xFFFFFFFFu - (uint32_t)c;
+    // key(f) > ck exactly when f > fck, key(f) == ck when f == fck (-0 and +0
+    // share a key and compare equal; no score is NaN)
+    S.fck[tid] = key_to_float((uint32_t)(c >> 32));
     S.mkey[tid] = 0u;
   }
   __syncthreads();
@@ -333,6 +337,8 @@ __global__ void __launch_bounds__(kRangeThreads, 512 / kRangeThreads) k_attend_r
   for (int64_t w0 = t0; w0 < t1; w0 += kRangeWin) {
     const int wl = (int)min64(kRangeWin, t1 - w0);
     const int wq = (wl + 3) / 4;  // score rows hold whole quads (their length is a multiple of 4)
+    // every token of the window is a middle token (no sink, recent or past-the-end checks)
+    const bool inner = w0 >= lo && w0 + kRangeWin <= hi && w0 + kRangeWin <= t1;
     __syncthreads();              // the previous window is done
     constexpr int WB = win_batch<GP>();
     for (int q0 = tid; q0 < wq; q0 += WB * kRangeThreads) {
@@ -349,24 +355,25 @@ __global__ void __launch_bounds__(kRangeThreads, 512 / kRangeThreads) k_attend_r
         const int qd = q0 + u * kRangeThreads;
         if (qd >= wq) break;
         uint32_t packed = 0;
+        const uint32_t xq = (uint32_t)(w0 + 4 * qd);  // the quad's first token
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int64_t x = w0 + 4 * qd + j;
-          uint32_t bits = 0u;
-          if (x < t1) {
-            if (x < lo || x >= hi) {
-              bits = all;
-            } else {
+        for (int g = 0; g < GP; ++g) {
+          if (g >= G) break;
+          const float fc = S.fck[g];
+          const uint32_t ci = S.ci[g];
+          const float f[4] = {v[u][g].x, v[u][g].y, v[u][g].z, v[u][g].w};
 #pragma unroll
-              for (int g = 0; g < GP; ++g) {
-                if (g >= G) break;
-                const float f = j == 0 ? v[u][g].x : (j == 1 ? v[u][g].y : (j == 2 ? v[u][g].z : v[u][g].w));
-                const uint32_t key = ordered_key(f);
-                if (key > S.ck[g] || (key == S.ck[g] && (uint32_t)x <= S.ci[g])) bits |= 1u << g;
-              }
-            }
+          for (int j = 0; j < 4; ++j)
+            if (f[j] > fc || (f[j] == fc && xq + j <= ci)) packed |= 1u << (8 * j + g);
+        }
+        if (!inner) {
+          // tokens past the range's end take nothing; sinks and recent tokens every head
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t x = xq + j;
+            if (x >= (uint32_t)t1) packed &= ~(0xFFu << (8 * j));
+            else if (x < (uint32_t)lo || x >= (uint32_t)hi) packed |= all << (8 * j);
           }
-          packed |= bits << (8 * j);
         }
         reinterpret_cast<uint32_t*>(S.wbits)[qd] = packed;
       }
