@@ -11,7 +11,10 @@
 // Dense: the same with rows = all stored tokens and every head selected.
 #include "common.cuh"
 
+#include <stddef.h>
+
 #include <algorithm>
+#include <type_traits>
 
 namespace bpkv {
 
@@ -243,7 +246,7 @@ constexpr int kRangeWin = 4096;       // selection window
 constexpr int kWinQuads = kRangeWin / 4 / kRangeThreads;  // 4-token quads per thread and window
 // quads whose scores a thread loads at once (fewer with more heads: registers)
 template <int GP>
-__host__ __device__ constexpr int win_batch() { return GP >= 8 ? kWinQuads / 2 : kWinQuads; }
+__host__ __device__ constexpr int win_batch() { return GP >= 8 ? kWinQuads / 4 : GP >= 4 ? kWinQuads / 2 : kWinQuads; }
 constexpr int kQPitch = 36;           // floats per (head, quarter) row of q in shared memory
 constexpr int kRcMaxPart = 1024;      // row cache slots of one range
 
@@ -279,14 +282,19 @@ struct RangeArgs {
   uint32_t* rc_stats;              // [N][H][2] rows found, rows (summed over the step's layers)
 };
 
+// Shared memory of a range CTA for up to GP heads (kRc: with the row cache's
+// arrays).  The logit buffer later holds the per-slot partial outputs
+// [slot][head][D] and the merge's range weights.
+template <int GP, bool kRc>
 struct RangeSmem {
+  static constexpr int kRcRows = kRc ? kRangeMaxRows : 1, kRcPart = kRc ? kRcMaxPart : 1;
   int32_t rows[kRangeMaxRows];
-  int32_t rsrc[kRangeMaxRows];  // row cache: slot of a row read from it; -2 - slot for a row read over
+  int32_t rsrc[kRcRows];        // row cache: slot of a row read from it; -2 - slot for a row read over
                                 // the link and then written there; -1 otherwise
-  int32_t claim[kRcMaxPart];    // row cache: the range's slots (INT32_MAX: serving a row this step)
+  int32_t claim[kRcPart];       // row cache: the range's slots (INT32_MAX: serving a row this step)
   uint8_t rmask[kRangeMaxRows];
-  float logit[kRangeMaxRows][BPKV_MAX_GROUP];
-  float q[BPKV_MAX_GROUP * 4 * kQPitch];  // [head][quarter][kQPitch], 32 used
+  __align__(16) float logit[kRangeMaxRows][GP];  // read and written as float4 (slot partials)
+  __align__(16) float q[GP * 4 * kQPitch];       // [head][quarter][kQPitch], 32 used; read as float4
   __align__(16) uint8_t wbits[kRangeWin];
   uint32_t ck[BPKV_MAX_GROUP], ci[BPKV_MAX_GROUP];
   float fck[BPKV_MAX_GROUP];              // each head's cut key as a float
@@ -302,10 +310,15 @@ __device__ __forceinline__ float key_to_float(uint32_t k) {
 }
 
 template <int GP, bool kRc>
-__global__ void __launch_bounds__(kRangeThreads, 512 / kRangeThreads) k_attend_ranges(RangeArgs a) {
+__global__ void __launch_bounds__(kRangeThreads, GP <= 4 ? 3 : 2) k_attend_ranges(RangeArgs a) {
   pdl_enter();
   extern __shared__ __align__(16) unsigned char range_raw[];
-  RangeSmem& S = *reinterpret_cast<RangeSmem*>(range_raw);
+  RangeSmem<GP, kRc>& S = *reinterpret_cast<RangeSmem<GP, kRc>*>(range_raw);
+  static_assert(sizeof(S.logit) >= sizeof(float) * (kRangeThreads / 32) * GP * kD, "slot partials fit the logits");
+  using SmemT = RangeSmem<GP, kRc>;
+  static_assert(offsetof(SmemT, logit) % 16 == 0 && offsetof(SmemT, q) % 16 == 0 && offsetof(SmemT, wbits) % 16 == 0,
+                "vector-accessed shared arrays on 16-byte boundaries");
+  static_assert(sizeof(S.logit) >= sizeof(float) * kRangeMaxRanges * GP, "merge weights fit the logits");
   const int rg = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
   const int64_t unit = (int64_t)s * a.n_heads + h;
   const int G = a.group;
@@ -771,22 +784,28 @@ cudaError_t launch_attend_ranges(const bpkv_cache& c, const float* q, const floa
               c.cap_tokens, c.n_kv_heads, c.group, rt, nr, part, tickets, out, pending, c.seq_len, seq_tick,
               rc && rc_part > 0 ? c.rc_rows : nullptr, rc ? c.rc_tok : nullptr, rc && rc_part > 0 ? c.rc_slots : 0,
               rc_part, rc_stats};
-  const int smem = (int)sizeof(RangeSmem);
-  auto go = [&](auto kern) -> cudaError_t {
+  auto go = [&](auto kern, auto gp, auto rcv) -> cudaError_t {
+    const int smem = (int)sizeof(RangeSmem<decltype(gp)::value, decltype(rcv)::value>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(nr, c.n_kv_heads, c.n_seq), dim3(kRangeThreads), (size_t)smem, st, a);
   };
+  using T = std::true_type;
+  using F = std::false_type;
+  using G1 = std::integral_constant<int, 1>;
+  using G2 = std::integral_constant<int, 2>;
+  using G4 = std::integral_constant<int, 4>;
+  using G8 = std::integral_constant<int, 8>;
   if (a.rc_slots) {
-    if (c.group <= 1) return go(k_attend_ranges<1, true>);
-    if (c.group <= 2) return go(k_attend_ranges<2, true>);
-    if (c.group <= 4) return go(k_attend_ranges<4, true>);
-    return go(k_attend_ranges<8, true>);
+    if (c.group <= 1) return go(k_attend_ranges<1, true>, G1{}, T{});
+    if (c.group <= 2) return go(k_attend_ranges<2, true>, G2{}, T{});
+    if (c.group <= 4) return go(k_attend_ranges<4, true>, G4{}, T{});
+    return go(k_attend_ranges<8, true>, G8{}, T{});
   }
-  if (c.group <= 1) return go(k_attend_ranges<1, false>);
-  if (c.group <= 2) return go(k_attend_ranges<2, false>);
-  if (c.group <= 4) return go(k_attend_ranges<4, false>);
-  return go(k_attend_ranges<8, false>);
+  if (c.group <= 1) return go(k_attend_ranges<1, false>, G1{}, F{});
+  if (c.group <= 2) return go(k_attend_ranges<2, false>, G2{}, F{});
+  if (c.group <= 4) return go(k_attend_ranges<4, false>, G4{}, F{});
+  return go(k_attend_ranges<8, false>, G8{}, F{});
 }
 
 int attend_chunks(int64_t rows, bool dense) {
