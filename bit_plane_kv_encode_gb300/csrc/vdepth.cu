@@ -16,19 +16,29 @@
 // row r is read to depth t_r = its items taken, and o_h = sum_r p_h(r) vhat_r(t_r)
 // with vhat = s ((c_t + 1/2) 2^(4-t) - 8) and vhat = 0 at t = 0.
 //
-// One CTA per unit.  The greedy order is one total order of 64-bit keys
-// (value bits, then the complemented item index), so the taken items are
-// exactly the B_V largest keys: a radix select over the key bits finds the
-// B_V-th largest key and every item at or above it is taken.
+// One cluster of kVdCluster CTAs per unit, rows dealt round-robin to the
+// CTAs (row r to CTA r mod kVdCluster).  The softmax maxima and sums, the
+// radix histograms and the output are reduced across the cluster through
+// distributed shared memory at hardware cluster barriers.  The greedy order
+// is one total order of 64-bit keys (value bits, then the complemented item
+// index), so the taken items are exactly the B_V largest keys: a radix select
+// over the key bits finds the B_V-th largest key and every item at or above
+// it is taken.
 #include "common.cuh"
+
+#include <cooperative_groups.h>
+
+namespace cg = cooperative_groups;
 
 namespace bpkv {
 
 // ---------------------------------------------------------------- stage 2
 
-constexpr int kVdThreads = 768;
+constexpr int kVdCluster = 8;                          // CTAs per unit
+constexpr int kVdThreads = 256;
 constexpr int kVdWarps = kVdThreads / 32;
-constexpr int kVdMaxRows = 2048;  // union rows of one unit (G k)
+constexpr int kVdMaxRows = 2048;                       // union rows of one unit (G k)
+constexpr int kVdLocal = kVdMaxRows / kVdCluster;      // rows of one CTA
 constexpr int kVdBatch = 4;       // rows a warp loads at once (the value phase: one row per 8 lanes)
 
 struct VdArgs {
@@ -50,15 +60,18 @@ struct VdArgs {
 
 template <int GP>
 struct VdSmem {
-  float p[GP][kVdMaxRows];   // logits, then probabilities
-  float a[kVdMaxRows];       // a_r
-  uint8_t dep[kVdMaxRows];
+  float p[GP][kVdLocal];     // this CTA's rows: logits, then probabilities
+  float a[kVdLocal];         // a_r
+  uint8_t dep[kVdLocal];
   float q[GP][kD];
-  float o[GP][kD];
+  float o[GP][kD];           // this CTA's share of the output
   float red[kVdWarps][GP];
-  uint32_t hist[256];
+  float cmax[GP], csum[GP];  // this CTA's softmax maximum and sum per head
+  uint32_t hist[256];        // this CTA's radix histogram
+  uint32_t hsum[256];        // the cluster's
   unsigned long long prefix;
   uint32_t need;
+  uint32_t done;             // 0: select on; 1: every positive item taken; 2: the bin at prefix taken whole
 };
 
 __device__ __forceinline__ float vd_warp_sum(float x) {
@@ -87,10 +100,14 @@ __global__ void __launch_bounds__(kVdThreads) k_attend_vdepth(VdArgs a) {
   pdl_enter();
   extern __shared__ __align__(16) unsigned char vd_raw[];
   VdSmem<GP>& S = *reinterpret_cast<VdSmem<GP>*>(vd_raw);
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = (int)cl.block_rank();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t unit = blockIdx.x;
+  const int64_t unit = blockIdx.x / kVdCluster;
   const int G = a.group;
   const int n_u = min(a.ucount[unit], min(a.u_cap, kVdMaxRows));
+  const int n_loc = n_u > rank ? (n_u - rank + kVdCluster - 1) / kVdCluster : 0;  // rows rank + kVdCluster i
+  auto row_of = [&](int i) { return rank + kVdCluster * i; };
   const int32_t* rows = a.uidx + unit * a.u_cap;
   const uint8_t* masks = a.umask + unit * a.u_cap;
   const uint16_t* kr = a.k_rows + unit * a.cap * kD;
@@ -101,23 +118,23 @@ __global__ void __launch_bounds__(kVdThreads) k_attend_vdepth(VdArgs a) {
   }
   __syncthreads();
   // logits q_h . k_r / sqrt(D) of the heads that selected row r (warp per row,
-  // four channels per lane), -inf elsewhere
-  // kVdBatch rows per warp at a time, their loads issued together
+  // four channels per lane), -inf elsewhere; kVdBatch rows per warp at a
+  // time, their loads issued together
   const float scale = rsqrtf((float)kD);
-  for (int r0 = warp; r0 < n_u; r0 += kVdWarps * kVdBatch) {
+  for (int i0 = warp; i0 < n_loc; i0 += kVdWarps * kVdBatch) {
     uint2 kv[kVdBatch];
 #pragma unroll
     for (int u = 0; u < kVdBatch; ++u) {
-      const int r = min(r0 + u * kVdWarps, n_u - 1);
-      kv[u] = *reinterpret_cast<const uint2*>(kr + (int64_t)rows[r] * kD + 4 * lane);
+      const int i = min(i0 + u * kVdWarps, n_loc - 1);
+      kv[u] = *reinterpret_cast<const uint2*>(kr + (int64_t)rows[row_of(i)] * kD + 4 * lane);
     }
 #pragma unroll
     for (int u = 0; u < kVdBatch; ++u) {
-      const int r = r0 + u * kVdWarps;
-      if (r >= n_u) break;  // uniform across the warp
+      const int i = i0 + u * kVdWarps;
+      if (i >= n_loc) break;  // uniform across the warp
       const float k0 = __uint_as_float(kv[u].x << 16), k1 = __uint_as_float(kv[u].x & 0xFFFF0000u);
       const float k2 = __uint_as_float(kv[u].y << 16), k3 = __uint_as_float(kv[u].y & 0xFFFF0000u);
-      const uint32_t m = masks[r];
+      const uint32_t m = masks[row_of(i)];
 #pragma unroll
       for (int h = 0; h < GP; ++h) {
         const float* qh = S.q[h] + 4 * lane;
@@ -126,64 +143,81 @@ __global__ void __launch_bounds__(kVdThreads) k_attend_vdepth(VdArgs a) {
         d = fmaf(qh[2], k2, d);
         d = fmaf(qh[3], k3, d);
         d = vd_warp_sum(d);
-        if (lane == 0) S.p[h][r] = (h < G && ((m >> h) & 1)) ? d * scale : -INFINITY;
+        if (lane == 0) S.p[h][i] = (h < G && ((m >> h) & 1)) ? d * scale : -INFINITY;
       }
     }
   }
   __syncthreads();
-  // softmax per head: max, exponentials, sum, probabilities
+  // softmax per head over the whole unit: the cluster's maximum, exponentials,
+  // the cluster's sum, probabilities
   float mx[GP], z[GP];
 #pragma unroll
   for (int h = 0; h < GP; ++h) {
     float v = -INFINITY;
-    for (int r = tid; r < n_u; r += kVdThreads) v = fmaxf(v, S.p[h][r]);
+    for (int i = tid; i < n_loc; i += kVdThreads) v = fmaxf(v, S.p[h][i]);
     v = vd_warp_max(v);
     if (lane == 0) S.red[warp][h] = v;
   }
   __syncthreads();
+  if (tid < GP) {
+    float v = -INFINITY;
+    for (int w = 0; w < kVdWarps; ++w) v = fmaxf(v, S.red[w][tid]);
+    S.cmax[tid] = v;
+  }
+  cl.sync();
 #pragma unroll
   for (int h = 0; h < GP; ++h) {
     mx[h] = -INFINITY;
-    for (int w = 0; w < kVdWarps; ++w) mx[h] = fmaxf(mx[h], S.red[w][h]);
+    for (int c = 0; c < kVdCluster; ++c) mx[h] = fmaxf(mx[h], cl.map_shared_rank(S.cmax, c)[h]);
   }
-  __syncthreads();
 #pragma unroll
   for (int h = 0; h < GP; ++h) {
     float v = 0.f;
-    for (int r = tid; r < n_u; r += kVdThreads) {
-      const float l = S.p[h][r];
+    for (int i = tid; i < n_loc; i += kVdThreads) {
+      const float l = S.p[h][i];
       const float e = l == -INFINITY ? 0.f : __expf(l - mx[h]);
-      S.p[h][r] = e;
+      S.p[h][i] = e;
       v += e;
     }
     v = vd_warp_sum(v);
     if (lane == 0) S.red[warp][h] = v;
   }
   __syncthreads();
+  if (tid < GP) {
+    float v = 0.f;
+    for (int w = 0; w < kVdWarps; ++w) v += S.red[w][tid];
+    S.csum[tid] = v;
+  }
+  cl.sync();
 #pragma unroll
   for (int h = 0; h < GP; ++h) {
     z[h] = 0.f;
-    for (int w = 0; w < kVdWarps; ++w) z[h] += S.red[w][h];
+    for (int c = 0; c < kVdCluster; ++c) z[h] += cl.map_shared_rank(S.csum, c)[h];
   }
   // probabilities and row weights a_r = sum_h p_h(r)^2 (heads in order)
-  for (int r = tid; r < n_u; r += kVdThreads) {
+  for (int i = tid; i < n_loc; i += kVdThreads) {
     float acc = 0.f;
 #pragma unroll
     for (int h = 0; h < GP; ++h) {
-      const float pr = z[h] > 0.f ? S.p[h][r] / z[h] : 0.f;
-      S.p[h][r] = pr;
+      const float pr = z[h] > 0.f ? S.p[h][i] / z[h] : 0.f;
+      S.p[h][i] = pr;
       acc = fmaf(pr, pr, acc);
     }
-    S.a[r] = acc;
+    S.a[i] = acc;
   }
   if (tid == 0) {
     S.prefix = 0ull;
     S.need = (uint32_t)max(a.budget_v, 0);
+    S.done = 0u;
   }
   __syncthreads();
   // radix select, eight bits at a time from the top, of the need-th largest
-  // key among the 4 n_u items (the last one taken); fewer positive items than
-  // the budget: every positive item is taken (the cut falls to key 1)
+  // key among the unit's 4 n_u items (the last one taken), each CTA counting
+  // its rows' items and every CTA reading the cluster's sum.  It stops early
+  // when the bin holding that key is taken whole (the cut is then the bin's
+  // lowest key); with fewer positive items than the budget every positive
+  // item is taken (the cut falls to key 1).  Every CTA takes the same
+  // decisions.
   unsigned long long cut = ~0ull;
   if (S.need > 0) {
     for (int shift = 56; shift >= 0; shift -= 8) {
@@ -191,9 +225,19 @@ __global__ void __launch_bounds__(kVdThreads) k_attend_vdepth(VdArgs a) {
       __syncthreads();
       const unsigned long long pre = S.prefix;
       const unsigned long long hi_mask = shift == 56 ? 0ull : (~0ull << (shift + 8));
-      for (int it = tid; it < 4 * n_u; it += kVdThreads) {
-        const unsigned long long k = vd_key(S.a[it >> 2], it >> 2, it & 3);
+      for (int it = tid; it < 4 * n_loc; it += kVdThreads) {
+        const unsigned long long k = vd_key(S.a[it >> 2], row_of(it >> 2), it & 3);
         if (k != 0ull && (k & hi_mask) == pre) atomicAdd(&S.hist[(k >> shift) & 0xFF], 1u);
+      }
+      cl.sync();  // every CTA's histogram is complete
+      for (int e = tid; e < 256; e += kVdThreads) {
+        uint32_t hv[kVdCluster];
+#pragma unroll
+        for (int c = 0; c < kVdCluster; ++c) hv[c] = cl.map_shared_rank(S.hist, c)[e];
+        uint32_t v = 0u;
+#pragma unroll
+        for (int c = 0; c < kVdCluster; ++c) v += hv[c];
+        S.hsum[e] = v;
       }
       __syncthreads();
       if (warp == 0) {
@@ -201,7 +245,7 @@ __global__ void __launch_bounds__(kVdThreads) k_attend_vdepth(VdArgs a) {
         uint32_t need = S.need, acc = 0;
         int sel = -1;
         for (int base = 224; base >= 0 && sel < 0; base -= 32) {
-          const uint32_t c = S.hist[base + lane];
+          const uint32_t c = S.hsum[base + lane];
           // inclusive sum from the top of this 32-bin slice (lane 31 highest)
           uint32_t incl = c;
 #pragma unroll
@@ -222,33 +266,36 @@ __global__ void __launch_bounds__(kVdThreads) k_attend_vdepth(VdArgs a) {
         }
         if (lane == 0) {
           if (sel < 0) {
-            S.need = 0u;  // fewer positive items than the budget
+            S.done = 1u;  // fewer positive items than the budget
           } else {
             S.prefix = pre | ((unsigned long long)sel << shift);
             S.need = need;
+            if (S.hsum[sel] == need) S.done = 2u;  // the bin is taken whole
           }
         }
       }
-      __syncthreads();
-      if (S.need == 0u) break;
+      cl.sync();  // every CTA has read the histograms (before they are cleared) and has its decision
+      if (S.done != 0u) break;
     }
-    cut = S.need == 0u ? 1ull : S.prefix;
+    cut = S.done == 1u ? 1ull : S.prefix;
   }
   __syncthreads();
   // depth of each row: its items at or above the cut
-  for (int r = tid; r < n_u; r += kVdThreads) {
+  for (int i = tid; i < n_loc; i += kVdThreads) {
+    const int r = row_of(i);
     int t = 0;
     if (a.budget_v > 0) {
 #pragma unroll
-      for (int tt = 0; tt < 4; ++tt) t += vd_key(S.a[r], r, tt) >= cut ? 1 : 0;
+      for (int tt = 0; tt < 4; ++tt) t += vd_key(S.a[i], r, tt) >= cut ? 1 : 0;
     }
-    S.dep[r] = (uint8_t)t;
+    S.dep[i] = (uint8_t)t;
     if (a.vdepth) a.vdepth[unit * a.u_cap + r] = (uint8_t)t;
-    if (a.weight) a.weight[unit * a.u_cap + r] = S.a[r];
+    if (a.weight) a.weight[unit * a.u_cap + r] = S.a[i];
   }
   __syncthreads();
-  // o_h = sum_r p_h(r) vhat_r(t_r): warp per row, lane channels l, l + 32,
-  // l + 64, l + 96 (word 0 bits l and l + 32, word 1 bits l and l + 32)
+  // o_h = sum_r p_h(r) vhat_r(t_r) over this CTA's rows: warp per row, lane
+  // channels l, l + 32, l + 64, l + 96 (word 0 bits l and l + 32, word 1 bits
+  // l and l + 32)
   float acc[GP][4];
 #pragma unroll
   for (int h = 0; h < GP; ++h)
@@ -259,22 +306,22 @@ __global__ void __launch_bounds__(kVdThreads) k_attend_vdepth(VdArgs a) {
   // kVdBatch rows per warp at a time: each lane loads one of the rows' plane
   // words (row u: words 2 p + w at lanes 8 u + 2 p + w) and their scales, the
   // warp shares them by shuffles
-  for (int r0 = warp; r0 < n_u; r0 += kVdWarps * kVdBatch) {
+  for (int i0 = warp; i0 < n_loc; i0 += kVdWarps * kVdBatch) {
     uint64_t wl = 0ull;
     uint16_t sl = 0;
     {
-      const int u = lane >> 3, r = r0 + u * kVdWarps;
-      if (u < kVdBatch && r < n_u && (lane & 7) < 2 * S.dep[r]) {
-        const int64_t tok = rows[r];
+      const int u = lane >> 3, i = i0 + u * kVdWarps;
+      if (u < kVdBatch && i < n_loc && (lane & 7) < 2 * S.dep[i]) {
+        const int64_t tok = rows[row_of(i)];
         wl = vpu[tok * (kPlanes * kD / 64) + (lane & 7)];
         if ((lane & 7) == 0) sl = vsu[tok];
       }
     }
 #pragma unroll
     for (int u = 0; u < kVdBatch; ++u) {
-      const int r = r0 + u * kVdWarps;
-      if (r >= n_u) break;  // uniform across the warp
-      const int t = S.dep[r];
+      const int i = i0 + u * kVdWarps;
+      if (i >= n_loc) break;  // uniform across the warp
+      const int t = S.dep[i];
       if (t == 0) continue;
       const float s = fp16_bits_to_float((uint16_t)__shfl_sync(0xffffffffu, (uint32_t)sl, 8 * u));
       uint32_t c[4] = {0u, 0u, 0u, 0u};
@@ -289,21 +336,27 @@ __global__ void __launch_bounds__(kVdThreads) k_attend_vdepth(VdArgs a) {
       const float step = ldexpf(s, 4 - t);  // s 2^(4 - t)
       float vh[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) vh[i] = fmaf((float)c[i] + 0.5f, step, -8.f * s);
+      for (int k = 0; k < 4; ++k) vh[k] = fmaf((float)c[k] + 0.5f, step, -8.f * s);
 #pragma unroll
       for (int h = 0; h < GP; ++h) {
-        const float pr = S.p[h][r];
+        const float pr = S.p[h][i];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc[h][i] = fmaf(pr, vh[i], acc[h][i]);
+        for (int k = 0; k < 4; ++k) acc[h][k] = fmaf(pr, vh[k], acc[h][k]);
       }
     }
   }
 #pragma unroll
   for (int h = 0; h < GP; ++h)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) atomicAdd(&S.o[h][lane + 32 * i], acc[h][i]);
-  __syncthreads();
-  for (int e = tid; e < G * kD; e += kVdThreads) a.out[unit * G * kD + e] = S.o[e / kD][e % kD];
+    for (int k = 0; k < 4; ++k) atomicAdd(&S.o[h][lane + 32 * k], acc[h][k]);
+  cl.sync();  // every CTA's share of the output is complete
+  // CTA rank adds the cluster's shares of its slice of the G D outputs (CTAs in rank order)
+  for (int e = rank * kVdThreads + tid; e < G * kD; e += kVdCluster * kVdThreads) {
+    float v = 0.f;
+    for (int c = 0; c < kVdCluster; ++c) v += cl.map_shared_rank(&S.o[0][0], c)[e];
+    a.out[unit * G * kD + e] = v;
+  }
+  cl.sync();  // no CTA leaves while another still reads its shared memory
 }
 
 size_t vdepth_smem(int group) {
@@ -318,7 +371,21 @@ cudaError_t launch_vdepth_gp(const VdArgs& a, unsigned units, cudaStream_t st) {
   const int smem = (int)sizeof(VdSmem<GP>);
   cudaError_t e = cudaFuncSetAttribute(k_attend_vdepth<GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_attend_vdepth<GP>, dim3(units), dim3(kVdThreads), (size_t)smem, st, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(units * kVdCluster);
+  cfg.blockDim = dim3(kVdThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kVdCluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k_attend_vdepth<GP>, a);
 }
 
 cudaError_t launch_attend_vdepth(const bpkv_cache& c, const float* q, const int32_t* uidx, const uint8_t* umask,
