@@ -34,8 +34,8 @@ namespace bpkv {
 
 // ---------------------------------------------------------------- stage 2
 
-constexpr int kVdCluster = 8;                          // CTAs per unit
-constexpr int kVdThreads = 256;
+constexpr int kVdCluster = 8;                          // CTAs per unit (16 measured slower)
+constexpr int kVdThreads = 512;
 constexpr int kVdWarps = kVdThreads / 32;
 constexpr int kVdMaxRows = 2048;                       // union rows of one unit (G k)
 constexpr int kVdLocal = kVdMaxRows / kVdCluster;      // rows of one CTA
@@ -371,6 +371,10 @@ cudaError_t launch_vdepth_gp(const VdArgs& a, unsigned units, cudaStream_t st) {
   const int smem = (int)sizeof(VdSmem<GP>);
   cudaError_t e = cudaFuncSetAttribute(k_attend_vdepth<GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  if (kVdCluster > 8) {
+    e = cudaFuncSetAttribute(k_attend_vdepth<GP>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(units * kVdCluster);
   cfg.blockDim = dim3(kVdThreads);
