@@ -407,3 +407,22 @@ def test_topk_long_rows_level1(pk, orc, n, ties):
         for g in range(G):
             want = orc.topk(sc[0, h, g].numpy().astype(np.float64), k)
             assert np.array_equal(got[0, h, g], want), (h, g)
+
+
+@pytest.mark.parametrize("n,n_sink,n_recent,k,ties", [(140000, 5, 30, 512, 0.0), (98307, 7, 33, 300, 0.5),
+                                                      (70001, 0, 0, 64, 0.0), (65537, 3, 1, 37, 0.9)])
+def test_topk_streaming_cut_unaligned(pk, orc, n, n_sink, n_recent, k, ties):
+    """Grids too large to run cooperatively (the row bucket kernel, then the
+    streaming cut over token-aligned 8192-token chunks) with sink and recent
+    counts that are not multiples of 4: the middle range starts and ends
+    inside 16-byte score groups and inside chunks."""
+    from workload.gen import random_scores
+    N, H, G = 1, 8, 4  # 32 rows: more CTAs than fit at once for every n here
+    kk, vv = _rand_kv(N, H, n, seed=15)
+    c = build_cache(kk, vv, G)
+    sc = random_scores(N * H * G, n, seed=n + k, tie_frac=ties).reshape(N, H, G, n)
+    got = _topk_rows(pk, c, sc, k, n_sink, n_recent)
+    for h in range(H):
+        for g in range(G):
+            want = orc.topk(sc[0, h, g].numpy().astype(np.float64), k, n_sink, n_recent)
+            assert np.array_equal(got[0, h, g], want), (h, g)
