@@ -125,3 +125,21 @@ def test_step_selection_edges(pk, orc, n_tok, k, fixed):
     inp.k, inp.v = inp.k.cpu(), inp.v.cpu()
     for h in (0, 5):
         check_unit(orc, cfg, inp, cache, d, idx, out, 0, h, depth_rule=1, fixed=fixed, what=f"n{n_tok} k{k} h{h}")
+
+
+@pytest.mark.parametrize("n_sink,n_recent,n_tok", [(5, 30, 70001), (0, 1, 65536 + 1023), (7, 0, 40000 + 3)])
+def test_step_unaligned_sink_recent(pk, orc, n_sink, n_recent, n_tok):
+    """Decode steps through the row buckets and the streaming cut (a grid
+    larger than fits at once: 2 sequences x 8 KV heads x 4 heads) with sink
+    and recent counts that are not multiples of 4, so the middle range starts
+    and ends inside score groups and selection windows; every head of the
+    sampled units is checked against the oracle."""
+    import dataclasses
+    from workload import CONFIGS, gen_layer
+    cfg = dataclasses.replace(CONFIGS["multi_session"], n_seq=2, n_tokens=n_tok, n_sink=n_sink, n_recent=n_recent,
+                              k=n_sink + n_recent + 200)
+    inp = gen_layer(cfg, 0, device="cuda")
+    cache, d, idx, out = decode_one_layer(inp, cfg)
+    inp.k, inp.v = inp.k.cpu(), inp.v.cpu()
+    for (s, h) in [(0, 0), (1, 5)]:
+        check_unit(orc, cfg, inp, cache, d, idx, out, s, h, what=f"sink{n_sink} recent{n_recent} s{s}h{h}")
