@@ -747,18 +747,24 @@ __global__ void __launch_bounds__(kRangeThreads, GP <= 4 ? 3 : 2) k_attend_range
   }
 }
 
-// Tokens per range: a multiple of kRangeAlign; up to kMergeBlock ranges per
-// unit while a range stays within one selection window, up to
-// kRangeMaxRanges for longer sequences.
-int64_t range_tokens(int64_t n_max, int group) {
-  (void)group;
+// Tokens per range: a multiple of kRangeAlign.  Up to kMergeBlock ranges per
+// unit while a range stays within one selection window; longer sequences get
+// ranges of at least one window, as many as fill the GPU's resident CTAs
+// about once over all units (at most kRangeMaxRanges).
+int64_t range_tokens(const bpkv_cache& c) {
+  const int64_t n_max = c.n_max;
   auto size_for = [&](int64_t ranges) {
     int64_t rt = (n_max + ranges - 1) / ranges;
     rt = (rt + kRangeAlign - 1) / kRangeAlign * kRangeAlign;
     return rt < kRangeAlign ? (int64_t)kRangeAlign : rt;
   };
   const int64_t rt = size_for(kMergeBlock);
-  return rt <= kRangeWin ? rt : std::max<int64_t>(kRangeWin, size_for(kRangeMaxRanges));
+  if (rt <= kRangeWin) return rt;
+  const int64_t units = std::max<int64_t>(1, (int64_t)c.n_seq * c.n_kv_heads);
+  const int64_t per_sm = (c.residency == 1 || c.group > 4) ? 2 : 3;  // resident CTAs per SM
+  const int64_t slots = 152 * per_sm;
+  const int64_t ranges = std::min<int64_t>(kRangeMaxRanges, std::max<int64_t>(1, slots / units));
+  return std::max<int64_t>(kRangeWin, std::max<int64_t>(size_for(ranges), size_for(kRangeMaxRanges)));
 }
 
 size_t attend_ranges_part_bytes(const bpkv_cache& c) {
@@ -767,7 +773,7 @@ size_t attend_ranges_part_bytes(const bpkv_cache& c) {
 
 // A range's union rows (at most its tokens, and at most G k) must fit the row buffers.
 bool attend_ranges_eligible(const bpkv_cache& c, int32_t k) {
-  const int64_t rows = min64(range_tokens(c.n_max, c.group), (int64_t)c.group * k);
+  const int64_t rows = min64(range_tokens(c), (int64_t)c.group * k);
   return rows <= kRangeMaxRows;
 }
 
@@ -775,7 +781,7 @@ cudaError_t launch_attend_ranges(const bpkv_cache& c, const float* q, const floa
                                  const unsigned long long* cut, int32_t n_sink, int32_t n_recent, float* part,
                                  uint32_t* tickets, float* out, int32_t pending, uint32_t* seq_tick,
                                  cudaStream_t st, uint32_t* rc_stats) {
-  const int64_t rt = range_tokens(c.n_max, c.group);
+  const int64_t rt = range_tokens(c);
   const int32_t nr = (int32_t)((c.n_max + rt - 1) / rt);
   if (nr == 0) return cudaSuccess;
   const bool rc = c.residency == 1 && c.rc_slots > 0 && rc_stats;
