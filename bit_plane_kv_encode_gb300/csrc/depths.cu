@@ -3,11 +3,12 @@
 //
 // Water-filling: one CTA per (sequence, KV head).  The 4 D items (j, t) are
 // keyed by (value desc, item index asc) with item index 4 j + t, so equal values
-// order by channel and, within a channel, by depth.  A bitonic sort in shared
-// memory orders the 512 keys, a block scan accumulates their quarter-bit costs
-// (5 for a channel's first bit: 4 for the plane + 1 for its fp16 scale; 4 after)
-// and the items before the first one that does not fit, or is worthless, are
-// taken.  This is the greedy heap's result computed as a single water level.
+// order by channel and, within a channel, by depth.  The items before the
+// first one that does not fit, or is worthless, are taken, with quarter-bit
+// costs (5 for a channel's first bit: 4 for the plane + 1 for its fp16 scale;
+// 4 after); a cost-weighted radix select over the 512 keys finds that item
+// (depths_core.cuh).  This is the greedy heap's result computed as a single
+// water level.
 //
 // In a decode step the same CTA also builds the unit's scan plan (channel
 // groups, plane rows, weights q 2^(4-t-pos)) once, so that every scan CTA of
