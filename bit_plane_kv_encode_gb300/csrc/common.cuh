@@ -46,7 +46,7 @@ constexpr int kTopkBins = 4096;  // level-0 histogram: top 12 bits of the ordere
 
 // per row: candidates gathered, CTAs done, CTAs at the barrier, spare, then
 // the row's bucket as k_bucket found it (key prefix, rank left in it, keys in
-// it, spare)
+// it, level of the prefix: 0, or 1 once narrowed by the level-1 histogram)
 constexpr int kSelCounters = 8;
 constexpr int64_t kLongRowTokens = 262144;  // rows this long get a parallel level-1 histogram
 

@@ -467,7 +467,7 @@ __global__ void __launch_bounds__(kCutThreads, 2) k_cut(CutArgs a) {
   cut_finish(S, a, row, r, sc, ctr, cand, nb, rem, prefix, 0);
 }
 
-// Streaming form (the row's bucket found by k_bucket, refined by k_hist1's
+// Streaming form (the row's bucket found by k_bucket, narrowed by the
 // level-1 histogram on long rows): grid (chunks of kStreamChunk tokens in
 // absolute position, rows); each thread loads kStreamVec 16-byte groups of
 // scores (tokens 4 (t + 256 j) .. + 3 of the chunk) at once, then keeps the
@@ -479,25 +479,27 @@ __global__ void __launch_bounds__(kCutThreads, 4) k_cut_stream(CutArgs a) {
   pdl_enter();
   __shared__ CutSmem S;
   const int row = blockIdx.y, tid = threadIdx.x, lane = tid & 31;
-  const RowRange r = row_range(a.seq_len[row / a.rows_per_seq] + a.pending, a.k, a.n_sink, a.n_recent);
-  if (r.cnt <= r.m || r.m == 0) {
-    if (blockIdx.x == 0 && tid == 0) a.cut[row] = r.cnt <= r.m ? 0ull : ~0ull;
-    return;
-  }
   const float* sc = a.scores + (int64_t)row * a.ld;
   uint32_t* ctr = a.ctr + (int64_t)kSelCounters * row;
   unsigned long long* cand = a.cand + (int64_t)row * kRankCap;
-  uint32_t prefix = ctr[4], rem = ctr[5], nb = ctr[6];  // the row's level-0 bucket (k_bucket)
-  int lvl = 0;
-  if (nb > (uint32_t)kRankCap && a.hist1) {
-    // the level-1 histogram of this bucket (counted by k_hist1) narrows it
-    uint32_t h[kBinsPerThread];
-    const int top1 = bins_of_thread(a.hist1 + (int64_t)row * kTopkBins, kTopkBins, h);
-    find_bucket(S, h, top1, rem);
-    prefix = (prefix << 12) | S.tb;
-    nb = S.nb;
-    rem = S.rem;
-    lvl = 1;
+  // the chunk's scores, the row's length and its bucket (k_bucket) read
+  // together: none of the loads waits for another
+  const uint32_t x0 = (uint32_t)blockIdx.x * kStreamChunk;  // the chunk's first token
+  const uint32_t ld = (uint32_t)a.ld;
+  const float4* p = reinterpret_cast<const float4*>(sc + x0);
+  float4 v[kStreamVec];
+#pragma unroll
+  for (int j = 0; j < kStreamVec; ++j) {
+    const uint32_t x = x0 + 4 * (tid + kCutThreads * j);
+    v[j] = x < ld ? p[tid + kCutThreads * j] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const int64_t n_row = a.seq_len[row / a.rows_per_seq];
+  const uint32_t prefix = ctr[4], rem = ctr[5], nb = ctr[6];
+  const int lvl = (int)ctr[7];
+  const RowRange r = row_range(n_row + a.pending, a.k, a.n_sink, a.n_recent);
+  if (r.cnt <= r.m || r.m == 0) {
+    if (blockIdx.x == 0 && tid == 0) a.cut[row] = r.cnt <= r.m ? 0ull : ~0ull;
+    return;
   }
   if (nb <= (uint32_t)kRankCap) {
     // the bucket as an interval of floats: key(f) in [klo, khi] exactly when
@@ -511,15 +513,7 @@ __global__ void __launch_bounds__(kCutThreads, 4) k_cut_stream(CutArgs a) {
     };
     const float flo = key_float(klo);
     const float fhi = khi == 0x7FFFFFFFu ? __uint_as_float(0x80000001u) : key_float(khi);
-    const uint32_t x0 = (uint32_t)blockIdx.x * kStreamChunk;  // the chunk's first token
-    const uint32_t lo = (uint32_t)r.lo, hi = (uint32_t)r.hi, ld = (uint32_t)a.ld;
-    const float4* p = reinterpret_cast<const float4*>(sc + x0);
-    float4 v[kStreamVec];
-#pragma unroll
-    for (int j = 0; j < kStreamVec; ++j) {
-      const uint32_t x = x0 + 4 * (tid + kCutThreads * j);
-      v[j] = x < ld ? p[tid + kCutThreads * j] : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    const uint32_t lo = (uint32_t)r.lo, hi = (uint32_t)r.hi;
     // bit 4 j + e: token x0 + 4 (tid + 256 j) + e is a middle token in the bucket
     uint32_t match = 0;
     const bool inner = x0 >= lo && x0 + kStreamChunk <= hi;  // every token of the chunk is a middle token
@@ -566,25 +560,29 @@ __global__ void __launch_bounds__(kCutThreads, 4) k_cut_stream(CutArgs a) {
 
 // ------------------------------------------------------------------ k_bucket
 
-// Per row (one CTA each): the level-0 bucket holding the m-th largest middle
-// key, from the row's counted histogram, stored in the row's counters
-// [4 .. 6] (key prefix, rank left in the bucket, keys in the bucket) for
-// k_hist1 and k_cut, so that their many CTAs need not each read and scan the
-// 4096 bins.
+// Per row (one CTA each), kLevel 0: the level-0 bucket holding the m-th
+// largest middle key, from the row's counted histogram, stored in the row's
+// counters [4 .. 7] (key prefix, rank left in the bucket, keys in the bucket,
+// level) for k_hist1 and k_cut_stream, so that their many CTAs need not each
+// read and scan the 4096 bins.  kLevel 1 (long rows, after k_hist1): a bucket
+// of more than kRankCap keys narrowed by its level-1 histogram.
+template <int kLevel>
 __global__ void __launch_bounds__(kCutThreads) k_bucket(CutArgs a) {
   pdl_enter();
   __shared__ CutSmem S;
   const int row = blockIdx.x;
+  uint32_t* ctr = a.ctr + (int64_t)kSelCounters * row;
+  if (kLevel == 1 && ctr[6] <= (uint32_t)kRankCap) return;  // small enough to rank (or no bucket)
   uint32_t h[kBinsPerThread];
-  const int top = bins_of_thread(a.hist + (int64_t)row * kTopkBins, kTopkBins, h);
+  const int top = bins_of_thread((kLevel == 1 ? a.hist1 : a.hist) + (int64_t)row * kTopkBins, kTopkBins, h);
   const RowRange r = row_range(a.seq_len[row / a.rows_per_seq] + a.pending, a.k, a.n_sink, a.n_recent);
-  if (r.cnt <= r.m || r.m == 0) return;  // k_cut decides these rows without a bucket
-  find_bucket(S, h, top, (uint32_t)r.m);
+  if (r.cnt <= r.m || r.m == 0) return;  // k_cut_stream decides these rows without a bucket
+  find_bucket(S, h, top, kLevel == 1 ? ctr[5] : (uint32_t)r.m);
   if (threadIdx.x == 0) {
-    uint32_t* ctr = a.ctr + (int64_t)kSelCounters * row;
-    ctr[4] = S.tb;
+    ctr[4] = kLevel == 1 ? (ctr[4] << 12) | S.tb : S.tb;
     ctr[5] = S.rem;
     ctr[6] = S.nb;
+    ctr[7] = (uint32_t)kLevel;
   }
 }
 
@@ -765,12 +763,15 @@ cudaError_t launch_cut(const bpkv_cache& c, const float* scores, int64_t ld, int
   CutArgs a{scores,   ld,           c.seq_len, b.hist, l1 ? b.hist1 : nullptr, b.cand, b.ctr, b.cut, status,
             c.n_kv_heads * c.group, k, n_sink, n_recent, build_hist ? 1 : 0, pending, cpc};
   if (build_hist) return launch_coop_pdl(k_cut, run_grid(c, 1), dim3(kCutThreads), 0, st, a);
-  // each row's bucket once, then (long rows) the level-1 histogram, then the
-  // cut, both over runs of chunks sized for about one wave
-  cudaError_t e = launch_pdl(k_bucket, dim3((unsigned)(c.n_seq * c.n_kv_heads * c.group)), dim3(kCutThreads), 0, st, a);
+  // each row's bucket once, then (long rows) the level-1 histogram and the
+  // bucket narrowed by it, then the cut
+  const dim3 rows((unsigned)(c.n_seq * c.n_kv_heads * c.group));
+  cudaError_t e = launch_pdl(k_bucket<0>, rows, dim3(kCutThreads), 0, st, a);
   if (e != cudaSuccess) return e;
   if (l1) {
     e = launch_pdl(k_hist1, run_grid(c, cpc), dim3(kCutThreads), 0, st, a);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(k_bucket<1>, rows, dim3(kCutThreads), 0, st, a);
     if (e != cudaSuccess) return e;
   }
   const dim3 grid((unsigned)((c.n_max + kStreamChunk - 1) / kStreamChunk), (unsigned)(c.n_seq * c.n_kv_heads * c.group));
