@@ -214,29 +214,60 @@ __device__ __forceinline__ int bins_of_thread(const uint32_t* hist, int nbins, u
 
 // Rank S.cand[0..nc) by value and set S.cut to the rem-th largest.  S.cand is
 // zero-padded to an even count (0 ranks below every candidate).  Small sets
-// are ranked by counting; larger ones sorted (bitonic, descending, padded with
-// zeros to a power of two: S.cand holds kRankCap + 2 entries).
+// are ranked by counting; larger ones by a radix select (S.hist as its
+// histogram).
 __device__ __forceinline__ void rank_cut(CutSmem& S, int nc, uint32_t rem) {
   if (nc > 128) {
-    int P = 256;
-    while (P < nc) P <<= 1;
-    for (int e = nc + (int)threadIdx.x; e < P; e += blockDim.x) S.cand[e] = 0ull;
-    __syncthreads();
-    for (int kk = 2; kk <= P; kk <<= 1) {
-      for (int j = kk >> 1; j > 0; j >>= 1) {
-        for (int t = threadIdx.x; t < P / 2; t += blockDim.x) {
-          const int i = 2 * t - (t & (j - 1));  // lower element of the pair, partner i + j
-          const bool desc = (i & kk) == 0;
-          const unsigned long long x = S.cand[i], y = S.cand[i + j];
-          if ((x < y) == desc) {
-            S.cand[i] = y;
-            S.cand[i + j] = x;
-          }
-        }
-        __syncthreads();
+    // radix select of the rem-th largest (the values are distinct), eight
+    // bits at a time from the top: descend into the bin holding it until
+    // that bin holds it alone
+    const int tid = threadIdx.x, lane = tid & 31;
+    if (rem < 1 || (int)rem > nc) return;
+    unsigned long long pre = 0ull;  // the bits above `shift` fixed so far
+    uint32_t need = rem;
+    int shift = 56;
+    for (;; shift -= 8) {
+      for (int b = tid; b < 256; b += blockDim.x) S.hist[b] = 0u;
+      __syncthreads();
+      const unsigned long long hi_mask = shift == 56 ? 0ull : (~0ull << (shift + 8));
+      for (int e = tid; e < nc; e += blockDim.x) {
+        const unsigned long long x = S.cand[e];
+        if ((x & hi_mask) == pre) atomicAdd(&S.hist[(x >> shift) & 0xFFu], 1u);
       }
+      __syncthreads();
+      if (tid < 32) {
+        // bins from the top, 32 at a time: the bin where the running count reaches need
+        uint32_t acc = 0;
+        for (int base = 224; base >= 0; base -= 32) {
+          const uint32_t c = S.hist[base + lane];
+          uint32_t incl = c;  // keys in bins base + lane .. base + 31
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
+            if (lane + o < 32) incl += y;
+          }
+          const uint32_t hit = __ballot_sync(0xffffffffu, acc + incl >= need && acc + incl - c < need);
+          if (hit) {
+            const int l = 31 - __clz(hit);
+            if (lane == l) {
+              S.tb = (uint32_t)(base + l);
+              S.rem = need - (acc + incl - c);
+              S.nb = c;
+            }
+            break;
+          }
+          acc += __shfl_sync(0xffffffffu, incl, 0);
+        }
+      }
+      __syncthreads();
+      pre |= (unsigned long long)S.tb << shift;
+      need = S.rem;
+      if (S.nb == 1u || shift == 0) break;
     }
-    if (threadIdx.x == 0 && rem >= 1 && (int)rem <= nc) S.cut = S.cand[rem - 1];
+    // the one value with the fixed bits
+    const unsigned long long mask = ~0ull << shift;
+    for (int e = tid; e < nc; e += blockDim.x)
+      if ((S.cand[e] & mask) == pre) S.cut = S.cand[e];
     return;
   }
   const int nc2 = (nc + 1) & ~1;
