@@ -50,17 +50,15 @@ __device__ __forceinline__ void zero_hist(const DepthArgs& a, int64_t unit) {
   if (a.ctr && (int)threadIdx.x < kSelCounters * a.group) a.ctr[unit * kSelCounters * a.group + threadIdx.x] = 0u;
 }
 
-// Build the scan plan of this unit from the depths the CTA just wrote (each
-// thread j < D reads back its own depth) and store it.
+// Build the scan plan of this unit from the depths the CTA just found (thread
+// j < D holds its channel's in t) and store it.
 template <int GP>
-__device__ void emit_plan(const DepthArgs& a, int64_t unit, const uint8_t* dep) {
+__device__ void emit_plan(const DepthArgs& a, int64_t unit, int t) {
   __shared__ ScanPlan<GP> P;
   __shared__ PlanScratch X;
   const int tid = threadIdx.x;
-  int t = 0;
   float qv[GP];
   if (tid < kD) {
-    t = dep[tid];
     const float* qp = a.q + unit * a.group * kD;
 #pragma unroll
     for (int hh = 0; hh < GP; ++hh) qv[hh] = hh < a.group ? qp[hh * kD + tid] : 0.f;
@@ -78,9 +76,9 @@ __global__ void __launch_bounds__(kScanThreads) k_alloc_depths(DepthArgs a) {
   if (a.tickets && threadIdx.x == 0) a.tickets[unit] = 0u;
   if (a.hist) zero_hist(a, unit);
   uint8_t* dep = a.depths + (int64_t)unit * kD;
-  alloc_depths_cta(S, a.q + (int64_t)unit * a.group * kD, a.sigma2 + (int64_t)unit * kD, a.group, a.budget_q[s],
-                   dep);
-  if (a.plan) emit_plan<GP>(a, unit, dep);
+  const int t = alloc_depths_cta(S, a.q + (int64_t)unit * a.group * kD, a.sigma2 + (int64_t)unit * kD, a.group,
+                                 a.budget_q[s], dep);
+  if (a.plan) emit_plan<GP>(a, unit, t);
 }
 
 template <int GP>
@@ -91,8 +89,8 @@ __global__ void __launch_bounds__(kScanThreads) k_fixed_depths(DepthArgs a) {
   if (a.tickets && threadIdx.x == 0) a.tickets[unit] = 0u;
   if (a.hist) zero_hist(a, unit);
   uint8_t* dep = a.depths + (int64_t)unit * kD;
-  fixed_depths_cta(S, a.q + (int64_t)unit * a.group * kD, a.group, a.n_channels, a.depth, dep);
-  if (a.plan) emit_plan<GP>(a, unit, dep);
+  const int t = fixed_depths_cta(S, a.q + (int64_t)unit * a.group * kD, a.group, a.n_channels, a.depth, dep);
+  if (a.plan) emit_plan<GP>(a, unit, t);
 }
 
 template <typename F>
@@ -196,15 +194,18 @@ __global__ void __launch_bounds__(kScanThreads) k_front(FrontArgs a) {
     __syncthreads();
     d.q = a.q_rot;
   }
+  int t = 0;  // thread j < D: channel j's depth
   if (a.depth_rule == BPKV_DEPTH_WATERFILL) {
-    alloc_depths_cta(S, d.q + unit * G * kD, a.d.sigma2 + unit * kD, G, a.d.budget_q[s], dep);
+    t = alloc_depths_cta(S, d.q + unit * G * kD, a.d.sigma2 + unit * kD, G, a.d.budget_q[s], dep);
   } else if (a.depth_rule == BPKV_DEPTH_GIVEN) {
-    // each thread writes the entry it reads back in emit_plan
-    if (threadIdx.x < kD) dep[threadIdx.x] = (uint8_t)min((int)a.depths_in[unit * kD + threadIdx.x], 4);
+    if (threadIdx.x < kD) {
+      t = min((int)a.depths_in[unit * kD + threadIdx.x], 4);
+      dep[threadIdx.x] = (uint8_t)t;
+    }
   } else {
-    fixed_depths_cta(S, d.q + unit * G * kD, G, a.d.n_channels, a.d.depth, dep);
+    t = fixed_depths_cta(S, d.q + unit * G * kD, G, a.d.n_channels, a.d.depth, dep);
   }
-  emit_plan<GP>(d, unit, dep);
+  emit_plan<GP>(d, unit, t);
 }
 
 cudaError_t launch_front(const bpkv_cache& c, const uint16_t* k_new, const uint16_t* v_new, int32_t t_new,

@@ -19,7 +19,8 @@ struct DepthSmem {
 };
 
 // Water-filling for one (sequence, KV head): qp [G][D], s2 [D], budget B in
-// quarter-bits; depths written to out[0..D).  Needs blockDim.x == 256.
+// quarter-bits; depths written to out[0..D) and returned to thread j < D (its
+// channel's), 0 to the others.  Needs blockDim.x == 256.
 //
 // The items (j, t) in descending key order (value g_j 4^-t, then the lower
 // item index 4 j + t first) are taken until the first one, X, whose running
@@ -30,8 +31,8 @@ struct DepthSmem {
 // passes the budget left holds X.  Once X is alone in its bin the taken items
 // are exactly those whose key bits above the level's shift exceed the bin's;
 // if every positive item fits, all of them are taken.
-static __device__ void alloc_depths_cta(DepthSmem& S, const float* __restrict__ qp, const float* __restrict__ s2, int G,
-                                 int B, uint8_t* out) {
+static __device__ int alloc_depths_cta(DepthSmem& S, const float* __restrict__ qp, const float* __restrict__ s2, int G,
+                                        int B, uint8_t* out) {
   const int tid = threadIdx.x, lane = tid & 31;
   unsigned long long key[4] = {0ull, 0ull, 0ull, 0ull};
   if (tid < kD) {
@@ -121,8 +122,8 @@ static __device__ void alloc_depths_cta(DepthSmem& S, const float* __restrict__ 
     pre |= (unsigned long long)S.cut_bin << shift;
   }
   // depth of channel tid: its items taken (keys in descending order per channel)
+  int t = 0;
   if (tid < kD) {
-    int t = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const bool taken = key[i] != 0ull && (S.done == 1 || (key[i] >> S.shift) > S.top);
@@ -131,12 +132,14 @@ static __device__ void alloc_depths_cta(DepthSmem& S, const float* __restrict__ 
     out[tid] = static_cast<uint8_t>(t);
   }
   __syncthreads();
+  return t;
 }
 
 // Fixed sets: the n_channels channels with the largest sum_h |q_hj| (ties to
-// the lower index) at depth t.  Threads 0..127 take part.
-static __device__ void fixed_depths_cta(DepthSmem& S, const float* __restrict__ qp, int G, int n_channels, int t,
-                                 uint8_t* out) {
+// the lower index) at depth t; returned to thread j < D as for the
+// water-filling.  Threads 0..127 take part.
+static __device__ int fixed_depths_cta(DepthSmem& S, const float* __restrict__ qp, int G, int n_channels, int t,
+                                       uint8_t* out) {
   const int j = threadIdx.x;
   float acc = 0.f;
   if (j < kD) {
@@ -144,12 +147,15 @@ static __device__ void fixed_depths_cta(DepthSmem& S, const float* __restrict__ 
     S.asum[j] = acc;
   }
   __syncthreads();
+  int d = 0;
   if (j < kD) {
     int rank = 0;
     for (int i = 0; i < kD; ++i) rank += (S.asum[i] > acc) || (S.asum[i] == acc && i < j);
-    out[j] = static_cast<uint8_t>(rank < n_channels ? t : 0);
+    d = rank < n_channels ? t : 0;
+    out[j] = static_cast<uint8_t>(d);
   }
   __syncthreads();
+  return d;
 }
 
 }  // namespace bpkv
