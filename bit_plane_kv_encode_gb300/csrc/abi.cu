@@ -19,20 +19,21 @@ bool attend_ranges_eligible(const bpkv_cache& c, int32_t k);
 cudaError_t launch_attend_ranges(const bpkv_cache& c, const float* q, const float* scores, int64_t ld,
                                  const unsigned long long* cut, int32_t n_sink, int32_t n_recent, float* part,
                                  uint32_t* tickets, float* out, int32_t pending, uint32_t* seq_tick,
-                                 cudaStream_t st, uint32_t* rc_stats = nullptr);
+                                 cudaStream_t st, uint32_t* rc_stats = nullptr, const uint32_t* selmap = nullptr);
 cudaError_t launch_scan(const bpkv_cache& c, const float* q, const uint8_t* depths, float* scores, int64_t ld,
                         cudaStream_t st, const void* plan = nullptr, uint32_t* hist = nullptr,
                         int32_t n_sink = 0, int32_t n_recent = 0, int32_t pending = 0,
                         int32_t* status = nullptr);
 cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
                         int32_t n_recent, const SelBufs& b, HistState hs, int32_t* idx, int32_t* status,
-                        cudaStream_t st, int32_t pending = 0);
+                        cudaStream_t st, int32_t pending = 0, uint32_t* selmap = nullptr);
 cudaError_t launch_front(const bpkv_cache& c, const uint16_t* k_new, const uint16_t* v_new, int32_t t_new,
                          const float* q, const float* sigma2, const int32_t* budget_q, int32_t depth_rule,
                          int32_t n_channels, int32_t depth, uint8_t* depths, void* plan, uint32_t* hist,
                          uint32_t* hist1, uint32_t* ctr, uint32_t* tickets, uint32_t* seq_tick, cudaStream_t st,
                          const uint8_t* depths_in, float* q_rot, int32_t* status = nullptr);
 bool scan_counts_hist(const bpkv_cache& c);
+bool cut_counts_hist(const bpkv_cache& c);
 cudaError_t launch_union(const bpkv_cache& c, const int32_t* idx, int32_t k, int32_t* uidx, uint8_t* umask,
                          int32_t* ucount, cudaStream_t st);
 cudaError_t launch_attend(const bpkv_cache& c, const float* q, const int32_t* uidx, const uint8_t* umask,
@@ -93,7 +94,7 @@ cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 // Workspace layout: status word, then the buffers each call family needs.
 struct Layout {
   size_t scores = 0, hist = 0, hist1 = 0, ctr = 0, cand = 0, cut = 0, part = 0, depths = 0, idx = 0, uidx = 0, umask = 0,
-         ucount = 0, tickets = 0, seq_tick = 0, plan = 0, q_rot = 0, rc_stats = 0, total = 0;
+         ucount = 0, tickets = 0, seq_tick = 0, plan = 0, q_rot = 0, rc_stats = 0, selmap = 0, total = 0;
 };
 
 Layout layout(const bpkv_cache& c, int32_t k, int32_t what) {
@@ -150,6 +151,9 @@ Layout layout(const bpkv_cache& c, int32_t k, int32_t what) {
     // the row cache's counts of the step: rows found in it, rows
     L.rc_stats = off;
     off = align_up(off + 2 * NH * sizeof(uint32_t));
+    // the cut's bits of each head's chosen middle tokens, for the attention
+    L.selmap = off;
+    off = align_up(off + NH * c.group * (size_t)(c.cap_tokens / 32) * sizeof(uint32_t));
   }
   L.total = off;
   return L;
@@ -443,13 +447,15 @@ int bpkv_decode_step(bpkv_cache* layers, int32_t n_layers, const bpkv_step_args*
       // cuts only (lists when asked for); the attention selects by cut, forms
       // the union per token range and finally raises seq_len
       int32_t* iout = a->idx_out ? a->idx_out + (size_t)l * NH * G * a->k : nullptr;
+      // the streaming cut also marks the chosen tokens for the attention
+      uint32_t* selmap = cut_counts_hist(c) ? nullptr : reinterpret_cast<uint32_t*>(at(ws, L.selmap));
       BPKV_TRY(cuda_status(
-          launch_topk(c, scores, c.cap_tokens, a->k, a->n_sink, a->n_recent, sb, hs, iout, status, st, 1)));
+          launch_topk(c, scores, c.cap_tokens, a->k, a->n_sink, a->n_recent, sb, hs, iout, status, st, 1, selmap)));
       BPKV_TRY(mark(l, 4));
       BPKV_TRY(mark(l, 5));
       BPKV_TRY(cuda_status(launch_attend_ranges(c, q, scores, c.cap_tokens, sb.cut, a->n_sink, a->n_recent, part,
                                                 tickets, out, 1, seq_tick, st,
-                                                reinterpret_cast<uint32_t*>(at(ws, L.rc_stats)))));
+                                                reinterpret_cast<uint32_t*>(at(ws, L.rc_stats)), selmap)));
       BPKV_TRY(mark(l, 6));
       continue;
     }

@@ -280,6 +280,11 @@ struct RangeArgs {
   int32_t rc_slots;                // 0: no row cache
   int32_t rc_part;                 // slots per range
   uint32_t* rc_stats;              // [N][H][2] rows found, rows (summed over the step's layers)
+  // optional: the cut kernel's bits of each head's chosen middle tokens
+  // ([N][H][G][map_words], bit x % 32 of word x / 32); without it the
+  // selection compares the scores with the cuts
+  const uint32_t* selmap;
+  int64_t map_words;
 };
 
 // Shared memory of a range CTA for up to GP heads (kRc: with the row cache's
@@ -303,6 +308,16 @@ struct RangeSmem {
   float lslot[kRangeThreads / 32][BPKV_MAX_GROUP];
   uint32_t n_rows, is_last;
 };
+
+// Bits of the tokens [max(a, x), min(b, x + 32)) in the word of tokens x .. x + 31.
+__device__ __forceinline__ uint32_t span_bits(int64_t x, int64_t a, int64_t b) {
+  const int64_t s = max64(a - x, 0), e = min64(b - x, 32);
+  if (e <= s) return 0u;
+  const uint32_t upto = e >= 32 ? 0xFFFFFFFFu : ((1u << e) - 1u);
+  return upto & ~((1u << s) - 1u);
+}
+
+constexpr int kMapPer = 2;  // map words (32 tokens) per thread and round
 
 // Inverse of ordered_key.
 __device__ __forceinline__ float key_to_float(uint32_t k) {
@@ -340,86 +355,158 @@ __global__ void __launch_bounds__(kRangeThreads, GP <= 4 ? 3 : 2) k_attend_range
     S.mkey[tid] = 0u;
   }
   __syncthreads();
-  // selection, in windows of kRangeWin tokens: thread = 4-token quads, all
-  // heads' scores of a quad loaded at once (kWinQuads quads in flight); the quads'
-  // head masks go to shared memory, then each thread compacts a run of
-  // consecutive tokens in order.
-  const float* sc = a.scores + unit * G * a.ld;
-  const uint32_t all = (1u << G) - 1u;
   uint32_t carry = 0;
-  for (int64_t w0 = t0; w0 < t1; w0 += kRangeWin) {
-    const int wl = (int)min64(kRangeWin, t1 - w0);
-    const int wq = (wl + 3) / 4;  // score rows hold whole quads (their length is a multiple of 4)
-    // every token of the window is a middle token (no sink, recent or past-the-end checks)
-    const bool inner = w0 >= lo && w0 + kRangeWin <= hi && w0 + kRangeWin <= t1;
-    __syncthreads();              // the previous window is done
-    constexpr int WB = win_batch<GP>();
-    for (int q0 = tid; q0 < wq; q0 += WB * kRangeThreads) {
-      float4 v[WB][GP];
+  if (a.selmap) {
+    // selection from the cut kernel's bits of the chosen middle tokens (a
+    // head whose cut is 0 chose every middle token, one whose cut is all ones
+    // none); sinks and recent tokens every head.  Each thread takes kMapPer
+    // consecutive words of 32 tokens per round and compacts their tokens in
+    // order.
+    const uint32_t* mp = a.selmap + unit * G * a.map_words;
+    const int64_t nw = (t1 - t0 + 31) / 32;  // t0 is a multiple of 32
+    for (int64_t i0 = 0; i0 < nw; i0 += (int64_t)kMapPer * kRangeThreads) {
+      __syncthreads();  // the previous round is done with warp_tot
+      uint32_t hw[kMapPer][GP];
+      uint32_t c_sel = 0;
 #pragma unroll
-      for (int u = 0; u < WB; ++u) {
-        const int qd = min(q0 + u * kRangeThreads, wq - 1);  // unconditional loads
-#pragma unroll
-        for (int g = 0; g < GP; ++g)
-          if (g < G) v[u][g] = *reinterpret_cast<const float4*>(sc + g * a.ld + w0 + 4 * qd);
-      }
-#pragma unroll
-      for (int u = 0; u < WB; ++u) {
-        const int qd = q0 + u * kRangeThreads;
-        if (qd >= wq) break;
-        uint32_t packed = 0;
-        const uint32_t xq = (uint32_t)(w0 + 4 * qd);  // the quad's first token
+      for (int k = 0; k < kMapPer; ++k) {
+        const int64_t i = i0 + (int64_t)tid * kMapPer + k;
+        const int64_t x = t0 + 32 * i;
+        const uint32_t valid = i < nw ? span_bits(x, x, t1) : 0u;
+        const uint32_t mid = valid & span_bits(x, lo, hi);
+        uint32_t u = 0;
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
-          if (g >= G) break;
-          const float fc = S.fck[g];
-          const uint32_t ci = S.ci[g];
-          const float f[4] = {v[u][g].x, v[u][g].y, v[u][g].z, v[u][g].w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (f[j] > fc || (f[j] == fc && xq + j <= ci)) packed |= 1u << (8 * j + g);
-        }
-        if (!inner) {
-          // tokens past the range's end take nothing; sinks and recent tokens every head
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t x = xq + j;
-            if (x >= (uint32_t)t1) packed &= ~(0xFFu << (8 * j));
-            else if (x < (uint32_t)lo || x >= (uint32_t)hi) packed |= all << (8 * j);
+          uint32_t w = 0u;
+          if (g < G && valid) {
+            const uint32_t ckg = S.ck[g], cig = S.ci[g];
+            if (ckg == 0u && cig == 0xFFFFFFFFu) w = 0xFFFFFFFFu;     // cut 0: every middle token
+            else if (ckg == 0xFFFFFFFFu && cig == 0u) w = 0u;         // cut all ones: none
+            else w = mp[g * a.map_words + (x >> 5)];
+            w = (w & mid) | (valid & ~mid);
           }
+          hw[k][g] = w;
+          u |= w;
         }
-        reinterpret_cast<uint32_t*>(S.wbits)[qd] = packed;
+        c_sel += __popc(u);
       }
-    }
-    __syncthreads();
-    const int run = (wl + kRangeThreads - 1) / kRangeThreads, j0 = tid * run;
-    uint32_t c_sel = 0;
-    for (int j = 0; j < run; ++j) c_sel += (j0 + j < wl && S.wbits[j0 + j] != 0);
-    uint32_t x = c_sel;
+      uint32_t xs = c_sel;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) S.warp_tot[warp] = x;
-    __syncthreads();
-    uint32_t pos = carry + x - c_sel, total = 0;
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, xs, o);
+        if (lane >= o) xs += y;
+      }
+      if (lane == 31) S.warp_tot[warp] = xs;
+      __syncthreads();
+      uint32_t pos = carry + xs - c_sel, total = 0;
 #pragma unroll
-    for (int w = 0; w < kRangeThreads / 32; ++w) {
-      const uint32_t t = S.warp_tot[w];
-      pos += w < warp ? t : 0u;
-      total += t;
-    }
-    for (int j = 0; j < run; ++j) {
-      if (j0 + j < wl && S.wbits[j0 + j] != 0) {
-        if (pos < (uint32_t)kRangeMaxRows) {
-          S.rows[pos] = (int32_t)(w0 + j0 + j);
-          S.rmask[pos] = S.wbits[j0 + j];
+      for (int w = 0; w < kRangeThreads / 32; ++w) {
+        const uint32_t t = S.warp_tot[w];
+        pos += w < warp ? t : 0u;
+        total += t;
+      }
+#pragma unroll
+      for (int k = 0; k < kMapPer; ++k) {
+        const int64_t x = t0 + 32 * (i0 + (int64_t)tid * kMapPer + k);
+        uint32_t u = 0;
+#pragma unroll
+        for (int g = 0; g < GP; ++g) u |= hw[k][g];
+        while (u) {
+          const int b = __ffs(u) - 1;
+          u &= u - 1u;
+          if (pos < (uint32_t)kRangeMaxRows) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int g = 0; g < GP; ++g) m |= ((hw[k][g] >> b) & 1u) << g;
+            S.rows[pos] = (int32_t)(x + b);
+            S.rmask[pos] = (uint8_t)m;
+          }
+          ++pos;
         }
-        ++pos;
       }
+      carry += total;
     }
-    carry += total;
+  } else {
+    // selection, in windows of kRangeWin tokens: thread = 4-token quads, all
+    // heads' scores of a quad loaded at once (kWinQuads quads in flight); the quads'
+    // head masks go to shared memory, then each thread compacts a run of
+    // consecutive tokens in order.
+    const float* sc = a.scores + unit * G * a.ld;
+    const uint32_t all = (1u << G) - 1u;
+    for (int64_t w0 = t0; w0 < t1; w0 += kRangeWin) {
+      const int wl = (int)min64(kRangeWin, t1 - w0);
+      const int wq = (wl + 3) / 4;  // score rows hold whole quads (their length is a multiple of 4)
+      // every token of the window is a middle token (no sink, recent or past-the-end checks)
+      const bool inner = w0 >= lo && w0 + kRangeWin <= hi && w0 + kRangeWin <= t1;
+      __syncthreads();              // the previous window is done
+      constexpr int WB = win_batch<GP>();
+      for (int q0 = tid; q0 < wq; q0 += WB * kRangeThreads) {
+        float4 v[WB][GP];
+  #pragma unroll
+        for (int u = 0; u < WB; ++u) {
+          const int qd = min(q0 + u * kRangeThreads, wq - 1);  // unconditional loads
+  #pragma unroll
+          for (int g = 0; g < GP; ++g)
+            if (g < G) v[u][g] = *reinterpret_cast<const float4*>(sc + g * a.ld + w0 + 4 * qd);
+        }
+  #pragma unroll
+        for (int u = 0; u < WB; ++u) {
+          const int qd = q0 + u * kRangeThreads;
+          if (qd >= wq) break;
+          uint32_t packed = 0;
+          const uint32_t xq = (uint32_t)(w0 + 4 * qd);  // the quad's first token
+  #pragma unroll
+          for (int g = 0; g < GP; ++g) {
+            if (g >= G) break;
+            const float fc = S.fck[g];
+            const uint32_t ci = S.ci[g];
+            const float f[4] = {v[u][g].x, v[u][g].y, v[u][g].z, v[u][g].w};
+  #pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (f[j] > fc || (f[j] == fc && xq + j <= ci)) packed |= 1u << (8 * j + g);
+          }
+          if (!inner) {
+            // tokens past the range's end take nothing; sinks and recent tokens every head
+  #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t x = xq + j;
+              if (x >= (uint32_t)t1) packed &= ~(0xFFu << (8 * j));
+              else if (x < (uint32_t)lo || x >= (uint32_t)hi) packed |= all << (8 * j);
+            }
+          }
+          reinterpret_cast<uint32_t*>(S.wbits)[qd] = packed;
+        }
+      }
+      __syncthreads();
+      const int run = (wl + kRangeThreads - 1) / kRangeThreads, j0 = tid * run;
+      uint32_t c_sel = 0;
+      for (int j = 0; j < run; ++j) c_sel += (j0 + j < wl && S.wbits[j0 + j] != 0);
+      uint32_t x = c_sel;
+  #pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) S.warp_tot[warp] = x;
+      __syncthreads();
+      uint32_t pos = carry + x - c_sel, total = 0;
+  #pragma unroll
+      for (int w = 0; w < kRangeThreads / 32; ++w) {
+        const uint32_t t = S.warp_tot[w];
+        pos += w < warp ? t : 0u;
+        total += t;
+      }
+      for (int j = 0; j < run; ++j) {
+        if (j0 + j < wl && S.wbits[j0 + j] != 0) {
+          if (pos < (uint32_t)kRangeMaxRows) {
+            S.rows[pos] = (int32_t)(w0 + j0 + j);
+            S.rmask[pos] = S.wbits[j0 + j];
+          }
+          ++pos;
+        }
+      }
+      carry += total;
+    }
   }
   if (tid == 0) S.n_rows = min(carry, (uint32_t)kRangeMaxRows);
   __syncthreads();
@@ -780,7 +867,7 @@ bool attend_ranges_eligible(const bpkv_cache& c, int32_t k) {
 cudaError_t launch_attend_ranges(const bpkv_cache& c, const float* q, const float* scores, int64_t ld,
                                  const unsigned long long* cut, int32_t n_sink, int32_t n_recent, float* part,
                                  uint32_t* tickets, float* out, int32_t pending, uint32_t* seq_tick,
-                                 cudaStream_t st, uint32_t* rc_stats) {
+                                 cudaStream_t st, uint32_t* rc_stats, const uint32_t* selmap) {
   const int64_t rt = range_tokens(c);
   const int32_t nr = (int32_t)((c.n_max + rt - 1) / rt);
   if (nr == 0) return cudaSuccess;
@@ -789,7 +876,7 @@ cudaError_t launch_attend_ranges(const bpkv_cache& c, const float* q, const floa
   RangeArgs a{c.k_rows, c.v_rows, c.seq_len,     q,       scores, ld,      cut,    n_sink, n_recent,
               c.cap_tokens, c.n_kv_heads, c.group, rt, nr, part, tickets, out, pending, c.seq_len, seq_tick,
               rc && rc_part > 0 ? c.rc_rows : nullptr, rc ? c.rc_tok : nullptr, rc && rc_part > 0 ? c.rc_slots : 0,
-              rc_part, rc_stats};
+              rc_part, rc_stats, selmap, ld / 32};
   auto go = [&](auto kern, auto gp, auto rcv) -> cudaError_t {
     const int smem = (int)sizeof(RangeSmem<decltype(gp)::value, decltype(rcv)::value>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

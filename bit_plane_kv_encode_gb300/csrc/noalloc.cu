@@ -22,7 +22,7 @@ cudaError_t launch_scan(const bpkv_cache& c, const float* q, const uint8_t* dept
                         int32_t* status = nullptr);
 cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
                         int32_t n_recent, const SelBufs& b, HistState hs, int32_t* idx, int32_t* status,
-                        cudaStream_t st, int32_t pending = 0);
+                        cudaStream_t st, int32_t pending = 0, uint32_t* selmap = nullptr);
 bool scan_counts_hist(const bpkv_cache& c);
 }  // namespace bpkv
 

@@ -147,6 +147,11 @@ struct CutArgs {
   int32_t build_hist;          // count hist here (zero on entry; cooperative launch) instead of reading it
   int32_t pending;             // tokens appended in this step but not yet in seq_len
   int32_t chunks_per_cta;      // consecutive chunks of kCutChunk keys per CTA (1 when build_hist)
+  // optional (k_cut_stream): [rows][map_words] the chosen middle tokens, one
+  // bit per token (bit x % 32 of word x / 32); words of tokens past n_max
+  // are left as they are
+  uint32_t* selmap;
+  int64_t map_words;
 };
 
 struct __align__(16) CutSmem {
@@ -392,17 +397,41 @@ __device__ void cut_finish(CutSmem& S, const CutArgs& a, int row, const RowRange
   __syncthreads();
   if (!S.is_last) return;
   if (tid == 0) S.cut = ~0ull;
+  uint32_t* mrow = a.selmap ? a.selmap + (int64_t)row * a.map_words : nullptr;
   if (nb <= (uint32_t)kRankCap) {
     const int nc = (int)min(__ldcg(ctr), (uint32_t)kRankCap);
     for (int e = tid; e < nc; e += kCutThreads) S.cand[e] = __ldcg(cand + e);
     if (tid == 0) S.cand[nc] = 0ull;
     __syncthreads();
     rank_cut(S, nc, rem);
+    __syncthreads();
+    if (mrow && S.cut != ~0ull) {
+      // the bucket's chosen keys join the map (the keys above the bucket are in it)
+      for (int e = tid; e < nc; e += kCutThreads) {
+        const unsigned long long v = S.cand[e];
+        if (v >= S.cut) {
+          const uint32_t x = 0xFFFFFFFFu - (uint32_t)v;
+          atomicOr(mrow + (x >> 5), 1u << (x & 31u));
+        }
+      }
+    }
   } else {
     // refine in the shared histogram buffer
     if (tid == 0) S.nb = nb;
     __syncthreads();
     cut_refine(S, sc, r.lo, r.cnt, rem, prefix, lvl);
+    __syncthreads();
+    if (mrow && S.cut != ~0ull) {
+      // the chosen keys of the streamed bucket join the map
+      const int sh = level_shift(lvl);
+      const unsigned long long cut = S.cut;
+      const int64_t lo = r.lo;
+      for_row_keys(sc, lo, 0, r.cnt, [&](int64_t e, uint32_t key) {
+        const uint32_t x = (uint32_t)(lo + e);
+        if ((key >> sh) == prefix && (((unsigned long long)key << 32) | (0xFFFFFFFFu - x)) >= cut)
+          atomicOr(mrow + (x >> 5), 1u << (x & 31u));
+      });
+    }
   }
   __syncthreads();
   if (tid == 0) {
@@ -505,6 +534,7 @@ __global__ void __launch_bounds__(kCutThreads, 2) k_cut(CutArgs a) {
 // middle tokens whose key is in the bucket and appends them.
 constexpr int kStreamVec = 8;                              // float4 loads per thread
 constexpr int kStreamChunk = 4 * kStreamVec * kCutThreads;  // 8192 tokens per CTA
+static_assert(kStreamVec == 8, "a thread's 32 tokens are eight nibbles of the selection map");
 
 __global__ void __launch_bounds__(kCutThreads, 4) k_cut_stream(CutArgs a) {
   pdl_enter();
@@ -532,38 +562,65 @@ __global__ void __launch_bounds__(kCutThreads, 4) k_cut_stream(CutArgs a) {
     if (blockIdx.x == 0 && tid == 0) a.cut[row] = r.cnt <= r.m ? 0ull : ~0ull;
     return;
   }
-  if (nb <= (uint32_t)kRankCap) {
-    // the bucket as an interval of floats: key(f) in [klo, khi] exactly when
-    // flo <= f <= fhi (the order-preserving key is monotone; -0 and +0 share
-    // a key, so a bucket ending just below +0's key ends at the negative
-    // float nearest 0)
-    const int sh = level_shift(lvl);
-    const uint32_t klo = prefix << sh, khi = klo | ((1u << sh) - 1u);
-    auto key_float = [](uint32_t k) {
-      return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-    };
-    const float flo = key_float(klo);
-    const float fhi = khi == 0x7FFFFFFFu ? __uint_as_float(0x80000001u) : key_float(khi);
-    const uint32_t lo = (uint32_t)r.lo, hi = (uint32_t)r.hi;
-    // bit 4 j + e: token x0 + 4 (tid + 256 j) + e is a middle token in the bucket
-    uint32_t match = 0;
-    const bool inner = x0 >= lo && x0 + kStreamChunk <= hi;  // every token of the chunk is a middle token
+  // the bucket as an interval of floats: key(f) in [klo, khi] exactly when
+  // flo <= f <= fhi, and key(f) > khi exactly when f > fhi (the
+  // order-preserving key is monotone; -0 and +0 share a key, so a bucket
+  // ending just below +0's key ends at the negative float nearest 0)
+  const int sh = level_shift(lvl);
+  const uint32_t klo = prefix << sh, khi = klo | ((1u << sh) - 1u);
+  auto key_float = [](uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+  };
+  const float flo = key_float(klo);
+  const float fhi = khi == 0x7FFFFFFFu ? __uint_as_float(0x80000001u) : key_float(khi);
+  const uint32_t lo = (uint32_t)r.lo, hi = (uint32_t)r.hi;
+  // bit 4 j + e: token x0 + 4 (tid + 256 j) + e is a middle token in the
+  // bucket (match) or above it (above: every such token is chosen)
+  uint32_t match = 0, above = 0;
+#pragma unroll
+  for (int j = 0; j < kStreamVec; ++j) {
+    const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (f[e] > fhi) above |= 1u << (4 * j + e);
+      else if (f[e] >= flo) match |= 1u << (4 * j + e);
+    }
+  }
+  if (!(x0 >= lo && x0 + kStreamChunk <= hi)) {  // not every token of the chunk is a middle token
+    uint32_t mid = 0;
 #pragma unroll
     for (int j = 0; j < kStreamVec; ++j) {
-      const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+      const uint32_t x = x0 + 4 * (tid + kCutThreads * j);
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        if (f[e] >= flo && f[e] <= fhi) match |= 1u << (4 * j + e);
+        if (x + e >= lo && x + e < hi) mid |= 1u << (4 * j + e);
     }
-    if (!inner) {
-#pragma unroll
-      for (int j = 0; j < kStreamVec; ++j) {
-        const uint32_t x = x0 + 4 * (tid + kCutThreads * j);
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (x + e < lo || x + e >= hi) match &= ~(1u << (4 * j + e));
-      }
+    match &= mid;
+    above &= mid;
+  }
+  if (a.selmap) {
+    // the map's words of this chunk (the last CTA adds the bucket's chosen
+    // tokens): word (x0 + 1024 j) / 32 + tid / 8 is nibble j of lanes
+    // 8 (lane / 8) .. + 7, so an 8 x 8 nibble transpose within each group of
+    // eight lanes leaves word j = lane % 8 in each lane
+    uint32_t w = above;
+    const int l8 = lane & 7;
+    {
+      const uint32_t p = __shfl_xor_sync(0xffffffffu, w, 4);
+      w = (l8 & 4) ? ((w & 0xFFFF0000u) | (p >> 16)) : ((w & 0x0000FFFFu) | (p << 16));
     }
+    {
+      const uint32_t p = __shfl_xor_sync(0xffffffffu, w, 2);
+      w = (l8 & 2) ? ((w & 0xFF00FF00u) | ((p >> 8) & 0x00FF00FFu)) : ((w & 0x00FF00FFu) | ((p << 8) & 0xFF00FF00u));
+    }
+    {
+      const uint32_t p = __shfl_xor_sync(0xffffffffu, w, 1);
+      w = (l8 & 1) ? ((w & 0xF0F0F0F0u) | ((p >> 4) & 0x0F0F0F0Fu)) : ((w & 0x0F0F0F0Fu) | ((p << 4) & 0xF0F0F0F0u));
+    }
+    const uint32_t xw = x0 + 1024u * (uint32_t)l8 + 32u * (uint32_t)(tid >> 3);  // the word's first token
+    if (xw < ld) a.selmap[(int64_t)row * a.map_words + (xw >> 5)] = w;
+  }
+  if (nb <= (uint32_t)kRankCap) {
     const uint32_t cnt = __popc(match);
     uint32_t incl = cnt;
 #pragma unroll
@@ -786,13 +843,16 @@ bool scan_counts_hist(const bpkv_cache& c) { return !cut_counts_hist(c) && (c.re
 // a parallel level-1 histogram (k_hist1) before the cut.
 bool long_rows(const bpkv_cache& c) { return c.n_max >= kLongRowTokens; }
 
+// selmap (optional, streaming form only): the chosen middle tokens' bits,
+// [rows][ld / 32] words (ld a multiple of 32).
 cudaError_t launch_cut(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
                        int32_t n_recent, const SelBufs& b, bool build_hist, int32_t pending, int32_t* status,
-                       cudaStream_t st) {
+                       cudaStream_t st, uint32_t* selmap) {
   const bool l1 = !build_hist && long_rows(c);
   const int32_t cpc = build_hist ? 1 : chunks_per_cta(c);
   CutArgs a{scores,   ld,           c.seq_len, b.hist, l1 ? b.hist1 : nullptr, b.cand, b.ctr, b.cut, status,
-            c.n_kv_heads * c.group, k, n_sink, n_recent, build_hist ? 1 : 0, pending, cpc};
+            c.n_kv_heads * c.group, k, n_sink, n_recent, build_hist ? 1 : 0, pending, cpc,
+            build_hist ? nullptr : selmap, ld / 32};
   if (build_hist) return launch_coop_pdl(k_cut, run_grid(c, 1), dim3(kCutThreads), 0, st, a);
   // each row's bucket once, then (long rows) the level-1 histogram and the
   // bucket narrowed by it, then the cut
@@ -822,10 +882,11 @@ cudaError_t launch_lists(const bpkv_cache& c, const float* scores, int64_t ld, i
 // Top-k of every row: the cuts into b.cut and, when idx is given, the index
 // lists.  Histograms still to be counted are counted by the cut kernel itself
 // (cooperative launch) or, when its grid cannot be resident at once, by k_hist
-// first.
+// first.  selmap: see launch_cut (written when the cut is not the cooperative
+// one, i.e. when !cut_counts_hist(c) or the histograms come counted).
 cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
                         int32_t n_recent, const SelBufs& b, HistState hs, int32_t* idx, int32_t* status,
-                        cudaStream_t st, int32_t pending) {
+                        cudaStream_t st, int32_t pending, uint32_t* selmap) {
   cudaError_t e;
   bool build = false;
   if (hs == HistState::kDirty) {
@@ -840,7 +901,7 @@ cudaError_t launch_topk(const bpkv_cache& c, const float* scores, int64_t ld, in
       if (e != cudaSuccess) return e;
     }
   }
-  e = launch_cut(c, scores, ld, k, n_sink, n_recent, b, build, pending, status, st);
+  e = launch_cut(c, scores, ld, k, n_sink, n_recent, b, build, pending, status, st, selmap);
   if (e != cudaSuccess || !idx) return e;
   return launch_lists(c, scores, ld, k, n_sink, n_recent, b.cut, idx, status, pending, st);
 }
