@@ -606,9 +606,9 @@ def bench_vdepth(args, dev) -> dict:
         del passes, ws, io, graph
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
-    out["note"] = ("'vdepth': front, scan, cut with index lists, union, value-depth stage (one CTA per unit: exact-key "
-                   "softmax, row weights, plane allocation, value rows read to their depths); 'full': the default "
-                   "path (range attention over full bf16 rows); attend_us is the last stage of each")
+    out["note"] = ("'vdepth': front, scan, cut with index lists, union, value-depth stage (a cluster of 8 CTAs per "
+                   "unit: exact-key softmax, row weights, plane allocation, value rows read to their depths); 'full': "
+                   "the default path (range attention over full bf16 rows); attend_us is the last stage of each")
     return out
 
 
