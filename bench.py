@@ -50,16 +50,16 @@ def launches_per_pass(cap: int, rows: int, group: int) -> int:
     """Kernels bpkv_decode_step launches per layer: the front kernel (append
     beside depths and plan), the scan, the cut and the range attention.  When
     the cut's grid (one CTA per 4096 middle keys and row) is not resident at
-    once (2 CTAs per SM), the row buckets kernel runs before the cut, with the
-    level-1 histogram kernel and the bucket narrowed by it on rows of 262144
-    keys or more, and the level-0 histogram kernel first when the scan does not
-    count it (more than 4 query heads per KV head).  The bench sizes launches by
-    the capacity."""
+    once (2 CTAs per SM), the row buckets kernel runs before the streaming cut
+    and the row rank kernel after it, with the level-1 histogram kernel and the
+    bucket narrowed by it on rows of 262144 keys or more, and the level-0
+    histogram kernel first when the scan does not count it (more than 4 query
+    heads per KV head).  The bench sizes launches by the capacity."""
     long_rows = cap - 1 >= 262144
     cut_ctas = rows * ((cap - 1 - 36 + 4095) // 4096)
     if cut_ctas <= 2 * SM_COUNT:
         return 4
-    return 5 + (2 if long_rows else 0) + (1 if group > 4 else 0)
+    return 6 + (2 if long_rows else 0) + (1 if group > 4 else 0)
 
 
 FALLBACK_HBM_GBS = 6800.0

@@ -221,23 +221,25 @@ __device__ __forceinline__ int bins_of_thread(const uint32_t* hist, int nbins, u
 // zero-padded to an even count (0 ranks below every candidate).  Small sets
 // are ranked by counting; larger ones by a radix select (S.hist as its
 // histogram).
-__device__ __forceinline__ void rank_cut(CutSmem& S, int nc, uint32_t rem) {
+__device__ __forceinline__ void rank_cut(CutSmem& S, int nc, uint32_t rem, int shared_bits) {
   if (nc > 128) {
     // radix select of the rem-th largest (the values are distinct), eight
-    // bits at a time from the top: descend into the bin holding it until
-    // that bin holds it alone
+    // bits at a time from the top below the shared_bits every value shares:
+    // descend into the bin holding it until that bin holds it alone
     const int tid = threadIdx.x, lane = tid & 31;
     if (rem < 1 || (int)rem > nc) return;
-    unsigned long long pre = 0ull;  // the bits above `shift` fixed so far
+    int fixed_lo = 64 - shared_bits;  // the bits from fixed_lo up are fixed in pre
+    unsigned long long pre = fixed_lo >= 64 ? 0ull : (S.cand[0] & (~0ull << fixed_lo));
     uint32_t need = rem;
-    int shift = 56;
-    for (;; shift -= 8) {
+    while (true) {
+      const int shift = max(fixed_lo - 8, 0);
+      const uint32_t dmask = (1u << (fixed_lo - shift)) - 1u;
       for (int b = tid; b < 256; b += blockDim.x) S.hist[b] = 0u;
       __syncthreads();
-      const unsigned long long hi_mask = shift == 56 ? 0ull : (~0ull << (shift + 8));
+      const unsigned long long hi_mask = fixed_lo >= 64 ? 0ull : (~0ull << fixed_lo);
       for (int e = tid; e < nc; e += blockDim.x) {
         const unsigned long long x = S.cand[e];
-        if ((x & hi_mask) == pre) atomicAdd(&S.hist[(x >> shift) & 0xFFu], 1u);
+        if ((x & hi_mask) == pre) atomicAdd(&S.hist[(x >> shift) & dmask], 1u);
       }
       __syncthreads();
       if (tid < 32) {
@@ -267,10 +269,11 @@ __device__ __forceinline__ void rank_cut(CutSmem& S, int nc, uint32_t rem) {
       __syncthreads();
       pre |= (unsigned long long)S.tb << shift;
       need = S.rem;
-      if (S.nb == 1u || shift == 0) break;
+      fixed_lo = shift;
+      if (S.nb == 1u || fixed_lo == 0) break;
     }
     // the one value with the fixed bits
-    const unsigned long long mask = ~0ull << shift;
+    const unsigned long long mask = ~0ull << fixed_lo;
     for (int e = tid; e < nc; e += blockDim.x)
       if ((S.cand[e] & mask) == pre) S.cut = S.cand[e];
     return;
@@ -330,7 +333,7 @@ __device__ void cut_refine(CutSmem& S, const float* __restrict__ sc, int64_t lo,
     const int nc = (int)min(S.n_cand, (uint32_t)kRankCap);
     if (tid == 0) S.cand[nc] = 0ull;
     __syncthreads();
-    rank_cut(S, nc, rem);
+    rank_cut(S, nc, rem, 32 - level_shift(lvl));
     return;
   }
   // a single key value tk repeated more than kRankCap times: its rem-th
@@ -380,22 +383,14 @@ __device__ __forceinline__ void row_barrier(uint32_t* bar, uint32_t count, int32
   __syncthreads();
 }
 
-// The end of a row's cut: the last CTA of the row to finish (the barrier
-// orders the CTA's candidate writes before thread 0's cumulative fence) ranks
-// the candidates, or refines a bucket of more than kRankCap keys, and stores
-// the cut; it also clears the row's counters.  Whole block.
-__device__ void cut_finish(CutSmem& S, const CutArgs& a, int row, const RowRange& r, const float* __restrict__ sc,
+// The end of a row's cut, by one CTA once every candidate of the row is
+// written: it ranks the candidates, or refines a bucket of more than kRankCap
+// keys, stores the cut, adds the bucket's chosen tokens to the selection map
+// (when there is one) and clears the row's counters.  Whole block.
+__device__ void cut_decide(CutSmem& S, const CutArgs& a, int row, const RowRange& r, const float* __restrict__ sc,
                            uint32_t* ctr, const unsigned long long* cand, uint32_t nb, uint32_t rem, uint32_t prefix,
                            int lvl) {
   const int tid = threadIdx.x;
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    S.is_last = (atomicAdd(ctr + 1, 1u) == gridDim.x - 1) ? 1u : 0u;
-    if (S.is_last) __threadfence();
-  }
-  __syncthreads();
-  if (!S.is_last) return;
   if (tid == 0) S.cut = ~0ull;
   uint32_t* mrow = a.selmap ? a.selmap + (int64_t)row * a.map_words : nullptr;
   if (nb <= (uint32_t)kRankCap) {
@@ -403,7 +398,7 @@ __device__ void cut_finish(CutSmem& S, const CutArgs& a, int row, const RowRange
     for (int e = tid; e < nc; e += kCutThreads) S.cand[e] = __ldcg(cand + e);
     if (tid == 0) S.cand[nc] = 0ull;
     __syncthreads();
-    rank_cut(S, nc, rem);
+    rank_cut(S, nc, rem, 32 - level_shift(lvl));
     __syncthreads();
     if (mrow && S.cut != ~0ull) {
       // the bucket's chosen keys join the map (the keys above the bucket are in it)
@@ -440,6 +435,23 @@ __device__ void cut_finish(CutSmem& S, const CutArgs& a, int row, const RowRange
 #pragma unroll
     for (int i = 0; i < kSelCounters; ++i) ctr[i] = 0u;  // every CTA of the row is past its waits
   }
+}
+
+// The row's CTAs, after their part: the last one to arrive decides the cut
+// (the barrier orders the CTA's candidate writes before thread 0's cumulative
+// fence; the ticket is counter 1).
+__device__ void cut_finish(CutSmem& S, const CutArgs& a, int row, const RowRange& r, const float* __restrict__ sc,
+                           uint32_t* ctr, const unsigned long long* cand, uint32_t nb, uint32_t rem, uint32_t prefix,
+                           int lvl) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    S.is_last = (atomicAdd(ctr + 1, 1u) == gridDim.x - 1) ? 1u : 0u;
+    if (S.is_last) __threadfence();
+  }
+  __syncthreads();
+  if (!S.is_last) return;
+  cut_decide(S, a, row, r, sc, ctr, cand, nb, rem, prefix, lvl);
 }
 
 // Append this warp's matching keys (bit b of `match`: key keys[b] of token
@@ -531,14 +543,14 @@ __global__ void __launch_bounds__(kCutThreads, 2) k_cut(CutArgs a) {
 // level-1 histogram on long rows): grid (chunks of kStreamChunk tokens in
 // absolute position, rows); each thread loads kStreamVec 16-byte groups of
 // scores (tokens 4 (t + 256 j) .. + 3 of the chunk) at once, then keeps the
-// middle tokens whose key is in the bucket and appends them.
+// middle tokens whose key is in the bucket and appends them.  k_rank then
+// decides each row's cut.
 constexpr int kStreamVec = 8;                              // float4 loads per thread
 constexpr int kStreamChunk = 4 * kStreamVec * kCutThreads;  // 8192 tokens per CTA
 static_assert(kStreamVec == 8, "a thread's 32 tokens are eight nibbles of the selection map");
 
 __global__ void __launch_bounds__(kCutThreads, 4) k_cut_stream(CutArgs a) {
   pdl_enter();
-  __shared__ CutSmem S;
   const int row = blockIdx.y, tid = threadIdx.x, lane = tid & 31;
   const float* sc = a.scores + (int64_t)row * a.ld;
   uint32_t* ctr = a.ctr + (int64_t)kSelCounters * row;
@@ -555,7 +567,7 @@ __global__ void __launch_bounds__(kCutThreads, 4) k_cut_stream(CutArgs a) {
     v[j] = x < ld ? p[tid + kCutThreads * j] : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   const int64_t n_row = a.seq_len[row / a.rows_per_seq];
-  const uint32_t prefix = ctr[4], rem = ctr[5], nb = ctr[6];
+  const uint32_t prefix = ctr[4], nb = ctr[6];
   const int lvl = (int)ctr[7];
   const RowRange r = row_range(n_row + a.pending, a.k, a.n_sink, a.n_recent);
   if (r.cnt <= r.m || r.m == 0) {
@@ -643,7 +655,19 @@ __global__ void __launch_bounds__(kCutThreads, 4) k_cut_stream(CutArgs a) {
       }
     }
   }
-  cut_finish(S, a, row, r, sc, ctr, cand, nb, rem, prefix, lvl);
+}
+
+// After k_cut_stream, one CTA per row: the row's cut (cut_decide).
+__global__ void __launch_bounds__(kCutThreads) k_rank(CutArgs a) {
+  pdl_enter();
+  __shared__ CutSmem S;
+  const int row = blockIdx.x;
+  const RowRange r = row_range(a.seq_len[row / a.rows_per_seq] + a.pending, a.k, a.n_sink, a.n_recent);
+  if (r.cnt <= r.m || r.m == 0) return;  // k_cut_stream stored these rows' cuts
+  uint32_t* ctr = a.ctr + (int64_t)kSelCounters * row;
+  const uint32_t prefix = ctr[4], rem = ctr[5], nb = ctr[6];
+  const int lvl = (int)ctr[7];
+  cut_decide(S, a, row, r, a.scores + (int64_t)row * a.ld, ctr, a.cand + (int64_t)row * kRankCap, nb, rem, prefix, lvl);
 }
 
 // ------------------------------------------------------------------ k_bucket
@@ -855,7 +879,7 @@ cudaError_t launch_cut(const bpkv_cache& c, const float* scores, int64_t ld, int
             build_hist ? nullptr : selmap, ld / 32};
   if (build_hist) return launch_coop_pdl(k_cut, run_grid(c, 1), dim3(kCutThreads), 0, st, a);
   // each row's bucket once, then (long rows) the level-1 histogram and the
-  // bucket narrowed by it, then the cut
+  // bucket narrowed by it, then the streaming filter and each row's rank
   const dim3 rows((unsigned)(c.n_seq * c.n_kv_heads * c.group));
   cudaError_t e = launch_pdl(k_bucket<0>, rows, dim3(kCutThreads), 0, st, a);
   if (e != cudaSuccess) return e;
@@ -865,8 +889,10 @@ cudaError_t launch_cut(const bpkv_cache& c, const float* scores, int64_t ld, int
     e = launch_pdl(k_bucket<1>, rows, dim3(kCutThreads), 0, st, a);
     if (e != cudaSuccess) return e;
   }
-  const dim3 grid((unsigned)((c.n_max + kStreamChunk - 1) / kStreamChunk), (unsigned)(c.n_seq * c.n_kv_heads * c.group));
-  return launch_pdl(k_cut_stream, grid, dim3(kCutThreads), 0, st, a);
+  const dim3 grid((unsigned)((c.n_max + kStreamChunk - 1) / kStreamChunk), rows.x);
+  e = launch_pdl(k_cut_stream, grid, dim3(kCutThreads), 0, st, a);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_rank, rows, dim3(kCutThreads), 0, st, a);
 }
 
 cudaError_t launch_lists(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
