@@ -12,7 +12,7 @@ import ctypes
 
 from ._binding import (  # noqa: F401
     BpkvError, bpkv_alloc_depths, bpkv_cache, bpkv_calibrate_channels, bpkv_clear_status, bpkv_decode_step,
-    bpkv_dense_attend, bpkv_encode_append, bpkv_fixed_depths, bpkv_read_status, bpkv_rotate, bpkv_row_cache_stats, bpkv_scan, bpkv_scan_topk, bpkv_scan_topk_noalloc, bpkv_selftest_wait, bpkv_sparse_attend, bpkv_sparse_attend_vdepth,
+    bpkv_dense_attend, bpkv_encode_append, bpkv_fixed_depths, bpkv_read_status, bpkv_rotate, bpkv_row_cache_stats, bpkv_scan, bpkv_scan_topk, bpkv_scan_topk_noalloc, bpkv_selection_map, bpkv_selftest_wait, bpkv_sparse_attend, bpkv_sparse_attend_vdepth,
     bpkv_status_string, bpkv_step_args, bpkv_topk, bpkv_union, bpkv_version, bpkv_workspace_size, header_symbols, load)
 
 HEAD_DIM = 128

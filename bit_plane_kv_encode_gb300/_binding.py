@@ -53,6 +53,7 @@ _SIGS = {
     "bpkv_read_status": ([P, P, P], ctypes.c_int),
     "bpkv_selftest_wait": ([P, i32, i32, P], ctypes.c_int),
     "bpkv_row_cache_stats": ([P, i32, P, P, P], ctypes.c_int),
+    "bpkv_selection_map": ([P, i32, P, P, P], ctypes.c_int),
     "bpkv_encode_append": ([P, P, P, i32, P], ctypes.c_int),
     "bpkv_alloc_depths": ([P, P, P, P, P, P], ctypes.c_int),
     "bpkv_fixed_depths": ([P, P, i32, i32, P, P], ctypes.c_int),
@@ -156,6 +157,15 @@ def bpkv_row_cache_stats(cache, k: int, ws, stream=None):
     out = np.zeros((cache.n_seq, cache.n_kv_heads, 2), dtype=np.uint32)
     _check("bpkv_row_cache_stats", load().bpkv_row_cache_stats(ctypes.byref(cache), int(k), _ptr(ws),
                                                                 out.ctypes.data_as(ctypes.c_void_p), _stream(stream)))
+    return out
+
+
+def bpkv_selection_map(cache, k: int, ws, stream=None):
+    """The last step's selection map of its last layer: numpy uint32 [N][H][G][cap_tokens / 32]."""
+    import numpy as np
+    out = np.zeros((cache.n_seq, cache.n_kv_heads, cache.group, cache.cap_tokens // 32), dtype=np.uint32)
+    _check("bpkv_selection_map", load().bpkv_selection_map(ctypes.byref(cache), int(k), _ptr(ws),
+                                                            out.ctypes.data_as(ctypes.c_void_p), _stream(stream)))
     return out
 
 

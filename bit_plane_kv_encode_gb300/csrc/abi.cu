@@ -242,6 +242,17 @@ int bpkv_row_cache_stats(const bpkv_cache* c, int32_t k, const void* ws, uint32_
   return BPKV_OK;
 }
 
+int bpkv_selection_map(const bpkv_cache* c, int32_t k, const void* ws, uint32_t* out, void* stream) {
+  BPKV_TRY(check_cache(c));
+  if (!ws || !out || k < 1 || k > kMaxK) return BPKV_EINVAL;
+  if (cut_counts_hist(*c)) return BPKV_EUNSUPPORTED;  // the cooperative cut writes no map
+  const Layout L = layout(*c, k, BPKV_WS_STEP);
+  const size_t words = (size_t)c->n_seq * c->n_kv_heads * c->group * (size_t)(c->cap_tokens / 32);
+  BPKV_TRY(cuda_status(cudaStreamSynchronize(as_stream(stream))));
+  return cuda_status(cudaMemcpy(out, static_cast<const unsigned char*>(ws) + L.selmap, words * sizeof(uint32_t),
+                                cudaMemcpyDeviceToHost));
+}
+
 int bpkv_encode_append(bpkv_cache* c, const uint16_t* k_new, const uint16_t* v_new, int32_t t_new, void* stream) {
   BPKV_TRY(check_cache(c));
   if (t_new < 1 || !k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)) return BPKV_EINVAL;

@@ -399,6 +399,22 @@ typedef struct bpkv_step_args {
  */
 int bpkv_row_cache_stats(const bpkv_cache *c, int32_t k, const void *ws, uint32_t *out, void *stream);
 
+/*
+ * The selection the range attention read in the last layer of the last
+ * bpkv_decode_step that used this workspace (Fathom page, section 2 "Top-k
+ * decoding": each query head's top (k - 36) middle tokens): synchronises
+ * `stream`, then copies the map to the host array out of N H G (cap_tokens /
+ * 32) words, row (seq, h, g) at ((seq H + h) G + g) (cap_tokens / 32).  Bit
+ * x % 32 of word x / 32 is set when middle token x (n_sink <= x < n -
+ * n_recent) was chosen by query head g; sinks and recent tokens are not in
+ * the map, and neither are the rows of a head that chose every middle token
+ * or none (their words are left as they were).  The streaming cut writes the
+ * map; the cooperative cut of small problems (whole grid resident) does not,
+ * and then BPKV_EUNSUPPORTED is returned.  The workspace must be the step's
+ * (same cache shape and k).
+ */
+int bpkv_selection_map(const bpkv_cache *c, int32_t k, const void *ws, uint32_t *out, void *stream);
+
 #define BPKV_STAGE_EVENTS 7
 #define BPKV_STEP_VDEPTH 1      /* read the value rows to per-row depths (bpkv_sparse_attend_vdepth)
                                    instead of in full; the cache needs value planes */

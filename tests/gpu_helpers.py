@@ -81,11 +81,12 @@ def check_topk_sets(gpu_idx: np.ndarray, ref_idx: np.ndarray, ref_score: np.ndar
 
 
 def decode_one_layer(inp, cfg, depth_rule=0, fixed=(0, 0), budgets=None, residency="hbm", dev="cuda", flags=0,
-                     lists=True, depths_in=None, basis=None):
+                     lists=True, depths_in=None, basis=None, keep=None):
     """Prefill n-1 tokens of a generated layer, then one bpkv_decode_step (appends
     token n-1 and runs the whole path).  Returns (cache, depths, idx, out) with
     depths [N][H][D], idx [N][H][G][k], out [N][H][G][D] on the device; with
-    lists=False the step writes no index lists (idx stays zero)."""
+    lists=False the step writes no index lists (idx stays zero).  keep: a dict
+    that receives the step's workspace ("ws")."""
     import bit_plane_kv_encode_gb300 as pk
     N, H, n, D = inp.k.shape
     G = cfg.group
@@ -111,6 +112,8 @@ def decode_one_layer(inp, cfg, depth_rule=0, fixed=(0, 0), budgets=None, residen
     pk.sync_n_max([cache], arr)
     torch.cuda.synchronize()
     assert pk.bpkv_read_status(ws) == 0
+    if keep is not None:
+        keep["ws"] = ws
     return cache, depths[0], idx[0], out[0]
 
 
