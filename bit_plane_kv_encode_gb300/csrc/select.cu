@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kCutThreads) k_hist(HistArgs a) {
 
 // ------------------------------------------------------------------ k_cut
 
-constexpr int kRankCap = 1024;  // bucket size ranked directly
+constexpr int kRankCap = 1024;  // bucket size ranked directly (a multiple of kCutThreads)
 
 struct CutArgs {
   const float* scores;
@@ -394,8 +394,14 @@ __device__ void cut_decide(CutSmem& S, const CutArgs& a, int row, const RowRange
   if (tid == 0) S.cut = ~0ull;
   uint32_t* mrow = a.selmap ? a.selmap + (int64_t)row * a.map_words : nullptr;
   if (nb <= (uint32_t)kRankCap) {
+    // every candidate slot loaded beside the count (slots past it are unused)
+    unsigned long long cv[kRankCap / kCutThreads];
+#pragma unroll
+    for (int i = 0; i < kRankCap / kCutThreads; ++i) cv[i] = __ldcg(cand + tid + kCutThreads * i);
     const int nc = (int)min(__ldcg(ctr), (uint32_t)kRankCap);
-    for (int e = tid; e < nc; e += kCutThreads) S.cand[e] = __ldcg(cand + e);
+#pragma unroll
+    for (int i = 0; i < kRankCap / kCutThreads; ++i)
+      if (tid + kCutThreads * i < nc) S.cand[tid + kCutThreads * i] = cv[i];
     if (tid == 0) S.cand[nc] = 0ull;
     __syncthreads();
     rank_cut(S, nc, rem, 32 - level_shift(lvl));
