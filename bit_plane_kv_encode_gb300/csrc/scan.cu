@@ -127,14 +127,19 @@ __device__ __forceinline__ void scan_unit_pipe(const ScanArgs& a, PipeSmem<GP>& 
           if (w1) o[hh * a.ld + 32] = v1[hh];
           if constexpr (kSmemHist) {
             if (hist) {
+              // the order-preserving key straight from the bits (-0 made +0
+              // first): bin = key >> 20 counts in word bin / 2 = key >> 21,
+              // half (bin & 1) = key bit 20
               uint32_t* H = S.hist + hh * (kTopkBins / 2);
               if (in0) {
-                const uint32_t bin = ordered_key(v0[hh]) >> 20;
-                atomicAdd(H + (bin >> 1), 1u << ((bin & 1u) * 16));
+                const uint32_t u = __float_as_uint(__fadd_rn(v0[hh], 0.f));
+                const uint32_t key = u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+                atomicAdd(H + (key >> 21), 1u << ((key >> 16) & 16u));
               }
               if (in1) {
-                const uint32_t bin = ordered_key(v1[hh]) >> 20;
-                atomicAdd(H + (bin >> 1), 1u << ((bin & 1u) * 16));
+                const uint32_t u = __float_as_uint(__fadd_rn(v1[hh], 0.f));
+                const uint32_t key = u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+                atomicAdd(H + (key >> 21), 1u << ((key >> 16) & 16u));
               }
             }
           }
