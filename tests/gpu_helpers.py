@@ -144,3 +144,29 @@ def check_unit(orc, cfg, inp, cache, depths, idx, out, s, h, depth_rule=0, fixed
         assert err <= ATTN_ATOL, f"{what} g{g} attention err {err} ({'same set' if d == 0 else f'{d} near-ties'})"
         same += d == 0
     return same, ref
+
+
+def check_selection_map(pk, cfg, cache, idx, ws, n):
+    """The range attention's selection map (bpkv_selection_map) holds exactly
+    the middle tokens of the step's index lists on every row, bit for bit.
+    Returns False (nothing checked) when the step took the cooperative cut,
+    which writes no map."""
+    import numpy as np
+    try:
+        smap = pk.bpkv_selection_map(cache.c, cfg.k, ws)
+    except pk.BpkvError:
+        return False
+    idx = idx.cpu().numpy() if hasattr(idx, "cpu") else idx
+    lo = min(cfg.n_sink, n)
+    hi = max(n - cfg.n_recent, lo)
+    bits = np.unpackbits(smap.view(np.uint8), bitorder="little").reshape(*smap.shape[:3], -1)
+    N, H, G = smap.shape[:3]
+    for s in range(N):
+        for h in range(H):
+            for g in range(G):
+                want = set(int(x) for x in idx[s, h, g] if lo <= x < hi)
+                if len(want) == hi - lo or not want:
+                    continue  # every middle token or none: the map row is not written
+                got = set(int(x) for x in np.nonzero(bits[s, h, g, lo:hi])[0] + lo)
+                assert got == want, f"s{s} h{h} g{g}: map has {len(got)} middle tokens, lists {len(want)}"
+    return True
