@@ -836,10 +836,33 @@ int cut_slots() {
   return slots[dev] > 0 ? slots[dev] : 0;
 }
 
-// Chunks per CTA so that the (runs, rows) grid fits in about one wave.
-int32_t chunks_per_cta(const bpkv_cache& c) {
+// Resident CTAs of a histogram kernel (k_hist: which 0, k_hist1: which 1) on
+// the current device (looked up once per device); 4 per SM of 152 if unknown.
+int64_t hist_slots(int which) {
+  constexpr int kDevs = 64;
+  static int slots[2][kDevs] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return 4 * 152;
+  std::lock_guard<std::mutex> lock(mu);
+  if (slots[which][dev] == 0) {
+    int sms = 0, per_sm = 0;
+    const cudaError_t e = which == 0
+                              ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_hist, kCutThreads, 0)
+                              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_hist1, kCutThreads, 0);
+    if (e != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return 4 * 152;
+    slots[which][dev] = sms * per_sm > 0 ? sms * per_sm : 4 * 152;
+  }
+  return slots[which][dev];
+}
+
+// Chunks per CTA of a histogram kernel: about two waves of its resident
+// CTAs, so that each CTA streams few chunks (one dependent round of loads
+// each) and flushes its bins once.
+int32_t hist_chunks_per_cta(const bpkv_cache& c, int which) {
   const int64_t rows = (int64_t)c.n_seq * c.n_kv_heads * c.group, chunks = cut_chunks(c);
-  const int64_t slots = cut_slots() > 0 ? cut_slots() : 2 * 152;
+  const int64_t slots = 2 * hist_slots(which);
   const int64_t cpc = (chunks * rows + slots - 1) / slots;
   return (int32_t)(cpc < 1 ? 1 : cpc);
 }
@@ -850,7 +873,7 @@ dim3 run_grid(const bpkv_cache& c, int32_t cpc) {
 
 cudaError_t launch_hist(const bpkv_cache& c, const float* scores, int64_t ld, int32_t k, int32_t n_sink,
                         int32_t n_recent, uint32_t* hist, int32_t pending, cudaStream_t st) {
-  const int32_t cpc = chunks_per_cta(c);
+  const int32_t cpc = hist_chunks_per_cta(c, 0);
   HistArgs a{scores, ld, c.seq_len, hist, c.n_kv_heads * c.group, k, n_sink, n_recent, pending, cpc};
   return launch_pdl(k_hist, run_grid(c, cpc), dim3(kCutThreads), 0, st, a);
 }
@@ -879,7 +902,7 @@ cudaError_t launch_cut(const bpkv_cache& c, const float* scores, int64_t ld, int
                        int32_t n_recent, const SelBufs& b, bool build_hist, int32_t pending, int32_t* status,
                        cudaStream_t st, uint32_t* selmap) {
   const bool l1 = !build_hist && long_rows(c);
-  const int32_t cpc = build_hist ? 1 : chunks_per_cta(c);
+  const int32_t cpc = build_hist ? 1 : hist_chunks_per_cta(c, 1);  // k_hist1's runs
   CutArgs a{scores,   ld,           c.seq_len, b.hist, l1 ? b.hist1 : nullptr, b.cand, b.ctr, b.cut, status,
             c.n_kv_heads * c.group, k, n_sink, n_recent, build_hist ? 1 : 0, pending, cpc,
             build_hist ? nullptr : selmap, ld / 32};
