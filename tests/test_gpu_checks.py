@@ -1,9 +1,10 @@
 """The bounds-checked build (the library compiled with -DBPKV_CHECKS=1): the
 scan's plan builder, copies, weight formation and group loop check every
 index they compute against its array and record BPKV_DEV_BOUNDS in the status
-word instead of touching memory outside it.  The decode-step, host and
-selection-edge GPU tests run once more against that library in a child
-process; each of them asserts a clean status word after its steps."""
+word instead of touching memory outside it.  The decode-step (caches in
+device memory), basis, calibration and scan GPU tests run once more against
+that library in a child process; each of them asserts a clean status word
+after its steps."""
 import os
 import subprocess
 import sys

@@ -151,13 +151,13 @@ def test_step_unaligned_sink_recent(pk, orc, n_sink, n_recent, n_tok):
 
 
 @pytest.mark.parametrize("n_sink,n_recent,n_tok,residency", [(4, 32, 70001, "hbm"), (5, 30, 65536 + 1023, "hbm"),
-                                                             (0, 0, 40000 + 3, "hbm"), (4, 32, 70001, "host")])
+                                                             (0, 0, 40000 + 3, "hbm")])
 def test_selection_map_matches_lists(pk, n_sink, n_recent, n_tok, residency):
     """The selection map the range attention reads (written by the streaming
     cut: the tokens above each row's bucket, then the bucket's chosen ones by
     the row's rank kernel) holds exactly the middle tokens of the step's own
-    index lists, bit for bit, on every row; caches in device memory and in
-    pinned host memory."""
+    index lists, bit for bit, on every row (caches in pinned host memory:
+    test_gpu_host.py)."""
     import dataclasses
     from workload import CONFIGS, gen_layer
     cfg = dataclasses.replace(CONFIGS["multi_session"], n_seq=2, n_tokens=n_tok, n_sink=n_sink, n_recent=n_recent,

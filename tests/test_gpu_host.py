@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import bits16, bits64, build_cache, check_unit
+from gpu_helpers import bits16, bits64, build_cache, check_selection_map, check_unit, decode_one_layer
 
 pytestmark = pytest.mark.gpu
 
@@ -144,3 +144,16 @@ def test_row_cache_identical_and_hits(pk):
     assert (stats[0][..., 0] == 0).all() and (stats[0][..., 1] > 0).all()  # first step: all misses
     later = np.stack(stats[1:])
     assert later[..., 0].sum() > 0.5 * later.sum(), later.sum(axis=(1, 2))
+
+
+def test_host_selection_map_matches_lists(pk):
+    """A decode step over caches in pinned host memory (the scan's host form
+    and the row-cache attention): the selection map the attention reads holds
+    exactly the middle tokens of the step's index lists on every row."""
+    import dataclasses
+    from workload import CONFIGS, gen_layer
+    cfg = dataclasses.replace(CONFIGS["multi_session"], n_seq=2, n_tokens=70001, n_sink=4, n_recent=32, k=336)
+    inp = gen_layer(cfg, 0, device="cuda")
+    keep = {}
+    cache, d, idx, out = decode_one_layer(inp, cfg, keep=keep, residency="host")
+    assert check_selection_map(pk, cfg, cache, idx, keep["ws"], cfg.n_tokens)
